@@ -1,0 +1,376 @@
+"""Pins for the CPU oracle: checks against what the Unweight blog post and
+plain mathematics fix, never against the oracle's own formulas retyped.
+
+Each test names what pins it: the BF16 number format, a hand-worked example
+(tests/golden), brute force over tiny alphabets, the textbook Huffman
+construction, the Kraft inequality, the entropy bound, or an independent
+numpy computation.
+"""
+import heapq
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import workloads as wl
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- BF16 fields
+def test_field_split_hand_values(oracle):
+    # BF16 = 1 sign bit, 8 exponent bits, 7 mantissa bits (Unweight blog, BF16 layout paragraph).
+    cases = {
+        0x3F80: (127, 0x00),   # +1.0
+        0xBF80: (127, 0x80),   # -1.0
+        0x3FC0: (127, 0x40),   # +1.5  (mantissa 1000000b)
+        0x4049: (128, 0x49),   # +3.140625
+        0x0001: (0, 0x01),     # smallest positive subnormal
+        0x8000: (0, 0x80),     # -0.0
+        0x7F80: (255, 0x00),   # +inf
+        0xFFC1: (255, 0xC1),   # negative NaN with payload 1000001b
+    }
+    w = np.array(list(cases), np.uint16)
+    e, sm = oracle.split(w)
+    for i, (ee, ss) in enumerate(cases.values()):
+        assert (e[i], sm[i]) == (ee, ss)
+
+
+def test_field_split_matches_float_value(oracle):
+    # For every normal BF16 pattern, the value is (-1)^s * 2^(e-127) * (1 + m/128):
+    # recover s, e, m from the float value with frexp and compare.
+    pats = wl.all_bf16_patterns().ravel()
+    e, sm = oracle.split(pats)
+    with np.errstate(invalid="ignore"):
+        vals = wl.bf16_to_f32(pats).astype(np.float64)
+    normal = np.isfinite(vals) & (np.abs(vals) >= 2.0 ** -126)
+    frac, ex = np.frexp(np.abs(vals[normal]))          # |v| = frac * 2^ex, frac in [0.5, 1)
+    assert np.array_equal(e[normal].astype(np.int64), ex - 1 + 127)
+    mant = np.round((frac * 2 - 1) * 128).astype(np.int64)
+    assert np.array_equal((sm[normal] & 0x7F).astype(np.int64), mant)
+    assert np.array_equal(sm[normal] >> 7, np.signbit(vals[normal]).astype(np.uint8))
+
+
+def test_join_inverts_split_for_every_pattern(oracle):
+    pats = wl.all_bf16_patterns().ravel()
+    e, sm = oracle.split(pats)
+    back = np.array([oracle.join(a, b) for a, b in zip(e[::97], sm[::97])], np.uint16)
+    assert np.array_equal(back, pats[::97])
+
+
+# ---------------------------------------------------------------- histogram / palette
+def test_histogram_matches_frexp_exponents(oracle):
+    w = wl.normal_weights(64, 512, 0.02, seed=3)
+    v = wl.bf16_to_f32(w).astype(np.float64).ravel()
+    _, ex = np.frexp(np.abs(v))
+    biased = np.where(v == 0, 0, ex - 1 + 127)      # no subnormals at this scale
+    assert np.array_equal(oracle.histogram(w), np.bincount(biased, minlength=256).astype(np.uint64))
+
+
+def test_palette_order_ties_and_limit(oracle):
+    c = np.zeros(256, np.uint64)
+    # 20 distinct exponents; counts chosen so that ties decide the order.
+    for v, n in [(100, 7), (120, 5), (121, 5), (90, 5), (3, 1), (200, 0)]:
+        c[v] = n
+    for v in range(130, 145):
+        c[v] = 2
+    pal = oracle.palette(c)
+    assert pal[:4] == [100, 90, 120, 121]          # count desc, then exponent asc
+    assert pal[4:] == list(range(130, 142))         # 12 of the 15 twos, smallest first
+    assert len(pal) == 16 and 3 not in pal and 200 not in pal
+
+
+def test_palette_skips_zero_counts(oracle):
+    c = np.zeros(256, np.uint64)
+    c[[5, 9]] = [3, 1]
+    assert oracle.palette(c) == [5, 9]
+
+
+# ---------------------------------------------------------------- escapes
+def test_escape_flags_one_decision_per_row_of_64(oracle):
+    # A group of 64 is escaped iff it holds an exponent outside the palette
+    # (Unweight blog, paragraph on rows of 64 with rare exponents).
+    w = np.full((2, 128), 0x3C00, np.uint16)     # exponent 120 everywhere
+    w[0, 70] = 0x3800                             # exponent 112 in group (0, 1)
+    pal = [120]
+    assert list(oracle.escape_flags(w, pal)) == [0, 1, 0, 0]
+    assert list(oracle.escape_flags(w, [120, 112])) == [0, 0, 0, 0]
+
+
+# ---------------------------------------------------------------- code lengths
+def _brute_force_min_cost(freq, lmax):
+    """Enumerate every per-symbol length vector (not count vectors)."""
+    idx = [i for i, f in enumerate(freq) if f > 0]
+    best = None
+    for lens in itertools.product(range(1, lmax + 1), repeat=len(idx)):
+        if sum(2.0 ** -l for l in lens) <= 1.0 + 1e-12:
+            cost = sum(freq[i] * l for i, l in zip(idx, lens))
+            best = cost if best is None else min(best, cost)
+    return best
+
+
+def _huffman_cost(freq):
+    h = [f for f in freq if f > 0]
+    if len(h) == 1:
+        return h[0]
+    heapq.heapify(h)
+    cost = 0
+    while len(h) > 1:
+        a, b = heapq.heappop(h), heapq.heappop(h)
+        cost += a + b
+        heapq.heappush(h, a + b)
+    return cost
+
+
+def _cost(freq, lens):
+    return sum(f * l for f, l in zip(freq, lens))
+
+
+def _kraft(lens):
+    return sum(2.0 ** -l for l in lens if l > 0)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_code_lengths_brute_force_tiny_alphabets(oracle, seed):
+    rng = np.random.default_rng(seed)
+    m = int(rng.integers(1, 7))
+    lmax = int(rng.integers(max(1, math.ceil(math.log2(m)) if m > 1 else 1), 7))
+    freq = [int(v) for v in rng.integers(0, 50, m)]
+    if seed % 5 == 0:
+        freq = [int(v) for v in rng.integers(1, 4, m)]      # many ties
+    lens = oracle.code_lengths(freq, lmax)
+    if sum(freq) == 0:
+        assert all(l == 0 for l in lens)
+        return
+    assert all((l == 0) == (f == 0) for l, f in zip(lens, freq))
+    assert max(lens) <= lmax and _kraft(lens) <= 1.0
+    assert _cost(freq, lens) == _brute_force_min_cost(freq, lmax)
+
+
+def test_code_lengths_tie_rule(oracle):
+    # freq (2,2,1,1): optimal cost 12 is reached by (2,2,2,2) and by
+    # (1,2,3,3).  The rule prefers more symbols on shorter levels
+    # (lexicographically larger (n_1, n_2, ...)): (1,2,3,3).
+    assert oracle.code_lengths([2, 2, 1, 1], 6) == [1, 2, 3, 3]
+    # equal frequencies: lower palette index gets the shorter code
+    assert oracle.code_lengths([1, 1, 1], 6) == [1, 2, 2]
+
+
+def test_code_lengths_hand_examples(oracle):
+    assert oracle.code_lengths([1, 1, 1, 1], 6) == [2, 2, 2, 2]
+    assert oracle.code_lengths([8, 4, 2, 1, 1], 6) == [1, 2, 3, 4, 4]      # textbook Huffman
+    assert oracle.code_lengths([8, 4, 2, 1, 1], 3) == [1, 3, 3, 3, 3]      # worked: cost 32 < 34
+    assert oracle.code_lengths([0, 7, 0], 6) == [0, 1, 0]                  # one symbol -> 1 bit
+    assert oracle.code_lengths([40, 16, 8], 6) == [1, 2, 2]
+    with pytest.raises(ValueError):
+        oracle.code_lengths([1] * 5, 2)                                    # 5 symbols > 2^2
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_code_lengths_equal_textbook_huffman_when_limit_is_loose(oracle, seed):
+    rng = np.random.default_rng(100 + seed)
+    m = int(rng.integers(2, 12))
+    freq = [int(v) for v in rng.integers(1, 1000, m)]
+    lens = oracle.code_lengths(freq, 15)
+    assert _cost(freq, lens) == _huffman_cost(freq)
+    assert abs(_kraft(lens) - 1.0) < 1e-12          # an optimal code is complete
+
+
+def test_mean_length_within_one_bit_of_entropy(oracle):
+    # Textbook bound H <= L < H + 1 on the symbol distribution of the coded
+    # groups of a N(0, 0.02) matrix (the blog: ~2.6 bits of entropy).
+    w = wl.normal_weights(512, 1024, 0.02, seed=0)
+    pal = oracle.palette(oracle.histogram(w))
+    flags = oracle.escape_flags(w, pal).astype(bool)
+    e = ((w.astype(np.uint32) >> 7) & 0xFF).reshape(-1, 64)[~flags]
+    freq = np.array([(e == v).sum() for v in pal], np.float64)
+    lens = oracle.code_lengths(freq.astype(np.uint64), 6)
+    p = freq / freq.sum()
+    H = -(p[p > 0] * np.log2(p[p > 0])).sum()
+    L = (p * np.array(lens)).sum()
+    assert H <= L < H + 1
+    assert 2.4 < H < 2.8
+
+
+# ---------------------------------------------------------------- canonical codes
+def test_canonical_codes_hand_example(oracle):
+    # lengths by symbol: s0:3 s1:2 s2:3 s3:2 -> order (2,s1) (2,s3) (3,s0) (3,s2)
+    assert oracle.canonical_codes([3, 2, 3, 2]) == [0b100, 0b00, 0b101, 0b01]
+    assert oracle.canonical_codes([1, 2, 2]) == [0b0, 0b10, 0b11]
+    assert oracle.canonical_codes([0, 1, 0]) == [0, 0, 0]
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_canonical_codes_are_prefix_free(oracle, seed):
+    rng = np.random.default_rng(seed)
+    freq = rng.integers(0, 10_000, 16).astype(np.uint64)
+    lens = oracle.code_lengths(freq, 6)
+    codes = oracle.canonical_codes(lens)
+    words = [format(c, "0%db" % l) for c, l in zip(codes, lens) if l > 0]
+    for a, b in itertools.permutations(words, 2):
+        assert not b.startswith(a)
+
+
+# ---------------------------------------------------------------- hand-worked blobs
+def _golden(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def _worked_matrix():
+    g = _golden("worked_example_1x64.json")
+    i = np.arange(64)
+    e = np.array(g["exponent_period"])[i % 8]
+    w = ((i % 2) << 15) | (e << 7) | i
+    return w.astype(np.uint16).reshape(1, 64), g
+
+
+def test_worked_example_blob(oracle):
+    w, g = _worked_matrix()
+    blob, info = oracle.compress(w)
+    b = np.frombuffer(blob, np.uint8)
+    assert info["palette"] == g["palette"]
+    assert info["code_len"][:3] == g["code_len"] and info["code_bits"] == g["code_bits"]
+    assert len(blob) == g["blob_bytes"]
+    for k, v in g["sections"].items():
+        assert info[k] == v
+    assert b[:4].tobytes() == b"UWB1"
+    assert b[g["sections"]["off_glen"]] == g["glen"]
+    code = b[g["sections"]["off_code"]: g["sections"]["off_code"] + 16].tobytes().hex()
+    assert code == g["code_region_hex"]
+    sm = b[256:320]
+    assert list(sm) == [((k % 2) << 7) | k for k in range(64)]
+    tc = np.frombuffer(blob[768:776], np.uint32)
+    te = np.frombuffer(blob[1024:1032], np.uint32)
+    assert list(tc) == g["tcode"] and list(te) == g["tesc"]
+    assert np.array_equal(oracle.decompress(blob), w)
+
+
+def test_worked_escape_example(oracle):
+    g = _golden("worked_example_escape_1x128.json")
+    k = np.arange(128)
+    e = np.where(k < 64, 100 + (k % 16), 100)
+    e[127] = 99
+    w = ((e << 7) | (k % 128)).astype(np.uint16).reshape(1, 128)
+    blob, info = oracle.compress(w)
+    b = np.frombuffer(blob, np.uint8)
+    assert info["palette"] == g["palette"] and info["code_len"] == g["code_len"]
+    assert info["n_escaped"] == g["n_escaped"]
+    assert list(b[info["off_glen"]: info["off_glen"] + 2]) == g["glen"]
+    assert b[info["off_code"]: info["off_code"] + 32].tobytes().hex() == g["code_region_hex"]
+    assert list(np.frombuffer(b[info["off_tcode"]: info["off_tcode"] + 12].tobytes(), np.uint32)) == g["tcode"]
+    assert list(np.frombuffer(b[info["off_tesc"]: info["off_tesc"] + 12].tobytes(), np.uint32)) == g["tesc"]
+    assert list(b[info["off_esc"]: info["off_esc"] + 64]) == [100] * 63 + [99]
+    assert np.array_equal(oracle.decompress(blob), w)
+
+
+# ---------------------------------------------------------------- round trips
+def test_round_trip_every_bf16_pattern(oracle):
+    w = wl.all_bf16_patterns()
+    blob, info = oracle.compress(w)
+    assert info["n_escaped"] == 1024 - 64          # 16 exponents per sign coded
+    assert np.array_equal(oracle.decompress(blob), w)
+
+
+@pytest.mark.parametrize("shape", [(1, 64), (3, 128), (33, 192), (65, 1024), (256, 1024)])
+def test_round_trip_normal_and_ragged(oracle, shape):
+    w = wl.normal_weights(*shape, sigma=0.02, seed=shape[0])
+    blob, info = oracle.compress(w)
+    assert np.array_equal(oracle.decompress(blob), w)
+    assert info["n_tiles"] == -(-shape[0] // 32) * (shape[1] // 64)
+
+
+def test_round_trip_heavy_tailed_has_escapes(oracle):
+    w = wl.heavy_tailed_weights(512, 512, seed=0)
+    blob, info = oracle.compress(w)
+    assert 0.02 < info["n_escaped"] / info["n_groups"] < 0.2
+    assert np.array_equal(oracle.decompress(blob), w)
+
+
+def test_round_trip_single_symbol_and_all_escaped(oracle):
+    z = np.zeros((5, 128), np.uint16)
+    blob, info = oracle.compress(z)
+    assert info["code_len"][0] == 1 and info["code_bits"] == 64 * 10
+    assert np.array_equal(oracle.decompress(blob), z)
+    # every group holds 32 distinct exponents: at most 16 fit the palette
+    k = np.arange(64)
+    row = (((100 + k % 32) << 7) | k).astype(np.uint16)
+    a = np.tile(row, (4, 3))
+    blob, info = oracle.compress(a)
+    assert info["n_escaped"] == info["n_groups"] == 12
+    assert np.array_equal(oracle.decompress(blob), a)
+
+
+def test_sign_and_mantissa_stored_untouched(oracle):
+    # The blob's sign+mantissa section is a permutation of the raw bytes.
+    w = wl.normal_weights(40, 256, 0.02, seed=9)
+    blob, info = oracle.compress(w)
+    sm_blob = np.frombuffer(blob, np.uint8)[info["off_sm"]: info["off_sm"] + w.size]
+    raw = ((w >> 8) & 0x80) | (w & 0x7F)
+    assert np.array_equal(np.sort(sm_blob), np.sort(raw.ravel().astype(np.uint8)))
+
+
+def test_decoder_rejects_corruption(oracle):
+    w, _ = _worked_matrix()
+    blob = bytearray(oracle.compress(w)[0])
+    bad = bytearray(blob)
+    bad[0] ^= 1
+    assert oracle.decompress_status(bytes(bad)) == -1
+    bad = bytearray(blob)
+    bad[512] = 12                                  # glen says 12 bytes, code has 11
+    assert oracle.decompress_status(bytes(bad)) == -3
+
+
+# ---------------------------------------------------------------- statistics
+def test_exponent_statistics_match_the_blog(oracle):
+    # Top-16 exponents cover >99% and the entropy is ~2.6 bits (blog, exponent skew).
+    w = wl.normal_weights(1024, 1024, 0.02, seed=0)
+    c = oracle.histogram(w).astype(np.float64)
+    pal = oracle.palette(c.astype(np.uint64))
+    assert c[pal].sum() / c.sum() > 0.99
+    p = c[c > 0] / c.sum()
+    assert 2.4 < -(p * np.log2(p)).sum() < 2.8
+    blob, info = oracle.compress(w)
+    ratio = len(blob) / (2 * w.size)
+    assert 0.66 < ratio < 0.71                     # blog: ~30% fewer MLP bytes
+
+
+# ---------------------------------------------------------------- fp64 matmul
+def test_matmul_one_hot_picks_columns(oracle):
+    w = wl.normal_weights(8, 128, 0.02, seed=1)
+    x = np.zeros((1, 128), np.uint16)
+    x[0, 37] = 0x3F80                                 # 1.0
+    y, a = oracle.matmul_f64(x, w)
+    assert np.array_equal(y[0], wl.bf16_to_f32(w[:, 37]).astype(np.float64))
+    assert np.array_equal(a[0], np.abs(y[0]))
+
+
+def test_matmul_exact_small_integers(oracle):
+    rng = np.random.default_rng(5)
+    xi = rng.integers(-8, 9, (3, 64)).astype(np.float32)
+    wi = rng.integers(-8, 9, (5, 64)).astype(np.float32)
+    y, _ = oracle.matmul_f64(wl.bf16_bits(xi), wl.bf16_bits(wi))
+    assert np.array_equal(y, xi.astype(np.int64) @ wi.astype(np.int64).T)
+
+
+def test_matmul_agrees_with_numpy_and_row_window(oracle):
+    w = wl.normal_weights(40, 256, 0.02, seed=2)
+    x = wl.activations(2, 256, seed=2)
+    ref = wl.bf16_to_f32(x).astype(np.float64) @ wl.bf16_to_f32(w).astype(np.float64).T
+    y, a = oracle.matmul_f64(x, w)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-15)
+    y2, _ = oracle.matmul_f64(x, w, n0=7, nr=9)
+    assert np.array_equal(y2, y[:, 7:16])
+    assert np.all(a >= np.abs(y))
+
+
+def test_swiglu_closed_form(oracle):
+    g = wl.bf16_bits(np.array([0.0, 1.0, -2.0, 3.5], np.float32))
+    u = wl.bf16_bits(np.array([5.0, 2.0, 1.0, -1.0], np.float32))
+    h = oracle.swiglu_f64(g, u)
+    z = np.array([0.0, 1.0, -2.0, 3.5])
+    assert np.allclose(h, z * (1 / (1 + np.exp(-z))) * np.array([5.0, 2.0, 1.0, -1.0]), rtol=1e-15)
+    assert h[0] == 0.0
