@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark: compressed-weight GEMV throughput on GB300.
+
+Workload: the Llama-3.1-8B-shaped gate_proj, W 14336 x 4096 BF16 drawn from
+N(0, 0.02) (seed 0), compressed once on the host (offline, as the Unweight
+blog builds its bundles ahead of time), then y = x W^T at batch 1 with the
+weights still compressed in HBM.  One step = one uw_matmul call with the
+plan uw_autotune picked.  The timed steps rotate over several device copies
+of the blob whose total size exceeds twice the L2 cache, so every step reads
+its weights from HBM.
+
+Prints one JSON line (rank 0).  `value` is compressed blob bytes read per
+second over all ranks (GB/s); the line also carries the compression ratio,
+the roofline of the fused kernel, the same library's uncompressed BF16 GEMV,
+the decompress-then-GEMV strategy and cuBLAS for context, an end-to-end
+number through the public API with host buffers, the CPU oracle timed on
+the host, and the SM clocks sampled during the timed region.
+
+--impl reference times the CPU oracle (decode + fp64 GEMV) on the host's
+cores on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "compressed-weight GEMV/GEMM GB/s (% of 8 TB/s HBM) and ratio vs BF16"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+ROWS, COLS, BATCH = 14336, 4096, 1
+WORKLOAD = "gate_proj 14336x4096 BF16 N(0,0.02) seed 0, compressed; y = x W^T, batch 1"
+KERNEL_SOURCES = ["decode.cuh", "gemv.cu", "format.h", "kernels.h"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-context", action="store_true", help="skip the context measurements")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "lossless_bf16_weight_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the fused kernel from the committed ncu
+    summary, only if the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "fused_gemv_gate_proj_b1.traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        if t.get("kernel_hash") == kernel_hash():
+            return float(t["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+        time.sleep(0.05)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        except Exception:
+            pass
+        return rows
+
+    @staticmethod
+    def summarize(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- oracle (CPU)
+def oracle_rate(sample_rows: int, reps: int = 1):
+    """Time the oracle's decode + fp64 GEMV on the first sample_rows rows."""
+    import oracle
+    import workloads as wl
+
+    oracle.build()
+    w = wl.normal_weights(ROWS, COLS, 0.02, seed=0)[:sample_rows]
+    x = wl.activations(BATCH, COLS, seed=0)
+    blob, _ = oracle.compress(w)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        wd = oracle.decompress(blob)
+        oracle.matmul_f64(x, wd)
+    dt = (time.perf_counter() - t0) / reps
+    return len(blob), dt
+
+
+def cpu_baseline(sample_rows: int = ROWS):
+    nbytes, dt = oracle_rate(sample_rows)
+    return {"value": round(nbytes / dt / 1e9, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "rows 0..%d of the gate_proj (%d weights): oracle bit-by-bit decode + fp64 GEMV, "
+                      "single thread, one pass" % (sample_rows - 1, sample_rows * COLS)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    import workloads as wl
+
+    oracle.build()
+    # size each step so that warmup + steps stay within ~2 minutes
+    probe_bytes, probe_dt = oracle_rate(32)
+    per_row = probe_dt / 32
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(ROWS, budget / per_row)))
+    w = wl.normal_weights(ROWS, COLS, 0.02, seed=0)[:rows]
+    x = wl.activations(BATCH, COLS, seed=0)
+    blob, _ = oracle.compress(w)
+    for _ in range(args.warmup):
+        oracle.matmul_f64(x, oracle.decompress(blob))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.matmul_f64(x, oracle.decompress(blob))
+    dt = time.perf_counter() - t0
+    value = len(blob) * args.steps / dt / 1e9
+    sample = ("rows 0..%d of the gate_proj per step (%d weights): oracle bit-by-bit decode + fp64 GEMV, "
+              "single thread" % (rows - 1, rows * COLS))
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "rows": ROWS, "cols": COLS, "batch": BATCH},
+            "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- ours (GPU)
+def time_graph(torch, fn, steps: int, warmup: int, group: int, stream):
+    """Run fn(i) `warmup` times, then time exactly `steps` calls: whole CUDA
+    graphs of `group` calls plus eager calls for the remainder."""
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(group):
+            fn(i)
+    torch.cuda.synchronize()
+    n_graph, rem = divmod(steps, group)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    return g, n_graph, rem, e0, e1
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import lossless_bf16_weight_gb300 as uw
+    import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    if not os.path.exists(uw.LIB_PATH):
+        uw.build()
+    uw.load()
+
+    w = wl.normal_weights(ROWS, COLS, 0.02, seed=0)
+    x = wl.activations(BATCH, COLS, seed=0)
+    t0 = time.perf_counter()
+    blob = uw.compress(w)
+    compress_s = time.perf_counter() - t0
+    desc = uw.blob_info(blob)
+    nblob = int(desc.blob_bytes)
+    ratio = nblob / (2 * ROWS * COLS)
+
+    props = torch.cuda.get_device_properties(local)
+    l2 = getattr(props, "L2_cache_size", 126 << 20)
+    copies = max(3, math.ceil(2.5 * l2 / nblob) + 1)
+    blobs = [torch.from_numpy(blob).cuda() for _ in range(copies)]
+    xd = torch.from_numpy(x.view(np.int16)).cuda()
+    yd = torch.empty(BATCH, ROWS, dtype=torch.int16, device="cuda")
+
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    tune_ws = torch.empty(uw.autotune_workspace_size(desc, [BATCH]), dtype=torch.uint8, device="cuda")
+    plan = uw.autotune(desc, blobs[0], [BATCH], tune_ws, stream)[0]
+    del tune_ws
+    ws = torch.empty(uw.workspace_size(desc, BATCH, plan), dtype=torch.uint8, device="cuda")
+    uw.workspace_init(ws, stream)
+    launches_per_step = 1 if plan.strategy == uw.STRATEGY_FUSED else 2
+
+    def step(i):
+        uw.matmul(desc, blobs[i % copies], xd, yd, ws, plan, stream)
+
+    group = copies * max(1, 100 // copies)
+    g, n_graph, rem, e0, e1 = time_graph(torch, step, args.steps, args.warmup, group, stream)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n_graph):
+        g.replay()
+    for i in range(rem):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    samples = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status = uw.check_status(ws, stream)
+    assert status == 0, "device reported status %d" % status
+
+    per_step_s = ms / 1e3 / args.steps
+    value = nblob * args.steps * world / (ms / 1e3) / 1e9
+    algo_bytes = nblob + 2 * BATCH * COLS + 2 * BATCH * ROWS
+    kernel_s = per_step_s / launches_per_step if plan.strategy == uw.STRATEGY_FUSED else None
+    hbm, hbm_kind = peaks()
+    achieved = algo_bytes / per_step_s / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows": ROWS, "cols": COLS, "batch": BATCH,
+                   "plan": {"strategy": "fused" if plan.strategy == uw.STRATEGY_FUSED else "decompress+gemv",
+                            "variant": uw.variant_name(plan.strategy, plan.variant)},
+                   "l2": "rotating %d device copies of the blob (%.0f MB > 2x L2 %.0f MB)" % (
+                       copies, copies * nblob / 1e6, l2 / 1e6),
+                   "parallelism": "replicas x%d" % world},
+        "ratio_vs_bf16": round(ratio, 4),
+        "pct_of_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "compressed_bytes": nblob, "bf16_bytes": 2 * ROWS * COLS,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": profiled_traffic(),
+                     "peak_kind": hbm_kind, "bytes_per_launch": algo_bytes},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": ClockSampler.summarize(samples),
+        "compress_host_s": round(compress_s, 3),
+    }
+
+    if not args.no_context:
+        line["context"] = context_measurements(torch, uw, w, x, desc, blobs, xd, stream, plan)
+        line["e2e"] = e2e_measurement(torch, uw, desc, blobs, x, stream, plan, args)
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _time_steps(torch, fn, steps, stream, copies):
+    group = copies * max(1, 50 // copies)
+    g, n_graph, rem, e0, e1 = time_graph(torch, fn, steps, 10, group, stream)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n_graph):
+        g.replay()
+    for i in range(rem):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps * 1e3  # microseconds per step
+
+
+def context_measurements(torch, uw, w, x, desc, blobs, xd, stream, plan):
+    """Same library's uncompressed GEMV, the decompress-then-GEMV strategy
+    and cuBLAS (torch.matmul) on the same shape, each from HBM."""
+    out = {}
+    steps = 2000
+    bf16_bytes = 2 * ROWS * COLS
+    l2 = getattr(torch.cuda.get_device_properties(torch.cuda.current_device()), "L2_cache_size", 126 << 20)
+    wcopies = max(3, math.ceil(2.5 * l2 / bf16_bytes) + 1)
+    wdev = [torch.from_numpy(w.view(np.int16)).cuda() for _ in range(wcopies)]
+    yd = torch.empty(BATCH, ROWS, dtype=torch.int16, device="cuda")
+    d = uw.Desc()
+    d.rows, d.cols = ROWS, COLS
+    variant = plan.variant
+    ws = torch.empty(uw.workspace_size(d, BATCH, uw.Plan(uw.STRATEGY_FUSED, variant, BATCH, 0.0)),
+                     dtype=torch.uint8, device="cuda")
+    uw.workspace_init(ws, stream)
+    us = _time_steps(torch, lambda i: uw.matmul_bf16(wdev[i % wcopies], xd, yd, ws, variant, stream), steps, stream,
+                     wcopies)
+    out["uncompressed_gemv_same_variant"] = {"us": round(us, 3), "weight_GBps": round(bf16_bytes / us / 1e3, 1)}
+    best_unc = (us, uw.variant_name(1, variant))
+    for v in range(uw.variant_count(1)):
+        if v == variant:
+            continue
+        wsv = torch.empty(uw.workspace_size(d, BATCH, uw.Plan(1, v, BATCH, 0.0)), dtype=torch.uint8, device="cuda")
+        uw.workspace_init(wsv, stream)
+        try:
+            u2 = _time_steps(torch, lambda i: uw.matmul_bf16(wdev[i % wcopies], xd, yd, wsv, v, stream), 500,
+                             stream, wcopies)
+        except Exception:
+            continue
+        if u2 < best_unc[0]:
+            best_unc = (u2, uw.variant_name(1, v))
+    out["uncompressed_gemv_best"] = {"us": round(best_unc[0], 3), "variant": best_unc[1],
+                                     "weight_GBps": round(bf16_bytes / best_unc[0] / 1e3, 1)}
+    pd = uw.Plan(uw.STRATEGY_DECOMPRESS_GEMM, variant, BATCH, 0.0)
+    wsd = torch.empty(uw.workspace_size(desc, BATCH, pd), dtype=torch.uint8, device="cuda")
+    uw.workspace_init(wsd, stream)
+    us_d = _time_steps(torch, lambda i: uw.matmul(desc, blobs[i % len(blobs)], xd, yd, wsd, pd, stream), 500,
+                       stream, len(blobs))
+    out["decompress_then_gemv"] = {"us": round(us_d, 3)}
+    wsdc = torch.empty(256, dtype=torch.uint8, device="cuda")
+    uw.workspace_init(wsdc, stream)
+    wout = torch.empty(ROWS, COLS, dtype=torch.int16, device="cuda")
+    us_dc = _time_steps(torch, lambda i: uw.decompress(desc, blobs[i % len(blobs)], wout, wsdc, stream), 500,
+                        stream, len(blobs))
+    out["decompress_only"] = {"us": round(us_dc, 3),
+                              "GBps_read_plus_write": round((desc.blob_bytes + bf16_bytes) / us_dc / 1e3, 1)}
+    xb = xd.view(torch.bfloat16)
+    wb = [t.view(torch.bfloat16) for t in wdev]
+    us_c = _time_steps(torch, lambda i: torch.matmul(xb, wb[i % wcopies].t()), 500, stream, wcopies)
+    out["cublas_bf16_torch_matmul"] = {"us": round(us_c, 3), "weight_GBps": round(bf16_bytes / us_c / 1e3, 1)}
+    return out
+
+
+def e2e_measurement(torch, uw, desc, blobs, x, stream, plan, args):
+    """Through the public API with host buffers: per step, copy x from pinned
+    host memory, run uw_matmul, copy y back to pinned host memory."""
+    steps = min(args.steps, 5000)
+    xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+    yh = torch.empty(BATCH, ROWS, dtype=torch.int16).pin_memory()
+    xd = torch.empty_like(xh, device="cuda")
+    yd = torch.empty(BATCH, ROWS, dtype=torch.int16, device="cuda")
+    ws = torch.empty(uw.workspace_size(desc, BATCH, plan), dtype=torch.uint8, device="cuda")
+    uw.workspace_init(ws, stream)
+
+    def step(i):
+        xd.copy_(xh, non_blocking=True)
+        uw.matmul(desc, blobs[i % len(blobs)], xd, yd, ws, plan, stream)
+        yh.copy_(yd, non_blocking=True)
+
+    us = _time_steps(torch, step, steps, stream, len(blobs))
+    return {"value": round(desc.blob_bytes / us / 1e3, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(xh.numel() * 2), "d2h_bytes_per_step": int(yh.numel() * 2),
+            "us_per_step": round(us, 3)}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,190 @@
+/*
+ * uw.h -- C ABI of the lossless BF16 weight compression library for NVIDIA
+ * GB300 (sm_103a).
+ *
+ * The method is the one the Unweight blog post ("Unweight: how we compressed
+ * an LLM 22% without sacrificing quality", Cloudflare) describes:
+ *   - a BF16 weight is 1 sign bit, 8 exponent bits and 7 mantissa bits; sign
+ *     and mantissa look random and are stored raw, one byte per weight
+ *     (paragraphs on the BF16 layout and on what is left uncompressed);
+ *   - the exponent byte is Huffman coded over a per-matrix palette of the 16
+ *     most common exponents (paragraphs on exponent skew and Huffman coding);
+ *   - a row of 64 weights that holds an exponent outside the palette keeps
+ *     its 64 raw exponent bytes: one decision per row (paragraph on rare
+ *     exponents);
+ *   - at inference the weights are either decompressed back to BF16 in HBM
+ *     and multiplied, or decoded on chip and fed straight to the matrix
+ *     multiply without ever being written back (paragraphs on the four
+ *     execution pipelines and the reconstructive matmul);
+ *   - an autotuner measures each choice per weight matrix and batch size
+ *     (paragraph on the autotuner).
+ *
+ * Conventions for every entry point:
+ *   - Weights W are [rows, cols] row-major BF16 (uint16 bit patterns), the
+ *     layout of a PyTorch Linear weight (out_features x in_features).
+ *     Activations x are [batch, cols] row-major BF16; outputs y are
+ *     [batch, rows] row-major BF16; y = x W^T with fp32 accumulation and
+ *     round-to-nearest-even to BF16.
+ *   - cols must be a positive multiple of 64 and rows positive, otherwise
+ *     UW_ERR_SHAPE.
+ *   - The caller owns all memory.  The library allocates no device memory:
+ *     pointers marked _dev are device pointers, _host host pointers.
+ *     Scratch space ("workspace") is passed in by the caller; its size comes
+ *     from uw_workspace_size and it must be cleared once with
+ *     uw_workspace_init before first use.  Kernels leave it ready for the
+ *     next call.  One workspace must not be used by two calls that may run
+ *     at the same time.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device work is enqueued on it and the call returns without
+ *     waiting, except where a function says it synchronises.
+ *   - Errors are returned as uw_status; nothing throws across the ABI.
+ *     Errors found by the GPU while decoding (a blob corrupted after
+ *     uw_blob_info checked its header) are recorded in the workspace and
+ *     reported by uw_check_status.
+ */
+#ifndef UW_H
+#define UW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    UW_OK = 0,
+    UW_ERR_INVALID_ARG = 1,      /* NULL pointer, negative size, bad plan      */
+    UW_ERR_SHAPE = 2,            /* rows <= 0, cols <= 0 or cols % 64 != 0     */
+    UW_ERR_BUFFER_TOO_SMALL = 3, /* output or workspace buffer too small       */
+    UW_ERR_CORRUPT = 4,          /* blob header or data inconsistent           */
+    UW_ERR_CUDA = 5,             /* a CUDA runtime call failed                 */
+    UW_ERR_TIMEOUT = 6,          /* a bounded device wait gave up              */
+    UW_ERR_UNSUPPORTED = 7,      /* valid request this build cannot run        */
+    UW_ERR_INTERNAL = 8
+} uw_status;
+
+/* Execution strategies (the blog's pipelines).  DECOMPRESS_GEMM restores
+ * BF16 weights into the workspace, then multiplies them.  FUSED decodes in
+ * registers / shared memory and never writes the weights back. */
+enum {
+    UW_STRATEGY_DEFAULT = -1,
+    UW_STRATEGY_DECOMPRESS_GEMM = 0,
+    UW_STRATEGY_FUSED = 1
+};
+
+/* Description of a compressed matrix, filled by uw_blob_info from the blob
+ * header (host copy).  All offsets are byte offsets from the blob start. */
+typedef struct {
+    int64_t rows, cols;
+    uint64_t blob_bytes;     /* total blob size                              */
+    uint64_t code_bits;      /* Huffman bits of all coded groups (no padding) */
+    uint64_t n_groups;       /* rows * cols / 64                              */
+    uint64_t n_escaped;      /* groups stored with raw exponents              */
+    uint64_t n_tiles;        /* ceil(rows / 32) * cols / 64                   */
+    int32_t n_palette;       /* palette entries in use (0..16)                */
+    int32_t lmax;            /* longest code length (6 in format version 1)   */
+    uint8_t palette[16];     /* exponent value of each symbol                 */
+    uint8_t code_len[16];    /* code length of each symbol, 0 = unused        */
+    uint64_t off_sm, off_glen, off_tcode, off_tesc, off_code, off_esc;
+} uw_desc;
+
+/* One tuned choice for (matrix, batch). */
+typedef struct {
+    int32_t strategy;        /* UW_STRATEGY_*                                  */
+    int32_t variant;         /* kernel variant inside the strategy             */
+    int64_t batch;           /* batch size the choice was measured at          */
+    float us;                /* measured time of one call, microseconds        */
+} uw_plan;
+
+/* uw_compress -- build the compressed blob of one weight matrix on the host.
+ * Follows the blog's paragraphs on exponent skew, Huffman coding of the
+ * exponent byte and rows of 64 with rare exponents: exponent histogram ->
+ * 16-entry palette -> escaped groups -> length-limited minimum-redundancy
+ * canonical code -> blob (format UWB1, laid out in the library source csrc/format.h).
+ *   w_host     [rows, cols] BF16 bits, host memory, read only.
+ *   blob_out   host buffer of *blob_bytes bytes, or NULL to query the size.
+ *   blob_bytes in: capacity of blob_out; out: size of the blob.
+ * Returns UW_ERR_BUFFER_TOO_SMALL (with *blob_bytes set) when blob_out is
+ * NULL or too small.  Uses the host's cores (OpenMP); deterministic. */
+uw_status uw_compress(const uint16_t *w_host, int64_t rows, int64_t cols,
+                      void *blob_out, size_t *blob_bytes);
+
+/* uw_blob_info -- validate a blob's header and section table (host copy of
+ * at least the first 256 bytes and its declared size) and fill *out.
+ *   bytes  size of the buffer holding the blob (>= header's blob size).
+ * Returns UW_ERR_CORRUPT for a bad magic, version, shape or section that
+ * does not fit. */
+uw_status uw_blob_info(const void *blob_host, size_t bytes, uw_desc *out);
+
+/* uw_workspace_size -- bytes of workspace the given call needs.
+ *   batch     activation rows of the uw_matmul call (0 for uw_decompress).
+ *   plan      the plan the call will use, or NULL for the default plan.   */
+uw_status uw_workspace_size(const uw_desc *d, int64_t batch, const uw_plan *plan,
+                            size_t *bytes);
+
+/* uw_workspace_init -- clear a freshly allocated workspace (stream ordered). */
+uw_status uw_workspace_init(void *ws_dev, size_t ws_bytes, void *stream);
+
+/* uw_decompress -- restore the exact BF16 weights into HBM (the blog's
+ * "full decode" pipeline).
+ *   blob_dev   device copy of the blob described by d.
+ *   w_dev      [rows, cols] BF16 output, device memory.
+ *   ws_dev     workspace (error word only; >= uw_workspace_size(d, 0, NULL)). */
+uw_status uw_decompress(const uw_desc *d, const void *blob_dev, uint16_t *w_dev,
+                        void *ws_dev, size_t ws_bytes, void *stream);
+
+/* uw_matmul -- y = x W^T with W still compressed (the blog's reconstructive
+ * matmul, or decompress-then-multiply, as the plan says).
+ *   x_dev   [batch, cols] BF16;  y_dev  [batch, rows] BF16 (written).
+ *   plan    strategy/variant to run, or NULL for the library's default for
+ *           this shape and batch.
+ * The result is bit-identical to uw_matmul_bf16 with the same variant on the
+ * original weights. */
+uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uint16_t *x_dev,
+                    int64_t batch, uint16_t *y_dev, const uw_plan *plan,
+                    void *ws_dev, size_t ws_bytes, void *stream);
+
+/* uw_matmul_bf16 -- the same kernels fed uncompressed BF16 weights: the
+ * baseline that compression is measured against.
+ *   w_dev   [rows, cols] BF16 device weights.  variant as in uw_plan. */
+uw_status uw_matmul_bf16(const uint16_t *w_dev, int64_t rows, int64_t cols,
+                         const uint16_t *x_dev, int64_t batch, uint16_t *y_dev,
+                         int32_t variant, void *ws_dev, size_t ws_bytes, void *stream);
+
+/* uw_autotune -- measure every (strategy, variant) candidate for each batch
+ * size and return the fastest per batch (the blog's autotuner, which picks a
+ * pipeline per weight matrix and batch size from measured throughput).
+ * Each timed call follows an overwrite of the L2 cache, so the weights are
+ * read from HBM.  Synchronises `stream`.  The workspace (size from
+ * uw_autotune_workspace_size) holds the run workspace, x and y scratch and
+ * the L2 overwrite buffer; it is left cleared for uw_matmul.
+ *   batches    n batch sizes; plans_out  n results (us = median time). */
+uw_status uw_autotune(const uw_desc *d, const void *blob_dev, const int64_t *batches,
+                      int32_t n, uw_plan *plans_out, void *ws_dev, size_t ws_bytes,
+                      void *stream);
+uw_status uw_autotune_workspace_size(const uw_desc *d, const int64_t *batches, int32_t n,
+                                     size_t *bytes);
+
+/* uw_swiglu -- h = bf16(silu(g) * u), silu(z) = z / (1 + e^-z) in fp32,
+ * the glue between the gate/up and down projections of a SwiGLU MLP.
+ * g_dev, u_dev, h_dev: n BF16 values each, device memory. */
+uw_status uw_swiglu(const uint16_t *g_dev, const uint16_t *u_dev, uint16_t *h_dev,
+                    int64_t n, void *stream);
+
+/* uw_check_status -- synchronise `stream`, read and clear the error word the
+ * kernels record in the workspace.  Returns UW_OK, UW_ERR_CORRUPT or
+ * UW_ERR_TIMEOUT (or UW_ERR_CUDA if the stream itself failed). */
+uw_status uw_check_status(void *ws_dev, void *stream);
+
+/* Variant names for diagnostics; NULL for an unknown (strategy, variant). */
+const char *uw_variant_name(int32_t strategy, int32_t variant);
+int32_t uw_variant_count(int32_t strategy);
+
+const char *uw_status_string(uw_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UW_H */

@@ -1,0 +1,226 @@
+"""Python binding of the lossless BF16 weight compression library (libuw.so).
+
+Every function here only marshals arguments into the C ABI declared in
+include/uw.h and has the same name without the ``uw_`` prefix.  All compute
+runs in the library's CUDA kernels (and its host compressor); PyTorch
+tensors merely provide device memory and the current CUDA stream.  There is
+no fallback: if libuw.so is missing, ``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libuw.so")
+
+UW_OK = 0
+STATUS_NAMES = {0: "UW_OK", 1: "UW_ERR_INVALID_ARG", 2: "UW_ERR_SHAPE", 3: "UW_ERR_BUFFER_TOO_SMALL",
+                4: "UW_ERR_CORRUPT", 5: "UW_ERR_CUDA", 6: "UW_ERR_TIMEOUT", 7: "UW_ERR_UNSUPPORTED",
+                8: "UW_ERR_INTERNAL"}
+STRATEGY_DEFAULT, STRATEGY_DECOMPRESS_GEMM, STRATEGY_FUSED = -1, 0, 1
+
+
+class UwError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s: %s (%d)" % (what, STATUS_NAMES.get(status, "?"), status))
+        self.status = status
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [
+        ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+        ("blob_bytes", ctypes.c_uint64), ("code_bits", ctypes.c_uint64),
+        ("n_groups", ctypes.c_uint64), ("n_escaped", ctypes.c_uint64), ("n_tiles", ctypes.c_uint64),
+        ("n_palette", ctypes.c_int32), ("lmax", ctypes.c_int32),
+        ("palette", ctypes.c_uint8 * 16), ("code_len", ctypes.c_uint8 * 16),
+        ("off_sm", ctypes.c_uint64), ("off_glen", ctypes.c_uint64), ("off_tcode", ctypes.c_uint64),
+        ("off_tesc", ctypes.c_uint64), ("off_code", ctypes.c_uint64), ("off_esc", ctypes.c_uint64),
+    ]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("strategy", ctypes.c_int32), ("variant", ctypes.c_int32),
+                ("batch", ctypes.c_int64), ("us", ctypes.c_float)]
+
+    def __repr__(self):
+        return "Plan(strategy=%d, variant=%d, batch=%d, us=%.2f)" % (
+            self.strategy, self.variant, self.batch, self.us)
+
+
+_lib = None
+
+# (name, restype, argtypes) of every symbol in include/uw.h
+_P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+SIGNATURES = [
+    ("uw_compress", ctypes.c_int, [_P, _I64, _I64, _P, ctypes.POINTER(_SZ)]),
+    ("uw_blob_info", ctypes.c_int, [_P, _SZ, ctypes.POINTER(Desc)]),
+    ("uw_workspace_size", ctypes.c_int, [ctypes.POINTER(Desc), _I64, ctypes.POINTER(Plan), ctypes.POINTER(_SZ)]),
+    ("uw_workspace_init", ctypes.c_int, [_P, _SZ, _P]),
+    ("uw_decompress", ctypes.c_int, [ctypes.POINTER(Desc), _P, _P, _P, _SZ, _P]),
+    ("uw_matmul", ctypes.c_int, [ctypes.POINTER(Desc), _P, _P, _I64, _P, ctypes.POINTER(Plan), _P, _SZ, _P]),
+    ("uw_matmul_bf16", ctypes.c_int, [_P, _I64, _I64, _P, _I64, _P, _I32, _P, _SZ, _P]),
+    ("uw_autotune", ctypes.c_int, [ctypes.POINTER(Desc), _P, ctypes.POINTER(_I64), _I32, ctypes.POINTER(Plan),
+                                   _P, _SZ, _P]),
+    ("uw_autotune_workspace_size", ctypes.c_int, [ctypes.POINTER(Desc), ctypes.POINTER(_I64), _I32,
+                                                  ctypes.POINTER(_SZ)]),
+    ("uw_swiglu", ctypes.c_int, [_P, _P, _P, _I64, _P]),
+    ("uw_check_status", ctypes.c_int, [_P, _P]),
+    ("uw_variant_name", ctypes.c_char_p, [_I32, _I32]),
+    ("uw_variant_count", ctypes.c_int32, [_I32]),
+    ("uw_status_string", ctypes.c_char_p, [ctypes.c_int]),
+]
+
+
+def build(force: bool = False) -> str:
+    from .build import build as _build
+    return _build(force=force)
+
+
+def load():
+    """Load libuw.so (built beforehand by build()).  Raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libuw.so is not built (run lossless_bf16_weight_gb300.build())")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, res, args in SIGNATURES:
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != UW_OK:
+        raise UwError(status, what)
+
+
+def _ptr(t) -> int:
+    """Device or host address of a torch tensor or numpy array."""
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _plan_ptr(plan):
+    return None if plan is None else ctypes.byref(plan)
+
+
+# ---------------------------------------------------------------- host side
+def compress(w: np.ndarray) -> np.ndarray:
+    """uw_compress: BF16 weight matrix (uint16 bits, [rows, cols]) -> blob bytes (uint8)."""
+    w = np.ascontiguousarray(w)
+    if w.dtype != np.uint16 or w.ndim != 2:
+        raise TypeError("w must be a 2-D uint16 array of BF16 bit patterns")
+    L = load()
+    size = ctypes.c_size_t(0)
+    s = L.uw_compress(w.ctypes.data, w.shape[0], w.shape[1], None, ctypes.byref(size))
+    if s != 3:  # UW_ERR_BUFFER_TOO_SMALL answers the size query
+        _check(s, "uw_compress")
+    blob = np.empty(size.value, np.uint8)
+    _check(L.uw_compress(w.ctypes.data, w.shape[0], w.shape[1], blob.ctypes.data, ctypes.byref(size)),
+           "uw_compress")
+    return blob
+
+
+def blob_info(blob) -> Desc:
+    """uw_blob_info on a host copy of the blob (numpy uint8 or bytes)."""
+    b = np.frombuffer(blob, np.uint8) if isinstance(blob, (bytes, bytearray)) else np.ascontiguousarray(blob)
+    d = Desc()
+    _check(load().uw_blob_info(b.ctypes.data, b.size, ctypes.byref(d)), "uw_blob_info")
+    return d
+
+
+def blob_info_status(blob) -> int:
+    b = np.frombuffer(blob, np.uint8) if isinstance(blob, (bytes, bytearray)) else np.ascontiguousarray(blob)
+    d = Desc()
+    return int(load().uw_blob_info(b.ctypes.data, b.size, ctypes.byref(d)))
+
+
+def workspace_size(desc: Desc, batch: int = 0, plan: Plan | None = None) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().uw_workspace_size(ctypes.byref(desc), batch, _plan_ptr(plan), ctypes.byref(n)),
+           "uw_workspace_size")
+    return n.value
+
+
+def autotune_workspace_size(desc: Desc, batches) -> int:
+    arr = (ctypes.c_int64 * len(batches))(*batches)
+    n = ctypes.c_size_t(0)
+    _check(load().uw_autotune_workspace_size(ctypes.byref(desc), arr, len(batches), ctypes.byref(n)),
+           "uw_autotune_workspace_size")
+    return n.value
+
+
+def variant_count(strategy: int) -> int:
+    return int(load().uw_variant_count(strategy))
+
+
+def variant_name(strategy: int, variant: int) -> str | None:
+    r = load().uw_variant_name(strategy, variant)
+    return None if r is None else r.decode()
+
+
+def status_string(status: int) -> str:
+    return load().uw_status_string(status).decode()
+
+
+# ---------------------------------------------------------------- device side
+def workspace_init(ws, stream=None):
+    _check(load().uw_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "uw_workspace_init")
+
+
+def decompress(desc: Desc, blob_dev, w_out, ws, stream=None):
+    _check(load().uw_decompress(ctypes.byref(desc), _ptr(blob_dev), _ptr(w_out), _ptr(ws),
+                                ws.numel() * ws.element_size(), _stream(stream)), "uw_decompress")
+
+
+def matmul(desc: Desc, blob_dev, x, y, ws, plan: Plan | None = None, stream=None):
+    """y[batch, rows] = x[batch, cols] W^T with W compressed in blob_dev."""
+    batch = x.shape[0] if x.dim() == 2 else 1
+    _check(load().uw_matmul(ctypes.byref(desc), _ptr(blob_dev), _ptr(x), batch, _ptr(y), _plan_ptr(plan),
+                            _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "uw_matmul")
+
+
+def matmul_status(desc: Desc, blob_dev, x, y, ws, plan: Plan | None = None, stream=None) -> int:
+    batch = x.shape[0] if x.dim() == 2 else 1
+    return int(load().uw_matmul(ctypes.byref(desc), _ptr(blob_dev), _ptr(x), batch, _ptr(y), _plan_ptr(plan),
+                                _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def matmul_bf16(w, x, y, ws, variant: int = -1, stream=None):
+    rows, cols = w.shape
+    batch = x.shape[0] if x.dim() == 2 else 1
+    _check(load().uw_matmul_bf16(_ptr(w), rows, cols, _ptr(x), batch, _ptr(y), variant, _ptr(ws),
+                                 ws.numel() * ws.element_size(), _stream(stream)), "uw_matmul_bf16")
+
+
+def autotune(desc: Desc, blob_dev, batches, ws, stream=None) -> list[Plan]:
+    arr = (ctypes.c_int64 * len(batches))(*batches)
+    plans = (Plan * len(batches))()
+    _check(load().uw_autotune(ctypes.byref(desc), _ptr(blob_dev), arr, len(batches), plans, _ptr(ws),
+                              ws.numel() * ws.element_size(), _stream(stream)), "uw_autotune")
+    return list(plans)
+
+
+def swiglu(g, u, h, stream=None):
+    _check(load().uw_swiglu(_ptr(g), _ptr(u), _ptr(h), g.numel(), _stream(stream)), "uw_swiglu")
+
+
+def check_status(ws, stream=None) -> int:
+    """uw_check_status: synchronises and returns the device error status (0 = ok)."""
+    return int(load().uw_check_status(_ptr(ws), _stream(stream)))

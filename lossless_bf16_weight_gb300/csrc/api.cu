@@ -1,0 +1,415 @@
+// C ABI entry points: blob validation, workspace layout, dispatch to the
+// kernels.  No device memory is allocated here; everything comes from the
+// caller's buffers.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "format.h"
+#include "kernels.h"
+#include "uw.h"
+
+namespace uw {
+
+namespace {
+
+uint32_t rd32(const uint8_t *p) {
+    uint32_t v;
+    std::memcpy(&v, p, 4);
+    return v;
+}
+uint64_t rd64(const uint8_t *p) {
+    uint64_t v;
+    std::memcpy(&v, p, 8);
+    return v;
+}
+
+cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+// CUDA-core kernel variants: warps per CTA x split count.
+constexpr int kWarpChoices[3] = {4, 8, 16};
+constexpr int kSplitChoices = 5;  // 1, 2, 4, 8, 16
+constexpr int kGemvVariants = 3 * kSplitChoices;
+constexpr int kMaxBatchChunk = 8;
+
+struct GemvVariant {
+    int warps, splits;
+};
+
+GemvVariant gemv_variant(int v) { return {kWarpChoices[v % 3], 1 << (v / 3)}; }
+
+int pad_batch(int64_t b) {
+    const int c = int(std::min<int64_t>(b, kMaxBatchChunk));
+    return c <= 1 ? 1 : c <= 2 ? 2 : c <= 4 ? 4 : 8;
+}
+
+// Default variant: 8 warps; enough CTAs to fill the GPU twice when the
+// matrix has few row blocks; at least one tile per warp.
+int default_gemv_variant(int64_t rows, int64_t cols, int64_t batch) {
+    const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
+    const int64_t gpr = cols / kGroup;
+    const int bp = pad_batch(batch);
+    int si = 0;
+    while (si + 1 < kSplitChoices && nrb * (int64_t(1) << si) < 2 * 152 &&
+           gpr / (int64_t(1) << (si + 1)) >= 8)
+        si++;
+    while (si + 1 < kSplitChoices && gemv_smem_bytes(cols, 8, 1 << si, bp, true) > size_t(kMaxSmemPerBlock))
+        si++;
+    return 1 + 3 * si;
+}
+
+WsLayout layout_for(int64_t rows, int64_t cols, int64_t batch, int strategy, int variant) {
+    WsLayout L;
+    const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
+    const GemvVariant gv = gemv_variant(variant);
+    const int bp = pad_batch(batch);
+    L.status = 0;
+    L.counters = 256;
+    L.partial = align_up(L.counters + 4 * uint64_t(nrb), 256);
+    L.weights = align_up(L.partial + 4 * uint64_t(nrb) * gv.splits * bp * 32, 256);
+    L.total = L.weights;
+    if (strategy == UW_STRATEGY_DECOMPRESS_GEMM)
+        L.total = align_up(L.weights + 2 * uint64_t(rows) * uint64_t(cols), 256);
+    return L;
+}
+
+struct ResolvedPlan {
+    int strategy, variant;
+};
+
+uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t batch, ResolvedPlan *out) {
+    out->strategy = UW_STRATEGY_FUSED;
+    out->variant = default_gemv_variant(rows, cols, batch);
+    if (plan) {
+        if (plan->strategy != UW_STRATEGY_DEFAULT) {
+            if (plan->strategy != UW_STRATEGY_FUSED && plan->strategy != UW_STRATEGY_DECOMPRESS_GEMM)
+                return UW_ERR_INVALID_ARG;
+            out->strategy = plan->strategy;
+        }
+        if (plan->variant >= 0) {
+            if (plan->variant >= kGemvVariants)
+                return UW_ERR_INVALID_ARG;
+            out->variant = plan->variant;
+        }
+    }
+    return UW_OK;
+}
+
+// Batch rows go through the CUDA-core kernel in chunks of at most 8.
+uw_status run_gemv(GemvParams p, int variant, bool compressed, cudaStream_t stream) {
+    const GemvVariant gv = gemv_variant(variant);
+    p.splits = gv.splits;
+    const int64_t total = p.batch;
+    for (int64_t b0 = 0; b0 < total; b0 += kMaxBatchChunk) {
+        GemvParams q = p;
+        q.batch = std::min<int64_t>(kMaxBatchChunk, total - b0);
+        q.x = p.x + b0 * p.cols;
+        q.y = p.y + b0 * p.rows;
+        const uw_status s = launch_gemv(q, gv.warps, pad_batch(q.batch), compressed, stream);
+        if (s != UW_OK)
+            return s;
+    }
+    return UW_OK;
+}
+
+}  // namespace
+
+bool ensure_smem_limit(const void *kernel, size_t bytes) {
+    struct Entry {
+        const void *kernel;
+        int device;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return false;
+    std::lock_guard<std::mutex> lock(mu);
+    for (Entry &e : done)
+        if (e.kernel == kernel && e.device == dev) {
+            if (e.bytes >= bytes)
+                return true;
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)) != cudaSuccess)
+                return false;
+            e.bytes = bytes;
+            return true;
+        }
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)) != cudaSuccess)
+        return false;
+    done.push_back({kernel, dev, bytes});
+    return true;
+}
+
+void canonical_code_values(const uint8_t len[16], uint16_t code[16]) {
+    int per_len[kLmax + 2] = {};
+    for (int s = 0; s < 16; s++)
+        if (len[s] <= kLmax)
+            per_len[len[s]]++;
+    per_len[0] = 0;
+    uint32_t next[kLmax + 2] = {};
+    uint32_t c = 0;
+    for (int l = 1; l <= kLmax; l++) {
+        c = (c + per_len[l - 1]) << 1;
+        next[l] = c;
+    }
+    for (int s = 0; s < 16; s++)
+        code[s] = (len[s] && len[s] <= kLmax) ? uint16_t(next[len[s]]++) : 0;
+}
+
+void fill_blob_view(const uw_desc &d, const void *blob_dev, BlobView *v) {
+    const uint8_t *b = static_cast<const uint8_t *>(blob_dev);
+    v->sm = b + d.off_sm;
+    v->glen = b + d.off_glen;
+    v->tcode = reinterpret_cast<const uint32_t *>(b + d.off_tcode);
+    v->tesc = reinterpret_cast<const uint32_t *>(b + d.off_tesc);
+    v->code = b + d.off_code;
+    v->esc = b + d.off_esc;
+    v->code_bytes = d.off_esc - d.off_code;
+    v->n_escaped = d.n_escaped;
+    v->rows = d.rows;
+    v->cols = d.cols;
+    uint16_t code[16];
+    canonical_code_values(d.code_len, code);
+    std::memset(v->prefix6, 0, sizeof v->prefix6);
+    for (int s = 0; s < d.n_palette; s++) {
+        const int l = d.code_len[s];
+        if (!l)
+            continue;
+        const int lo = code[s] << (6 - l), hi = (code[s] + 1) << (6 - l);
+        for (int p = lo; p < hi && p < 64; p++)
+            v->prefix6[p] = uint16_t((d.palette[s] << 4) | l);
+    }
+}
+
+}  // namespace uw
+
+using namespace uw;
+
+extern "C" const char *uw_status_string(uw_status s) {
+    switch (s) {
+        case UW_OK: return "ok";
+        case UW_ERR_INVALID_ARG: return "invalid argument";
+        case UW_ERR_SHAPE: return "unsupported shape (rows, cols > 0 and cols % 64 == 0 required)";
+        case UW_ERR_BUFFER_TOO_SMALL: return "buffer too small";
+        case UW_ERR_CORRUPT: return "corrupt blob";
+        case UW_ERR_CUDA: return "CUDA error";
+        case UW_ERR_TIMEOUT: return "device wait timed out";
+        case UW_ERR_UNSUPPORTED: return "unsupported request";
+        case UW_ERR_INTERNAL: return "internal error";
+    }
+    return "unknown status";
+}
+
+extern "C" uw_status uw_blob_info(const void *blob_host, size_t bytes, uw_desc *out) {
+    if (!blob_host || !out)
+        return UW_ERR_INVALID_ARG;
+    const uint8_t *b = static_cast<const uint8_t *>(blob_host);
+    if (bytes < size_t(kHeaderBytes) || rd32(b + hdr::magic) != kMagic || rd32(b + hdr::version) != kVersion)
+        return UW_ERR_CORRUPT;
+    uw_desc d;
+    std::memset(&d, 0, sizeof d);
+    d.rows = int64_t(rd64(b + hdr::rows));
+    d.cols = int64_t(rd64(b + hdr::cols));
+    d.lmax = int32_t(rd32(b + hdr::lmax));
+    d.n_palette = int32_t(rd32(b + hdr::n_palette));
+    std::memcpy(d.palette, b + hdr::palette, 16);
+    std::memcpy(d.code_len, b + hdr::code_len, 16);
+    d.n_groups = rd64(b + hdr::n_groups);
+    d.n_escaped = rd64(b + hdr::n_escaped);
+    d.n_tiles = rd64(b + hdr::n_tiles);
+    d.code_bits = rd64(b + hdr::code_bits);
+    d.off_sm = rd64(b + hdr::off_sm);
+    d.off_glen = rd64(b + hdr::off_glen);
+    d.off_tcode = rd64(b + hdr::off_tcode);
+    d.off_tesc = rd64(b + hdr::off_tesc);
+    d.off_code = rd64(b + hdr::off_code);
+    d.off_esc = rd64(b + hdr::off_esc);
+    d.blob_bytes = rd64(b + hdr::blob_bytes);
+    if (rd32(b + hdr::group) != uint32_t(kGroup) || rd32(b + hdr::tile_rows) != uint32_t(kTileRows) ||
+        d.lmax != kLmax || d.n_palette < 0 || d.n_palette > kPalette)
+        return UW_ERR_CORRUPT;
+    if (d.rows <= 0 || d.cols <= 0 || d.cols % kGroup || d.rows > (int64_t(1) << 40) || d.cols > (int64_t(1) << 40))
+        return UW_ERR_CORRUPT;
+    const uint64_t rows = uint64_t(d.rows), cols = uint64_t(d.cols);
+    const uint64_t gpr = cols / kGroup;
+    const uint64_t ntiles = (rows + kTileRows - 1) / kTileRows * gpr;
+    if (d.n_groups != rows * gpr || d.n_tiles != ntiles || d.n_escaped > d.n_groups)
+        return UW_ERR_CORRUPT;
+    // sections in order, 256-aligned, inside the blob
+    const uint64_t sec[6] = {d.off_sm, d.off_glen, d.off_tcode, d.off_tesc, d.off_code, d.off_esc};
+    for (uint64_t o : sec)
+        if (o % kSectionAlign)
+            return UW_ERR_CORRUPT;
+    if (d.off_sm != uint64_t(kHeaderBytes) || d.off_glen < d.off_sm + rows * cols ||
+        d.off_tcode < d.off_glen + d.n_groups || d.off_tesc < d.off_tcode + 4 * (ntiles + 1) ||
+        d.off_code < d.off_tesc + 4 * (ntiles + 1) || d.off_esc < d.off_code ||
+        d.off_esc + 64 * d.n_escaped > d.blob_bytes || d.blob_bytes > bytes)
+        return UW_ERR_CORRUPT;
+    // a prefix code on the palette, lengths within the limit
+    double kraft = 0.0;
+    for (int s = 0; s < kPalette; s++) {
+        if (d.code_len[s] > kLmax || (s >= d.n_palette && d.code_len[s]))
+            return UW_ERR_CORRUPT;
+        if (d.code_len[s])
+            kraft += 1.0 / double(1u << d.code_len[s]);
+        for (int t = 0; t < s && s < d.n_palette; t++)
+            if (d.palette[t] == d.palette[s])
+                return UW_ERR_CORRUPT;
+    }
+    if (kraft > 1.0)
+        return UW_ERR_CORRUPT;
+    // tile tables against the group lengths
+    const uint32_t *tcode = reinterpret_cast<const uint32_t *>(b + d.off_tcode);
+    const uint32_t *tesc = reinterpret_cast<const uint32_t *>(b + d.off_tesc);
+    const uint8_t *glen = b + d.off_glen;
+    if (tcode[0] != 0 || tesc[0] != 0 || tesc[ntiles] != d.n_escaped ||
+        uint64_t(tcode[ntiles]) * 16 > d.off_esc - d.off_code)
+        return UW_ERR_CORRUPT;
+    uint64_t bits_hint = 0;
+    for (uint64_t t = 0; t < ntiles; t++) {
+        const uint64_t rb = t / gpr, kg = t % gpr;
+        const uint64_t R = std::min<uint64_t>(kTileRows, rows - rb * kTileRows);
+        const uint64_t q0 = kTileRows * rb * gpr + R * kg;
+        uint64_t sum = 0, nz = 0;
+        for (uint64_t j = 0; j < R; j++) {
+            const unsigned g = glen[q0 + j];
+            if (g > unsigned(kMaxGroupCodeBytes))
+                return UW_ERR_CORRUPT;
+            sum += g;
+            nz += g == 0;
+        }
+        if (tcode[t + 1] < tcode[t] || uint64_t(tcode[t + 1] - tcode[t]) != (sum + 15) / 16 ||
+            tesc[t + 1] < tesc[t] || tesc[t + 1] - tesc[t] != nz)
+            return UW_ERR_CORRUPT;
+        bits_hint += sum;
+    }
+    if (d.code_bits > 8 * bits_hint || d.code_bits + 8 * (d.n_groups - d.n_escaped) < 8 * bits_hint)
+        return UW_ERR_CORRUPT;
+    *out = d;
+    return UW_OK;
+}
+
+extern "C" uw_status uw_workspace_size(const uw_desc *d, int64_t batch, const uw_plan *plan, size_t *bytes) {
+    if (!d || !bytes || batch < 0)
+        return UW_ERR_INVALID_ARG;
+    ResolvedPlan rp;
+    const uw_status s = resolve_plan(plan, d->rows, d->cols, std::max<int64_t>(batch, 1), &rp);
+    if (s != UW_OK)
+        return s;
+    *bytes = layout_for(d->rows, d->cols, std::max<int64_t>(batch, 1), rp.strategy, rp.variant).total;
+    return UW_OK;
+}
+
+extern "C" uw_status uw_workspace_init(void *ws, size_t ws_bytes, void *stream) {
+    if (!ws)
+        return UW_ERR_INVALID_ARG;
+    return cudaMemsetAsync(ws, 0, ws_bytes, as_stream(stream)) == cudaSuccess ? UW_OK : UW_ERR_CUDA;
+}
+
+extern "C" uw_status uw_check_status(void *ws, void *stream) {
+    if (!ws)
+        return UW_ERR_INVALID_ARG;
+    uint32_t word = 0;
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemcpyAsync(&word, ws, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return UW_ERR_CUDA;
+    if (!word)
+        return UW_OK;
+    if (cudaMemsetAsync(ws, 0, 4, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+        return UW_ERR_CUDA;
+    return (word & kStatusTimeout) ? UW_ERR_TIMEOUT : UW_ERR_CORRUPT;
+}
+
+extern "C" uw_status uw_decompress(const uw_desc *d, const void *blob_dev, uint16_t *w_dev, void *ws,
+                                   size_t ws_bytes, void *stream) {
+    if (!d || !blob_dev || !w_dev || !ws)
+        return UW_ERR_INVALID_ARG;
+    if (ws_bytes < 256)
+        return UW_ERR_BUFFER_TOO_SMALL;
+    BlobView v;
+    fill_blob_view(*d, blob_dev, &v);
+    return launch_decompress(v, w_dev, static_cast<uint32_t *>(ws), as_stream(stream));
+}
+
+extern "C" uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uint16_t *x, int64_t batch,
+                               uint16_t *y, const uw_plan *plan, void *ws, size_t ws_bytes, void *stream) {
+    if (!d || !blob_dev || !x || !y || !ws || batch <= 0)
+        return UW_ERR_INVALID_ARG;
+    ResolvedPlan rp;
+    uw_status s = resolve_plan(plan, d->rows, d->cols, batch, &rp);
+    if (s != UW_OK)
+        return s;
+    const WsLayout L = layout_for(d->rows, d->cols, batch, rp.strategy, rp.variant);
+    if (ws_bytes < L.total)
+        return UW_ERR_BUFFER_TOO_SMALL;
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    GemvParams p{};
+    fill_blob_view(*d, blob_dev, &p.v);
+    p.x = x;
+    p.y = y;
+    p.partial = reinterpret_cast<float *>(wsb + L.partial);
+    p.counters = reinterpret_cast<uint32_t *>(wsb + L.counters);
+    p.status = reinterpret_cast<uint32_t *>(wsb + L.status);
+    p.rows = d->rows;
+    p.cols = d->cols;
+    p.batch = batch;
+    if (rp.strategy == UW_STRATEGY_DECOMPRESS_GEMM) {
+        uint16_t *w = reinterpret_cast<uint16_t *>(wsb + L.weights);
+        s = launch_decompress(p.v, w, p.status, as_stream(stream));
+        if (s != UW_OK)
+            return s;
+        p.w = w;
+        return run_gemv(p, rp.variant, false, as_stream(stream));
+    }
+    return run_gemv(p, rp.variant, true, as_stream(stream));
+}
+
+extern "C" uw_status uw_matmul_bf16(const uint16_t *w, int64_t rows, int64_t cols, const uint16_t *x,
+                                    int64_t batch, uint16_t *y, int32_t variant, void *ws, size_t ws_bytes,
+                                    void *stream) {
+    if (!w || !x || !y || !ws || batch <= 0)
+        return UW_ERR_INVALID_ARG;
+    if (rows <= 0 || cols <= 0 || cols % kGroup)
+        return UW_ERR_SHAPE;
+    if (variant >= kGemvVariants)
+        return UW_ERR_INVALID_ARG;
+    const int v = variant < 0 ? default_gemv_variant(rows, cols, batch) : variant;
+    const WsLayout L = layout_for(rows, cols, batch, UW_STRATEGY_FUSED, v);
+    if (ws_bytes < L.total)
+        return UW_ERR_BUFFER_TOO_SMALL;
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    GemvParams p{};
+    p.w = w;
+    p.x = x;
+    p.y = y;
+    p.partial = reinterpret_cast<float *>(wsb + L.partial);
+    p.counters = reinterpret_cast<uint32_t *>(wsb + L.counters);
+    p.status = reinterpret_cast<uint32_t *>(wsb + L.status);
+    p.rows = rows;
+    p.cols = cols;
+    p.batch = batch;
+    return run_gemv(p, v, false, as_stream(stream));
+}
+
+extern "C" uw_status uw_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h, int64_t n, void *stream) {
+    if (!g || !u || !h || n < 0)
+        return UW_ERR_INVALID_ARG;
+    return launch_swiglu(g, u, h, n, as_stream(stream));
+}
+
+extern "C" int32_t uw_variant_count(int32_t strategy) {
+    return (strategy == UW_STRATEGY_FUSED || strategy == UW_STRATEGY_DECOMPRESS_GEMM) ? kGemvVariants : 0;
+}
+
+extern "C" const char *uw_variant_name(int32_t strategy, int32_t variant) {
+    static const char *names[kGemvVariants] = {
+        "w4s1", "w8s1", "w16s1", "w4s2", "w8s2", "w16s2", "w4s4", "w8s4",
+        "w16s4", "w4s8", "w8s8", "w16s8", "w4s16", "w8s16", "w16s16"};
+    if (uw_variant_count(strategy) == 0 || variant < 0 || variant >= kGemvVariants)
+        return nullptr;
+    return names[variant];
+}

@@ -1,0 +1,97 @@
+// Decompress a blob back to BF16 weights in HBM (the Unweight blog's "full
+// decode" pipeline: the restored matrix can then go to any GEMM).
+//
+// Each warp decodes consecutive tiles with the shared tile decoder
+// (decode.cuh).  Lane j produces the 64 BF16 weights of row j; they pass
+// through a per-warp 4 KB shared-memory buffer (16-byte chunks XOR-swizzled
+// by row, conflict-free both ways) so that the global stores are coalesced
+// 128-byte row segments.
+#include "decode.cuh"
+#include "kernels.h"
+
+namespace uw {
+
+namespace {
+
+constexpr int kDecompWarps = 8;
+constexpr int kTilesPerWarp = 4;
+constexpr int kOutBufBytes = kTileRows * kGroup * 2;  // 4096
+
+__global__ void __launch_bounds__(kDecompWarps * 32, 2)
+    decompress_kernel(const BlobView v, uint16_t *__restrict__ out, uint32_t *status) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const DecodeShared ds = carve_common(smem);
+    uint32_t *wbuf = reinterpret_cast<uint32_t *>(smem + kCommonSmemBytes + size_t(warp) * kWarpBufBytes);
+    uint4 *obuf = reinterpret_cast<uint4 *>(smem + kCommonSmemBytes + size_t(kDecompWarps) * kWarpBufBytes +
+                                            size_t(warp) * kOutBufBytes);
+
+    const int64_t gpr = v.cols / kGroup;
+    const int64_t ntiles = (v.rows + kTileRows - 1) / kTileRows * gpr;
+    const int64_t t_lo = (int64_t(blockIdx.x) * kDecompWarps + warp) * kTilesPerWarp;
+    const int64_t t_hi = t_lo + kTilesPerWarp < ntiles ? t_lo + kTilesPerWarp : ntiles;
+
+    TileRaw raw;
+    uint32_t offs_next = 0;
+    if (t_lo < t_hi) {
+        tile_load(v, t_lo, tile_offsets_load(v, t_lo), raw);
+        if (t_lo + 1 < t_hi)
+            offs_next = tile_offsets_load(v, t_lo + 1);
+    }
+    build_tables(ds, v);
+    __syncthreads();
+
+    for (int64_t t = t_lo; t < t_hi; t++) {
+        const TileCoord tc = tile_coord(v, t);
+        uint4 sm[4];
+#pragma unroll
+        for (int c = 0; c < 4; c++)
+            sm[c] = raw.sm[c];
+        LaneStream ls;
+        tile_setup(v, ds, raw, tc.R, wbuf, ls, status);
+        if (t + 1 < t_hi) {
+            tile_load(v, t + 1, offs_next, raw);
+            if (t + 2 < t_hi)
+                offs_next = tile_offsets_load(v, t + 2);
+        }
+        uint32_t q[4];
+#pragma unroll
+        for (int I = 0; I < 32; I++) {
+            q[I & 3] = decode_pair(ls, I, sm_word(sm, I >> 1));
+            if ((I & 3) == 3) {
+                const int c = I >> 2;  // 16-byte chunk of the row segment
+                obuf[lane * 8 + (c ^ (lane & 7))] = make_uint4(q[0], q[1], q[2], q[3]);
+            }
+        }
+        tile_check(ls, status);
+        __syncwarp();
+        // coalesced stores: 4 rows x 128 bytes per instruction
+        const int c = lane & 7;
+#pragma unroll
+        for (int it = 0; it < 8; it++) {
+            const int r = it * 4 + (lane >> 3);
+            if (r < tc.R) {
+                const uint4 val = obuf[r * 8 + (c ^ (r & 7))];
+                uint16_t *dst = out + (tc.rb * kTileRows + r) * v.cols + tc.kg * kGroup + c * 8;
+                *reinterpret_cast<uint4 *>(dst) = val;
+            }
+        }
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status, cudaStream_t stream) {
+    const int64_t gpr = v.cols / kGroup;
+    const int64_t ntiles = (v.rows + kTileRows - 1) / kTileRows * gpr;
+    const int64_t per_cta = int64_t(kDecompWarps) * kTilesPerWarp;
+    const int64_t grid = (ntiles + per_cta - 1) / per_cta;
+    const size_t smem = size_t(kCommonSmemBytes) + size_t(kDecompWarps) * (kWarpBufBytes + kOutBufBytes);
+    if (!ensure_smem(decompress_kernel, smem))
+        return UW_ERR_CUDA;
+    decompress_kernel<<<dim3(unsigned(grid)), dim3(kDecompWarps * 32), smem, stream>>>(v, w_out, status);
+    return cudaGetLastError() == cudaSuccess ? UW_OK : UW_ERR_CUDA;
+}
+
+}  // namespace uw

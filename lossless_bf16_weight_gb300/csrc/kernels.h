@@ -1,0 +1,52 @@
+// Host-side interface between the C ABI entry points and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <mutex>
+#include <vector>
+#include <cstdint>
+
+#include "decode.cuh"
+#include "uw.h"
+
+namespace uw {
+
+constexpr int kMaxSmemPerBlock = 227 * 1024;
+
+struct GemvParams {
+    BlobView v;            // compressed weights (fused kernel)
+    const uint16_t *w;     // uncompressed weights (twin kernel)
+    const uint16_t *x;     // [batch, cols]
+    uint16_t *y;           // [batch, rows]
+    float *partial;        // [row blocks * splits][bp][32] split partial sums
+    uint32_t *counters;    // [row blocks] arrival counters, left at zero
+    uint32_t *status;      // device error word
+    int64_t rows, cols, batch;
+    int splits;
+};
+
+size_t gemv_smem_bytes(int64_t cols, int warps, int splits, int bp, bool compressed);
+uw_status launch_gemv(const GemvParams &p, int warps, int bp, bool compressed, cudaStream_t stream);
+
+uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status, cudaStream_t stream);
+uw_status launch_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h, int64_t n, cudaStream_t stream);
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device);
+// later launches skip the call, so they stay capturable in CUDA graphs.
+bool ensure_smem_limit(const void *kernel, size_t bytes);
+template <class Kernel>
+inline bool ensure_smem(Kernel *kern, size_t bytes) {
+    return ensure_smem_limit(reinterpret_cast<const void *>(kern), bytes);
+}
+
+// Host helpers (api.cu).
+void canonical_code_values(const uint8_t len[16], uint16_t code[16]);
+void fill_blob_view(const uw_desc &d, const void *blob_dev, BlobView *v);
+
+// Workspace layout: [status word | counters | split partials | weights].
+struct WsLayout {
+    size_t status = 0, counters = 0, partial = 0, weights = 0, total = 0;
+};
+
+}  // namespace uw

@@ -24,7 +24,7 @@
  *   [LUT16K]    the decoder keeps a ~16 KB Huffman lookup table in SMEM.
  *   [MATMUL]    the compressed weights feed y = x W^T (decode once, multiply).
  *
- * Readings taken where the page is silent (each is listed in the design doc):
+ * Readings taken where the page is silent:
  *   - "row of 64" = 64 consecutive weights along K inside one output row.
  *   - the Huffman alphabet is the palette (<=16 symbols); escaped groups are
  *     outside the code and keep their 64 raw exponent bytes.

@@ -41,5 +41,7 @@ def oracle():
 def uw():
     """The library's Python binding (builds the shared library if needed)."""
     import lossless_bf16_weight_gb300 as lib
+    if not os.path.exists(lib.LIB_PATH):
+        lib.build()
     lib.load()
     return lib

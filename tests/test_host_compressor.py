@@ -1,0 +1,123 @@
+"""Library host side against the oracle (no GPU needed): the blob the
+library writes must be byte-identical to the oracle's, its header checks
+must reject corrupted blobs, and the shared library must export every
+entry point include/uw.h declares."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib(uw):
+    return uw
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "uw.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(uw_\w+)\s*\(", text, re.M)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 14
+    so = ctypes.CDLL(lib.LIB_PATH)
+    bound = {n for n, _, _ in lib.SIGNATURES}
+    for n in names:
+        assert hasattr(so, n), n
+        assert n in bound, n
+
+
+CASES = {
+    "small": lambda: wl.normal_weights(256, 1024, 0.02, seed=0),
+    "ragged_rows": lambda: wl.normal_weights(77, 192, 0.02, seed=4),
+    "one_row": lambda: wl.normal_weights(1, 64, 0.02, seed=5),
+    "heavy": lambda: wl.heavy_tailed_weights(512, 512, seed=0),
+    "all_patterns": wl.all_bf16_patterns,
+    "zeros": lambda: np.zeros((40, 128), np.uint16),
+    "wide_sigma": lambda: wl.normal_weights(64, 4096, 0.04, seed=7),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_blob_identical_to_oracle(lib, oracle, name):
+    w = CASES[name]()
+    ob, oinfo = oracle.compress(w)
+    lb = lib.compress(w)
+    d = lib.blob_info(lb)
+    assert list(d.palette)[: d.n_palette] == oinfo["palette"]
+    assert list(d.code_len) == oinfo["code_len"]
+    assert d.code_bits == oinfo["code_bits"] and d.n_escaped == oinfo["n_escaped"]
+    assert lb.tobytes() == ob
+    assert np.array_equal(oracle.decompress(lb.tobytes()), w)
+
+
+def test_blob_identical_to_oracle_gate_proj_shape(lib, oracle):
+    w = wl.normal_weights(1024, 4096, 0.02, seed=11)
+    assert lib.compress(w).tobytes() == oracle.compress(w)[0]
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_code_lengths_equal_oracle_on_skewed_histograms(lib, oracle, seed):
+    # Random exponent histograms (through real matrices) exercise the code
+    # length choice and its tie rule against the oracle's exhaustive search.
+    rng = np.random.default_rng(seed)
+    m = int(rng.integers(2, 17))
+    probs = rng.dirichlet(np.full(m, 0.3 if seed % 2 else 3.0))
+    exps = 100 + rng.choice(m, size=(64, 256), p=probs)
+    w = ((exps.astype(np.uint16) << 7) | rng.integers(0, 256, (64, 256)).astype(np.uint16) & 0x807F)
+    d = lib.blob_info(lib.compress(w))
+    _, oinfo = oracle.compress(w)
+    assert list(d.code_len) == oinfo["code_len"]
+
+
+def test_compress_rejects_bad_shapes(lib):
+    L = lib.load()
+    n = ctypes.c_size_t(0)
+    w = np.zeros((4, 64), np.uint16)
+    assert L.uw_compress(w.ctypes.data, 4, 63, None, ctypes.byref(n)) == 2
+    assert L.uw_compress(w.ctypes.data, 0, 64, None, ctypes.byref(n)) == 2
+    assert L.uw_compress(w.ctypes.data, 4, 0, None, ctypes.byref(n)) == 2
+    assert L.uw_compress(None, 4, 64, None, ctypes.byref(n)) == 1
+    assert L.uw_compress(w.ctypes.data, 4, 64, None, ctypes.byref(n)) == 3 and n.value > 0
+
+
+def _corrupt(blob, pos, value):
+    b = bytearray(blob.tobytes())
+    b[pos] = value
+    return bytes(b)
+
+
+def test_blob_info_rejects_corruption(lib):
+    w = wl.normal_weights(64, 256, 0.02, seed=1)
+    blob = lib.compress(w)
+    d = lib.blob_info(blob)
+    assert lib.blob_info_status(blob) == 0
+    assert lib.blob_info_status(_corrupt(blob, 0, 0)) == 4                 # magic
+    assert lib.blob_info_status(_corrupt(blob, 4, 9)) == 4                 # version
+    assert lib.blob_info_status(_corrupt(blob, 24, 32)) == 4               # group size
+    assert lib.blob_info_status(_corrupt(blob, 56, 9)) == 4                # code length > 6
+    assert lib.blob_info_status(blob[: len(blob) - 256]) == 4              # truncated
+    assert lib.blob_info_status(_corrupt(blob, d.off_glen, 0)) == 4        # glen vs tile table
+    assert lib.blob_info_status(_corrupt(blob, d.off_glen + 3, 49)) == 4   # glen > 48
+    assert lib.blob_info_status(_corrupt(blob, d.off_tcode + 4, 200)) == 4 # tile offsets
+    assert lib.blob_info_status(blob.tobytes()[:200]) == 4                  # shorter than header
+
+
+def test_compression_ratio_and_statistics(lib):
+    # ~30% fewer bytes for N(0, 0.02) weights (blog: ~30% on MLP weights).
+    w = wl.normal_weights(1024, 4096, 0.02, seed=0)
+    blob = lib.compress(w)
+    d = lib.blob_info(blob)
+    ratio = d.blob_bytes / (2 * w.size)
+    assert 0.66 < ratio < 0.70, ratio
+    mean_len = d.code_bits / (64 * (d.n_groups - d.n_escaped))
+    assert 2.6 < mean_len < 2.8
+    assert d.n_escaped / d.n_groups < 0.01
