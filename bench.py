@@ -50,7 +50,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--no-context", action="store_true", help="skip the context measurements")
+    ap.add_argument("--no-context", action="store_true", help="skip the context and end-to-end measurements")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     return ap.parse_args()
 
 
@@ -322,7 +323,8 @@ def run_ours(args):
         line["context"] = context_measurements(torch, uw, w, x, desc, blobs, xd, stream, plan)
         line["e2e"] = e2e_measurement(torch, uw, desc, blobs, x, stream, plan, args)
     if rank == 0:
-        line["cpu_baseline"] = cpu_baseline()
+        if not args.no_cpu:
+            line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
