@@ -166,6 +166,27 @@ uw_status uw_autotune(const uw_desc *d, const void *blob_dev, const int64_t *bat
 uw_status uw_autotune_workspace_size(const uw_desc *d, const int64_t *batches, int32_t n,
                                      size_t *bytes);
 
+/* uw_matmul_noalloc -- uw_matmul with the default plan for callers that
+ * cannot allocate device memory: code that must not call cudaMalloc (it can
+ * synchronise the device or is not allowed in its context), plug-ins whose
+ * host framework owns all device memory, or callers that simply have no
+ * workspace buffer to hand over.  The Unweight blog has no counterpart;
+ * this is a convenience of this library.
+ * Scratch comes from a fixed array of 1 MiB inside the library, which every
+ * GPU that loads the library keeps until the process exits.  The call
+ * allocates nothing; the caller still passes x_dev [batch, cols] and
+ * y_dev [batch, rows] and gets the same result as uw_matmul with plan NULL.
+ * Returns UW_ERR_UNSUPPORTED when the call would need more than 1 MiB of
+ * scratch (uw_workspace_size(d, batch, NULL) > 1 MiB; then use uw_matmul).
+ * The first call on each device looks up the array's device address, so
+ * make that first call before any stream capture.  All calls share the one
+ * array: calls that may overlap on the GPU (other streams, other threads)
+ * race and must not be issued.  Decode errors found on the GPU are not
+ * reported here; use uw_matmul with a workspace and uw_check_status for
+ * that. */
+uw_status uw_matmul_noalloc(const uw_desc *d, const void *blob_dev, const uint16_t *x_dev,
+                            int64_t batch, uint16_t *y_dev, void *stream);
+
 /* uw_swiglu -- h = bf16(silu(g) * u), silu(z) = z / (1 + e^-z) in fp32,
  * the glue between the gate/up and down projections of a SwiGLU MLP.
  * g_dev, u_dev, h_dev: n BF16 values each, device memory. */

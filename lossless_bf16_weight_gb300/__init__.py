@@ -66,6 +66,7 @@ SIGNATURES = [
                                    _P, _SZ, _P]),
     ("uw_autotune_workspace_size", ctypes.c_int, [ctypes.POINTER(Desc), ctypes.POINTER(_I64), _I32,
                                                   ctypes.POINTER(_SZ)]),
+    ("uw_matmul_noalloc", ctypes.c_int, [ctypes.POINTER(Desc), _P, _P, _I64, _P, _P]),
     ("uw_swiglu", ctypes.c_int, [_P, _P, _P, _I64, _P]),
     ("uw_check_status", ctypes.c_int, [_P, _P]),
     ("uw_variant_name", ctypes.c_char_p, [_I32, _I32]),
@@ -200,6 +201,13 @@ def matmul_status(desc: Desc, blob_dev, x, y, ws, plan: Plan | None = None, stre
     batch = x.shape[0] if x.dim() == 2 else 1
     return int(load().uw_matmul(ctypes.byref(desc), _ptr(blob_dev), _ptr(x), batch, _ptr(y), _plan_ptr(plan),
                                 _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def matmul_noalloc(desc: Desc, blob_dev, x, y, stream=None) -> int:
+    """uw_matmul_noalloc: fused matmul with library-held scratch; returns the status."""
+    batch = x.shape[0] if x.dim() == 2 else 1
+    return int(load().uw_matmul_noalloc(ctypes.byref(desc), _ptr(blob_dev), _ptr(x), batch, _ptr(y),
+                                        _stream(stream)))
 
 
 def matmul_bf16(w, x, y, ws, variant: int = -1, stream=None):
