@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-context", action="store_true", help="skip the context and end-to-end measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--plan", default=None,
+                    help="fixed plan instead of autotuning: fused:<variant> or decompress:<variant>")
     return ap.parse_args()
 
 
@@ -222,6 +224,15 @@ def time_graph(torch, fn, steps: int, warmup: int, group: int, stream):
     return g, n_graph, rem, e0, e1
 
 
+def fixed_plan(uw, text):
+    kind, name = text.split(":")
+    strategy = uw.STRATEGY_FUSED if kind == "fused" else uw.STRATEGY_DECOMPRESS_GEMM
+    for v in range(uw.variant_count(strategy)):
+        if uw.variant_name(strategy, v) == name:
+            return uw.Plan(strategy, v, BATCH, 0.0)
+    raise SystemExit("unknown variant %s" % name)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -257,9 +268,12 @@ def run_ours(args):
 
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
-    tune_ws = torch.empty(uw.autotune_workspace_size(desc, [BATCH]), dtype=torch.uint8, device="cuda")
-    plan = uw.autotune(desc, blobs[0], [BATCH], tune_ws, stream)[0]
-    del tune_ws
+    if args.plan:
+        plan = fixed_plan(uw, args.plan)
+    else:
+        tune_ws = torch.empty(uw.autotune_workspace_size(desc, [BATCH]), dtype=torch.uint8, device="cuda")
+        plan = uw.autotune(desc, blobs[0], [BATCH], tune_ws, stream)[0]
+        del tune_ws
     ws = torch.empty(uw.workspace_size(desc, BATCH, plan), dtype=torch.uint8, device="cuda")
     uw.workspace_init(ws, stream)
     launches_per_step = 1 if plan.strategy == uw.STRATEGY_FUSED else 2

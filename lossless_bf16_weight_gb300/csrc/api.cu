@@ -28,28 +28,63 @@ uint64_t rd64(const uint8_t *p) {
 
 cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
-// CUDA-core kernel variants: warps per CTA x split count.
+// CUDA-core kernel variants.
+//   0..14  row-block CTAs (gemv.cu): warps per CTA x split count
+//   15..26 column CTAs, batch 1 only (gemv_kg.cu): warps per CTA x grid
+//          size in full waves (1..4) of the GPU; the row blocks per CTA
+//          follow from the matrix and the SM count
 constexpr int kWarpChoices[3] = {4, 8, 16};
 constexpr int kSplitChoices = 5;  // 1, 2, 4, 8, 16
-constexpr int kGemvVariants = 3 * kSplitChoices;
+constexpr int kRowVariants = 3 * kSplitChoices;
+constexpr int kColWaves = 4;
+constexpr int kColVariants = 3 * kColWaves;
+constexpr int kGemvVariants = kRowVariants + kColVariants;
 constexpr int kMaxBatchChunk = 8;
 
 struct GemvVariant {
-    int warps, splits;
+    bool column;
+    int warps, splits, rb;
 };
 
-GemvVariant gemv_variant(int v) { return {kWarpChoices[v % 3], 1 << (v / 3)}; }
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n <= 0)
+        return 152;
+    return n;
+}
+
+GemvVariant gemv_variant(int v, int64_t rows, int64_t cols) {
+    if (v < kRowVariants)
+        return {false, kWarpChoices[v % 3], 1 << (v / 3), 0};
+    const int i = v - kRowVariants;
+    const int w = kWarpChoices[i % 3];
+    const int waves = 1 + i / 3;
+    const int64_t gpr = cols / kGroup;
+    const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
+    const int64_t splits = (gpr + w - 1) / w;
+    const int64_t slots = int64_t(sm_count()) * col_blocks_per_sm(w) * waves;  // CTAs per wave x waves
+    int64_t rb = (nrb * splits + slots - 1) / slots;
+    rb = rb < 2 ? 2 : (rb + 1) / 2 * 2;  // tiles go in pairs
+    // keep the CTAs of one SM within its shared memory
+    while (rb > 2 && gemv_kg_smem_bytes(w, int(rb), true) * col_blocks_per_sm(w) > size_t(kSmemPerSm))
+        rb -= 2;
+    return {true, w, int(splits), int(rb)};
+}
 
 int pad_batch(int64_t b) {
     const int c = int(std::min<int64_t>(b, kMaxBatchChunk));
     return c <= 1 ? 1 : c <= 2 ? 2 : c <= 4 ? 4 : 8;
 }
 
-// Default variant: 8 warps; enough CTAs to fill the GPU twice when the
-// matrix has few row blocks; at least one tile per warp.
+// Default variant.  Batch 1: column CTAs of 8 warps with the most row blocks
+// per CTA that still gives about two CTAs per SM.  Otherwise row-block CTAs
+// of 8 warps, split along K when the matrix has few row blocks.
 int default_gemv_variant(int64_t rows, int64_t cols, int64_t batch) {
     const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
     const int64_t gpr = cols / kGroup;
+    if (batch == 1)
+        return kRowVariants + 4;  // 8 warps, two waves
     const int bp = pad_batch(batch);
     int si = 0;
     while (si + 1 < kSplitChoices && nrb * (int64_t(1) << si) < 2 * 152 &&
@@ -63,8 +98,8 @@ int default_gemv_variant(int64_t rows, int64_t cols, int64_t batch) {
 WsLayout layout_for(int64_t rows, int64_t cols, int64_t batch, int strategy, int variant) {
     WsLayout L;
     const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
-    const GemvVariant gv = gemv_variant(variant);
-    const int bp = pad_batch(batch);
+    const GemvVariant gv = gemv_variant(variant, rows, cols);
+    const int bp = gv.column ? 1 : pad_batch(batch);
     L.status = 0;
     L.counters = 256;
     L.partial = align_up(L.counters + 4 * uint64_t(nrb), 256);
@@ -97,9 +132,16 @@ uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t 
     return UW_OK;
 }
 
-// Batch rows go through the CUDA-core kernel in chunks of at most 8.
+// Batch rows go through the CUDA-core kernels in chunks of at most 8; the
+// column kernels take batch 1 only.
 uw_status run_gemv(GemvParams p, int variant, bool compressed, cudaStream_t stream) {
-    const GemvVariant gv = gemv_variant(variant);
+    const GemvVariant gv = gemv_variant(variant, p.rows, p.cols);
+    if (gv.column) {
+        if (p.batch != 1)
+            return UW_ERR_UNSUPPORTED;
+        p.splits = gv.splits;
+        return launch_gemv_kg(p, gv.warps, gv.rb, compressed, stream);
+    }
     p.splits = gv.splits;
     const int64_t total = p.batch;
     for (int64_t b0 = 0; b0 < total; b0 += kMaxBatchChunk) {
@@ -407,8 +449,10 @@ extern "C" int32_t uw_variant_count(int32_t strategy) {
 
 extern "C" const char *uw_variant_name(int32_t strategy, int32_t variant) {
     static const char *names[kGemvVariants] = {
-        "w4s1", "w8s1", "w16s1", "w4s2", "w8s2", "w16s2", "w4s4", "w8s4",
-        "w16s4", "w4s8", "w8s8", "w16s8", "w4s16", "w8s16", "w16s16"};
+        "w4s1", "w8s1", "w16s1", "w4s2", "w8s2", "w16s2", "w4s4", "w8s4", "w16s4",
+        "w4s8", "w8s8", "w16s8", "w4s16", "w8s16", "w16s16",
+        "col_w4x1", "col_w8x1", "col_w16x1", "col_w4x2", "col_w8x2", "col_w16x2",
+        "col_w4x3", "col_w8x3", "col_w16x3", "col_w4x4", "col_w8x4", "col_w16x4"};
     if (uw_variant_count(strategy) == 0 || variant < 0 || variant >= kGemvVariants)
         return nullptr;
     return names[variant];

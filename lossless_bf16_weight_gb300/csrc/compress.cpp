@@ -10,7 +10,9 @@
 //      dynamic program over the levels of the code tree;
 //   6. canonical codes in (length, palette index) order;
 //   7. blob: raw sign+mantissa bytes, group byte lengths, tile offsets,
-//      byte-aligned MSB-first group codes, raw exponents of escaped groups.
+//      byte-aligned group codes (stream bits fill each byte from bit 0 up,
+//      each code enters most significant bit first), raw exponents of
+//      escaped groups.
 // Every pass is parallel over rows or tiles with OpenMP; the result does not
 // depend on the thread count.
 #include <omp.h>
@@ -145,22 +147,29 @@ void canonical_codes(const uint8_t len[kPalette], uint16_t code[kPalette]) {
         code[s] = len[s] ? static_cast<uint16_t>(next[len[s]]++) : 0;
 }
 
-// MSB-first bit packer for one group; returns the number of bits.
+// Bit packer for one group: stream bit i goes to bit i%8 of byte i/8, and
+// each code enters the stream most significant bit first, so the code is
+// appended bit-reversed to a little-endian accumulator.  Returns the bits.
 int pack_group(const uint16_t *w, const Codebook &cb, uint8_t *out /* >= 48 bytes */) {
     uint64_t acc = 0;
     int pending = 0, bits = 0, pos = 0;
     for (int i = 0; i < kGroup; i++) {
         const int s = cb.sym_of[exponent_of(w[i])];
-        acc = (acc << cb.len[s]) | cb.code[s];
-        pending += cb.len[s];
-        bits += cb.len[s];
+        const int l = cb.len[s];
+        uint32_t rev = 0;
+        for (int b = 0; b < l; b++)
+            rev |= ((cb.code[s] >> b) & 1u) << (l - 1 - b);
+        acc |= uint64_t(rev) << pending;
+        pending += l;
+        bits += l;
         while (pending >= 8) {
-            out[pos++] = static_cast<uint8_t>(acc >> (pending - 8));
+            out[pos++] = static_cast<uint8_t>(acc & 0xFFu);
+            acc >>= 8;
             pending -= 8;
         }
     }
     if (pending)
-        out[pos++] = static_cast<uint8_t>(acc << (8 - pending));
+        out[pos++] = static_cast<uint8_t>(acc & 0xFFu);
     return bits;
 }
 

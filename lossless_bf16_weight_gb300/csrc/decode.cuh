@@ -2,25 +2,29 @@
 //
 // One warp decodes one tile (32 rows x 64 columns): lane j owns the 64-weight
 // group of row j (Unweight blog, paragraph on rows of 64).  Per tile:
+//   * the tile's code bytes are copied with cp.async straight into one of
+//     the warp's two shared-memory code buffers while the previous tile is
+//     being decoded, and its sign+mantissa bytes are loaded into registers;
 //   * the group byte lengths (glen) give each lane its code offset by an
-//     exclusive warp prefix sum (shuffles), and each escaped lane its rank
-//     among the escaped groups by ballot + popc;
-//   * the tile's code bytes are staged in the warp's shared-memory buffer
-//     (byte-swapped into big-endian words so that bit 31 of a word is the
-//     first code bit);
-//   * every step looks up a 12-bit window in a 4096-entry table that decodes
-//     two codes at once (codes are at most 6 bits).  An entry holds both
-//     exponents already in BF16 position (bits 14..7 and 30..23) and the
-//     number of bits the two codes take (bits 3..0);
+//     exclusive warp prefix sum (shuffles); ballot + popc give each escaped
+//     group its rank among the tile's escaped groups;
+//   * read as little-endian 32-bit words, stream bit i is bit i%32 of word
+//     i/32, so a funnel shift right brings the next bits to the bottom;
+//   * every step looks up a 12-bit window (first stream bit = bit 0) in a
+//     4096-entry table that decodes two codes at once (codes are at most 6
+//     bits).  An entry holds both exponents already in BF16 position (bits
+//     14..7 and 30..23) and the bits the two codes take (bits 3..0);
 //   * the exponent pair is merged with two raw sign+mantissa bytes by one
 //     byte permute (sign-replicating) and one three-input logic op, giving
 //     two BF16 weights in one 32-bit register (the blog's reconstruction:
 //     exponent + sign/mantissa bytes -> BF16, paragraph on the consumer
 //     warps of the reconstructive matmul).
-// Escaped groups and lanes without a row use the same loop: they read a
-// fixed stream of 12-bit numbers 0..31 through a private 32-entry table that
-// holds their raw exponents (or zeros), so the hot loop has no branch on
-// the group kind.
+// Escaped groups (rare) and lanes without a row run the same loop on a
+// fixed stream of 12-bit numbers 0..31 through a 32-entry table of zero
+// exponents, so the hot loop has no branch on the group kind; the escaped
+// groups are then redone in a short second pass from their raw exponent
+// bytes.  Every lane's sum is independent of the other lanes', so the
+// second pass gives exactly what a single pass would.
 #pragma once
 #include <cuda_runtime.h>
 
@@ -55,8 +59,9 @@ struct BlobView {
 };
 
 constexpr int kLutEntries = 4096;
-constexpr int kFakeWords = 16;                      // stream of 12-bit values 0..31 (+slack)
-constexpr int kWarpBufBytes = 4096 + 64;            // codes + escape tables + read slack
+constexpr int kFakeWords = 16;                             // stream of 12-bit values 0..31 (+slack)
+constexpr int kCodeBufBytes = kMaxTileCodeBytes + 64;      // one tile's codes + read slack
+constexpr int kWarpBufBytes = 2 * kCodeBufBytes;           // two buffers: decode one, fill the other
 constexpr int kCommonSmemBytes = kLutEntries * 4 + kFakeWords * 4 + 32 * 4 + 64 * 2;
 
 // Shared memory common to every decoding CTA.
@@ -89,19 +94,22 @@ __device__ __forceinline__ void build_tables(const DecodeShared &s, const BlobVi
         for (int b = 0; b < 32; b++) {
             const int p = wi * 32 + b;              // bit position in the stream
             const int val = p / 12;                 // 12-bit field holding it
-            const uint32_t bit = val < 32 ? (uint32_t(val) >> (11 - p % 12)) & 1u : 0u;
-            word |= bit << (31 - b);
+            const uint32_t bit = val < 32 ? (uint32_t(val) >> (p % 12)) & 1u : 0u;
+            word |= bit << b;
         }
         s.fake[wi] = word;
     }
     __syncthreads();
+    // Window w holds stream bits in order from bit 0; codes enter the stream
+    // most significant bit first, so the code-order window is w reversed.
     for (int w = tid; w < kLutEntries; w += nt) {
-        const uint32_t a = s.prefix6[w >> 6];
+        const uint32_t r = __brev(uint32_t(w)) >> 20;
+        const uint32_t a = s.prefix6[r >> 6];
         const uint32_t la = a & 15u;
         uint32_t entry = 0;
         if (la) {
-            const uint32_t w2 = (uint32_t(w) << la) & 0xFFFu;
-            const uint32_t b = s.prefix6[w2 >> 6];
+            const uint32_t r2 = (r << la) & 0xFFFu;
+            const uint32_t b = s.prefix6[r2 >> 6];
             const uint32_t lb = b & 15u;
             if (lb)
                 entry = ((b >> 4) << 23) | ((a >> 4) << 7) | (la + lb);
@@ -125,45 +133,50 @@ __device__ __forceinline__ uint32_t lop3_merge(uint32_t sm_part, uint32_t exp_pa
     return r;
 }
 
-// Per-tile, per-lane decode state set up by tile_setup().
-struct LaneStream {
-    const uint32_t *wp;    // next word to load
-    const uint32_t *lutp;  // pair table of this lane (shared table, escape table or zeros)
-    uint32_t hi, lo, c;    // 64-bit window and bit position (low 7 bits exact)
-    uint32_t c0;           // starting bit offset (for the consumed-bits check)
-    const uint32_t *wp0;
-    int coded;             // lane holds Huffman codes (checked at the end)
-    uint32_t glen;
+// Where a tile's data lives: rows 32*rb .. 32*rb+R-1, group column kg.
+struct TileLoc {
+    int64_t q0;  // index of the tile's first group (group order of the blob)
+    int R;       // rows in the tile
 };
 
-// Registers holding one tile's raw inputs, loaded ahead of use.
-struct TileRaw {
-    uint4 sm[4];     // lane's 64 sign+mantissa bytes
-    uint4 code[3];   // up to 96 16-byte chunks of the tile's code region
-    uint32_t glen;   // lane's group byte length
-    uint32_t beg16, n16;  // code region (16-byte units)
-    uint32_t esc0, nesc;  // escape index of the tile and escaped groups in it
-    int bad;              // offsets failed validation
-};
-
-// Tile coordinates.
-struct TileCoord {
-    int64_t rb, kg;  // row block and group column
-    int R;           // rows in this block
-};
-
-__device__ __forceinline__ TileCoord tile_coord(const BlobView &v, int64_t t) {
-    const int64_t gpr = v.cols / kGroup;
-    TileCoord tc;
-    tc.rb = t / gpr;
-    tc.kg = t - tc.rb * gpr;
-    const int64_t left = v.rows - tc.rb * kTileRows;
-    tc.R = left < kTileRows ? int(left) : kTileRows;
-    return tc;
+__device__ __forceinline__ TileLoc tile_loc(const BlobView &v, int64_t rb, int64_t kg, int64_t gpr) {
+    TileLoc L;
+    const int64_t left = v.rows - rb * kTileRows;
+    L.R = left < kTileRows ? int(left) : kTileRows;
+    L.q0 = int64_t(kTileRows) * rb * gpr + int64_t(L.R) * kg;
+    return L;
 }
 
-// Load the offsets of tile t into lanes 0..3 (tcode[t], tcode[t+1],
-// tesc[t], tesc[t+1]); issued one tile earlier than the data they locate.
+// A tile's lane-held bookkeeping: the lane's glen, and the tile's offsets
+// (lanes 0..3 hold tcode[t], tcode[t+1], tesc[t], tesc[t+1]).
+struct TileMeta {
+    uint32_t glen;
+    uint32_t offs;
+};
+
+struct TileOffsets {
+    uint32_t c0, n16;     // code region start and size, 16-byte units
+    uint32_t esc0, nesc;  // first escaped group of the tile, escaped groups in it
+    bool bad;             // offsets out of range
+};
+
+__device__ __forceinline__ TileOffsets unpack_offsets(const BlobView &v, uint32_t offs, int R) {
+    const uint32_t c0 = __shfl_sync(0xffffffffu, offs, 0);
+    const uint32_t c1 = __shfl_sync(0xffffffffu, offs, 1);
+    const uint32_t e0 = __shfl_sync(0xffffffffu, offs, 2);
+    const uint32_t e1 = __shfl_sync(0xffffffffu, offs, 3);
+    TileOffsets o;
+    o.c0 = c0;
+    o.n16 = c1 - c0;
+    o.esc0 = e0;
+    o.nesc = e1 - e0;
+    o.bad = (c1 < c0) || (o.n16 * 16u > uint32_t(kMaxTileCodeBytes)) || (uint64_t(c1) * 16u > v.code_bytes) ||
+            (e1 < e0) || (o.nesc > uint32_t(R)) || (uint64_t(e1) > v.n_escaped);
+    return o;
+}
+
+// Load the offsets of tile t = rb * (cols/64) + kg into lanes 0..3
+// (tcode[t], tcode[t+1], tesc[t], tesc[t+1]); issued ahead of the data.
 __device__ __forceinline__ uint32_t tile_offsets_load(const BlobView &v, int64_t t) {
     const int lane = threadIdx.x & 31;
     uint32_t off = 0;
@@ -174,139 +187,189 @@ __device__ __forceinline__ uint32_t tile_offsets_load(const BlobView &v, int64_t
     return off;
 }
 
-// Issue the global loads of tile t (no shared-memory traffic).  `offs` comes
-// from tile_offsets_load(v, t).
-__device__ __forceinline__ void tile_load(const BlobView &v, int64_t t, uint32_t offs, TileRaw &r) {
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Validate the tile's offsets, load the lane's glen and start copying the
+// code region into the code buffer at shared address `cbuf` (cp.async, one
+// commit group).  `offs` comes from tile_offsets_load.
+__device__ __forceinline__ void tile_fetch_codes(const BlobView &v, const TileLoc &L, uint32_t offs, uint32_t cbuf,
+                                                 TileMeta &m) {
     const int lane = threadIdx.x & 31;
-    const TileCoord tc = tile_coord(v, t);
-    const int64_t gpr = v.cols / kGroup;
-    const uint32_t c0 = __shfl_sync(0xffffffffu, offs, 0);
-    const uint32_t c1 = __shfl_sync(0xffffffffu, offs, 1);
-    const uint32_t e0 = __shfl_sync(0xffffffffu, offs, 2);
-    const uint32_t e1 = __shfl_sync(0xffffffffu, offs, 3);
-    r.beg16 = c0;
-    r.n16 = c1 - c0;
-    r.esc0 = e0;
-    r.nesc = e1 - e0;
-    r.bad = (c1 < c0) || (r.n16 * 16u > uint32_t(kMaxTileCodeBytes)) ||
-            (uint64_t(c1) * 16u > v.code_bytes) || (e1 < e0) || (r.nesc > uint32_t(tc.R)) ||
-            (uint64_t(e1) > v.n_escaped);
-    const int64_t q0 = int64_t(kTileRows) * tc.rb * gpr + int64_t(tc.R) * tc.kg;
-    const bool valid = lane < tc.R;
-    r.glen = valid ? __ldg(v.glen + q0 + lane) : 0u;
-    const uint8_t *smt = v.sm + q0 * kGroup;
+    const TileOffsets o = unpack_offsets(v, offs, L.R);
+    m.offs = offs;
+    m.glen = lane < L.R ? __ldg(v.glen + L.q0 + lane) : 0u;
+    if (!o.bad) {
+        const uint8_t *src = v.code + size_t(o.c0) * 16;
+#pragma unroll
+        for (int c = 0; c < 3; c++) {
+            const uint32_t idx = uint32_t(lane + 32 * c);
+            if (idx < o.n16)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                             :: "r"(cbuf + 16u * idx), "l"(src + 16 * size_t(idx)) : "memory");
+        }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// The lane's 64 sign+mantissa bytes (16-byte chunk c of row j sits at
+// (c*R + j)*16 inside the tile).
+__device__ __forceinline__ void tile_load_sm(const BlobView &v, const TileLoc &L, uint4 (&sm)[4]) {
+    const int lane = threadIdx.x & 31;
+    const uint8_t *smt = v.sm + L.q0 * kGroup;
 #pragma unroll
     for (int c = 0; c < 4; c++)
-        r.sm[c] = valid ? __ldg(reinterpret_cast<const uint4 *>(smt + (size_t(c) * tc.R + lane) * 16))
-                        : make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int c = 0; c < 3; c++) {
-        const uint32_t idx = uint32_t(lane + 32 * c);
-        r.code[c] = (!r.bad && idx < r.n16)
-                        ? __ldg(reinterpret_cast<const uint4 *>(v.code + (size_t(r.beg16) + idx) * 16))
-                        : make_uint4(0, 0, 0, 0);
+        sm[c] = lane < L.R ? __ldg(reinterpret_cast<const uint4 *>(smt + (size_t(c) * L.R + lane) * 16))
+                           : make_uint4(0, 0, 0, 0);
+}
+
+// One 16-byte chunk (weights 16c .. 16c+15 of the lane's group).
+__device__ __forceinline__ uint4 tile_load_sm_chunk(const BlobView &v, const TileLoc &L, int c) {
+    const int lane = threadIdx.x & 31;
+    const uint8_t *smt = v.sm + L.q0 * kGroup;
+    return lane < L.R ? __ldg(reinterpret_cast<const uint4 *>(smt + (size_t(c) * L.R + lane) * 16))
+                      : make_uint4(0, 0, 0, 0);
+}
+
+// Ask for the tile's sign+mantissa bytes (64*R contiguous bytes, one
+// 128-byte line per lane) ahead of the loads that use them; costs no
+// registers.  kL1 brings them into this SM's L1, otherwise into L2.
+template <bool kL1 = false>
+__device__ __forceinline__ void tile_prefetch_sm(const BlobView &v, const TileLoc &L) {
+    const int lane = threadIdx.x & 31;
+    if (kL1) {
+        if (lane * 2 < L.R)
+            asm volatile("prefetch.global.L1 [%0];" :: "l"(v.sm + L.q0 * kGroup + 128 * lane));
+    } else if (lane == 0 && L.R > 0) {
+        // one bulk request on the TMA engine for the whole 64*R-byte region
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                     :: "l"(v.sm + L.q0 * kGroup), "r"(uint32_t(kGroup * L.R)) : "memory");
     }
 }
 
-__device__ __forceinline__ uint32_t bswap32(uint32_t x) { return prmt(x, 0u, 0x0123u); }
+// Per-tile, per-lane decode state.  Addresses are 32-bit shared addresses.
+struct LaneStream {
+    uint32_t lo, hi, nx;   // current, next and (already loaded) following stream word
+    uint32_t c;            // bit position in lo (low 5 bits); low 7 bits exact
+    uint32_t wp;           // address of the next word to load
+    uint32_t lut;          // pair table of this lane (codes) or the zero table
+    uint32_t base;         // 8 * (first wp) + start bit: bits used = 8 * wp + (c & 31) - base
+    uint32_t glen;         // bytes the lane must use (48 for lanes on the fixed stream)
+};
 
-// Stage the tile's codes and escape tables in the warp buffer and set up
-// the lane's stream.  Returns whether the tile passed validation.
-__device__ __forceinline__ bool tile_setup(const BlobView &v, const DecodeShared &s, const TileRaw &r,
-                                           int R, uint32_t *wbuf, LaneStream &ls, uint32_t *status) {
+// Wait for the tile's codes, validate, and set up every lane's stream.
+// Returns the mask of lanes whose group is escaped (0 for a bad tile, whose
+// lanes all decode zeros; the error is recorded in *status) and, in *esc0,
+// the index of the tile's first escaped group.
+__device__ __forceinline__ uint32_t tile_begin(const BlobView &v, const DecodeShared &s, const TileMeta &m, int R,
+                                               uint32_t cbuf, LaneStream &ls, uint32_t *status, uint32_t *esc0) {
     const int lane = threadIdx.x & 31;
     const bool valid = lane < R;
-    // byte-swapped code words into the warp buffer
-#pragma unroll
-    for (int c = 0; c < 3; c++) {
-        const uint32_t idx = uint32_t(lane + 32 * c);
-        if (idx < r.n16 && !r.bad) {
-            uint4 q = r.code[c];
-            q.x = bswap32(q.x);
-            q.y = bswap32(q.y);
-            q.z = bswap32(q.z);
-            q.w = bswap32(q.w);
-            reinterpret_cast<uint4 *>(wbuf)[idx] = q;
-        }
-    }
-    // code offsets by an exclusive warp prefix sum of the byte lengths
-    const uint32_t g = r.glen;
+    const TileOffsets o = unpack_offsets(v, m.offs, R);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
+    const uint32_t g = m.glen;
     uint32_t incl = g;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+        const uint32_t u = __shfl_up_sync(0xffffffffu, incl, d);
         if (lane >= d)
-            incl += o;
+            incl += u;
     }
     const uint32_t off = incl - g;
     const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
     const uint32_t esc_mask = __ballot_sync(0xffffffffu, valid && g == 0);
-    const uint32_t nesc = __popc(esc_mask);
-    const uint32_t region = r.n16 * 16u;
-    bool bad = r.bad || total > region || nesc != r.nesc || region + 128u * nesc > 4096u;
+    const bool over = o.bad || total > o.n16 * 16u;
+    const bool bad = over || uint32_t(__popc(esc_mask)) != o.nesc;
     if (bad && lane == 0)
-        atomicOr(status, r.bad || total > region ? kStatusBadTile : kStatusBadEscape);
-    // escape tables: 32 entries per escaped lane after the code region
-    uint32_t *esc_tab = wbuf + region / 4;
-    if (!bad) {
-        uint32_t m = esc_mask;
-        int rank = 0;
-        while (m) {
-            const uint16_t two = __ldg(reinterpret_cast<const uint16_t *>(v.esc + (uint64_t(r.esc0) + rank) * 64) + lane);
-            const uint32_t e0 = two & 0xFFu, e1 = two >> 8;
-            esc_tab[rank * 32 + lane] = (e1 << 23) | (e0 << 7) | 12u;
-            m &= m - 1;
-            rank++;
-        }
-    }
-    __syncwarp();
-    const uint32_t my_rank = __popc(esc_mask & ((1u << lane) - 1u));
-    ls.coded = !bad && valid && g != 0;
-    ls.glen = g;
-    if (ls.coded) {
-        const uint32_t *w0 = wbuf + (off >> 2);
-        ls.c0 = 8u * (off & 3u);
-        ls.hi = w0[0];
-        ls.lo = w0[1];
-        ls.wp = w0 + 2;
-        ls.lutp = s.lut;
+        atomicOr(status, over ? kStatusBadTile : kStatusBadEscape);
+    *esc0 = o.esc0;
+    uint32_t w0, c0;
+    if (!bad && valid && g != 0) {
+        w0 = cbuf + (off & ~3u);
+        c0 = 8u * (off & 3u);
+        ls.lut = smem_addr(s.lut);
+        ls.glen = g;
     } else {
-        ls.c0 = 0;
-        ls.hi = s.fake[0];
-        ls.lo = s.fake[1];
-        ls.wp = s.fake + 2;
-        ls.lutp = (!bad && valid && g == 0) ? esc_tab + my_rank * 32 : s.zeros;
+        w0 = smem_addr(s.fake);
+        c0 = 0;
+        ls.lut = smem_addr(s.zeros);
+        ls.glen = 48;  // the fixed stream is 32 fields of 12 bits
     }
-    ls.wp0 = ls.wp;
-    ls.c = ls.c0;
-    return !bad;
+    ls.lo = lds32(w0);
+    ls.hi = lds32(w0 + 4);
+    ls.nx = lds32(w0 + 8);
+    ls.wp = w0 + 12;
+    ls.c = c0;
+    ls.base = 8u * ls.wp + c0;
+    return bad ? 0u : esc_mask;
+}
+
+// Raw exponent bytes of the calling lane's escaped group (lane must be in
+// the mask returned by tile_begin).
+__device__ __forceinline__ void escape_load(const BlobView &v, uint32_t esc0, uint32_t esc_mask, uint4 (&e)[4]) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = __popc(esc_mask & ((1u << lane) - 1u));
+    const uint4 *src = reinterpret_cast<const uint4 *>(v.esc + (uint64_t(esc0) + rank) * 64);
+#pragma unroll
+    for (int c = 0; c < 4; c++)
+        e[c] = __ldg(src + c);
 }
 
 // One step: decode the exponents of weights 2i, 2i+1 and merge them with the
 // sign+mantissa bytes.  `sm4` holds the bytes of weights 4*(i/2)..+3.
 // `I` is a compile-time constant once the caller's 32-step loop is unrolled.
 __device__ __forceinline__ uint32_t decode_pair(LaneStream &ls, int I, uint32_t sm4) {
-    const uint32_t win = __funnelshift_l(ls.lo, ls.hi, ls.c);
-    const uint32_t ent = ls.lutp[win >> 20];
-    const uint32_t c2 = ls.c + ent;  // bits above 6 collect junk; the low 7 stay exact
-    if ((c2 ^ ls.c) & 32u) {
-        ls.hi = ls.lo;
-        ls.lo = *ls.wp++;
-    }
-    ls.c = c2;
+    // window = next 32 stream bits (funnel right); entry = table[window & 4095];
+    // c += entry (its bits above 6 only add junk above the exact low 7);
+    // when bit 5 of c flips the window has moved into the next word: shift
+    // the words and load the one after, predicated rather than branched.  The
+    // loaded word is needed only at the following crossing, so the load is
+    // off the step-to-step dependency chain.
+    uint32_t ent;
+    asm volatile(
+        "{\n\t"
+        ".reg .b32 win, addr, c2, t;\n\t"
+        ".reg .pred p;\n\t"
+        "shf.r.wrap.b32 win, %1, %2, %4;\n\t"
+        "and.b32 win, win, 4095;\n\t"
+        "mad.lo.u32 addr, win, 4, %6;\n\t"     // integer multiply-add: FMA pipe, not ALU
+        "ld.shared.u32 %0, [addr];\n\t"
+        "mad.lo.u32 c2, %0, 1, %4;\n\t"
+        "xor.b32 t, c2, %4;\n\t"
+        "and.b32 t, t, 32;\n\t"
+        "setp.ne.u32 p, t, 0;\n\t"
+        "@p mov.b32 %1, %2;\n\t"
+        "@p mov.b32 %2, %3;\n\t"
+        "@p ld.shared.u32 %3, [%5];\n\t"
+        "@p mad.lo.u32 %5, 1, 4, %5;\n\t"
+        "mov.b32 %4, c2;\n\t"
+        "}"
+        : "=r"(ent), "+r"(ls.lo), "+r"(ls.hi), "+r"(ls.nx), "+r"(ls.c), "+r"(ls.wp)
+        : "r"(ls.lut)
+        : "memory");
     // sign-replicate byte permute: bytes (b0, sign(b0), b1, sign(b1)) for the
     // even pair of the word, (b2, sign(b2), b3, sign(b3)) for the odd one
     const uint32_t y = prmt(sm4, 0u, (I & 1) ? 0xB3A2u : 0x9180u);
     return lop3_merge(y, ent);
 }
 
-// After the 32 steps: a coded lane must have used exactly its byte length.
+// After the 32 steps: every lane must have used exactly its byte length.
 __device__ __forceinline__ void tile_check(const LaneStream &ls, uint32_t *status) {
-    if (ls.coded) {
-        const uint32_t used = 32u * uint32_t(ls.wp - ls.wp0) + (ls.c & 31u) - ls.c0;
-        if (((used + 7u) >> 3) != ls.glen)
-            atomicOr(status, uint32_t(kStatusBadCode));
-    }
+    const uint32_t used = 8u * ls.wp + (ls.c & 31u) - ls.base;
+    if (((used + 7u) >> 3) != ls.glen)
+        atomicOr(status, uint32_t(kStatusBadCode));
+}
+
+__device__ __forceinline__ uint32_t word4(const uint4 &q, int w) {
+    return (w & 3) == 0 ? q.x : (w & 3) == 1 ? q.y : (w & 3) == 2 ? q.z : q.w;
 }
 
 __device__ __forceinline__ uint32_t sm_word(const uint4 (&sm)[4], int w) {
@@ -317,6 +380,15 @@ __device__ __forceinline__ uint32_t sm_word(const uint4 (&sm)[4], int w) {
         case 2: return q.z;
         default: return q.w;
     }
+}
+
+// Pair I of an escaped group: its two raw exponents (bytes 2I, 2I+1 of `e`)
+// moved to BF16 position, merged with the sign+mantissa bytes as in
+// decode_pair.
+__device__ __forceinline__ uint32_t escape_pair(const uint4 (&e)[4], int I, uint32_t sm4) {
+    const uint32_t two = prmt(sm_word(e, I >> 1), 0u, (I & 1) ? 0x4342u : 0x4140u);  // e_lo | e_hi << 16
+    const uint32_t y = prmt(sm4, 0u, (I & 1) ? 0xB3A2u : 0x9180u);
+    return lop3_merge(y, two << 7);
 }
 
 }  // namespace uw

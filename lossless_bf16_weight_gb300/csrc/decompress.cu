@@ -31,10 +31,16 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
     const int64_t t_lo = (int64_t(blockIdx.x) * kDecompWarps + warp) * kTilesPerWarp;
     const int64_t t_hi = t_lo + kTilesPerWarp < ntiles ? t_lo + kTilesPerWarp : ntiles;
 
-    TileRaw raw;
+    // this warp's tiles t_lo .. t_hi-1, walked as (row block, group column)
+    int64_t rb = t_lo / gpr, kg = t_lo - (t_lo / gpr) * gpr;
+    TileMeta meta{};
+    uint4 smn[4];
     uint32_t offs_next = 0;
+    const uint32_t cbuf0 = smem_addr(wbuf);
     if (t_lo < t_hi) {
-        tile_load(v, t_lo, tile_offsets_load(v, t_lo), raw);
+        const TileLoc L = tile_loc(v, rb, kg, gpr);
+        tile_fetch_codes(v, L, tile_offsets_load(v, t_lo), cbuf0, meta);
+        tile_load_sm(v, L, smn);
         if (t_lo + 1 < t_hi)
             offs_next = tile_offsets_load(v, t_lo + 1);
     }
@@ -42,15 +48,24 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
     __syncthreads();
 
     for (int64_t t = t_lo; t < t_hi; t++) {
-        const TileCoord tc = tile_coord(v, t);
+        const TileLoc L = tile_loc(v, rb, kg, gpr);
+        const int64_t rb_cur = rb, kg_cur = kg;
+        if (++kg == gpr) {
+            kg = 0;
+            rb++;
+        }
+        const uint32_t cbuf = cbuf0 + uint32_t((t - t_lo) & 1) * kCodeBufBytes;
         uint4 sm[4];
 #pragma unroll
         for (int c = 0; c < 4; c++)
-            sm[c] = raw.sm[c];
+            sm[c] = smn[c];
+        uint32_t esc0;
         LaneStream ls;
-        tile_setup(v, ds, raw, tc.R, wbuf, ls, status);
+        const uint32_t esc_mask = tile_begin(v, ds, meta, L.R, cbuf, ls, status, &esc0);
         if (t + 1 < t_hi) {
-            tile_load(v, t + 1, offs_next, raw);
+            const TileLoc N = tile_loc(v, rb, kg, gpr);
+            tile_fetch_codes(v, N, offs_next, cbuf0 + uint32_t((t + 1 - t_lo) & 1) * kCodeBufBytes, meta);
+            tile_load_sm(v, N, smn);
             if (t + 2 < t_hi)
                 offs_next = tile_offsets_load(v, t + 2);
         }
@@ -64,15 +79,30 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
             }
         }
         tile_check(ls, status);
+        if (esc_mask) {  // escaped groups: redo those lanes from raw exponents
+            if ((esc_mask >> lane) & 1u) {
+                uint4 e[4];
+                escape_load(v, esc0, esc_mask, e);
+#pragma unroll
+                for (int I = 0; I < 32; I += 4) {
+                    uint32_t q2[4];
+#pragma unroll
+                    for (int k = 0; k < 4; k++)
+                        q2[k] = escape_pair(e, I + k, sm_word(sm, (I + k) >> 1));
+                    const int c = I >> 2;
+                    obuf[lane * 8 + (c ^ (lane & 7))] = make_uint4(q2[0], q2[1], q2[2], q2[3]);
+                }
+            }
+        }
         __syncwarp();
         // coalesced stores: 4 rows x 128 bytes per instruction
         const int c = lane & 7;
 #pragma unroll
         for (int it = 0; it < 8; it++) {
             const int r = it * 4 + (lane >> 3);
-            if (r < tc.R) {
+            if (r < L.R) {
                 const uint4 val = obuf[r * 8 + (c ^ (r & 7))];
-                uint16_t *dst = out + (tc.rb * kTileRows + r) * v.cols + tc.kg * kGroup + c * 8;
+                uint16_t *dst = out + (rb_cur * kTileRows + r) * v.cols + kg_cur * kGroup + c * 8;
                 *reinterpret_cast<uint4 *>(dst) = val;
             }
         }

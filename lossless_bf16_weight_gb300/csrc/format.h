@@ -20,8 +20,11 @@
 // 32*rb*cols + 64*R*kg + (c*R + j)*16 + b: one 16-byte chunk per row and
 // chunk index c, so that 32 lanes loading chunk c read 512 contiguous bytes.
 //
-// Codes: canonical, assigned in (length, palette index) order, written MSB
-// first; at most kLmax = 6 bits so that a 12-bit window holds two codes.
+// Codes: canonical, assigned in (length, palette index) order, at most
+// kLmax = 6 bits so that a 12-bit window holds two codes.  Bit order: the
+// code stream fills each byte from bit 0 up (stream bit i = bit i%8 of byte
+// i/8), each code entering most significant bit first; read as 32-bit
+// little-endian words, stream bit i is bit i%32 of word i/32.
 #pragma once
 #include <cstdint>
 

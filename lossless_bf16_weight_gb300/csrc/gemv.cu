@@ -74,13 +74,16 @@ __device__ __forceinline__ void gemv_body(const GemvParams &p) {
     float *red = reinterpret_cast<float *>(smem + off);
 
     // Start the first tile's loads before the shared tables are built.
-    TileRaw raw;
+    TileMeta meta{};
+    uint4 smn[4];
     uint32_t offs_next = 0;
     uint4 wcur[8], wnext[8];
+    const uint32_t cbuf0 = kCompressed ? smem_addr(wbuf) : 0u;
     if (kCompressed) {
         if (w_lo < w_hi) {
-            const uint32_t o = tile_offsets_load(p.v, rb * gpr + w_lo);
-            tile_load(p.v, rb * gpr + w_lo, o, raw);
+            const TileLoc L = tile_loc(p.v, rb, w_lo, gpr);
+            tile_fetch_codes(p.v, L, tile_offsets_load(p.v, rb * gpr + w_lo), cbuf0, meta);
+            tile_load_sm(p.v, L, smn);
             if (w_lo + 1 < w_hi)
                 offs_next = tile_offsets_load(p.v, rb * gpr + w_lo + 1);
         }
@@ -118,24 +121,43 @@ __device__ __forceinline__ void gemv_body(const GemvParams &p) {
         const float *xk = xs + (kg - kg_lo) * kGroup * BP;
         float4 x4[BP];
         if (kCompressed) {
+            const uint32_t cbuf = cbuf0 + uint32_t((kg - w_lo) & 1) * kCodeBufBytes;
             uint4 sm[4];
 #pragma unroll
             for (int c = 0; c < 4; c++)
-                sm[c] = raw.sm[c];
+                sm[c] = smn[c];
+            uint32_t esc0;
             LaneStream ls;
-            tile_setup(p.v, ds, raw, R, wbuf, ls, p.status);
+            const uint32_t esc_mask = tile_begin(p.v, ds, meta, R, cbuf, ls, p.status, &esc0);
             if (kg + 1 < w_hi) {
-                tile_load(p.v, t + 1, offs_next, raw);
+                const TileLoc L = tile_loc(p.v, rb, kg + 1, gpr);
+                tile_fetch_codes(p.v, L, offs_next, cbuf0 + uint32_t((kg + 1 - w_lo) & 1) * kCodeBufBytes, meta);
+                tile_load_sm(p.v, L, smn);
                 if (kg + 2 < w_hi)
                     offs_next = tile_offsets_load(p.v, t + 2);
             }
+            float2 saved[BP];
+#pragma unroll
+            for (int b = 0; b < BP; b++)
+                saved[b] = acc[b];
 #pragma unroll
             for (int I = 0; I < 32; I++) {
                 const uint32_t pair = decode_pair(ls, I, sm_word(sm, I >> 1));
                 fma_pair<BP>(pair, I, xk, x4, acc);
             }
             tile_check(ls, p.status);
-            __syncwarp();
+            if (esc_mask) {  // escaped groups: redo those lanes from raw exponents
+                if ((esc_mask >> lane) & 1u) {
+                    uint4 e[4];
+                    escape_load(p.v, esc0, esc_mask, e);
+#pragma unroll
+                    for (int b = 0; b < BP; b++)
+                        acc[b] = saved[b];
+#pragma unroll
+                    for (int I = 0; I < 32; I++)
+                        fma_pair<BP>(escape_pair(e, I, sm_word(sm, I >> 1)), I, xk, x4, acc);
+                }
+            }
         } else {
 #pragma unroll
             for (int c = 0; c < 8; c++)

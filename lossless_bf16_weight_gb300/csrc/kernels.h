@@ -13,6 +13,7 @@
 namespace uw {
 
 constexpr int kMaxSmemPerBlock = 227 * 1024;
+constexpr int kSmemPerSm = 228 * 1024 - 3 * 1024;  // minus the per-CTA reservation of 3 CTAs
 
 struct GemvParams {
     BlobView v;            // compressed weights (fused kernel)
@@ -28,6 +29,13 @@ struct GemvParams {
 
 size_t gemv_smem_bytes(int64_t cols, int warps, int splits, int bp, bool compressed);
 uw_status launch_gemv(const GemvParams &p, int warps, int bp, bool compressed, cudaStream_t stream);
+
+// Batch-1 GEMV on column CTAs: W warps (one 64-column group each) x
+// rb_per_cta row blocks per CTA; `col_blocks_per_sm` is the occupancy the
+// kernel is compiled for.
+inline int col_blocks_per_sm(int warps) { return warps >= 16 ? 1 : 24 / warps; }
+size_t gemv_kg_smem_bytes(int warps, int rb_per_cta, bool compressed);
+uw_status launch_gemv_kg(const GemvParams &p, int warps, int rb_per_cta, bool compressed, cudaStream_t stream);
 
 uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status, cudaStream_t stream);
 uw_status launch_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h, int64_t n, cudaStream_t stream);

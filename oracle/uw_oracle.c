@@ -35,7 +35,10 @@
  *   - among equally short codes, pick the lexicographically largest count
  *     vector (n_1, ..., n_LMAX), symbols ranked by (frequency desc, palette
  *     index asc); canonical code values by (length, palette index).
- *   - codes are written MSB first, each group starts on a byte boundary.
+ *   - bit order: the code stream fills each byte from its least significant
+ *     bit up (stream bit i is bit i%8 of byte i/8, the convention of
+ *     DEFLATE); each code enters the stream most significant code bit
+ *     first; each group starts on a byte boundary.
  *
  * The fp64 matrix product is the plain definition y[b,n] = sum_k x[b,k] W[n,k].
  */
@@ -289,7 +292,8 @@ static uint64_t get_u64(const uint8_t *p)
     return v;
 }
 
-/* Code bits of one group (symbols s[0..63]) written MSB first into out[48];
+/* Code bits of one group (symbols s[0..63]) into out[48], each code most
+ * significant bit first, stream bit i stored as bit i%8 of byte i/8;
  * returns the number of bits. */
 static int encode_group(const int *sym, const uint8_t *len, const uint16_t *code, uint8_t *out)
 {
@@ -299,7 +303,7 @@ static int encode_group(const int *sym, const uint8_t *len, const uint16_t *code
         int l = len[sym[i]];
         for (int b = l - 1; b >= 0; b--) {
             unsigned v = (code[sym[i]] >> b) & 1u;
-            out[bit / 8] |= (uint8_t)(v << (7 - bit % 8));
+            out[bit / 8] |= (uint8_t)(v << (bit % 8));
             bit++;
         }
     }
@@ -594,7 +598,7 @@ int uwo_decompress(const uint8_t *blob, int64_t bytes, uint16_t *w)
                         while (s < 0) {
                             if (l >= UWO_LMAX || bit >= 8 * (int64_t)gl)
                                 return -2;
-                            unsigned b = (blob[cpos + bit / 8] >> (7 - bit % 8)) & 1u;
+                            unsigned b = (blob[cpos + bit / 8] >> (bit % 8)) & 1u;
                             v = (v << 1) | b;
                             l++;
                             bit++;
