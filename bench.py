@@ -41,7 +41,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 ROWS, COLS, BATCH = 14336, 4096, 1
 WORKLOAD = "gate_proj 14336x4096 BF16 N(0,0.02) seed 0, compressed; y = x W^T, batch 1"
-KERNEL_SOURCES = ["decode.cuh", "gemv.cu", "format.h", "kernels.h"]
+KERNEL_SOURCES = ["decode.cuh", "gemv_kg.cu", "format.h", "kernels.h"]
 
 
 def parse():

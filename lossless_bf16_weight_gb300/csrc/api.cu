@@ -77,14 +77,13 @@ int pad_batch(int64_t b) {
     return c <= 1 ? 1 : c <= 2 ? 2 : c <= 4 ? 4 : 8;
 }
 
-// Default variant.  Batch 1: column CTAs of 8 warps with the most row blocks
-// per CTA that still gives about two CTAs per SM.  Otherwise row-block CTAs
+// Default variant.  Batch 1: column CTAs of 16 warps, one wave of the GPU.  Otherwise row-block CTAs
 // of 8 warps, split along K when the matrix has few row blocks.
 int default_gemv_variant(int64_t rows, int64_t cols, int64_t batch) {
     const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
     const int64_t gpr = cols / kGroup;
     if (batch == 1)
-        return kRowVariants + 4;  // 8 warps, two waves
+        return kRowVariants + 2;  // 16 warps, one wave
     const int bp = pad_batch(batch);
     int si = 0;
     while (si + 1 < kSplitChoices && nrb * (int64_t(1) << si) < 2 * 152 &&
@@ -211,6 +210,8 @@ void fill_blob_view(const uw_desc &d, const void *blob_dev, BlobView *v) {
     v->esc = b + d.off_esc;
     v->code_bytes = d.off_esc - d.off_code;
     v->n_escaped = d.n_escaped;
+    v->code16 = uint32_t((d.off_esc - d.off_code) / 16 > 0xFFFFFFFFull ? 0xFFFFFFFFull : (d.off_esc - d.off_code) / 16);
+    v->n_esc32 = uint32_t(d.n_escaped);
     v->rows = d.rows;
     v->cols = d.cols;
     uint16_t code[16];

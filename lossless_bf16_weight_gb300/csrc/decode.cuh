@@ -52,6 +52,8 @@ struct BlobView {
     const uint8_t *esc;
     uint64_t code_bytes;  // size of the code section
     uint64_t n_escaped;
+    uint32_t code16;      // code section size in 16-byte units (fits: tile offsets are u32)
+    uint32_t n_esc32;     // escaped groups (fits: escape offsets are u32)
     int64_t rows, cols;
     // 6-bit prefix -> (exponent << 4) | code length; 0 where no code starts
     // with that prefix.
@@ -60,7 +62,10 @@ struct BlobView {
 
 constexpr int kLutEntries = 4096;
 constexpr int kFakeWords = 16;                             // stream of 12-bit values 0..31 (+slack)
-constexpr int kCodeBufBytes = kMaxTileCodeBytes + 64;      // one tile's codes + read slack
+// One tile's shared buffer: its code region, then the raw exponent bytes of
+// its escaped groups ((32 - e) * 48 + 64 * e <= 2048 bytes), then read slack.
+constexpr int kTileBufData = 2048;
+constexpr int kCodeBufBytes = kTileBufData + 64;
 constexpr int kWarpBufBytes = 2 * kCodeBufBytes;           // two buffers: decode one, fill the other
 constexpr int kCommonSmemBytes = kLutEntries * 4 + kFakeWords * 4 + 32 * 4 + 64 * 2;
 
@@ -135,56 +140,40 @@ __device__ __forceinline__ uint32_t lop3_merge(uint32_t sm_part, uint32_t exp_pa
 
 // Where a tile's data lives: rows 32*rb .. 32*rb+R-1, group column kg.
 struct TileLoc {
-    int64_t q0;  // index of the tile's first group (group order of the blob)
-    int R;       // rows in the tile
+    const uint8_t *sm;    // the tile's sign+mantissa bytes (64 * R)
+    const uint8_t *glen;  // the tile's group byte lengths (R)
+    int R;                // rows in the tile
 };
 
 __device__ __forceinline__ TileLoc tile_loc(const BlobView &v, int64_t rb, int64_t kg, int64_t gpr) {
     TileLoc L;
     const int64_t left = v.rows - rb * kTileRows;
     L.R = left < kTileRows ? int(left) : kTileRows;
-    L.q0 = int64_t(kTileRows) * rb * gpr + int64_t(L.R) * kg;
+    const int64_t q0 = int64_t(kTileRows) * rb * gpr + int64_t(L.R) * kg;  // first group of the tile
+    L.sm = v.sm + q0 * kGroup;
+    L.glen = v.glen + q0;
     return L;
 }
 
-// A tile's lane-held bookkeeping: the lane's glen, and the tile's offsets
-// (lanes 0..3 hold tcode[t], tcode[t+1], tesc[t], tesc[t+1]).
+__device__ __forceinline__ int tile_rows(const BlobView &v, int64_t rb) {
+    const int64_t left = v.rows - rb * kTileRows;
+    return left < kTileRows ? int(left) : kTileRows;
+}
+
+// A tile's bookkeeping as fetched: the lane's glen, and warp-uniform
+// values: first escaped group, and n16 | nesc << 8 | bad << 16.
 struct TileMeta {
     uint32_t glen;
-    uint32_t offs;
+    uint32_t esc0;
+    uint32_t pk;
 };
-
-struct TileOffsets {
-    uint32_t c0, n16;     // code region start and size, 16-byte units
-    uint32_t esc0, nesc;  // first escaped group of the tile, escaped groups in it
-    bool bad;             // offsets out of range
-};
-
-__device__ __forceinline__ TileOffsets unpack_offsets(const BlobView &v, uint32_t offs, int R) {
-    const uint32_t c0 = __shfl_sync(0xffffffffu, offs, 0);
-    const uint32_t c1 = __shfl_sync(0xffffffffu, offs, 1);
-    const uint32_t e0 = __shfl_sync(0xffffffffu, offs, 2);
-    const uint32_t e1 = __shfl_sync(0xffffffffu, offs, 3);
-    TileOffsets o;
-    o.c0 = c0;
-    o.n16 = c1 - c0;
-    o.esc0 = e0;
-    o.nesc = e1 - e0;
-    o.bad = (c1 < c0) || (o.n16 * 16u > uint32_t(kMaxTileCodeBytes)) || (uint64_t(c1) * 16u > v.code_bytes) ||
-            (e1 < e0) || (o.nesc > uint32_t(R)) || (uint64_t(e1) > v.n_escaped);
-    return o;
-}
 
 // Load the offsets of tile t = rb * (cols/64) + kg into lanes 0..3
 // (tcode[t], tcode[t+1], tesc[t], tesc[t+1]); issued ahead of the data.
 __device__ __forceinline__ uint32_t tile_offsets_load(const BlobView &v, int64_t t) {
     const int lane = threadIdx.x & 31;
-    uint32_t off = 0;
-    if (lane < 2)
-        off = __ldg(v.tcode + t + lane);
-    else if (lane < 4)
-        off = __ldg(v.tesc + t + (lane - 2));
-    return off;
+    const uint32_t *src = lane < 2 ? v.tcode + t + lane : v.tesc + t + (lane - 2);
+    return lane < 4 ? __ldg(src) : 0u;
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -197,61 +186,64 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     return v;
 }
 
-// Validate the tile's offsets, load the lane's glen and start copying the
-// code region into the code buffer at shared address `cbuf` (cp.async, one
-// commit group).  `offs` comes from tile_offsets_load.
-__device__ __forceinline__ void tile_fetch_codes(const BlobView &v, const TileLoc &L, uint32_t offs, uint32_t cbuf,
-                                                 TileMeta &m) {
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
+
+// The lane's 64 sign+mantissa bytes: chunk c of row j sits at (c*R + j)*16
+// inside the tile (zeros for lanes without a row).
+__device__ __forceinline__ void tile_sm_load(const TileLoc &L, uint4 (&sm)[4]) {
     const int lane = threadIdx.x & 31;
-    const TileOffsets o = unpack_offsets(v, offs, L.R);
-    m.offs = offs;
-    m.glen = lane < L.R ? __ldg(v.glen + L.q0 + lane) : 0u;
-    if (!o.bad) {
-        const uint8_t *src = v.code + size_t(o.c0) * 16;
+    const uint8_t *smb = L.sm + 16 * lane;
+    const int stride = 16 * L.R;
 #pragma unroll
-        for (int c = 0; c < 3; c++) {
-            const uint32_t idx = uint32_t(lane + 32 * c);
-            if (idx < o.n16)
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                             :: "r"(cbuf + 16u * idx), "l"(src + 16 * size_t(idx)) : "memory");
+    for (int c = 0; c < 4; c++)
+        sm[c] = lane < L.R ? __ldg(reinterpret_cast<const uint4 *>(smb + c * stride)) : make_uint4(0, 0, 0, 0);
+}
+
+// Fetch a tile: validate its offsets (`offs` from tile_offsets_load), load
+// the lane's glen and 64 sign+mantissa bytes into registers, and start
+// copying its code region followed by its escaped groups' raw exponents
+// into the tile buffer at shared address `cbuf` (cp.async, one commit
+// group).
+__device__ __forceinline__ void tile_fetch(const BlobView &v, const TileLoc &L, uint32_t offs, uint32_t cbuf,
+                                           TileMeta &m, uint4 (&sm)[4]) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t c0 = __shfl_sync(0xffffffffu, offs, 0);
+    const uint32_t c1 = __shfl_sync(0xffffffffu, offs, 1);
+    const uint32_t e0 = __shfl_sync(0xffffffffu, offs, 2);
+    const uint32_t e1 = __shfl_sync(0xffffffffu, offs, 3);
+    const uint32_t n16 = c1 - c0, nesc = e1 - e0;
+    const bool bad = c1 < c0 || n16 > uint32_t(kMaxTileCodeBytes / 16) || c1 > v.code16 || e1 < e0 ||
+                     nesc > uint32_t(L.R) || e1 > v.n_esc32 || n16 * 16u + nesc * 64u > uint32_t(kTileBufData);
+    m.pk = bad ? (1u << 16) : (n16 | (nesc << 8));
+    m.esc0 = e0;
+    m.glen = lane < L.R ? __ldg(L.glen + lane) : 0u;
+    tile_sm_load(L, sm);
+    if (!bad) {
+        const uint8_t *src = v.code + size_t(c0) * 16 + 16 * lane;
+        const uint32_t dst = cbuf + 16u * lane;
+#pragma unroll
+        for (int c = 0; c < 3; c++)
+            if (uint32_t(lane + 32 * c) < n16)
+                cp_async16(dst + 512u * c, src + 512 * c);
+        if (nesc) {
+            const uint8_t *esrc = v.esc + size_t(e0) * 64 + 16 * lane;
+            const uint32_t edst = cbuf + 16u * n16 + 16u * lane;
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+                if (uint32_t(lane + 32 * c) < 4 * nesc)
+                    cp_async16(edst + 512u * c, esrc + 512 * c);
         }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-// The lane's 64 sign+mantissa bytes (16-byte chunk c of row j sits at
-// (c*R + j)*16 inside the tile).
-__device__ __forceinline__ void tile_load_sm(const BlobView &v, const TileLoc &L, uint4 (&sm)[4]) {
-    const int lane = threadIdx.x & 31;
-    const uint8_t *smt = v.sm + L.q0 * kGroup;
-#pragma unroll
-    for (int c = 0; c < 4; c++)
-        sm[c] = lane < L.R ? __ldg(reinterpret_cast<const uint4 *>(smt + (size_t(c) * L.R + lane) * 16))
-                           : make_uint4(0, 0, 0, 0);
-}
-
-// One 16-byte chunk (weights 16c .. 16c+15 of the lane's group).
-__device__ __forceinline__ uint4 tile_load_sm_chunk(const BlobView &v, const TileLoc &L, int c) {
-    const int lane = threadIdx.x & 31;
-    const uint8_t *smt = v.sm + L.q0 * kGroup;
-    return lane < L.R ? __ldg(reinterpret_cast<const uint4 *>(smt + (size_t(c) * L.R + lane) * 16))
-                      : make_uint4(0, 0, 0, 0);
-}
-
-// Ask for the tile's sign+mantissa bytes (64*R contiguous bytes, one
-// 128-byte line per lane) ahead of the loads that use them; costs no
-// registers.  kL1 brings them into this SM's L1, otherwise into L2.
-template <bool kL1 = false>
-__device__ __forceinline__ void tile_prefetch_sm(const BlobView &v, const TileLoc &L) {
-    const int lane = threadIdx.x & 31;
-    if (kL1) {
-        if (lane * 2 < L.R)
-            asm volatile("prefetch.global.L1 [%0];" :: "l"(v.sm + L.q0 * kGroup + 128 * lane));
-    } else if (lane == 0 && L.R > 0) {
-        // one bulk request on the TMA engine for the whole 64*R-byte region
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-                     :: "l"(v.sm + L.q0 * kGroup), "r"(uint32_t(kGroup * L.R)) : "memory");
-    }
 }
 
 // Per-tile, per-lane decode state.  Addresses are 32-bit shared addresses.
@@ -266,13 +258,12 @@ struct LaneStream {
 
 // Wait for the tile's codes, validate, and set up every lane's stream.
 // Returns the mask of lanes whose group is escaped (0 for a bad tile, whose
-// lanes all decode zeros; the error is recorded in *status) and, in *esc0,
-// the index of the tile's first escaped group.
-__device__ __forceinline__ uint32_t tile_begin(const BlobView &v, const DecodeShared &s, const TileMeta &m, int R,
-                                               uint32_t cbuf, LaneStream &ls, uint32_t *status, uint32_t *esc0) {
+// lanes all decode zeros; the error is recorded in *status).
+__device__ __forceinline__ uint32_t tile_begin(const DecodeShared &s, const TileMeta &m, int R, uint32_t cbuf,
+                                               LaneStream &ls, uint32_t *status) {
     const int lane = threadIdx.x & 31;
     const bool valid = lane < R;
-    const TileOffsets o = unpack_offsets(v, m.offs, R);
+    const uint32_t n16 = m.pk & 0xFFu, nesc = (m.pk >> 8) & 0xFFu;
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
     const uint32_t g = m.glen;
@@ -286,11 +277,10 @@ __device__ __forceinline__ uint32_t tile_begin(const BlobView &v, const DecodeSh
     const uint32_t off = incl - g;
     const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
     const uint32_t esc_mask = __ballot_sync(0xffffffffu, valid && g == 0);
-    const bool over = o.bad || total > o.n16 * 16u;
-    const bool bad = over || uint32_t(__popc(esc_mask)) != o.nesc;
+    const bool over = (m.pk >> 16) != 0 || total > n16 * 16u;
+    const bool bad = over || uint32_t(__popc(esc_mask)) != nesc;
     if (bad && lane == 0)
         atomicOr(status, over ? kStatusBadTile : kStatusBadEscape);
-    *esc0 = o.esc0;
     uint32_t w0, c0;
     if (!bad && valid && g != 0) {
         w0 = cbuf + (off & ~3u);
@@ -312,15 +302,21 @@ __device__ __forceinline__ uint32_t tile_begin(const BlobView &v, const DecodeSh
     return bad ? 0u : esc_mask;
 }
 
-// Raw exponent bytes of the calling lane's escaped group (lane must be in
-// the mask returned by tile_begin).
-__device__ __forceinline__ void escape_load(const BlobView &v, uint32_t esc0, uint32_t esc_mask, uint4 (&e)[4]) {
+// Shared address of a fetched tile's raw escape bytes (after its codes).
+__device__ __forceinline__ uint32_t escape_base(const TileMeta &m, uint32_t cbuf) {
+    return cbuf + 16u * (m.pk & 0xFFu);
+}
+
+// Raw exponent bytes of the calling lane's escaped group, from the tile
+// buffer (lane must be in the mask returned by tile_begin; `ebase` from
+// escape_base).
+__device__ __forceinline__ void escape_read(uint32_t ebase, uint32_t esc_mask, uint4 (&e)[4]) {
     const int lane = threadIdx.x & 31;
     const uint32_t rank = __popc(esc_mask & ((1u << lane) - 1u));
-    const uint4 *src = reinterpret_cast<const uint4 *>(v.esc + (uint64_t(esc0) + rank) * 64);
+    const uint32_t a = ebase + 64u * rank;
 #pragma unroll
     for (int c = 0; c < 4; c++)
-        e[c] = __ldg(src + c);
+        e[c] = lds128(a + 16u * c);
 }
 
 // One step: decode the exponents of weights 2i, 2i+1 and merge them with the

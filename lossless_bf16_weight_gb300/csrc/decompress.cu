@@ -38,9 +38,7 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
     uint32_t offs_next = 0;
     const uint32_t cbuf0 = smem_addr(wbuf);
     if (t_lo < t_hi) {
-        const TileLoc L = tile_loc(v, rb, kg, gpr);
-        tile_fetch_codes(v, L, tile_offsets_load(v, t_lo), cbuf0, meta);
-        tile_load_sm(v, L, smn);
+        tile_fetch(v, tile_loc(v, rb, kg, gpr), tile_offsets_load(v, t_lo), cbuf0, meta, smn);
         if (t_lo + 1 < t_hi)
             offs_next = tile_offsets_load(v, t_lo + 1);
     }
@@ -48,7 +46,7 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
     __syncthreads();
 
     for (int64_t t = t_lo; t < t_hi; t++) {
-        const TileLoc L = tile_loc(v, rb, kg, gpr);
+        const int R = tile_rows(v, rb);
         const int64_t rb_cur = rb, kg_cur = kg;
         if (++kg == gpr) {
             kg = 0;
@@ -59,13 +57,12 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
 #pragma unroll
         for (int c = 0; c < 4; c++)
             sm[c] = smn[c];
-        uint32_t esc0;
         LaneStream ls;
-        const uint32_t esc_mask = tile_begin(v, ds, meta, L.R, cbuf, ls, status, &esc0);
+        const uint32_t esc_mask = tile_begin(ds, meta, R, cbuf, ls, status);
+        const uint32_t ebase = escape_base(meta, cbuf);
         if (t + 1 < t_hi) {
-            const TileLoc N = tile_loc(v, rb, kg, gpr);
-            tile_fetch_codes(v, N, offs_next, cbuf0 + uint32_t((t + 1 - t_lo) & 1) * kCodeBufBytes, meta);
-            tile_load_sm(v, N, smn);
+            tile_fetch(v, tile_loc(v, rb, kg, gpr), offs_next, cbuf0 + uint32_t((t + 1 - t_lo) & 1) * kCodeBufBytes,
+                       meta, smn);
             if (t + 2 < t_hi)
                 offs_next = tile_offsets_load(v, t + 2);
         }
@@ -82,7 +79,7 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
         if (esc_mask) {  // escaped groups: redo those lanes from raw exponents
             if ((esc_mask >> lane) & 1u) {
                 uint4 e[4];
-                escape_load(v, esc0, esc_mask, e);
+                escape_read(ebase, esc_mask, e);
 #pragma unroll
                 for (int I = 0; I < 32; I += 4) {
                     uint32_t q2[4];
@@ -100,7 +97,7 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
 #pragma unroll
         for (int it = 0; it < 8; it++) {
             const int r = it * 4 + (lane >> 3);
-            if (r < L.R) {
+            if (r < R) {
                 const uint4 val = obuf[r * 8 + (c ^ (r & 7))];
                 uint16_t *dst = out + (rb_cur * kTileRows + r) * v.cols + kg_cur * kGroup + c * 8;
                 *reinterpret_cast<uint4 *>(dst) = val;

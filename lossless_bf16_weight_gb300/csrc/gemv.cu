@@ -81,9 +81,8 @@ __device__ __forceinline__ void gemv_body(const GemvParams &p) {
     const uint32_t cbuf0 = kCompressed ? smem_addr(wbuf) : 0u;
     if (kCompressed) {
         if (w_lo < w_hi) {
-            const TileLoc L = tile_loc(p.v, rb, w_lo, gpr);
-            tile_fetch_codes(p.v, L, tile_offsets_load(p.v, rb * gpr + w_lo), cbuf0, meta);
-            tile_load_sm(p.v, L, smn);
+            tile_fetch(p.v, tile_loc(p.v, rb, w_lo, gpr), tile_offsets_load(p.v, rb * gpr + w_lo), cbuf0, meta,
+                       smn);
             if (w_lo + 1 < w_hi)
                 offs_next = tile_offsets_load(p.v, rb * gpr + w_lo + 1);
         }
@@ -126,13 +125,12 @@ __device__ __forceinline__ void gemv_body(const GemvParams &p) {
 #pragma unroll
             for (int c = 0; c < 4; c++)
                 sm[c] = smn[c];
-            uint32_t esc0;
             LaneStream ls;
-            const uint32_t esc_mask = tile_begin(p.v, ds, meta, R, cbuf, ls, p.status, &esc0);
+            const uint32_t esc_mask = tile_begin(ds, meta, R, cbuf, ls, p.status);
+            const uint32_t ebase = escape_base(meta, cbuf);
             if (kg + 1 < w_hi) {
-                const TileLoc L = tile_loc(p.v, rb, kg + 1, gpr);
-                tile_fetch_codes(p.v, L, offs_next, cbuf0 + uint32_t((kg + 1 - w_lo) & 1) * kCodeBufBytes, meta);
-                tile_load_sm(p.v, L, smn);
+                tile_fetch(p.v, tile_loc(p.v, rb, kg + 1, gpr), offs_next,
+                           cbuf0 + uint32_t((kg + 1 - w_lo) & 1) * kCodeBufBytes, meta, smn);
                 if (kg + 2 < w_hi)
                     offs_next = tile_offsets_load(p.v, t + 2);
             }
@@ -149,7 +147,7 @@ __device__ __forceinline__ void gemv_body(const GemvParams &p) {
             if (esc_mask) {  // escaped groups: redo those lanes from raw exponents
                 if ((esc_mask >> lane) & 1u) {
                     uint4 e[4];
-                    escape_load(p.v, esc0, esc_mask, e);
+                    escape_read(ebase, esc_mask, e);
 #pragma unroll
                     for (int b = 0; b < BP; b++)
                         acc[b] = saved[b];

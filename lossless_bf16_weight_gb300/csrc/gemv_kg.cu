@@ -17,9 +17,9 @@
 // mixed-precision fma.rn.f32.bf16 (BF16 x BF16 is exact in fp32, so each
 // step is one correctly rounded fp32 add of the exact product).
 //
-// Loads run one tile pair ahead: code regions by cp.async into the warp's
-// second pair of shared buffers; glen and the sign+mantissa bytes into
-// registers.
+// Loads run one tile pair ahead: code regions and escaped groups' raw
+// exponents by cp.async into the warp's second pair of shared buffers; glen
+// and the sign+mantissa bytes into registers.
 //
 // Order of the sum for output n (row j of block rb):
 //   tile partial  = acc_even + acc_odd       (k even / odd within the group)
@@ -52,18 +52,13 @@ __device__ __forceinline__ void prefetch_bf16_row(const GemvParams &p, int64_t r
         asm volatile("prefetch.global.L2 [%0];" :: "l"(p.w + n * p.cols + kg * kGroup));
 }
 
-// Resident CTAs per SM the register budget is sized for: 24 warps.
-template <int W>
-constexpr int kColBlocksPerSm = W >= 16 ? 1 : 24 / W;
-
 // The two accumulators of an escaped group's lane, rebuilt from its raw
 // exponent bytes (rare; kept out of line so that it costs the hot loop no
-// registers).
-__device__ __noinline__ float2 escaped_tile_sum(const BlobView &v, uint32_t esc0, uint32_t em, const TileLoc &L,
-                                                uint32_t xw) {
+// registers, so the sign+mantissa bytes are loaded again).
+__device__ __noinline__ float2 escaped_tile_sum(uint32_t ebase, uint32_t em, const TileLoc &L, uint32_t xw) {
     uint4 e[4], sm[4];
-    escape_load(v, esc0, em, e);
-    tile_load_sm(v, L, sm);
+    escape_read(ebase, em, e);
+    tile_sm_load(L, sm);
     float b0 = 0.f, b1 = 0.f;
 #pragma unroll
     for (int I = 0; I < 32; I++)
@@ -82,7 +77,7 @@ __device__ __forceinline__ void gemv_col_body(const GemvParams &p, int rb_per_ct
     const int split = blockIdx.y;
     const int64_t kg = int64_t(split) * W + warp;
     const bool active = kg < gpr;
-    const TileMeta empty = {0u, 0u};
+    const TileMeta empty = {0u, 0u, 0u};
 
     // shared memory: [common tables][x slab W x 32 pairs][per warp 4 code buffers]
     // [tile partials rb_per_cta x W x 32]
@@ -119,14 +114,10 @@ __device__ __forceinline__ void gemv_col_body(const GemvParams &p, int rb_per_ct
         nsmB[c] = make_uint4(0, 0, 0, 0);
     }
     if (kCompressed && npair > 0) {
-        const TileLoc LA = tile_loc(p.v, rb0, kg, gpr);
-        tile_load_sm(p.v, LA, nsmA);
-        tile_fetch_codes(p.v, LA, tile_offsets_load(p.v, rb0 * gpr + kg), cb0, mA);
-        if (ntile > 1) {
-            const TileLoc LB = tile_loc(p.v, rb0 + 1, kg, gpr);
-            tile_load_sm(p.v, LB, nsmB);
-            tile_fetch_codes(p.v, LB, tile_offsets_load(p.v, (rb0 + 1) * gpr + kg), cb0 + kCodeBufBytes, mB);
-        }
+        tile_fetch(p.v, tile_loc(p.v, rb0, kg, gpr), tile_offsets_load(p.v, rb0 * gpr + kg), cb0, mA, nsmA);
+        if (ntile > 1)
+            tile_fetch(p.v, tile_loc(p.v, rb0 + 1, kg, gpr), tile_offsets_load(p.v, (rb0 + 1) * gpr + kg),
+                       cb0 + kCodeBufBytes, mB, nsmB);
         if (ntile > 2)
             offA = tile_offsets_load(p.v, (rb0 + 2) * gpr + kg);
         if (ntile > 3)
@@ -146,10 +137,8 @@ __device__ __forceinline__ void gemv_col_body(const GemvParams &p, int rb_per_ct
         const bool hasB = rbB < rb1;
         float aA0 = 0.f, aA1 = 0.f, aB0 = 0.f, aB1 = 0.f;
         if (kCompressed) {
-            const TileLoc LA = tile_loc(p.v, rbA, kg, gpr);
-            TileLoc LB = tile_loc(p.v, hasB ? rbB : rbA, kg, gpr);
-            if (!hasB)
-                LB.R = 0;  // an empty tile: every lane decodes zeros
+            const int RA = tile_rows(p.v, rbA);
+            const int RB = hasB ? tile_rows(p.v, rbB) : 0;  // no tile B: every lane decodes zeros
             const uint32_t bufA = cb0 + uint32_t(i & 1) * 2 * kCodeBufBytes, bufB = bufA + kCodeBufBytes;
             uint4 smA[4], smB[4];  // this pair's sign+mantissa bytes, loaded during the previous pair
 #pragma unroll
@@ -158,19 +147,15 @@ __device__ __forceinline__ void gemv_col_body(const GemvParams &p, int rb_per_ct
                 smB[c] = nsmB[c];
             }
             LaneStream la, lb;
-            uint32_t escA, escB;
-            const uint32_t emA = tile_begin(p.v, ds, mA, LA.R, bufA, la, p.status, &escA);
-            const uint32_t emB = tile_begin(p.v, ds, mB, LB.R, bufB, lb, p.status, &escB);
+            const uint32_t emA = tile_begin(ds, mA, RA, bufA, la, p.status);
+            const uint32_t emB = tile_begin(ds, mB, RB, bufB, lb, p.status);
+            const uint32_t ebA = escape_base(mA, bufA), ebB = escape_base(mB, bufB);
             // fetch the next pair while this one is decoded
             if (i + 1 < npair) {
                 const uint32_t nA = cb0 + uint32_t((i + 1) & 1) * 2 * kCodeBufBytes;
-                const TileLoc NA = tile_loc(p.v, rbA + 2, kg, gpr);
-                tile_fetch_codes(p.v, NA, offA, nA, mA);
-                tile_load_sm(p.v, NA, nsmA);
+                tile_fetch(p.v, tile_loc(p.v, rbA + 2, kg, gpr), offA, nA, mA, nsmA);
                 if (rbB + 2 < rb1) {
-                    const TileLoc NB = tile_loc(p.v, rbB + 2, kg, gpr);
-                    tile_fetch_codes(p.v, NB, offB, nA + kCodeBufBytes, mB);
-                    tile_load_sm(p.v, NB, nsmB);
+                    tile_fetch(p.v, tile_loc(p.v, rbB + 2, kg, gpr), offB, nA + kCodeBufBytes, mB, nsmB);
                 } else {
                     mB = empty;
 #pragma unroll
@@ -192,12 +177,12 @@ __device__ __forceinline__ void gemv_col_body(const GemvParams &p, int rb_per_ct
             tile_check(lb, p.status);
             if (emA | emB) {  // escaped groups: redo those lanes from raw exponents
                 if ((emA >> lane) & 1u) {
-                    const float2 r = escaped_tile_sum(p.v, escA, emA, LA, xw);
+                    const float2 r = escaped_tile_sum(ebA, emA, tile_loc(p.v, rbA, kg, gpr), xw);
                     aA0 = r.x;
                     aA1 = r.y;
                 }
                 if ((emB >> lane) & 1u) {
-                    const float2 r = escaped_tile_sum(p.v, escB, emB, LB, xw);
+                    const float2 r = escaped_tile_sum(ebB, emB, tile_loc(p.v, rbB, kg, gpr), xw);
                     aB0 = r.x;
                     aB1 = r.y;
                 }
@@ -277,7 +262,7 @@ __device__ __forceinline__ void gemv_col_body(const GemvParams &p, int rb_per_ct
 }
 
 template <int W, bool kCompressed>
-__global__ void __launch_bounds__(W * 32, kColBlocksPerSm<W>) gemv_kg_kernel(const GemvParams p, int rb_per_cta) {
+__global__ void __launch_bounds__(W * 32, col_blocks_per_sm(W)) gemv_kg_kernel(const GemvParams p, int rb_per_cta) {
     gemv_col_body<W, kCompressed>(p, rb_per_cta);
 }
 

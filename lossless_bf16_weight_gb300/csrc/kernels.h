@@ -33,7 +33,8 @@ uw_status launch_gemv(const GemvParams &p, int warps, int bp, bool compressed, c
 // Batch-1 GEMV on column CTAs: W warps (one 64-column group each) x
 // rb_per_cta row blocks per CTA; `col_blocks_per_sm` is the occupancy the
 // kernel is compiled for.
-inline int col_blocks_per_sm(int warps) { return warps >= 16 ? 1 : 24 / warps; }
+// 16 warps per SM leaves each thread 128 registers.
+constexpr int col_blocks_per_sm(int warps) { return warps >= 16 ? 1 : 16 / warps; }
 size_t gemv_kg_smem_bytes(int warps, int rb_per_cta, bool compressed);
 uw_status launch_gemv_kg(const GemvParams &p, int warps, int rb_per_cta, bool compressed, cudaStream_t stream);
 
