@@ -28,22 +28,30 @@ uint64_t rd64(const uint8_t *p) {
 
 cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
-// CUDA-core kernel variants.
+// Kernel variants.
 //   0..14  row-block CTAs (gemv.cu): warps per CTA x split count
 //   15..26 column CTAs, batch 1 only (gemv_kg.cu): warps per CTA x grid
 //          size in full waves (1..4) of the GPU; the row blocks per CTA
 //          follow from the matrix and the SM count
+//   27..34 tensor-core CTAs (gemm_tc.cu): producer groups G (2, 4) x K
+//          splits (1, 2, 4, 8, capped at the number of 64-column groups)
 constexpr int kWarpChoices[3] = {4, 8, 16};
 constexpr int kSplitChoices = 5;  // 1, 2, 4, 8, 16
 constexpr int kRowVariants = 3 * kSplitChoices;
 constexpr int kColWaves = 4;
 constexpr int kColVariants = 3 * kColWaves;
-constexpr int kGemvVariants = kRowVariants + kColVariants;
+constexpr int kTcGroups[2] = {2, 4};
+constexpr int kTcSplitChoices = 4;  // 1, 2, 4, 8
+constexpr int kTcVariants = 2 * kTcSplitChoices;
+constexpr int kTcFirst = kRowVariants + kColVariants;
+constexpr int kGemvVariants = kTcFirst + kTcVariants;
 constexpr int kMaxBatchChunk = 8;
 
+enum class Kind { kRow, kColumn, kTensor };
+
 struct GemvVariant {
-    bool column;
-    int warps, splits, rb;
+    Kind kind;
+    int warps, splits, rb;  // warps: CTA warps (row, column) or producer groups G (tensor)
 };
 
 int sm_count() {
@@ -55,12 +63,17 @@ int sm_count() {
 }
 
 GemvVariant gemv_variant(int v, int64_t rows, int64_t cols) {
+    const int64_t gpr = cols / kGroup;
     if (v < kRowVariants)
-        return {false, kWarpChoices[v % 3], 1 << (v / 3), 0};
+        return {Kind::kRow, kWarpChoices[v % 3], 1 << (v / 3), 0};
+    if (v >= kTcFirst) {
+        const int i = v - kTcFirst;
+        const int64_t splits = std::min<int64_t>(int64_t(1) << (i % kTcSplitChoices), gpr);
+        return {Kind::kTensor, kTcGroups[i / kTcSplitChoices], int(splits), 0};
+    }
     const int i = v - kRowVariants;
     const int w = kWarpChoices[i % 3];
     const int waves = 1 + i / 3;
-    const int64_t gpr = cols / kGroup;
     const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
     const int64_t splits = (gpr + w - 1) / w;
     const int64_t slots = int64_t(sm_count()) * col_blocks_per_sm(w) * waves;  // CTAs per wave x waves
@@ -69,7 +82,28 @@ GemvVariant gemv_variant(int v, int64_t rows, int64_t cols) {
     // keep the CTAs of one SM within its shared memory
     while (rb > 2 && gemv_kg_smem_bytes(w, int(rb), true) * col_blocks_per_sm(w) > size_t(kSmemPerSm))
         rb -= 2;
-    return {true, w, int(splits), int(rb)};
+    return {Kind::kColumn, w, int(splits), int(rb)};
+}
+
+// Tensor-core default: four producer groups while their stages fit, and the
+// K split (1, 2, 4, 8) whose grid fills the GPU's waves best (ties to fewer
+// splits).
+int default_tc_variant(int64_t rows, int64_t cols, int64_t batch) {
+    const int64_t np = std::min<int64_t>((batch + 15) / 16 * 16, kTcMaxBatch);
+    const int gi = gemm_tc_stages(4, int(np), true) >= 4 ? 1 : 0;
+    const int64_t mblocks = (rows + 127) / 128, gpr = cols / kGroup, sms = sm_count();
+    int best = 0;
+    double best_eff = -1.0;
+    for (int si = 0; si < kTcSplitChoices; si++) {
+        const int64_t sp = std::min<int64_t>(int64_t(1) << si, gpr);
+        const int64_t ctas = mblocks * sp;
+        const double eff = double(ctas) / double((ctas + sms - 1) / sms * sms);
+        if (eff > best_eff + 0.02) {
+            best_eff = eff;
+            best = si;
+        }
+    }
+    return kTcFirst + gi * kTcSplitChoices + best;
 }
 
 int pad_batch(int64_t b) {
@@ -77,13 +111,16 @@ int pad_batch(int64_t b) {
     return c <= 1 ? 1 : c <= 2 ? 2 : c <= 4 ? 4 : 8;
 }
 
-// Default variant.  Batch 1: column CTAs of 16 warps, one wave of the GPU.  Otherwise row-block CTAs
+// Default variant.  Batch 1: column CTAs of 16 warps, one wave of the GPU.
+// Batch 16 and up: tensor-core CTAs.  Otherwise row-block CTAs
 // of 8 warps, split along K when the matrix has few row blocks.
 int default_gemv_variant(int64_t rows, int64_t cols, int64_t batch) {
     const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
     const int64_t gpr = cols / kGroup;
     if (batch == 1)
         return kRowVariants + 2;  // 16 warps, one wave
+    if (batch >= 16)
+        return default_tc_variant(rows, cols, batch);
     const int bp = pad_batch(batch);
     int si = 0;
     while (si + 1 < kSplitChoices && nrb * (int64_t(1) << si) < 2 * 152 &&
@@ -98,11 +135,14 @@ WsLayout layout_for(int64_t rows, int64_t cols, int64_t batch, int strategy, int
     WsLayout L;
     const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
     const GemvVariant gv = gemv_variant(variant, rows, cols);
-    const int bp = gv.column ? 1 : pad_batch(batch);
+    const int bp = gv.kind == Kind::kColumn ? 1 : pad_batch(batch);
+    const uint64_t partial_floats = gv.kind == Kind::kTensor
+                                        ? uint64_t(gemm_tc_partial_floats(rows, batch, gv.splits))
+                                        : uint64_t(nrb) * gv.splits * bp * 32;
     L.status = 0;
     L.counters = 256;
     L.partial = align_up(L.counters + 4 * uint64_t(nrb), 256);
-    L.weights = align_up(L.partial + 4 * uint64_t(nrb) * gv.splits * bp * 32, 256);
+    L.weights = align_up(L.partial + 4 * partial_floats, 256);
     L.total = L.weights;
     if (strategy == UW_STRATEGY_DECOMPRESS_GEMM)
         L.total = align_up(L.weights + 2 * uint64_t(rows) * uint64_t(cols), 256);
@@ -131,11 +171,27 @@ uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t 
     return UW_OK;
 }
 
-// Batch rows go through the CUDA-core kernels in chunks of at most 8; the
-// column kernels take batch 1 only.
+// Batch rows go through the CUDA-core row kernels in chunks of at most 8;
+// the column kernels take batch 1 only; the tensor-core kernels take any
+// batch (chunks of 256 inside the launcher).
 uw_status run_gemv(GemvParams p, int variant, bool compressed, cudaStream_t stream) {
     const GemvVariant gv = gemv_variant(variant, p.rows, p.cols);
-    if (gv.column) {
+    if (gv.kind == Kind::kTensor) {
+        TcParams t{};
+        t.v = p.v;
+        t.w = p.w;
+        t.x = p.x;
+        t.y = p.y;
+        t.partial = p.partial;
+        t.counters = p.counters;
+        t.status = p.status;
+        t.rows = p.rows;
+        t.cols = p.cols;
+        t.batch = p.batch;
+        t.splits = gv.splits;
+        return launch_gemm_tc(t, gv.warps, compressed, stream);
+    }
+    if (gv.kind == Kind::kColumn) {
         if (p.batch != 1)
             return UW_ERR_UNSUPPORTED;
         p.splits = gv.splits;
@@ -453,7 +509,8 @@ extern "C" const char *uw_variant_name(int32_t strategy, int32_t variant) {
         "w4s1", "w8s1", "w16s1", "w4s2", "w8s2", "w16s2", "w4s4", "w8s4", "w16s4",
         "w4s8", "w8s8", "w16s8", "w4s16", "w8s16", "w16s16",
         "col_w4x1", "col_w8x1", "col_w16x1", "col_w4x2", "col_w8x2", "col_w16x2",
-        "col_w4x3", "col_w8x3", "col_w16x3", "col_w4x4", "col_w8x4", "col_w16x4"};
+        "col_w4x3", "col_w8x3", "col_w16x3", "col_w4x4", "col_w8x4", "col_w16x4",
+        "tc_g2s1", "tc_g2s2", "tc_g2s4", "tc_g2s8", "tc_g4s1", "tc_g4s2", "tc_g4s4", "tc_g4s8"};
     if (uw_variant_count(strategy) == 0 || variant < 0 || variant >= kGemvVariants)
         return nullptr;
     return names[variant];

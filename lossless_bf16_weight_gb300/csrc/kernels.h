@@ -38,6 +38,28 @@ constexpr int col_blocks_per_sm(int warps) { return warps >= 16 ? 1 : 16 / warps
 size_t gemv_kg_smem_bytes(int warps, int rb_per_cta, bool compressed);
 uw_status launch_gemv_kg(const GemvParams &p, int warps, int rb_per_cta, bool compressed, cudaStream_t stream);
 
+// Tensor-core matmul (gemm_tc.cu): CTAs of 4G producer warps + 1 MMA warp,
+// 128 rows of W each, `splits` K ranges; batches above kTcMaxBatch run as
+// several launches.
+constexpr int kTcMaxBatch = 256;
+struct TcParams {
+    BlobView v;            // compressed weights (fused kernel)
+    const uint16_t *w;     // uncompressed weights (twin kernel)
+    const uint16_t *x;     // [batch, cols]
+    uint16_t *y;           // [batch, rows]
+    float *partial;        // [row blocks of 128][splits][Np][128] split partial sums
+    uint32_t *counters;    // [row blocks of 128] arrival counters, left at zero
+    uint32_t *status;      // device error word
+    int64_t rows, cols, batch;
+    int splits;
+    int S, Np;             // stages, padded batch (set by the launcher)
+    uint32_t tmem_cols;    // tensor-memory columns allocated (set by the launcher)
+};
+size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed);
+int gemm_tc_stages(int G, int Np, bool compressed);
+int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits);
+uw_status launch_gemm_tc(const TcParams &p, int G, bool compressed, cudaStream_t stream);
+
 uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status, cudaStream_t stream);
 uw_status launch_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h, int64_t n, cudaStream_t stream);
 
