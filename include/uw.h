@@ -87,6 +87,8 @@ typedef struct {
     uint8_t palette[16];     /* exponent value of each symbol                 */
     uint8_t code_len[16];    /* code length of each symbol, 0 = unused        */
     uint64_t off_sm, off_glen, off_tcode, off_tesc, off_code, off_esc;
+    uint64_t max_tile_bytes; /* largest code region + escaped exponents of one
+                                tile (sizes the kernels' on-chip tile buffers) */
 } uw_desc;
 
 /* One tuned choice for (matrix, batch). */

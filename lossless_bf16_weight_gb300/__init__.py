@@ -38,6 +38,7 @@ class Desc(ctypes.Structure):
         ("palette", ctypes.c_uint8 * 16), ("code_len", ctypes.c_uint8 * 16),
         ("off_sm", ctypes.c_uint64), ("off_glen", ctypes.c_uint64), ("off_tcode", ctypes.c_uint64),
         ("off_tesc", ctypes.c_uint64), ("off_code", ctypes.c_uint64), ("off_esc", ctypes.c_uint64),
+        ("max_tile_bytes", ctypes.c_uint64),
     ]
 
 

@@ -62,7 +62,7 @@ int sm_count() {
     return n;
 }
 
-GemvVariant gemv_variant(int v, int64_t rows, int64_t cols) {
+GemvVariant gemv_variant(int v, int64_t rows, int64_t cols, uint32_t tbuf = kWorstTileBuf) {
     const int64_t gpr = cols / kGroup;
     if (v < kRowVariants)
         return {Kind::kRow, kWarpChoices[v % 3], 1 << (v / 3), 0};
@@ -75,14 +75,12 @@ GemvVariant gemv_variant(int v, int64_t rows, int64_t cols) {
     const int w = kWarpChoices[i % 3];
     const int waves = 1 + i / 3;
     const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
-    const int64_t splits = (gpr + w - 1) / w;
-    const int64_t slots = int64_t(sm_count()) * col_blocks_per_sm(w) * waves;  // CTAs per wave x waves
-    int64_t rb = (nrb * splits + slots - 1) / slots;
-    rb = rb < 2 ? 2 : (rb + 1) / 2 * 2;  // tiles go in pairs
-    // keep the CTAs of one SM within its shared memory
-    while (rb > 2 && gemv_kg_smem_bytes(w, int(rb), true) * col_blocks_per_sm(w) > size_t(kSmemPerSm))
-        rb -= 2;
-    return {Kind::kColumn, w, int(splits), int(rb)};
+    const int64_t slots = int64_t(sm_count()) * waves;  // one CTA per SM per wave
+    int64_t rb = (nrb + slots - 1) / slots;
+    // keep the CTA within one SM's shared memory
+    while (rb > 1 && gemv_kg_smem_bytes(w, int(rb), true, tbuf - kTileSlack, int(gpr)) > size_t(kMaxSmemPerBlock) - 1024)
+        rb--;
+    return {Kind::kColumn, w, 1, int(rb)};
 }
 
 // Tensor-core default: four producer groups while their stages fit, and the
@@ -90,7 +88,7 @@ GemvVariant gemv_variant(int v, int64_t rows, int64_t cols) {
 // splits).
 int default_tc_variant(int64_t rows, int64_t cols, int64_t batch) {
     const int64_t np = std::min<int64_t>((batch + 15) / 16 * 16, kTcMaxBatch);
-    const int gi = gemm_tc_stages(4, int(np), true) >= 4 ? 1 : 0;
+    const int gi = gemm_tc_stages(4, int(np), true, kWorstTileBuf) >= 4 ? 1 : 0;
     const int64_t mblocks = (rows + 127) / 128, gpr = cols / kGroup, sms = sm_count();
     int best = 0;
     double best_eff = -1.0;
@@ -126,7 +124,7 @@ int default_gemv_variant(int64_t rows, int64_t cols, int64_t batch) {
     while (si + 1 < kSplitChoices && nrb * (int64_t(1) << si) < 2 * 152 &&
            gpr / (int64_t(1) << (si + 1)) >= 8)
         si++;
-    while (si + 1 < kSplitChoices && gemv_smem_bytes(cols, 8, 1 << si, bp, true) > size_t(kMaxSmemPerBlock))
+    while (si + 1 < kSplitChoices && gemv_smem_bytes(cols, 8, 1 << si, bp, true, kWorstTileBuf) > size_t(kMaxSmemPerBlock))
         si++;
     return 1 + 3 * si;
 }
@@ -175,7 +173,7 @@ uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t 
 // the column kernels take batch 1 only; the tensor-core kernels take any
 // batch (chunks of 256 inside the launcher).
 uw_status run_gemv(GemvParams p, int variant, bool compressed, cudaStream_t stream) {
-    const GemvVariant gv = gemv_variant(variant, p.rows, p.cols);
+    const GemvVariant gv = gemv_variant(variant, p.rows, p.cols, compressed ? p.v.tbuf : kWorstTileBuf);
     if (gv.kind == Kind::kTensor) {
         TcParams t{};
         t.v = p.v;
@@ -256,6 +254,11 @@ void canonical_code_values(const uint8_t len[16], uint16_t code[16]) {
         code[s] = (len[s] && len[s] <= kLmax) ? uint16_t(next[len[s]]++) : 0;
 }
 
+uint32_t tile_data_bytes(const uw_desc &d) {
+    const uint64_t t = (std::max<uint64_t>(d.max_tile_bytes, 16) + 15) / 16 * 16;
+    return uint32_t(std::min<uint64_t>(t, kMaxTileData));
+}
+
 void fill_blob_view(const uw_desc &d, const void *blob_dev, BlobView *v) {
     const uint8_t *b = static_cast<const uint8_t *>(blob_dev);
     v->sm = b + d.off_sm;
@@ -268,6 +271,12 @@ void fill_blob_view(const uw_desc &d, const void *blob_dev, BlobView *v) {
     v->n_escaped = d.n_escaped;
     v->code16 = uint32_t((d.off_esc - d.off_code) / 16 > 0xFFFFFFFFull ? 0xFFFFFFFFull : (d.off_esc - d.off_code) / 16);
     v->n_esc32 = uint32_t(d.n_escaped);
+    v->gpr = uint32_t(d.cols / kGroup);
+    v->nfull = uint32_t(d.rows / kTileRows);
+    v->tail_rows = uint32_t(d.rows % kTileRows);
+    v->ntiles = uint32_t(std::min<uint64_t>(d.n_tiles, 0xFFFFFFFFull));
+    v->tdata = tile_data_bytes(d);
+    v->tbuf = v->tdata + kTileSlack;
     v->rows = d.rows;
     v->cols = d.cols;
     uint16_t code[16];
@@ -367,7 +376,7 @@ extern "C" uw_status uw_blob_info(const void *blob_host, size_t bytes, uw_desc *
     if (tcode[0] != 0 || tesc[0] != 0 || tesc[ntiles] != d.n_escaped ||
         uint64_t(tcode[ntiles]) * 16 > d.off_esc - d.off_code)
         return UW_ERR_CORRUPT;
-    uint64_t bits_hint = 0;
+    uint64_t bits_hint = 0, max_tile = 0;
     for (uint64_t t = 0; t < ntiles; t++) {
         const uint64_t rb = t / gpr, kg = t % gpr;
         const uint64_t R = std::min<uint64_t>(kTileRows, rows - rb * kTileRows);
@@ -384,7 +393,9 @@ extern "C" uw_status uw_blob_info(const void *blob_host, size_t bytes, uw_desc *
             tesc[t + 1] < tesc[t] || tesc[t + 1] - tesc[t] != nz)
             return UW_ERR_CORRUPT;
         bits_hint += sum;
+        max_tile = std::max<uint64_t>(max_tile, 16 * uint64_t(tcode[t + 1] - tcode[t]) + 64 * nz);
     }
+    d.max_tile_bytes = max_tile;
     if (d.code_bits > 8 * bits_hint || d.code_bits + 8 * (d.n_groups - d.n_escaped) < 8 * bits_hint)
         return UW_ERR_CORRUPT;
     *out = d;

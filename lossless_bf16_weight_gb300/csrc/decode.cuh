@@ -1,30 +1,32 @@
-// Device-side tile decoder shared by the decompress and fused matmul kernels.
+// Device-side tile decoder shared by the decompress and matmul kernels.
 //
 // One warp decodes one tile (32 rows x 64 columns): lane j owns the 64-weight
 // group of row j (Unweight blog, paragraph on rows of 64).  Per tile:
-//   * the tile's code bytes are copied with cp.async straight into one of
-//     the warp's two shared-memory code buffers while the previous tile is
-//     being decoded, and its sign+mantissa bytes are loaded into registers;
+//   * the tile's code bytes (and the raw exponents of its escaped groups)
+//     are copied with cp.async into one of the warp's shared-memory tile
+//     buffers while the previous tile is being decoded, and its
+//     sign+mantissa bytes are loaded into registers;
 //   * the group byte lengths (glen) give each lane its code offset by an
 //     exclusive warp prefix sum (shuffles); ballot + popc give each escaped
 //     group its rank among the tile's escaped groups;
 //   * read as little-endian 32-bit words, stream bit i is bit i%32 of word
 //     i/32, so a funnel shift right brings the next bits to the bottom;
-//   * every step looks up a 12-bit window (first stream bit = bit 0) in a
-//     4096-entry table that decodes two codes at once (codes are at most 6
-//     bits).  An entry holds both exponents already in BF16 position (bits
-//     14..7 and 30..23) and the bits the two codes take (bits 3..0);
+//   * every step looks up a 12-bit window in a 4096-entry table that decodes
+//     two codes at once (codes are at most 6 bits).  An entry holds both
+//     exponents already in BF16 position (bits 14..7 and 30..23) and the bits
+//     the two codes take (bits 3..0).  The funnel shift starts two bits early
+//     so that the window arrives multiplied by 4, i.e. as the entry's byte
+//     offset;
 //   * the exponent pair is merged with two raw sign+mantissa bytes by one
 //     byte permute (sign-replicating) and one three-input logic op, giving
 //     two BF16 weights in one 32-bit register (the blog's reconstruction:
 //     exponent + sign/mantissa bytes -> BF16, paragraph on the consumer
 //     warps of the reconstructive matmul).
-// Escaped groups (rare) and lanes without a row run the same loop on a
-// fixed stream of 12-bit numbers 0..31 through a 32-entry table of zero
-// exponents, so the hot loop has no branch on the group kind; the escaped
-// groups are then redone in a short second pass from their raw exponent
-// bytes.  Every lane's sum is independent of the other lanes', so the
-// second pass gives exactly what a single pass would.
+// Escaped groups (rare) and lanes without a row run the same loop over a
+// block of zero bytes, so the hot loop has no branch on the group kind; the
+// escaped groups are then redone in a short second pass from their raw
+// exponent bytes.  Every lane's sum is independent of the other lanes', so
+// the second pass gives exactly what a single pass would.
 #pragma once
 #include <cuda_runtime.h>
 
@@ -54,6 +56,12 @@ struct BlobView {
     uint64_t n_escaped;
     uint32_t code16;      // code section size in 16-byte units (fits: tile offsets are u32)
     uint32_t n_esc32;     // escaped groups (fits: escape offsets are u32)
+    uint32_t tdata;       // tile buffer capacity: the blob's largest tile, a multiple of 16
+    uint32_t tbuf;        // tile buffer stride: tdata + kTileSlack
+    uint32_t gpr;         // 64-column groups per row (32-bit kernels: tiles < 2^32)
+    uint32_t nfull;       // full 32-row blocks
+    uint32_t tail_rows;   // rows of the last, partial block (0: none)
+    uint32_t ntiles;      // tiles (the tile tables hold ntiles + 1 entries)
     int64_t rows, cols;
     // 6-bit prefix -> (exponent << 4) | code length; 0 where no code starts
     // with that prefix.
@@ -61,49 +69,39 @@ struct BlobView {
 };
 
 constexpr int kLutEntries = 4096;
-constexpr int kFakeWords = 16;                             // stream of 12-bit values 0..31 (+slack)
+constexpr int kZeroWords = 32;                             // zero stream for lanes without codes
 // One tile's shared buffer: its code region, then the raw exponent bytes of
-// its escaped groups ((32 - e) * 48 + 64 * e <= 2048 bytes), then read slack.
-constexpr int kTileBufData = 2048;
-constexpr int kCodeBufBytes = kTileBufData + 64;
-constexpr int kWarpBufBytes = 2 * kCodeBufBytes;           // two buffers: decode one, fill the other
-constexpr int kCommonSmemBytes = kLutEntries * 4 + kFakeWords * 4 + 32 * 4 + 64 * 2;
+// its escaped groups ((32 - e) * 48 + 64 * e <= 2048 bytes), then read
+// slack.  Buffers are sized for the largest tile of the blob at hand.
+constexpr uint32_t kMaxTileData = 2048;
+constexpr uint32_t kTileSlack = 64;
+constexpr int kCommonSmemBytes = kLutEntries * 4 + kZeroWords * 4 + 64 * 2;
 
-// Shared memory common to every decoding CTA.
+// Shared memory common to every decoding CTA.  The tile buffers must come
+// after it: a lane whose codes start on a word boundary begins reading one
+// word before its buffer.
 struct DecodeShared {
     uint32_t *lut;       // [4096] pair table
-    uint32_t *fake;      // [16]   stream 0, 1, ..., 31 in 12-bit fields
-    uint32_t *zeros;     // [32]   entries with no exponent, 12 bits each
+    uint32_t *zero;      // [32]   zero bytes: the stream of lanes without codes
     uint16_t *prefix6;   // [64]
 };
 
 __device__ __forceinline__ DecodeShared carve_common(unsigned char *smem) {
     DecodeShared s;
     s.lut = reinterpret_cast<uint32_t *>(smem);
-    s.fake = s.lut + kLutEntries;
-    s.zeros = s.fake + kFakeWords;
-    s.prefix6 = reinterpret_cast<uint16_t *>(s.zeros + 32);
+    s.zero = s.lut + kLutEntries;
+    s.prefix6 = reinterpret_cast<uint16_t *>(s.zero + kZeroWords);
     return s;
 }
 
-// Fill the pair table and the fixed streams.  Must be followed by
+// Fill the pair table and the zero stream.  Must be followed by
 // __syncthreads() before use.
 __device__ __forceinline__ void build_tables(const DecodeShared &s, const BlobView &v) {
     const int tid = threadIdx.x, nt = blockDim.x;
     for (int i = tid; i < 64; i += nt)
         s.prefix6[i] = v.prefix6[i];
-    for (int i = tid; i < 32; i += nt)
-        s.zeros[i] = 12u;
-    for (int wi = tid; wi < kFakeWords; wi += nt) {
-        uint32_t word = 0;
-        for (int b = 0; b < 32; b++) {
-            const int p = wi * 32 + b;              // bit position in the stream
-            const int val = p / 12;                 // 12-bit field holding it
-            const uint32_t bit = val < 32 ? (uint32_t(val) >> (p % 12)) & 1u : 0u;
-            word |= bit << b;
-        }
-        s.fake[wi] = word;
-    }
+    for (int i = tid; i < kZeroWords; i += nt)
+        s.zero[i] = 0u;
     __syncthreads();
     // Window w holds stream bits in order from bit 0; codes enter the stream
     // most significant bit first, so the code-order window is w reversed.
@@ -155,18 +153,43 @@ __device__ __forceinline__ TileLoc tile_loc(const BlobView &v, int64_t rb, int64
     return L;
 }
 
+// The same with 32-bit indices, t = rb * gpr + kg.  A partial last block
+// holds R < 32 rows, so its tiles start (32 - R) * kg groups before 32 * t.
+__device__ __forceinline__ TileLoc tile_loc32(const BlobView &v, uint32_t rb, uint32_t kg, uint32_t t) {
+    TileLoc L;
+    const bool full = rb < v.nfull;
+    L.R = full ? kTileRows : int(v.tail_rows);
+    const uint32_t short_by = full ? 0u : (kTileRows - v.tail_rows) * kg;
+    L.sm = v.sm + uint64_t(t) * (kTileRows * kGroup) - uint64_t(short_by) * kGroup;
+    L.glen = v.glen + uint64_t(t) * kTileRows - short_by;
+    return L;
+}
+
+__device__ __forceinline__ int tile_rows32(const BlobView &v, uint32_t rb) {
+    return rb < v.nfull ? kTileRows : int(v.tail_rows);
+}
+
 __device__ __forceinline__ int tile_rows(const BlobView &v, int64_t rb) {
     const int64_t left = v.rows - rb * kTileRows;
     return left < kTileRows ? int(left) : kTileRows;
 }
 
-// A tile's bookkeeping as fetched: the lane's glen, and warp-uniform
-// values: first escaped group, and n16 | nesc << 8 | bad << 16.
+// A tile's bookkeeping as fetched: the lane's glen (any value for lanes
+// without a row), and warp-uniform values: first escaped group, and
+// n16 | nesc << 8 | bad << 16.  The loads are consumed only by tile_begin,
+// so fetching never waits for them.
 struct TileMeta {
     uint32_t glen;
     uint32_t esc0;
     uint32_t pk;
 };
+
+// Load the offsets of tile t into lanes 0..3 (32-bit tile index).
+__device__ __forceinline__ uint32_t tile_offsets_load32(const BlobView &v, uint32_t t) {
+    const int lane = threadIdx.x & 31, l = lane & 3;
+    const uint32_t *src = (l < 2 ? v.tcode + l : v.tesc + (l - 2)) + t;
+    return lane < 4 ? __ldg(src) : 0u;
+}
 
 // Load the offsets of tile t = rb * (cols/64) + kg into lanes 0..3
 // (tcode[t], tcode[t+1], tesc[t], tesc[t+1]); issued ahead of the data.
@@ -198,23 +221,37 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
 }
 
 // The lane's 64 sign+mantissa bytes: chunk c of row j sits at (c*R + j)*16
-// inside the tile (zeros for lanes without a row).
+// inside the tile.  Lanes without a row read row 0's bytes (their results
+// are never used).
 __device__ __forceinline__ void tile_sm_load(const TileLoc &L, uint4 (&sm)[4]) {
     const int lane = threadIdx.x & 31;
-    const uint8_t *smb = L.sm + 16 * lane;
+    const uint8_t *smb = L.sm + 16 * (lane < L.R ? lane : 0);
     const int stride = 16 * L.R;
 #pragma unroll
     for (int c = 0; c < 4; c++)
-        sm[c] = lane < L.R ? __ldg(reinterpret_cast<const uint4 *>(smb + c * stride)) : make_uint4(0, 0, 0, 0);
+        sm[c] = __ldg(reinterpret_cast<const uint4 *>(smb + c * stride));
 }
 
-// Fetch a tile: validate its offsets (`offs` from tile_offsets_load), load
-// the lane's glen and 64 sign+mantissa bytes into registers, and start
-// copying its code region followed by its escaped groups' raw exponents
-// into the tile buffer at shared address `cbuf` (cp.async, one commit
-// group).
-__device__ __forceinline__ void tile_fetch(const BlobView &v, const TileLoc &L, uint32_t offs, uint32_t cbuf,
-                                           TileMeta &m, uint4 (&sm)[4]) {
+// Ask L2 to bring in a tile's sign+mantissa bytes (one lane issues it).
+__device__ __forceinline__ void tile_prefetch_sm_l2(const TileLoc &L) {
+    if ((threadIdx.x & 31) == 0 && L.R > 0)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(L.sm), "r"(uint32_t(64 * L.R)) : "memory");
+}
+
+// Load chunks c0, c0+1 of the lane's sign+mantissa bytes (see tile_sm_load).
+__device__ __forceinline__ void tile_sm_load_half(const TileLoc &L, int c0, uint4 &a, uint4 &b) {
+    const int lane = threadIdx.x & 31;
+    const uint8_t *smb = L.sm + 16 * (lane < L.R ? lane : 0) + c0 * 16 * L.R;
+    a = __ldg(reinterpret_cast<const uint4 *>(smb));
+    b = __ldg(reinterpret_cast<const uint4 *>(smb + 16 * L.R));
+}
+
+// Fetch a tile's codes: validate its offsets (`offs` from
+// tile_offsets_load), load the lane's glen, and start copying its code
+// region followed by its escaped groups' raw exponents into the tile buffer
+// at shared address `cbuf` (cp.async, one commit group).
+__device__ __forceinline__ void tile_fetch_codes(const BlobView &v, const TileLoc &L, uint32_t offs, uint32_t cbuf,
+                                                 TileMeta &m) {
     const int lane = threadIdx.x & 31;
     const uint32_t c0 = __shfl_sync(0xffffffffu, offs, 0);
     const uint32_t c1 = __shfl_sync(0xffffffffu, offs, 1);
@@ -222,11 +259,10 @@ __device__ __forceinline__ void tile_fetch(const BlobView &v, const TileLoc &L, 
     const uint32_t e1 = __shfl_sync(0xffffffffu, offs, 3);
     const uint32_t n16 = c1 - c0, nesc = e1 - e0;
     const bool bad = c1 < c0 || n16 > uint32_t(kMaxTileCodeBytes / 16) || c1 > v.code16 || e1 < e0 ||
-                     nesc > uint32_t(L.R) || e1 > v.n_esc32 || n16 * 16u + nesc * 64u > uint32_t(kTileBufData);
+                     nesc > uint32_t(L.R) || e1 > v.n_esc32 || n16 * 16u + nesc * 64u > v.tdata;
     m.pk = bad ? (1u << 16) : (n16 | (nesc << 8));
     m.esc0 = e0;
-    m.glen = lane < L.R ? __ldg(L.glen + lane) : 0u;
-    tile_sm_load(L, sm);
+    m.glen = __ldg(L.glen + (lane < L.R ? lane : 0));  // lanes without a row: ignored by tile_begin
     if (!bad) {
         const uint8_t *src = v.code + size_t(c0) * 16 + 16 * lane;
         const uint32_t dst = cbuf + 16u * lane;
@@ -246,27 +282,35 @@ __device__ __forceinline__ void tile_fetch(const BlobView &v, const TileLoc &L, 
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
+// tile_fetch_codes, plus the lane's 64 sign+mantissa bytes into registers.
+__device__ __forceinline__ void tile_fetch(const BlobView &v, const TileLoc &L, uint32_t offs, uint32_t cbuf,
+                                           TileMeta &m, uint4 (&sm)[4]) {
+    tile_fetch_codes(v, L, offs, cbuf, m);
+    tile_sm_load(L, sm);
+}
+
 // Per-tile, per-lane decode state.  Addresses are 32-bit shared addresses.
+// With P the shared-memory bit address of the next code bit and lo the word
+// at byte address A, the low five bits of c are P - 8A - 2: the funnel shift
+// by c puts the next 12 stream bits at bits 2..13.  c only grows; bit 5
+// flips whenever the window moves past a word.
 struct LaneStream {
     uint32_t lo, hi, nx;   // current, next and (already loaded) following stream word
-    uint32_t c;            // bit position in lo (low 5 bits); low 7 bits exact
+    uint32_t c;            // see above; low 7 bits exact
     uint32_t wp;           // address of the next word to load
-    uint32_t lut;          // pair table of this lane (codes) or the zero table
-    uint32_t base;         // 8 * (first wp) + start bit: bits used = 8 * wp + (c & 31) - base
-    uint32_t glen;         // bytes the lane must use (48 for lanes on the fixed stream)
+    uint32_t expect;       // 8 * wp + (c & 31) after the lane's last code, + 0..7; 0: unchecked
 };
 
 // Wait for the tile's codes, validate, and set up every lane's stream.
 // Returns the mask of lanes whose group is escaped (0 for a bad tile, whose
-// lanes all decode zeros; the error is recorded in *status).
-__device__ __forceinline__ uint32_t tile_begin(const DecodeShared &s, const TileMeta &m, int R, uint32_t cbuf,
-                                               LaneStream &ls, uint32_t *status) {
+// lanes all decode the zero stream; the error is recorded in *status).
+// tile_begin for data already in shared memory (nothing to wait for).
+__device__ __forceinline__ uint32_t tile_begin_ready(const DecodeShared &s, const TileMeta &m, int R, uint32_t cbuf,
+                                                     LaneStream &ls, uint32_t *status) {
     const int lane = threadIdx.x & 31;
     const bool valid = lane < R;
     const uint32_t n16 = m.pk & 0xFFu, nesc = (m.pk >> 8) & 0xFFu;
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncwarp();
-    const uint32_t g = m.glen;
+    const uint32_t g = valid ? m.glen : 0u;
     uint32_t incl = g;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -281,25 +325,25 @@ __device__ __forceinline__ uint32_t tile_begin(const DecodeShared &s, const Tile
     const bool bad = over || uint32_t(__popc(esc_mask)) != nesc;
     if (bad && lane == 0)
         atomicOr(status, over ? kStatusBadTile : kStatusBadEscape);
-    uint32_t w0, c0;
-    if (!bad && valid && g != 0) {
-        w0 = cbuf + (off & ~3u);
-        c0 = 8u * (off & 3u);
-        ls.lut = smem_addr(s.lut);
-        ls.glen = g;
-    } else {
-        w0 = smem_addr(s.fake);
-        c0 = 0;
-        ls.lut = smem_addr(s.zeros);
-        ls.glen = 48;  // the fixed stream is 32 fields of 12 bits
-    }
+    const bool coded = !bad && g != 0;
+    // a stream starting on a word boundary begins one word early (c = 30)
+    const uint32_t sub = (off & 3u) ? 0u : 4u;
+    const uint32_t w0 = coded ? cbuf + (off & ~3u) - sub : smem_addr(s.zero);
+    const uint32_t c0 = (8u * (off & 3u) - 2u) & 31u;
     ls.lo = lds32(w0);
     ls.hi = lds32(w0 + 4);
     ls.nx = lds32(w0 + 8);
     ls.wp = w0 + 12;
     ls.c = c0;
-    ls.base = 8u * ls.wp + c0;
+    ls.expect = coded ? 8u * ls.wp + c0 + 8u * g : 0u;
     return bad ? 0u : esc_mask;
+}
+
+__device__ __forceinline__ uint32_t tile_begin(const DecodeShared &s, const TileMeta &m, int R, uint32_t cbuf,
+                                               LaneStream &ls, uint32_t *status) {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
+    return tile_begin_ready(s, m, R, cbuf, ls, status);
 }
 
 // Shared address of a fetched tile's raw escape bytes (after its codes).
@@ -320,10 +364,11 @@ __device__ __forceinline__ void escape_read(uint32_t ebase, uint32_t esc_mask, u
 }
 
 // One step: decode the exponents of weights 2i, 2i+1 and merge them with the
-// sign+mantissa bytes.  `sm4` holds the bytes of weights 4*(i/2)..+3.
-// `I` is a compile-time constant once the caller's 32-step loop is unrolled.
-__device__ __forceinline__ uint32_t decode_pair(LaneStream &ls, int I, uint32_t sm4) {
-    // window = next 32 stream bits (funnel right); entry = table[window & 4095];
+// sign+mantissa bytes.  `sm4` holds the bytes of weights 4*(i/2)..+3; `lut`
+// is the shared address of the pair table.  `I` is a compile-time constant
+// once the caller's 32-step loop is unrolled.
+__device__ __forceinline__ uint32_t decode_pair(LaneStream &ls, uint32_t lut, int I, uint32_t sm4) {
+    // window*4 = funnel(lo, hi) >> c, bits 2..13; entry = table[window];
     // c += entry (its bits above 6 only add junk above the exact low 7);
     // when bit 5 of c flips the window has moved into the next word: shift
     // the words and load the one after, predicated rather than branched.  The
@@ -335,21 +380,21 @@ __device__ __forceinline__ uint32_t decode_pair(LaneStream &ls, int I, uint32_t 
         ".reg .b32 win, addr, c2, t;\n\t"
         ".reg .pred p;\n\t"
         "shf.r.wrap.b32 win, %1, %2, %4;\n\t"
-        "and.b32 win, win, 4095;\n\t"
-        "mad.lo.u32 addr, win, 4, %6;\n\t"     // integer multiply-add: FMA pipe, not ALU
+        "and.b32 win, win, 16380;\n\t"
+        "add.u32 addr, win, %6;\n\t"
         "ld.shared.u32 %0, [addr];\n\t"
-        "mad.lo.u32 c2, %0, 1, %4;\n\t"
+        "add.u32 c2, %0, %4;\n\t"
         "xor.b32 t, c2, %4;\n\t"
         "and.b32 t, t, 32;\n\t"
         "setp.ne.u32 p, t, 0;\n\t"
         "@p mov.b32 %1, %2;\n\t"
         "@p mov.b32 %2, %3;\n\t"
         "@p ld.shared.u32 %3, [%5];\n\t"
-        "@p mad.lo.u32 %5, 1, 4, %5;\n\t"
+        "@p add.u32 %5, %5, 4;\n\t"
         "mov.b32 %4, c2;\n\t"
         "}"
         : "=r"(ent), "+r"(ls.lo), "+r"(ls.hi), "+r"(ls.nx), "+r"(ls.c), "+r"(ls.wp)
-        : "r"(ls.lut)
+        : "r"(lut)
         : "memory");
     // sign-replicate byte permute: bytes (b0, sign(b0), b1, sign(b1)) for the
     // even pair of the word, (b2, sign(b2), b3, sign(b3)) for the odd one
@@ -357,10 +402,23 @@ __device__ __forceinline__ uint32_t decode_pair(LaneStream &ls, int I, uint32_t 
     return lop3_merge(y, ent);
 }
 
-// After the 32 steps: every lane must have used exactly its byte length.
+// After the 32 steps: every lane with codes must have used its byte length
+// exactly (its last code ends in the length's final byte).
 __device__ __forceinline__ void tile_check(const LaneStream &ls, uint32_t *status) {
-    const uint32_t used = 8u * ls.wp + (ls.c & 31u) - ls.base;
-    if (((used + 7u) >> 3) != ls.glen)
+    const uint32_t pos = 8u * ls.wp + (ls.c & 31u);
+    if (ls.expect != 0u && ls.expect - pos >= 8u)
+        atomicOr(status, uint32_t(kStatusBadCode));
+}
+
+// The same check folded into a per-lane flag (nonzero: some group was bad);
+// report it once with tile_check_flush.
+__device__ __forceinline__ uint32_t tile_check_bits(const LaneStream &ls) {
+    const uint32_t pos = 8u * ls.wp + (ls.c & 31u);
+    return (ls.expect != 0u) & (ls.expect - pos >= 8u);
+}
+
+__device__ __forceinline__ void tile_check_flush(uint32_t bad, uint32_t *status) {
+    if (__any_sync(0xffffffffu, bad != 0u) && (threadIdx.x & 31) == 0)
         atomicOr(status, uint32_t(kStatusBadCode));
 }
 

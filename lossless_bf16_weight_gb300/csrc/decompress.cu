@@ -22,8 +22,10 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
     extern __shared__ __align__(16) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const DecodeShared ds = carve_common(smem);
-    uint32_t *wbuf = reinterpret_cast<uint32_t *>(smem + kCommonSmemBytes + size_t(warp) * kWarpBufBytes);
-    uint4 *obuf = reinterpret_cast<uint4 *>(smem + kCommonSmemBytes + size_t(kDecompWarps) * kWarpBufBytes +
+    const uint32_t lut = smem_addr(ds.lut);
+    const uint32_t tbuf = v.tbuf;
+    uint32_t *wbuf = reinterpret_cast<uint32_t *>(smem + kCommonSmemBytes + size_t(warp) * 2 * tbuf);
+    uint4 *obuf = reinterpret_cast<uint4 *>(smem + kCommonSmemBytes + size_t(kDecompWarps) * 2 * tbuf +
                                             size_t(warp) * kOutBufBytes);
 
     const int64_t gpr = v.cols / kGroup;
@@ -52,7 +54,7 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
             kg = 0;
             rb++;
         }
-        const uint32_t cbuf = cbuf0 + uint32_t((t - t_lo) & 1) * kCodeBufBytes;
+        const uint32_t cbuf = cbuf0 + uint32_t((t - t_lo) & 1) * tbuf;
         uint4 sm[4];
 #pragma unroll
         for (int c = 0; c < 4; c++)
@@ -61,7 +63,7 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
         const uint32_t esc_mask = tile_begin(ds, meta, R, cbuf, ls, status);
         const uint32_t ebase = escape_base(meta, cbuf);
         if (t + 1 < t_hi) {
-            tile_fetch(v, tile_loc(v, rb, kg, gpr), offs_next, cbuf0 + uint32_t((t + 1 - t_lo) & 1) * kCodeBufBytes,
+            tile_fetch(v, tile_loc(v, rb, kg, gpr), offs_next, cbuf0 + uint32_t((t + 1 - t_lo) & 1) * tbuf,
                        meta, smn);
             if (t + 2 < t_hi)
                 offs_next = tile_offsets_load(v, t + 2);
@@ -69,7 +71,7 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
         uint32_t q[4];
 #pragma unroll
         for (int I = 0; I < 32; I++) {
-            q[I & 3] = decode_pair(ls, I, sm_word(sm, I >> 1));
+            q[I & 3] = decode_pair(ls, lut, I, sm_word(sm, I >> 1));
             if ((I & 3) == 3) {
                 const int c = I >> 2;  // 16-byte chunk of the row segment
                 obuf[lane * 8 + (c ^ (lane & 7))] = make_uint4(q[0], q[1], q[2], q[3]);
@@ -114,7 +116,7 @@ uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status
     const int64_t ntiles = (v.rows + kTileRows - 1) / kTileRows * gpr;
     const int64_t per_cta = int64_t(kDecompWarps) * kTilesPerWarp;
     const int64_t grid = (ntiles + per_cta - 1) / per_cta;
-    const size_t smem = size_t(kCommonSmemBytes) + size_t(kDecompWarps) * (kWarpBufBytes + kOutBufBytes);
+    const size_t smem = size_t(kCommonSmemBytes) + size_t(kDecompWarps) * (2 * size_t(v.tbuf) + kOutBufBytes);
     if (!ensure_smem(decompress_kernel, smem))
         return UW_ERR_CUDA;
     decompress_kernel<<<dim3(unsigned(grid)), dim3(kDecompWarps * 32), smem, stream>>>(v, w_out, status);

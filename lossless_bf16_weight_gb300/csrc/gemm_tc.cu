@@ -107,7 +107,7 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
     uint32_t offs_next = 0;
     if (kCompressed) {
         ds = carve_common(dec);
-        cbuf0 = smem_addr(dec + kCommonSmemBytes + size_t(warp) * kWarpBufBytes);
+        cbuf0 = smem_addr(dec + kCommonSmemBytes + size_t(warp) * 2 * p.v.tbuf);
         if (rb_ok && grp < nk) {
             tile_fetch(p.v, tile_loc(p.v, rb, kg_lo + grp, gpr), tile_offsets_load(p.v, rb * gpr + kg_lo + grp),
                        cbuf0, meta, smn);
@@ -120,6 +120,7 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
+    const uint32_t lut = kCompressed ? smem_addr(ds.lut) : 0u;
 
     if (producer) {
         const int64_t left = p.rows - rb * kTileRows;  // rows of this row block (p.v is unset for bf16)
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
             if (kCompressed) {
                 uint32_t q[32];
                 if (rb_ok) {
-                    const uint32_t cbuf = cbuf0 + uint32_t(it & 1) * kCodeBufBytes;
+                    const uint32_t cbuf = cbuf0 + uint32_t(it & 1) * p.v.tbuf;
                     uint4 sm[4];
 #pragma unroll
                     for (int c = 0; c < 4; c++)
@@ -144,13 +145,13 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
                     const uint32_t eb = escape_base(meta, cbuf);
                     if (i + G < nk) {
                         tile_fetch(p.v, tile_loc(p.v, rb, kg + G, gpr), offs_next,
-                                   cbuf0 + uint32_t((it + 1) & 1) * kCodeBufBytes, meta, smn);
+                                   cbuf0 + uint32_t((it + 1) & 1) * p.v.tbuf, meta, smn);
                         if (i + 2 * G < nk)
                             offs_next = tile_offsets_load(p.v, rb * gpr + kg + 2 * G);
                     }
 #pragma unroll
                     for (int I = 0; I < 32; I++)
-                        q[I] = decode_pair(ls, I, sm_word(sm, I >> 1));
+                        q[I] = decode_pair(ls, lut, I, sm_word(sm, I >> 1));
                     tile_check(ls, p.status);
                     if ((em >> lane) & 1u) {  // escaped group: rebuild from its raw exponents
                         uint4 e[4];
@@ -271,16 +272,16 @@ uw_status launch_tc_one(const TcParams &p, size_t smem, cudaStream_t stream) {
 
 }  // namespace
 
-size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed) {
+size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed, uint32_t tbuf) {
     size_t s = 1024 + size_t(S) * (kAStageBytes + size_t(Np) * 128);
     if (compressed)
-        s += size_t(kCommonSmemBytes) + size_t(4 * G) * kWarpBufBytes;
+        s += size_t(kCommonSmemBytes) + size_t(4 * G) * 2 * tbuf;
     return s;
 }
 
-int gemm_tc_stages(int G, int Np, bool compressed) {
+int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tbuf) {
     int S = kTcMaxStages;
-    while (S > 1 && gemm_tc_smem_bytes(G, S, Np, compressed) > size_t(kMaxSmemPerBlock - 1024))
+    while (S > 1 && gemm_tc_smem_bytes(G, S, Np, compressed, tbuf) > size_t(kMaxSmemPerBlock - 1024))
         S--;
     return S;
 }
@@ -305,10 +306,10 @@ uw_status launch_gemm_tc(const TcParams &base, int G, bool compressed, cudaStrea
         p.tmem_cols = 32;
         while (p.tmem_cols < uint32_t(p.Np))
             p.tmem_cols <<= 1;
-        p.S = gemm_tc_stages(G, p.Np, compressed);
+        p.S = gemm_tc_stages(G, p.Np, compressed, p.v.tbuf);
         if (p.S < G)
             return UW_ERR_UNSUPPORTED;
-        const size_t smem = gemm_tc_smem_bytes(G, p.S, p.Np, compressed);
+        const size_t smem = gemm_tc_smem_bytes(G, p.S, p.Np, compressed, p.v.tbuf);
         uw_status s;
         if (G == 2)
             s = compressed ? launch_tc_one<2, true>(p, smem, stream) : launch_tc_one<2, false>(p, smem, stream);

@@ -66,8 +66,8 @@ __device__ __forceinline__ void gemv_body(const GemvParams &p) {
     if (kCompressed) {
         ds = carve_common(smem);
         off = kCommonSmemBytes;
-        wbuf = reinterpret_cast<uint32_t *>(smem + off + size_t(warp) * kWarpBufBytes);
-        off += size_t(W) * kWarpBufBytes;
+        wbuf = reinterpret_cast<uint32_t *>(smem + off + size_t(warp) * 2 * p.v.tbuf);
+        off += size_t(W) * 2 * p.v.tbuf;
     }
     float *xs = reinterpret_cast<float *>(smem + off);
     off += size_t(nk) * kGroup * BP * 4;
@@ -109,6 +109,7 @@ __device__ __forceinline__ void gemv_body(const GemvParams &p) {
         xs[((kk >> 2) * BP + b) * 4 + (kk & 3)] = xv;
     }
     __syncthreads();
+    const uint32_t lut = kCompressed ? smem_addr(ds.lut) : 0u;
 
     float2 acc[BP];
 #pragma unroll
@@ -120,7 +121,7 @@ __device__ __forceinline__ void gemv_body(const GemvParams &p) {
         const float *xk = xs + (kg - kg_lo) * kGroup * BP;
         float4 x4[BP];
         if (kCompressed) {
-            const uint32_t cbuf = cbuf0 + uint32_t((kg - w_lo) & 1) * kCodeBufBytes;
+            const uint32_t cbuf = cbuf0 + uint32_t((kg - w_lo) & 1) * p.v.tbuf;
             uint4 sm[4];
 #pragma unroll
             for (int c = 0; c < 4; c++)
@@ -130,7 +131,7 @@ __device__ __forceinline__ void gemv_body(const GemvParams &p) {
             const uint32_t ebase = escape_base(meta, cbuf);
             if (kg + 1 < w_hi) {
                 tile_fetch(p.v, tile_loc(p.v, rb, kg + 1, gpr), offs_next,
-                           cbuf0 + uint32_t((kg + 1 - w_lo) & 1) * kCodeBufBytes, meta, smn);
+                           cbuf0 + uint32_t((kg + 1 - w_lo) & 1) * p.v.tbuf, meta, smn);
                 if (kg + 2 < w_hi)
                     offs_next = tile_offsets_load(p.v, t + 2);
             }
@@ -140,7 +141,7 @@ __device__ __forceinline__ void gemv_body(const GemvParams &p) {
                 saved[b] = acc[b];
 #pragma unroll
             for (int I = 0; I < 32; I++) {
-                const uint32_t pair = decode_pair(ls, I, sm_word(sm, I >> 1));
+                const uint32_t pair = decode_pair(ls, lut, I, sm_word(sm, I >> 1));
                 fma_pair<BP>(pair, I, xk, x4, acc);
             }
             tile_check(ls, p.status);
@@ -254,17 +255,17 @@ uw_status launch_bp(const GemvParams &p, int bp, size_t smem, cudaStream_t strea
 
 }  // namespace
 
-size_t gemv_smem_bytes(int64_t cols, int warps, int splits, int bp, bool compressed) {
+size_t gemv_smem_bytes(int64_t cols, int warps, int splits, int bp, bool compressed, uint32_t tbuf) {
     const int64_t gpr = cols / kGroup;
     const int64_t nk_max = (gpr + splits - 1) / splits;
-    size_t s = compressed ? size_t(kCommonSmemBytes) + size_t(warps) * kWarpBufBytes : 0;
+    size_t s = compressed ? size_t(kCommonSmemBytes) + size_t(warps) * 2 * tbuf : 0;
     s += size_t(nk_max) * kGroup * bp * 4;
     s += size_t(warps) * bp * 32 * 4;
     return s;
 }
 
 uw_status launch_gemv(const GemvParams &p, int warps, int bp, bool compressed, cudaStream_t stream) {
-    const size_t smem = gemv_smem_bytes(p.cols, warps, p.splits, bp, compressed);
+    const size_t smem = gemv_smem_bytes(p.cols, warps, p.splits, bp, compressed, p.v.tbuf);
     if (smem > size_t(kMaxSmemPerBlock))
         return UW_ERR_UNSUPPORTED;
     if (compressed) {

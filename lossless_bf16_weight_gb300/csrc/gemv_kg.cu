@@ -1,39 +1,42 @@
-// Batch-1 GEMV with the activation vector held in registers ("column" CTAs),
-// y = x W^T, fp32 accumulation.
+// Batch-1 GEMV on "column range" CTAs, y = x W^T, fp32 accumulation.
 //
-// A CTA of W warps covers W consecutive 64-column groups (warp w owns group
-// kg0 + w) of a range of 32-row blocks.  The CTA's x values sit in shared
-// memory as BF16 pairs (one broadcast load per step serves both tiles).
-// Each warp walks down its column two tiles at a time (row blocks rb and
-// rb+1), interleaving the two tiles step by step so that every lane runs two
-// independent dependency chains:
-//   * compressed source: each tile is decoded on chip (decode.cuh) and each
-//     BF16 weight pair is multiplied straight from the register it was
+// A CTA owns `rb_per_cta` consecutive 32-row blocks and every column.  Its W
+// warps split the 64-column groups into W contiguous ranges (warp w: groups
+// k0(w) .. k1(w)-1).  A warp walks its row blocks and, within one, its groups
+// two at a time: a "pair" is the tiles (rb, kg) and (rb, kg+1), which sit
+// next to each other in every section of the blob.
+//   * compressed source: the copy engine brings each pair's glen, code
+//     region, escaped exponents and sign+mantissa bytes into one of the
+//     warp's two shared-memory stages (bulk copies completing on an
+//     mbarrier), one pair ahead of the decode.  The two tiles of a pair are
+//     decoded side by side (two dependency chains per lane, decode.cuh) and
+//     each BF16 weight pair is multiplied straight from the register it was
 //     rebuilt in -- the weights never exist in memory (Unweight blog,
-//     paragraphs on the reconstructive matmul and on decompressing into
-//     fast on-chip memory);
-//   * bf16 source: the same warps load the uncompressed weights.
-// Both share this body, so the results are bit-identical.  Products use the
-// mixed-precision fma.rn.f32.bf16 (BF16 x BF16 is exact in fp32, so each
-// step is one correctly rounded fp32 add of the exact product).
-//
-// Loads run one tile pair ahead: code regions and escaped groups' raw
-// exponents by cp.async into the warp's second pair of shared buffers; glen
-// and the sign+mantissa bytes into registers.
+//     paragraphs on the reconstructive matmul and on decompressing into fast
+//     on-chip memory);
+//   * bf16 source: the same warps load the uncompressed rows.
+// Both compute every tile partial and every sum below in the same order, so
+// the results are bit-identical.  Products use the mixed-precision
+// fma.rn.f32.bf16 (BF16 x BF16 is exact in fp32, so each step is one
+// correctly rounded fp32 add of the exact product).
 //
 // Order of the sum for output n (row j of block rb):
-//   tile partial  = acc_even + acc_odd       (k even / odd within the group)
-//   CTA partial   = ((p(kg0) + p(kg0+1)) + p(kg0+2)) + ...   over its W groups
-//   y             = ((split0 + split1) + split2) + ...       split s = CTA column s
+//   tile partial  p(kg) = acc_even + acc_odd     (k even / odd within the group)
+//   warp partial  s_w   = ((0 + p(k0)) + p(k0+1)) + ...   over the warp's groups
+//   y                   = ((s_0 + s_1) + s_2) + ...        over the warps
 // then round to nearest even BF16.
 #include <cuda_bf16.h>
 
 #include "decode.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace uw {
 
 namespace {
+
+constexpr int kPairStages = 2;
+constexpr int kMaxColWarps = 32;
 
 __device__ __forceinline__ void fma_bf16x2(float &a0, float &a1, uint32_t w, uint32_t x) {
     asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
@@ -45,252 +48,372 @@ __device__ __forceinline__ void fma_bf16x2(float &a0, float &a1, uint32_t w, uin
         : "r"(w), "r"(x));
 }
 
-__device__ __forceinline__ void prefetch_bf16_row(const GemvParams &p, int64_t rb, int64_t kg) {
-    const int lane = threadIdx.x & 31;
-    const int64_t n = rb * kTileRows + lane;
-    if (n < p.rows)
-        asm volatile("prefetch.global.L2 [%0];" :: "l"(p.w + n * p.cols + kg * kGroup));
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
 }
 
-// The two accumulators of an escaped group's lane, rebuilt from its raw
-// exponent bytes (rare; kept out of line so that it costs the hot loop no
-// registers, so the sign+mantissa bytes are loaded again).
-__device__ __noinline__ float2 escaped_tile_sum(uint32_t ebase, uint32_t em, const TileLoc &L, uint32_t xw) {
-    uint4 e[4], sm[4];
-    escape_read(ebase, em, e);
-    tile_sm_load(L, sm);
-    float b0 = 0.f, b1 = 0.f;
-#pragma unroll
-    for (int I = 0; I < 32; I++)
-        fma_bf16x2(b0, b1, escape_pair(e, I, sm_word(sm, I >> 1)), lds32(xw + 4 * I));
-    return make_float2(b0, b1);
+// Group range of warp w out of W over gpr groups.
+__device__ __forceinline__ void warp_cols(uint32_t gpr, int w, int W, uint32_t &k0, uint32_t &k1) {
+    k0 = uint32_t(uint64_t(gpr) * uint32_t(w) / uint32_t(W));
+    k1 = uint32_t(uint64_t(gpr) * uint32_t(w + 1) / uint32_t(W));
 }
 
-template <int W, bool kCompressed>
-__device__ __forceinline__ void gemv_col_body(const GemvParams &p, int rb_per_cta) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t gpr = p.cols / kGroup;
-    const int64_t nrb = (p.rows + kTileRows - 1) / kTileRows;
-    const int64_t rb0 = int64_t(blockIdx.x) * rb_per_cta;
-    const int64_t rb1 = rb0 + rb_per_cta < nrb ? rb0 + rb_per_cta : nrb;
-    const int split = blockIdx.y;
-    const int64_t kg = int64_t(split) * W + warp;
-    const bool active = kg < gpr;
-    const TileMeta empty = {0u, 0u, 0u};
+// Fill the CTA's x slab: gpr groups x 32 BF16 pairs.
+__device__ __forceinline__ void load_x_all(const GemvParams &p, uint32_t *xs, uint32_t gpr) {
+    const uint32_t *x32 = reinterpret_cast<const uint32_t *>(p.x);
+    for (uint32_t i = threadIdx.x; i < gpr * 32u; i += blockDim.x)
+        xs[i] = __ldg(x32 + i);
+}
 
-    // shared memory: [common tables][x slab W x 32 pairs][per warp 4 code buffers]
-    // [tile partials rb_per_cta x W x 32]
-    size_t off = 0;
-    DecodeShared ds{};
-    if (kCompressed) {
-        ds = carve_common(smem);
-        off = kCommonSmemBytes;
-    }
-    uint32_t *xs = reinterpret_cast<uint32_t *>(smem + off);
-    off += size_t(W) * 32 * 4;
-    const uint32_t xw = smem_addr(xs + warp * 32);
-    uint32_t cb0 = 0;  // warp's four code buffers: pair parity x (A, B)
-    if (kCompressed) {
-        cb0 = smem_addr(smem + off + size_t(warp) * 4 * kCodeBufBytes);
-        off += size_t(W) * 4 * kCodeBufBytes;
-    }
-    float *red = reinterpret_cast<float *>(smem + off);  // [rb_per_cta][W][32]
-
-    for (int i = threadIdx.x; i < W * 32; i += blockDim.x) {
-        const int64_t g = int64_t(split) * W + (i >> 5);
-        const uint16_t *xp = p.x + g * kGroup + 2 * (i & 31);
-        xs[i] = g < gpr ? (uint32_t(xp[0]) | (uint32_t(xp[1]) << 16)) : 0u;
-    }
-
-    const int64_t ntile = active ? rb1 - rb0 : 0;
-    const int64_t npair = (ntile + 1) / 2;
-    TileMeta mA = empty, mB = empty;
-    uint32_t offA = 0, offB = 0;  // offsets of the next pair to fetch
-    uint4 nsmA[4], nsmB[4];  // sign+mantissa bytes of the next pair
-#pragma unroll
-    for (int c = 0; c < 4; c++) {
-        nsmA[c] = make_uint4(0, 0, 0, 0);
-        nsmB[c] = make_uint4(0, 0, 0, 0);
-    }
-    if (kCompressed && npair > 0) {
-        tile_fetch(p.v, tile_loc(p.v, rb0, kg, gpr), tile_offsets_load(p.v, rb0 * gpr + kg), cb0, mA, nsmA);
-        if (ntile > 1)
-            tile_fetch(p.v, tile_loc(p.v, rb0 + 1, kg, gpr), tile_offsets_load(p.v, (rb0 + 1) * gpr + kg),
-                       cb0 + kCodeBufBytes, mB, nsmB);
-        if (ntile > 2)
-            offA = tile_offsets_load(p.v, (rb0 + 2) * gpr + kg);
-        if (ntile > 3)
-            offB = tile_offsets_load(p.v, (rb0 + 3) * gpr + kg);
-    } else if (!kCompressed && npair > 0) {
-        prefetch_bf16_row(p, rb0, kg);
-        if (ntile > 1)
-            prefetch_bf16_row(p, rb0 + 1, kg);
-    }
-    if (kCompressed)
-        build_tables(ds, p.v);
-    __syncthreads();
-
-#pragma unroll 1
-    for (int64_t i = 0; i < npair; i++) {
-        const int64_t rbA = rb0 + 2 * i, rbB = rbA + 1;
-        const bool hasB = rbB < rb1;
-        float aA0 = 0.f, aA1 = 0.f, aB0 = 0.f, aB1 = 0.f;
-        if (kCompressed) {
-            const int RA = tile_rows(p.v, rbA);
-            const int RB = hasB ? tile_rows(p.v, rbB) : 0;  // no tile B: every lane decodes zeros
-            const uint32_t bufA = cb0 + uint32_t(i & 1) * 2 * kCodeBufBytes, bufB = bufA + kCodeBufBytes;
-            uint4 smA[4], smB[4];  // this pair's sign+mantissa bytes, loaded during the previous pair
-#pragma unroll
-            for (int c = 0; c < 4; c++) {
-                smA[c] = nsmA[c];
-                smB[c] = nsmB[c];
-            }
-            LaneStream la, lb;
-            const uint32_t emA = tile_begin(ds, mA, RA, bufA, la, p.status);
-            const uint32_t emB = tile_begin(ds, mB, RB, bufB, lb, p.status);
-            const uint32_t ebA = escape_base(mA, bufA), ebB = escape_base(mB, bufB);
-            // fetch the next pair while this one is decoded
-            if (i + 1 < npair) {
-                const uint32_t nA = cb0 + uint32_t((i + 1) & 1) * 2 * kCodeBufBytes;
-                tile_fetch(p.v, tile_loc(p.v, rbA + 2, kg, gpr), offA, nA, mA, nsmA);
-                if (rbB + 2 < rb1) {
-                    tile_fetch(p.v, tile_loc(p.v, rbB + 2, kg, gpr), offB, nA + kCodeBufBytes, mB, nsmB);
-                } else {
-                    mB = empty;
-#pragma unroll
-                    for (int c = 0; c < 4; c++)
-                        nsmB[c] = make_uint4(0, 0, 0, 0);
-                }
-                if (rbA + 4 < rb1)
-                    offA = tile_offsets_load(p.v, (rbA + 4) * gpr + kg);
-                if (rbB + 4 < rb1)
-                    offB = tile_offsets_load(p.v, (rbB + 4) * gpr + kg);
-            }
-#pragma unroll
-            for (int I = 0; I < 32; I++) {
-                const uint32_t x2 = lds32(xw + 4 * I);
-                fma_bf16x2(aA0, aA1, decode_pair(la, I, sm_word(smA, I >> 1)), x2);
-                fma_bf16x2(aB0, aB1, decode_pair(lb, I, sm_word(smB, I >> 1)), x2);
-            }
-            tile_check(la, p.status);
-            tile_check(lb, p.status);
-            if (emA | emB) {  // escaped groups: redo those lanes from raw exponents
-                if ((emA >> lane) & 1u) {
-                    const float2 r = escaped_tile_sum(ebA, emA, tile_loc(p.v, rbA, kg, gpr), xw);
-                    aA0 = r.x;
-                    aA1 = r.y;
-                }
-                if ((emB >> lane) & 1u) {
-                    const float2 r = escaped_tile_sum(ebB, emB, tile_loc(p.v, rbB, kg, gpr), xw);
-                    aB0 = r.x;
-                    aB1 = r.y;
-                }
-            }
-        } else {
-            if (rbA + 2 < rb1)
-                prefetch_bf16_row(p, rbA + 2, kg);
-            if (rbB + 2 < rb1)
-                prefetch_bf16_row(p, rbB + 2, kg);
-            const int64_t nA = rbA * kTileRows + lane, nB = rbB * kTileRows + lane;
-            const uint4 *srcA = reinterpret_cast<const uint4 *>(p.w + nA * p.cols + kg * kGroup);
-            const uint4 *srcB = reinterpret_cast<const uint4 *>(p.w + (hasB ? nB : nA) * p.cols + kg * kGroup);
-            const bool okA = nA < p.rows, okB = hasB && nB < p.rows;
-#pragma unroll 1
-            for (int q = 0; q < 4; q++) {
-                const uint4 wA0 = okA ? __ldg(srcA + 2 * q) : make_uint4(0, 0, 0, 0);
-                const uint4 wA1 = okA ? __ldg(srcA + 2 * q + 1) : make_uint4(0, 0, 0, 0);
-                const uint4 wB0 = okB ? __ldg(srcB + 2 * q) : make_uint4(0, 0, 0, 0);
-                const uint4 wB1 = okB ? __ldg(srcB + 2 * q + 1) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                for (int k = 0; k < 8; k++) {
-                    const uint32_t x2 = lds32(xw + 4 * (8 * q + k));
-                    fma_bf16x2(aA0, aA1, word4(k < 4 ? wA0 : wA1, k & 3), x2);
-                    fma_bf16x2(aB0, aB1, word4(k < 4 ? wB0 : wB1, k & 3), x2);
-                }
-            }
-        }
-        red[(int(rbA - rb0) * W + warp) * 32 + lane] = aA0 + aA1;
-        if (hasB)
-            red[(int(rbB - rb0) * W + warp) * 32 + lane] = aB0 + aB1;
-    }
-    if (!active)
-        for (int64_t rb = rb0; rb < rb1; rb++)
-            red[(int(rb - rb0) * W + warp) * 32 + lane] = 0.f;
-    __syncthreads();
-
-    // CTA partial per (row block, row): sum over the W groups in order.
-    const int nsplit = gridDim.y;
-    const int nrows_cta = int(rb1 - rb0) * 32;
-    for (int t = threadIdx.x; t < nrows_cta; t += blockDim.x) {
-        const int rl = t >> 5, j = t & 31;
+// y for the CTA's rows: the warp partials in order.
+template <int W>
+__device__ __forceinline__ void cta_reduce(const GemvParams &p, const float *red, uint32_t rb0, uint32_t nrbc) {
+    for (uint32_t t = threadIdx.x; t < nrbc * 32u; t += blockDim.x) {
+        const uint32_t rl = t >> 5, j = t & 31;
         float s = red[(rl * W) * 32 + j];
 #pragma unroll
         for (int w = 1; w < W; w++)
             s += red[(rl * W + w) * 32 + j];
-        const int64_t n = (rb0 + rl) * kTileRows + j;
-        if (nsplit == 1) {
-            if (n < p.rows)
-                p.y[n] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
-        } else {
-            p.partial[(rb0 + rl) * kTileRows * nsplit + int64_t(split) * kTileRows + j] = s;
+        const int64_t n = int64_t(rb0 + rl) * kTileRows + j;
+        if (n < p.rows)
+            p.y[n] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+    }
+}
+
+// Offsets of the pair at tile t (lanes 0..2: tcode[t..t+2], lanes 3..5:
+// tesc[t..t+2]; indices past the table end read its last entry).
+__device__ __forceinline__ uint32_t pair_offsets_load(const BlobView &v, uint32_t t) {
+    const int lane = threadIdx.x & 31;
+    const int l = lane < 6 ? lane : 0;
+    const uint32_t k = t + uint32_t(l % 3);
+    return __ldg((l < 3 ? v.tcode : v.tesc) + (k < v.ntiles ? k : v.ntiles));
+}
+
+// What the decode needs to know about a staged pair (warp-uniform; kept in
+// shared memory next to the stage so that the loop body is not duplicated).
+struct PairMeta {
+    uint32_t pkA, pkB;   // n16 | nesc << 8 | bad << 16 of each tile
+    uint32_t n16A, n16B, nescA, pad[3];
+};
+
+// Validate the pair's offsets `o` and start its bulk copies into stage `st`:
+//   [0, 64)                      glen of A and B (full row blocks only)
+//   [64, 64 + 2*tdata)           code regions of A then B, then escaped exponents of A then B
+//   [smoff, smoff + 128*R)       sign+mantissa bytes of A then B
+// A pair with bad offsets copies no codes and is decoded as zeros (the error
+// is recorded by tile_begin).
+__device__ __forceinline__ void pair_issue(const BlobView &v, uint32_t o, uint32_t rb, uint32_t kgA, bool hasB,
+                                           uint32_t t, uint32_t st, uint32_t smoff, uint32_t bar, PairMeta *meta) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t c0 = __shfl_sync(0xffffffffu, o, 0), c1 = __shfl_sync(0xffffffffu, o, 1);
+    const uint32_t c2r = __shfl_sync(0xffffffffu, o, 2), e0 = __shfl_sync(0xffffffffu, o, 3);
+    const uint32_t e1 = __shfl_sync(0xffffffffu, o, 4), e2r = __shfl_sync(0xffffffffu, o, 5);
+    const uint32_t c2 = hasB ? c2r : c1, e2 = hasB ? e2r : e1;
+    const bool full = rb < v.nfull;
+    const uint32_t R = full ? uint32_t(kTileRows) : v.tail_rows;
+    const uint32_t n16A = c1 - c0, n16B = c2 - c1, nescA = e1 - e0, nescB = e2 - e1;
+    const uint32_t lim16 = uint32_t(kMaxTileCodeBytes / 16);
+    const bool bad = n16A > lim16 || n16B > lim16 || nescA > R || nescB > R || n16A * 16u + nescA * 64u > v.tdata ||
+                     n16B * 16u + nescB * 64u > v.tdata || c2 > v.code16 || e2 > v.n_esc32;
+    if (lane == 0) {
+        meta->pkA = bad ? (1u << 16) : (n16A | (nescA << 8));
+        meta->pkB = !hasB ? 0u : bad ? (1u << 16) : (n16B | (nescB << 8));
+        meta->n16A = bad ? 0u : n16A;
+        meta->n16B = bad ? 0u : n16B;
+        meta->nescA = bad ? 0u : nescA;
+    }
+    const uint32_t ntile = hasB ? 2u : 1u;
+    const uint64_t q0 = uint64_t(t) * kTileRows - (full ? 0u : (kTileRows - R) * kgA);  // first group of A
+    const uint32_t code_bytes = bad ? 0u : (c2 - c0) * 16u;
+    const uint32_t esc_bytes = bad ? 0u : (e2 - e0) * 64u;
+    const uint32_t sm_bytes = uint32_t(kGroup) * R * ntile;
+    const uint32_t glen_bytes = full ? uint32_t(kTileRows) * ntile : 0u;
+    if (lane == 0) {
+        mbar_expect_tx(bar, code_bytes + esc_bytes + sm_bytes + glen_bytes);
+        if (glen_bytes)
+            bulk_g2s(st, v.glen + q0, glen_bytes, bar);
+        if (code_bytes)
+            bulk_g2s(st + 64u, v.code + size_t(c0) * 16, code_bytes, bar);
+        if (esc_bytes)
+            bulk_g2s(st + 64u + code_bytes, v.esc + size_t(e0) * 64, esc_bytes, bar);
+        bulk_g2s(st + smoff, v.sm + q0 * kGroup, sm_bytes, bar);
+    }
+}
+
+// An escaped group's two accumulators, from its raw exponents and
+// sign+mantissa bytes in the stage (rare; out of line).
+__device__ __noinline__ float2 escaped_sum(uint32_t ebase, uint32_t em, uint32_t sm_lane, uint32_t stride,
+                                           const uint32_t *x) {
+    uint4 e[4], sm[4];
+    escape_read(ebase, em, e);
+#pragma unroll
+    for (int c = 0; c < 4; c++)
+        sm[c] = lds128(sm_lane + uint32_t(c) * stride);
+    float b0 = 0.f, b1 = 0.f;
+#pragma unroll
+    for (int I = 0; I < 32; I++)
+        fma_bf16x2(b0, b1, escape_pair(e, I, sm_word(sm, I >> 1)), __ldg(x + I));
+    return make_float2(b0, b1);
+}
+
+// Walks the warp's pairs in order: row block by row block, group pairs within.
+struct PairCursor {
+    uint32_t rb, kgA;
+    __device__ __forceinline__ void next(uint32_t k0, uint32_t k1) {
+        kgA += 2;
+        if (kgA >= k1) {
+            kgA = k0;
+            rb++;
         }
     }
-    if (nsplit == 1)
-        return;
-    __threadfence();
-    __syncthreads();
-    __shared__ int last;
-    if (threadIdx.x == 0)
-        last = atomicAdd(p.counters + blockIdx.x, 1u) == uint32_t(nsplit - 1);
-    __syncthreads();
-    if (!last)
-        return;
-    __threadfence();
-    for (int t = threadIdx.x; t < nrows_cta; t += blockDim.x) {
-        const int rl = t >> 5, j = t & 31;
-        const float *ps = p.partial + (rb0 + rl) * kTileRows * nsplit + j;
-        float tot = __ldcg(ps);
-        for (int sp = 1; sp < nsplit; sp++)
-            tot += __ldcg(ps + sp * kTileRows);
-        const int64_t n = (rb0 + rl) * kTileRows + j;
-        if (n < p.rows)
-            p.y[n] = __bfloat16_as_ushort(__float2bfloat16_rn(tot));
+};
+
+template <int W>
+__device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_per_cta) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ __align__(8) uint64_t bars[kMaxColWarps * kPairStages];
+    __shared__ PairMeta metas[kMaxColWarps * kPairStages];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const BlobView &v = p.v;
+    const uint32_t gpr = v.gpr;
+    const uint32_t nrb = v.nfull + (v.tail_rows ? 1u : 0u);
+    const uint32_t rb0 = blockIdx.x * uint32_t(rb_per_cta);
+    const uint32_t rb1 = rb0 + uint32_t(rb_per_cta) < nrb ? rb0 + uint32_t(rb_per_cta) : nrb;
+    const uint32_t nrbc = rb1 - rb0;
+    uint32_t k0, k1;
+    warp_cols(gpr, warp, W, k0, k1);
+    const uint32_t np = (k1 - k0 + 1) / 2;  // pairs per row block
+    const uint32_t npairs = np * nrbc;
+    const uint32_t sbytes = (64u + 2u * v.tdata + 64u + 4096u + 127u) & ~127u;
+    const uint32_t smoff = 64u + 2u * v.tdata + 64u;
+
+    // shared memory: [common tables][warp partials rb_per_cta x W x 32][pad to 128]
+    // [per warp kPairStages stages]
+    const DecodeShared ds = carve_common(smem);
+    float *red = reinterpret_cast<float *>(smem + kCommonSmemBytes);
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t stage_lo = (sbase + uint32_t(kCommonSmemBytes) + uint32_t(rb_per_cta) * W * 128u + 127u) & ~127u;
+    const uint32_t st0 = stage_lo + uint32_t(warp) * kPairStages * sbytes;
+    const uint32_t bar0 = smem_addr(&bars[warp * kPairStages]);
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kPairStages; s++)
+            mbar_init(bar0 + 8u * s, 1);
+        mbar_init_fence();
     }
-    if (threadIdx.x == 0)
-        p.counters[blockIdx.x] = 0;
+    __syncwarp();
+
+    // start the first pairs' copies, then build the tables while they fly
+    PairMeta *meta = &metas[warp * kPairStages];
+    PairCursor issue{rb0, k0};
+    uint32_t nissued = 0;
+    uint32_t o_next = npairs ? pair_offsets_load(v, rb0 * gpr + k0) : 0u;
+#pragma unroll
+    for (int s = 0; s < kPairStages; s++) {
+        if (nissued < npairs) {
+            pair_issue(v, o_next, issue.rb, issue.kgA, issue.kgA + 1 < k1, issue.rb * gpr + issue.kgA,
+                       st0 + uint32_t(s) * sbytes, smoff, bar0 + 8u * s, meta + s);
+            issue.next(k0, k1);
+            nissued++;
+            if (nissued < npairs)
+                o_next = pair_offsets_load(v, issue.rb * gpr + issue.kgA);
+        }
+    }
+    build_tables(ds, v);
+    __syncthreads();
+    const uint32_t lut = smem_addr(ds.lut);
+
+    PairCursor cur{rb0, k0};
+    float s_w = 0.f;  // this warp's partial for row `lane` of row block cur.rb
+    uint32_t bad = 0;
+    if (npairs == 0)
+        for (uint32_t rl = 0; rl < nrbc; rl++)
+            red[(rl * W + warp) * 32 + lane] = 0.f;
+
+#pragma unroll 1
+    for (uint32_t j = 0; j < npairs; j++) {
+        const uint32_t s = j % kPairStages;
+        const uint32_t st = st0 + s * sbytes, bar = bar0 + 8u * s;
+        mbar_wait(bar, (j / kPairStages) & 1u, p.status, kStatusTimeout);
+        const PairMeta m = meta[s];
+        const bool hasB = cur.kgA + 1 < k1;
+        const bool full = cur.rb < v.nfull;
+        const int R = full ? kTileRows : int(v.tail_rows);
+        // glen: from the stage, or (partial row block) straight from the blob
+        uint32_t gA, gB;
+        if (full) {
+            gA = lds_u8(st + uint32_t(lane));
+            gB = lds_u8(st + 32u + uint32_t(lane));
+        } else {
+            const uint64_t q0 = uint64_t(cur.rb * gpr + cur.kgA) * kTileRows - uint64_t(kTileRows - R) * cur.kgA;
+            const uint32_t l = uint32_t(lane) < uint32_t(R) ? uint32_t(lane) : 0u;
+            gA = __ldg(v.glen + q0 + l);
+            gB = hasB ? __ldg(v.glen + q0 + uint32_t(R) + l) : 0u;
+        }
+        LaneStream la, lb;
+        const uint32_t cA = st + 64u, cB = cA + 16u * m.n16A;
+        const uint32_t emA = tile_begin_ready(ds, TileMeta{gA, 0u, m.pkA}, R, cA, la, p.status);
+        const uint32_t emB = tile_begin_ready(ds, TileMeta{gB, 0u, m.pkB}, hasB ? R : 0, cB, lb, p.status);
+        const uint32_t ebA = cA + 16u * (m.n16A + m.n16B), ebB = ebA + 64u * m.nescA;
+        const uint32_t stride = 16u * uint32_t(R);
+        const uint32_t smA = st + smoff + 16u * uint32_t(lane), smB = smA + 64u * uint32_t(R);
+        // x of the two groups, 4 pairs per load, one load ahead (broadcast, L1-resident)
+        const uint4 *xA = reinterpret_cast<const uint4 *>(p.x) + size_t(cur.kgA) * 8;
+        const uint4 *xB = xA + (hasB ? 8 : 0);
+        float aA0 = 0.f, aA1 = 0.f, aB0 = 0.f, aB1 = 0.f;
+        uint4 sA = lds128(smA), sB = lds128(smB), nA = sA, nB = sB;
+        uint4 x4A = __ldg(xA), x4B = __ldg(xB), nxA = x4A, nxB = x4B;
+#pragma unroll
+        for (int I = 0; I < 32; I++) {
+            if ((I & 7) == 0 && I < 24) {  // next chunk of sign+mantissa bytes
+                nA = lds128(smA + uint32_t((I >> 3) + 1) * stride);
+                nB = lds128(smB + uint32_t((I >> 3) + 1) * stride);
+            }
+            if ((I & 3) == 0) {
+                if (I > 0) {
+                    x4A = nxA;
+                    x4B = nxB;
+                }
+                if (I < 28) {
+                    nxA = __ldg(xA + (I >> 2) + 1);
+                    nxB = __ldg(xB + (I >> 2) + 1);
+                }
+            }
+            fma_bf16x2(aA0, aA1, decode_pair(la, lut, I, word4(sA, (I >> 1) & 3)), word4(x4A, I));
+            fma_bf16x2(aB0, aB1, decode_pair(lb, lut, I, word4(sB, (I >> 1) & 3)), word4(x4B, I));
+            if ((I & 7) == 7) {
+                sA = nA;
+                sB = nB;
+            }
+        }
+        bad |= tile_check_bits(la) | tile_check_bits(lb);
+        if ((emA >> lane) & 1u) {
+            const float2 r = escaped_sum(ebA, emA, smA, stride, reinterpret_cast<const uint32_t *>(xA));
+            aA0 = r.x;
+            aA1 = r.y;
+        }
+        if ((emB >> lane) & 1u) {
+            const float2 r = escaped_sum(ebB, emB, smB, stride, reinterpret_cast<const uint32_t *>(xB));
+            aB0 = r.x;
+            aB1 = r.y;
+        }
+        s_w = s_w + (aA0 + aA1);
+        if (hasB)
+            s_w = s_w + (aB0 + aB1);
+        const uint32_t rb_done = cur.rb;
+        cur.next(k0, k1);
+        if (cur.rb != rb_done) {  // the warp's last pair of this row block
+            red[((rb_done - rb0) * W + warp) * 32 + lane] = s_w;
+            s_w = 0.f;
+        }
+        // the stage is free: start the pair kPairStages ahead
+        __syncwarp();
+        if (nissued < npairs) {
+            pair_issue(v, o_next, issue.rb, issue.kgA, issue.kgA + 1 < k1, issue.rb * gpr + issue.kgA, st, smoff, bar,
+                       meta + s);
+            issue.next(k0, k1);
+            nissued++;
+            if (nissued < npairs)
+                o_next = pair_offsets_load(v, issue.rb * gpr + issue.kgA);
+        }
+        __syncwarp();
+    }
+    tile_check_flush(bad, p.status);
+    __syncthreads();
+    cta_reduce<W>(p, red, rb0, nrbc);
+}
+
+template <int W>
+__device__ __forceinline__ void gemv_col_bf16(const GemvParams &p, int rb_per_cta) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t gpr = uint32_t(p.cols / kGroup);
+    const uint32_t nrb = uint32_t((p.rows + kTileRows - 1) / kTileRows);
+    const uint32_t rb0 = blockIdx.x * uint32_t(rb_per_cta);
+    const uint32_t rb1 = rb0 + uint32_t(rb_per_cta) < nrb ? rb0 + uint32_t(rb_per_cta) : nrb;
+    const uint32_t nrbc = rb1 - rb0;
+    uint32_t k0, k1;
+    warp_cols(gpr, warp, W, k0, k1);
+
+    // shared memory: [x slab gpr x 32 pairs][warp partials rb_per_cta x W x 32]
+    uint32_t *xs = reinterpret_cast<uint32_t *>(smem);
+    float *red = reinterpret_cast<float *>(smem + size_t(gpr) * 128);
+    load_x_all(p, xs, gpr);
+    __syncthreads();
+
+#pragma unroll 1
+    for (uint32_t rl = 0; rl < nrbc; rl++) {
+        const int64_t n = int64_t(rb0 + rl) * kTileRows + lane;
+        const bool ok = n < p.rows;
+        const uint4 *row = reinterpret_cast<const uint4 *>(p.w + (ok ? n : 0) * p.cols);
+        float s_w = 0.f;
+        uint4 cur[8], nxt[8];
+#pragma unroll
+        for (int c = 0; c < 8; c++)
+            nxt[c] = (ok && k0 < k1) ? __ldg(row + size_t(k0) * 8 + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll 1
+        for (uint32_t kg = k0; kg < k1; kg++) {
+#pragma unroll
+            for (int c = 0; c < 8; c++)
+                cur[c] = nxt[c];
+            if (kg + 1 < k1) {
+#pragma unroll
+                for (int c = 0; c < 8; c++)
+                    nxt[c] = ok ? __ldg(row + size_t(kg + 1) * 8 + c) : make_uint4(0, 0, 0, 0);
+            }
+            const uint32_t xaddr = smem_addr(xs) + kg * 128u;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int I = 0; I < 32; I++)
+                fma_bf16x2(a0, a1, word4(cur[I >> 2], I & 3), lds32(xaddr + 4u * I));
+            s_w = s_w + (a0 + a1);
+        }
+        red[(rl * W + warp) * 32 + lane] = s_w;
+    }
+    __syncthreads();
+    cta_reduce<W>(p, red, rb0, nrbc);
 }
 
 template <int W, bool kCompressed>
-__global__ void __launch_bounds__(W * 32, col_blocks_per_sm(W)) gemv_kg_kernel(const GemvParams p, int rb_per_cta) {
-    gemv_col_body<W, kCompressed>(p, rb_per_cta);
+__global__ void __launch_bounds__(W * 32, 1) gemv_kg_kernel(const GemvParams p, int rb_per_cta) {
+    if constexpr (kCompressed)
+        gemv_col_compressed<W>(p, rb_per_cta);
+    else
+        gemv_col_bf16<W>(p, rb_per_cta);
 }
 
 template <int W, bool kCompressed>
 uw_status launch_kg_one(const GemvParams &p, int rb_per_cta, cudaStream_t stream) {
-    const size_t smem = gemv_kg_smem_bytes(W, rb_per_cta, kCompressed);
+    const size_t smem = gemv_kg_smem_bytes(W, rb_per_cta, kCompressed, p.v.tdata, int(p.cols / kGroup));
+    if (smem > size_t(kMaxSmemPerBlock) - 1024)
+        return UW_ERR_UNSUPPORTED;
     auto kern = gemv_kg_kernel<W, kCompressed>;
     if (!ensure_smem(kern, smem))
         return UW_ERR_CUDA;
     const int64_t nrb = (p.rows + kTileRows - 1) / kTileRows;
-    const int64_t gpr = p.cols / kGroup;
-    const dim3 grid(unsigned((nrb + rb_per_cta - 1) / rb_per_cta), unsigned((gpr + W - 1) / W));
+    const dim3 grid(unsigned((nrb + rb_per_cta - 1) / rb_per_cta));
     kern<<<grid, dim3(W * 32), smem, stream>>>(p, rb_per_cta);
     return cudaGetLastError() == cudaSuccess ? UW_OK : UW_ERR_CUDA;
 }
 
 }  // namespace
 
-size_t gemv_kg_smem_bytes(int warps, int rb_per_cta, bool compressed) {
-    size_t s = compressed ? size_t(kCommonSmemBytes) + size_t(warps) * 4 * kCodeBufBytes : 0;
-    return s + size_t(warps) * 32 * 4 + size_t(rb_per_cta) * warps * 32 * 4;
+size_t gemv_kg_smem_bytes(int warps, int rb_per_cta, bool compressed, uint32_t tdata, int gpr) {
+    const size_t red = size_t(rb_per_cta) * warps * 128;
+    if (!compressed)
+        return size_t(gpr) * 128 + red;
+    const size_t sbytes = (64u + 2u * tdata + 64u + 4096u + 127u) & ~size_t(127);
+    return size_t(kCommonSmemBytes) + red + 128 + size_t(warps) * kPairStages * sbytes;
 }
 
 uw_status launch_gemv_kg(const GemvParams &p, int warps, int rb_per_cta, bool compressed, cudaStream_t stream) {
     if (p.batch != 1 || rb_per_cta < 1)
         return UW_ERR_UNSUPPORTED;
-    if (gemv_kg_smem_bytes(warps, rb_per_cta, compressed) > size_t(kMaxSmemPerBlock))
-        return UW_ERR_UNSUPPORTED;
+    if (uint64_t(p.rows / kTileRows + 1) * (p.cols / kGroup) >= (uint64_t(1) << 32))
+        return UW_ERR_UNSUPPORTED;  // tile indices are 32-bit
     switch (warps) {
         case 4: return compressed ? launch_kg_one<4, true>(p, rb_per_cta, stream)
                                   : launch_kg_one<4, false>(p, rb_per_cta, stream);

@@ -27,15 +27,12 @@ struct GemvParams {
     int splits;
 };
 
-size_t gemv_smem_bytes(int64_t cols, int warps, int splits, int bp, bool compressed);
+size_t gemv_smem_bytes(int64_t cols, int warps, int splits, int bp, bool compressed, uint32_t tbuf);
 uw_status launch_gemv(const GemvParams &p, int warps, int bp, bool compressed, cudaStream_t stream);
 
-// Batch-1 GEMV on column CTAs: W warps (one 64-column group each) x
-// rb_per_cta row blocks per CTA; `col_blocks_per_sm` is the occupancy the
-// kernel is compiled for.
-// 16 warps per SM leaves each thread 128 registers.
-constexpr int col_blocks_per_sm(int warps) { return warps >= 16 ? 1 : 16 / warps; }
-size_t gemv_kg_smem_bytes(int warps, int rb_per_cta, bool compressed);
+// Batch-1 GEMV on column-range CTAs: W warps splitting all 64-column groups,
+// rb_per_cta row blocks per CTA, one CTA per SM.
+size_t gemv_kg_smem_bytes(int warps, int rb_per_cta, bool compressed, uint32_t tdata, int gpr);
 uw_status launch_gemv_kg(const GemvParams &p, int warps, int rb_per_cta, bool compressed, cudaStream_t stream);
 
 // Tensor-core matmul (gemm_tc.cu): CTAs of 4G producer warps + 1 MMA warp,
@@ -55,8 +52,8 @@ struct TcParams {
     int S, Np;             // stages, padded batch (set by the launcher)
     uint32_t tmem_cols;    // tensor-memory columns allocated (set by the launcher)
 };
-size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed);
-int gemm_tc_stages(int G, int Np, bool compressed);
+size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed, uint32_t tbuf);
+int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tbuf);
 int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits);
 uw_status launch_gemm_tc(const TcParams &p, int G, bool compressed, cudaStream_t stream);
 
@@ -71,9 +68,13 @@ inline bool ensure_smem(Kernel *kern, size_t bytes) {
     return ensure_smem_limit(reinterpret_cast<const void *>(kern), bytes);
 }
 
+// Tile buffer stride assumed where no blob is at hand (the largest possible).
+constexpr uint32_t kWorstTileBuf = kMaxTileData + kTileSlack;
+
 // Host helpers (api.cu).
 void canonical_code_values(const uint8_t len[16], uint16_t code[16]);
 void fill_blob_view(const uw_desc &d, const void *blob_dev, BlobView *v);
+uint32_t tile_data_bytes(const uw_desc &d);  // a blob's tile buffer capacity
 
 // Workspace layout: [status word | counters | split partials | weights].
 struct WsLayout {
