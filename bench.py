@@ -44,6 +44,171 @@ WORKLOAD = "gate_proj 14336x4096 BF16 N(0,0.02) seed 0, compressed; y = x W^T, b
 KERNEL_SOURCES = ["decode.cuh", "gemv_kg.cu", "format.h", "kernels.h"]
 
 
+def launch_stats(torch, fn, stream, reps: int = 30, warm: int = 5, flush=None):
+    """Per-call device time (us) with CUDA events on the launching stream:
+    median, p10, p90 over `reps` calls, the L2 flushed before each one."""
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    times = []
+    for r in range(warm + reps):
+        if flush is not None:
+            flush.add_(1)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        if r >= warm:
+            times.append(e0.elapsed_time(e1) * 1000.0)
+    t = np.sort(np.array(times))
+    return {"median": round(float(np.median(t)), 2), "p10": round(float(t[int(0.1 * (len(t) - 1))]), 2),
+            "p90": round(float(t[int(0.9 * (len(t) - 1))]), 2)}
+
+
+def run_workloads(args):
+    """One JSON line per measured workload besides the headline one: the
+    1024 x 1024 matrix, the SwiGLU MLP layer at batches 1/8/32, the
+    heavy-tailed matrix at batches 1/16/64/256 and the 32-layer model with
+    the autotuner's plan per matrix and batch."""
+    import torch
+
+    import lossless_bf16_weight_gb300 as uw
+    import workloads as wl
+    if not os.path.exists(uw.LIB_PATH):
+        uw.build()
+    uw.load()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 << 20)
+    flush = torch.zeros(2 * l2 // 4, dtype=torch.int32, device="cuda")
+    hbm, hbm_kind = peaks()
+    tflops_peak = 1953.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tflops_peak = float(json.load(f).get("bf16_tflops", tflops_peak))
+    except (OSError, ValueError):
+        pass
+    which = set(args.workloads.split(","))
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+    class Mat:
+        def __init__(self, w):
+            self.blob = uw.compress(w)
+            self.desc = uw.blob_info(self.blob)
+            self.dev = torch.from_numpy(self.blob).cuda()
+            self.rows, self.cols = w.shape
+
+        def plan(self, batch):
+            ws = torch.empty(uw.autotune_workspace_size(self.desc, [batch]), dtype=torch.uint8, device="cuda")
+            p = uw.autotune(self.desc, self.dev, [batch], ws, stream)[0]
+            return p
+
+        def ws(self, batch, plan):
+            t = torch.empty(max(uw.workspace_size(self.desc, batch, plan), 256), dtype=torch.uint8, device="cuda")
+            uw.workspace_init(t, stream)
+            return t
+
+    def name(p):
+        return ("fused:" if p.strategy == uw.STRATEGY_FUSED else "decompress:") + uw.variant_name(p.strategy, p.variant)
+
+    if "small" in which or "all" in which:
+        w = wl.workload_weights("small")
+        m = Mat(w)
+        x = dev(wl.activations(1, 1024))
+        y = torch.empty(1, 1024, dtype=torch.int16, device="cuda")
+        plan = m.plan(1)
+        ws = m.ws(1, plan)
+        t = launch_stats(torch, lambda: uw.matmul(m.desc, m.dev, x, y, ws, plan, stream), stream, flush=flush)
+        wout = torch.empty(1024, 1024, dtype=torch.int16, device="cuda")
+        td = launch_stats(torch, lambda: uw.decompress(m.desc, m.dev, wout, ws, stream), stream, flush=flush)
+        print(json.dumps({"workload": "small 1024x1024 N(0,0.02), batch 1", "ratio_vs_bf16": round(
+            m.desc.blob_bytes / (2 * 1024 * 1024), 4), "plan": name(plan), "fused_us": t,
+            "fused_GBps": round(m.desc.blob_bytes / t["median"] / 1e3, 1), "decompress_us": td,
+            "decompress_GBps_read_plus_write": round((m.desc.blob_bytes + 2 * 1024 * 1024) / td["median"] / 1e3, 1),
+            "note": "L2 flushed before each call, but a 1.4 MB blob is one L2 fill: not an HBM-bound number"}),
+            flush=True)
+
+    if "mlp" in which or "all" in which:
+        spec = wl.WORKLOADS["mlp"]
+        mats = [Mat(wl.normal_weights(*shape, spec["sigma"], seed)) for shape, seed in zip(spec["shapes"], spec["seeds"])]
+        nbytes = sum(m.desc.blob_bytes for m in mats)
+        rows = []
+        for batch in spec["batches"]:
+            plans = [m.plan(batch) for m in mats]
+            wss = [m.ws(batch, p) for m, p in zip(mats, plans)]
+            x = dev(wl.activations(batch, wl.GATE_SHAPE[1]))
+            gt = torch.empty(batch, wl.GATE_SHAPE[0], dtype=torch.int16, device="cuda")
+            up = torch.empty_like(gt)
+            h = torch.empty_like(gt)
+            y = torch.empty(batch, wl.DOWN_SHAPE[0], dtype=torch.int16, device="cuda")
+
+            def layer():
+                uw.matmul(mats[0].desc, mats[0].dev, x, gt, wss[0], plans[0], stream)
+                uw.matmul(mats[1].desc, mats[1].dev, x, up, wss[1], plans[1], stream)
+                uw.swiglu(gt, up, h, stream)
+                uw.matmul(mats[2].desc, mats[2].dev, h, y, wss[2], plans[2], stream)
+            t = launch_stats(torch, layer, stream, flush=flush)
+            gbs = nbytes / t["median"] / 1e3
+            rows.append({"batch": batch, "layer_us": t, "GBps": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4),
+                         "plans": [name(p) for p in plans]})
+        print(json.dumps({"workload": "SwiGLU MLP layer gate/up 14336x4096, down 4096x14336, N(0,0.02)",
+                          "compressed_bytes": nbytes, "ratio_vs_bf16": round(nbytes / (2 * 3 * 14336 * 4096), 4),
+                          "peak_GBps": hbm, "peak_kind": hbm_kind, "batches": rows}), flush=True)
+
+    if "heavy" in which or "all" in which:
+        w = wl.workload_weights("heavy")
+        m = Mat(w)
+        rows = []
+        for batch in wl.WORKLOADS["heavy"]["batches"]:
+            plan = m.plan(batch)
+            ws = m.ws(batch, plan)
+            x = dev(wl.activations(batch, 4096))
+            y = torch.empty(batch, 4096, dtype=torch.int16, device="cuda")
+            t = launch_stats(torch, lambda: uw.matmul(m.desc, m.dev, x, y, ws, plan, stream), stream, flush=flush)
+            tf = 2.0 * batch * 4096 * 4096 / t["median"] / 1e6
+            rows.append({"batch": batch, "plan": name(plan), "us": t,
+                         "GBps": round(m.desc.blob_bytes / t["median"] / 1e3, 1),
+                         "TFLOPs": round(tf, 2), "frac_of_bf16_peak": round(tf / tflops_peak, 4)})
+        print(json.dumps({"workload": "heavy-tailed 4096x4096 t4*0.02 (+0.1% x100, 0.01% zeros)",
+                          "escaped_fraction": round(m.desc.n_escaped / m.desc.n_groups, 4),
+                          "ratio_vs_bf16": round(m.desc.blob_bytes / (2 * 4096 * 4096), 4), "batches": rows}),
+              flush=True)
+
+    if "model" in which or "all" in which:
+        spec = wl.WORKLOADS["model"]
+        mats = [Mat(wl.model_matrix(layer, j)) for layer in range(spec["layers"]) for j in range(3)]
+        nbytes = sum(m.desc.blob_bytes for m in mats)
+        wout = torch.empty(wl.GATE_SHAPE, dtype=torch.int16, device="cuda")
+        ws0 = mats[0].ws(1, None)
+        td = launch_stats(torch, lambda: [uw.decompress(m.desc, m.dev, wout, ws0, stream) for m in mats], stream,
+                          reps=3, warm=1)
+        rows = []
+        for batch in spec["batches"]:
+            plans = [m.plan(batch) for m in mats]
+            wss = [m.ws(batch, p) for m, p in zip(mats, plans)]
+            x = dev(wl.activations(batch, 14336))
+            y = torch.empty(batch, 14336, dtype=torch.int16, device="cuda")
+
+            def sweep():
+                for m, p, ws in zip(mats, plans, wss):
+                    uw.matmul(m.desc, m.dev, x, y, ws, p, stream)
+            t = launch_stats(torch, sweep, stream, reps=3, warm=1)
+            choice = {}
+            for p in plans:
+                choice[name(p)] = choice.get(name(p), 0) + 1
+            rows.append({"batch": batch, "all_96_us": t, "GBps": round(nbytes / t["median"] / 1e3, 1),
+                         "plans": choice})
+            del wss
+        print(json.dumps({"workload": "32 MLP layers (96 matrices), sigma_l ~ U[0.01, 0.04]",
+                          "compressed_bytes": nbytes, "ratio_vs_bf16": round(nbytes / (2 * 96 * 14336 * 4096), 4),
+                          "decompress_all_us": td,
+                          "decompress_GBps_read_plus_write": round(
+                              (nbytes + 2 * 96 * 14336 * 4096) / td["median"] / 1e3, 1),
+                          "batches": rows}), flush=True)
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -54,6 +219,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--plan", default=None,
                     help="fixed plan instead of autotuning: fused:<variant> or decompress:<variant>")
+    ap.add_argument("--workloads", default=None,
+                    help="instead of the headline line, one line per workload: small,mlp,heavy,model or all")
     return ap.parse_args()
 
 
@@ -207,6 +374,20 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- ours (GPU)
+def max_over_ranks(torch, dist, ms: float, device) -> float:
+    """The slowest rank's time: every replica's timed region ends when the
+    last one does."""
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(nblob: int, steps: int, world: int, ms: float) -> float:
+    """GB/s of compressed bytes read by all replicas: each of the `world`
+    ranks reads the whole blob once per step (weak scaling)."""
+    return nblob * steps * world / (ms / 1e3) / 1e9
+
+
 def time_graph(torch, fn, steps: int, warmup: int, group: int, stream):
     """Run fn(i) `warmup` times, then time exactly `steps` calls: whole CUDA
     graphs of `group` calls plus eager calls for the remainder."""
@@ -300,14 +481,12 @@ def run_ours(args):
     samples = clocks.stop()
     ms = e0.elapsed_time(e1)
     if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(torch, dist, ms, "cuda")
     status = uw.check_status(ws, stream)
     assert status == 0, "device reported status %d" % status
 
     per_step_s = ms / 1e3 / args.steps
-    value = nblob * args.steps * world / (ms / 1e3) / 1e9
+    value = replica_throughput(nblob, args.steps, world, ms)
     algo_bytes = nblob + 2 * BATCH * COLS + 2 * BATCH * ROWS
     kernel_s = per_step_s / launches_per_step if plan.strategy == uw.STRATEGY_FUSED else None
     hbm, hbm_kind = peaks()
@@ -436,7 +615,9 @@ def e2e_measurement(torch, uw, desc, blobs, x, stream, plan, args):
 
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.workloads:
+        run_workloads(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

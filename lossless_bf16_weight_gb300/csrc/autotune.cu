@@ -119,6 +119,11 @@ extern "C" uw_status uw_autotune(const uw_desc *d, const void *blob_dev, const i
                     cudaEventElapsedTime(&ms, e0, e1);
                     if (r >= kWarm)
                         times.push_back(ms * 1000.f);
+                    // a candidate 4x slower than the best so far cannot win: stop timing it
+                    if (best.us > 0.f && ms * 1000.f > 4.f * best.us && r + 1 >= kWarm) {
+                        times.clear();
+                        break;
+                    }
                 }
                 if (!ok || times.empty())
                     continue;
