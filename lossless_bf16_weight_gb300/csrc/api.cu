@@ -33,16 +33,16 @@ cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 //   15..26 column CTAs, batch 1 only (gemv_kg.cu): warps per CTA x grid
 //          size in full waves (1..4) of the GPU; the row blocks per CTA
 //          follow from the matrix and the SM count
-//   27..34 tensor-core CTAs (gemm_tc.cu): producer groups G (2, 4) x K
+//   27..38 tensor-core CTAs (gemm_tc.cu): producer groups G (1, 2, 3) x K
 //          splits (1, 2, 4, 8, capped at the number of 64-column groups)
 constexpr int kWarpChoices[3] = {4, 8, 16};
 constexpr int kSplitChoices = 5;  // 1, 2, 4, 8, 16
 constexpr int kRowVariants = 3 * kSplitChoices;
 constexpr int kColWaves = 4;
 constexpr int kColVariants = 3 * kColWaves;
-constexpr int kTcGroups[2] = {2, 4};
+constexpr int kTcGroups[3] = {1, 2, 3};
 constexpr int kTcSplitChoices = 4;  // 1, 2, 4, 8
-constexpr int kTcVariants = 2 * kTcSplitChoices;
+constexpr int kTcVariants = 3 * kTcSplitChoices;
 constexpr int kTcFirst = kRowVariants + kColVariants;
 constexpr int kGemvVariants = kTcFirst + kTcVariants;
 constexpr int kMaxBatchChunk = 8;
@@ -83,12 +83,17 @@ GemvVariant gemv_variant(int v, int64_t rows, int64_t cols, uint32_t tbuf = kWor
     return {Kind::kColumn, w, 1, int(rb)};
 }
 
-// Tensor-core default: four producer groups while their stages fit, and the
-// K split (1, 2, 4, 8) whose grid fills the GPU's waves best (ties to fewer
-// splits).
+// Tensor-core default: the most producer groups whose stages fit (each
+// group keeps two K steps in flight), and the K split (1, 2, 4, 8) whose grid
+// fills the GPU's waves best (ties to fewer splits).
 int default_tc_variant(int64_t rows, int64_t cols, int64_t batch) {
     const int64_t np = std::min<int64_t>((batch + 15) / 16 * 16, kTcMaxBatch);
-    const int gi = gemm_tc_stages(4, int(np), true, kWorstTileBuf) >= 4 ? 1 : 0;
+    int gi = 0;
+    for (int i = 2; i > 0; i--)
+        if (gemm_tc_stages(kTcGroups[i], int(np), true, kWorstTileBuf - kTileSlack) >= 2 * kTcGroups[i] + 2) {
+            gi = i;
+            break;
+        }
     const int64_t mblocks = (rows + 127) / 128, gpr = cols / kGroup, sms = sm_count();
     int best = 0;
     double best_eff = -1.0;
@@ -521,7 +526,8 @@ extern "C" const char *uw_variant_name(int32_t strategy, int32_t variant) {
         "w4s8", "w8s8", "w16s8", "w4s16", "w8s16", "w16s16",
         "col_w4x1", "col_w8x1", "col_w16x1", "col_w4x2", "col_w8x2", "col_w16x2",
         "col_w4x3", "col_w8x3", "col_w16x3", "col_w4x4", "col_w8x4", "col_w16x4",
-        "tc_g2s1", "tc_g2s2", "tc_g2s4", "tc_g2s8", "tc_g4s1", "tc_g4s2", "tc_g4s4", "tc_g4s8"};
+        "tc_g1s1", "tc_g1s2", "tc_g1s4", "tc_g1s8", "tc_g2s1", "tc_g2s2", "tc_g2s4", "tc_g2s8",
+        "tc_g3s1", "tc_g3s2", "tc_g3s4", "tc_g3s8"};
     if (uw_variant_count(strategy) == 0 || variant < 0 || variant >= kGemvVariants)
         return nullptr;
     return names[variant];

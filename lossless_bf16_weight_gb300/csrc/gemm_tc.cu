@@ -4,35 +4,41 @@
 //
 // D = W x^T is computed as tcgen05.mma tiles with M = 128 rows of W (the A
 // operand) and N = the batch padded to a multiple of 16 (the B operand),
-// K = 16 per instruction.  A CTA owns 128 rows and one of `splits` ranges
-// of 64-column groups (one group = one pipeline stage, four MMAs).
+// K = 16 per instruction.  A CTA owns 128 rows (four 32-row blocks) and one
+// of `splits` ranges of 64-column groups; each group is one pipeline stage
+// (K step) of four MMAs.
+//
+// The A operand lives in tensor memory: a producer warp holds the 64 BF16
+// weights of its 32 rows of a K step in registers (lane = row) and writes
+// them with one tcgen05.st into the stage's 32 tensor-memory columns (two
+// BF16 per column); the MMA reads A from there and B (x) from shared memory.
 //
 // Warp roles (CTA of 4G + 1 warps):
-//   producers  warps 0 .. 4G-1: warp w fills the A rows 32*(w%4) .. +31 of
-//              the stages of K steps i = w/4, w/4 + G, ...  and a quarter of
-//              the stage's B rows (x, by cp.async; rows past the batch are
-//              zero-filled);
-//                * compressed source: each warp decodes its 32 x 64 tile on
-//                  chip (decode.cuh) into registers and stores the BF16 rows
-//                  into the swizzled stage -- the weights go from the blob to
-//                  the tensor cores without touching HBM (Unweight blog,
-//                  paragraphs on the reconstructive matmul and on decoding
-//                  into shared memory);
-//                * bf16 source: the same warps copy the uncompressed rows.
+//   producers  warp w < 4G owns row block w % 4 and the group pairs
+//              p = w/4, w/4 + G, ... (K steps 2p, 2p+1):
+//                * compressed source: the copy engine stages each pair
+//                  (pair_stage.cuh) and the warp decodes its two tiles side
+//                  by side (decode.cuh) into registers -- the weights go from
+//                  the blob to the tensor cores without touching HBM or
+//                  shared memory (Unweight blog, paragraphs on the
+//                  reconstructive matmul and on decoding on chip);
+//                * bf16 source: the same warps load the uncompressed rows.
+//              It also copies a quarter of each of its K steps' B rows (x,
+//              by cp.async; rows past the batch are zero-filled).
 //   MMA warp   warp 4G: one thread waits for each stage, issues its four
 //              MMAs and commits them to the stage's "empty" barrier.
 //   epilogue   warps 0..3 read the accumulator (tensor-memory lane quarter
 //              = warp index) and write y, or fp32 split partials; the last
 //              CTA of a row block adds the splits in order.
 // Both sources feed the same MMA sequence, so their outputs are
-// bit-identical.  Stage s holds A (16 KB) and B (Np x 128 bytes) in the
-// 128-byte-swizzled K-major layout of tc.cuh.
+// bit-identical.
 #include <cuda_bf16.h>
 
 #include <algorithm>
 
 #include "decode.cuh"
 #include "kernels.h"
+#include "pair_stage.cuh"
 #include "tc.cuh"
 
 namespace uw {
@@ -40,10 +46,34 @@ namespace uw {
 namespace {
 
 constexpr int kTcM = 128;
-constexpr int kTcMaxStages = 8;
-constexpr uint32_t kAStageBytes = kTcM * kGroup * 2;  // 16384
+constexpr int kTcMaxStages = 12;
+constexpr uint32_t kTmemCols = 512;
 
-// The quarter `qtr` of the stage's x rows: Np/4 rows x 8 chunks of 16 bytes.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+        :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+           "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+           "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+           "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem]^T for one K slice of 16; issued by one thread.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                       bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(uint32_t(accumulate)) : "memory");
+}
+
+// The quarter `qtr` of a K step's x rows: Np/4 rows x 8 chunks of 16 bytes.
 __device__ __forceinline__ void load_x_quarter(const TcParams &p, uint32_t b_st, int64_t kg, int qtr, int lane) {
     const int per = p.Np >> 2;
     const int nchunk = per * 8;  // a multiple of 32: Np is a multiple of 16
@@ -55,66 +85,91 @@ __device__ __forceinline__ void load_x_quarter(const TcParams &p, uint32_t b_st,
     }
 }
 
+// An escaped group's 32 BF16 pairs, from its raw exponents and the
+// sign+mantissa bytes in the stage.
+__device__ __forceinline__ void escaped_pairs(uint32_t ebase, uint32_t em, uint32_t sm_lane, uint32_t stride,
+                                              uint32_t (&q)[32]) {
+    uint4 e[4], sm[4];
+    escape_read(ebase, em, e);
+#pragma unroll
+    for (int c = 0; c < 4; c++)
+        sm[c] = lds128(sm_lane + uint32_t(c) * stride);
+#pragma unroll
+    for (int I = 0; I < 32; I++)
+        q[I] = escape_pair(e, I, sm_word(sm, I >> 1));
+}
+
 template <int G, bool kCompressed>
 __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcParams p) {
     constexpr int P = 4 * G;  // producer warps
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[2 * kTcMaxStages + 1];
+    __shared__ __align__(8) uint64_t pbars[P * kPairStages];
+    __shared__ PairMeta metas[P * kPairStages];
     __shared__ uint32_t tmem_slot;
     __shared__ int last_cta;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const BlobView &v = p.v;
     const int S = p.S, Np = p.Np;
-    const int64_t gpr = p.cols / kGroup;
-    const int64_t nrb = (p.rows + kTileRows - 1) / kTileRows;
-    const int64_t mb = blockIdx.x;
+    const uint32_t gpr = uint32_t(p.cols / kGroup);
+    const uint32_t nrb = uint32_t((p.rows + kTileRows - 1) / kTileRows);
+    const uint32_t mb = blockIdx.x;
     const int split = blockIdx.y;
-    const int64_t kg_lo = gpr * split / p.splits, kg_hi = gpr * (split + 1) / p.splits;
-    const int nk = int(kg_hi - kg_lo);
+    const uint32_t kg_lo = uint32_t(uint64_t(gpr) * split / p.splits);
+    const uint32_t kg_hi = uint32_t(uint64_t(gpr) * (split + 1) / p.splits);
+    const uint32_t nk = kg_hi - kg_lo, npr = (nk + 1) / 2;
+    const uint32_t a0col = p.a0col;  // first tensor-memory column of the A stages
 
-    // shared memory: [pad to 1024][A stages][B stages][decode tables][code buffers]
+    // shared memory: [pad to 1024][B stages][decode tables][per producer warp kPairStages pair stages]
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
-    const uint32_t a0 = raw + pad;
     const uint32_t bstage = uint32_t(Np) * 128u;
-    const uint32_t b0 = a0 + uint32_t(S) * kAStageBytes;
-    unsigned char *dec = smem_raw + pad + size_t(S) * (kAStageBytes + bstage);
+    const uint32_t b0 = raw + pad;
+    unsigned char *dec = smem_raw + pad + size_t(S) * bstage;
     const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[kTcMaxStages]);
     const uint32_t done = smem_addr(&bars[2 * kTcMaxStages]);
+    const uint32_t sbytes = pair_stage_bytes(v.tdata), smoff = pair_stage_smoff(v.tdata);
+    const uint32_t pst0 = (smem_addr(dec + kCommonSmemBytes) + 127u) & ~127u;
 
     if (warp == P)
-        tmem_alloc(smem_addr(&tmem_slot), p.tmem_cols);
+        tmem_alloc(smem_addr(&tmem_slot), kTmemCols);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; s++) {
             mbar_init(full0 + 8u * s, 4);
             mbar_init(empty0 + 8u * s, 1);
         }
         mbar_init(done, 1);
+        for (int i = 0; i < P * kPairStages; i++)
+            mbar_init(smem_addr(&pbars[i]), 1);
         mbar_init_fence();
     }
+    __syncthreads();
 
-    // producer identity: row block rb (of 32 rows), K steps grp, grp + G, ...
+    // producer identity: row block rb, pairs g, g + G, ...
     const int rbl = warp & 3, grp = warp >> 2;
-    const int64_t rb = mb * 4 + rbl;
+    const uint32_t rb = mb * 4 + uint32_t(rbl);
     const bool producer = warp < P;
     const bool rb_ok = producer && rb < nrb;
+    const uint32_t my_pairs = producer && uint32_t(grp) < npr ? (npr - uint32_t(grp) + G - 1) / G : 0u;
+    const uint32_t st0 = pst0 + uint32_t(warp) * kPairStages * sbytes;
+    const uint32_t pbar0 = smem_addr(&pbars[producer ? warp * kPairStages : 0]);
+    PairMeta *meta = &metas[producer ? warp * kPairStages : 0];
     DecodeShared ds{};
-    uint32_t cbuf0 = 0;
-    TileMeta meta{0u, 0u, 0u};
-    uint4 smn[4];
-#pragma unroll
-    for (int c = 0; c < 4; c++)
-        smn[c] = make_uint4(0, 0, 0, 0);
-    uint32_t offs_next = 0;
+    uint32_t nissued = 0, o_next = 0;
     if (kCompressed) {
         ds = carve_common(dec);
-        cbuf0 = smem_addr(dec + kCommonSmemBytes + size_t(warp) * 2 * p.v.tbuf);
-        if (rb_ok && grp < nk) {
-            tile_fetch(p.v, tile_loc(p.v, rb, kg_lo + grp, gpr), tile_offsets_load(p.v, rb * gpr + kg_lo + grp),
-                       cbuf0, meta, smn);
-            if (grp + G < nk)
-                offs_next = tile_offsets_load(p.v, rb * gpr + kg_lo + grp + G);
+        if (rb_ok && my_pairs > 0) {
+            o_next = pair_offsets_load(v, rb * gpr + kg_lo + 2u * uint32_t(grp));
+            for (int s = 0; s < kPairStages && nissued < my_pairs; s++) {
+                const uint32_t kgA = kg_lo + 2u * (uint32_t(grp) + nissued * G);
+                pair_issue(v, o_next, rb, kgA, kgA + 1 < kg_hi, rb * gpr + kgA, st0 + uint32_t(s) * sbytes, smoff,
+                           pbar0 + 8u * s, meta + s);
+                nissued++;
+                if (nissued < my_pairs)
+                    o_next = pair_offsets_load(v, rb * gpr + kg_lo + 2u * (uint32_t(grp) + nissued * G));
+            }
         }
-        build_tables(ds, p.v);
+        build_tables(ds, v);
     }
     tc_fence_before();
     __syncthreads();
@@ -123,110 +178,151 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
     const uint32_t lut = kCompressed ? smem_addr(ds.lut) : 0u;
 
     if (producer) {
-        const int64_t left = p.rows - rb * kTileRows;  // rows of this row block (p.v is unset for bf16)
-        const int R = !rb_ok ? 0 : left < kTileRows ? int(left) : kTileRows;
-        const uint32_t arow = uint32_t(32 * rbl + lane);
-        int it = 0;
+        const int R = !rb_ok ? 0 : rb < v.nfull || !kCompressed ? int(std::min<int64_t>(kTileRows, p.rows - int64_t(rb) * kTileRows))
+                                                                  : int(v.tail_rows);
+        const uint32_t trow = tmem + (uint32_t(32 * rbl) << 16) + a0col;
+        uint32_t bad = 0;
 #pragma unroll 1
-        for (int i = grp; i < nk; i += G, it++) {
-            const int s = i % S, u = i / S;
-            const uint32_t a_st = a0 + uint32_t(s) * kAStageBytes, b_st = b0 + uint32_t(s) * bstage;
-            const int64_t kg = kg_lo + i;
+        for (uint32_t j = 0; j < my_pairs; j++) {
+            const uint32_t pi = uint32_t(grp) + j * G;  // pair index in the CTA's K range
+            const uint32_t i0 = 2u * pi, kgA = kg_lo + i0;
+            const bool hasB = kgA + 1 < kg_hi;
+            uint32_t qA[32], qB[32];
             if (kCompressed) {
-                uint32_t q[32];
                 if (rb_ok) {
-                    const uint32_t cbuf = cbuf0 + uint32_t(it & 1) * p.v.tbuf;
-                    uint4 sm[4];
-#pragma unroll
-                    for (int c = 0; c < 4; c++)
-                        sm[c] = smn[c];
-                    LaneStream ls;
-                    const uint32_t em = tile_begin(ds, meta, R, cbuf, ls, p.status);
-                    const uint32_t eb = escape_base(meta, cbuf);
-                    if (i + G < nk) {
-                        tile_fetch(p.v, tile_loc(p.v, rb, kg + G, gpr), offs_next,
-                                   cbuf0 + uint32_t((it + 1) & 1) * p.v.tbuf, meta, smn);
-                        if (i + 2 * G < nk)
-                            offs_next = tile_offsets_load(p.v, rb * gpr + kg + 2 * G);
+                    const uint32_t s = j % kPairStages;
+                    const uint32_t st = st0 + s * sbytes, pb = pbar0 + 8u * s;
+                    mbar_wait(pb, (j / kPairStages) & 1u, p.status, kStatusTimeout);
+                    const PairMeta m = meta[s];
+                    const bool full = rb < v.nfull;
+                    uint32_t gA, gB;
+                    if (full) {
+                        gA = lds_u8(st + uint32_t(lane));
+                        gB = lds_u8(st + 32u + uint32_t(lane));
+                    } else {
+                        const uint64_t q0 = uint64_t(rb * gpr + kgA) * kTileRows - uint64_t(kTileRows - R) * kgA;
+                        const uint32_t l = uint32_t(lane) < uint32_t(R) ? uint32_t(lane) : 0u;
+                        gA = __ldg(v.glen + q0 + l);
+                        gB = hasB ? __ldg(v.glen + q0 + uint32_t(R) + l) : 0u;
                     }
+                    LaneStream la, lb;
+                    const uint32_t cA = st + 64u, cB = cA + 16u * m.n16A;
+                    const uint32_t emA = tile_begin_ready(ds, TileMeta{gA, 0u, m.pkA}, R, cA, la, p.status);
+                    const uint32_t emB = tile_begin_ready(ds, TileMeta{gB, 0u, m.pkB}, hasB ? R : 0, cB, lb, p.status);
+                    const uint32_t ebA = cA + 16u * (m.n16A + m.n16B), ebB = ebA + 64u * m.nescA;
+                    const uint32_t stride = 16u * uint32_t(R);
+                    const uint32_t smA = st + smoff + 16u * uint32_t(lane), smB = smA + 64u * uint32_t(R);
+                    uint4 sA = lds128(smA), sB = lds128(smB), nA = sA, nB = sB;
 #pragma unroll
-                    for (int I = 0; I < 32; I++)
-                        q[I] = decode_pair(ls, lut, I, sm_word(sm, I >> 1));
-                    tile_check(ls, p.status);
-                    if ((em >> lane) & 1u) {  // escaped group: rebuild from its raw exponents
-                        uint4 e[4];
-                        escape_read(eb, em, e);
-#pragma unroll
-                        for (int I = 0; I < 32; I++)
-                            q[I] = escape_pair(e, I, sm_word(sm, I >> 1));
+                    for (int I = 0; I < 32; I++) {
+                        if ((I & 7) == 0 && I < 24) {
+                            nA = lds128(smA + uint32_t((I >> 3) + 1) * stride);
+                            nB = lds128(smB + uint32_t((I >> 3) + 1) * stride);
+                        }
+                        qA[I] = decode_pair(la, lut, I, word4(sA, (I >> 1) & 3));
+                        qB[I] = decode_pair(lb, lut, I, word4(sB, (I >> 1) & 3));
+                        if ((I & 7) == 7) {
+                            sA = nA;
+                            sB = nB;
+                        }
                     }
+                    bad |= tile_check_bits(la) | tile_check_bits(lb);
+                    if ((emA >> lane) & 1u)
+                        escaped_pairs(ebA, emA, smA, stride, qA);
+                    if ((emB >> lane) & 1u)
+                        escaped_pairs(ebB, emB, smB, stride, qB);
+                    // the pair stage is free: start the pair kPairStages ahead
+                    __syncwarp();
+                    if (nissued < my_pairs) {
+                        const uint32_t kgN = kg_lo + 2u * (uint32_t(grp) + nissued * G);
+                        pair_issue(v, o_next, rb, kgN, kgN + 1 < kg_hi, rb * gpr + kgN, st, smoff, pb, meta + s);
+                        nissued++;
+                        if (nissued < my_pairs)
+                            o_next = pair_offsets_load(v, rb * gpr + kg_lo + 2u * (uint32_t(grp) + nissued * G));
+                    }
+                    __syncwarp();
                 } else {
 #pragma unroll
-                    for (int I = 0; I < 32; I++)
-                        q[I] = 0u;
+                    for (int I = 0; I < 32; I++) {
+                        qA[I] = 0u;
+                        qB[I] = 0u;
+                    }
                 }
-                if (u > 0)
-                    mbar_wait(empty0 + 8u * s, uint32_t(u - 1) & 1u, p.status, kStatusTimeout);
-                load_x_quarter(p, b_st, kg, rbl, lane);
-                cp_async_commit();
-#pragma unroll
-                for (int c = 0; c < 8; c++)
-                    sts128(a_st + sw128_offset(arow, uint32_t(c)), q[4 * c], q[4 * c + 1], q[4 * c + 2],
-                           q[4 * c + 3]);
             } else {
-                if (u > 0)
-                    mbar_wait(empty0 + 8u * s, uint32_t(u - 1) & 1u, p.status, kStatusTimeout);
-                load_x_quarter(p, b_st, kg, rbl, lane);
-                const int64_t n = rb * kTileRows + lane;
-                const bool ok = rb_ok && lane < R;
-                const uint16_t *src = ok ? p.w + n * p.cols + kg * kGroup : p.w;
+                const int64_t n = int64_t(rb) * kTileRows + lane;
+                const bool ok = rb_ok && n < p.rows;
+                const uint4 *row = reinterpret_cast<const uint4 *>(p.w + (ok ? n : 0) * p.cols) + size_t(kgA) * 8;
 #pragma unroll
-                for (int c = 0; c < 8; c++)
-                    cp_async16_zfill(a_st + sw128_offset(arow, uint32_t(c)), ok ? src + 8 * c : src, ok ? 16u : 0u);
-                cp_async_commit();
+                for (int c = 0; c < 8; c++) {
+                    const uint4 a = ok ? __ldg(row + c) : make_uint4(0, 0, 0, 0);
+                    const uint4 b = ok && hasB ? __ldg(row + 8 + c) : make_uint4(0, 0, 0, 0);
+                    qA[4 * c] = a.x, qA[4 * c + 1] = a.y, qA[4 * c + 2] = a.z, qA[4 * c + 3] = a.w;
+                    qB[4 * c] = b.x, qB[4 * c + 1] = b.y, qB[4 * c + 2] = b.z, qB[4 * c + 3] = b.w;
+                }
             }
+            // hand the two K steps to the MMA warp once their stages are free
+            const uint32_t sA_ = i0 % uint32_t(S), sB_ = (i0 + 1) % uint32_t(S);
+            const uint32_t uA = i0 / uint32_t(S), uB = (i0 + 1) / uint32_t(S);
+            if (uA > 0)
+                mbar_wait(empty0 + 8u * sA_, (uA - 1) & 1u, p.status, kStatusTimeout);
+            if (hasB && uB > 0)
+                mbar_wait(empty0 + 8u * sB_, (uB - 1) & 1u, p.status, kStatusTimeout);
+            tc_fence_after();
+            tmem_st32(trow + 32u * sA_, qA);
+            load_x_quarter(p, b0 + sA_ * bstage, kgA, rbl, lane);
+            if (hasB) {
+                tmem_st32(trow + 32u * sB_, qB);
+                load_x_quarter(p, b0 + sB_ * bstage, kgA + 1, rbl, lane);
+            }
+            cp_async_commit();
             cp_async_wait_all();
             fence_proxy_async_smem();
+            tmem_st_wait();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(full0 + 8u * s);
+            if (lane == 0) {
+                mbar_arrive(full0 + 8u * sA_);
+                if (hasB)
+                    mbar_arrive(full0 + 8u * sB_);
+            }
         }
+        tile_check_flush(bad, p.status);
     } else if (lane == 0) {  // the MMA warp
         const uint32_t idesc = idesc_bf16_f32(kTcM, Np);
 #pragma unroll 1
-        for (int i = 0; i < nk; i++) {
-            const int s = i % S;
-            mbar_wait(full0 + 8u * s, uint32_t(i / S) & 1u, p.status, kStatusTimeout);
+        for (uint32_t i = 0; i < nk; i++) {
+            const uint32_t s = i % uint32_t(S);
+            mbar_wait(full0 + 8u * s, (i / uint32_t(S)) & 1u, p.status, kStatusTimeout);
             tc_fence_after();
-            const uint32_t a_st = a0 + uint32_t(s) * kAStageBytes, b_st = b0 + uint32_t(s) * bstage;
+            const uint32_t b_st = b0 + s * bstage;
 #pragma unroll
             for (int k = 0; k < 4; k++)
-                mma_bf16(tmem, sdesc_sw128(a_st + 32u * k), sdesc_sw128(b_st + 32u * k), idesc, (i | k) != 0);
+                mma_ts(tmem, tmem + a0col + 32u * s + 8u * k, sdesc_sw128(b_st + 32u * k), idesc, (i | k) != 0);
             mma_commit(empty0 + 8u * s);
         }
         mma_commit(done);
     }
     __syncwarp();
 
-    // epilogue: TMEM lane quarter `warp` holds rows n0 + 32*warp + lane
-    const int64_t n = mb * kTcM + 32 * warp + lane;
+    // epilogue: tensor-memory lane quarter `warp` holds rows n0 + 32*warp + lane
+    const int64_t n = int64_t(mb) * kTcM + 32 * warp + lane;
     if (warp < 4) {
         mbar_wait(done, 0u, p.status, kStatusTimeout);
         tc_fence_after();
 #pragma unroll 1
         for (int c0 = 0; c0 < Np; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(tmem + (uint32_t(32 * warp) << 16) + uint32_t(c0), v);
+            uint32_t vv[16];
+            tmem_ld16(tmem + (uint32_t(32 * warp) << 16) + uint32_t(c0), vv);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; j++) {
                 const int b = c0 + j;
                 if (b < p.batch && n < p.rows) {
-                    const float f = __uint_as_float(v[j]);
+                    const float f = __uint_as_float(vv[j]);
                     if (p.splits == 1)
                         p.y[int64_t(b) * p.rows + n] = __bfloat16_as_ushort(__float2bfloat16_rn(f));
                     else
-                        p.partial[((mb * p.splits + split) * Np + b) * kTcM + 32 * warp + lane] = f;
+                        p.partial[((int64_t(mb) * p.splits + split) * Np + b) * kTcM + 32 * warp + lane] = f;
                 }
             }
         }
@@ -234,7 +330,7 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
     tc_fence_before();
     __syncthreads();
     if (warp == P)
-        tmem_dealloc(tmem, p.tmem_cols);
+        tmem_dealloc(tmem, kTmemCols);
     if (p.splits == 1)
         return;
 
@@ -247,14 +343,16 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
     if (!last_cta)
         return;
     __threadfence();
-    if (warp < 4 && n < p.rows) {
-        for (int b = 0; b < p.batch; b++) {
-            const float *ps = p.partial + (mb * p.splits * Np + b) * kTcM + 32 * warp + lane;
-            float tot = __ldcg(ps);
-            for (int sp = 1; sp < p.splits; sp++)
-                tot += __ldcg(ps + int64_t(sp) * Np * kTcM);
-            p.y[int64_t(b) * p.rows + n] = __bfloat16_as_ushort(__float2bfloat16_rn(tot));
-        }
+    for (int t = threadIdx.x; t < p.batch * kTcM; t += blockDim.x) {
+        const int b = t / kTcM, r = t % kTcM;
+        const int64_t nn = int64_t(mb) * kTcM + r;
+        if (nn >= p.rows)
+            continue;
+        const float *ps = p.partial + (int64_t(mb) * p.splits * Np + b) * kTcM + r;
+        float tot = __ldcg(ps);
+        for (int sp = 1; sp < p.splits; sp++)
+            tot += __ldcg(ps + int64_t(sp) * Np * kTcM);
+        p.y[int64_t(b) * p.rows + nn] = __bfloat16_as_ushort(__float2bfloat16_rn(tot));
     }
     if (threadIdx.x == 0)
         p.counters[mb] = 0;
@@ -270,18 +368,21 @@ uw_status launch_tc_one(const TcParams &p, size_t smem, cudaStream_t stream) {
     return cudaGetLastError() == cudaSuccess ? UW_OK : UW_ERR_CUDA;
 }
 
+// Tensor-memory columns before the A stages (the accumulator's Np, rounded up to 32).
+uint32_t a0_col(int Np) { return (uint32_t(Np) + 31u) & ~31u; }
+
 }  // namespace
 
-size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed, uint32_t tbuf) {
-    size_t s = 1024 + size_t(S) * (kAStageBytes + size_t(Np) * 128);
+size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed, uint32_t tdata) {
+    size_t s = 1024 + size_t(S) * size_t(Np) * 128;
     if (compressed)
-        s += size_t(kCommonSmemBytes) + size_t(4 * G) * 2 * tbuf;
+        s += size_t(kCommonSmemBytes) + 128 + size_t(4 * G) * kPairStages * pair_stage_bytes(tdata);
     return s;
 }
 
-int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tbuf) {
-    int S = kTcMaxStages;
-    while (S > 1 && gemm_tc_smem_bytes(G, S, Np, compressed, tbuf) > size_t(kMaxSmemPerBlock - 1024))
+int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tdata) {
+    int S = std::min<int>(kTcMaxStages, int((kTmemCols - a0_col(Np)) / 32));
+    while (S > 1 && gemm_tc_smem_bytes(G, S, Np, compressed, tdata) > size_t(kMaxSmemPerBlock - 1024))
         S--;
     return S;
 }
@@ -295,26 +396,29 @@ int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits) {
 
 uw_status launch_gemm_tc(const TcParams &base, int G, bool compressed, cudaStream_t stream) {
     const int64_t gpr = base.cols / kGroup;
-    if (base.splits < 1 || base.splits > gpr || (G != 2 && G != 4))
+    if (base.splits < 1 || base.splits > gpr || G < 1 || G > 3)
         return UW_ERR_UNSUPPORTED;
+    if (uint64_t(base.rows / kTileRows + 1) * uint64_t(gpr) >= (uint64_t(1) << 32))
+        return UW_ERR_UNSUPPORTED;  // tile indices are 32-bit
     for (int64_t b0 = 0; b0 < base.batch; b0 += kTcMaxBatch) {
         TcParams p = base;
         p.batch = std::min<int64_t>(kTcMaxBatch, base.batch - b0);
         p.x = base.x + b0 * base.cols;
         p.y = base.y + b0 * base.rows;
         p.Np = int((p.batch + 15) / 16 * 16);
-        p.tmem_cols = 32;
-        while (p.tmem_cols < uint32_t(p.Np))
-            p.tmem_cols <<= 1;
-        p.S = gemm_tc_stages(G, p.Np, compressed, p.v.tbuf);
-        if (p.S < G)
-            return UW_ERR_UNSUPPORTED;
-        const size_t smem = gemm_tc_smem_bytes(G, p.S, p.Np, compressed, p.v.tbuf);
+        p.a0col = a0_col(p.Np);
+        p.tmem_cols = kTmemCols;
+        p.S = gemm_tc_stages(G, p.Np, compressed, p.v.tdata);
+        if (p.S < 2 * G)
+            return UW_ERR_UNSUPPORTED;  // each producer group works on two K steps at once
+        const size_t smem = gemm_tc_smem_bytes(G, p.S, p.Np, compressed, p.v.tdata);
         uw_status s;
-        if (G == 2)
+        if (G == 1)
+            s = compressed ? launch_tc_one<1, true>(p, smem, stream) : launch_tc_one<1, false>(p, smem, stream);
+        else if (G == 2)
             s = compressed ? launch_tc_one<2, true>(p, smem, stream) : launch_tc_one<2, false>(p, smem, stream);
         else
-            s = compressed ? launch_tc_one<4, true>(p, smem, stream) : launch_tc_one<4, false>(p, smem, stream);
+            s = compressed ? launch_tc_one<3, true>(p, smem, stream) : launch_tc_one<3, false>(p, smem, stream);
         if (s != UW_OK)
             return s;
     }

@@ -51,9 +51,10 @@ struct TcParams {
     int splits;
     int S, Np;             // stages, padded batch (set by the launcher)
     uint32_t tmem_cols;    // tensor-memory columns allocated (set by the launcher)
+    uint32_t a0col;        // first tensor-memory column of the A stages (set by the launcher)
 };
-size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed, uint32_t tbuf);
-int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tbuf);
+size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed, uint32_t tdata);
+int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tdata);
 int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits);
 uw_status launch_gemm_tc(const TcParams &p, int G, bool compressed, cudaStream_t stream);
 

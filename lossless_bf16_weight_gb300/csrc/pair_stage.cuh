@@ -1,0 +1,106 @@
+// Staging of tile pairs by the copy engine, shared by the batch-1 GEMV and
+// the tensor-core matmul.
+//
+// A "pair" is the tiles (rb, kg) and (rb, kg+1): they sit next to each other
+// in every section of the blob, so one bulk copy per section brings both --
+// their glen, their code regions followed by their escaped groups' raw
+// exponents, and their sign+mantissa bytes -- into one shared-memory stage,
+// completing on an mbarrier.  A warp keeps kPairStages stages and works one
+// pair ahead.
+#pragma once
+#include <cstdint>
+
+#include "decode.cuh"
+#include "tc.cuh"
+
+namespace uw {
+
+constexpr int kPairStages = 2;
+
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Bytes of one pair stage, and the offset of its sign+mantissa bytes.
+__host__ __device__ constexpr uint32_t pair_stage_bytes(uint32_t tdata) {
+    return (64u + 2u * tdata + 64u + 4096u + 127u) & ~127u;
+}
+__host__ __device__ constexpr uint32_t pair_stage_smoff(uint32_t tdata) { return 64u + 2u * tdata + 64u; }
+
+// Offsets of the pair at tile t (lanes 0..2: tcode[t..t+2], lanes 3..5:
+// tesc[t..t+2]; indices past the table end read its last entry).
+__device__ __forceinline__ uint32_t pair_offsets_load(const BlobView &v, uint32_t t) {
+    const int lane = threadIdx.x & 31;
+    const int l = lane < 6 ? lane : 0;
+    const uint32_t k = t + uint32_t(l % 3);
+    return __ldg((l < 3 ? v.tcode : v.tesc) + (k < v.ntiles ? k : v.ntiles));
+}
+
+// What the decode needs to know about a staged pair (warp-uniform; kept in
+// shared memory next to the stage so that the loop body is not duplicated).
+struct PairMeta {
+    uint32_t pkA, pkB;   // n16 | nesc << 8 | bad << 16 of each tile
+    uint32_t n16A, n16B, nescA, pad[3];
+};
+
+// Validate the pair's offsets `o` and start its bulk copies into stage `st`:
+//   [0, 64)                      glen of A and B (full row blocks only)
+//   [64, 64 + 2*tdata)           code regions of A then B, then escaped exponents of A then B
+//   [smoff, smoff + 128*R)       sign+mantissa bytes of A then B
+// A pair with bad offsets copies no codes and is decoded as zeros (the error
+// is recorded by tile_begin).
+__device__ __forceinline__ void pair_issue(const BlobView &v, uint32_t o, uint32_t rb, uint32_t kgA, bool hasB,
+                                           uint32_t t, uint32_t st, uint32_t smoff, uint32_t bar, PairMeta *meta) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t c0 = __shfl_sync(0xffffffffu, o, 0), c1 = __shfl_sync(0xffffffffu, o, 1);
+    const uint32_t c2r = __shfl_sync(0xffffffffu, o, 2), e0 = __shfl_sync(0xffffffffu, o, 3);
+    const uint32_t e1 = __shfl_sync(0xffffffffu, o, 4), e2r = __shfl_sync(0xffffffffu, o, 5);
+    const uint32_t c2 = hasB ? c2r : c1, e2 = hasB ? e2r : e1;
+    const bool full = rb < v.nfull;
+    const uint32_t R = full ? uint32_t(kTileRows) : v.tail_rows;
+    const uint32_t n16A = c1 - c0, n16B = c2 - c1, nescA = e1 - e0, nescB = e2 - e1;
+    const uint32_t lim16 = uint32_t(kMaxTileCodeBytes / 16);
+    const bool bad = n16A > lim16 || n16B > lim16 || nescA > R || nescB > R || n16A * 16u + nescA * 64u > v.tdata ||
+                     n16B * 16u + nescB * 64u > v.tdata || c2 > v.code16 || e2 > v.n_esc32;
+    if (lane == 0) {
+        meta->pkA = bad ? (1u << 16) : (n16A | (nescA << 8));
+        meta->pkB = !hasB ? 0u : bad ? (1u << 16) : (n16B | (nescB << 8));
+        meta->n16A = bad ? 0u : n16A;
+        meta->n16B = bad ? 0u : n16B;
+        meta->nescA = bad ? 0u : nescA;
+    }
+    const uint32_t ntile = hasB ? 2u : 1u;
+    const uint64_t q0 = uint64_t(t) * kTileRows - (full ? 0u : (kTileRows - R) * kgA);  // first group of A
+    const uint32_t code_bytes = bad ? 0u : (c2 - c0) * 16u;
+    const uint32_t esc_bytes = bad ? 0u : (e2 - e0) * 64u;
+    const uint32_t sm_bytes = uint32_t(kGroup) * R * ntile;
+    const uint32_t glen_bytes = full ? uint32_t(kTileRows) * ntile : 0u;
+    if (lane == 0) {
+        mbar_expect_tx(bar, code_bytes + esc_bytes + sm_bytes + glen_bytes);
+        if (glen_bytes)
+            bulk_g2s(st, v.glen + q0, glen_bytes, bar);
+        if (code_bytes)
+            bulk_g2s(st + 64u, v.code + size_t(c0) * 16, code_bytes, bar);
+        if (esc_bytes)
+            bulk_g2s(st + 64u + code_bytes, v.esc + size_t(e0) * 64, esc_bytes, bar);
+        bulk_g2s(st + smoff, v.sm + q0 * kGroup, sm_bytes, bar);
+    }
+}
+
+
+// The warp's pairs in order: row block by row block, group pairs within
+// [k0, k1).
+struct PairCursor {
+    uint32_t rb, kgA;
+    __device__ __forceinline__ void next(uint32_t k0, uint32_t k1) {
+        kgA += 2;
+        if (kgA >= k1) {
+            kgA = k0;
+            rb++;
+        }
+    }
+};
+
+}  // namespace uw
