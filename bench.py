@@ -41,7 +41,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 ROWS, COLS, BATCH = 14336, 4096, 1
 WORKLOAD = "gate_proj 14336x4096 BF16 N(0,0.02) seed 0, compressed; y = x W^T, batch 1"
-KERNEL_SOURCES = ["decode.cuh", "gemv_kg.cu", "format.h", "kernels.h"]
+KERNEL_SOURCES = ["decode.cuh", "gemv_kg.cu", "pair_stage.cuh", "tc.cuh", "format.h", "kernels.h"]
 
 
 def launch_stats(torch, fn, stream, reps: int = 30, warm: int = 5, flush=None):
@@ -219,6 +219,7 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--plan", default=None,
                     help="fixed plan instead of autotuning: fused:<variant> or decompress:<variant>")
+    ap.add_argument("--batch", type=int, default=BATCH, help="rows of x (the headline workload is batch 1)")
     ap.add_argument("--workloads", default=None,
                     help="instead of the headline line, one line per workload: small,mlp,heavy,model or all")
     return ap.parse_args()
@@ -614,7 +615,11 @@ def e2e_measurement(torch, uw, desc, blobs, x, stream, plan, args):
 
 
 def main():
+    global BATCH, WORKLOAD
     args = parse()
+    if args.batch != BATCH:  # another batch of the same matrix (profiling, context); the headline is batch 1
+        BATCH = args.batch
+        WORKLOAD = WORKLOAD.replace("batch 1", "batch %d" % BATCH)
     if args.workloads:
         run_workloads(args)
     elif args.impl == "reference":

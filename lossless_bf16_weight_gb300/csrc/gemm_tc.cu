@@ -232,6 +232,7 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
                     if ((emB >> lane) & 1u)
                         escaped_pairs(ebB, emB, smB, stride, qB);
                     // the pair stage is free: start the pair kPairStages ahead
+                    fence_proxy_async_smem();
                     __syncwarp();
                     if (nissued < my_pairs) {
                         const uint32_t kgN = kg_lo + 2u * (uint32_t(grp) + nissued * G);

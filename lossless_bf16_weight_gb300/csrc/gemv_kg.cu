@@ -231,7 +231,9 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
             red[((rb_done - rb0) * W + warp) * 32 + lane] = s_w;
             s_w = 0.f;
         }
-        // the stage is free: start the pair kPairStages ahead
+        // the stage is free: start the pair kPairStages ahead (the reads above
+        // come before the copy engine's writes)
+        fence_proxy_async_smem();
         __syncwarp();
         if (nissued < npairs) {
             pair_issue(v, o_next, issue.rb, issue.kgA, issue.kgA + 1 < k1, issue.rb * gpr + issue.kgA, st, smoff, bar,
