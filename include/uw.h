@@ -138,9 +138,11 @@ uw_status uw_decompress(const uw_desc *d, const void *blob_dev, uint16_t *w_dev,
 
 /* uw_matmul -- y = x W^T with W still compressed (the blog's reconstructive
  * matmul, or decompress-then-multiply, as the plan says).
- *   x_dev   [batch, cols] BF16;  y_dev  [batch, rows] BF16 (written).
+ *   x_dev   [batch, cols] BF16, 16-byte aligned;  y_dev  [batch, rows] BF16
+ *           (written).
  *   plan    strategy/variant to run, or NULL for the library's default for
- *           this shape and batch.
+ *           this shape and batch.  A variant whose on-chip buffers do not fit
+ *           this blob or batch returns UW_ERR_UNSUPPORTED without running.
  * The result is bit-identical to uw_matmul_bf16 with the same variant on the
  * original weights. */
 uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uint16_t *x_dev,
@@ -149,7 +151,9 @@ uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uint16_t *x_de
 
 /* uw_matmul_bf16 -- the same kernels fed uncompressed BF16 weights: the
  * baseline that compression is measured against.
- *   w_dev   [rows, cols] BF16 device weights.  variant as in uw_plan. */
+ *   w_dev   [rows, cols] BF16 device weights, x_dev [batch, cols]; both
+ *           16-byte aligned (UW_ERR_INVALID_ARG otherwise).  variant as in
+ *           uw_plan. */
 uw_status uw_matmul_bf16(const uint16_t *w_dev, int64_t rows, int64_t cols,
                          const uint16_t *x_dev, int64_t batch, uint16_t *y_dev,
                          int32_t variant, void *ws_dev, size_t ws_bytes, void *stream);

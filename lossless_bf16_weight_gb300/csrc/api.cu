@@ -452,7 +452,7 @@ extern "C" uw_status uw_decompress(const uw_desc *d, const void *blob_dev, uint1
 
 extern "C" uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uint16_t *x, int64_t batch,
                                uint16_t *y, const uw_plan *plan, void *ws, size_t ws_bytes, void *stream) {
-    if (!d || !blob_dev || !x || !y || !ws || batch <= 0)
+    if (!d || !blob_dev || !x || !y || !ws || batch <= 0 || (reinterpret_cast<uintptr_t>(x) & 15))
         return UW_ERR_INVALID_ARG;
     ResolvedPlan rp;
     uw_status s = resolve_plan(plan, d->rows, d->cols, batch, &rp);
@@ -486,7 +486,8 @@ extern "C" uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uin
 extern "C" uw_status uw_matmul_bf16(const uint16_t *w, int64_t rows, int64_t cols, const uint16_t *x,
                                     int64_t batch, uint16_t *y, int32_t variant, void *ws, size_t ws_bytes,
                                     void *stream) {
-    if (!w || !x || !y || !ws || batch <= 0)
+    if (!w || !x || !y || !ws || batch <= 0 || (reinterpret_cast<uintptr_t>(x) & 15) ||
+        (reinterpret_cast<uintptr_t>(w) & 15))
         return UW_ERR_INVALID_ARG;
     if (rows <= 0 || cols <= 0 || cols % kGroup)
         return UW_ERR_SHAPE;
