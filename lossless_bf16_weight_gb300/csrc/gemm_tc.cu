@@ -85,21 +85,30 @@ __device__ __forceinline__ void load_x_quarter(const TcParams &p, uint32_t b_st,
     }
 }
 
-// An escaped group's 32 BF16 pairs, from its raw exponents and the
-// sign+mantissa bytes in the stage.
-__device__ __forceinline__ void escaped_pairs(uint32_t ebase, uint32_t em, uint32_t sm_lane, uint32_t stride,
-                                              uint32_t (&q)[32]) {
-    uint4 e[4], sm[4];
+// An escaped group's 32 BF16 pairs, from its raw exponents (in the pair
+// stage) and its four sign+mantissa chunks.
+__device__ __forceinline__ void escaped_pairs(uint32_t ebase, uint32_t em, const uint4 (&sm)[4], uint32_t (&q)[32]) {
+    uint4 e[4];
     escape_read(ebase, em, e);
-#pragma unroll
-    for (int c = 0; c < 4; c++)
-        sm[c] = lds128(sm_lane + uint32_t(c) * stride);
 #pragma unroll
     for (int I = 0; I < 32; I++)
         q[I] = escape_pair(e, I, sm_word(sm, I >> 1));
 }
 
-template <int G, bool kCompressed>
+// The four sign+mantissa chunks of a lane's row: from the pair stage in
+// shared memory, or from global memory.
+__device__ __forceinline__ void sm_chunks(uint32_t s_lane, uint32_t stride, uint4 (&sm)[4]) {
+#pragma unroll
+    for (int c = 0; c < 4; c++)
+        sm[c] = lds128(s_lane + uint32_t(c) * stride);
+}
+__device__ __forceinline__ void sm_chunks(const uint8_t *g_lane, uint32_t stride, uint4 (&sm)[4]) {
+#pragma unroll
+    for (int c = 0; c < 4; c++)
+        sm[c] = __ldg(reinterpret_cast<const uint4 *>(g_lane + c * stride));
+}
+
+template <int G, bool kCompressed, bool kSmStaged>
 __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcParams p) {
     constexpr int P = 4 * G;  // producer warps
     extern __shared__ unsigned char smem_raw[];
@@ -128,7 +137,9 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
     unsigned char *dec = smem_raw + pad + size_t(S) * bstage;
     const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[kTcMaxStages]);
     const uint32_t done = smem_addr(&bars[2 * kTcMaxStages]);
-    const uint32_t sbytes = pair_stage_bytes(v.tdata), smoff = pair_stage_smoff(v.tdata);
+    // pair stages: with the sign+mantissa bytes (kSmStaged) or codes only
+    const uint32_t sbytes = kSmStaged ? pair_stage_bytes(v.tdata) : code_stage_bytes(v.tdata);
+    const uint32_t smoff = pair_stage_smoff(v.tdata);
     const uint32_t pst0 = (smem_addr(dec + kCommonSmemBytes) + 127u) & ~127u;
 
     if (warp == P)
@@ -162,8 +173,12 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
             o_next = pair_offsets_load(v, rb * gpr + kg_lo + 2u * uint32_t(grp));
             for (int s = 0; s < kPairStages && nissued < my_pairs; s++) {
                 const uint32_t kgA = kg_lo + 2u * (uint32_t(grp) + nissued * G);
-                pair_issue(v, o_next, rb, kgA, kgA + 1 < kg_hi, rb * gpr + kgA, st0 + uint32_t(s) * sbytes, smoff,
-                           pbar0 + 8u * s, meta + s);
+                if constexpr (kSmStaged)
+                    pair_issue(v, o_next, rb, kgA, kgA + 1 < kg_hi, rb * gpr + kgA, st0 + uint32_t(s) * sbytes, smoff,
+                               pbar0 + 8u * s, meta + s);
+                else
+                    pair_issue_codes(v, o_next, rb, kgA, kgA + 1 < kg_hi, rb * gpr + kgA, st0 + uint32_t(s) * sbytes,
+                                     pbar0 + 8u * s, meta + s);
                 nissued++;
                 if (nissued < my_pairs)
                     o_next = pair_offsets_load(v, rb * gpr + kg_lo + 2u * (uint32_t(grp) + nissued * G));
@@ -182,6 +197,17 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
                                                                   : int(v.tail_rows);
         const uint32_t trow = tmem + (uint32_t(32 * rbl) << 16) + a0col;
         uint32_t bad = 0;
+        // sign+mantissa bytes of the current pair, and its chunk 0 in registers
+        const uint8_t *sm_cur = nullptr;
+        uint4 c0A = make_uint4(0, 0, 0, 0), c0B = c0A;
+        if (kCompressed && !kSmStaged && rb_ok && my_pairs > 0) {
+            uint32_t R0;
+            const uint32_t kg0 = kg_lo + 2u * uint32_t(grp);
+            sm_cur = pair_sm_base(v, rb, kg0, rb * gpr + kg0, R0);
+            const uint8_t *a = sm_cur + 16u * (uint32_t(lane) < R0 ? uint32_t(lane) : 0u);
+            c0A = __ldg(reinterpret_cast<const uint4 *>(a));
+            c0B = __ldg(reinterpret_cast<const uint4 *>(kg0 + 1 < kg_hi ? a + 64u * R0 : a));
+        }
 #pragma unroll 1
         for (uint32_t j = 0; j < my_pairs; j++) {
             const uint32_t pi = uint32_t(grp) + j * G;  // pair index in the CTA's K range
@@ -210,14 +236,38 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
                     const uint32_t emA = tile_begin_ready(ds, TileMeta{gA, 0u, m.pkA}, R, cA, la, p.status);
                     const uint32_t emB = tile_begin_ready(ds, TileMeta{gB, 0u, m.pkB}, hasB ? R : 0, cB, lb, p.status);
                     const uint32_t ebA = cA + 16u * (m.n16A + m.n16B), ebB = ebA + 64u * m.nescA;
+                    // sign+mantissa bytes straight from L2 (prefetched there with the codes), one
+                    // 16-byte chunk ahead; chunk 0 of this pair was loaded during the previous one
                     const uint32_t stride = 16u * uint32_t(R);
+                    const uint32_t lc = uint32_t(lane) < uint32_t(R) ? uint32_t(lane) : 0u;
+                    const uint8_t *gA_sm = sm_cur + 16u * lc, *gB_sm = hasB ? gA_sm + 64u * uint32_t(R) : gA_sm;
+                    const bool more = j + 1 < my_pairs;
+                    uint32_t Rn = 0;
+                    const uint32_t kgN1 = kgA + 2u * G;
+                    const uint8_t *sm_nxt = !kSmStaged && more ? pair_sm_base(v, rb, kgN1, rb * gpr + kgN1, Rn) : sm_cur;
                     const uint32_t smA = st + smoff + 16u * uint32_t(lane), smB = smA + 64u * uint32_t(R);
-                    uint4 sA = lds128(smA), sB = lds128(smB), nA = sA, nB = sB;
+                    uint4 sA = c0A, sB = c0B;
+                    if constexpr (kSmStaged) {
+                        sA = lds128(smA);
+                        sB = lds128(smB);
+                    }
+                    uint4 nA = sA, nB = sB;
 #pragma unroll
                     for (int I = 0; I < 32; I++) {
-                        if ((I & 7) == 0 && I < 24) {
-                            nA = lds128(smA + uint32_t((I >> 3) + 1) * stride);
-                            nB = lds128(smB + uint32_t((I >> 3) + 1) * stride);
+                        if ((I & 7) == 0) {
+                            if constexpr (kSmStaged) {
+                                if (I < 24) {
+                                    nA = lds128(smA + uint32_t((I >> 3) + 1) * stride);
+                                    nB = lds128(smB + uint32_t((I >> 3) + 1) * stride);
+                                }
+                            } else if (I < 24) {
+                                nA = __ldg(reinterpret_cast<const uint4 *>(gA_sm + uint32_t((I >> 3) + 1) * stride));
+                                nB = __ldg(reinterpret_cast<const uint4 *>(gB_sm + uint32_t((I >> 3) + 1) * stride));
+                            } else if (more) {
+                                const uint8_t *a = sm_nxt + 16u * lc;
+                                nA = __ldg(reinterpret_cast<const uint4 *>(a));
+                                nB = __ldg(reinterpret_cast<const uint4 *>(kgN1 + 1 < kg_hi ? a + 64u * Rn : a));
+                            }
                         }
                         qA[I] = decode_pair(la, lut, I, word4(sA, (I >> 1) & 3));
                         qB[I] = decode_pair(lb, lut, I, word4(sB, (I >> 1) & 3));
@@ -227,16 +277,35 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
                         }
                     }
                     bad |= tile_check_bits(la) | tile_check_bits(lb);
-                    if ((emA >> lane) & 1u)
-                        escaped_pairs(ebA, emA, smA, stride, qA);
-                    if ((emB >> lane) & 1u)
-                        escaped_pairs(ebB, emB, smB, stride, qB);
+                    if ((emA | emB) & (1u << lane)) {
+                        uint4 smc[4];
+                        if ((emA >> lane) & 1u) {
+                            if constexpr (kSmStaged)
+                                sm_chunks(smA, stride, smc);
+                            else
+                                sm_chunks(gA_sm, stride, smc);
+                            escaped_pairs(ebA, emA, smc, qA);
+                        }
+                        if ((emB >> lane) & 1u) {
+                            if constexpr (kSmStaged)
+                                sm_chunks(smB, stride, smc);
+                            else
+                                sm_chunks(gB_sm, stride, smc);
+                            escaped_pairs(ebB, emB, smc, qB);
+                        }
+                    }
+                    c0A = sA;  // chunk 0 of the next pair
+                    c0B = sB;
+                    sm_cur = sm_nxt;
                     // the pair stage is free: start the pair kPairStages ahead
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (nissued < my_pairs) {
                         const uint32_t kgN = kg_lo + 2u * (uint32_t(grp) + nissued * G);
-                        pair_issue(v, o_next, rb, kgN, kgN + 1 < kg_hi, rb * gpr + kgN, st, smoff, pb, meta + s);
+                        if constexpr (kSmStaged)
+                            pair_issue(v, o_next, rb, kgN, kgN + 1 < kg_hi, rb * gpr + kgN, st, smoff, pb, meta + s);
+                        else
+                            pair_issue_codes(v, o_next, rb, kgN, kgN + 1 < kg_hi, rb * gpr + kgN, st, pb, meta + s);
                         nissued++;
                         if (nissued < my_pairs)
                             o_next = pair_offsets_load(v, rb * gpr + kg_lo + 2u * (uint32_t(grp) + nissued * G));
@@ -359,9 +428,9 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
         p.counters[mb] = 0;
 }
 
-template <int G, bool kCompressed>
+template <int G, bool kCompressed, bool kSmStaged>
 uw_status launch_tc_one(const TcParams &p, size_t smem, cudaStream_t stream) {
-    auto kern = gemm_tc_kernel<G, kCompressed>;
+    auto kern = gemm_tc_kernel<G, kCompressed, kSmStaged>;
     if (!ensure_smem(kern, smem))
         return UW_ERR_CUDA;
     const dim3 grid(unsigned((p.rows + kTcM - 1) / kTcM), unsigned(p.splits));
@@ -372,21 +441,30 @@ uw_status launch_tc_one(const TcParams &p, size_t smem, cudaStream_t stream) {
 // Tensor-memory columns before the A stages (the accumulator's Np, rounded up to 32).
 uint32_t a0_col(int Np) { return (uint32_t(Np) + 31u) & ~31u; }
 
-}  // namespace
-
-size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed, uint32_t tdata) {
+// Shared memory of a launch; `staged`: the producers' pair stages hold the
+// sign+mantissa bytes too (otherwise the producers read those from L2).
+size_t tc_smem(int G, int S, int Np, bool compressed, bool staged, uint32_t tdata) {
     size_t s = 1024 + size_t(S) * size_t(Np) * 128;
     if (compressed)
-        s += size_t(kCommonSmemBytes) + 128 + size_t(4 * G) * kPairStages * pair_stage_bytes(tdata);
+        s += size_t(kCommonSmemBytes) + 128 +
+             size_t(4 * G) * kPairStages * (staged ? pair_stage_bytes(tdata) : code_stage_bytes(tdata));
     return s;
 }
 
-int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tdata) {
+int tc_stages(int G, int Np, bool compressed, bool staged, uint32_t tdata) {
     int S = std::min<int>(kTcMaxStages, int((kTmemCols - a0_col(Np)) / 32));
-    while (S > 1 && gemm_tc_smem_bytes(G, S, Np, compressed, tdata) > size_t(kMaxSmemPerBlock - 1024))
+    while (S > 1 && tc_smem(G, S, Np, compressed, staged, tdata) > size_t(kMaxSmemPerBlock - 1024))
         S--;
     return S;
 }
+
+}  // namespace
+
+size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed, uint32_t tdata) {
+    return tc_smem(G, S, Np, compressed, false, tdata);
+}
+
+int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tdata) { return tc_stages(G, Np, compressed, false, tdata); }
 
 int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits) {
     if (splits <= 1)
@@ -409,17 +487,26 @@ uw_status launch_gemm_tc(const TcParams &base, int G, bool compressed, cudaStrea
         p.Np = int((p.batch + 15) / 16 * 16);
         p.a0col = a0_col(p.Np);
         p.tmem_cols = kTmemCols;
-        p.S = gemm_tc_stages(G, p.Np, compressed, p.v.tdata);
+        // stage the sign+mantissa bytes in shared memory when that leaves each
+        // producer group its two K steps (and some slack); read them from L2 otherwise
+        bool staged = compressed && tc_stages(G, p.Np, true, true, p.v.tdata) >= 2 * G + 2;
+        p.S = tc_stages(G, p.Np, compressed, staged, p.v.tdata);
         if (p.S < 2 * G)
             return UW_ERR_UNSUPPORTED;  // each producer group works on two K steps at once
-        const size_t smem = gemm_tc_smem_bytes(G, p.S, p.Np, compressed, p.v.tdata);
+        const size_t smem = tc_smem(G, p.S, p.Np, compressed, staged, p.v.tdata);
         uw_status s;
-        if (G == 1)
-            s = compressed ? launch_tc_one<1, true>(p, smem, stream) : launch_tc_one<1, false>(p, smem, stream);
-        else if (G == 2)
-            s = compressed ? launch_tc_one<2, true>(p, smem, stream) : launch_tc_one<2, false>(p, smem, stream);
+        if (!compressed)
+            s = G == 1 ? launch_tc_one<1, false, false>(p, smem, stream)
+                : G == 2 ? launch_tc_one<2, false, false>(p, smem, stream)
+                         : launch_tc_one<3, false, false>(p, smem, stream);
+        else if (staged)
+            s = G == 1 ? launch_tc_one<1, true, true>(p, smem, stream)
+                : G == 2 ? launch_tc_one<2, true, true>(p, smem, stream)
+                         : launch_tc_one<3, true, true>(p, smem, stream);
         else
-            s = compressed ? launch_tc_one<3, true>(p, smem, stream) : launch_tc_one<3, false>(p, smem, stream);
+            s = G == 1 ? launch_tc_one<1, true, false>(p, smem, stream)
+                : G == 2 ? launch_tc_one<2, true, false>(p, smem, stream)
+                         : launch_tc_one<3, true, false>(p, smem, stream);
         if (s != UW_OK)
             return s;
     }

@@ -90,6 +90,63 @@ __device__ __forceinline__ void pair_issue(const BlobView &v, uint32_t o, uint32
 }
 
 
+// Code stage of a pair without its sign+mantissa bytes:
+//   [0, 64)                      glen of A and B (full row blocks only)
+//   [64, 64 + 2*tdata)           code regions of A then B, then escaped exponents of A then B
+//   then 64 bytes of read slack
+__host__ __device__ constexpr uint32_t code_stage_bytes(uint32_t tdata) {
+    return (64u + 2u * tdata + 64u + 127u) & ~127u;
+}
+
+// First byte of the pair's sign+mantissa bytes (tile A's; tile B's follow
+// 64 * R bytes later) and R.
+__device__ __forceinline__ const uint8_t *pair_sm_base(const BlobView &v, uint32_t rb, uint32_t kgA, uint32_t t,
+                                                       uint32_t &R) {
+    const bool full = rb < v.nfull;
+    R = full ? uint32_t(kTileRows) : v.tail_rows;
+    const uint64_t q0 = uint64_t(t) * kTileRows - (full ? 0u : (kTileRows - R) * kgA);
+    return v.sm + q0 * kGroup;
+}
+
+// pair_issue without the sign+mantissa bytes (the caller reads those from
+// global memory), plus an L2 prefetch of them.
+__device__ __forceinline__ void pair_issue_codes(const BlobView &v, uint32_t o, uint32_t rb, uint32_t kgA, bool hasB,
+                                                 uint32_t t, uint32_t st, uint32_t bar, PairMeta *meta) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t c0 = __shfl_sync(0xffffffffu, o, 0), c1 = __shfl_sync(0xffffffffu, o, 1);
+    const uint32_t c2r = __shfl_sync(0xffffffffu, o, 2), e0 = __shfl_sync(0xffffffffu, o, 3);
+    const uint32_t e1 = __shfl_sync(0xffffffffu, o, 4), e2r = __shfl_sync(0xffffffffu, o, 5);
+    const uint32_t c2 = hasB ? c2r : c1, e2 = hasB ? e2r : e1;
+    uint32_t R;
+    const uint8_t *sm = pair_sm_base(v, rb, kgA, t, R);
+    const bool full = rb < v.nfull;
+    const uint32_t n16A = c1 - c0, n16B = c2 - c1, nescA = e1 - e0, nescB = e2 - e1;
+    const uint32_t lim16 = uint32_t(kMaxTileCodeBytes / 16);
+    const bool bad = n16A > lim16 || n16B > lim16 || nescA > R || nescB > R || n16A * 16u + nescA * 64u > v.tdata ||
+                     n16B * 16u + nescB * 64u > v.tdata || c2 > v.code16 || e2 > v.n_esc32;
+    const uint32_t ntile = hasB ? 2u : 1u;
+    const uint64_t q0 = uint64_t(sm - v.sm) / kGroup;
+    const uint32_t code_bytes = bad ? 0u : (c2 - c0) * 16u;
+    const uint32_t esc_bytes = bad ? 0u : (e2 - e0) * 64u;
+    const uint32_t glen_bytes = full ? uint32_t(kTileRows) * ntile : 0u;
+    if (lane == 0) {
+        meta->pkA = bad ? (1u << 16) : (n16A | (nescA << 8));
+        meta->pkB = !hasB ? 0u : bad ? (1u << 16) : (n16B | (nescB << 8));
+        meta->n16A = bad ? 0u : n16A;
+        meta->n16B = bad ? 0u : n16B;
+        meta->nescA = bad ? 0u : nescA;
+        mbar_expect_tx(bar, code_bytes + esc_bytes + glen_bytes);
+        if (glen_bytes)
+            bulk_g2s(st, v.glen + q0, glen_bytes, bar);
+        if (code_bytes)
+            bulk_g2s(st + 64u, v.code + size_t(c0) * 16, code_bytes, bar);
+        if (esc_bytes)
+            bulk_g2s(st + 64u + code_bytes, v.esc + size_t(e0) * 64, esc_bytes, bar);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(sm), "r"(uint32_t(kGroup) * R * ntile)
+                     : "memory");
+    }
+}
+
 // The warp's pairs in order: row block by row block, group pairs within
 // [k0, k1).
 struct PairCursor {
