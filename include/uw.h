@@ -83,7 +83,7 @@ typedef struct {
     uint64_t n_escaped;      /* groups stored with raw exponents              */
     uint64_t n_tiles;        /* ceil(rows / 32) * cols / 64                   */
     int32_t n_palette;       /* palette entries in use (0..16)                */
-    int32_t lmax;            /* longest code length (6 in format version 1)   */
+    int32_t lmax;            /* longest code length (5 in format version 2)   */
     uint8_t palette[16];     /* exponent value of each symbol                 */
     uint8_t code_len[16];    /* code length of each symbol, 0 = unused        */
     uint64_t off_sm, off_glen, off_tcode, off_tesc, off_code, off_esc;

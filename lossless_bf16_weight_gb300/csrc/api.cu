@@ -286,14 +286,14 @@ void fill_blob_view(const uw_desc &d, const void *blob_dev, BlobView *v) {
     v->cols = d.cols;
     uint16_t code[16];
     canonical_code_values(d.code_len, code);
-    std::memset(v->prefix6, 0, sizeof v->prefix6);
+    std::memset(v->prefix, 0, sizeof v->prefix);
     for (int s = 0; s < d.n_palette; s++) {
         const int l = d.code_len[s];
         if (!l)
             continue;
-        const int lo = code[s] << (6 - l), hi = (code[s] + 1) << (6 - l);
-        for (int p = lo; p < hi && p < 64; p++)
-            v->prefix6[p] = uint16_t((d.palette[s] << 4) | l);
+        const int lo = code[s] << (kLmax - l), hi = (code[s] + 1) << (kLmax - l);
+        for (int p = lo; p < hi && p < kPrefixEntries; p++)
+            v->prefix[p] = uint16_t((d.palette[s] << 4) | l);
     }
 }
 

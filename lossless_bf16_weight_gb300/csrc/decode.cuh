@@ -11,12 +11,16 @@
 //     group its rank among the tile's escaped groups;
 //   * read as little-endian 32-bit words, stream bit i is bit i%32 of word
 //     i/32, so a funnel shift right brings the next bits to the bottom;
-//   * every step looks up a 12-bit window in a 4096-entry table that decodes
-//     two codes at once (codes are at most 6 bits).  An entry holds both
+//   * every step looks up a 10-bit window in a 1024-entry table that decodes
+//     two codes at once (codes are at most 5 bits).  An entry holds both
 //     exponents already in BF16 position (bits 14..7 and 30..23) and the bits
-//     the two codes take (bits 3..0).  The funnel shift starts two bits early
-//     so that the window arrives multiplied by 4, i.e. as the entry's byte
-//     offset;
+//     the two codes take (bits 3..0).  The funnel shift starts kShift bits
+//     early so that the window arrives pre-scaled: by 4 (kShift = 2) to index
+//     one shared table, or by 128 (kShift = 7) to index 32 lane-private
+//     copies of it, copy l holding entry w at word 32*w + l.  Lane l then
+//     always reads bank l, so a lookup is a single shared-memory wavefront
+//     whatever the 32 windows are (one shared table costs about four: the
+//     windows are random);
 //   * the exponent pair is merged with two raw sign+mantissa bytes by one
 //     byte permute (sign-replicating) and one three-input logic op, giving
 //     two BF16 weights in one 32-bit register (the blog's reconstruction:
@@ -43,6 +47,8 @@ enum StatusFlag : uint32_t {
     kStatusTimeout = 8u,    // a bounded wait gave up
 };
 
+constexpr int kPrefixEntries = 1 << kLmax;
+
 // Device view of a blob (pointers into the device copy) plus the small
 // tables the host derives from the header.
 struct BlobView {
@@ -63,63 +69,89 @@ struct BlobView {
     uint32_t tail_rows;   // rows of the last, partial block (0: none)
     uint32_t ntiles;      // tiles (the tile tables hold ntiles + 1 entries)
     int64_t rows, cols;
-    // 6-bit prefix -> (exponent << 4) | code length; 0 where no code starts
-    // with that prefix.
-    uint16_t prefix6[64];
+    // kLmax-bit prefix -> (exponent << 4) | code length; 0 where no code
+    // starts with that prefix.
+    uint16_t prefix[kPrefixEntries];
 };
 
-constexpr int kLutEntries = 4096;
+constexpr int kWindowBits = 2 * kLmax;                     // two codes always fit
+constexpr int kLutEntries = 1 << kWindowBits;              // 1024
+constexpr int kPrivateLutBytes = kLutEntries * 32 * 4;     // 32 lane-private copies: 128 KB
 constexpr int kZeroWords = 32;                             // zero stream for lanes without codes
 // One tile's shared buffer: its code region, then the raw exponent bytes of
 // its escaped groups ((32 - e) * 48 + 64 * e <= 2048 bytes), then read
 // slack.  Buffers are sized for the largest tile of the blob at hand.
 constexpr uint32_t kMaxTileData = 2048;
 constexpr uint32_t kTileSlack = 64;
-constexpr int kCommonSmemBytes = kLutEntries * 4 + kZeroWords * 4 + 64 * 2;
+constexpr int kCommonSmemBytes = kLutEntries * 4 + kZeroWords * 4 + kPrefixEntries * 2;
 
 // Shared memory common to every decoding CTA.  The tile buffers must come
 // after it: a lane whose codes start on a word boundary begins reading one
 // word before its buffer.
 struct DecodeShared {
-    uint32_t *lut;       // [4096] pair table
+    uint32_t *lut;       // [1024] pair table (or, when built private, 32 copies elsewhere)
     uint32_t *zero;      // [32]   zero bytes: the stream of lanes without codes
-    uint16_t *prefix6;   // [64]
+    uint16_t *prefix;    // [32]
 };
 
 __device__ __forceinline__ DecodeShared carve_common(unsigned char *smem) {
     DecodeShared s;
     s.lut = reinterpret_cast<uint32_t *>(smem);
     s.zero = s.lut + kLutEntries;
-    s.prefix6 = reinterpret_cast<uint16_t *>(s.zero + kZeroWords);
+    s.prefix = reinterpret_cast<uint16_t *>(s.zero + kZeroWords);
     return s;
+}
+
+// Table entry of window w.  The window holds stream bits in order from bit
+// 0; codes enter the stream most significant bit first, so the code-order
+// window is w reversed.
+__device__ __forceinline__ uint32_t pair_entry(const uint16_t *prefix, uint32_t w) {
+    const uint32_t r = __brev(w) >> (32 - kWindowBits);
+    const uint32_t a = prefix[r >> kLmax];
+    const uint32_t la = a & 15u;
+    uint32_t entry = 0;
+    if (la) {
+        const uint32_t r2 = (r << la) & uint32_t(kLutEntries - 1);
+        const uint32_t b = prefix[r2 >> kLmax];
+        const uint32_t lb = b & 15u;
+        if (lb)
+            entry = ((b >> 4) << 23) | ((a >> 4) << 7) | (la + lb);
+    }
+    return entry;
+}
+
+__device__ __forceinline__ void build_prefix_zero(const DecodeShared &s, const BlobView &v) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    for (int i = tid; i < kPrefixEntries; i += nt)
+        s.prefix[i] = v.prefix[i];
+    for (int i = tid; i < kZeroWords; i += nt)
+        s.zero[i] = 0u;
+    __syncthreads();
 }
 
 // Fill the pair table and the zero stream.  Must be followed by
 // __syncthreads() before use.
 __device__ __forceinline__ void build_tables(const DecodeShared &s, const BlobView &v) {
-    const int tid = threadIdx.x, nt = blockDim.x;
-    for (int i = tid; i < 64; i += nt)
-        s.prefix6[i] = v.prefix6[i];
-    for (int i = tid; i < kZeroWords; i += nt)
-        s.zero[i] = 0u;
+    build_prefix_zero(s, v);
+    for (int w = threadIdx.x; w < kLutEntries; w += blockDim.x)
+        s.lut[w] = pair_entry(s.prefix, uint32_t(w));
+}
+
+// The same with the pair table as 32 lane-private copies at shared address
+// `priv` (kPrivateLutBytes, 16-byte aligned; entry w of copy l at word
+// 32*w + l) for decode_pair<kShiftPrivate>.  Must be followed by
+// __syncthreads() before use.
+__device__ __forceinline__ void build_tables_private(const DecodeShared &s, const BlobView &v, uint32_t priv) {
+    build_tables(s, v);  // the 1024 entries once, in s.lut
     __syncthreads();
-    // Window w holds stream bits in order from bit 0; codes enter the stream
-    // most significant bit first, so the code-order window is w reversed.
-    for (int w = tid; w < kLutEntries; w += nt) {
-        const uint32_t r = __brev(uint32_t(w)) >> 20;
-        const uint32_t a = s.prefix6[r >> 6];
-        const uint32_t la = a & 15u;
-        uint32_t entry = 0;
-        if (la) {
-            const uint32_t r2 = (r << la) & 0xFFFu;
-            const uint32_t b = s.prefix6[r2 >> 6];
-            const uint32_t lb = b & 15u;
-            if (lb)
-                entry = ((b >> 4) << 23) | ((a >> 4) << 7) | (la + lb);
-        }
-        s.lut[w] = entry;
+    for (int i = threadIdx.x; i < kLutEntries * 8; i += blockDim.x) {
+        const uint32_t e = s.lut[uint32_t(i) >> 3];
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" :: "r"(priv + 16u * uint32_t(i)), "r"(e) : "memory");
     }
 }
+
+constexpr int kShiftShared = 2;   // window x 4: byte offset into one table
+constexpr int kShiftPrivate = 7;  // window x 128: byte offset of the entry's row of 32 copies
 
 // PTX prmt in its generic mode: a selector nibble with bit 3 set fills the
 // target byte with the sign bit of the selected byte.
@@ -291,9 +323,10 @@ __device__ __forceinline__ void tile_fetch(const BlobView &v, const TileLoc &L, 
 
 // Per-tile, per-lane decode state.  Addresses are 32-bit shared addresses.
 // With P the shared-memory bit address of the next code bit and lo the word
-// at byte address A, the low five bits of c are P - 8A - 2: the funnel shift
-// by c puts the next 12 stream bits at bits 2..13.  c only grows; bit 5
-// flips whenever the window moves past a word.
+// at byte address A, the low five bits of c are P - 8A - kShift, P - 8A in
+// [kShift, kShift + 32): the funnel shift by c puts the next 10 stream bits
+// at bits kShift .. kShift+9.  c only grows; bit 5 flips whenever the window
+// moves past a word.
 struct LaneStream {
     uint32_t lo, hi, nx;   // current, next and (already loaded) following stream word
     uint32_t c;            // see above; low 7 bits exact
@@ -305,8 +338,10 @@ struct LaneStream {
 // Returns the mask of lanes whose group is escaped (0 for a bad tile, whose
 // lanes all decode the zero stream; the error is recorded in *status).
 // tile_begin for data already in shared memory (nothing to wait for).
+template <int kShift = kShiftShared>
 __device__ __forceinline__ uint32_t tile_begin_ready(const DecodeShared &s, const TileMeta &m, int R, uint32_t cbuf,
                                                      LaneStream &ls, uint32_t *status) {
+    static_assert(kShift >= 0 && kShift <= 8, "a stream starting at byte 1..3 of a word must have P - 8A >= kShift");
     const int lane = threadIdx.x & 31;
     const bool valid = lane < R;
     const uint32_t n16 = m.pk & 0xFFu, nesc = (m.pk >> 8) & 0xFFu;
@@ -326,10 +361,10 @@ __device__ __forceinline__ uint32_t tile_begin_ready(const DecodeShared &s, cons
     if (bad && lane == 0)
         atomicOr(status, over ? kStatusBadTile : kStatusBadEscape);
     const bool coded = !bad && g != 0;
-    // a stream starting on a word boundary begins one word early (c = 30)
+    // a stream starting on a word boundary begins one word early (P - 8A = 32)
     const uint32_t sub = (off & 3u) ? 0u : 4u;
     const uint32_t w0 = coded ? cbuf + (off & ~3u) - sub : smem_addr(s.zero);
-    const uint32_t c0 = (8u * (off & 3u) - 2u) & 31u;
+    const uint32_t c0 = (8u * (off & 3u) - uint32_t(kShift)) & 31u;
     ls.lo = lds32(w0);
     ls.hi = lds32(w0 + 4);
     ls.nx = lds32(w0 + 8);
@@ -343,7 +378,7 @@ __device__ __forceinline__ uint32_t tile_begin(const DecodeShared &s, const Tile
                                                LaneStream &ls, uint32_t *status) {
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
-    return tile_begin_ready(s, m, R, cbuf, ls, status);
+    return tile_begin_ready<kShiftShared>(s, m, R, cbuf, ls, status);
 }
 
 // Shared address of a fetched tile's raw escape bytes (after its codes).
@@ -365,10 +400,12 @@ __device__ __forceinline__ void escape_read(uint32_t ebase, uint32_t esc_mask, u
 
 // One step: decode the exponents of weights 2i, 2i+1 and merge them with the
 // sign+mantissa bytes.  `sm4` holds the bytes of weights 4*(i/2)..+3; `lut`
-// is the shared address of the pair table.  `I` is a compile-time constant
-// once the caller's 32-step loop is unrolled.
+// is the shared address of the pair table (kShiftShared), or of the lane's
+// column of the private copies, i.e. their base + 4 * lane (kShiftPrivate).
+// `I` is a compile-time constant once the caller's 32-step loop is unrolled.
+template <int kShift = kShiftShared>
 __device__ __forceinline__ uint32_t decode_pair(LaneStream &ls, uint32_t lut, int I, uint32_t sm4) {
-    // window*4 = funnel(lo, hi) >> c, bits 2..13; entry = table[window];
+    // window << kShift = funnel(lo, hi) >> c, masked; entry = table[window];
     // c += entry (its bits above 6 only add junk above the exact low 7);
     // when bit 5 of c flips the window has moved into the next word: shift
     // the words and load the one after, predicated rather than branched.  The
@@ -380,7 +417,7 @@ __device__ __forceinline__ uint32_t decode_pair(LaneStream &ls, uint32_t lut, in
         ".reg .b32 win, addr, c2, t;\n\t"
         ".reg .pred p;\n\t"
         "shf.r.wrap.b32 win, %1, %2, %4;\n\t"
-        "and.b32 win, win, 16380;\n\t"
+        "and.b32 win, win, %7;\n\t"
         "add.u32 addr, win, %6;\n\t"
         "ld.shared.u32 %0, [addr];\n\t"
         "add.u32 c2, %0, %4;\n\t"
@@ -394,7 +431,7 @@ __device__ __forceinline__ uint32_t decode_pair(LaneStream &ls, uint32_t lut, in
         "mov.b32 %4, c2;\n\t"
         "}"
         : "=r"(ent), "+r"(ls.lo), "+r"(ls.hi), "+r"(ls.nx), "+r"(ls.c), "+r"(ls.wp)
-        : "r"(lut)
+        : "r"(lut), "n"((kLutEntries - 1) << kShift)
         : "memory");
     // sign-replicate byte permute: bytes (b0, sign(b0), b1, sign(b1)) for the
     // even pair of the word, (b2, sign(b2), b3, sign(b3)) for the odd one

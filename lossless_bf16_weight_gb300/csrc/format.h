@@ -21,7 +21,7 @@
 // chunk index c, so that 32 lanes loading chunk c read 512 contiguous bytes.
 //
 // Codes: canonical, assigned in (length, palette index) order, at most
-// kLmax = 6 bits so that a 12-bit window holds two codes.  Bit order: the
+// kLmax = 5 bits so that a 10-bit window holds two codes.  Bit order: the
 // code stream fills each byte from bit 0 up (stream bit i = bit i%8 of byte
 // i/8), each code entering most significant bit first; read as 32-bit
 // little-endian words, stream bit i is bit i%32 of word i/32.
@@ -31,15 +31,15 @@
 namespace uw {
 
 constexpr uint32_t kMagic = 0x31425755u;  // "UWB1"
-constexpr uint32_t kVersion = 1;
+constexpr uint32_t kVersion = 2;  // 2: codes of at most 5 bits
 constexpr int kGroup = 64;
 constexpr int kTileRows = 32;
-constexpr int kLmax = 6;
+constexpr int kLmax = 5;
 constexpr int kPalette = 16;
 constexpr int kHeaderBytes = 256;
 constexpr int kSectionAlign = 256;
-constexpr int kMaxGroupCodeBytes = kGroup * kLmax / 8;            // 48
-constexpr int kMaxTileCodeBytes = kTileRows * kMaxGroupCodeBytes;  // 1536 (multiple of 16)
+constexpr int kMaxGroupCodeBytes = kGroup * kLmax / 8;            // 40
+constexpr int kMaxTileCodeBytes = kTileRows * kMaxGroupCodeBytes;  // 1280 (multiple of 16)
 
 namespace hdr {
 constexpr int magic = 0, version = 4, rows = 8, cols = 16, group = 24, tile_rows = 28,

@@ -169,8 +169,13 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
     uint32_t nissued = 0, o_next = 0;
     if (kCompressed) {
         ds = carve_common(dec);
+        // the first two pairs' offsets in one round trip, the tables built
+        // while they arrive, then the pairs' copies started
+        if (rb_ok && my_pairs > 0)
+            o_next = pair_offsets_load2(v, rb * gpr + kg_lo + 2u * uint32_t(grp),
+                                        rb * gpr + kg_lo + 2u * (uint32_t(grp) + G));
+        build_tables(ds, v);
         if (rb_ok && my_pairs > 0) {
-            o_next = pair_offsets_load(v, rb * gpr + kg_lo + 2u * uint32_t(grp));
             for (int s = 0; s < kPairStages && nissued < my_pairs; s++) {
                 const uint32_t kgA = kg_lo + 2u * (uint32_t(grp) + nissued * G);
                 if constexpr (kSmStaged)
@@ -180,11 +185,11 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
                     pair_issue_codes(v, o_next, rb, kgA, kgA + 1 < kg_hi, rb * gpr + kgA, st0 + uint32_t(s) * sbytes,
                                      pbar0 + 8u * s, meta + s);
                 nissued++;
-                if (nissued < my_pairs)
-                    o_next = pair_offsets_load(v, rb * gpr + kg_lo + 2u * (uint32_t(grp) + nissued * G));
+                o_next = pair_offsets_shift(o_next);
             }
+            if (nissued < my_pairs)
+                o_next = pair_offsets_load(v, rb * gpr + kg_lo + 2u * (uint32_t(grp) + nissued * G));
         }
-        build_tables(ds, v);
     }
     tc_fence_before();
     __syncthreads();

@@ -76,8 +76,9 @@ __device__ __forceinline__ void cta_reduce(const GemvParams &p, const float *red
     }
 }
 
-// An escaped group's two accumulators, from its raw exponents and
-// sign+mantissa bytes in the stage (rare; out of line).
+// An escaped group's two accumulators, from its raw exponents (in the
+// stage) and its sign+mantissa bytes: in the stage (shared address) or in
+// global memory (rare; out of line).
 __device__ __noinline__ float2 escaped_sum(uint32_t ebase, uint32_t em, uint32_t sm_lane, uint32_t stride,
                                            const uint32_t *x) {
     uint4 e[4], sm[4];
@@ -92,11 +93,31 @@ __device__ __noinline__ float2 escaped_sum(uint32_t ebase, uint32_t em, uint32_t
     return make_float2(b0, b1);
 }
 
-template <int W>
+__device__ __noinline__ float2 escaped_sum_global(uint32_t ebase, uint32_t em, const uint8_t *sm_lane,
+                                                  uint32_t stride, const uint32_t *x) {
+    uint4 e[4], sm[4];
+    escape_read(ebase, em, e);
+#pragma unroll
+    for (int c = 0; c < 4; c++)
+        sm[c] = __ldg(reinterpret_cast<const uint4 *>(sm_lane + c * stride));
+    float b0 = 0.f, b1 = 0.f;
+#pragma unroll
+    for (int I = 0; I < 32; I++)
+        fma_bf16x2(b0, b1, escape_pair(e, I, sm_word(sm, I >> 1)), __ldg(x + I));
+    return make_float2(b0, b1);
+}
+
+// kPrivate: the pair table as 32 lane-private copies (every lookup one
+// shared-memory wavefront); the stages then hold only the codes and the
+// sign+mantissa bytes are read from L2, where the copy engine prefetches
+// them when the pair is issued.  Otherwise one shared table and stages that
+// hold the sign+mantissa bytes too.
+template <int W, bool kPrivate>
 __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_per_cta) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t bars[kMaxColWarps * kPairStages];
     __shared__ PairMeta metas[kMaxColWarps * kPairStages];
+    constexpr int kShift = kPrivate ? kShiftPrivate : kShiftShared;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const BlobView &v = p.v;
     const uint32_t gpr = v.gpr;
@@ -108,15 +129,17 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
     warp_cols(gpr, warp, W, k0, k1);
     const uint32_t np = (k1 - k0 + 1) / 2;  // pairs per row block
     const uint32_t npairs = np * nrbc;
-    const uint32_t sbytes = pair_stage_bytes(v.tdata);
+    const uint32_t sbytes = kPrivate ? code_stage_bytes(v.tdata) : pair_stage_bytes(v.tdata);
     const uint32_t smoff = pair_stage_smoff(v.tdata);
 
-    // shared memory: [common tables][warp partials rb_per_cta x W x 32][pad to 128]
-    // [per warp kPairStages stages]
-    const DecodeShared ds = carve_common(smem);
-    float *red = reinterpret_cast<float *>(smem + kCommonSmemBytes);
-    const uint32_t sbase = smem_addr(smem);
-    const uint32_t stage_lo = (sbase + uint32_t(kCommonSmemBytes) + uint32_t(rb_per_cta) * W * 128u + 127u) & ~127u;
+    // shared memory: [private tables (kPrivate)][common tables][warp partials
+    // rb_per_cta x W x 32][pad to 128][per warp kPairStages stages]
+    const uint32_t priv = smem_addr(smem);
+    unsigned char *common = smem + (kPrivate ? kPrivateLutBytes : 0);
+    const DecodeShared ds = carve_common(common);
+    float *red = reinterpret_cast<float *>(common + kCommonSmemBytes);
+    const uint32_t cbase = smem_addr(common);
+    const uint32_t stage_lo = (cbase + uint32_t(kCommonSmemBytes) + uint32_t(rb_per_cta) * W * 128u + 127u) & ~127u;
     const uint32_t st0 = stage_lo + uint32_t(warp) * kPairStages * sbytes;
     const uint32_t bar0 = smem_addr(&bars[warp * kPairStages]);
 
@@ -128,25 +151,37 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
     }
     __syncwarp();
 
-    // start the first pairs' copies, then build the tables while they fly
+    // the first two pairs' offsets in one round trip, the tables built while
+    // they arrive, then the pairs' copies started
     PairMeta *meta = &metas[warp * kPairStages];
     PairCursor issue{rb0, k0};
     uint32_t nissued = 0;
-    uint32_t o_next = npairs ? pair_offsets_load(v, rb0 * gpr + k0) : 0u;
+    PairCursor second = issue;
+    second.next(k0, k1);
+    uint32_t o_next = npairs ? pair_offsets_load2(v, rb0 * gpr + k0, second.rb * gpr + second.kgA) : 0u;
+    if constexpr (kPrivate)
+        build_tables_private(ds, v, priv);
+    else
+        build_tables(ds, v);
 #pragma unroll
     for (int s = 0; s < kPairStages; s++) {
         if (nissued < npairs) {
-            pair_issue(v, o_next, issue.rb, issue.kgA, issue.kgA + 1 < k1, issue.rb * gpr + issue.kgA,
-                       st0 + uint32_t(s) * sbytes, smoff, bar0 + 8u * s, meta + s);
+            if constexpr (kPrivate)
+                pair_issue_codes(v, o_next, issue.rb, issue.kgA, issue.kgA + 1 < k1, issue.rb * gpr + issue.kgA,
+                                 st0 + uint32_t(s) * sbytes, bar0 + 8u * s, meta + s);
+            else
+                pair_issue(v, o_next, issue.rb, issue.kgA, issue.kgA + 1 < k1, issue.rb * gpr + issue.kgA,
+                           st0 + uint32_t(s) * sbytes, smoff, bar0 + 8u * s, meta + s);
             issue.next(k0, k1);
             nissued++;
-            if (nissued < npairs)
-                o_next = pair_offsets_load(v, issue.rb * gpr + issue.kgA);
+            o_next = pair_offsets_shift(o_next);  // the second pair's (lanes 8..13)
         }
     }
-    build_tables(ds, v);
+    if (nissued < npairs)
+        o_next = pair_offsets_load(v, issue.rb * gpr + issue.kgA);
     __syncthreads();
-    const uint32_t lut = smem_addr(ds.lut);
+    grid_dep_wait();  // x may come from the kernel before
+    const uint32_t lut = kPrivate ? priv + 4u * uint32_t(lane) : smem_addr(ds.lut);
 
     PairCursor cur{rb0, k0};
     float s_w = 0.f;  // this warp's partial for row `lane` of row block cur.rb
@@ -154,6 +189,17 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
     if (npairs == 0)
         for (uint32_t rl = 0; rl < nrbc; rl++)
             red[(rl * W + warp) * 32 + lane] = 0.f;
+    // kPrivate: sign+mantissa bytes of the current pair, and its chunk 0 in
+    // registers (loaded during the previous pair)
+    const uint8_t *sm_cur = nullptr;
+    uint4 c0A = make_uint4(0, 0, 0, 0), c0B = c0A;
+    if (kPrivate && npairs > 0) {
+        uint32_t R0;
+        sm_cur = pair_sm_base(v, rb0, k0, rb0 * gpr + k0, R0);
+        const uint8_t *a = sm_cur + 16u * (uint32_t(lane) < R0 ? uint32_t(lane) : 0u);
+        c0A = __ldg(reinterpret_cast<const uint4 *>(a));
+        c0B = __ldg(reinterpret_cast<const uint4 *>(k0 + 1 < k1 ? a + 64u * R0 : a));
+    }
 
 #pragma unroll 1
     for (uint32_t j = 0; j < npairs; j++) {
@@ -177,22 +223,54 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
         }
         LaneStream la, lb;
         const uint32_t cA = st + 64u, cB = cA + 16u * m.n16A;
-        const uint32_t emA = tile_begin_ready(ds, TileMeta{gA, 0u, m.pkA}, R, cA, la, p.status);
-        const uint32_t emB = tile_begin_ready(ds, TileMeta{gB, 0u, m.pkB}, hasB ? R : 0, cB, lb, p.status);
+        const uint32_t emA = tile_begin_ready<kShift>(ds, TileMeta{gA, 0u, m.pkA}, R, cA, la, p.status);
+        const uint32_t emB = tile_begin_ready<kShift>(ds, TileMeta{gB, 0u, m.pkB}, hasB ? R : 0, cB, lb, p.status);
         const uint32_t ebA = cA + 16u * (m.n16A + m.n16B), ebB = ebA + 64u * m.nescA;
         const uint32_t stride = 16u * uint32_t(R);
         const uint32_t smA = st + smoff + 16u * uint32_t(lane), smB = smA + 64u * uint32_t(R);
+        // kPrivate: the pair's bytes in global memory, and the next pair's
+        const uint32_t lc = uint32_t(lane) < uint32_t(R) ? uint32_t(lane) : 0u;
+        const uint8_t *gA_sm = sm_cur + 16u * lc, *gB_sm = hasB ? gA_sm + 64u * uint32_t(R) : gA_sm;
+        const bool more = j + 1 < npairs;
+        PairCursor nxt = cur;
+        nxt.next(k0, k1);
+        uint32_t Rn = 0;
+        const uint8_t *sm_nxt = kPrivate && more ? pair_sm_base(v, nxt.rb, nxt.kgA, nxt.rb * gpr + nxt.kgA, Rn) : sm_cur;
+        // an escaped group is redone after the loop from its sign+mantissa
+        // bytes in global memory: have them in L1 by then
+        if (kPrivate && ((emA | emB) >> lane) & 1u) {
+            const uint8_t *e = ((emA >> lane) & 1u) ? gA_sm : gB_sm;
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+                asm volatile("prefetch.global.L1 [%0];" :: "l"(e + c * stride));
+        }
         // x of the two groups, 4 pairs per load, one load ahead (broadcast, L1-resident)
         const uint4 *xA = reinterpret_cast<const uint4 *>(p.x) + size_t(cur.kgA) * 8;
         const uint4 *xB = xA + (hasB ? 8 : 0);
         float aA0 = 0.f, aA1 = 0.f, aB0 = 0.f, aB1 = 0.f;
-        uint4 sA = lds128(smA), sB = lds128(smB), nA = sA, nB = sB;
+        uint4 sA = c0A, sB = c0B;
+        if constexpr (!kPrivate) {
+            sA = lds128(smA);
+            sB = lds128(smB);
+        }
+        uint4 nA = sA, nB = sB;
         uint4 x4A = __ldg(xA), x4B = __ldg(xB), nxA = x4A, nxB = x4B;
 #pragma unroll
         for (int I = 0; I < 32; I++) {
-            if ((I & 7) == 0 && I < 24) {  // next chunk of sign+mantissa bytes
-                nA = lds128(smA + uint32_t((I >> 3) + 1) * stride);
-                nB = lds128(smB + uint32_t((I >> 3) + 1) * stride);
+            if ((I & 7) == 0) {  // next chunk of sign+mantissa bytes
+                if constexpr (!kPrivate) {
+                    if (I < 24) {
+                        nA = lds128(smA + uint32_t((I >> 3) + 1) * stride);
+                        nB = lds128(smB + uint32_t((I >> 3) + 1) * stride);
+                    }
+                } else if (I < 24) {
+                    nA = __ldg(reinterpret_cast<const uint4 *>(gA_sm + uint32_t((I >> 3) + 1) * stride));
+                    nB = __ldg(reinterpret_cast<const uint4 *>(gB_sm + uint32_t((I >> 3) + 1) * stride));
+                } else if (more) {  // chunk 0 of the next pair
+                    const uint8_t *a = sm_nxt + 16u * (uint32_t(lane) < Rn ? uint32_t(lane) : 0u);
+                    nA = __ldg(reinterpret_cast<const uint4 *>(a));
+                    nB = __ldg(reinterpret_cast<const uint4 *>(nxt.kgA + 1 < k1 ? a + 64u * Rn : a));
+                }
             }
             if ((I & 3) == 0) {
                 if (I > 0) {
@@ -204,8 +282,8 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
                     nxB = __ldg(xB + (I >> 2) + 1);
                 }
             }
-            fma_bf16x2(aA0, aA1, decode_pair(la, lut, I, word4(sA, (I >> 1) & 3)), word4(x4A, I));
-            fma_bf16x2(aB0, aB1, decode_pair(lb, lut, I, word4(sB, (I >> 1) & 3)), word4(x4B, I));
+            fma_bf16x2(aA0, aA1, decode_pair<kShift>(la, lut, I, word4(sA, (I >> 1) & 3)), word4(x4A, I));
+            fma_bf16x2(aB0, aB1, decode_pair<kShift>(lb, lut, I, word4(sB, (I >> 1) & 3)), word4(x4B, I));
             if ((I & 7) == 7) {
                 sA = nA;
                 sB = nB;
@@ -213,20 +291,25 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
         }
         bad |= tile_check_bits(la) | tile_check_bits(lb);
         if ((emA >> lane) & 1u) {
-            const float2 r = escaped_sum(ebA, emA, smA, stride, reinterpret_cast<const uint32_t *>(xA));
+            const float2 r = kPrivate ? escaped_sum_global(ebA, emA, gA_sm, stride, reinterpret_cast<const uint32_t *>(xA))
+                                      : escaped_sum(ebA, emA, smA, stride, reinterpret_cast<const uint32_t *>(xA));
             aA0 = r.x;
             aA1 = r.y;
         }
         if ((emB >> lane) & 1u) {
-            const float2 r = escaped_sum(ebB, emB, smB, stride, reinterpret_cast<const uint32_t *>(xB));
+            const float2 r = kPrivate ? escaped_sum_global(ebB, emB, gB_sm, stride, reinterpret_cast<const uint32_t *>(xB))
+                                      : escaped_sum(ebB, emB, smB, stride, reinterpret_cast<const uint32_t *>(xB));
             aB0 = r.x;
             aB1 = r.y;
         }
+        c0A = sA;  // kPrivate: chunk 0 of the next pair
+        c0B = sB;
+        sm_cur = sm_nxt;
         s_w = s_w + (aA0 + aA1);
         if (hasB)
             s_w = s_w + (aB0 + aB1);
         const uint32_t rb_done = cur.rb;
-        cur.next(k0, k1);
+        cur = nxt;
         if (cur.rb != rb_done) {  // the warp's last pair of this row block
             red[((rb_done - rb0) * W + warp) * 32 + lane] = s_w;
             s_w = 0.f;
@@ -236,8 +319,12 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
         fence_proxy_async_smem();
         __syncwarp();
         if (nissued < npairs) {
-            pair_issue(v, o_next, issue.rb, issue.kgA, issue.kgA + 1 < k1, issue.rb * gpr + issue.kgA, st, smoff, bar,
-                       meta + s);
+            if constexpr (kPrivate)
+                pair_issue_codes(v, o_next, issue.rb, issue.kgA, issue.kgA + 1 < k1, issue.rb * gpr + issue.kgA, st,
+                                 bar, meta + s);
+            else
+                pair_issue(v, o_next, issue.rb, issue.kgA, issue.kgA + 1 < k1, issue.rb * gpr + issue.kgA, st, smoff,
+                           bar, meta + s);
             issue.next(k0, k1);
             nissued++;
             if (nissued < npairs)
@@ -265,6 +352,7 @@ __device__ __forceinline__ void gemv_col_bf16(const GemvParams &p, int rb_per_ct
     // shared memory: [x slab gpr x 32 pairs][warp partials rb_per_cta x W x 32]
     uint32_t *xs = reinterpret_cast<uint32_t *>(smem);
     float *red = reinterpret_cast<float *>(smem + size_t(gpr) * 128);
+    grid_dep_wait();  // x may come from the kernel before
     load_x_all(p, xs, gpr);
     __syncthreads();
 
@@ -301,36 +389,52 @@ __device__ __forceinline__ void gemv_col_bf16(const GemvParams &p, int rb_per_ct
     cta_reduce<W>(p, red, rb0, nrbc);
 }
 
-template <int W, bool kCompressed>
+template <int W, bool kCompressed, bool kPrivate>
 __global__ void __launch_bounds__(W * 32, 1) gemv_kg_kernel(const GemvParams p, int rb_per_cta) {
+    grid_dep_launch();
     if constexpr (kCompressed)
-        gemv_col_compressed<W>(p, rb_per_cta);
+        gemv_col_compressed<W, kPrivate>(p, rb_per_cta);
     else
         gemv_col_bf16<W>(p, rb_per_cta);
 }
 
-template <int W, bool kCompressed>
+size_t kg_smem(int warps, int rb_per_cta, bool compressed, bool priv, uint32_t tdata, int gpr) {
+    const size_t red = size_t(rb_per_cta) * warps * 128;
+    if (!compressed)
+        return size_t(gpr) * 128 + red;
+    const size_t sbytes = priv ? code_stage_bytes(tdata) : pair_stage_bytes(tdata);
+    return (priv ? size_t(kPrivateLutBytes) : 0) + size_t(kCommonSmemBytes) + red + 128 +
+           size_t(warps) * kPairStages * sbytes;
+}
+
+template <int W, bool kCompressed, bool kPrivate>
 uw_status launch_kg_one(const GemvParams &p, int rb_per_cta, cudaStream_t stream) {
-    const size_t smem = gemv_kg_smem_bytes(W, rb_per_cta, kCompressed, p.v.tdata, int(p.cols / kGroup));
+    const size_t smem = kg_smem(W, rb_per_cta, kCompressed, kPrivate, p.v.tdata, int(p.cols / kGroup));
     if (smem > size_t(kMaxSmemPerBlock) - 1024)
         return UW_ERR_UNSUPPORTED;
-    auto kern = gemv_kg_kernel<W, kCompressed>;
+    auto kern = gemv_kg_kernel<W, kCompressed, kPrivate>;
     if (!ensure_smem(kern, smem))
         return UW_ERR_CUDA;
     const int64_t nrb = (p.rows + kTileRows - 1) / kTileRows;
     const dim3 grid(unsigned((nrb + rb_per_cta - 1) / rb_per_cta));
-    kern<<<grid, dim3(W * 32), smem, stream>>>(p, rb_per_cta);
-    return cudaGetLastError() == cudaSuccess ? UW_OK : UW_ERR_CUDA;
+    return launch_overlapped(kern, grid, dim3(W * 32), smem, stream, p, rb_per_cta) == cudaSuccess ? UW_OK
+                                                                                             : UW_ERR_CUDA;
+}
+
+// Compressed source: the private-table form when its shared memory fits,
+// else one shared table.  Both decode the same weights, so the results are
+// identical.
+template <int W>
+uw_status launch_kg_compressed(const GemvParams &p, int rb_per_cta, cudaStream_t stream) {
+    if (kg_smem(W, rb_per_cta, true, true, p.v.tdata, int(p.cols / kGroup)) <= size_t(kMaxSmemPerBlock) - 1024)
+        return launch_kg_one<W, true, true>(p, rb_per_cta, stream);
+    return launch_kg_one<W, true, false>(p, rb_per_cta, stream);
 }
 
 }  // namespace
 
 size_t gemv_kg_smem_bytes(int warps, int rb_per_cta, bool compressed, uint32_t tdata, int gpr) {
-    const size_t red = size_t(rb_per_cta) * warps * 128;
-    if (!compressed)
-        return size_t(gpr) * 128 + red;
-    const size_t sbytes = pair_stage_bytes(tdata);
-    return size_t(kCommonSmemBytes) + red + 128 + size_t(warps) * kPairStages * sbytes;
+    return kg_smem(warps, rb_per_cta, compressed, false, tdata, gpr);
 }
 
 uw_status launch_gemv_kg(const GemvParams &p, int warps, int rb_per_cta, bool compressed, cudaStream_t stream) {
@@ -339,12 +443,12 @@ uw_status launch_gemv_kg(const GemvParams &p, int warps, int rb_per_cta, bool co
     if (uint64_t(p.rows / kTileRows + 1) * (p.cols / kGroup) >= (uint64_t(1) << 32))
         return UW_ERR_UNSUPPORTED;  // tile indices are 32-bit
     switch (warps) {
-        case 4: return compressed ? launch_kg_one<4, true>(p, rb_per_cta, stream)
-                                  : launch_kg_one<4, false>(p, rb_per_cta, stream);
-        case 8: return compressed ? launch_kg_one<8, true>(p, rb_per_cta, stream)
-                                  : launch_kg_one<8, false>(p, rb_per_cta, stream);
-        case 16: return compressed ? launch_kg_one<16, true>(p, rb_per_cta, stream)
-                                   : launch_kg_one<16, false>(p, rb_per_cta, stream);
+        case 4: return compressed ? launch_kg_compressed<4>(p, rb_per_cta, stream)
+                                  : launch_kg_one<4, false, false>(p, rb_per_cta, stream);
+        case 8: return compressed ? launch_kg_compressed<8>(p, rb_per_cta, stream)
+                                  : launch_kg_one<8, false, false>(p, rb_per_cta, stream);
+        case 16: return compressed ? launch_kg_compressed<16>(p, rb_per_cta, stream)
+                                   : launch_kg_one<16, false, false>(p, rb_per_cta, stream);
     }
     return UW_ERR_UNSUPPORTED;
 }

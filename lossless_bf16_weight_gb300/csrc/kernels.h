@@ -69,6 +69,28 @@ inline bool ensure_smem(Kernel *kern, size_t bytes) {
     return ensure_smem_limit(reinterpret_cast<const void *>(kern), bytes);
 }
 
+// Launch with programmatic dependent launch allowed: the kernel may begin
+// while the kernel before it in the stream drains.  Only for kernels that
+// execute grid_dep_wait() before reading anything an earlier kernel wrote and
+// before writing anything an earlier kernel may still read; their prologue
+// (tables, first copies of the constant blob) then overlaps the earlier
+// kernel's tail.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                     Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Tile buffer stride assumed where no blob is at hand (the largest possible).
 constexpr uint32_t kWorstTileBuf = kMaxTileData + kTileSlack;
 

@@ -38,6 +38,18 @@ __device__ __forceinline__ uint32_t pair_offsets_load(const BlobView &v, uint32_
     return __ldg((l < 3 ? v.tcode : v.tesc) + (k < v.ntiles ? k : v.ntiles));
 }
 
+// The same for two pairs in one round trip: t0 into lanes 0..5, t1 into
+// lanes 8..13 (read the second with pair_offsets_shift).
+__device__ __forceinline__ uint32_t pair_offsets_load2(const BlobView &v, uint32_t t0, uint32_t t1) {
+    const int lane = threadIdx.x & 31;
+    const int l = (lane & 7) < 6 ? (lane & 7) : 0;
+    const uint32_t k = (lane < 8 ? t0 : t1) + uint32_t(l % 3);
+    return __ldg((l < 3 ? v.tcode : v.tesc) + (k < v.ntiles ? k : v.ntiles));
+}
+
+// Move lanes 8..13 of a pair_offsets_load2 result down to lanes 0..5.
+__device__ __forceinline__ uint32_t pair_offsets_shift(uint32_t o) { return __shfl_down_sync(0xffffffffu, o, 8); }
+
 // What the decode needs to know about a staged pair (warp-uniform; kept in
 // shared memory next to the stage so that the loop body is not duplicated).
 struct PairMeta {

@@ -25,7 +25,7 @@ _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 
 GROUP = 64
 TILE_ROWS = 32
-LMAX = 6
+LMAX = 5
 PALETTE = 16
 
 

@@ -30,8 +30,9 @@
  *     outside the code and keep their 64 raw exponent bytes.
  *   - palette = 16 most frequent exponents over the whole matrix, ties to the
  *     smaller exponent value; exponents with zero count are never included.
- *   - one code per matrix; code length limit LMAX = 6 so that a 12-bit window
- *     always holds two whole codes (4096 entries x 4 B = the page's 16 KB).
+ *   - one code per matrix; code length limit LMAX = 5 so that a 10-bit window
+ *     always holds two whole codes (a 1024-entry pair table; the page's own
+ *     table is about 16 KB, sized for its hardware).
  *   - among equally short codes, pick the lexicographically largest count
  *     vector (n_1, ..., n_LMAX), symbols ranked by (frequency desc, palette
  *     index asc); canonical code values by (length, palette index).
@@ -49,10 +50,10 @@
 
 #define UWO_GROUP 64      /* weights per group ("row of 64")         */
 #define UWO_TROWS 32      /* rows per tile (one lane per row)        */
-#define UWO_LMAX 6        /* longest code                             */
+#define UWO_LMAX 5        /* longest code                             */
 #define UWO_PAL 16        /* palette size                             */
 #define UWO_MAGIC 0x31425755u /* "UWB1" little endian                 */
-#define UWO_VERSION 1u
+#define UWO_VERSION 2u
 #define UWO_HEADER 256
 
 /* ------------------------------------------------------------------------

@@ -103,7 +103,7 @@ def test_blob_info_rejects_corruption(lib):
     assert lib.blob_info_status(_corrupt(blob, 0, 0)) == 4                 # magic
     assert lib.blob_info_status(_corrupt(blob, 4, 9)) == 4                 # version
     assert lib.blob_info_status(_corrupt(blob, 24, 32)) == 4               # group size
-    assert lib.blob_info_status(_corrupt(blob, 56, 9)) == 4                # code length > 6
+    assert lib.blob_info_status(_corrupt(blob, 56, 9)) == 4                # code length > 5
     assert lib.blob_info_status(blob[: len(blob) - 256]) == 4              # truncated
     assert lib.blob_info_status(_corrupt(blob, d.off_glen, 0)) == 4        # glen vs tile table
     assert lib.blob_info_status(_corrupt(blob, d.off_glen + 3, 49)) == 4   # glen > 48
@@ -117,7 +117,8 @@ def test_compression_ratio_and_statistics(lib):
     blob = lib.compress(w)
     d = lib.blob_info(blob)
     ratio = d.blob_bytes / (2 * w.size)
-    assert 0.66 < ratio < 0.70, ratio
+    assert 0.68 < ratio < 0.71, ratio
+    # codes limited to 5 bits: about 0.4 bit above the ~2.6-bit entropy
     mean_len = d.code_bits / (64 * (d.n_groups - d.n_escaped))
-    assert 2.6 < mean_len < 2.8
+    assert 2.8 < mean_len < 3.1
     assert d.n_escaped / d.n_groups < 0.01
