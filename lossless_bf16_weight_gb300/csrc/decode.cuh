@@ -137,13 +137,12 @@ __device__ __forceinline__ void build_tables(const DecodeShared &s, const BlobVi
         s.lut[w] = pair_entry(s.prefix, uint32_t(w));
 }
 
-// The same with the pair table as 32 lane-private copies at shared address
-// `priv` (kPrivateLutBytes, 16-byte aligned; entry w of copy l at word
-// 32*w + l) for decode_pair<kShiftPrivate>.  Must be followed by
+// Second half of a private-table build: after build_tables and a
+// __syncthreads(), copy the pair table into 32 lane-private copies at shared
+// address `priv` (kPrivateLutBytes, 16-byte aligned; entry w of copy l at
+// word 32*w + l) for decode_pair<kShiftPrivate>.  Must be followed by
 // __syncthreads() before use.
-__device__ __forceinline__ void build_tables_private(const DecodeShared &s, const BlobView &v, uint32_t priv) {
-    build_tables(s, v);  // the 1024 entries once, in s.lut
-    __syncthreads();
+__device__ __forceinline__ void replicate_private(const DecodeShared &s, uint32_t priv) {
     for (int i = threadIdx.x; i < kLutEntries * 8; i += blockDim.x) {
         const uint32_t e = s.lut[uint32_t(i) >> 3];
         asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" :: "r"(priv + 16u * uint32_t(i)), "r"(e) : "memory");

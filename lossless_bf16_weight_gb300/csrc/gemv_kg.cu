@@ -151,18 +151,18 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
     }
     __syncwarp();
 
-    // the first two pairs' offsets in one round trip, the tables built while
-    // they arrive, then the pairs' copies started
+    // Prologue, ordered so that the memory round trips overlap the table
+    // build: the first two pairs' offsets (one round trip); the 1024 table
+    // entries; the two pairs' copies as soon as the offsets are in; chunk 0
+    // of the first pair's sign+mantissa bytes; then the private copies of the
+    // table while the copies fly.
     PairMeta *meta = &metas[warp * kPairStages];
     PairCursor issue{rb0, k0};
     uint32_t nissued = 0;
     PairCursor second = issue;
     second.next(k0, k1);
     uint32_t o_next = npairs ? pair_offsets_load2(v, rb0 * gpr + k0, second.rb * gpr + second.kgA) : 0u;
-    if constexpr (kPrivate)
-        build_tables_private(ds, v, priv);
-    else
-        build_tables(ds, v);
+    build_tables(ds, v);
 #pragma unroll
     for (int s = 0; s < kPairStages; s++) {
         if (nissued < npairs) {
@@ -177,18 +177,6 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
             o_next = pair_offsets_shift(o_next);  // the second pair's (lanes 8..13)
         }
     }
-    if (nissued < npairs)
-        o_next = pair_offsets_load(v, issue.rb * gpr + issue.kgA);
-    __syncthreads();
-    grid_dep_wait();  // x may come from the kernel before
-    const uint32_t lut = kPrivate ? priv + 4u * uint32_t(lane) : smem_addr(ds.lut);
-
-    PairCursor cur{rb0, k0};
-    float s_w = 0.f;  // this warp's partial for row `lane` of row block cur.rb
-    uint32_t bad = 0;
-    if (npairs == 0)
-        for (uint32_t rl = 0; rl < nrbc; rl++)
-            red[(rl * W + warp) * 32 + lane] = 0.f;
     // kPrivate: sign+mantissa bytes of the current pair, and its chunk 0 in
     // registers (loaded during the previous pair)
     const uint8_t *sm_cur = nullptr;
@@ -200,6 +188,22 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
         c0A = __ldg(reinterpret_cast<const uint4 *>(a));
         c0B = __ldg(reinterpret_cast<const uint4 *>(k0 + 1 < k1 ? a + 64u * R0 : a));
     }
+    if (nissued < npairs)
+        o_next = pair_offsets_load(v, issue.rb * gpr + issue.kgA);
+    if constexpr (kPrivate) {
+        __syncthreads();
+        replicate_private(ds, priv);
+    }
+    __syncthreads();
+    grid_dep_wait();  // x may come from the kernel before
+    const uint32_t lut = kPrivate ? priv + 4u * uint32_t(lane) : smem_addr(ds.lut);
+
+    PairCursor cur{rb0, k0};
+    float s_w = 0.f;  // this warp's partial for row `lane` of row block cur.rb
+    uint32_t bad = 0;
+    if (npairs == 0)
+        for (uint32_t rl = 0; rl < nrbc; rl++)
+            red[(rl * W + warp) * 32 + lane] = 0.f;
 
 #pragma unroll 1
     for (uint32_t j = 0; j < npairs; j++) {
