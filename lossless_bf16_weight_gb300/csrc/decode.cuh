@@ -230,6 +230,12 @@ __device__ __forceinline__ uint32_t tile_offsets_load(const BlobView &v, int64_t
     return lane < 4 ? __ldg(src) : 0u;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start
+// launching, and wait until every earlier kernel has completed and its
+// writes are visible.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

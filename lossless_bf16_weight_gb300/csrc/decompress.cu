@@ -20,6 +20,7 @@ constexpr int kOutBufBytes = kTileRows * kGroup * 2;  // 4096
 __global__ void __launch_bounds__(kDecompWarps * 32, 2)
     decompress_kernel(const BlobView v, uint16_t *__restrict__ out, uint32_t *status) {
     extern __shared__ __align__(16) unsigned char smem[];
+    grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const DecodeShared ds = carve_common(smem);
     const uint32_t lut = smem_addr(ds.lut);
@@ -46,6 +47,7 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
     }
     build_tables(ds, v);
     __syncthreads();
+    grid_dep_wait();  // the output may still be read by the kernel before
 
     for (int64_t t = t_lo; t < t_hi; t++) {
         const int R = tile_rows(v, rb);
@@ -119,8 +121,10 @@ uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status
     const size_t smem = size_t(kCommonSmemBytes) + size_t(kDecompWarps) * (2 * size_t(v.tbuf) + kOutBufBytes);
     if (!ensure_smem(decompress_kernel, smem))
         return UW_ERR_CUDA;
-    decompress_kernel<<<dim3(unsigned(grid)), dim3(kDecompWarps * 32), smem, stream>>>(v, w_out, status);
-    return cudaGetLastError() == cudaSuccess ? UW_OK : UW_ERR_CUDA;
+    return launch_overlapped(decompress_kernel, dim3(unsigned(grid)), dim3(kDecompWarps * 32), smem, stream, v, w_out,
+                             status) == cudaSuccess
+               ? UW_OK
+               : UW_ERR_CUDA;
 }
 
 }  // namespace uw

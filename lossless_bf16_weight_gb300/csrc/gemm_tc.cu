@@ -194,6 +194,11 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Let the next kernel launch only now that this CTA holds its tensor
+    // memory: a later CTA on this SM then waits in its own allocation for
+    // this one to finish, never the other way round.
+    grid_dep_launch();
+    grid_dep_wait();  // x (and the twin's weights) may come from the kernel before; the split partials are reused
     const uint32_t tmem = tmem_slot;
     const uint32_t lut = kCompressed ? smem_addr(ds.lut) : 0u;
 
@@ -439,8 +444,7 @@ uw_status launch_tc_one(const TcParams &p, size_t smem, cudaStream_t stream) {
     if (!ensure_smem(kern, smem))
         return UW_ERR_CUDA;
     const dim3 grid(unsigned((p.rows + kTcM - 1) / kTcM), unsigned(p.splits));
-    kern<<<grid, dim3((4 * G + 1) * 32), smem, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? UW_OK : UW_ERR_CUDA;
+    return launch_overlapped(kern, grid, dim3((4 * G + 1) * 32), smem, stream, p) == cudaSuccess ? UW_OK : UW_ERR_CUDA;
 }
 
 // Tensor-memory columns before the A stages (the accumulator's Np, rounded up to 32).

@@ -87,6 +87,7 @@ __device__ __forceinline__ void gemv_body(const GemvParams &p) {
                 offs_next = tile_offsets_load(p.v, rb * gpr + w_lo + 1);
         }
     } else {
+        grid_dep_wait();  // the weights may come from the kernel before (decompress)
         const uint16_t *src = p.w + (rb * kTileRows + lane) * p.cols + w_lo * kGroup;
 #pragma unroll
         for (int c = 0; c < 8; c++)
@@ -94,8 +95,10 @@ __device__ __forceinline__ void gemv_body(const GemvParams &p) {
                                                  : make_uint4(0, 0, 0, 0);
     }
 
-    if (kCompressed)
+    if (kCompressed) {
         build_tables(ds, p.v);
+        grid_dep_wait();  // x may come from the kernel before
+    }
     // x slab: xs[((kk >> 2) * BP + b) * 4 + (kk & 3)] = x[b, 64*kg_lo + kk]
     const int64_t nkk = nk * kGroup;
     for (int64_t i = threadIdx.x; i < nkk * BP; i += blockDim.x) {
@@ -229,6 +232,7 @@ struct Occupancy<16> { static constexpr int kMinBlocks = 1; };
 
 template <int W, int BP, bool kCompressed>
 __global__ void __launch_bounds__(W * 32, Occupancy<W>::kMinBlocks) gemv_kernel(const GemvParams p) {
+    grid_dep_launch();
     gemv_body<W, BP, kCompressed>(p);
 }
 
@@ -238,8 +242,9 @@ uw_status launch_one(const GemvParams &p, size_t smem, cudaStream_t stream) {
     if (!ensure_smem(kern, smem))
         return UW_ERR_CUDA;
     const int64_t nrb = (p.rows + kTileRows - 1) / kTileRows;
-    kern<<<dim3(unsigned(nrb * p.splits)), dim3(W * 32), smem, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? UW_OK : UW_ERR_CUDA;
+    return launch_overlapped(kern, dim3(unsigned(nrb * p.splits)), dim3(W * 32), smem, stream, p) == cudaSuccess
+               ? UW_OK
+               : UW_ERR_CUDA;
 }
 
 template <int W, bool kCompressed>

@@ -19,6 +19,8 @@ __device__ __forceinline__ uint16_t swiglu1(uint16_t g, uint16_t u) {
 
 __global__ void swiglu_kernel(const uint16_t *__restrict__ g, const uint16_t *__restrict__ u,
                               uint16_t *__restrict__ h, int64_t n) {
+    grid_dep_launch();
+    grid_dep_wait();  // g and u come from the kernels before
     const int64_t n8 = n / 8;
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
     for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
@@ -51,8 +53,9 @@ uw_status launch_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h, int64
         blocks = 1;
     if (blocks > 152 * 16)
         blocks = 152 * 16;
-    swiglu_kernel<<<dim3(unsigned(blocks)), dim3(256), 0, stream>>>(g, u, h, n);
-    return cudaGetLastError() == cudaSuccess ? UW_OK : UW_ERR_CUDA;
+    return launch_overlapped(swiglu_kernel, dim3(unsigned(blocks)), dim3(256), 0, stream, g, u, h, n) == cudaSuccess
+               ? UW_OK
+               : UW_ERR_CUDA;
 }
 
 }  // namespace uw

@@ -164,10 +164,4 @@ __host__ __device__ constexpr uint32_t sw128_offset(uint32_t r, uint32_t c) {
     return (r >> 3) * 1024u + (r & 7u) * 128u + ((c ^ (r & 7u)) << 4);
 }
 
-// Programmatic dependent launch: let the next kernel in the stream start
-// launching, and wait until every earlier kernel has completed and its
-// writes are visible.
-__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 }  // namespace uw
