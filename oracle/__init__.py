@@ -83,6 +83,7 @@ def _L():
         lib.uwo_decompress.restype = ctypes.c_int
         lib.uwo_matmul_f64.argtypes = [P, I64, P, I64, I64, I64, I64, P, P]
         lib.uwo_swiglu_f64.argtypes = [P, P, I64, P]
+        lib.uwo_palette4.argtypes = [P, I64, I64, P, ctypes.c_int, P]
         lib.uwo_join.argtypes = [ctypes.c_uint, ctypes.c_uint]
         lib.uwo_join.restype = ctypes.c_uint16
         _lib = lib
@@ -231,3 +232,15 @@ def swiglu_f64(g, u) -> np.ndarray:
     h = np.zeros(g.size, np.float64)
     _L().uwo_swiglu_f64(_p(g), _p(u), g.size, _p(h))
     return h
+
+
+def palette4(w, pal) -> np.ndarray:
+    """[PALETTE] the 4-bit palette index of every weight in the library's
+    palette-4 layout (rows*cols/2 bytes); escaped groups hold index 0."""
+    w = _u16(w)
+    rows, cols = w.shape
+    p = np.zeros(16, np.uint8)
+    p[: len(pal)] = pal
+    out = np.zeros(rows * cols // 2, np.uint8)
+    _L().uwo_palette4(_p(w), rows, cols, _p(p), len(pal), _p(out))
+    return out

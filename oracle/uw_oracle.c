@@ -23,6 +23,11 @@
  *               one decision per row, no per-element branch.
  *   [LUT16K]    the decoder keeps a ~16 KB Huffman lookup table in SMEM.
  *   [MATMUL]    the compressed weights feed y = x W^T (decode once, multiply).
+ *   [PALETTE]   the palette pipelines: Huffman-coded exponents turned into
+ *               4-bit palette indices (at run time or once at model load),
+ *               from which the matmul rebuilds BF16 on the fly (paragraphs
+ *               on the four execution pipelines and on the palette format
+ *               at model load).
  *
  * Readings taken where the page is silent:
  *   - "row of 64" = 64 consecutive weights along K inside one output row.
@@ -623,6 +628,44 @@ int uwo_decompress(const uint8_t *blob, int64_t bytes, uint16_t *w)
         }
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * [PALETTE] 4-bit palette index of every weight of a matrix.
+ * Definition: for a weight in a group that is not escaped, its index is the
+ * position of its exponent in the blob's palette (header order); escaped
+ * groups get index 0 (their exponents stay in the escape section).
+ * Layout (the library's palette-4 form): like the sign+mantissa section at
+ * half the width.  Group q = 32*rb*gpr + R*kg + j (row j of row block rb,
+ * R rows in the block) owns 32 bytes in two 16-byte chunks; chunk c holds
+ * weights 32c .. 32c+31 at byte 32*q0 + (c*R + j)*16 of the buffer, q0 =
+ * 32*rb*gpr + R*kg the tile's first group, and weight 32c + 2i + b is nibble
+ * b (0 = low) of byte i of the chunk.  out: rows*cols/2 bytes, overwritten.
+ */
+void uwo_palette4(const uint16_t *w, int64_t rows, int64_t cols, const uint8_t *palette, int npal, uint8_t *out)
+{
+    int64_t gpr = cols / UWO_GROUP;
+    memset(out, 0, (size_t)(rows * cols / 2));
+    for (int64_t n = 0; n < rows; n++) {
+        int64_t rb = n / UWO_TROWS, j = n % UWO_TROWS;
+        int64_t left = rows - rb * UWO_TROWS;
+        int64_t R = left < UWO_TROWS ? left : UWO_TROWS;
+        for (int64_t kg = 0; kg < gpr; kg++) {
+            int idx[UWO_GROUP], escaped = 0;
+            for (int k = 0; k < UWO_GROUP; k++) {
+                unsigned e = (w[n * cols + kg * UWO_GROUP + k] >> 7) & 0xFFu;
+                idx[k] = palette_index(palette, npal, e);
+                if (idx[k] < 0)
+                    escaped = 1;
+            }
+            int64_t q0 = UWO_TROWS * rb * gpr + R * kg;
+            for (int k = 0; k < UWO_GROUP; k++) {
+                int v = escaped ? 0 : idx[k];
+                int c = k / 32, i = (k % 32) / 2, b = k % 2;
+                out[32 * q0 + (c * R + j) * 16 + i] |= (uint8_t)(v << (4 * b));
+            }
+        }
+    }
 }
 
 /* ------------------------------------------------------------------------

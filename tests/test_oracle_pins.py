@@ -267,6 +267,71 @@ def test_worked_escape_example(oracle):
     assert np.array_equal(oracle.decompress(blob), w)
 
 
+# ---------------------------------------------------------------- palette-4 form
+
+def test_palette4_worked_example(oracle):
+    # The 1 x 64 worked matrix: exponents 120,120,120,121,120,121,120,119
+    # repeating, palette (120, 121, 119), so indices 0,0,0,1,0,1,0,2
+    # repeating.  Byte i of a chunk packs weights 2i (low nibble) and 2i+1:
+    # 0x00, 0x10, 0x10, 0x20 repeating; one row, so chunk 1 follows chunk 0.
+    w, g = _worked_matrix()
+    assert oracle.palette4(w, g["palette"]).tobytes().hex() == "00101020" * 8
+
+
+def test_palette4_escaped_group_is_zero(oracle):
+    # The escape example: group 0 has exponent 100 + (k mod 16) = palette
+    # index k mod 16, so byte i of either chunk is (2i mod 16) | (2i+1 mod 16) << 4;
+    # group 1 is escaped and holds zeros.  One row: group kg at bytes 32kg..32kg+31.
+    g = _golden("worked_example_escape_1x128.json")
+    k = np.arange(128)
+    e = np.where(k < 64, 100 + (k % 16), 100)
+    e[127] = 99
+    w = ((e << 7) | (k % 128)).astype(np.uint16).reshape(1, 128)
+    p4 = oracle.palette4(w, g["palette"])
+    chunk = [(2 * i) % 16 | (((2 * i + 1) % 16) << 4) for i in range(16)]
+    assert list(p4[:32]) == chunk + chunk
+    assert not p4[32:].any()
+
+
+def _palette4_numpy(w, pal, esc):
+    """The palette-4 layout built with whole-array reshapes (a second reading
+    of the layout, written independently of the oracle's per-weight loop)."""
+    rows, cols = w.shape
+    gpr = cols // 64
+    lut = np.zeros(256, np.int64)
+    lut[np.array(pal, np.int64)] = np.arange(len(pal))
+    idx = lut[(w.astype(np.int64) >> 7) & 0xFF]
+    idx[np.repeat(esc.reshape(rows, gpr).astype(bool), 64, axis=1)] = 0
+    out = np.zeros(rows * cols // 2, np.uint8)
+    for rb in range((rows + 31) // 32):
+        R = min(32, rows - 32 * rb)
+        blk = idx[32 * rb: 32 * rb + R].reshape(R, gpr, 2, 16, 2)     # row, group, chunk, byte, nibble
+        packed = (blk[..., 0] | (blk[..., 1] << 4)).astype(np.uint8)   # [R, gpr, 2, 16]
+        base = 32 * 32 * rb * gpr
+        out[base: base + 32 * R * gpr] = packed.transpose(1, 2, 0, 3).ravel()
+    return out
+
+
+@pytest.mark.parametrize("shape", [(1, 64), (33, 128), (70, 192), (64, 64)])
+def test_palette4_layout_and_round_trip(oracle, shape):
+    rows, cols = shape
+    w = wl.heavy_tailed_weights(rows, cols, seed=rows + cols)
+    pal = oracle.palette(oracle.histogram(w))
+    esc = oracle.escape_flags(w, pal)
+    p4 = oracle.palette4(w, pal)
+    assert np.array_equal(p4, _palette4_numpy(w, pal, esc))
+    # every weight of a group that is not escaped comes back from its index
+    e, sm = oracle.split(w)
+    ok = ~np.repeat(esc.reshape(rows, cols // 64).astype(bool), 64, axis=1).ravel()
+    lut = np.zeros(256, np.int64)
+    lut[np.array(pal, np.int64)] = np.arange(len(pal))
+    assert np.array_equal(np.array(pal, np.int64)[lut[e[ok]]], e[ok].astype(np.int64))
+    # the index of every position is used exactly once: nibble histogram
+    nib = np.concatenate([p4 & 15, p4 >> 4])
+    want = np.bincount(np.where(ok, lut[e], 0), minlength=16)
+    assert np.array_equal(np.bincount(nib, minlength=16), want)
+
+
 # ---------------------------------------------------------------- round trips
 def test_round_trip_every_bf16_pattern(oracle):
     w = wl.all_bf16_patterns()
