@@ -66,11 +66,15 @@ typedef enum {
 
 /* Execution strategies (the blog's pipelines).  DECOMPRESS_GEMM restores
  * BF16 weights into the workspace, then multiplies them.  FUSED decodes in
- * registers / shared memory and never writes the weights back. */
+ * registers / shared memory and never writes the weights back.  PALETTE4
+ * transcodes the Huffman codes into 4-bit palette indices in the workspace
+ * (a quarter of the bytes a full decode writes), then multiplies from those
+ * (uw_matmul_palette4). */
 enum {
     UW_STRATEGY_DEFAULT = -1,
     UW_STRATEGY_DECOMPRESS_GEMM = 0,
-    UW_STRATEGY_FUSED = 1
+    UW_STRATEGY_FUSED = 1,
+    UW_STRATEGY_PALETTE4 = 2
 };
 
 /* Description of a compressed matrix, filled by uw_blob_info from the blob
@@ -157,6 +161,41 @@ uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uint16_t *x_de
 uw_status uw_matmul_bf16(const uint16_t *w_dev, int64_t rows, int64_t cols,
                          const uint16_t *x_dev, int64_t batch, uint16_t *y_dev,
                          int32_t variant, void *ws_dev, size_t ws_bytes, void *stream);
+
+/* The palette-4 form of a blob (the blog's palette pipelines: the Huffman
+ * codes turned into 4-bit palette indices at run time, or once when the
+ * model is loaded, from which the matmul rebuilds BF16 on the fly;
+ * paragraphs on the four execution pipelines and on the palette format at
+ * model load).  Every weight's 4-bit index into the blob's palette, laid out
+ * like the blob's sign+mantissa section at half the width: group q (row j of
+ * row block rb, column group kg; R rows in the block) owns 32 bytes in two
+ * 16-byte chunks, chunk c (weights 32c..32c+31) at byte 32*q0 + (c*R + j)*16
+ * with q0 = 32*rb*(cols/64) + R*kg, weight 32c + 2i + b in nibble b (0 = low)
+ * of byte i.  Escaped groups hold index 0; their exponents stay in the blob.
+ *
+ * uw_palette4_bytes -- size of the form: rows * cols / 2 bytes. */
+uw_status uw_palette4_bytes(const uw_desc *d, size_t *bytes);
+
+/* uw_transcode_palette4 -- write the palette-4 form of the blob.
+ *   blob_dev   device copy of the blob described by d.
+ *   p4_dev     uw_palette4_bytes(d) bytes of device memory, 16-byte aligned
+ *              (written).
+ *   ws_dev     workspace (error word only; >= uw_workspace_size(d, 0, NULL)). */
+uw_status uw_transcode_palette4(const uw_desc *d, const void *blob_dev, void *p4_dev,
+                                void *ws_dev, size_t ws_bytes, void *stream);
+
+/* uw_matmul_palette4 -- y = x W^T from the palette-4 form p4_dev (made by
+ * uw_transcode_palette4 from blob_dev) plus the blob's sign+mantissa bytes,
+ * group lengths and escaped exponents.
+ *   variant  a column variant (batch 1 only) or a tensor-core variant, -1 for
+ *            the default; row variants return UW_ERR_UNSUPPORTED.
+ *   ws_dev   workspace of at least uw_workspace_size(d, batch, plan) for a
+ *            FUSED plan with the same variant.
+ * The result is bit-identical to uw_matmul_bf16 with the same variant on the
+ * original weights. */
+uw_status uw_matmul_palette4(const uw_desc *d, const void *blob_dev, const void *p4_dev,
+                             const uint16_t *x_dev, int64_t batch, uint16_t *y_dev, int32_t variant,
+                             void *ws_dev, size_t ws_bytes, void *stream);
 
 /* uw_autotune -- measure every (strategy, variant) candidate for each batch
  * size and return the fastest per batch (the blog's autotuner, which picks a

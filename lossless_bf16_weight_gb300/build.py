@@ -21,7 +21,7 @@ LIB = os.path.join(HERE, "libuw.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["compress.cpp", "api.cu", "autotune.cu", "gemv.cu", "gemv_kg.cu", "gemm_tc.cu", "decompress.cu", "swiglu.cu",
+SOURCES = ["compress.cpp", "api.cu", "autotune.cu", "gemv.cu", "gemv_kg.cu", "gemm_tc.cu", "decompress.cu", "transcode.cu", "swiglu.cu",
            "noalloc.cu"]
 
 

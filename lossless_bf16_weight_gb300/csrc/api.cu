@@ -149,6 +149,8 @@ WsLayout layout_for(int64_t rows, int64_t cols, int64_t batch, int strategy, int
     L.total = L.weights;
     if (strategy == UW_STRATEGY_DECOMPRESS_GEMM)
         L.total = align_up(L.weights + 2 * uint64_t(rows) * uint64_t(cols), 256);
+    else if (strategy == UW_STRATEGY_PALETTE4)  // the palette-4 form, 4 bits per weight
+        L.total = align_up(L.weights + uint64_t(rows) * uint64_t(cols) / 2, 256);
     return L;
 }
 
@@ -156,12 +158,19 @@ struct ResolvedPlan {
     int strategy, variant;
 };
 
+// Default variant of the palette-4 kernels: the column GEMV at batch 1, the
+// tensor cores otherwise (there is no palette-4 row kernel).
+int default_p4_variant(int64_t rows, int64_t cols, int64_t batch) {
+    return batch == 1 ? default_gemv_variant(rows, cols, 1) : default_tc_variant(rows, cols, batch);
+}
+
 uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t batch, ResolvedPlan *out) {
     out->strategy = UW_STRATEGY_FUSED;
-    out->variant = default_gemv_variant(rows, cols, batch);
+    out->variant = -1;
     if (plan) {
         if (plan->strategy != UW_STRATEGY_DEFAULT) {
-            if (plan->strategy != UW_STRATEGY_FUSED && plan->strategy != UW_STRATEGY_DECOMPRESS_GEMM)
+            if (plan->strategy != UW_STRATEGY_FUSED && plan->strategy != UW_STRATEGY_DECOMPRESS_GEMM &&
+                plan->strategy != UW_STRATEGY_PALETTE4)
                 return UW_ERR_INVALID_ARG;
             out->strategy = plan->strategy;
         }
@@ -171,18 +180,23 @@ uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t 
             out->variant = plan->variant;
         }
     }
+    if (out->variant < 0)
+        out->variant = out->strategy == UW_STRATEGY_PALETTE4 ? default_p4_variant(rows, cols, batch)
+                                                             : default_gemv_variant(rows, cols, batch);
     return UW_OK;
 }
 
 // Batch rows go through the CUDA-core row kernels in chunks of at most 8;
 // the column kernels take batch 1 only; the tensor-core kernels take any
 // batch (chunks of 256 inside the launcher).
-uw_status run_gemv(GemvParams p, int variant, bool compressed, cudaStream_t stream) {
+uw_status run_gemv(GemvParams p, int variant, int src, cudaStream_t stream) {
+    const bool compressed = src == kSrcHuffman;
     const GemvVariant gv = gemv_variant(variant, p.rows, p.cols, compressed ? p.v.tbuf : kWorstTileBuf);
     if (gv.kind == Kind::kTensor) {
         TcParams t{};
         t.v = p.v;
         t.w = p.w;
+        t.p4 = p.p4;
         t.x = p.x;
         t.y = p.y;
         t.partial = p.partial;
@@ -192,14 +206,16 @@ uw_status run_gemv(GemvParams p, int variant, bool compressed, cudaStream_t stre
         t.cols = p.cols;
         t.batch = p.batch;
         t.splits = gv.splits;
-        return launch_gemm_tc(t, gv.warps, compressed, stream);
+        return launch_gemm_tc(t, gv.warps, src, stream);
     }
     if (gv.kind == Kind::kColumn) {
         if (p.batch != 1)
             return UW_ERR_UNSUPPORTED;
         p.splits = gv.splits;
-        return launch_gemv_kg(p, gv.warps, gv.rb, compressed, stream);
+        return launch_gemv_kg(p, gv.warps, gv.rb, src, stream);
     }
+    if (src == kSrcPalette4)
+        return UW_ERR_UNSUPPORTED;  // no palette-4 row kernel
     p.splits = gv.splits;
     const int64_t total = p.batch;
     for (int64_t b0 = 0; b0 < total; b0 += kMaxBatchChunk) {
@@ -286,6 +302,9 @@ void fill_blob_view(const uw_desc &d, const void *blob_dev, BlobView *v) {
     v->cols = d.cols;
     uint16_t code[16];
     canonical_code_values(d.code_len, code);
+    std::memcpy(v->palette, d.palette, sizeof v->palette);
+    for (int s = d.n_palette; s < 16; s++)
+        v->palette[s] = 0;
     std::memset(v->prefix, 0, sizeof v->prefix);
     for (int s = 0; s < d.n_palette; s++) {
         const int l = d.code_len[s];
@@ -478,9 +497,62 @@ extern "C" uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uin
         if (s != UW_OK)
             return s;
         p.w = w;
-        return run_gemv(p, rp.variant, false, as_stream(stream));
+        return run_gemv(p, rp.variant, kSrcBf16, as_stream(stream));
     }
-    return run_gemv(p, rp.variant, true, as_stream(stream));
+    if (rp.strategy == UW_STRATEGY_PALETTE4) {
+        uint8_t *p4 = wsb + L.weights;
+        s = launch_transcode_p4(p.v, p4, p.status, as_stream(stream));
+        if (s != UW_OK)
+            return s;
+        p.p4 = p4;
+        return run_gemv(p, rp.variant, kSrcPalette4, as_stream(stream));
+    }
+    return run_gemv(p, rp.variant, kSrcHuffman, as_stream(stream));
+}
+
+extern "C" uw_status uw_palette4_bytes(const uw_desc *d, size_t *bytes) {
+    if (!d || !bytes)
+        return UW_ERR_INVALID_ARG;
+    *bytes = size_t(uint64_t(d->rows) * uint64_t(d->cols) / 2);
+    return UW_OK;
+}
+
+extern "C" uw_status uw_transcode_palette4(const uw_desc *d, const void *blob_dev, void *p4_dev, void *ws,
+                                           size_t ws_bytes, void *stream) {
+    if (!d || !blob_dev || !p4_dev || !ws || (reinterpret_cast<uintptr_t>(p4_dev) & 15))
+        return UW_ERR_INVALID_ARG;
+    if (ws_bytes < 256)
+        return UW_ERR_BUFFER_TOO_SMALL;
+    BlobView v;
+    fill_blob_view(*d, blob_dev, &v);
+    return launch_transcode_p4(v, static_cast<uint8_t *>(p4_dev), static_cast<uint32_t *>(ws), as_stream(stream));
+}
+
+extern "C" uw_status uw_matmul_palette4(const uw_desc *d, const void *blob_dev, const void *p4_dev,
+                                        const uint16_t *x, int64_t batch, uint16_t *y, int32_t variant, void *ws,
+                                        size_t ws_bytes, void *stream) {
+    if (!d || !blob_dev || !p4_dev || !x || !y || !ws || batch <= 0 || (reinterpret_cast<uintptr_t>(x) & 15) ||
+        (reinterpret_cast<uintptr_t>(p4_dev) & 15))
+        return UW_ERR_INVALID_ARG;
+    if (variant >= kGemvVariants)
+        return UW_ERR_INVALID_ARG;
+    const int v = variant < 0 ? default_p4_variant(d->rows, d->cols, batch) : variant;
+    const WsLayout L = layout_for(d->rows, d->cols, batch, UW_STRATEGY_FUSED, v);
+    if (ws_bytes < L.total)
+        return UW_ERR_BUFFER_TOO_SMALL;
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    GemvParams p{};
+    fill_blob_view(*d, blob_dev, &p.v);
+    p.p4 = static_cast<const uint8_t *>(p4_dev);
+    p.x = x;
+    p.y = y;
+    p.partial = reinterpret_cast<float *>(wsb + L.partial);
+    p.counters = reinterpret_cast<uint32_t *>(wsb + L.counters);
+    p.status = reinterpret_cast<uint32_t *>(wsb + L.status);
+    p.rows = d->rows;
+    p.cols = d->cols;
+    p.batch = batch;
+    return run_gemv(p, v, kSrcPalette4, as_stream(stream));
 }
 
 extern "C" uw_status uw_matmul_bf16(const uint16_t *w, int64_t rows, int64_t cols, const uint16_t *x,
@@ -508,7 +580,7 @@ extern "C" uw_status uw_matmul_bf16(const uint16_t *w, int64_t rows, int64_t col
     p.rows = rows;
     p.cols = cols;
     p.batch = batch;
-    return run_gemv(p, v, false, as_stream(stream));
+    return run_gemv(p, v, kSrcBf16, as_stream(stream));
 }
 
 extern "C" uw_status uw_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h, int64_t n, void *stream) {
@@ -518,7 +590,10 @@ extern "C" uw_status uw_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h
 }
 
 extern "C" int32_t uw_variant_count(int32_t strategy) {
-    return (strategy == UW_STRATEGY_FUSED || strategy == UW_STRATEGY_DECOMPRESS_GEMM) ? kGemvVariants : 0;
+    return (strategy == UW_STRATEGY_FUSED || strategy == UW_STRATEGY_DECOMPRESS_GEMM ||
+            strategy == UW_STRATEGY_PALETTE4)
+               ? kGemvVariants
+               : 0;
 }
 
 extern "C" const char *uw_variant_name(int32_t strategy, int32_t variant) {

@@ -72,6 +72,7 @@ struct BlobView {
     // kLmax-bit prefix -> (exponent << 4) | code length; 0 where no code
     // starts with that prefix.
     uint16_t prefix[kPrefixEntries];
+    uint8_t palette[16];  // exponent of each palette index (unused entries 0)
 };
 
 constexpr int kWindowBits = 2 * kLmax;                     // two codes always fit
@@ -134,6 +135,26 @@ __device__ __forceinline__ void build_prefix_zero(const DecodeShared &s, const B
 __device__ __forceinline__ void build_tables(const DecodeShared &s, const BlobView &v) {
     build_prefix_zero(s, v);
     for (int w = threadIdx.x; w < kLutEntries; w += blockDim.x)
+        s.lut[w] = pair_entry(s.prefix, uint32_t(w));
+}
+
+// The pair table with palette indices in place of exponents (index of the
+// first code at bits 7..10, of the second at bits 23..26), for transcoding
+// to the palette-4 form.  Must be followed by __syncthreads() before use.
+__device__ __forceinline__ void build_tables_palette_index(const DecodeShared &s, const BlobView &v) {
+    const int tid = threadIdx.x;
+    if (tid < kPrefixEntries) {
+        const uint32_t p = v.prefix[tid];
+        uint32_t idx = 0;
+        for (int i = 15; i >= 0; i--)  // the first palette entry with this exponent
+            if (v.palette[i] == (p >> 4))
+                idx = uint32_t(i);
+        s.prefix[tid] = uint16_t((idx << 4) | (p & 15u));
+    }
+    if (tid < kZeroWords)
+        s.zero[tid] = 0u;
+    __syncthreads();
+    for (int w = tid; w < kLutEntries; w += blockDim.x)
         s.lut[w] = pair_entry(s.prefix, uint32_t(w));
 }
 
@@ -403,13 +424,13 @@ __device__ __forceinline__ void escape_read(uint32_t ebase, uint32_t esc_mask, u
         e[c] = lds128(a + 16u * c);
 }
 
-// One step: decode the exponents of weights 2i, 2i+1 and merge them with the
-// sign+mantissa bytes.  `sm4` holds the bytes of weights 4*(i/2)..+3; `lut`
-// is the shared address of the pair table (kShiftShared), or of the lane's
-// column of the private copies, i.e. their base + 4 * lane (kShiftPrivate).
-// `I` is a compile-time constant once the caller's 32-step loop is unrolled.
+// One step of the lane's stream: look up the next two codes and advance past
+// them; returns the table entry (both exponents in BF16 position, or both
+// palette indices, and the bits taken).  `lut` is the shared address of the
+// pair table (kShiftShared), or of the lane's column of the private copies,
+// i.e. their base + 4 * lane (kShiftPrivate).
 template <int kShift = kShiftShared>
-__device__ __forceinline__ uint32_t decode_pair(LaneStream &ls, uint32_t lut, int I, uint32_t sm4) {
+__device__ __forceinline__ uint32_t decode_entry(LaneStream &ls, uint32_t lut) {
     // window << kShift = funnel(lo, hi) >> c, masked; entry = table[window];
     // c += entry (its bits above 6 only add junk above the exact low 7);
     // when bit 5 of c flips the window has moved into the next word: shift
@@ -438,6 +459,15 @@ __device__ __forceinline__ uint32_t decode_pair(LaneStream &ls, uint32_t lut, in
         : "=r"(ent), "+r"(ls.lo), "+r"(ls.hi), "+r"(ls.nx), "+r"(ls.c), "+r"(ls.wp)
         : "r"(lut), "n"((kLutEntries - 1) << kShift)
         : "memory");
+    return ent;
+}
+
+// One step: decode the exponents of weights 2i, 2i+1 and merge them with the
+// sign+mantissa bytes.  `sm4` holds the bytes of weights 4*(i/2)..+3.  `I`
+// is a compile-time constant once the caller's 32-step loop is unrolled.
+template <int kShift = kShiftShared>
+__device__ __forceinline__ uint32_t decode_pair(LaneStream &ls, uint32_t lut, int I, uint32_t sm4) {
+    const uint32_t ent = decode_entry<kShift>(ls, lut);
     // sign-replicate byte permute: bytes (b0, sign(b0), b1, sign(b1)) for the
     // even pair of the word, (b2, sign(b2), b3, sign(b3)) for the odd one
     const uint32_t y = prmt(sm4, 0u, (I & 1) ? 0xB3A2u : 0x9180u);

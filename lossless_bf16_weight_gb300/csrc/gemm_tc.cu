@@ -108,9 +108,11 @@ __device__ __forceinline__ void sm_chunks(const uint8_t *g_lane, uint32_t stride
         sm[c] = __ldg(reinterpret_cast<const uint4 *>(g_lane + c * stride));
 }
 
-template <int G, bool kCompressed, bool kSmStaged>
+template <int G, int kSrc, bool kSmStaged>
 __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcParams p) {
     constexpr int P = 4 * G;  // producer warps
+    constexpr bool kCompressed = kSrc == kSrcHuffman;
+    constexpr bool kP4 = kSrc == kSrcPalette4;
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[2 * kTcMaxStages + 1];
     __shared__ __align__(8) uint64_t pbars[P * kPairStages];
@@ -167,6 +169,14 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
     PairMeta *meta = &metas[producer ? warp * kPairStages : 0];
     DecodeShared ds{};
     uint32_t nissued = 0, o_next = 0;
+    // palette-4 source: one 256-entry pair table (entry b = palette[b >> 4] << 23 |
+    // palette[b & 15] << 7) where the decode tables would be
+    const uint32_t ptab = smem_addr(dec);
+    if constexpr (kP4) {
+        for (int b = threadIdx.x; b < 256; b += blockDim.x)
+            reinterpret_cast<uint32_t *>(dec)[b] =
+                (uint32_t(v.palette[b >> 4]) << 23) | (uint32_t(v.palette[b & 15]) << 7);
+    }
     if (kCompressed) {
         ds = carve_common(dec);
         // the first two pairs' offsets in one round trip, the tables built
@@ -328,6 +338,49 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
                         qB[I] = 0u;
                     }
                 }
+            } else if constexpr (kP4) {
+                // 4-bit palette indices and sign+mantissa bytes of the lane's row,
+                // rebuilt through the pair table, one tile after the other; escaped
+                // groups from their raw exponents
+                const bool ok = rb_ok && lane < R;
+                const uint32_t lc = ok ? uint32_t(lane) : 0u;
+                auto rebuild = [&](uint32_t kg, bool has, uint32_t (&q)[32]) {
+                    const uint64_t q0 = uint64_t(kTileRows) * rb * gpr + uint64_t(R) * kg;
+                    uint4 ix[2], sx[4];
+#pragma unroll
+                    for (int c = 0; c < 2; c++)
+                        ix[c] = __ldg(reinterpret_cast<const uint4 *>(p.p4 + 32 * q0 + 16 * lc + c * 16 * R));
+#pragma unroll
+                    for (int c = 0; c < 4; c++)
+                        sx[c] = __ldg(reinterpret_cast<const uint4 *>(v.sm + 64 * q0 + 16 * lc + c * 16 * R));
+                    const uint32_t g = __ldg(v.glen + q0 + lc);
+#pragma unroll
+                    for (int I = 0; I < 32; I++) {
+                        const uint32_t b = (word4(ix[I >> 4], (I >> 2) & 3) >> (8 * (I & 3))) & 0xFFu;
+                        q[I] = lop3_merge(prmt(sm_word(sx, I >> 1), 0u, (I & 1) ? 0xB3A2u : 0x9180u),
+                                          lds32(ptab + 4u * b));
+                    }
+                    const uint32_t em = __ballot_sync(0xffffffffu, ok && has && g == 0u);
+                    if ((em >> lane) & 1u) {
+                        const uint32_t t = rb * gpr + kg;
+                        const uint4 *ep = reinterpret_cast<const uint4 *>(
+                            v.esc + 64 * uint64_t(__ldg(v.tesc + t) + __popc(em & ((1u << lane) - 1u))));
+                        uint4 e[4];
+#pragma unroll
+                        for (int c = 0; c < 4; c++)
+                            e[c] = __ldg(ep + c);
+#pragma unroll
+                        for (int I = 0; I < 32; I++)
+                            q[I] = escape_pair(e, I, sm_word(sx, I >> 1));
+                    }
+                    if (!(ok && has)) {
+#pragma unroll
+                        for (int I = 0; I < 32; I++)
+                            q[I] = 0u;
+                    }
+                };
+                rebuild(kgA, true, qA);
+                rebuild(hasB ? kgA + 1 : kgA, hasB, qB);
             } else {
                 const int64_t n = int64_t(rb) * kTileRows + lane;
                 const bool ok = rb_ok && n < p.rows;
@@ -438,31 +491,41 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
         p.counters[mb] = 0;
 }
 
-template <int G, bool kCompressed, bool kSmStaged>
+template <int G, int kSrc, bool kSmStaged>
 uw_status launch_tc_one(const TcParams &p, size_t smem, cudaStream_t stream) {
-    auto kern = gemm_tc_kernel<G, kCompressed, kSmStaged>;
+    auto kern = gemm_tc_kernel<G, kSrc, kSmStaged>;
     if (!ensure_smem(kern, smem))
         return UW_ERR_CUDA;
     const dim3 grid(unsigned((p.rows + kTcM - 1) / kTcM), unsigned(p.splits));
     return launch_overlapped(kern, grid, dim3((4 * G + 1) * 32), smem, stream, p) == cudaSuccess ? UW_OK : UW_ERR_CUDA;
 }
 
+template <int kSrc, bool kSmStaged>
+uw_status launch_tc_g(const TcParams &p, int G, size_t smem, cudaStream_t stream) {
+    return G == 1 ? launch_tc_one<1, kSrc, kSmStaged>(p, smem, stream)
+           : G == 2 ? launch_tc_one<2, kSrc, kSmStaged>(p, smem, stream)
+                    : launch_tc_one<3, kSrc, kSmStaged>(p, smem, stream);
+}
+
 // Tensor-memory columns before the A stages (the accumulator's Np, rounded up to 32).
 uint32_t a0_col(int Np) { return (uint32_t(Np) + 31u) & ~31u; }
 
-// Shared memory of a launch; `staged`: the producers' pair stages hold the
-// sign+mantissa bytes too (otherwise the producers read those from L2).
-size_t tc_smem(int G, int S, int Np, bool compressed, bool staged, uint32_t tdata) {
+// Shared memory of a launch; `staged` (Huffman source): the producers' pair
+// stages hold the sign+mantissa bytes too (otherwise the producers read
+// those from L2).
+size_t tc_smem(int G, int S, int Np, int src, bool staged, uint32_t tdata) {
     size_t s = 1024 + size_t(S) * size_t(Np) * 128;
-    if (compressed)
+    if (src == kSrcHuffman)
         s += size_t(kCommonSmemBytes) + 128 +
              size_t(4 * G) * kPairStages * (staged ? pair_stage_bytes(tdata) : code_stage_bytes(tdata));
+    else if (src == kSrcPalette4)
+        s += 256 * 4;  // the pair table
     return s;
 }
 
-int tc_stages(int G, int Np, bool compressed, bool staged, uint32_t tdata) {
+int tc_stages(int G, int Np, int src, bool staged, uint32_t tdata) {
     int S = std::min<int>(kTcMaxStages, int((kTmemCols - a0_col(Np)) / 32));
-    while (S > 1 && tc_smem(G, S, Np, compressed, staged, tdata) > size_t(kMaxSmemPerBlock - 1024))
+    while (S > 1 && tc_smem(G, S, Np, src, staged, tdata) > size_t(kMaxSmemPerBlock - 1024))
         S--;
     return S;
 }
@@ -470,10 +533,12 @@ int tc_stages(int G, int Np, bool compressed, bool staged, uint32_t tdata) {
 }  // namespace
 
 size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed, uint32_t tdata) {
-    return tc_smem(G, S, Np, compressed, false, tdata);
+    return tc_smem(G, S, Np, compressed ? kSrcHuffman : kSrcBf16, false, tdata);
 }
 
-int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tdata) { return tc_stages(G, Np, compressed, false, tdata); }
+int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tdata) {
+    return tc_stages(G, Np, compressed ? kSrcHuffman : kSrcBf16, false, tdata);
+}
 
 int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits) {
     if (splits <= 1)
@@ -482,7 +547,7 @@ int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits) {
     return (rows + kTcM - 1) / kTcM * splits * np * kTcM;
 }
 
-uw_status launch_gemm_tc(const TcParams &base, int G, bool compressed, cudaStream_t stream) {
+uw_status launch_gemm_tc(const TcParams &base, int G, int src, cudaStream_t stream) {
     const int64_t gpr = base.cols / kGroup;
     if (base.splits < 1 || base.splits > gpr || G < 1 || G > 3)
         return UW_ERR_UNSUPPORTED;
@@ -496,26 +561,23 @@ uw_status launch_gemm_tc(const TcParams &base, int G, bool compressed, cudaStrea
         p.Np = int((p.batch + 15) / 16 * 16);
         p.a0col = a0_col(p.Np);
         p.tmem_cols = kTmemCols;
-        // stage the sign+mantissa bytes in shared memory when that leaves each
-        // producer group its two K steps (and some slack); read them from L2 otherwise
-        bool staged = compressed && tc_stages(G, p.Np, true, true, p.v.tdata) >= 2 * G + 2;
-        p.S = tc_stages(G, p.Np, compressed, staged, p.v.tdata);
+        // Huffman source: stage the sign+mantissa bytes in shared memory when that
+        // leaves each producer group its two K steps (and some slack); read them
+        // from L2 otherwise
+        const bool staged = src == kSrcHuffman && tc_stages(G, p.Np, kSrcHuffman, true, p.v.tdata) >= 2 * G + 2;
+        p.S = tc_stages(G, p.Np, src, staged, p.v.tdata);
         if (p.S < 2 * G)
             return UW_ERR_UNSUPPORTED;  // each producer group works on two K steps at once
-        const size_t smem = tc_smem(G, p.S, p.Np, compressed, staged, p.v.tdata);
+        const size_t smem = tc_smem(G, p.S, p.Np, src, staged, p.v.tdata);
         uw_status s;
-        if (!compressed)
-            s = G == 1 ? launch_tc_one<1, false, false>(p, smem, stream)
-                : G == 2 ? launch_tc_one<2, false, false>(p, smem, stream)
-                         : launch_tc_one<3, false, false>(p, smem, stream);
+        if (src == kSrcBf16)
+            s = launch_tc_g<kSrcBf16, false>(p, G, smem, stream);
+        else if (src == kSrcPalette4)
+            s = launch_tc_g<kSrcPalette4, false>(p, G, smem, stream);
         else if (staged)
-            s = G == 1 ? launch_tc_one<1, true, true>(p, smem, stream)
-                : G == 2 ? launch_tc_one<2, true, true>(p, smem, stream)
-                         : launch_tc_one<3, true, true>(p, smem, stream);
+            s = launch_tc_g<kSrcHuffman, true>(p, G, smem, stream);
         else
-            s = G == 1 ? launch_tc_one<1, true, false>(p, smem, stream)
-                : G == 2 ? launch_tc_one<2, true, false>(p, smem, stream)
-                         : launch_tc_one<3, true, false>(p, smem, stream);
+            s = launch_tc_g<kSrcHuffman, false>(p, G, smem, stream);
         if (s != UW_OK)
             return s;
     }

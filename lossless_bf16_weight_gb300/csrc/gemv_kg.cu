@@ -343,7 +343,7 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
 
 template <int W>
 __device__ __forceinline__ void gemv_col_bf16(const GemvParams &p, int rb_per_cta) {
-    extern __shared__ __align__(16) unsigned char smem[];
+    extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t gpr = uint32_t(p.cols / kGroup);
     const uint32_t nrb = uint32_t((p.rows + kTileRows - 1) / kTileRows);
@@ -393,30 +393,145 @@ __device__ __forceinline__ void gemv_col_bf16(const GemvParams &p, int rb_per_ct
     cta_reduce<W>(p, red, rb0, nrbc);
 }
 
-template <int W, bool kCompressed, bool kPrivate>
+// Palette-4 source (the blog's palette pipelines): the twin's loop -- same
+// warps, groups and order of every sum, so the results are bit-identical --
+// with each group's BF16 pairs rebuilt from its 4-bit palette indices and its
+// sign+mantissa bytes.  A byte of two indices is looked up in a 256-entry
+// pair table (entry b = palette[b >> 4] << 23 | palette[b & 15] << 7, both
+// exponents in BF16 position) kept as 32 lane-private copies at a 32 KB-
+// aligned shared address, so that one three-input logic op both masks the
+// byte out of the index word and adds the lane's column, and every lookup
+// is one shared-memory wavefront.  Escaped groups (glen 0) take their
+// exponents from the blob's escape section instead.
+template <int W>
+__device__ __forceinline__ void gemv_col_p4(const GemvParams &p, int rb_per_cta) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const BlobView &v = p.v;
+    const uint32_t gpr = v.gpr;
+    const uint32_t nrb = v.nfull + (v.tail_rows ? 1u : 0u);
+    const uint32_t rb0 = blockIdx.x * uint32_t(rb_per_cta);
+    const uint32_t rb1 = rb0 + uint32_t(rb_per_cta) < nrb ? rb0 + uint32_t(rb_per_cta) : nrb;
+    const uint32_t nrbc = rb1 - rb0;
+    uint32_t k0, k1;
+    warp_cols(gpr, warp, W, k0, k1);
+
+    // shared memory: [pad to 32 KB][pair table 256 x 32 lanes][x slab gpr x 32 pairs]
+    // [warp partials rb_per_cta x W x 32]
+    const uint32_t base = smem_addr(smem);
+    const uint32_t tab = (base + 32767u) & ~32767u;
+    unsigned char *after = smem + (tab - base) + kP4TableBytes;
+    uint32_t *xs = reinterpret_cast<uint32_t *>(after);
+    float *red = reinterpret_cast<float *>(after + size_t(gpr) * 128);
+    for (int i = threadIdx.x; i < 256 * 8; i += blockDim.x) {
+        const uint32_t b = uint32_t(i) >> 3;
+        const uint32_t e = (uint32_t(v.palette[b >> 4]) << 23) | (uint32_t(v.palette[b & 15u]) << 7);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" :: "r"(tab + 16u * uint32_t(i)), "r"(e) : "memory");
+    }
+    grid_dep_wait();  // x may come from the kernel before
+    load_x_all(p, xs, gpr);
+    __syncthreads();
+    const uint32_t lbase = tab + 4u * uint32_t(lane);  // bits 7..14 clear
+
+#pragma unroll 1
+    for (uint32_t rl = 0; rl < nrbc; rl++) {
+        const uint32_t rb = rb0 + rl;
+        const uint32_t R = rb < v.nfull ? uint32_t(kTileRows) : v.tail_rows;
+        const bool ok = uint32_t(lane) < R;
+        const uint32_t lc = ok ? uint32_t(lane) : 0u;
+        const uint64_t qrb = uint64_t(kTileRows) * rb * gpr;  // first group of the row block
+        float s_w = 0.f;
+        uint4 ic[2], sc[4], in_[2], sn[4];
+        uint32_t gc = 0, gn = 0;
+        auto fetch = [&](uint32_t kg, uint4 (&ix)[2], uint4 (&sx)[4], uint32_t &g) {
+            const uint64_t q0 = qrb + uint64_t(R) * kg;
+            const uint8_t *ip = p.p4 + 32 * q0 + 16 * lc;
+            const uint8_t *sp = v.sm + 64 * q0 + 16 * lc;
+#pragma unroll
+            for (int c = 0; c < 2; c++)
+                ix[c] = __ldg(reinterpret_cast<const uint4 *>(ip + c * 16 * R));
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+                sx[c] = __ldg(reinterpret_cast<const uint4 *>(sp + c * 16 * R));
+            g = __ldg(v.glen + q0 + lc);
+        };
+        if (k0 < k1)
+            fetch(k0, in_, sn, gn);
+#pragma unroll 1
+        for (uint32_t kg = k0; kg < k1; kg++) {
+#pragma unroll
+            for (int c = 0; c < 2; c++)
+                ic[c] = in_[c];
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+                sc[c] = sn[c];
+            gc = gn;
+            if (kg + 1 < k1)
+                fetch(kg + 1, in_, sn, gn);
+            const uint32_t xaddr = smem_addr(xs) + kg * 128u;
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int I = 0; I < 32; I++) {
+                const uint32_t iw = word4(ic[I >> 4], (I >> 2) & 3);
+                const int sh = 8 * (I & 3) - 7;  // byte I&3 of the word, times 128
+                const uint32_t moved = sh < 0 ? iw << -sh : iw >> sh;
+                uint32_t off;
+                asm("lop3.b32 %0, %1, 0x7F80, %2, 0xEA;" : "=r"(off) : "r"(moved), "r"(lbase));  // (a & b) | c
+                const uint32_t y = prmt(sm_word(sc, I >> 1), 0u, (I & 1) ? 0xB3A2u : 0x9180u);
+                fma_bf16x2(a0, a1, lop3_merge(y, lds32(off)), lds32(xaddr + 4u * I));
+            }
+            // escaped groups: exponents from the escape section
+            const uint32_t em = __ballot_sync(0xffffffffu, ok && gc == 0u);
+            if ((em >> lane) & 1u) {
+                const uint32_t rank = __popc(em & ((1u << lane) - 1u));
+                const uint32_t t = rb * gpr + kg;
+                const uint4 *ep = reinterpret_cast<const uint4 *>(v.esc + 64 * uint64_t(__ldg(v.tesc + t) + rank));
+                uint4 e[4];
+#pragma unroll
+                for (int c = 0; c < 4; c++)
+                    e[c] = __ldg(ep + c);
+                a0 = 0.f;
+                a1 = 0.f;
+#pragma unroll
+                for (int I = 0; I < 32; I++)
+                    fma_bf16x2(a0, a1, escape_pair(e, I, sm_word(sc, I >> 1)), lds32(xaddr + 4u * I));
+            }
+            s_w = s_w + (a0 + a1);
+        }
+        red[(rl * W + warp) * 32 + lane] = s_w;
+    }
+    __syncthreads();
+    cta_reduce<W>(p, red, rb0, nrbc);
+}
+
+template <int W, int kSrc, bool kPrivate>
 __global__ void __launch_bounds__(W * 32, 1) gemv_kg_kernel(const GemvParams p, int rb_per_cta) {
     grid_dep_launch();
-    if constexpr (kCompressed)
+    if constexpr (kSrc == kSrcHuffman)
         gemv_col_compressed<W, kPrivate>(p, rb_per_cta);
+    else if constexpr (kSrc == kSrcPalette4)
+        gemv_col_p4<W>(p, rb_per_cta);
     else
         gemv_col_bf16<W>(p, rb_per_cta);
 }
 
-size_t kg_smem(int warps, int rb_per_cta, bool compressed, bool priv, uint32_t tdata, int gpr) {
+size_t kg_smem(int warps, int rb_per_cta, int src, bool priv, uint32_t tdata, int gpr) {
     const size_t red = size_t(rb_per_cta) * warps * 128;
-    if (!compressed)
+    if (src == kSrcBf16)
         return size_t(gpr) * 128 + red;
+    if (src == kSrcPalette4)  // worst-case pad to the 32 KB boundary, the table, x, partials
+        return 32768 + size_t(kP4TableBytes) + size_t(gpr) * 128 + red;
     const size_t sbytes = priv ? code_stage_bytes(tdata) : pair_stage_bytes(tdata);
     return (priv ? size_t(kPrivateLutBytes) : 0) + size_t(kCommonSmemBytes) + red + 128 +
            size_t(warps) * kPairStages * sbytes;
 }
 
-template <int W, bool kCompressed, bool kPrivate>
+template <int W, int kSrc, bool kPrivate>
 uw_status launch_kg_one(const GemvParams &p, int rb_per_cta, cudaStream_t stream) {
-    const size_t smem = kg_smem(W, rb_per_cta, kCompressed, kPrivate, p.v.tdata, int(p.cols / kGroup));
+    const size_t smem = kg_smem(W, rb_per_cta, kSrc, kPrivate, p.v.tdata, int(p.cols / kGroup));
     if (smem > size_t(kMaxSmemPerBlock) - 1024)
         return UW_ERR_UNSUPPORTED;
-    auto kern = gemv_kg_kernel<W, kCompressed, kPrivate>;
+    auto kern = gemv_kg_kernel<W, kSrc, kPrivate>;
     if (!ensure_smem(kern, smem))
         return UW_ERR_CUDA;
     const int64_t nrb = (p.rows + kTileRows - 1) / kTileRows;
@@ -425,34 +540,35 @@ uw_status launch_kg_one(const GemvParams &p, int rb_per_cta, cudaStream_t stream
                                                                                              : UW_ERR_CUDA;
 }
 
-// Compressed source: the private-table form when its shared memory fits,
-// else one shared table.  Both decode the same weights, so the results are
+// Huffman source: the private-table form when its shared memory fits, else
+// one shared table.  Both decode the same weights, so the results are
 // identical.
 template <int W>
-uw_status launch_kg_compressed(const GemvParams &p, int rb_per_cta, cudaStream_t stream) {
-    if (kg_smem(W, rb_per_cta, true, true, p.v.tdata, int(p.cols / kGroup)) <= size_t(kMaxSmemPerBlock) - 1024)
-        return launch_kg_one<W, true, true>(p, rb_per_cta, stream);
-    return launch_kg_one<W, true, false>(p, rb_per_cta, stream);
+uw_status launch_kg_src(const GemvParams &p, int rb_per_cta, int src, cudaStream_t stream) {
+    if (src == kSrcBf16)
+        return launch_kg_one<W, kSrcBf16, false>(p, rb_per_cta, stream);
+    if (src == kSrcPalette4)
+        return launch_kg_one<W, kSrcPalette4, false>(p, rb_per_cta, stream);
+    if (kg_smem(W, rb_per_cta, kSrcHuffman, true, p.v.tdata, int(p.cols / kGroup)) <= size_t(kMaxSmemPerBlock) - 1024)
+        return launch_kg_one<W, kSrcHuffman, true>(p, rb_per_cta, stream);
+    return launch_kg_one<W, kSrcHuffman, false>(p, rb_per_cta, stream);
 }
 
 }  // namespace
 
 size_t gemv_kg_smem_bytes(int warps, int rb_per_cta, bool compressed, uint32_t tdata, int gpr) {
-    return kg_smem(warps, rb_per_cta, compressed, false, tdata, gpr);
+    return kg_smem(warps, rb_per_cta, compressed ? kSrcHuffman : kSrcBf16, false, tdata, gpr);
 }
 
-uw_status launch_gemv_kg(const GemvParams &p, int warps, int rb_per_cta, bool compressed, cudaStream_t stream) {
+uw_status launch_gemv_kg(const GemvParams &p, int warps, int rb_per_cta, int src, cudaStream_t stream) {
     if (p.batch != 1 || rb_per_cta < 1)
         return UW_ERR_UNSUPPORTED;
     if (uint64_t(p.rows / kTileRows + 1) * (p.cols / kGroup) >= (uint64_t(1) << 32))
         return UW_ERR_UNSUPPORTED;  // tile indices are 32-bit
     switch (warps) {
-        case 4: return compressed ? launch_kg_compressed<4>(p, rb_per_cta, stream)
-                                  : launch_kg_one<4, false, false>(p, rb_per_cta, stream);
-        case 8: return compressed ? launch_kg_compressed<8>(p, rb_per_cta, stream)
-                                  : launch_kg_one<8, false, false>(p, rb_per_cta, stream);
-        case 16: return compressed ? launch_kg_compressed<16>(p, rb_per_cta, stream)
-                                   : launch_kg_one<16, false, false>(p, rb_per_cta, stream);
+        case 4: return launch_kg_src<4>(p, rb_per_cta, src, stream);
+        case 8: return launch_kg_src<8>(p, rb_per_cta, src, stream);
+        case 16: return launch_kg_src<16>(p, rb_per_cta, src, stream);
     }
     return UW_ERR_UNSUPPORTED;
 }

@@ -13,11 +13,20 @@
 namespace uw {
 
 constexpr int kMaxSmemPerBlock = 227 * 1024;
+
+// Where a matmul kernel gets its weights: uncompressed BF16 rows (the twin),
+// the Huffman-coded blob, or the palette-4 form (4-bit palette indices) next
+// to the blob's sign+mantissa bytes.
+constexpr int kSrcBf16 = 0;
+constexpr int kSrcHuffman = 1;
+constexpr int kSrcPalette4 = 2;
+constexpr int kP4TableBytes = 256 * 32 * 4;  // palette-4 pair table, 32 lane-private copies
 constexpr int kSmemPerSm = 228 * 1024 - 3 * 1024;  // minus the per-CTA reservation of 3 CTAs
 
 struct GemvParams {
     BlobView v;            // compressed weights (fused kernel)
     const uint16_t *w;     // uncompressed weights (twin kernel)
+    const uint8_t *p4;     // palette-4 indices (palette-4 kernels; sign+mantissa etc. from v)
     const uint16_t *x;     // [batch, cols]
     uint16_t *y;           // [batch, rows]
     float *partial;        // [row blocks * splits][bp][32] split partial sums
@@ -33,7 +42,7 @@ uw_status launch_gemv(const GemvParams &p, int warps, int bp, bool compressed, c
 // Batch-1 GEMV on column-range CTAs: W warps splitting all 64-column groups,
 // rb_per_cta row blocks per CTA, one CTA per SM.
 size_t gemv_kg_smem_bytes(int warps, int rb_per_cta, bool compressed, uint32_t tdata, int gpr);
-uw_status launch_gemv_kg(const GemvParams &p, int warps, int rb_per_cta, bool compressed, cudaStream_t stream);
+uw_status launch_gemv_kg(const GemvParams &p, int warps, int rb_per_cta, int src, cudaStream_t stream);
 
 // Tensor-core matmul (gemm_tc.cu): CTAs of 4G producer warps + 1 MMA warp,
 // 128 rows of W each, `splits` K ranges; batches above kTcMaxBatch run as
@@ -42,6 +51,7 @@ constexpr int kTcMaxBatch = 256;
 struct TcParams {
     BlobView v;            // compressed weights (fused kernel)
     const uint16_t *w;     // uncompressed weights (twin kernel)
+    const uint8_t *p4;     // palette-4 indices (palette-4 kernels; sign+mantissa etc. from v)
     const uint16_t *x;     // [batch, cols]
     uint16_t *y;           // [batch, rows]
     float *partial;        // [row blocks of 128][splits][Np][128] split partial sums
@@ -56,9 +66,11 @@ struct TcParams {
 size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed, uint32_t tdata);
 int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tdata);
 int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits);
-uw_status launch_gemm_tc(const TcParams &p, int G, bool compressed, cudaStream_t stream);
+uw_status launch_gemm_tc(const TcParams &p, int G, int src, cudaStream_t stream);
 
 uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status, cudaStream_t stream);
+// Palette-4 form of a blob: rows*cols/2 bytes at p4 (16-byte aligned).
+uw_status launch_transcode_p4(const BlobView &v, uint8_t *p4, uint32_t *status, cudaStream_t stream);
 uw_status launch_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h, int64_t n, cudaStream_t stream);
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device);

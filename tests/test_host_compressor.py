@@ -122,3 +122,15 @@ def test_compression_ratio_and_statistics(lib):
     mean_len = d.code_bits / (64 * (d.n_groups - d.n_escaped))
     assert 2.8 < mean_len < 3.1
     assert d.n_escaped / d.n_groups < 0.01
+
+
+def test_palette4_host_side(lib):
+    w = wl.normal_weights(96, 256, 0.02, seed=2)
+    d = lib.blob_info(lib.compress(w))
+    assert lib.palette4_bytes(d) == 96 * 256 // 2
+    L = lib.load()
+    # argument checks happen before any device work
+    assert L.uw_transcode_palette4(ctypes.byref(d), None, None, None, 0, None) == 1
+    assert L.uw_matmul_palette4(ctypes.byref(d), None, None, None, 1, None, -1, None, 0, None) == 1
+    assert lib.variant_count(lib.STRATEGY_PALETTE4) == lib.variant_count(lib.STRATEGY_FUSED)
+
