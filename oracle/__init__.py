@@ -84,6 +84,7 @@ def _L():
         lib.uwo_matmul_f64.argtypes = [P, I64, P, I64, I64, I64, I64, P, P]
         lib.uwo_swiglu_f64.argtypes = [P, P, I64, P]
         lib.uwo_palette4.argtypes = [P, I64, I64, P, ctypes.c_int, P]
+        lib.uwo_exponents.argtypes = [P, I64, I64, P]
         lib.uwo_join.argtypes = [ctypes.c_uint, ctypes.c_uint]
         lib.uwo_join.restype = ctypes.c_uint16
         _lib = lib
@@ -244,3 +245,14 @@ def palette4(w, pal) -> np.ndarray:
     out = np.zeros(rows * cols // 2, np.uint8)
     _L().uwo_palette4(_p(w), rows, cols, _p(p), len(pal), _p(out))
     return out
+
+
+def exponents(w) -> np.ndarray:
+    """[EXPONENT] the exponent byte of every weight in the library's exponent
+    form (laid out like the sign+mantissa section; rows*cols bytes)."""
+    w = _u16(w)
+    rows, cols = w.shape
+    out = np.zeros(rows * cols, np.uint8)
+    _L().uwo_exponents(_p(w), rows, cols, _p(out))
+    return out
+

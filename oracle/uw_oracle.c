@@ -23,6 +23,10 @@
  *               one decision per row, no per-element branch.
  *   [LUT16K]    the decoder keeps a ~16 KB Huffman lookup table in SMEM.
  *   [MATMUL]    the compressed weights feed y = x W^T (decode once, multiply).
+ *   [EXPONENT]  the exponent-only pipeline: only the exponent bytes are
+ *               decoded to memory, and the matmul merges them with the raw
+ *               sign+mantissa bytes (paragraph on the four execution
+ *               pipelines).
  *   [PALETTE]   the palette pipelines: Huffman-coded exponents turned into
  *               4-bit palette indices (at run time or once at model load),
  *               from which the matmul rebuilds BF16 on the fly (paragraphs
@@ -628,6 +632,30 @@ int uwo_decompress(const uint8_t *blob, int64_t bytes, uint16_t *w)
         }
     }
     return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * [EXPONENT] the exponent byte of every weight (escaped groups included),
+ * laid out like the blob's sign+mantissa section: group q = 32*rb*gpr +
+ * R*kg + j (row j of row block rb, R rows in the block) owns 64 bytes in four
+ * 16-byte chunks; chunk c (weights 16c .. 16c+15) sits at byte
+ * 64*q0 + (c*R + j)*16 of the buffer, q0 = 32*rb*gpr + R*kg, weight 16c + b
+ * at byte b of the chunk.  out: rows*cols bytes, overwritten.
+ */
+void uwo_exponents(const uint16_t *w, int64_t rows, int64_t cols, uint8_t *out)
+{
+    int64_t gpr = cols / UWO_GROUP;
+    for (int64_t n = 0; n < rows; n++) {
+        int64_t rb = n / UWO_TROWS, j = n % UWO_TROWS;
+        int64_t left = rows - rb * UWO_TROWS;
+        int64_t R = left < UWO_TROWS ? left : UWO_TROWS;
+        for (int64_t kg = 0; kg < gpr; kg++) {
+            int64_t q0 = UWO_TROWS * rb * gpr + R * kg;
+            for (int k = 0; k < UWO_GROUP; k++)
+                out[64 * q0 + ((k / 16) * R + j) * 16 + k % 16] =
+                    (uint8_t)((w[n * cols + kg * UWO_GROUP + k] >> 7) & 0xFFu);
+        }
+    }
 }
 
 /* ------------------------------------------------------------------------

@@ -332,6 +332,41 @@ def test_palette4_layout_and_round_trip(oracle, shape):
     assert np.array_equal(np.bincount(nib, minlength=16), want)
 
 
+# ---------------------------------------------------------------- exponent form
+
+def test_exponent_form_worked_example(oracle):
+    # One row: the exponents in weight order (chunk c = weights 16c..16c+15).
+    w, g = _worked_matrix()
+    assert list(oracle.exponents(w)) == [g["exponent_period"][k % 8] for k in range(64)]
+
+
+@pytest.mark.parametrize("shape", [(1, 64), (33, 128), (70, 192)])
+def test_exponent_form_is_the_sm_layout_of_exponents(oracle, shape):
+    # The blob's sign+mantissa section has the same layout: rebuilding every
+    # weight from (exponent form, sm section) at the same byte gives W back.
+    rows, cols = shape
+    w = wl.heavy_tailed_weights(rows, cols, seed=rows * 7 + cols)
+    blob, info = oracle.compress(w)
+    sm = np.frombuffer(blob, np.uint8)[info["off_sm"]: info["off_sm"] + rows * cols].astype(np.uint16)
+    ex = oracle.exponents(w).astype(np.uint16)
+    bits = ((sm & 0x80) << 8) | (ex << 7) | (sm & 0x7F)
+    # and the layout itself, read with whole-array reshapes
+    out = np.zeros(rows * cols, np.uint8)
+    e = ((w.astype(np.int64) >> 7) & 0xFF).astype(np.uint8)
+    gpr = cols // 64
+    for rb in range((rows + 31) // 32):
+        R = min(32, rows - 32 * rb)
+        blk = e[32 * rb: 32 * rb + R].reshape(R, gpr, 4, 16).transpose(1, 2, 0, 3)
+        out[64 * 32 * rb * gpr: 64 * 32 * rb * gpr + 64 * R * gpr] = blk.ravel()
+    assert np.array_equal(oracle.exponents(w), out)
+    want = np.zeros(rows * cols, np.uint16)
+    for rb in range((rows + 31) // 32):
+        R = min(32, rows - 32 * rb)
+        want[64 * 32 * rb * gpr: 64 * 32 * rb * gpr + 64 * R * gpr] = \
+            w[32 * rb: 32 * rb + R].reshape(R, gpr, 4, 16).transpose(1, 2, 0, 3).ravel()
+    assert np.array_equal(bits, want)
+
+
 # ---------------------------------------------------------------- round trips
 def test_round_trip_every_bf16_pattern(oracle):
     w = wl.all_bf16_patterns()
