@@ -69,12 +69,15 @@ typedef enum {
  * registers / shared memory and never writes the weights back.  PALETTE4
  * transcodes the Huffman codes into 4-bit palette indices in the workspace
  * (a quarter of the bytes a full decode writes), then multiplies from those
- * (uw_matmul_palette4). */
+ * (uw_matmul_palette4).  EXPONENT decodes only the exponent bytes into the
+ * workspace (half the bytes of a full decode), then multiplies, merging them
+ * with the raw sign+mantissa bytes (uw_matmul_exponents). */
 enum {
     UW_STRATEGY_DEFAULT = -1,
     UW_STRATEGY_DECOMPRESS_GEMM = 0,
     UW_STRATEGY_FUSED = 1,
-    UW_STRATEGY_PALETTE4 = 2
+    UW_STRATEGY_PALETTE4 = 2,
+    UW_STRATEGY_EXPONENT = 3
 };
 
 /* Description of a compressed matrix, filled by uw_blob_info from the blob
@@ -196,6 +199,31 @@ uw_status uw_transcode_palette4(const uw_desc *d, const void *blob_dev, void *p4
 uw_status uw_matmul_palette4(const uw_desc *d, const void *blob_dev, const void *p4_dev,
                              const uint16_t *x_dev, int64_t batch, uint16_t *y_dev, int32_t variant,
                              void *ws_dev, size_t ws_bytes, void *stream);
+
+/* The exponent form of a blob (the blog's exponent-only pipeline: only the
+ * exponent bytes are decoded to memory, and the matmul merges them with the
+ * raw sign+mantissa bytes; paragraph on the four execution pipelines).
+ * Every weight's exponent byte, escaped groups included, laid out like the
+ * blob's sign+mantissa section: group q owns 64 bytes in four 16-byte
+ * chunks, chunk c (weights 16c..16c+15) at byte 64*q0 + (c*R + j)*16 with q0
+ * and R as for the palette-4 form, weight 16c + b at byte b of the chunk.
+ *
+ * uw_exponent_bytes -- size of the form: rows * cols bytes. */
+uw_status uw_exponent_bytes(const uw_desc *d, size_t *bytes);
+
+/* uw_decode_exponents -- write the exponent form of the blob.
+ *   e_dev    uw_exponent_bytes(d) bytes of device memory, 16-byte aligned
+ *            (written).  Other arguments as for uw_transcode_palette4. */
+uw_status uw_decode_exponents(const uw_desc *d, const void *blob_dev, void *e_dev,
+                              void *ws_dev, size_t ws_bytes, void *stream);
+
+/* uw_matmul_exponents -- y = x W^T from the exponent form e_dev (made by
+ * uw_decode_exponents from blob_dev) plus the blob's sign+mantissa bytes.
+ * Arguments, variants and the bit-identity guarantee as for
+ * uw_matmul_palette4. */
+uw_status uw_matmul_exponents(const uw_desc *d, const void *blob_dev, const void *e_dev,
+                              const uint16_t *x_dev, int64_t batch, uint16_t *y_dev, int32_t variant,
+                              void *ws_dev, size_t ws_bytes, void *stream);
 
 /* uw_autotune -- measure every (strategy, variant) candidate for each batch
  * size and return the fastest per batch (the blog's autotuner, which picks a

@@ -20,7 +20,7 @@ UW_OK = 0
 STATUS_NAMES = {0: "UW_OK", 1: "UW_ERR_INVALID_ARG", 2: "UW_ERR_SHAPE", 3: "UW_ERR_BUFFER_TOO_SMALL",
                 4: "UW_ERR_CORRUPT", 5: "UW_ERR_CUDA", 6: "UW_ERR_TIMEOUT", 7: "UW_ERR_UNSUPPORTED",
                 8: "UW_ERR_INTERNAL"}
-STRATEGY_DEFAULT, STRATEGY_DECOMPRESS_GEMM, STRATEGY_FUSED, STRATEGY_PALETTE4 = -1, 0, 1, 2
+STRATEGY_DEFAULT, STRATEGY_DECOMPRESS_GEMM, STRATEGY_FUSED, STRATEGY_PALETTE4, STRATEGY_EXPONENT = -1, 0, 1, 2, 3
 
 
 class UwError(RuntimeError):
@@ -72,6 +72,9 @@ SIGNATURES = [
     ("uw_palette4_bytes", ctypes.c_int, [ctypes.POINTER(Desc), ctypes.POINTER(_SZ)]),
     ("uw_transcode_palette4", ctypes.c_int, [ctypes.POINTER(Desc), _P, _P, _P, _SZ, _P]),
     ("uw_matmul_palette4", ctypes.c_int, [ctypes.POINTER(Desc), _P, _P, _P, _I64, _P, _I32, _P, _SZ, _P]),
+    ("uw_exponent_bytes", ctypes.c_int, [ctypes.POINTER(Desc), ctypes.POINTER(_SZ)]),
+    ("uw_decode_exponents", ctypes.c_int, [ctypes.POINTER(Desc), _P, _P, _P, _SZ, _P]),
+    ("uw_matmul_exponents", ctypes.c_int, [ctypes.POINTER(Desc), _P, _P, _P, _I64, _P, _I32, _P, _SZ, _P]),
     ("uw_check_status", ctypes.c_int, [_P, _P]),
     ("uw_variant_name", ctypes.c_char_p, [_I32, _I32]),
     ("uw_variant_count", ctypes.c_int32, [_I32]),
@@ -250,6 +253,29 @@ def matmul_palette4_status(desc: Desc, blob_dev, p4, x, y, ws, variant: int = -1
 def matmul_palette4(desc: Desc, blob_dev, p4, x, y, ws, variant: int = -1, stream=None):
     """y[batch, rows] = x W^T from the palette-4 form p4 (plus the blob)."""
     _check(matmul_palette4_status(desc, blob_dev, p4, x, y, ws, variant, stream), "uw_matmul_palette4")
+
+
+def exponent_bytes(desc: Desc) -> int:
+    n = _SZ(0)
+    _check(load().uw_exponent_bytes(ctypes.byref(desc), ctypes.byref(n)), "uw_exponent_bytes")
+    return int(n.value)
+
+
+def decode_exponents(desc: Desc, blob_dev, e_out, ws, stream=None):
+    """uw_decode_exponents: the exponent byte of every weight into e_out."""
+    _check(load().uw_decode_exponents(ctypes.byref(desc), _ptr(blob_dev), _ptr(e_out), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _stream(stream)), "uw_decode_exponents")
+
+
+def matmul_exponents_status(desc: Desc, blob_dev, e, x, y, ws, variant: int = -1, stream=None) -> int:
+    batch = x.shape[0] if x.dim() == 2 else 1
+    return int(load().uw_matmul_exponents(ctypes.byref(desc), _ptr(blob_dev), _ptr(e), _ptr(x), batch, _ptr(y),
+                                          variant, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def matmul_exponents(desc: Desc, blob_dev, e, x, y, ws, variant: int = -1, stream=None):
+    """y[batch, rows] = x W^T from the exponent form e (plus the blob)."""
+    _check(matmul_exponents_status(desc, blob_dev, e, x, y, ws, variant, stream), "uw_matmul_exponents")
 
 
 def swiglu(g, u, h, stream=None):

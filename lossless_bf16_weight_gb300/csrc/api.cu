@@ -151,6 +151,8 @@ WsLayout layout_for(int64_t rows, int64_t cols, int64_t batch, int strategy, int
         L.total = align_up(L.weights + 2 * uint64_t(rows) * uint64_t(cols), 256);
     else if (strategy == UW_STRATEGY_PALETTE4)  // the palette-4 form, 4 bits per weight
         L.total = align_up(L.weights + uint64_t(rows) * uint64_t(cols) / 2, 256);
+    else if (strategy == UW_STRATEGY_EXPONENT)  // the exponent form, a byte per weight
+        L.total = align_up(L.weights + uint64_t(rows) * uint64_t(cols), 256);
     return L;
 }
 
@@ -170,7 +172,7 @@ uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t 
     if (plan) {
         if (plan->strategy != UW_STRATEGY_DEFAULT) {
             if (plan->strategy != UW_STRATEGY_FUSED && plan->strategy != UW_STRATEGY_DECOMPRESS_GEMM &&
-                plan->strategy != UW_STRATEGY_PALETTE4)
+                plan->strategy != UW_STRATEGY_PALETTE4 && plan->strategy != UW_STRATEGY_EXPONENT)
                 return UW_ERR_INVALID_ARG;
             out->strategy = plan->strategy;
         }
@@ -181,8 +183,9 @@ uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t 
         }
     }
     if (out->variant < 0)
-        out->variant = out->strategy == UW_STRATEGY_PALETTE4 ? default_p4_variant(rows, cols, batch)
-                                                             : default_gemv_variant(rows, cols, batch);
+        out->variant = (out->strategy == UW_STRATEGY_PALETTE4 || out->strategy == UW_STRATEGY_EXPONENT)
+                           ? default_p4_variant(rows, cols, batch)
+                           : default_gemv_variant(rows, cols, batch);
     return UW_OK;
 }
 
@@ -214,8 +217,8 @@ uw_status run_gemv(GemvParams p, int variant, int src, cudaStream_t stream) {
         p.splits = gv.splits;
         return launch_gemv_kg(p, gv.warps, gv.rb, src, stream);
     }
-    if (src == kSrcPalette4)
-        return UW_ERR_UNSUPPORTED;  // no palette-4 row kernel
+    if (src == kSrcPalette4 || src == kSrcExponent)
+        return UW_ERR_UNSUPPORTED;  // no row kernel for the intermediate forms
     p.splits = gv.splits;
     const int64_t total = p.batch;
     for (int64_t b0 = 0; b0 < total; b0 += kMaxBatchChunk) {
@@ -499,13 +502,14 @@ extern "C" uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uin
         p.w = w;
         return run_gemv(p, rp.variant, kSrcBf16, as_stream(stream));
     }
-    if (rp.strategy == UW_STRATEGY_PALETTE4) {
-        uint8_t *p4 = wsb + L.weights;
-        s = launch_transcode_p4(p.v, p4, p.status, as_stream(stream));
+    if (rp.strategy == UW_STRATEGY_PALETTE4 || rp.strategy == UW_STRATEGY_EXPONENT) {
+        const bool pal = rp.strategy == UW_STRATEGY_PALETTE4;
+        uint8_t *form = wsb + L.weights;
+        s = launch_transcode(p.v, form, pal, p.status, as_stream(stream));
         if (s != UW_OK)
             return s;
-        p.p4 = p4;
-        return run_gemv(p, rp.variant, kSrcPalette4, as_stream(stream));
+        p.p4 = form;
+        return run_gemv(p, rp.variant, pal ? kSrcPalette4 : kSrcExponent, as_stream(stream));
     }
     return run_gemv(p, rp.variant, kSrcHuffman, as_stream(stream));
 }
@@ -525,14 +529,15 @@ extern "C" uw_status uw_transcode_palette4(const uw_desc *d, const void *blob_de
         return UW_ERR_BUFFER_TOO_SMALL;
     BlobView v;
     fill_blob_view(*d, blob_dev, &v);
-    return launch_transcode_p4(v, static_cast<uint8_t *>(p4_dev), static_cast<uint32_t *>(ws), as_stream(stream));
+    return launch_transcode(v, static_cast<uint8_t *>(p4_dev), true, static_cast<uint32_t *>(ws), as_stream(stream));
 }
 
-extern "C" uw_status uw_matmul_palette4(const uw_desc *d, const void *blob_dev, const void *p4_dev,
-                                        const uint16_t *x, int64_t batch, uint16_t *y, int32_t variant, void *ws,
-                                        size_t ws_bytes, void *stream) {
-    if (!d || !blob_dev || !p4_dev || !x || !y || !ws || batch <= 0 || (reinterpret_cast<uintptr_t>(x) & 15) ||
-        (reinterpret_cast<uintptr_t>(p4_dev) & 15))
+namespace uw {
+namespace {
+uw_status matmul_formed(const uw_desc *d, const void *blob_dev, const void *form_dev, const uint16_t *x, int64_t batch,
+                        uint16_t *y, int32_t variant, void *ws, size_t ws_bytes, void *stream, int src) {
+    if (!d || !blob_dev || !form_dev || !x || !y || !ws || batch <= 0 || (reinterpret_cast<uintptr_t>(x) & 15) ||
+        (reinterpret_cast<uintptr_t>(form_dev) & 15))
         return UW_ERR_INVALID_ARG;
     if (variant >= kGemvVariants)
         return UW_ERR_INVALID_ARG;
@@ -543,7 +548,7 @@ extern "C" uw_status uw_matmul_palette4(const uw_desc *d, const void *blob_dev, 
     uint8_t *wsb = static_cast<uint8_t *>(ws);
     GemvParams p{};
     fill_blob_view(*d, blob_dev, &p.v);
-    p.p4 = static_cast<const uint8_t *>(p4_dev);
+    p.p4 = static_cast<const uint8_t *>(form_dev);
     p.x = x;
     p.y = y;
     p.partial = reinterpret_cast<float *>(wsb + L.partial);
@@ -552,7 +557,40 @@ extern "C" uw_status uw_matmul_palette4(const uw_desc *d, const void *blob_dev, 
     p.rows = d->rows;
     p.cols = d->cols;
     p.batch = batch;
-    return run_gemv(p, v, kSrcPalette4, as_stream(stream));
+    return run_gemv(p, v, src, as_stream(stream));
+}
+}  // namespace
+}  // namespace uw
+
+extern "C" uw_status uw_matmul_palette4(const uw_desc *d, const void *blob_dev, const void *p4_dev,
+                                        const uint16_t *x, int64_t batch, uint16_t *y, int32_t variant, void *ws,
+                                        size_t ws_bytes, void *stream) {
+    return uw::matmul_formed(d, blob_dev, p4_dev, x, batch, y, variant, ws, ws_bytes, stream, uw::kSrcPalette4);
+}
+
+extern "C" uw_status uw_exponent_bytes(const uw_desc *d, size_t *bytes) {
+    if (!d || !bytes)
+        return UW_ERR_INVALID_ARG;
+    *bytes = size_t(uint64_t(d->rows) * uint64_t(d->cols));
+    return UW_OK;
+}
+
+extern "C" uw_status uw_decode_exponents(const uw_desc *d, const void *blob_dev, void *e_dev, void *ws,
+                                         size_t ws_bytes, void *stream) {
+    if (!d || !blob_dev || !e_dev || !ws || (reinterpret_cast<uintptr_t>(e_dev) & 15))
+        return UW_ERR_INVALID_ARG;
+    if (ws_bytes < 256)
+        return UW_ERR_BUFFER_TOO_SMALL;
+    uw::BlobView v;
+    uw::fill_blob_view(*d, blob_dev, &v);
+    return uw::launch_transcode(v, static_cast<uint8_t *>(e_dev), false, static_cast<uint32_t *>(ws),
+                                uw::as_stream(stream));
+}
+
+extern "C" uw_status uw_matmul_exponents(const uw_desc *d, const void *blob_dev, const void *e_dev,
+                                         const uint16_t *x, int64_t batch, uint16_t *y, int32_t variant, void *ws,
+                                         size_t ws_bytes, void *stream) {
+    return uw::matmul_formed(d, blob_dev, e_dev, x, batch, y, variant, ws, ws_bytes, stream, uw::kSrcExponent);
 }
 
 extern "C" uw_status uw_matmul_bf16(const uint16_t *w, int64_t rows, int64_t cols, const uint16_t *x,
@@ -591,7 +629,7 @@ extern "C" uw_status uw_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h
 
 extern "C" int32_t uw_variant_count(int32_t strategy) {
     return (strategy == UW_STRATEGY_FUSED || strategy == UW_STRATEGY_DECOMPRESS_GEMM ||
-            strategy == UW_STRATEGY_PALETTE4)
+            strategy == UW_STRATEGY_PALETTE4 || strategy == UW_STRATEGY_EXPONENT)
                ? kGemvVariants
                : 0;
 }

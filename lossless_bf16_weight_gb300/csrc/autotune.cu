@@ -36,7 +36,7 @@ struct TuneLayout {
 TuneLayout tune_layout(const uw_desc *d, int64_t max_batch) {
     TuneLayout t{};
     size_t need = 0;
-    for (int strategy : {UW_STRATEGY_FUSED, UW_STRATEGY_DECOMPRESS_GEMM, UW_STRATEGY_PALETTE4})
+    for (int strategy : {UW_STRATEGY_FUSED, UW_STRATEGY_DECOMPRESS_GEMM, UW_STRATEGY_PALETTE4, UW_STRATEGY_EXPONENT})
         for (int v = 0; v < uw_variant_count(strategy); v++) {
             uw_plan p{strategy, v, max_batch, 0.f};
             size_t b = 0;
@@ -95,7 +95,7 @@ extern "C" uw_status uw_autotune(const uw_desc *d, const void *blob_dev, const i
     uw_status result = UW_OK;
     for (int i = 0; i < n && result == UW_OK; i++) {
         uw_plan best{UW_STRATEGY_FUSED, -1, batches[i], -1.f};
-        for (int strategy : {UW_STRATEGY_FUSED, UW_STRATEGY_DECOMPRESS_GEMM, UW_STRATEGY_PALETTE4}) {
+        for (int strategy : {UW_STRATEGY_FUSED, UW_STRATEGY_DECOMPRESS_GEMM, UW_STRATEGY_PALETTE4, UW_STRATEGY_EXPONENT}) {
             for (int v = 0; v < uw_variant_count(strategy) && result == UW_OK; v++) {
                 uw_plan p{strategy, v, batches[i], 0.f};
                 std::vector<float> times;

@@ -113,6 +113,7 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
     constexpr int P = 4 * G;  // producer warps
     constexpr bool kCompressed = kSrc == kSrcHuffman;
     constexpr bool kP4 = kSrc == kSrcPalette4;
+    constexpr bool kExp = kSrc == kSrcExponent;
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[2 * kTcMaxStages + 1];
     __shared__ __align__(8) uint64_t pbars[P * kPairStages];
@@ -338,27 +339,33 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
                         qB[I] = 0u;
                     }
                 }
-            } else if constexpr (kP4) {
-                // 4-bit palette indices and sign+mantissa bytes of the lane's row,
-                // rebuilt through the pair table, one tile after the other; escaped
-                // groups from their raw exponents
+            } else if constexpr (kP4 || kExp) {
+                // the intermediate form (4-bit palette indices rebuilt through the
+                // pair table, or exponent bytes) and the sign+mantissa bytes of the
+                // lane's row, one tile after the other; palette-4 escaped groups from
+                // their raw exponents
                 const bool ok = rb_ok && lane < R;
                 const uint32_t lc = ok ? uint32_t(lane) : 0u;
+                constexpr int NI = kP4 ? 2 : 4;  // 16-byte chunks of the form per row
                 auto rebuild = [&](uint32_t kg, bool has, uint32_t (&q)[32]) {
                     const uint64_t q0 = uint64_t(kTileRows) * rb * gpr + uint64_t(R) * kg;
-                    uint4 ix[2], sx[4];
+                    uint4 ix[NI], sx[4];
 #pragma unroll
-                    for (int c = 0; c < 2; c++)
-                        ix[c] = __ldg(reinterpret_cast<const uint4 *>(p.p4 + 32 * q0 + 16 * lc + c * 16 * R));
+                    for (int c = 0; c < NI; c++)
+                        ix[c] = __ldg(reinterpret_cast<const uint4 *>(p.p4 + 16 * NI * q0 + 16 * lc + c * 16 * R));
 #pragma unroll
                     for (int c = 0; c < 4; c++)
                         sx[c] = __ldg(reinterpret_cast<const uint4 *>(v.sm + 64 * q0 + 16 * lc + c * 16 * R));
-                    const uint32_t g = __ldg(v.glen + q0 + lc);
+                    const uint32_t g = kP4 ? __ldg(v.glen + q0 + lc) : 1u;
 #pragma unroll
                     for (int I = 0; I < 32; I++) {
-                        const uint32_t b = (word4(ix[I >> 4], (I >> 2) & 3) >> (8 * (I & 3))) & 0xFFu;
-                        q[I] = lop3_merge(prmt(sm_word(sx, I >> 1), 0u, (I & 1) ? 0xB3A2u : 0x9180u),
-                                          lds32(ptab + 4u * b));
+                        if constexpr (kP4) {
+                            const uint32_t b = (word4(ix[I >> 4], (I >> 2) & 3) >> (8 * (I & 3))) & 0xFFu;
+                            q[I] = lop3_merge(prmt(sm_word(sx, I >> 1), 0u, (I & 1) ? 0xB3A2u : 0x9180u),
+                                              lds32(ptab + 4u * b));
+                        } else {
+                            q[I] = escape_pair(ix, I, sm_word(sx, I >> 1));
+                        }
                     }
                     const uint32_t em = __ballot_sync(0xffffffffu, ok && has && g == 0u);
                     if ((em >> lane) & 1u) {
@@ -518,8 +525,8 @@ size_t tc_smem(int G, int S, int Np, int src, bool staged, uint32_t tdata) {
     if (src == kSrcHuffman)
         s += size_t(kCommonSmemBytes) + 128 +
              size_t(4 * G) * kPairStages * (staged ? pair_stage_bytes(tdata) : code_stage_bytes(tdata));
-    else if (src == kSrcPalette4)
-        s += 256 * 4;  // the pair table
+    else if (src == kSrcPalette4 || src == kSrcExponent)
+        s += 256 * 4;  // the pair table (palette-4)
     return s;
 }
 
@@ -574,6 +581,8 @@ uw_status launch_gemm_tc(const TcParams &base, int G, int src, cudaStream_t stre
             s = launch_tc_g<kSrcBf16, false>(p, G, smem, stream);
         else if (src == kSrcPalette4)
             s = launch_tc_g<kSrcPalette4, false>(p, G, smem, stream);
+        else if (src == kSrcExponent)
+            s = launch_tc_g<kSrcExponent, false>(p, G, smem, stream);
         else if (staged)
             s = launch_tc_g<kSrcHuffman, true>(p, G, smem, stream);
         else

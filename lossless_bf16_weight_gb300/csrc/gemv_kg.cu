@@ -393,18 +393,22 @@ __device__ __forceinline__ void gemv_col_bf16(const GemvParams &p, int rb_per_ct
     cta_reduce<W>(p, red, rb0, nrbc);
 }
 
-// Palette-4 source (the blog's palette pipelines): the twin's loop -- same
-// warps, groups and order of every sum, so the results are bit-identical --
-// with each group's BF16 pairs rebuilt from its 4-bit palette indices and its
-// sign+mantissa bytes.  A byte of two indices is looked up in a 256-entry
-// pair table (entry b = palette[b >> 4] << 23 | palette[b & 15] << 7, both
-// exponents in BF16 position) kept as 32 lane-private copies at a 32 KB-
-// aligned shared address, so that one three-input logic op both masks the
-// byte out of the index word and adds the lane's column, and every lookup
-// is one shared-memory wavefront.  Escaped groups (glen 0) take their
-// exponents from the blob's escape section instead.
-template <int W>
-__device__ __forceinline__ void gemv_col_p4(const GemvParams &p, int rb_per_cta) {
+// Palette-4 and exponent sources (the blog's palette and exponent-only
+// pipelines): the twin's loop -- same warps, groups and order of every sum,
+// so the results are bit-identical -- with each group's BF16 pairs rebuilt
+// from an intermediate form and its sign+mantissa bytes.
+//   * palette-4: a byte of two 4-bit indices is looked up in a 256-entry
+//     pair table (entry b = palette[b >> 4] << 23 | palette[b & 15] << 7,
+//     both exponents in BF16 position) kept as 32 lane-private copies at a
+//     32 KB-aligned shared address, so that one three-input logic op both
+//     masks the byte out of the index word and adds the lane's column, and
+//     every lookup is one shared-memory wavefront.  Escaped groups (glen 0)
+//     take their exponents from the blob's escape section instead.
+//   * exponents: the group's 64 exponent bytes, merged like raw escaped
+//     exponents (escaped groups need nothing else).
+template <int W, int kSrc>
+__device__ __forceinline__ void gemv_col_formed(const GemvParams &p, int rb_per_cta) {
+    constexpr bool kP4 = kSrc == kSrcPalette4;
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const BlobView &v = p.v;
@@ -423,10 +427,13 @@ __device__ __forceinline__ void gemv_col_p4(const GemvParams &p, int rb_per_cta)
     unsigned char *after = smem + (tab - base) + kP4TableBytes;
     uint32_t *xs = reinterpret_cast<uint32_t *>(after);
     float *red = reinterpret_cast<float *>(after + size_t(gpr) * 128);
-    for (int i = threadIdx.x; i < 256 * 8; i += blockDim.x) {
-        const uint32_t b = uint32_t(i) >> 3;
-        const uint32_t e = (uint32_t(v.palette[b >> 4]) << 23) | (uint32_t(v.palette[b & 15u]) << 7);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" :: "r"(tab + 16u * uint32_t(i)), "r"(e) : "memory");
+    if constexpr (kP4) {
+        for (int i = threadIdx.x; i < 256 * 8; i += blockDim.x) {
+            const uint32_t b = uint32_t(i) >> 3;
+            const uint32_t e = (uint32_t(v.palette[b >> 4]) << 23) | (uint32_t(v.palette[b & 15u]) << 7);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" :: "r"(tab + 16u * uint32_t(i)), "r"(e)
+                         : "memory");
+        }
     }
     grid_dep_wait();  // x may come from the kernel before
     load_x_all(p, xs, gpr);
@@ -441,26 +448,28 @@ __device__ __forceinline__ void gemv_col_p4(const GemvParams &p, int rb_per_cta)
         const uint32_t lc = ok ? uint32_t(lane) : 0u;
         const uint64_t qrb = uint64_t(kTileRows) * rb * gpr;  // first group of the row block
         float s_w = 0.f;
-        uint4 ic[2], sc[4], in_[2], sn[4];
+        constexpr int NI = kP4 ? 2 : 4;  // 16-byte chunks of the intermediate form per row
+        uint4 ic[NI], sc[4], in_[NI], sn[4];
         uint32_t gc = 0, gn = 0;
-        auto fetch = [&](uint32_t kg, uint4 (&ix)[2], uint4 (&sx)[4], uint32_t &g) {
+        auto fetch = [&](uint32_t kg, uint4 (&ix)[NI], uint4 (&sx)[4], uint32_t &g) {
             const uint64_t q0 = qrb + uint64_t(R) * kg;
-            const uint8_t *ip = p.p4 + 32 * q0 + 16 * lc;
+            const uint8_t *ip = p.p4 + 16 * NI * q0 + 16 * lc;
             const uint8_t *sp = v.sm + 64 * q0 + 16 * lc;
 #pragma unroll
-            for (int c = 0; c < 2; c++)
+            for (int c = 0; c < NI; c++)
                 ix[c] = __ldg(reinterpret_cast<const uint4 *>(ip + c * 16 * R));
 #pragma unroll
             for (int c = 0; c < 4; c++)
                 sx[c] = __ldg(reinterpret_cast<const uint4 *>(sp + c * 16 * R));
-            g = __ldg(v.glen + q0 + lc);
+            if constexpr (kP4)
+                g = __ldg(v.glen + q0 + lc);
         };
         if (k0 < k1)
             fetch(k0, in_, sn, gn);
 #pragma unroll 1
         for (uint32_t kg = k0; kg < k1; kg++) {
 #pragma unroll
-            for (int c = 0; c < 2; c++)
+            for (int c = 0; c < NI; c++)
                 ic[c] = in_[c];
 #pragma unroll
             for (int c = 0; c < 4; c++)
@@ -472,16 +481,20 @@ __device__ __forceinline__ void gemv_col_p4(const GemvParams &p, int rb_per_cta)
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
             for (int I = 0; I < 32; I++) {
-                const uint32_t iw = word4(ic[I >> 4], (I >> 2) & 3);
-                const int sh = 8 * (I & 3) - 7;  // byte I&3 of the word, times 128
-                const uint32_t moved = sh < 0 ? iw << -sh : iw >> sh;
-                uint32_t off;
-                asm("lop3.b32 %0, %1, 0x7F80, %2, 0xEA;" : "=r"(off) : "r"(moved), "r"(lbase));  // (a & b) | c
-                const uint32_t y = prmt(sm_word(sc, I >> 1), 0u, (I & 1) ? 0xB3A2u : 0x9180u);
-                fma_bf16x2(a0, a1, lop3_merge(y, lds32(off)), lds32(xaddr + 4u * I));
+                if constexpr (kP4) {
+                    const uint32_t iw = word4(ic[I >> 4], (I >> 2) & 3);
+                    const int sh = 8 * (I & 3) - 7;  // byte I&3 of the word, times 128
+                    const uint32_t moved = sh < 0 ? iw << -sh : iw >> sh;
+                    uint32_t off;
+                    asm("lop3.b32 %0, %1, 0x7F80, %2, 0xEA;" : "=r"(off) : "r"(moved), "r"(lbase));  // (a & b) | c
+                    const uint32_t y = prmt(sm_word(sc, I >> 1), 0u, (I & 1) ? 0xB3A2u : 0x9180u);
+                    fma_bf16x2(a0, a1, lop3_merge(y, lds32(off)), lds32(xaddr + 4u * I));
+                } else {
+                    fma_bf16x2(a0, a1, escape_pair(ic, I, sm_word(sc, I >> 1)), lds32(xaddr + 4u * I));
+                }
             }
-            // escaped groups: exponents from the escape section
-            const uint32_t em = __ballot_sync(0xffffffffu, ok && gc == 0u);
+            // palette-4, escaped groups: exponents from the escape section
+            const uint32_t em = kP4 ? __ballot_sync(0xffffffffu, ok && gc == 0u) : 0u;
             if ((em >> lane) & 1u) {
                 const uint32_t rank = __popc(em & ((1u << lane) - 1u));
                 const uint32_t t = rb * gpr + kg;
@@ -509,8 +522,8 @@ __global__ void __launch_bounds__(W * 32, 1) gemv_kg_kernel(const GemvParams p, 
     grid_dep_launch();
     if constexpr (kSrc == kSrcHuffman)
         gemv_col_compressed<W, kPrivate>(p, rb_per_cta);
-    else if constexpr (kSrc == kSrcPalette4)
-        gemv_col_p4<W>(p, rb_per_cta);
+    else if constexpr (kSrc == kSrcPalette4 || kSrc == kSrcExponent)
+        gemv_col_formed<W, kSrc>(p, rb_per_cta);
     else
         gemv_col_bf16<W>(p, rb_per_cta);
 }
@@ -519,7 +532,7 @@ size_t kg_smem(int warps, int rb_per_cta, int src, bool priv, uint32_t tdata, in
     const size_t red = size_t(rb_per_cta) * warps * 128;
     if (src == kSrcBf16)
         return size_t(gpr) * 128 + red;
-    if (src == kSrcPalette4)  // worst-case pad to the 32 KB boundary, the table, x, partials
+    if (src == kSrcPalette4 || src == kSrcExponent)  // worst-case pad to 32 KB, the table, x, partials
         return 32768 + size_t(kP4TableBytes) + size_t(gpr) * 128 + red;
     const size_t sbytes = priv ? code_stage_bytes(tdata) : pair_stage_bytes(tdata);
     return (priv ? size_t(kPrivateLutBytes) : 0) + size_t(kCommonSmemBytes) + red + 128 +
@@ -549,6 +562,8 @@ uw_status launch_kg_src(const GemvParams &p, int rb_per_cta, int src, cudaStream
         return launch_kg_one<W, kSrcBf16, false>(p, rb_per_cta, stream);
     if (src == kSrcPalette4)
         return launch_kg_one<W, kSrcPalette4, false>(p, rb_per_cta, stream);
+    if (src == kSrcExponent)
+        return launch_kg_one<W, kSrcExponent, false>(p, rb_per_cta, stream);
     if (kg_smem(W, rb_per_cta, kSrcHuffman, true, p.v.tdata, int(p.cols / kGroup)) <= size_t(kMaxSmemPerBlock) - 1024)
         return launch_kg_one<W, kSrcHuffman, true>(p, rb_per_cta, stream);
     return launch_kg_one<W, kSrcHuffman, false>(p, rb_per_cta, stream);

@@ -20,13 +20,14 @@ constexpr int kMaxSmemPerBlock = 227 * 1024;
 constexpr int kSrcBf16 = 0;
 constexpr int kSrcHuffman = 1;
 constexpr int kSrcPalette4 = 2;
+constexpr int kSrcExponent = 3;  // the exponent bytes next to the blob's sign+mantissa bytes
 constexpr int kP4TableBytes = 256 * 32 * 4;  // palette-4 pair table, 32 lane-private copies
 constexpr int kSmemPerSm = 228 * 1024 - 3 * 1024;  // minus the per-CTA reservation of 3 CTAs
 
 struct GemvParams {
     BlobView v;            // compressed weights (fused kernel)
     const uint16_t *w;     // uncompressed weights (twin kernel)
-    const uint8_t *p4;     // palette-4 indices (palette-4 kernels; sign+mantissa etc. from v)
+    const uint8_t *p4;     // palette-4 indices or exponent bytes (sign+mantissa etc. from v)
     const uint16_t *x;     // [batch, cols]
     uint16_t *y;           // [batch, rows]
     float *partial;        // [row blocks * splits][bp][32] split partial sums
@@ -51,7 +52,7 @@ constexpr int kTcMaxBatch = 256;
 struct TcParams {
     BlobView v;            // compressed weights (fused kernel)
     const uint16_t *w;     // uncompressed weights (twin kernel)
-    const uint8_t *p4;     // palette-4 indices (palette-4 kernels; sign+mantissa etc. from v)
+    const uint8_t *p4;     // palette-4 indices or exponent bytes (sign+mantissa etc. from v)
     const uint16_t *x;     // [batch, cols]
     uint16_t *y;           // [batch, rows]
     float *partial;        // [row blocks of 128][splits][Np][128] split partial sums
@@ -69,8 +70,9 @@ int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits);
 uw_status launch_gemm_tc(const TcParams &p, int G, int src, cudaStream_t stream);
 
 uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status, cudaStream_t stream);
-// Palette-4 form of a blob: rows*cols/2 bytes at p4 (16-byte aligned).
-uw_status launch_transcode_p4(const BlobView &v, uint8_t *p4, uint32_t *status, cudaStream_t stream);
+// Palette-4 form (rows*cols/2 bytes) or exponent form (rows*cols bytes) of a
+// blob at out (16-byte aligned).
+uw_status launch_transcode(const BlobView &v, uint8_t *out, bool palette4, uint32_t *status, cudaStream_t stream);
 uw_status launch_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h, int64_t n, cudaStream_t stream);
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device);

@@ -1,11 +1,15 @@
-// Transcode a blob's Huffman-coded exponents into the palette-4 form: the
-// 4-bit palette index of every weight (the Unweight blog's palette
-// pipelines: the Huffman codes turned into 4-bit palette indices at run time,
-// a quarter of the bytes a full decode writes, or once when the model is
-// loaded; paragraphs on the four execution pipelines and on the palette
-// format at model load).
+// Transcode a blob's Huffman-coded exponents into one of two intermediate
+// forms (the Unweight blog's paragraph on the four execution pipelines):
+//   * palette-4: the 4-bit palette index of every weight (the palette
+//     pipelines: at run time, a quarter of the bytes a full decode writes, or
+//     once when the model is loaded; paragraph on the palette format at model
+//     load);
+//   * exponents: the exponent byte of every weight, escaped groups included
+//     (the exponent-only pipeline: half the bytes a full decode writes),
+//     laid out like the sign+mantissa section: chunk c (weights 16c..16c+15)
+//     of group q at byte 64*q0 + (c*R + j)*16.
 //
-// Layout (half the width of the sign+mantissa section): group q = 32*rb*gpr
+// Palette-4 layout (half the width of the sign+mantissa section): group q = 32*rb*gpr
 // + R*kg + j (row j of row block rb, R rows in the block) owns 32 bytes in
 // two 16-byte chunks; chunk c (weights 32c .. 32c+31) sits at byte
 // 32*q0 + (c*R + j)*16, q0 = 32*rb*gpr + R*kg the tile's first group, and
@@ -13,9 +17,10 @@
 // index 0: their exponents stay in the blob's escape section.
 //
 // Each warp decodes consecutive tiles with the shared tile decoder
-// (decode.cuh) through a pair table whose entries carry palette indices;
-// lane j packs the 64 indices of row j into 32 bytes and stores its two
-// chunks (32 lanes x 16 bytes = 512 contiguous bytes per store).
+// (decode.cuh) through a pair table whose entries carry palette indices (or
+// exponents); lane j packs row j's 64 indices into 32 bytes (or its 64
+// exponents into 64 bytes) and stores its chunks (32 lanes x 16 bytes = 512
+// contiguous bytes per store).
 #include "decode.cuh"
 #include "kernels.h"
 
@@ -26,8 +31,9 @@ namespace {
 constexpr int kTcdWarps = 8;
 constexpr int kTcdTilesPerWarp = 4;
 
+template <bool kP4>
 __global__ void __launch_bounds__(kTcdWarps * 32, 2)
-    transcode_p4_kernel(const BlobView v, uint8_t *__restrict__ p4, uint32_t *status) {
+    transcode_kernel(const BlobView v, uint8_t *__restrict__ out, uint32_t *status) {
     extern __shared__ __align__(16) unsigned char smem[];
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -50,7 +56,10 @@ __global__ void __launch_bounds__(kTcdWarps * 32, 2)
         if (t_lo + 1 < t_hi)
             offs_next = tile_offsets_load(v, t_lo + 1);
     }
-    build_tables_palette_index(ds, v);
+    if constexpr (kP4)
+        build_tables_palette_index(ds, v);
+    else
+        build_tables(ds, v);
     __syncthreads();
     grid_dep_wait();  // the output may still be read by the kernel before
 
@@ -64,49 +73,77 @@ __global__ void __launch_bounds__(kTcdWarps * 32, 2)
         const uint32_t cbuf = cbuf0 + uint32_t((t - t_lo) & 1) * tbuf;
         LaneStream ls;
         const uint32_t esc_mask = tile_begin(ds, meta, R, cbuf, ls, status);
+        const uint32_t ebase = escape_base(meta, cbuf);  // before meta is reused for the next tile
         if (t + 1 < t_hi) {
             tile_fetch_codes(v, tile_loc(v, rb, kg, gpr), offs_next, cbuf0 + uint32_t((t + 1 - t_lo) & 1) * tbuf,
                              meta);
             if (t + 2 < t_hi)
                 offs_next = tile_offsets_load(v, t + 2);
         }
-        uint32_t wd[8];
-#pragma unroll
-        for (int k = 0; k < 8; k++)
-            wd[k] = 0u;
-#pragma unroll
-        for (int I = 0; I < 32; I++) {
-            const uint32_t ent = decode_entry(ls, lut);
-            const uint32_t byte = ((ent >> 7) & 15u) | ((ent >> 19) & 0xF0u);  // weights 2I (low), 2I+1
-            wd[I >> 2] |= byte << (8 * (I & 3));
-        }
-        tile_check(ls, status);
-        if ((esc_mask >> lane) & 1u) {
+        const int64_t q0 = int64_t(kTileRows) * rb_cur * gpr + int64_t(R) * kg_cur;
+        if constexpr (kP4) {
+            uint32_t wd[8];
 #pragma unroll
             for (int k = 0; k < 8; k++)
                 wd[k] = 0u;
-        }
-        if (lane < R) {
-            const int64_t q0 = int64_t(kTileRows) * rb_cur * gpr + int64_t(R) * kg_cur;
-            uint8_t *dst = p4 + 32 * q0 + 16 * lane;
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-            *reinterpret_cast<uint4 *>(dst + 16 * R) = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+#pragma unroll
+            for (int I = 0; I < 32; I++) {
+                const uint32_t ent = decode_entry(ls, lut);
+                const uint32_t byte = ((ent >> 7) & 15u) | ((ent >> 19) & 0xF0u);  // weights 2I (low), 2I+1
+                wd[I >> 2] |= byte << (8 * (I & 3));
+            }
+            tile_check(ls, status);
+            if ((esc_mask >> lane) & 1u) {
+#pragma unroll
+                for (int k = 0; k < 8; k++)
+                    wd[k] = 0u;
+            }
+            if (lane < R) {
+                uint8_t *dst = out + 32 * q0 + 16 * lane;
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+                *reinterpret_cast<uint4 *>(dst + 16 * R) = make_uint4(wd[4], wd[5], wd[6], wd[7]);
+            }
+        } else {
+            uint32_t wd[16];
+#pragma unroll
+            for (int k = 0; k < 16; k++)
+                wd[k] = 0u;
+#pragma unroll
+            for (int I = 0; I < 32; I++) {
+                const uint32_t ent = decode_entry(ls, lut);
+                const uint32_t two = ((ent >> 7) & 0xFFu) | ((ent >> 15) & 0xFF00u);  // exponents of 2I, 2I+1
+                wd[I >> 1] |= two << (16 * (I & 1));
+            }
+            tile_check(ls, status);
+            uint4 q[4];
+#pragma unroll
+            for (int c = 0; c < 4; c++)
+                q[c] = make_uint4(wd[4 * c], wd[4 * c + 1], wd[4 * c + 2], wd[4 * c + 3]);
+            if ((esc_mask >> lane) & 1u)  // the raw exponents, already in weight order
+                escape_read(ebase, esc_mask, q);
+            if (lane < R) {
+                uint8_t *dst = out + 64 * q0 + 16 * lane;
+#pragma unroll
+                for (int c = 0; c < 4; c++)
+                    *reinterpret_cast<uint4 *>(dst + 16 * c * R) = q[c];
+            }
         }
     }
 }
 
 }  // namespace
 
-uw_status launch_transcode_p4(const BlobView &v, uint8_t *p4, uint32_t *status, cudaStream_t stream) {
+uw_status launch_transcode(const BlobView &v, uint8_t *out, bool palette4, uint32_t *status, cudaStream_t stream) {
     const int64_t gpr = v.cols / kGroup;
     const int64_t ntiles = (v.rows + kTileRows - 1) / kTileRows * gpr;
     const int64_t per_cta = int64_t(kTcdWarps) * kTcdTilesPerWarp;
     const int64_t grid = (ntiles + per_cta - 1) / per_cta;
     const size_t smem = size_t(kCommonSmemBytes) + size_t(kTcdWarps) * 2 * size_t(v.tbuf);
-    if (!ensure_smem(transcode_p4_kernel, smem))
+    auto kern = palette4 ? transcode_kernel<true> : transcode_kernel<false>;
+    if (!ensure_smem(kern, smem))
         return UW_ERR_CUDA;
-    return launch_overlapped(transcode_p4_kernel, dim3(unsigned(grid)), dim3(kTcdWarps * 32), smem, stream, v, p4,
-                             status) == cudaSuccess
+    return launch_overlapped(kern, dim3(unsigned(grid)), dim3(kTcdWarps * 32), smem, stream, v, out, status) ==
+                   cudaSuccess
                ? UW_OK
                : UW_ERR_CUDA;
 }

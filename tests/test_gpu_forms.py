@@ -1,12 +1,13 @@
-"""Palette pipelines (the Unweight blog's palette transcode at run time and
-direct palette at model load): the Huffman codes turned into 4-bit palette
-indices on the GPU, and matmuls that rebuild BF16 from those indices.
+"""Palette and exponent-only pipelines (the Unweight blog's palette transcode
+at run time / direct palette at model load, and exponent-only decode): the
+Huffman codes turned into 4-bit palette indices, or into exponent bytes, on
+the GPU, and matmuls that rebuild BF16 from those forms.
 
-Checks: the transcoded form equals the oracle's palette-4 form byte for byte
-(escaped groups included, ragged row blocks included); every palette-4
-matmul output equals the same kernel fed uncompressed BF16 weights bit for
-bit, and lies within 4 * 2^-8 * sum_k |x_k w_k| of the fp64 oracle; the
-PALETTE4 strategy of uw_matmul gives the same bits as the fused Huffman
+Checks: each form equals the oracle's byte for byte (escaped groups
+included, ragged row blocks included); every matmul output from a form
+equals the same kernel fed uncompressed BF16 weights bit for bit, and lies
+within 4 * 2^-8 * sum_k |x_k w_k| of the fp64 oracle; the PALETTE4 and
+EXPONENT strategies of uw_matmul give the same bits as the fused Huffman
 path with the same variant."""
 import numpy as np
 import pytest
@@ -27,26 +28,37 @@ def g(uw):
     return _gpu
 
 
-def _palette4(g, uw, c):
-    p4 = torch.empty(uw.palette4_bytes(c.desc), dtype=torch.uint8, device="cuda")
+FORMS = ["palette4", "exponent"]
+
+
+def _form(g, uw, c, form):
+    n = uw.palette4_bytes(c.desc) if form == "palette4" else uw.exponent_bytes(c.desc)
+    out = torch.empty(n, dtype=torch.uint8, device="cuda")
     ws = c.ws()
-    uw.transcode_palette4(c.desc, c.blob_dev, p4, ws)
+    (uw.transcode_palette4 if form == "palette4" else uw.decode_exponents)(c.desc, c.blob_dev, out, ws)
     assert uw.check_status(ws) == 0
-    return p4
+    return out
 
 
-def _check_matmul(g, uw, oracle, c, p4, x, variant, sample_rows=None):
+def _oracle_form(oracle, c, form):
+    if form == "palette4":
+        return oracle.palette4(c.w, list(c.desc.palette)[: c.desc.n_palette])
+    return oracle.exponents(c.w)
+
+
+def _check_matmul(g, uw, oracle, c, fdev, x, variant, form, sample_rows=None):
     xd, wd = g.dev_bits(x), g.dev_bits(c.w)
     plan = uw.Plan(uw.STRATEGY_FUSED, variant, x.shape[0], 0.0)
     ws = c.ws(x.shape[0], plan)
     y = g.empty_bits(x.shape[0], c.desc.rows)
-    st = uw.matmul_palette4_status(c.desc, c.blob_dev, p4, xd, y, ws, variant)
+    call = uw.matmul_palette4_status if form == "palette4" else uw.matmul_exponents_status
+    st = call(c.desc, c.blob_dev, fdev, xd, y, ws, variant)
     if st == UNSUPPORTED:
         pytest.skip("variant %s does not fit batch %d" % (uw.variant_name(1, variant), x.shape[0]))
     assert st == 0
     assert uw.check_status(ws) == 0
     yh = g.host_bits(y)
-    assert np.array_equal(yh, g.matmul_bf16(wd, xd, variant)), "palette-4 != uncompressed twin"
+    assert np.array_equal(yh, g.matmul_bf16(wd, xd, variant)), form + " != uncompressed twin"
     rows = range(c.desc.rows) if sample_rows is None else sample_rows
     if sample_rows is None:
         y_ref, absum = oracle.matmul_f64(x, c.w)
@@ -58,11 +70,12 @@ def _check_matmul(g, uw, oracle, c, p4, x, variant, sample_rows=None):
     return yh
 
 
+@pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("shape,kind", [
     ((1, 64), "normal"), ((33, 128), "normal"), ((300, 1024), "normal"),
     ((70, 192), "heavy"), ((4096, 4096), "heavy"), ((14336, 4096), "gate"),
 ])
-def test_transcode_matches_oracle(g, uw, oracle, shape, kind):
+def test_form_matches_oracle(g, uw, oracle, shape, kind, form):
     if kind == "gate":
         w = wl.workload_weights("gate")
     elif kind == "heavy":
@@ -70,34 +83,40 @@ def test_transcode_matches_oracle(g, uw, oracle, shape, kind):
     else:
         w = wl.normal_weights(*shape, 0.02, seed=shape[0])
     c = g.Compressed(w)
-    p4 = _palette4(g, uw, c).cpu().numpy()
-    assert np.array_equal(p4, oracle.palette4(w, list(c.desc.palette)[: c.desc.n_palette]))
+    assert np.array_equal(_form(g, uw, c, form).cpu().numpy(), _oracle_form(oracle, c, form))
 
 
+@pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("variant", COL_VARIANTS)
-def test_every_column_variant(g, uw, oracle, variant):
+def test_every_column_variant(g, uw, oracle, variant, form):
     # 300 rows: ten row blocks, the last ragged (12 rows); heavy tails for escapes
     w = wl.heavy_tailed_weights(300, 1024, seed=variant)
     c = g.Compressed(w)
     assert c.desc.n_escaped > 0
     x = wl.activations(1, 1024, seed=variant)
-    _check_matmul(g, uw, oracle, c, _palette4(g, uw, c), x, variant)
+    _check_matmul(g, uw, oracle, c, _form(g, uw, c, form), x, variant, form)
 
 
+@pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("variant", TC_VARIANTS)
-def test_every_tc_variant(g, uw, oracle, variant):
+def test_every_tc_variant(g, uw, oracle, variant, form):
     w = wl.heavy_tailed_weights(300, 1024, seed=100 + variant)
     c = g.Compressed(w)
     x = wl.activations(40, 1024, seed=variant)
-    _check_matmul(g, uw, oracle, c, _palette4(g, uw, c), x, variant)
+    _check_matmul(g, uw, oracle, c, _form(g, uw, c, form), x, variant, form)
 
 
+@pytest.fixture(scope="module")
+def gate(g):
+    return g.Compressed(wl.workload_weights("gate"))
+
+
+@pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("batch", [1, 16, 64, 256])
-def test_gate_proj_full_size(g, uw, oracle, batch):
-    c = g.Compressed(wl.workload_weights("gate"))
+def test_gate_proj_full_size(g, uw, oracle, gate, batch, form):
     x = wl.activations(batch, 4096, seed=batch)
     rows = np.random.default_rng(batch).choice(14336, 24, replace=False)
-    _check_matmul(g, uw, oracle, c, _palette4(g, uw, c), x, -1, sample_rows=rows)
+    _check_matmul(g, uw, oracle, gate, _form(g, uw, gate, form), x, -1, form, sample_rows=rows)
 
 
 def test_strategy_palette4_equals_fused(g, uw):
@@ -106,8 +125,8 @@ def test_strategy_palette4_equals_fused(g, uw):
     for batch, variant in ((1, 17), (16, 35), (48, 31)):
         xd = g.dev_bits(wl.activations(batch, 2048, seed=batch))
         fused = c.matmul(xd, uw.Plan(uw.STRATEGY_FUSED, variant, batch, 0.0))
-        pal = c.matmul(xd, uw.Plan(uw.STRATEGY_PALETTE4, variant, batch, 0.0))
-        assert np.array_equal(fused, pal)
+        for strategy in (uw.STRATEGY_PALETTE4, uw.STRATEGY_EXPONENT):
+            assert np.array_equal(fused, c.matmul(xd, uw.Plan(strategy, variant, batch, 0.0)))
     # batch 4 has no palette-4 row kernel: the strategy's default is a tensor-core variant
     x = wl.activations(4, 2048, seed=4)
     xd, wd = g.dev_bits(x), g.dev_bits(w)
@@ -117,8 +136,8 @@ def test_strategy_palette4_equals_fused(g, uw):
 
 def test_row_variant_is_unsupported(g, uw):
     c = g.Compressed(wl.normal_weights(64, 256, 0.02, seed=1))
-    p4 = _palette4(g, uw, c)
     xd = g.dev_bits(wl.activations(4, 256, seed=1))
     y = g.empty_bits(4, 64)
     ws = c.ws(4)
-    assert uw.matmul_palette4_status(c.desc, c.blob_dev, p4, xd, y, ws, 0) == UNSUPPORTED
+    assert uw.matmul_palette4_status(c.desc, c.blob_dev, _form(g, uw, c, "palette4"), xd, y, ws, 0) == UNSUPPORTED
+    assert uw.matmul_exponents_status(c.desc, c.blob_dev, _form(g, uw, c, "exponent"), xd, y, ws, 0) == UNSUPPORTED

@@ -133,4 +133,8 @@ def test_palette4_host_side(lib):
     assert L.uw_transcode_palette4(ctypes.byref(d), None, None, None, 0, None) == 1
     assert L.uw_matmul_palette4(ctypes.byref(d), None, None, None, 1, None, -1, None, 0, None) == 1
     assert lib.variant_count(lib.STRATEGY_PALETTE4) == lib.variant_count(lib.STRATEGY_FUSED)
+    assert lib.exponent_bytes(d) == 96 * 256
+    assert L.uw_decode_exponents(ctypes.byref(d), None, None, None, 0, None) == 1
+    assert L.uw_matmul_exponents(ctypes.byref(d), None, None, None, 1, None, -1, None, 0, None) == 1
+    assert lib.variant_count(lib.STRATEGY_EXPONENT) == lib.variant_count(lib.STRATEGY_FUSED)
 
