@@ -111,7 +111,9 @@ def run_workloads(args):
             return t
 
     def name(p):
-        return ("fused:" if p.strategy == uw.STRATEGY_FUSED else "decompress:") + uw.variant_name(p.strategy, p.variant)
+        kind = {uw.STRATEGY_FUSED: "fused:", uw.STRATEGY_DECOMPRESS_GEMM: "decompress:",
+                uw.STRATEGY_PALETTE4: "palette4:", uw.STRATEGY_EXPONENT: "exponent:"}[p.strategy]
+        return kind + uw.variant_name(p.strategy, p.variant)
 
     if "small" in which or "all" in which:
         w = wl.workload_weights("small")
@@ -176,6 +178,47 @@ def run_workloads(args):
                           "ratio_vs_bf16": round(m.desc.blob_bytes / (2 * 4096 * 4096), 4), "batches": rows}),
               flush=True)
 
+    if "pipelines" in which or "all" in which:
+        # The blog's four execution pipelines on the gate matrix, each with its
+        # fastest variant: full decode + GEMM, exponent-only decode + merging
+        # matmul, palette transcode at run time + palette matmul, and the fused
+        # Huffman matmul; plus the palette form made once at load (direct palette).
+        m = Mat(wl.workload_weights("gate"))
+        p4 = torch.empty(uw.palette4_bytes(m.desc), dtype=torch.uint8, device="cuda")
+        ws0 = m.ws(1, None)
+        uw.transcode_palette4(m.desc, m.dev, p4, ws0, stream)
+        cands = {1: [15, 16, 17, 23, 26], 16: [27, 31, 35, 38], 64: [31, 35, 38, 34], 256: [31, 35, 32, 33]}
+        strategies = [("decompress+gemm", uw.STRATEGY_DECOMPRESS_GEMM), ("exponent", uw.STRATEGY_EXPONENT),
+                      ("palette4_runtime", uw.STRATEGY_PALETTE4), ("fused_huffman", uw.STRATEGY_FUSED)]
+        rows = []
+        for batch in (1, 16, 64, 256):
+            x = dev(wl.activations(batch, 4096))
+            y = torch.empty(batch, 14336, dtype=torch.int16, device="cuda")
+            row = {"batch": batch}
+            for label, strategy in strategies + [("palette4_at_load", None)]:
+                best = None
+                for v in cands[batch]:
+                    plan = uw.Plan(uw.STRATEGY_FUSED if strategy is None else strategy, v, batch, 0.0)
+                    ws = m.ws(batch, plan)
+                    if strategy is None:
+                        st = uw.matmul_palette4_status(m.desc, m.dev, p4, x, y, ws, v, stream)
+                        fn = lambda: uw.matmul_palette4(m.desc, m.dev, p4, x, y, ws, v, stream)
+                    else:
+                        st = uw.matmul_status(m.desc, m.dev, x, y, ws, plan, stream)
+                        fn = lambda: uw.matmul(m.desc, m.dev, x, y, ws, plan, stream)
+                    if st != 0:
+                        continue
+                    t = launch_stats(torch, fn, stream, reps=20, warm=3, flush=flush)
+                    if best is None or t["median"] < best[0]["median"]:
+                        best = (t, uw.variant_name(uw.STRATEGY_FUSED, v))
+                    del ws
+                if best is not None:
+                    row[label] = {"us": best[0], "variant": best[1]}
+            rows.append(row)
+        print(json.dumps({"workload": "execution pipelines, gate_proj 14336x4096 N(0,0.02)",
+                          "blob_bytes": m.desc.blob_bytes, "palette4_bytes": uw.palette4_bytes(m.desc),
+                          "batches": rows}), flush=True)
+
     if "model" in which or "all" in which:
         spec = wl.WORKLOADS["model"]
         mats = [Mat(wl.model_matrix(layer, j)) for layer in range(spec["layers"]) for j in range(3)]
@@ -221,7 +264,7 @@ def parse():
                     help="fixed plan instead of autotuning: fused:<variant> or decompress:<variant>")
     ap.add_argument("--batch", type=int, default=BATCH, help="rows of x (the headline workload is batch 1)")
     ap.add_argument("--workloads", default=None,
-                    help="instead of the headline line, one line per workload: small,mlp,heavy,model or all")
+                    help="instead of the headline line, one line per workload: small,mlp,heavy,pipelines,model or all")
     return ap.parse_args()
 
 

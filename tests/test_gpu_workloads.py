@@ -112,3 +112,19 @@ def test_model_slice_autotuned(g, uw, oracle):
                 y = c.matmul(xd, plan)
                 assert np.array_equal(y, g.matmul_bf16(wdev, xd, plan.variant))
                 _check_rows(g, oracle, x, w, y, _sample_rows(w.shape[0], 4, plan.batch))
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096), (1024, 4096)])
+@pytest.mark.parametrize("batch", [1, 16])
+def test_attention_projection_shapes(g, uw, oracle, shape, batch):
+    # Matrices outside the MLP: the Llama-3.1-8B-shaped attention projections
+    # (q and o 4096 x 4096; k and v 1024 x 4096 with grouped-query heads).
+    w = wl.normal_weights(*shape, 0.02, seed=shape[0] + batch)
+    c = g.Compressed(w)
+    assert np.array_equal(c.decompress(), w)
+    x = wl.activations(batch, shape[1], seed=batch)
+    xd = g.dev_bits(x)
+    y = c.matmul(xd)
+    assert np.array_equal(y, g.matmul_bf16(g.dev_bits(w), xd))   # both take the default variant
+    _check_rows(g, oracle, x, w, y, _sample_rows(shape[0], 16, batch))
+
