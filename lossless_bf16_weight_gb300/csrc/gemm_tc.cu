@@ -386,6 +386,16 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
                             q[I] = 0u;
                     }
                 };
+                // the next pair's form and sign+mantissa bytes (both tiles contiguous) into L2
+                if (lane == 0 && rb_ok && j + 1 < my_pairs) {
+                    const uint32_t kgN = kgA + 2u * G;
+                    const uint32_t nt = kgN + 1 < kg_hi ? 2u : 1u;
+                    const uint64_t q0 = uint64_t(kTileRows) * rb * gpr + uint64_t(R) * kgN;
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p.p4 + 16 * NI * q0),
+                                 "r"(16u * NI * uint32_t(R) * nt) : "memory");
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(v.sm + 64 * q0),
+                                 "r"(64u * uint32_t(R) * nt) : "memory");
+                }
                 rebuild(kgA, true, qA);
                 rebuild(hasB ? kgA + 1 : kgA, hasB, qB);
             } else {
