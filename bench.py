@@ -261,7 +261,7 @@ def parse():
     ap.add_argument("--no-context", action="store_true", help="skip the context and end-to-end measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--plan", default=None,
-                    help="fixed plan instead of autotuning: fused:<variant> or decompress:<variant>")
+                    help="fixed plan instead of autotuning: <fused|decompress|palette4|exponent>:<variant>")
     ap.add_argument("--batch", type=int, default=BATCH, help="rows of x (the headline workload is batch 1)")
     ap.add_argument("--workloads", default=None,
                     help="instead of the headline line, one line per workload: small,mlp,heavy,pipelines,model or all")
@@ -451,7 +451,8 @@ def time_graph(torch, fn, steps: int, warmup: int, group: int, stream):
 
 def fixed_plan(uw, text):
     kind, name = text.split(":")
-    strategy = uw.STRATEGY_FUSED if kind == "fused" else uw.STRATEGY_DECOMPRESS_GEMM
+    strategy = {"fused": uw.STRATEGY_FUSED, "decompress": uw.STRATEGY_DECOMPRESS_GEMM,
+                "palette4": uw.STRATEGY_PALETTE4, "exponent": uw.STRATEGY_EXPONENT}[kind]
     for v in range(uw.variant_count(strategy)):
         if uw.variant_name(strategy, v) == name:
             return uw.Plan(strategy, v, BATCH, 0.0)

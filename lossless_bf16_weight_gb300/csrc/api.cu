@@ -62,7 +62,9 @@ int sm_count() {
     return n;
 }
 
-GemvVariant gemv_variant(int v, int64_t rows, int64_t cols, uint32_t tbuf = kWorstTileBuf) {
+// `src`: the weights' source; only the Huffman stages constrain the row
+// blocks per column CTA (the other sources keep a few KB of shared memory).
+GemvVariant gemv_variant(int v, int64_t rows, int64_t cols, uint32_t tbuf = kWorstTileBuf, int src = kSrcHuffman) {
     const int64_t gpr = cols / kGroup;
     if (v < kRowVariants)
         return {Kind::kRow, kWarpChoices[v % 3], 1 << (v / 3), 0};
@@ -78,7 +80,8 @@ GemvVariant gemv_variant(int v, int64_t rows, int64_t cols, uint32_t tbuf = kWor
     const int64_t slots = int64_t(sm_count()) * waves;  // one CTA per SM per wave
     int64_t rb = (nrb + slots - 1) / slots;
     // keep the CTA within one SM's shared memory
-    while (rb > 1 && gemv_kg_smem_bytes(w, int(rb), true, tbuf - kTileSlack, int(gpr)) > size_t(kMaxSmemPerBlock) - 1024)
+    while (rb > 1 && src == kSrcHuffman &&
+           gemv_kg_smem_bytes(w, int(rb), true, tbuf - kTileSlack, int(gpr)) > size_t(kMaxSmemPerBlock) - 1024)
         rb--;
     return {Kind::kColumn, w, 1, int(rb)};
 }
@@ -194,7 +197,7 @@ uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t 
 // batch (chunks of 256 inside the launcher).
 uw_status run_gemv(GemvParams p, int variant, int src, cudaStream_t stream) {
     const bool compressed = src == kSrcHuffman;
-    const GemvVariant gv = gemv_variant(variant, p.rows, p.cols, compressed ? p.v.tbuf : kWorstTileBuf);
+    const GemvVariant gv = gemv_variant(variant, p.rows, p.cols, compressed ? p.v.tbuf : kWorstTileBuf, src);
     if (gv.kind == Kind::kTensor) {
         TcParams t{};
         t.v = p.v;
