@@ -138,7 +138,7 @@ uw_status uw_workspace_init(void *ws_dev, size_t ws_bytes, void *stream);
 /* uw_decompress -- restore the exact BF16 weights into HBM (the blog's
  * "full decode" pipeline).
  *   blob_dev   device copy of the blob described by d.
- *   w_dev      [rows, cols] BF16 output, device memory.
+ *   w_dev      [rows, cols] BF16 output, device memory, 16-byte aligned.
  *   ws_dev     workspace (error word only; >= uw_workspace_size(d, 0, NULL)). */
 uw_status uw_decompress(const uw_desc *d, const void *blob_dev, uint16_t *w_dev,
                         void *ws_dev, size_t ws_bytes, void *stream);

@@ -13,6 +13,14 @@
 
 namespace uw {
 
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n <= 0)
+        return 152;
+    return n;
+}
+
 namespace {
 
 uint32_t rd32(const uint8_t *p) {
@@ -54,13 +62,6 @@ struct GemvVariant {
     int warps, splits, rb;  // warps: CTA warps (row, column) or producer groups G (tensor)
 };
 
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        n <= 0)
-        return 152;
-    return n;
-}
 
 // `src`: the weights' source; only the Huffman stages constrain the row
 // blocks per column CTA (the other sources keep a few KB of shared memory).
@@ -466,7 +467,7 @@ extern "C" uw_status uw_check_status(void *ws, void *stream) {
 
 extern "C" uw_status uw_decompress(const uw_desc *d, const void *blob_dev, uint16_t *w_dev, void *ws,
                                    size_t ws_bytes, void *stream) {
-    if (!d || !blob_dev || !w_dev || !ws)
+    if (!d || !blob_dev || !w_dev || !ws || (reinterpret_cast<uintptr_t>(w_dev) & 15))
         return UW_ERR_INVALID_ARG;
     if (ws_bytes < 256)
         return UW_ERR_BUFFER_TOO_SMALL;

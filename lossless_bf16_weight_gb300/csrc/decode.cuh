@@ -400,11 +400,12 @@ __device__ __forceinline__ uint32_t tile_begin_ready(const DecodeShared &s, cons
     return bad ? 0u : esc_mask;
 }
 
+template <int kShift = kShiftShared>
 __device__ __forceinline__ uint32_t tile_begin(const DecodeShared &s, const TileMeta &m, int R, uint32_t cbuf,
                                                LaneStream &ls, uint32_t *status) {
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
-    return tile_begin_ready<kShiftShared>(s, m, R, cbuf, ls, status);
+    return tile_begin_ready<kShift>(s, m, R, cbuf, ls, status);
 }
 
 // Shared address of a fetched tile's raw escape bytes (after its codes).

@@ -75,6 +75,9 @@ uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status
 uw_status launch_transcode(const BlobView &v, uint8_t *out, bool palette4, uint32_t *status, cudaStream_t stream);
 uw_status launch_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h, int64_t n, cudaStream_t stream);
 
+// SMs of the current device (152 if the query fails).
+int sm_count();
+
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device);
 // later launches skip the call, so they stay capturable in CUDA graphs.
 bool ensure_smem_limit(const void *kernel, size_t bytes);
