@@ -141,3 +141,43 @@ def test_row_variant_is_unsupported(g, uw):
     ws = c.ws(4)
     assert uw.matmul_palette4_status(c.desc, c.blob_dev, _form(g, uw, c, "palette4"), xd, y, ws, 0) == UNSUPPORTED
     assert uw.matmul_exponents_status(c.desc, c.blob_dev, _form(g, uw, c, "exponent"), xd, y, ws, 0) == UNSUPPORTED
+
+
+def _all_escaped():
+    k = np.arange(64)
+    row = (((100 + k % 32) << 7) | k).astype(np.uint16)   # 32 distinct exponents in every group
+    return np.tile(row, (70, 5))
+
+
+DEGENERATE = [
+    ("one_group", lambda: wl.normal_weights(1, 64, 0.02, seed=1)),
+    ("tile_edges", lambda: wl.normal_weights(33, 2112, 0.02, seed=3)),
+    ("all_patterns", wl.all_bf16_patterns),                # NaN, Inf, subnormals, zeros
+    ("zeros", lambda: np.zeros((40, 128), np.uint16)),
+    ("all_escaped", _all_escaped),
+    ("one_exponent", lambda: (((np.arange(96 * 256) % 2) << 15) | (118 << 7) | (np.arange(96 * 256) % 128))
+     .astype(np.uint16).reshape(96, 256)),
+]
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("name", [d[0] for d in DEGENERATE])
+def test_degenerate_matrices(g, uw, oracle, name, form):
+    # The form byte for byte, and the matmul from it bit-identical to the
+    # uncompressed twin (non-finite weights included) for a column and a
+    # tensor-core variant.
+    w = dict(DEGENERATE)[name]()
+    c = g.Compressed(w)
+    fdev = _form(g, uw, c, form)
+    assert np.array_equal(fdev.cpu().numpy(), _oracle_form(oracle, c, form))
+    wd = g.dev_bits(w)
+    call = uw.matmul_palette4_status if form == "palette4" else uw.matmul_exponents_status
+    for batch, variant in ((1, 17), (16, 35)):
+        x = wl.activations(batch, w.shape[1], seed=batch)
+        xd = g.dev_bits(x)
+        ws = c.ws(batch, uw.Plan(uw.STRATEGY_FUSED, variant, batch, 0.0))
+        y = g.empty_bits(batch, w.shape[0])
+        assert call(c.desc, c.blob_dev, fdev, xd, y, ws, variant) == 0
+        assert uw.check_status(ws) == 0
+        assert np.array_equal(g.host_bits(y), g.matmul_bf16(wd, xd, variant))
+
