@@ -13,7 +13,7 @@
 // them with one tcgen05.st into the stage's 32 tensor-memory columns (two
 // BF16 per column); the MMA reads A from there and B (x) from shared memory.
 //
-// Warp roles (CTA of 4G + 1 warps):
+// Warp roles (CTA of 4G + 2 warps):
 //   producers  warp w < 4G owns row block w % 4 and the group pairs
 //              p = w/4, w/4 + G, ... (K steps 2p, 2p+1):
 //                * compressed source: the copy engine stages each pair
@@ -23,10 +23,13 @@
 //                  shared memory (Unweight blog, paragraphs on the
 //                  reconstructive matmul and on decoding on chip);
 //                * bf16 source: the same warps load the uncompressed rows.
-//              It also copies a quarter of each of its K steps' B rows (x,
-//              by cp.async; rows past the batch are zero-filled).
 //   MMA warp   warp 4G: one thread waits for each stage, issues its four
 //              MMAs and commits them to the stage's "empty" barrier.
+//   x loader   warp 4G+1: one thread brings each K step's B rows (x, 64
+//              columns x Np rows, 128-byte swizzled) into the stage with one
+//              tensor-map bulk copy as soon as the stage is free; rows past the
+//              batch are zero-filled by the copy.  A stage is full when its four
+//              producer warps have arrived and the copy has landed.
 //   epilogue   warps 0..3 read the accumulator (tensor-memory lane quarter
 //              = warp index) and write y, or fp32 split partials; the last
 //              CTA of a row block adds the splits in order.
@@ -34,7 +37,10 @@
 // bit-identical.
 #include <cuda_bf16.h>
 
+#include <cudaTypedefs.h>
+
 #include <algorithm>
+#include <mutex>
 
 #include "decode.cuh"
 #include "kernels.h"
@@ -73,18 +79,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         :: "r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(uint32_t(accumulate)) : "memory");
 }
 
-// The quarter `qtr` of a K step's x rows: Np/4 rows x 8 chunks of 16 bytes.
-__device__ __forceinline__ void load_x_quarter(const TcParams &p, uint32_t b_st, int64_t kg, int qtr, int lane) {
-    const int per = p.Np >> 2;
-    const int nchunk = per * 8;  // a multiple of 32: Np is a multiple of 16
-    for (int t = lane; t < nchunk; t += 32) {
-        const int b = qtr * per + (t >> 3), c = t & 7;
-        const bool ok = b < p.batch;
-        const uint16_t *src = ok ? p.x + int64_t(b) * p.cols + kg * kGroup + 8 * c : p.x;
-        cp_async16_zfill(b_st + sw128_offset(uint32_t(b), uint32_t(c)), src, ok ? 16u : 0u);
-    }
-}
-
 // An escaped group's 32 BF16 pairs, from its raw exponents (in the pair
 // stage) and its four sign+mantissa chunks.
 __device__ __forceinline__ void escaped_pairs(uint32_t ebase, uint32_t em, const uint4 (&sm)[4], uint32_t (&q)[32]) {
@@ -109,7 +103,7 @@ __device__ __forceinline__ void sm_chunks(const uint8_t *g_lane, uint32_t stride
 }
 
 template <int G, int kSrc, bool kSmStaged>
-__global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcParams p) {
+__global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
     constexpr int P = 4 * G;  // producer warps
     constexpr bool kCompressed = kSrc == kSrcHuffman;
     constexpr bool kP4 = kSrc == kSrcPalette4;
@@ -149,7 +143,7 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
         tmem_alloc(smem_addr(&tmem_slot), kTmemCols);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; s++) {
-            mbar_init(full0 + 8u * s, 4);
+            mbar_init(full0 + 8u * s, 5);  // four producer warps + the x copy's expect_tx
             mbar_init(empty0 + 8u * s, 1);
         }
         mbar_init(done, 1);
@@ -419,14 +413,8 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
                 mbar_wait(empty0 + 8u * sB_, (uB - 1) & 1u, p.status, kStatusTimeout);
             tc_fence_after();
             tmem_st32(trow + 32u * sA_, qA);
-            load_x_quarter(p, b0 + sA_ * bstage, kgA, rbl, lane);
-            if (hasB) {
+            if (hasB)
                 tmem_st32(trow + 32u * sB_, qB);
-                load_x_quarter(p, b0 + sB_ * bstage, kgA + 1, rbl, lane);
-            }
-            cp_async_commit();
-            cp_async_wait_all();
-            fence_proxy_async_smem();
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -437,20 +425,31 @@ __global__ void __launch_bounds__((4 * G + 1) * 32, 1) gemm_tc_kernel(const TcPa
             }
         }
         tile_check_flush(bad, p.status);
-    } else if (lane == 0) {  // the MMA warp
-        const uint32_t idesc = idesc_bf16_f32(kTcM, Np);
+    } else if (warp == P) {
+        if (lane == 0) {  // the MMA warp
+            const uint32_t idesc = idesc_bf16_f32(kTcM, Np);
+#pragma unroll 1
+            for (uint32_t i = 0; i < nk; i++) {
+                const uint32_t s = i % uint32_t(S);
+                mbar_wait(full0 + 8u * s, (i / uint32_t(S)) & 1u, p.status, kStatusTimeout);
+                tc_fence_after();
+                const uint32_t b_st = b0 + s * bstage;
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+                    mma_ts(tmem, tmem + a0col + 32u * s + 8u * k, sdesc_sw128(b_st + 32u * k), idesc, (i | k) != 0);
+                mma_commit(empty0 + 8u * s);
+            }
+            mma_commit(done);
+        }
+    } else if (lane == 0) {  // the x loader
 #pragma unroll 1
         for (uint32_t i = 0; i < nk; i++) {
-            const uint32_t s = i % uint32_t(S);
-            mbar_wait(full0 + 8u * s, (i / uint32_t(S)) & 1u, p.status, kStatusTimeout);
-            tc_fence_after();
-            const uint32_t b_st = b0 + s * bstage;
-#pragma unroll
-            for (int k = 0; k < 4; k++)
-                mma_ts(tmem, tmem + a0col + 32u * s + 8u * k, sdesc_sw128(b_st + 32u * k), idesc, (i | k) != 0);
-            mma_commit(empty0 + 8u * s);
+            const uint32_t s = i % uint32_t(S), u = i / uint32_t(S);
+            if (u > 0)
+                mbar_wait(empty0 + 8u * s, (u - 1) & 1u, p.status, kStatusTimeout);
+            mbar_expect_tx(full0 + 8u * s, bstage);
+            tma_load_2d(b0 + s * bstage, &p.xmap, int((kg_lo + i) * kGroup), 0, full0 + 8u * s);
         }
-        mma_commit(done);
     }
     __syncwarp();
 
@@ -514,7 +513,7 @@ uw_status launch_tc_one(const TcParams &p, size_t smem, cudaStream_t stream) {
     if (!ensure_smem(kern, smem))
         return UW_ERR_CUDA;
     const dim3 grid(unsigned((p.rows + kTcM - 1) / kTcM), unsigned(p.splits));
-    return launch_overlapped(kern, grid, dim3((4 * G + 1) * 32), smem, stream, p) == cudaSuccess ? UW_OK : UW_ERR_CUDA;
+    return launch_overlapped(kern, grid, dim3((4 * G + 2) * 32), smem, stream, p) == cudaSuccess ? UW_OK : UW_ERR_CUDA;
 }
 
 template <int kSrc, bool kSmStaged>
@@ -564,6 +563,37 @@ int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits) {
     return (rows + kTcM - 1) / kTcM * splits * np * kTcM;
 }
 
+// The driver's tensor-map encoder, looked up once through the runtime.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// x rows b0 .. b0+batch-1 as a 2-D tensor (cols inner), boxes of 64 columns x
+// Np rows with the 128-byte swizzle of the B stages; rows past the batch read
+// as zeros.
+bool encode_x_map(CUtensorMap *m, const uint16_t *x, int64_t cols, int64_t batch, int Np) {
+    const auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(batch)};
+    const cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(kGroup), cuuint32_t(Np)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 uw_status launch_gemm_tc(const TcParams &base, int G, int src, cudaStream_t stream) {
     const int64_t gpr = base.cols / kGroup;
     if (base.splits < 1 || base.splits > gpr || G < 1 || G > 3)
@@ -578,6 +608,8 @@ uw_status launch_gemm_tc(const TcParams &base, int G, int src, cudaStream_t stre
         p.Np = int((p.batch + 15) / 16 * 16);
         p.a0col = a0_col(p.Np);
         p.tmem_cols = kTmemCols;
+        if (!encode_x_map(&p.xmap, p.x, p.cols, p.batch, p.Np))
+            return UW_ERR_CUDA;
         // Huffman source: stage the sign+mantissa bytes in shared memory when that
         // leaves each producer group its two K steps (and some slack); read them
         // from L2 otherwise

@@ -1,5 +1,6 @@
 // Host-side interface between the C ABI entry points and the kernels.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -63,6 +64,8 @@ struct TcParams {
     int S, Np;             // stages, padded batch (set by the launcher)
     uint32_t tmem_cols;    // tensor-memory columns allocated (set by the launcher)
     uint32_t a0col;        // first tensor-memory column of the A stages (set by the launcher)
+    CUtensorMap xmap;      // x as a 2-D tensor (cols x batch rows), 64 x Np boxes, 128-byte
+                           // swizzle (set by the launcher)
 };
 size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed, uint32_t tdata);
 int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tdata);

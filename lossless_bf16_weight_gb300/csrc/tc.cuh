@@ -59,6 +59,15 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
 }
 
+// One box of a 2-D tensor map (kernel-parameter tensor map at `tmap`) into
+// shared memory at `dst`, completion counted on the mbarrier; coordinate x0
+// is the inner one (its byte offset must be a multiple of 16).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int x0, int x1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x0), "r"(x1), "r"(bar) : "memory");
+}
+
 // Bulk copy global -> shared by the copy engine; completion is counted on
 // the mbarrier.  Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
