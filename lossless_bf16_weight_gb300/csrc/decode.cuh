@@ -400,6 +400,54 @@ __device__ __forceinline__ uint32_t tile_begin_ready(const DecodeShared &s, cons
     return bad ? 0u : esc_mask;
 }
 
+// tile_begin_ready for the two tiles of a pair at once (B has RB = R or 0
+// rows): one warp prefix sum over both group lengths packed into one word
+// (a tile's sum is at most 32 * 255 < 2^16, so the halves never carry into
+// each other), the source lane's existence taken from the shuffle's own
+// predicate.  Returns both escape masks.
+template <int kShift = kShiftShared>
+__device__ __forceinline__ void pair_begin_ready(const DecodeShared &s, uint32_t gA, uint32_t gB, uint32_t pkA,
+                                                 uint32_t pkB, int R, int RB, uint32_t cbA, uint32_t cbB,
+                                                 LaneStream &la, LaneStream &lb, uint32_t *status, uint32_t &emA,
+                                                 uint32_t &emB) {
+    const int lane = threadIdx.x & 31;
+    const bool vA = lane < R, vB = lane < RB;
+    const uint32_t ga = vA ? gA : 0u, gb = vB ? gB : 0u;  // group lengths are bytes
+    const uint32_t g2 = ga | (gb << 16);
+    uint32_t incl = g2;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1)
+        asm("{\n\t.reg .b32 u;\n\t.reg .pred p;\n\t"
+            "shfl.sync.up.b32 u|p, %0, %1, 0, -1;\n\t"
+            "@p add.u32 %0, %0, u;\n\t}"
+            : "+r"(incl) : "r"(d));
+    const uint32_t off2 = incl - g2;
+    const uint32_t tot2 = __shfl_sync(0xffffffffu, incl, 31);
+    const uint32_t mA = __ballot_sync(0xffffffffu, vA && ga == 0u);
+    const uint32_t mB = __ballot_sync(0xffffffffu, vB && gb == 0u);
+    auto setup = [&](uint32_t g, uint32_t off, uint32_t total, uint32_t esc_mask, uint32_t pk, uint32_t cbuf,
+                     LaneStream &ls) -> uint32_t {
+        const uint32_t n16 = pk & 0xFFu, nesc = (pk >> 8) & 0xFFu;
+        const bool over = (pk >> 16) != 0 || total > n16 * 16u;
+        const bool bad = over || uint32_t(__popc(esc_mask)) != nesc;
+        if (bad && lane == 0)
+            atomicOr(status, over ? kStatusBadTile : kStatusBadEscape);
+        const bool coded = !bad && g != 0;
+        const uint32_t sub = (off & 3u) ? 0u : 4u;  // a stream starting on a word boundary begins one word early
+        const uint32_t w0 = coded ? cbuf + (off & ~3u) - sub : smem_addr(s.zero);
+        const uint32_t c0 = (8u * (off & 3u) - uint32_t(kShift)) & 31u;
+        ls.lo = lds32(w0);
+        ls.hi = lds32(w0 + 4);
+        ls.nx = lds32(w0 + 8);
+        ls.wp = w0 + 12;
+        ls.c = c0;
+        ls.expect = coded ? 8u * ls.wp + c0 + 8u * g : 0u;
+        return bad ? 0u : esc_mask;
+    };
+    emA = setup(ga, off2 & 0xFFFFu, tot2 & 0xFFFFu, mA, pkA, cbA, la);
+    emB = setup(gb, off2 >> 16, tot2 >> 16, mB, pkB, cbB, lb);
+}
+
 template <int kShift = kShiftShared>
 __device__ __forceinline__ uint32_t tile_begin(const DecodeShared &s, const TileMeta &m, int R, uint32_t cbuf,
                                                LaneStream &ls, uint32_t *status) {

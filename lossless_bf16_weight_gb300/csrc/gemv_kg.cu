@@ -227,8 +227,8 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
         }
         LaneStream la, lb;
         const uint32_t cA = st + 64u, cB = cA + 16u * m.n16A;
-        const uint32_t emA = tile_begin_ready<kShift>(ds, TileMeta{gA, 0u, m.pkA}, R, cA, la, p.status);
-        const uint32_t emB = tile_begin_ready<kShift>(ds, TileMeta{gB, 0u, m.pkB}, hasB ? R : 0, cB, lb, p.status);
+        uint32_t emA, emB;
+        pair_begin_ready<kShift>(ds, gA, gB, m.pkA, m.pkB, R, hasB ? R : 0, cA, cB, la, lb, p.status, emA, emB);
         const uint32_t ebA = cA + 16u * (m.n16A + m.n16B), ebB = ebA + 64u * m.nescA;
         const uint32_t stride = 16u * uint32_t(R);
         const uint32_t smA = st + smoff + 16u * uint32_t(lane), smB = smA + 64u * uint32_t(R);
