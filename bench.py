@@ -113,7 +113,7 @@ def run_workloads(args):
     def name(p):
         kind = {uw.STRATEGY_FUSED: "fused:", uw.STRATEGY_DECOMPRESS_GEMM: "decompress:",
                 uw.STRATEGY_PALETTE4: "palette4:", uw.STRATEGY_EXPONENT: "exponent:"}[p.strategy]
-        return kind + uw.variant_name(p.strategy, p.variant)
+        return kind + (uw.variant_name(p.strategy, p.variant) if p.variant >= 0 else "default")
 
     if "small" in which or "all" in which:
         w = wl.workload_weights("small")
@@ -219,9 +219,17 @@ def run_workloads(args):
                           "blob_bytes": m.desc.blob_bytes, "palette4_bytes": uw.palette4_bytes(m.desc),
                           "batches": rows}), flush=True)
 
+    model_cache = []
+
+    def model_mats():
+        if not model_cache:
+            spec = wl.WORKLOADS["model"]
+            model_cache.extend(Mat(wl.model_matrix(layer, j)) for layer in range(spec["layers"]) for j in range(3))
+        return model_cache
+
     if "model" in which or "all" in which:
         spec = wl.WORKLOADS["model"]
-        mats = [Mat(wl.model_matrix(layer, j)) for layer in range(spec["layers"]) for j in range(3)]
+        mats = model_mats()
         nbytes = sum(m.desc.blob_bytes for m in mats)
         wout = torch.empty(wl.GATE_SHAPE, dtype=torch.int16, device="cuda")
         ws0 = mats[0].ws(1, None)
@@ -252,6 +260,78 @@ def run_workloads(args):
                           "batches": rows}), flush=True)
 
 
+    if "chain" in which or "all" in which:
+        # The 32-layer model as one chain (uw_mlp_forward): every matrix
+        # fused; the tuner's plans run serially; the same with the hard
+        # matrices' preprocessing on a side stream and an SM split; half the
+        # layers "easy" (palette-4 form made at load) interleaved with hard
+        # ones; and every layer easy (the memory-hungry bound).
+        mats = model_mats()
+        nl = len(mats) // 3
+        nbytes = sum(m.desc.blob_bytes for m in mats)
+        ws0 = mats[0].ws(1, None)
+        forms = []
+        for i, m in enumerate(mats):
+            f = torch.empty(uw.palette4_bytes(m.desc), dtype=torch.uint8, device="cuda")
+            uw.transcode_palette4(m.desc, m.dev, f, ws0, stream)
+            forms.append(f)
+        side = torch.cuda.Stream()
+        default = uw.Plan(uw.STRATEGY_DEFAULT, -1, 0, 0.0)
+        p4 = uw.Plan(uw.STRATEGY_PALETTE4, -1, 0, 0.0)
+        fused = uw.Plan(uw.STRATEGY_FUSED, -1, 0, 0.0)
+        rows = []
+        for batch in (1, 64, 256):
+            x = dev(wl.activations(batch, wl.GATE_SHAPE[1]))
+            y = torch.empty(batch, wl.GATE_SHAPE[1], dtype=torch.int16, device="cuda")
+            row = {"batch": batch}
+
+            def entries(easy_layer, roles):
+                out = []
+                for i, m in enumerate(mats):
+                    easy = easy_layer(i // 3)
+                    out.append((m.desc, m.dev, forms[i] if easy else None, p4 if easy else roles[i % 3]))
+                return out
+
+            def run(label, ents, sched, use_side, tuned=None):
+                arr = uw.mlp_matrices(ents)
+                ws = torch.empty(uw.mlp_workspace_size(arr, batch, sched), dtype=torch.uint8, device="cuda")
+                uw.workspace_init(ws, stream)
+                sd = side if use_side else None
+                t = launch_stats(torch, lambda: uw.mlp_forward(arr, x, y, ws, sched, stream, sd), stream, reps=5,
+                                 warm=2)
+                if uw.check_status(ws, stream) != 0:
+                    raise RuntimeError("chain %s reported a decode error" % label)
+                r = {"forward_us": t, "tokens_per_s": round(batch / t["median"] * 1e6, 1),
+                     "GBps": round(nbytes / t["median"] / 1e3, 1)}
+                if tuned is not None:
+                    r["plans"] = [name(p) for p in tuned[0]]
+                    r["schedule"] = {"slots": tuned[1].slots, "dec_ctas": tuned[1].dec_ctas}
+                row[label] = r
+
+            def tune(ents, use_side):
+                arr = uw.mlp_matrices(ents)
+                ws = torch.empty(uw.mlp_autotune_workspace_size(arr, batch), dtype=torch.uint8, device="cuda")
+                uw.workspace_init(ws, stream)
+                return uw.mlp_autotune(arr, x, y, ws, 2, stream, side if use_side else None)
+
+            run("all_fused", entries(lambda l: False, [fused] * 3), uw.Schedule(2, 0), False)
+            hard = entries(lambda l: False, [default] * 3)
+            plans, sch = tune(hard, False)
+            run("tuned_serial", entries(lambda l: False, plans), sch, False, (plans, sch))
+            plans, sch = tune(hard, True)
+            run("tuned_concurrent", entries(lambda l: False, plans), sch, True, (plans, sch))
+            inter = entries(lambda l: l % 2 == 0, [default] * 3)
+            plans, sch = tune(inter, True)
+            run("interleaved_half_easy", entries(lambda l: l % 2 == 0, plans), sch, True, (plans, sch))
+            run("all_easy_palette4_at_load", entries(lambda l: True, [p4] * 3), uw.Schedule(2, 0), False)
+            rows.append(row)
+            print(json.dumps({"workload": "chain, batch %d" % batch, **row}), flush=True)
+        print(json.dumps({"workload": "%d-layer SwiGLU MLP chain (uw_mlp_forward), sigma_l ~ U[0.01, 0.04]" % nl,
+                          "compressed_bytes": nbytes,
+                          "palette4_form_bytes_per_easy_layer": sum(uw.palette4_bytes(m.desc) for m in mats[:3]),
+                          "batches": rows}), flush=True)
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -264,7 +344,8 @@ def parse():
                     help="fixed plan instead of autotuning: <fused|decompress|palette4|exponent>:<variant>")
     ap.add_argument("--batch", type=int, default=BATCH, help="rows of x (the headline workload is batch 1)")
     ap.add_argument("--workloads", default=None,
-                    help="instead of the headline line, one line per workload: small,mlp,heavy,pipelines,model or all")
+                    help="instead of the headline line, one line per workload: small,mlp,heavy,pipelines,model,chain "
+                         "or all")
     return ap.parse_args()
 
 

@@ -266,6 +266,94 @@ uw_status uw_matmul_noalloc(const uw_desc *d, const void *blob_dev, const uint16
 uw_status uw_swiglu(const uint16_t *g_dev, const uint16_t *u_dev, uint16_t *h_dev,
                     int64_t n, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * MLP chain with concurrent preprocessing.  Follows the Unweight blog's
+ * paragraphs on running the preprocess kernel (Huffman decoder or palette
+ * transcoder) beside the reconstructive matmul, on splitting the SMs between
+ * the two, on "hard" and "easy" layers, on double-buffered preprocess slots
+ * and on tuning gate, up and down in turn.
+ *
+ * Layer l maps x_l [batch, D] to x_{l+1} [batch, D]:
+ *     g = x_l Wg^T, u = x_l Wu^T   ([batch, F_l] each)
+ *     h = bf16(silu(g) * u)        (as uw_swiglu)
+ *     x_{l+1} = h Wd^T
+ * and the last layer writes y.  Matrices come three per layer, in the order
+ * gate [F_l, D], up [F_l, D], down [D, F_l].  Each runs under its own plan:
+ *   FUSED                          decoded inside the matmul (no preprocessing);
+ *   PALETTE4 with form_dev         "easy": the palette-4 form made at load by
+ *                                  uw_transcode_palette4 is read directly;
+ *   PALETTE4 without form_dev, EXPONENT, DECOMPRESS_GEMM
+ *                                  "hard": a preprocess kernel writes the
+ *                                  palette-4 form, the exponent form or the
+ *                                  BF16 weights into a slot of the workspace,
+ *                                  and the plan's matmul reads the slot.
+ * With a side stream, preprocessing runs there in the order the hard
+ * matrices are used, as far ahead as the slots allow: a slot is rewritten
+ * only after the matmul that read it has completed.  It waits for nothing
+ * else, so it overlaps the matmuls of the layers before it.  Each
+ * preprocess kernel is limited to dec_ctas SMs (one persistent CTA each,
+ * holding its SM by itself), which leaves the rest to the matmul beside it.
+ * Every matmul gives the same bits as under uw_matmul with its plan (and as
+ * uw_matmul_bf16 with its variant on the original weights), so the chain's
+ * output does not depend on the schedule. */
+typedef struct {
+    const uw_desc *desc;     /* host description of the blob                        */
+    const void *blob_dev;    /* device copy of the blob                             */
+    const void *form_dev;    /* palette-4 form made at load (16-byte aligned), or NULL */
+    uw_plan plan;            /* strategy and variant (-1: default); batch, us unused */
+} uw_mlp_matrix;
+
+typedef struct {
+    int32_t slots;           /* preprocess slots: 1, or 2 (double-buffered)          */
+    int32_t dec_ctas;        /* SMs of each preprocess kernel; 0: as many as its work
+                                needs (no split)                                      */
+} uw_schedule;
+
+/* uw_mlp_workspace_size -- bytes of workspace uw_mlp_forward needs for these
+ * matrices, plans, batch and schedule (NULL: 2 slots, no split). */
+uw_status uw_mlp_workspace_size(const uw_mlp_matrix *m, int32_t n_layers, int64_t batch,
+                                const uw_schedule *sched, size_t *bytes);
+
+/* uw_mlp_forward -- run the chain on `stream`, preprocessing on side_stream.
+ *   m          3 * n_layers matrices (gate, up, down per layer); shapes as
+ *              above with one D for all layers (UW_ERR_SHAPE otherwise).
+ *   x_dev      [batch, D] BF16, 16-byte aligned;  y_dev [batch, D] BF16 (written).
+ *   sched      slots and SM split, or NULL (2 slots, no split).
+ *   ws_dev     at least uw_mlp_workspace_size bytes, cleared once by
+ *              uw_workspace_init; decode errors are recorded in its first
+ *              word (read them with uw_check_status).
+ *   side_stream  a stream other than `stream` (created non-blocking), or NULL:
+ *              then each preprocess kernel runs on `stream` right before its
+ *              matmul and nothing overlaps.
+ * Stream ordered: the side stream first waits for all work already on
+ * `stream`, and `stream` ends waiting for the side stream, so the next call
+ * on `stream` may reuse the workspace.  Capturable in a CUDA graph when both
+ * streams are captured from `stream`. */
+uw_status uw_mlp_forward(const uw_mlp_matrix *m, int32_t n_layers, const uint16_t *x_dev,
+                         int64_t batch, uint16_t *y_dev, const uw_schedule *sched,
+                         void *ws_dev, size_t ws_bytes, void *stream, void *side_stream);
+
+/* uw_mlp_autotune -- choose, by coordinate descent on the measured time of
+ * whole uw_mlp_forward calls, one plan per role (gate, up, down) for the
+ * matrices without a load-time form, and the SM split: sweep the gate's
+ * candidates with up and down held, then up's, then down's, then dec_ctas,
+ * and repeat until a pass changes nothing (at most `passes` passes).
+ * Candidates: every strategy with its default variant, plus (batch >= 16)
+ * the tensor-core variants without a K split, whose grids leave SMs free.
+ * Matrices with a form keep PALETTE4 and their own variant.
+ *   m, n_layers, x_dev, batch, y_dev, streams as for uw_mlp_forward (the
+ *              plans in m are ignored; y is overwritten).
+ *   plans_out  3 plans (gate, up, down) with us = the best forward's time.
+ *   sched_out  the chosen schedule (2 slots).
+ *   ws_dev     at least uw_mlp_autotune_workspace_size bytes, cleared.
+ * Synchronises both streams. */
+uw_status uw_mlp_autotune(const uw_mlp_matrix *m, int32_t n_layers, const uint16_t *x_dev,
+                          int64_t batch, uint16_t *y_dev, int32_t passes, uw_plan *plans_out,
+                          uw_schedule *sched_out, void *ws_dev, size_t ws_bytes, void *stream,
+                          void *side_stream);
+uw_status uw_mlp_autotune_workspace_size(const uw_mlp_matrix *m, int32_t n_layers, int64_t batch,
+                                         size_t *bytes);
+
 /* uw_check_status -- synchronise `stream`, read and clear the error word the
  * kernels record in the workspace.  Returns UW_OK, UW_ERR_CORRUPT or
  * UW_ERR_TIMEOUT (or UW_ERR_CUDA if the stream itself failed). */

@@ -51,6 +51,20 @@ class Plan(ctypes.Structure):
             self.strategy, self.variant, self.batch, self.us)
 
 
+class MlpMatrix(ctypes.Structure):
+    """One weight matrix of an MLP chain (uw_mlp_matrix)."""
+    _fields_ = [("desc", ctypes.POINTER(Desc)), ("blob_dev", ctypes.c_void_p), ("form_dev", ctypes.c_void_p),
+                ("plan", Plan)]
+
+
+class Schedule(ctypes.Structure):
+    """Preprocess slots and SM split of an MLP chain (uw_schedule)."""
+    _fields_ = [("slots", ctypes.c_int32), ("dec_ctas", ctypes.c_int32)]
+
+    def __repr__(self):
+        return "Schedule(slots=%d, dec_ctas=%d)" % (self.slots, self.dec_ctas)
+
+
 _lib = None
 
 # (name, restype, argtypes) of every symbol in include/uw.h
@@ -75,6 +89,14 @@ SIGNATURES = [
     ("uw_exponent_bytes", ctypes.c_int, [ctypes.POINTER(Desc), ctypes.POINTER(_SZ)]),
     ("uw_decode_exponents", ctypes.c_int, [ctypes.POINTER(Desc), _P, _P, _P, _SZ, _P]),
     ("uw_matmul_exponents", ctypes.c_int, [ctypes.POINTER(Desc), _P, _P, _P, _I64, _P, _I32, _P, _SZ, _P]),
+    ("uw_mlp_workspace_size", ctypes.c_int, [ctypes.POINTER(MlpMatrix), _I32, _I64, ctypes.POINTER(Schedule),
+                                             ctypes.POINTER(_SZ)]),
+    ("uw_mlp_forward", ctypes.c_int, [ctypes.POINTER(MlpMatrix), _I32, _P, _I64, _P, ctypes.POINTER(Schedule),
+                                      _P, _SZ, _P, _P]),
+    ("uw_mlp_autotune", ctypes.c_int, [ctypes.POINTER(MlpMatrix), _I32, _P, _I64, _P, _I32, ctypes.POINTER(Plan),
+                                       ctypes.POINTER(Schedule), _P, _SZ, _P, _P]),
+    ("uw_mlp_autotune_workspace_size", ctypes.c_int, [ctypes.POINTER(MlpMatrix), _I32, _I64,
+                                                      ctypes.POINTER(_SZ)]),
     ("uw_check_status", ctypes.c_int, [_P, _P]),
     ("uw_variant_name", ctypes.c_char_p, [_I32, _I32]),
     ("uw_variant_count", ctypes.c_int32, [_I32]),
@@ -280,6 +302,65 @@ def matmul_exponents(desc: Desc, blob_dev, e, x, y, ws, variant: int = -1, strea
 
 def swiglu(g, u, h, stream=None):
     _check(load().uw_swiglu(_ptr(g), _ptr(u), _ptr(h), g.numel(), _stream(stream)), "uw_swiglu")
+
+
+# ---------------------------------------------------------------- MLP chain
+def mlp_matrices(entries) -> ctypes.Array:
+    """uw_mlp_matrix array from (desc, blob_dev, form_dev or None, plan or None)
+    entries, three per layer (gate, up, down).  Keep `entries` alive while
+    the array is used."""
+    arr = (MlpMatrix * len(entries))()
+    for i, (d, blob, form, plan) in enumerate(entries):
+        arr[i].desc = ctypes.pointer(d)
+        arr[i].blob_dev = _ptr(blob)
+        arr[i].form_dev = None if form is None else _ptr(form)
+        arr[i].plan = plan if plan is not None else Plan(STRATEGY_DEFAULT, -1, 0, 0.0)
+    return arr
+
+
+def _side(stream):
+    if stream is None:
+        return None
+    return ctypes.c_void_p(stream if isinstance(stream, int) else stream.cuda_stream)
+
+
+def _sched_ptr(sched):
+    return None if sched is None else ctypes.byref(sched)
+
+
+def mlp_workspace_size(mats, batch: int, sched: Schedule | None = None) -> int:
+    n = _SZ(0)
+    _check(load().uw_mlp_workspace_size(mats, len(mats) // 3, batch, _sched_ptr(sched), ctypes.byref(n)),
+           "uw_mlp_workspace_size")
+    return int(n.value)
+
+
+def mlp_forward_status(mats, x, y, ws, sched: Schedule | None = None, stream=None, side_stream=None) -> int:
+    """uw_mlp_forward: y = the chain of len(mats)//3 SwiGLU MLP layers applied to x."""
+    return int(load().uw_mlp_forward(mats, len(mats) // 3, _ptr(x), x.shape[0], _ptr(y), _sched_ptr(sched),
+                                     _ptr(ws), ws.numel() * ws.element_size(), _stream(stream),
+                                     _side(side_stream)))
+
+
+def mlp_forward(mats, x, y, ws, sched: Schedule | None = None, stream=None, side_stream=None):
+    _check(mlp_forward_status(mats, x, y, ws, sched, stream, side_stream), "uw_mlp_forward")
+
+
+def mlp_autotune_workspace_size(mats, batch: int) -> int:
+    n = _SZ(0)
+    _check(load().uw_mlp_autotune_workspace_size(mats, len(mats) // 3, batch, ctypes.byref(n)),
+           "uw_mlp_autotune_workspace_size")
+    return int(n.value)
+
+
+def mlp_autotune(mats, x, y, ws, passes: int = 2, stream=None, side_stream=None):
+    """uw_mlp_autotune: ([gate, up, down] plans, Schedule) by coordinate descent."""
+    plans = (Plan * 3)()
+    sched = Schedule()
+    _check(load().uw_mlp_autotune(mats, len(mats) // 3, _ptr(x), x.shape[0], _ptr(y), passes, plans,
+                                  ctypes.byref(sched), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream),
+                                  _side(side_stream)), "uw_mlp_autotune")
+    return list(plans), sched
 
 
 def check_status(ws, stream=None) -> int:

@@ -239,6 +239,22 @@ uw_status run_gemv(GemvParams p, int variant, int src, cudaStream_t stream) {
 
 }  // namespace
 
+uw_status plan_resolve(const uw_plan *plan, int64_t rows, int64_t cols, int64_t batch, int *strategy, int *variant) {
+    ResolvedPlan rp;
+    const uw_status s = resolve_plan(plan, rows, cols, batch, &rp);
+    *strategy = rp.strategy;
+    *variant = rp.variant;
+    return s;
+}
+
+WsLayout run_layout(int64_t rows, int64_t cols, int64_t batch, int variant) {
+    return layout_for(rows, cols, batch, UW_STRATEGY_FUSED, variant);
+}
+
+uw_status run_matmul(const GemvParams &p, int variant, int src, cudaStream_t stream) {
+    return run_gemv(p, variant, src, stream);
+}
+
 bool ensure_smem_limit(const void *kernel, size_t bytes) {
     struct Entry {
         const void *kernel;

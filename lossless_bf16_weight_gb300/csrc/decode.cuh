@@ -251,6 +251,34 @@ __device__ __forceinline__ uint32_t tile_offsets_load(const BlobView &v, int64_t
     return lane < 4 ? __ldg(src) : 0u;
 }
 
+// The tiles one warp of a decode kernel walks: runs of `per` consecutive
+// tiles (t = rb * gpr + kg), run number (k * gridDim.x + blockIdx.x) * W +
+// warp for k = 0, 1, ... while tiles remain.  A grid smaller than the number
+// of runs makes the kernel persistent (the SM split of a preprocess kernel
+// running beside a matmul).
+struct TileWalk {
+    uint32_t t, lo, rb, kg;  // current tile, first tile of its run, row block, group column
+};
+
+__device__ __forceinline__ void walk_seek(TileWalk &w, uint32_t t, uint32_t gpr) {
+    w.t = t;
+    w.lo = t;
+    w.rb = t / gpr;
+    w.kg = t - w.rb * gpr;
+}
+
+// step = gridDim.x * W * per: the distance between a warp's runs.
+__device__ __forceinline__ void walk_next(TileWalk &w, uint32_t per, uint32_t step, uint32_t ntiles, uint32_t gpr) {
+    w.t++;
+    if (w.t - w.lo == per || w.t >= ntiles) {
+        const uint32_t lo = (step < ntiles && w.lo < ntiles - step) ? w.lo + step : ntiles;
+        walk_seek(w, lo, gpr);
+    } else if (++w.kg == gpr) {
+        w.kg = 0;
+        w.rb++;
+    }
+}
+
 // Programmatic dependent launch: let the next kernel in the stream start
 // launching, and wait until every earlier kernel has completed and its
 // writes are visible.

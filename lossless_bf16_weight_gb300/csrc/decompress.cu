@@ -13,11 +13,13 @@ namespace uw {
 
 namespace {
 
-constexpr int kDecompWarps = 8;
+constexpr int kDecompWarps = 8;        // warps of a CTA launched over the whole matrix (two CTAs per SM)
+constexpr int kDecompWarpsSplit = 16;  // warps of a CTA of a capped, persistent grid (one CTA per SM)
 constexpr int kTilesPerWarp = 4;
 constexpr int kOutBufBytes = kTileRows * kGroup * 2;  // 4096
 
-__global__ void __launch_bounds__(kDecompWarps * 32, 2)
+template <int W>
+__global__ void __launch_bounds__(W * 32, 16 / W)
     decompress_kernel(const BlobView v, uint16_t *__restrict__ out, uint32_t *status) {
     extern __shared__ __align__(16) unsigned char smem[];
     grid_dep_launch();
@@ -26,37 +28,32 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
     const uint32_t lut = smem_addr(ds.lut);
     const uint32_t tbuf = v.tbuf;
     uint32_t *wbuf = reinterpret_cast<uint32_t *>(smem + kCommonSmemBytes + size_t(warp) * 2 * tbuf);
-    uint4 *obuf = reinterpret_cast<uint4 *>(smem + kCommonSmemBytes + size_t(kDecompWarps) * 2 * tbuf +
+    uint4 *obuf = reinterpret_cast<uint4 *>(smem + kCommonSmemBytes + size_t(W) * 2 * tbuf +
                                             size_t(warp) * kOutBufBytes);
 
-    const int64_t gpr = v.cols / kGroup;
-    const int64_t ntiles = (v.rows + kTileRows - 1) / kTileRows * gpr;
-    const int64_t t_lo = (int64_t(blockIdx.x) * kDecompWarps + warp) * kTilesPerWarp;
-    const int64_t t_hi = t_lo + kTilesPerWarp < ntiles ? t_lo + kTilesPerWarp : ntiles;
-
-    // this warp's tiles t_lo .. t_hi-1, walked as (row block, group column)
-    int64_t rb = t_lo / gpr, kg = t_lo - (t_lo / gpr) * gpr;
+    const uint32_t gpr = v.gpr, ntiles = v.ntiles;
+    const uint32_t step = gridDim.x * uint32_t(W * kTilesPerWarp);
+    const uint64_t first = (uint64_t(blockIdx.x) * W + warp) * kTilesPerWarp;
+    TileWalk cur, nxt;
+    walk_seek(cur, first < ntiles ? uint32_t(first) : ntiles, gpr);
+    nxt = cur;
+    walk_next(nxt, kTilesPerWarp, step, ntiles, gpr);
     TileMeta meta{};
     uint4 smn[4];
     uint32_t offs_next = 0;
     const uint32_t cbuf0 = smem_addr(wbuf);
-    if (t_lo < t_hi) {
-        tile_fetch(v, tile_loc(v, rb, kg, gpr), tile_offsets_load(v, t_lo), cbuf0, meta, smn);
-        if (t_lo + 1 < t_hi)
-            offs_next = tile_offsets_load(v, t_lo + 1);
+    if (cur.t < ntiles) {
+        tile_fetch(v, tile_loc32(v, cur.rb, cur.kg, cur.t), tile_offsets_load32(v, cur.t), cbuf0, meta, smn);
+        if (nxt.t < ntiles)
+            offs_next = tile_offsets_load32(v, nxt.t);
     }
     build_tables(ds, v);
     __syncthreads();
     grid_dep_wait();  // the output may still be read by the kernel before
 
-    for (int64_t t = t_lo; t < t_hi; t++) {
-        const int R = tile_rows(v, rb);
-        const int64_t rb_cur = rb, kg_cur = kg;
-        if (++kg == gpr) {
-            kg = 0;
-            rb++;
-        }
-        const uint32_t cbuf = cbuf0 + uint32_t((t - t_lo) & 1) * tbuf;
+    for (uint32_t i = 0; cur.t < ntiles; i++) {
+        const int R = tile_rows32(v, cur.rb);
+        const uint32_t cbuf = cbuf0 + (i & 1u) * tbuf;
         uint4 sm[4];
 #pragma unroll
         for (int c = 0; c < 4; c++)
@@ -64,11 +61,12 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
         LaneStream ls;
         const uint32_t esc_mask = tile_begin(ds, meta, R, cbuf, ls, status);
         const uint32_t ebase = escape_base(meta, cbuf);
-        if (t + 1 < t_hi) {
-            tile_fetch(v, tile_loc(v, rb, kg, gpr), offs_next, cbuf0 + uint32_t((t + 1 - t_lo) & 1) * tbuf,
-                       meta, smn);
-            if (t + 2 < t_hi)
-                offs_next = tile_offsets_load(v, t + 2);
+        TileWalk n2 = nxt;
+        if (nxt.t < ntiles) {
+            tile_fetch(v, tile_loc32(v, nxt.rb, nxt.kg, nxt.t), offs_next, cbuf0 + ((i + 1) & 1u) * tbuf, meta, smn);
+            walk_next(n2, kTilesPerWarp, step, ntiles, gpr);
+            if (n2.t < ntiles)
+                offs_next = tile_offsets_load32(v, n2.t);
         }
         uint32_t q[4];
 #pragma unroll
@@ -103,28 +101,40 @@ __global__ void __launch_bounds__(kDecompWarps * 32, 2)
             const int r = it * 4 + (lane >> 3);
             if (r < R) {
                 const uint4 val = obuf[r * 8 + (c ^ (r & 7))];
-                uint16_t *dst = out + (rb_cur * kTileRows + r) * v.cols + kg_cur * kGroup + c * 8;
+                uint16_t *dst = out + (int64_t(cur.rb) * kTileRows + r) * v.cols + int64_t(cur.kg) * kGroup + c * 8;
                 *reinterpret_cast<uint4 *>(dst) = val;
             }
         }
         __syncwarp();
+        cur = nxt;
+        nxt = n2;
     }
+}
+
+template <int W>
+uw_status launch_decompress_w(const BlobView &v, uint16_t *w_out, uint32_t *status, int64_t grid, size_t min_smem,
+                              cudaStream_t stream) {
+    size_t smem = size_t(kCommonSmemBytes) + size_t(W) * (2 * size_t(v.tbuf) + kOutBufBytes);
+    smem = smem < min_smem ? min_smem : smem;
+    if (!ensure_smem(decompress_kernel<W>, smem))
+        return UW_ERR_CUDA;
+    return launch_overlapped(decompress_kernel<W>, dim3(unsigned(grid)), dim3(W * 32), smem, stream, v, w_out,
+                             status) == cudaSuccess
+               ? UW_OK
+               : UW_ERR_CUDA;
 }
 
 }  // namespace
 
-uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status, cudaStream_t stream) {
-    const int64_t gpr = v.cols / kGroup;
-    const int64_t ntiles = (v.rows + kTileRows - 1) / kTileRows * gpr;
+uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status, cudaStream_t stream, int max_ctas) {
     const int64_t per_cta = int64_t(kDecompWarps) * kTilesPerWarp;
-    const int64_t grid = (ntiles + per_cta - 1) / per_cta;
-    const size_t smem = size_t(kCommonSmemBytes) + size_t(kDecompWarps) * (2 * size_t(v.tbuf) + kOutBufBytes);
-    if (!ensure_smem(decompress_kernel, smem))
-        return UW_ERR_CUDA;
-    return launch_overlapped(decompress_kernel, dim3(unsigned(grid)), dim3(kDecompWarps * 32), smem, stream, v, w_out,
-                             status) == cudaSuccess
-               ? UW_OK
-               : UW_ERR_CUDA;
+    const int64_t grid = (int64_t(v.ntiles) + per_cta - 1) / per_cta;
+    if (max_ctas <= 0 || max_ctas >= grid)
+        return launch_decompress_w<kDecompWarps>(v, w_out, status, grid, 0, stream);
+    // capped: persistent CTAs of 16 warps, each holding an SM to itself
+    const int64_t per_split = int64_t(kDecompWarpsSplit) * kTilesPerWarp;
+    const int64_t g = std::min<int64_t>(max_ctas, (int64_t(v.ntiles) + per_split - 1) / per_split);
+    return launch_decompress_w<kDecompWarpsSplit>(v, w_out, status, g, kExclusiveSmem, stream);
 }
 
 }  // namespace uw

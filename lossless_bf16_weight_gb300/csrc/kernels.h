@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstddef>
 #include <mutex>
 #include <vector>
@@ -72,10 +73,17 @@ int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tdata);
 int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits);
 uw_status launch_gemm_tc(const TcParams &p, int G, int src, cudaStream_t stream);
 
-uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status, cudaStream_t stream);
+// Preprocess kernels.  max_ctas > 0 caps the grid (the SM split of a
+// preprocess kernel running beside a matmul on another stream): the CTAs
+// then walk the tiles persistently, each asking for kExclusiveSmem of shared
+// memory so that it holds an SM by itself and leaves the other SMs whole.
+constexpr size_t kExclusiveSmem = 116 * 1024;
+uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status, cudaStream_t stream,
+                            int max_ctas = 0);
 // Palette-4 form (rows*cols/2 bytes) or exponent form (rows*cols bytes) of a
 // blob at out (16-byte aligned).
-uw_status launch_transcode(const BlobView &v, uint8_t *out, bool palette4, uint32_t *status, cudaStream_t stream);
+uw_status launch_transcode(const BlobView &v, uint8_t *out, bool palette4, uint32_t *status, cudaStream_t stream,
+                           int max_ctas = 0);
 uw_status launch_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h, int64_t n, cudaStream_t stream);
 
 // SMs of the current device (152 if the query fails).
@@ -123,5 +131,15 @@ uint32_t tile_data_bytes(const uw_desc &d);  // a blob's tile buffer capacity
 struct WsLayout {
     size_t status = 0, counters = 0, partial = 0, weights = 0, total = 0;
 };
+
+// Plan resolution and matmul dispatch (api.cu), shared by the MLP chain.
+//   plan_resolve       the strategy and variant a plan (or NULL) runs with.
+//   run_layout         where a matmul's status word, split counters and
+//                      partials sit in its workspace (`weights` = their end).
+//   run_matmul         one matmul; p.status/counters/partial laid out as
+//                      run_layout says, p.w / p.p4 / p.v by `src`.
+uw_status plan_resolve(const uw_plan *plan, int64_t rows, int64_t cols, int64_t batch, int *strategy, int *variant);
+WsLayout run_layout(int64_t rows, int64_t cols, int64_t batch, int variant);
+uw_status run_matmul(const GemvParams &p, int variant, int src, cudaStream_t stream);
 
 }  // namespace uw

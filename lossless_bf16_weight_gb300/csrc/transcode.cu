@@ -28,11 +28,12 @@ namespace uw {
 
 namespace {
 
-constexpr int kTcdWarps = 8;
+constexpr int kTcdWarps = 8;        // warps of a CTA launched over the whole matrix (two CTAs per SM)
+constexpr int kTcdWarpsSplit = 16;  // warps of a CTA of a capped, persistent grid (one CTA per SM)
 constexpr int kTcdTilesPerWarp = 4;
 
-template <bool kP4>
-__global__ void __launch_bounds__(kTcdWarps * 32, 2)
+template <bool kP4, int W>
+__global__ void __launch_bounds__(W * 32, 16 / W)
     transcode_kernel(const BlobView v, uint8_t *__restrict__ out, uint32_t *status) {
     extern __shared__ __align__(16) unsigned char smem[];
     grid_dep_launch();
@@ -42,19 +43,19 @@ __global__ void __launch_bounds__(kTcdWarps * 32, 2)
     const uint32_t tbuf = v.tbuf;
     const uint32_t cbuf0 = smem_addr(smem + kCommonSmemBytes + size_t(warp) * 2 * tbuf);
 
-    const int64_t gpr = v.cols / kGroup;
-    const int64_t ntiles = (v.rows + kTileRows - 1) / kTileRows * gpr;
-    const int64_t t_lo = (int64_t(blockIdx.x) * kTcdWarps + warp) * kTcdTilesPerWarp;
-    const int64_t t_hi = t_lo + kTcdTilesPerWarp < ntiles ? t_lo + kTcdTilesPerWarp : ntiles;
-
-    // this warp's tiles t_lo .. t_hi-1, walked as (row block, group column)
-    int64_t rb = t_lo / gpr, kg = t_lo - (t_lo / gpr) * gpr;
+    const uint32_t gpr = v.gpr, ntiles = v.ntiles;
+    const uint32_t step = gridDim.x * uint32_t(W * kTcdTilesPerWarp);
+    const uint64_t first = (uint64_t(blockIdx.x) * W + warp) * kTcdTilesPerWarp;
+    TileWalk cur, nxt;
+    walk_seek(cur, first < ntiles ? uint32_t(first) : ntiles, gpr);
+    nxt = cur;
+    walk_next(nxt, kTcdTilesPerWarp, step, ntiles, gpr);
     TileMeta meta{};
     uint32_t offs_next = 0;
-    if (t_lo < t_hi) {
-        tile_fetch_codes(v, tile_loc(v, rb, kg, gpr), tile_offsets_load(v, t_lo), cbuf0, meta);
-        if (t_lo + 1 < t_hi)
-            offs_next = tile_offsets_load(v, t_lo + 1);
+    if (cur.t < ntiles) {
+        tile_fetch_codes(v, tile_loc32(v, cur.rb, cur.kg, cur.t), tile_offsets_load32(v, cur.t), cbuf0, meta);
+        if (nxt.t < ntiles)
+            offs_next = tile_offsets_load32(v, nxt.t);
     }
     if constexpr (kP4)
         build_tables_palette_index(ds, v);
@@ -63,24 +64,20 @@ __global__ void __launch_bounds__(kTcdWarps * 32, 2)
     __syncthreads();
     grid_dep_wait();  // the output may still be read by the kernel before
 
-    for (int64_t t = t_lo; t < t_hi; t++) {
-        const int R = tile_rows(v, rb);
-        const int64_t rb_cur = rb, kg_cur = kg;
-        if (++kg == gpr) {
-            kg = 0;
-            rb++;
-        }
-        const uint32_t cbuf = cbuf0 + uint32_t((t - t_lo) & 1) * tbuf;
+    for (uint32_t i = 0; cur.t < ntiles; i++) {
+        const int R = tile_rows32(v, cur.rb);
+        const uint32_t cbuf = cbuf0 + (i & 1u) * tbuf;
         LaneStream ls;
         const uint32_t esc_mask = tile_begin(ds, meta, R, cbuf, ls, status);
         const uint32_t ebase = escape_base(meta, cbuf);  // before meta is reused for the next tile
-        if (t + 1 < t_hi) {
-            tile_fetch_codes(v, tile_loc(v, rb, kg, gpr), offs_next, cbuf0 + uint32_t((t + 1 - t_lo) & 1) * tbuf,
-                             meta);
-            if (t + 2 < t_hi)
-                offs_next = tile_offsets_load(v, t + 2);
+        TileWalk n2 = nxt;
+        if (nxt.t < ntiles) {
+            tile_fetch_codes(v, tile_loc32(v, nxt.rb, nxt.kg, nxt.t), offs_next, cbuf0 + ((i + 1) & 1u) * tbuf, meta);
+            walk_next(n2, kTcdTilesPerWarp, step, ntiles, gpr);
+            if (n2.t < ntiles)
+                offs_next = tile_offsets_load32(v, n2.t);
         }
-        const int64_t q0 = int64_t(kTileRows) * rb_cur * gpr + int64_t(R) * kg_cur;
+        const uint64_t q0 = uint64_t(kTileRows) * cur.rb * gpr + uint64_t(R) * cur.kg;
         if constexpr (kP4) {
             uint32_t wd[8];
 #pragma unroll
@@ -128,24 +125,36 @@ __global__ void __launch_bounds__(kTcdWarps * 32, 2)
                     *reinterpret_cast<uint4 *>(dst + 16 * c * R) = q[c];
             }
         }
+        cur = nxt;
+        nxt = n2;
     }
+}
+
+template <int W>
+uw_status launch_transcode_w(const BlobView &v, uint8_t *out, bool palette4, uint32_t *status, int64_t grid,
+                             size_t min_smem, cudaStream_t stream) {
+    size_t smem = size_t(kCommonSmemBytes) + size_t(W) * 2 * size_t(v.tbuf);
+    smem = smem < min_smem ? min_smem : smem;
+    auto kern = palette4 ? transcode_kernel<true, W> : transcode_kernel<false, W>;
+    if (!ensure_smem(kern, smem))
+        return UW_ERR_CUDA;
+    return launch_overlapped(kern, dim3(unsigned(grid)), dim3(W * 32), smem, stream, v, out, status) == cudaSuccess
+               ? UW_OK
+               : UW_ERR_CUDA;
 }
 
 }  // namespace
 
-uw_status launch_transcode(const BlobView &v, uint8_t *out, bool palette4, uint32_t *status, cudaStream_t stream) {
-    const int64_t gpr = v.cols / kGroup;
-    const int64_t ntiles = (v.rows + kTileRows - 1) / kTileRows * gpr;
+uw_status launch_transcode(const BlobView &v, uint8_t *out, bool palette4, uint32_t *status, cudaStream_t stream,
+                           int max_ctas) {
     const int64_t per_cta = int64_t(kTcdWarps) * kTcdTilesPerWarp;
-    const int64_t grid = (ntiles + per_cta - 1) / per_cta;
-    const size_t smem = size_t(kCommonSmemBytes) + size_t(kTcdWarps) * 2 * size_t(v.tbuf);
-    auto kern = palette4 ? transcode_kernel<true> : transcode_kernel<false>;
-    if (!ensure_smem(kern, smem))
-        return UW_ERR_CUDA;
-    return launch_overlapped(kern, dim3(unsigned(grid)), dim3(kTcdWarps * 32), smem, stream, v, out, status) ==
-                   cudaSuccess
-               ? UW_OK
-               : UW_ERR_CUDA;
+    const int64_t grid = (int64_t(v.ntiles) + per_cta - 1) / per_cta;
+    if (max_ctas <= 0 || max_ctas >= grid)
+        return launch_transcode_w<kTcdWarps>(v, out, palette4, status, grid, 0, stream);
+    // capped: persistent CTAs of 16 warps, each holding an SM to itself
+    const int64_t per_split = int64_t(kTcdWarpsSplit) * kTcdTilesPerWarp;
+    const int64_t g = std::min<int64_t>(max_ctas, (int64_t(v.ntiles) + per_split - 1) / per_split);
+    return launch_transcode_w<kTcdWarpsSplit>(v, out, palette4, status, g, kExclusiveSmem, stream);
 }
 
 }  // namespace uw
