@@ -286,10 +286,11 @@ def run_workloads(args):
             row = {"batch": batch}
 
             def entries(easy_layer, roles):
+                # roles: gate, up, down plans of the matrices without a form, then of those with one
                 out = []
                 for i, m in enumerate(mats):
                     easy = easy_layer(i // 3)
-                    out.append((m.desc, m.dev, forms[i] if easy else None, p4 if easy else roles[i % 3]))
+                    out.append((m.desc, m.dev, forms[i] if easy else None, roles[i % 3 + (3 if easy else 0)]))
                 return out
 
             def run(label, ents, sched, use_side, tuned=None):
@@ -314,16 +315,19 @@ def run_workloads(args):
                 uw.workspace_init(ws, stream)
                 return uw.mlp_autotune(arr, x, y, ws, 2, stream, side if use_side else None)
 
-            run("all_fused", entries(lambda l: False, [fused] * 3), uw.Schedule(2, 0), False)
-            hard = entries(lambda l: False, [default] * 3)
+            start = [default] * 3 + [p4] * 3
+            run("all_fused_default", entries(lambda l: False, [fused] * 6), uw.Schedule(2, 0), False)
+            hard = entries(lambda l: False, start)
             plans, sch = tune(hard, False)
-            run("tuned_serial", entries(lambda l: False, plans), sch, False, (plans, sch))
+            run("tuned_serial", entries(lambda l: False, plans), sch, False, (plans[:3], sch))
             plans, sch = tune(hard, True)
-            run("tuned_concurrent", entries(lambda l: False, plans), sch, True, (plans, sch))
-            inter = entries(lambda l: l % 2 == 0, [default] * 3)
+            run("tuned_concurrent", entries(lambda l: False, plans), sch, True, (plans[:3], sch))
+            inter = entries(lambda l: l % 2 == 0, start)
             plans, sch = tune(inter, True)
             run("interleaved_half_easy", entries(lambda l: l % 2 == 0, plans), sch, True, (plans, sch))
-            run("all_easy_palette4_at_load", entries(lambda l: True, [p4] * 3), uw.Schedule(2, 0), False)
+            easy = entries(lambda l: True, start)
+            plans, sch = tune(easy, False)
+            run("all_easy_palette4_at_load", entries(lambda l: True, plans), sch, False, (plans[3:], sch))
             rows.append(row)
             print(json.dumps({"workload": "chain, batch %d" % batch, **row}), flush=True)
         print(json.dumps({"workload": "%d-layer SwiGLU MLP chain (uw_mlp_forward), sigma_l ~ U[0.01, 0.04]" % nl,

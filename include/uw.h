@@ -334,16 +334,18 @@ uw_status uw_mlp_forward(const uw_mlp_matrix *m, int32_t n_layers, const uint16_
                          void *ws_dev, size_t ws_bytes, void *stream, void *side_stream);
 
 /* uw_mlp_autotune -- choose, by coordinate descent on the measured time of
- * whole uw_mlp_forward calls, one plan per role (gate, up, down) for the
- * matrices without a load-time form, and the SM split: sweep the gate's
- * candidates with up and down held, then up's, then down's, then dec_ctas,
- * and repeat until a pass changes nothing (at most `passes` passes).
- * Candidates: every strategy with its default variant, plus (batch >= 16)
- * the tensor-core variants without a K split, whose grids leave SMs free.
- * Matrices with a form keep PALETTE4 and their own variant.
+ * whole uw_mlp_forward calls, one plan per role and the SM split: sweep the
+ * gate's candidates with up and down held, then up's, then down's (first for
+ * the matrices without a load-time form, then for those with one), then
+ * dec_ctas, and repeat until a pass changes nothing (at most `passes`
+ * passes).  Candidates: every strategy with its default variant, plus
+ * (batch >= 16) the tensor-core variants with two or three producer groups
+ * and any K split (split 1 leaves SMs free beside the matmul); matrices with
+ * a form only PALETTE4.
  *   m, n_layers, x_dev, batch, y_dev, streams as for uw_mlp_forward (the
  *              plans in m are ignored; y is overwritten).
- *   plans_out  3 plans (gate, up, down) with us = the best forward's time.
+ *   plans_out  6 plans: gate, up, down of the matrices without a form, then
+ *              of those with one; us = the best forward's time.
  *   sched_out  the chosen schedule (2 slots).
  *   ws_dev     at least uw_mlp_autotune_workspace_size bytes, cleared.
  * Synchronises both streams. */

@@ -354,8 +354,9 @@ def mlp_autotune_workspace_size(mats, batch: int) -> int:
 
 
 def mlp_autotune(mats, x, y, ws, passes: int = 2, stream=None, side_stream=None):
-    """uw_mlp_autotune: ([gate, up, down] plans, Schedule) by coordinate descent."""
-    plans = (Plan * 3)()
+    """uw_mlp_autotune: (6 plans: gate, up, down without a form, then with
+    one; Schedule) by coordinate descent."""
+    plans = (Plan * 6)()
     sched = Schedule()
     _check(load().uw_mlp_autotune(mats, len(mats) // 3, _ptr(x), x.shape[0], _ptr(y), passes, plans,
                                   ctypes.byref(sched), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream),

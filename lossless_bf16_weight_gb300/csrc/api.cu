@@ -87,26 +87,38 @@ GemvVariant gemv_variant(int v, int64_t rows, int64_t cols, uint32_t tbuf = kWor
     return {Kind::kColumn, w, 1, int(rb)};
 }
 
-// Tensor-core default: the most producer groups whose stages fit (each
-// group keeps two K steps in flight), and the K split (1, 2, 4, 8) whose grid
-// fills the GPU's waves best (ties to fewer splits).
-int default_tc_variant(int64_t rows, int64_t cols, int64_t batch) {
+// Tile data bytes assumed for a Huffman blob that is not at hand.
+constexpr uint32_t kWorstTileData = kWorstTileBuf - kTileSlack;
+
+// Tensor-core default.  Producer groups: the most whose x stages fit for
+// this weight source (the kernel needs two K steps per group in flight).
+// K split: the one with the least estimated time, waves of the grid times
+// the K columns a CTA decodes, each split adding the partial sums it writes
+// and the last CTA reads back (np rows x 128 fp32 per CTA, weighted like six
+// K columns per batch row, fitted to the splits the chain tuner picks on
+// the MLP shapes); ties (within 2%) go to fewer splits.  This keeps one
+// split for 14336 x 4096 from batch 64 on and splits 4096 x 14336, whose 32
+// row blocks would fill a fifth of the GPU.
+// The result does not depend on the number of groups (the MMAs accumulate
+// in K order), so the source only changes the speed.
+int default_tc_variant(int64_t rows, int64_t cols, int64_t batch, int src, uint32_t tdata) {
     const int64_t np = std::min<int64_t>((batch + 15) / 16 * 16, kTcMaxBatch);
     int gi = 0;
     for (int i = 2; i > 0; i--)
-        if (gemm_tc_stages(kTcGroups[i], int(np), true, kWorstTileBuf - kTileSlack) >= 2 * kTcGroups[i] + 2) {
+        if (gemm_tc_stages(kTcGroups[i], int(np), src, tdata) >= 2 * kTcGroups[i]) {
             gi = i;
             break;
         }
     const int64_t mblocks = (rows + 127) / 128, gpr = cols / kGroup, sms = sm_count();
     int best = 0;
-    double best_eff = -1.0;
+    double best_cost = 0.0;
     for (int si = 0; si < kTcSplitChoices; si++) {
         const int64_t sp = std::min<int64_t>(int64_t(1) << si, gpr);
-        const int64_t ctas = mblocks * sp;
-        const double eff = double(ctas) / double((ctas + sms - 1) / sms * sms);
-        if (eff > best_eff + 0.02) {
-            best_eff = eff;
+        const int64_t waves = (mblocks * sp + sms - 1) / sms;
+        const double k = double(cols) / double(sp);
+        const double cost = double(waves) * (k + (sp > 1 ? 6.0 * double(np) : 0.0));
+        if (si == 0 || cost < best_cost * 0.98) {
+            best_cost = cost;
             best = si;
         }
     }
@@ -119,15 +131,17 @@ int pad_batch(int64_t b) {
 }
 
 // Default variant.  Batch 1: column CTAs of 16 warps, one wave of the GPU.
-// Batch 16 and up: tensor-core CTAs.  Otherwise row-block CTAs
-// of 8 warps, split along K when the matrix has few row blocks.
-int default_gemv_variant(int64_t rows, int64_t cols, int64_t batch) {
+// Batch 16 and up: tensor-core CTAs (sized for `src`, with the blob's tile
+// data bytes for the Huffman source).  Otherwise row-block CTAs of 8 warps,
+// split along K when the matrix has few row blocks.
+int default_gemv_variant(int64_t rows, int64_t cols, int64_t batch, int src = kSrcHuffman,
+                         uint32_t tdata = kWorstTileData) {
     const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
     const int64_t gpr = cols / kGroup;
     if (batch == 1)
         return kRowVariants + 2;  // 16 warps, one wave
     if (batch >= 16)
-        return default_tc_variant(rows, cols, batch);
+        return default_tc_variant(rows, cols, batch, src, tdata);
     const int bp = pad_batch(batch);
     int si = 0;
     while (si + 1 < kSplitChoices && nrb * (int64_t(1) << si) < 2 * 152 &&
@@ -166,11 +180,13 @@ struct ResolvedPlan {
 
 // Default variant of the palette-4 kernels: the column GEMV at batch 1, the
 // tensor cores otherwise (there is no palette-4 row kernel).
-int default_p4_variant(int64_t rows, int64_t cols, int64_t batch) {
-    return batch == 1 ? default_gemv_variant(rows, cols, 1) : default_tc_variant(rows, cols, batch);
+int default_p4_variant(int64_t rows, int64_t cols, int64_t batch, int src) {
+    return batch == 1 ? default_gemv_variant(rows, cols, 1) : default_tc_variant(rows, cols, batch, src, 0);
 }
 
-uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t batch, ResolvedPlan *out) {
+// tdata: the blob's tile data bytes (sizes the Huffman stages of the default).
+uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t batch, ResolvedPlan *out,
+                       uint32_t tdata = kWorstTileData) {
     out->strategy = UW_STRATEGY_FUSED;
     out->variant = -1;
     if (plan) {
@@ -186,10 +202,14 @@ uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t 
             out->variant = plan->variant;
         }
     }
-    if (out->variant < 0)
-        out->variant = (out->strategy == UW_STRATEGY_PALETTE4 || out->strategy == UW_STRATEGY_EXPONENT)
-                           ? default_p4_variant(rows, cols, batch)
-                           : default_gemv_variant(rows, cols, batch);
+    if (out->variant < 0) {
+        switch (out->strategy) {
+            case UW_STRATEGY_PALETTE4: out->variant = default_p4_variant(rows, cols, batch, kSrcPalette4); break;
+            case UW_STRATEGY_EXPONENT: out->variant = default_p4_variant(rows, cols, batch, kSrcExponent); break;
+            case UW_STRATEGY_DECOMPRESS_GEMM: out->variant = default_gemv_variant(rows, cols, batch, kSrcBf16); break;
+            default: out->variant = default_gemv_variant(rows, cols, batch, kSrcHuffman, tdata); break;
+        }
+    }
     return UW_OK;
 }
 
@@ -239,9 +259,9 @@ uw_status run_gemv(GemvParams p, int variant, int src, cudaStream_t stream) {
 
 }  // namespace
 
-uw_status plan_resolve(const uw_plan *plan, int64_t rows, int64_t cols, int64_t batch, int *strategy, int *variant) {
+uw_status plan_resolve(const uw_plan *plan, const uw_desc &d, int64_t batch, int *strategy, int *variant) {
     ResolvedPlan rp;
-    const uw_status s = resolve_plan(plan, rows, cols, batch, &rp);
+    const uw_status s = resolve_plan(plan, d.rows, d.cols, batch, &rp, tile_data_bytes(d));
     *strategy = rp.strategy;
     *variant = rp.variant;
     return s;
@@ -453,7 +473,7 @@ extern "C" uw_status uw_workspace_size(const uw_desc *d, int64_t batch, const uw
     if (!d || !bytes || batch < 0)
         return UW_ERR_INVALID_ARG;
     ResolvedPlan rp;
-    const uw_status s = resolve_plan(plan, d->rows, d->cols, std::max<int64_t>(batch, 1), &rp);
+    const uw_status s = resolve_plan(plan, d->rows, d->cols, std::max<int64_t>(batch, 1), &rp, tile_data_bytes(*d));
     if (s != UW_OK)
         return s;
     *bytes = layout_for(d->rows, d->cols, std::max<int64_t>(batch, 1), rp.strategy, rp.variant).total;
@@ -497,7 +517,7 @@ extern "C" uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uin
     if (!d || !blob_dev || !x || !y || !ws || batch <= 0 || (reinterpret_cast<uintptr_t>(x) & 15))
         return UW_ERR_INVALID_ARG;
     ResolvedPlan rp;
-    uw_status s = resolve_plan(plan, d->rows, d->cols, batch, &rp);
+    uw_status s = resolve_plan(plan, d->rows, d->cols, batch, &rp, tile_data_bytes(*d));
     if (s != UW_OK)
         return s;
     const WsLayout L = layout_for(d->rows, d->cols, batch, rp.strategy, rp.variant);
@@ -561,7 +581,7 @@ uw_status matmul_formed(const uw_desc *d, const void *blob_dev, const void *form
         return UW_ERR_INVALID_ARG;
     if (variant >= kGemvVariants)
         return UW_ERR_INVALID_ARG;
-    const int v = variant < 0 ? default_p4_variant(d->rows, d->cols, batch) : variant;
+    const int v = variant < 0 ? default_p4_variant(d->rows, d->cols, batch, src) : variant;
     const WsLayout L = layout_for(d->rows, d->cols, batch, UW_STRATEGY_FUSED, v);
     if (ws_bytes < L.total)
         return UW_ERR_BUFFER_TOO_SMALL;
@@ -623,7 +643,7 @@ extern "C" uw_status uw_matmul_bf16(const uint16_t *w, int64_t rows, int64_t col
         return UW_ERR_SHAPE;
     if (variant >= kGemvVariants)
         return UW_ERR_INVALID_ARG;
-    const int v = variant < 0 ? default_gemv_variant(rows, cols, batch) : variant;
+    const int v = variant < 0 ? default_gemv_variant(rows, cols, batch, kSrcBf16) : variant;
     const WsLayout L = layout_for(rows, cols, batch, UW_STRATEGY_FUSED, v);
     if (ws_bytes < L.total)
         return UW_ERR_BUFFER_TOO_SMALL;

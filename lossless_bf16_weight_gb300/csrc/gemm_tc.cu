@@ -548,13 +548,7 @@ int tc_stages(int G, int Np, int src, bool staged, uint32_t tdata) {
 
 }  // namespace
 
-size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed, uint32_t tdata) {
-    return tc_smem(G, S, Np, compressed ? kSrcHuffman : kSrcBf16, false, tdata);
-}
-
-int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tdata) {
-    return tc_stages(G, Np, compressed ? kSrcHuffman : kSrcBf16, false, tdata);
-}
+int gemm_tc_stages(int G, int Np, int src, uint32_t tdata) { return tc_stages(G, Np, src, false, tdata); }
 
 int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits) {
     if (splits <= 1)

@@ -68,8 +68,9 @@ struct TcParams {
     CUtensorMap xmap;      // x as a 2-D tensor (cols x batch rows), 64 x Np boxes, 128-byte
                            // swizzle (set by the launcher)
 };
-size_t gemm_tc_smem_bytes(int G, int S, int Np, bool compressed, uint32_t tdata);
-int gemm_tc_stages(int G, int Np, bool compressed, uint32_t tdata);
+// x stages the tensor-core kernel can keep with G producer groups, batch
+// rows Np, weights from `src` (tile data bytes tdata for the Huffman source).
+int gemm_tc_stages(int G, int Np, int src, uint32_t tdata);
 int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits);
 uw_status launch_gemm_tc(const TcParams &p, int G, int src, cudaStream_t stream);
 
@@ -138,7 +139,7 @@ struct WsLayout {
 //                      partials sit in its workspace (`weights` = their end).
 //   run_matmul         one matmul; p.status/counters/partial laid out as
 //                      run_layout says, p.w / p.p4 / p.v by `src`.
-uw_status plan_resolve(const uw_plan *plan, int64_t rows, int64_t cols, int64_t batch, int *strategy, int *variant);
+uw_status plan_resolve(const uw_plan *plan, const uw_desc &d, int64_t batch, int *strategy, int *variant);
 WsLayout run_layout(int64_t rows, int64_t cols, int64_t batch, int variant);
 uw_status run_matmul(const GemvParams &p, int variant, int src, cudaStream_t stream);
 

@@ -63,8 +63,10 @@ bool valid_desc(const uw_mlp_matrix &m) {
     return m.desc && m.blob_dev && m.desc->rows > 0 && m.desc->cols > 0 && m.desc->cols % kGroup == 0;
 }
 
-// Resolve every matrix's plan (role_plans: one per role for the matrices
-// without a form, overriding theirs; or NULL) and size the workspace.
+// Resolve every matrix's plan and size the workspace.  role_plans, when
+// given, overrides the matrices' own plans: entries 0..2 (gate, up, down)
+// for the matrices without a form, 3..5 for those with one (whose strategy
+// stays PALETTE4).
 uw_status plan_chain(const uw_mlp_matrix *m, int32_t n_layers, int64_t batch, const uw_plan *role_plans, Chain &c) {
     if (!m || n_layers <= 0 || batch <= 0)
         return UW_ERR_INVALID_ARG;
@@ -83,10 +85,13 @@ uw_status plan_chain(const uw_mlp_matrix *m, int32_t n_layers, int64_t batch, co
     for (int32_t i = 0; i < 3 * n_layers; i++) {
         const uw_desc &d = *m[i].desc;
         uw_plan pl = m[i].plan;
-        if (role_plans && !m[i].form_dev)
-            pl = role_plans[i % 3];
+        if (role_plans) {
+            pl = role_plans[i % 3 + (m[i].form_dev ? 3 : 0)];
+            if (m[i].form_dev)
+                pl.strategy = UW_STRATEGY_PALETTE4;
+        }
         Step &s = c.steps[size_t(i)];
-        uw_status st = plan_resolve(&pl, d.rows, d.cols, batch, &s.strategy, &s.variant);
+        uw_status st = plan_resolve(&pl, d, batch, &s.strategy, &s.variant);
         if (st != UW_OK)
             return st;
         const size_t n = size_t(d.rows) * size_t(d.cols);
@@ -273,28 +278,31 @@ uw_status run_chain(const uw_mlp_matrix *m, int32_t n_layers, const uint16_t *x,
     return s;
 }
 
-// Tensor-core variants without a K split (their grids leave SMs to a
-// preprocess kernel beside them), by name.
-std::vector<int> unsplit_tc_variants() {
+// Tensor-core variants with two or three producer groups (any K split;
+// split 1 leaves SMs to a preprocess kernel beside the matmul), by name.
+std::vector<int> tc_variants() {
     std::vector<int> out;
     const int n = uw_variant_count(UW_STRATEGY_FUSED);
     for (int v = 0; v < n; v++) {
         const char *name = uw_variant_name(UW_STRATEGY_FUSED, v);
-        const size_t len = name ? std::strlen(name) : 0;
-        if (len > 5 && std::strncmp(name, "tc_", 3) == 0 && std::strcmp(name + len - 2, "s1") == 0)
+        if (name && (std::strncmp(name, "tc_g2", 5) == 0 || std::strncmp(name, "tc_g3", 5) == 0))
             out.push_back(v);
     }
     return out;
 }
 
-std::vector<uw_plan> role_candidates(int64_t batch) {
+// Candidates of one role: the strategies (only PALETTE4 for the matrices
+// with a form) with their default variant, and from batch 16 the
+// tensor-core variants.
+std::vector<uw_plan> role_candidates(int64_t batch, bool with_form) {
     std::vector<uw_plan> c;
-    const int strategies[4] = {UW_STRATEGY_FUSED, UW_STRATEGY_EXPONENT, UW_STRATEGY_PALETTE4,
-                               UW_STRATEGY_DECOMPRESS_GEMM};
+    std::vector<int> strategies = {UW_STRATEGY_PALETTE4};
+    if (!with_form)
+        strategies = {UW_STRATEGY_FUSED, UW_STRATEGY_EXPONENT, UW_STRATEGY_PALETTE4, UW_STRATEGY_DECOMPRESS_GEMM};
     for (int st : strategies)
         c.push_back(uw_plan{st, -1, batch, 0.f});
     if (batch >= 16)
-        for (int v : unsplit_tc_variants())
+        for (int v : tc_variants())
             for (int st : strategies)
                 c.push_back(uw_plan{st, v, batch, 0.f});
     return c;
@@ -340,8 +348,8 @@ extern "C" uw_status uw_mlp_autotune_workspace_size(const uw_mlp_matrix *m, int3
     if (!bytes)
         return UW_ERR_INVALID_ARG;
     size_t most = 0;
-    for (const uw_plan &cand : role_candidates(batch)) {
-        const uw_plan roles[3] = {cand, cand, cand};
+    for (const uw_plan &cand : role_candidates(batch, false)) {
+        const uw_plan roles[6] = {cand, cand, cand, cand, cand, cand};
         Chain c;
         const uw_status s = plan_chain(m, n_layers, batch, roles, c);
         if (s == UW_ERR_INVALID_ARG || s == UW_ERR_SHAPE)
@@ -356,10 +364,14 @@ extern "C" uw_status uw_mlp_autotune_workspace_size(const uw_mlp_matrix *m, int3
 extern "C" uw_status uw_mlp_autotune(const uw_mlp_matrix *m, int32_t n_layers, const uint16_t *x, int64_t batch,
                                      uint16_t *y, int32_t passes, uw_plan *plans_out, uw_schedule *sched_out,
                                      void *ws, size_t ws_bytes, void *stream, void *side_stream) {
-    if (!x || !y || !ws || !plans_out || !sched_out || passes <= 0 || (reinterpret_cast<uintptr_t>(x) & 15))
+    if (!m || n_layers <= 0 || !x || !y || !ws || !plans_out || !sched_out || passes <= 0 ||
+        (reinterpret_cast<uintptr_t>(x) & 15))
         return UW_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream), side = static_cast<cudaStream_t>(side_stream);
-    const std::vector<uw_plan> cands = role_candidates(batch);
+    bool has_form[2] = {false, false};  // some matrix without / with a form
+    for (int32_t i = 0; i < 3 * n_layers; i++)
+        has_form[m[i].form_dev ? 1 : 0] = true;
+    const std::vector<uw_plan> cands[2] = {role_candidates(batch, false), role_candidates(batch, true)};
     std::vector<int> decs = {0};  // SM splits to try (only with a side stream)
     if (side && side != st)
         for (int d : {8, 16, 24, 32, 48, 64})
@@ -375,7 +387,7 @@ extern "C" uw_status uw_mlp_autotune(const uw_mlp_matrix *m, int32_t n_layers, c
     uint8_t *wsb = static_cast<uint8_t *>(ws);
     uw_status err = UW_OK;
     // median of 3 timed forwards after one warm-up; +inf for a plan that cannot run
-    auto measure = [&](const uw_plan roles[3], int dec) -> double {
+    auto measure = [&](const uw_plan roles[6], int dec) -> double {
         Chain c;
         if (plan_chain(m, n_layers, batch, roles, c) != UW_OK)
             return INFINITY;
@@ -407,14 +419,20 @@ extern "C" uw_status uw_mlp_autotune(const uw_mlp_matrix *m, int32_t n_layers, c
         std::sort(t, t + 3);
         return t[1];
     };
-    uw_plan roles[3] = {cands[0], cands[0], cands[0]};
+    // start: every role on its first candidate (fused, or palette-4 from the form)
+    uw_plan roles[6] = {cands[0][0], cands[0][0], cands[0][0], cands[1][0], cands[1][0], cands[1][0]};
     int dec = 0;
     double best = measure(roles, dec);
     for (int pass = 0; pass < passes && err == UW_OK; pass++) {
         bool changed = false;
-        for (int r = 0; r < 3 && err == UW_OK; r++)
-            for (const uw_plan &cand : cands) {
-                uw_plan trial[3] = {roles[0], roles[1], roles[2]};
+        for (int r = 0; r < 6 && err == UW_OK; r++) {
+            if (!has_form[r / 3])
+                continue;
+            for (const uw_plan &cand : cands[r / 3]) {
+                if (err != UW_OK)
+                    break;
+                uw_plan trial[6];
+                std::copy(roles, roles + 6, trial);
                 trial[r] = cand;
                 const double t = measure(trial, dec);
                 if (t < best * 0.99) {
@@ -423,6 +441,7 @@ extern "C" uw_status uw_mlp_autotune(const uw_mlp_matrix *m, int32_t n_layers, c
                     changed = true;
                 }
             }
+        }
         for (int d : decs) {
             if (d == dec || err != UW_OK)
                 continue;
@@ -442,7 +461,7 @@ extern "C" uw_status uw_mlp_autotune(const uw_mlp_matrix *m, int32_t n_layers, c
         return err;
     if (!std::isfinite(best))
         return UW_ERR_UNSUPPORTED;
-    for (int r = 0; r < 3; r++) {
+    for (int r = 0; r < 6; r++) {
         plans_out[r] = roles[r];
         plans_out[r].batch = batch;
         plans_out[r].us = float(best);

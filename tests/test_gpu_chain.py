@@ -225,9 +225,10 @@ def test_chain_autotune(g, uw, layers):
     ws = g.workspace(uw.mlp_autotune_workspace_size(mats, batch))
     side = torch.cuda.Stream()
     plans, sched = uw.mlp_autotune(mats, x, y, ws, passes=1, side_stream=side)
-    assert len(plans) == 3 and all(p.us > 0 for p in plans)
+    assert len(plans) == 6 and all(p.us > 0 for p in plans)
+    assert all(p.strategy == uw.STRATEGY_PALETTE4 for p in plans[3:])  # the matrices with a form
     assert sched.slots == 2 and sched.dec_ctas >= 0
-    tuned = [(d, b, f, plans[i % 3] if f is None else p) for i, (d, b, f, p) in enumerate(entries)]
+    tuned = [(d, b, f, plans[i % 3 + (3 if f is not None else 0)]) for i, (d, b, f, p) in enumerate(entries)]
     tmats = uw.mlp_matrices(tuned)
     y1, y2 = g.empty_bits(batch, D), g.empty_bits(batch, D)
     uw.mlp_forward(tmats, x, y1, ws, sched, side_stream=side)
