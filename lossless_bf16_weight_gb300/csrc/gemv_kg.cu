@@ -116,7 +116,6 @@ template <int W, bool kPrivate>
 __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_per_cta) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t bars[kMaxColWarps * kPairStages];
-    __shared__ PairMeta metas[kMaxColWarps * kPairStages];
     constexpr int kShift = kPrivate ? kShiftPrivate : kShiftShared;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const BlobView &v = p.v;
@@ -133,7 +132,8 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
     const uint32_t smoff = pair_stage_smoff(v.tdata);
 
     // shared memory: [private tables (kPrivate)][common tables][warp partials
-    // rb_per_cta x W x 32][pad to 128][per warp kPairStages stages]
+    // rb_per_cta x W x 32][pad to 128][per warp kPairStages stages][per warp
+    // kRecRing pair records]
     const uint32_t priv = smem_addr(smem);
     unsigned char *common = smem + (kPrivate ? kPrivateLutBytes : 0);
     const DecodeShared ds = carve_common(common);
@@ -142,6 +142,8 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
     const uint32_t stage_lo = (cbase + uint32_t(kCommonSmemBytes) + uint32_t(rb_per_cta) * W * 128u + 127u) & ~127u;
     const uint32_t st0 = stage_lo + uint32_t(warp) * kPairStages * sbytes;
     const uint32_t bar0 = smem_addr(&bars[warp * kPairStages]);
+    const uint32_t ring = stage_lo + uint32_t(W) * kPairStages * sbytes + uint32_t(warp) * kRecRing * kRecBytes;
+    const PairRecSpan span{npairs, rb0, k0, k1, np};
 
     if (lane == 0) {
 #pragma unroll
@@ -152,29 +154,20 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
     __syncwarp();
 
     // Prologue, ordered so that the memory round trips overlap the table
-    // build: the first two pairs' offsets (one round trip); the 1024 table
-    // entries; the two pairs' copies as soon as the offsets are in; chunk 0
-    // of the first pair's sign+mantissa bytes; then the private copies of the
-    // table while the copies fly.
-    PairMeta *meta = &metas[warp * kPairStages];
-    PairCursor issue{rb0, k0};
+    // build: the first kRecRound pairs' offsets (one round trip); the 1024
+    // table entries; their records and the first two pairs' copies as soon
+    // as the offsets are in; chunk 0 of the first pair's sign+mantissa bytes;
+    // then the private copies of the table while the copies fly.
     uint32_t nissued = 0;
-    PairCursor second = issue;
-    second.next(k0, k1);
-    uint32_t o_next = npairs ? pair_offsets_load2(v, rb0 * gpr + k0, second.rb * gpr + second.kgA) : 0u;
+    const RecLoad first = pair_recs_load(v, span, 0);
     build_tables(ds, v);
+    pair_recs_store(v, ring, span, 0, first);
 #pragma unroll
     for (int s = 0; s < kPairStages; s++) {
         if (nissued < npairs) {
-            if constexpr (kPrivate)
-                pair_issue_codes(v, o_next, issue.rb, issue.kgA, issue.kgA + 1 < k1, issue.rb * gpr + issue.kgA,
-                                 st0 + uint32_t(s) * sbytes, bar0 + 8u * s, meta + s);
-            else
-                pair_issue(v, o_next, issue.rb, issue.kgA, issue.kgA + 1 < k1, issue.rb * gpr + issue.kgA,
-                           st0 + uint32_t(s) * sbytes, smoff, bar0 + 8u * s, meta + s);
-            issue.next(k0, k1);
+            pair_issue_rec<!kPrivate>(v, ring + kRecBytes * nissued, st0 + uint32_t(s) * sbytes, smoff,
+                                      bar0 + 8u * s);
             nissued++;
-            o_next = pair_offsets_shift(o_next);  // the second pair's (lanes 8..13)
         }
     }
     // kPrivate: sign+mantissa bytes of the current pair, and its chunk 0 in
@@ -182,14 +175,12 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
     const uint8_t *sm_cur = nullptr;
     uint4 c0A = make_uint4(0, 0, 0, 0), c0B = c0A;
     if (kPrivate && npairs > 0) {
-        uint32_t R0;
-        sm_cur = pair_sm_base(v, rb0, k0, rb0 * gpr + k0, R0);
+        const uint32_t R0 = rb0 < v.nfull ? uint32_t(kTileRows) : v.tail_rows;
+        sm_cur = rec_sm(v, ring);
         const uint8_t *a = sm_cur + 16u * (uint32_t(lane) < R0 ? uint32_t(lane) : 0u);
         c0A = __ldg(reinterpret_cast<const uint4 *>(a));
         c0B = __ldg(reinterpret_cast<const uint4 *>(k0 + 1 < k1 ? a + 64u * R0 : a));
     }
-    if (nissued < npairs)
-        o_next = pair_offsets_load(v, issue.rb * gpr + issue.kgA);
     if constexpr (kPrivate) {
         __syncthreads();
         replicate_private(ds, priv);
@@ -210,7 +201,9 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
         const uint32_t s = j % kPairStages;
         const uint32_t st = st0 + s * sbytes, bar = bar0 + 8u * s;
         mbar_wait(bar, (j / kPairStages) & 1u, p.status, kStatusTimeout);
-        const PairMeta m = meta[s];
+        const uint32_t rec = ring + kRecBytes * (j % uint32_t(kRecRing));
+        const uint4 ra = lds128(rec), rbk = lds128(rec + 16u);
+        const uint32_t n16A = ra.w & 0xFFu, n16B = (ra.w >> 8) & 0xFFu, nescA = (ra.w >> 16) & 0x3Fu;
         const bool hasB = cur.kgA + 1 < k1;
         const bool full = cur.rb < v.nfull;
         const int R = full ? kTileRows : int(v.tail_rows);
@@ -226,10 +219,10 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
             gB = hasB ? __ldg(v.glen + q0 + uint32_t(R) + l) : 0u;
         }
         LaneStream la, lb;
-        const uint32_t cA = st + 64u, cB = cA + 16u * m.n16A;
+        const uint32_t cA = st + 64u, cB = cA + 16u * n16A;
         uint32_t emA, emB;
-        pair_begin_ready<kShift>(ds, gA, gB, m.pkA, m.pkB, R, hasB ? R : 0, cA, cB, la, lb, p.status, emA, emB);
-        const uint32_t ebA = cA + 16u * (m.n16A + m.n16B), ebB = ebA + 64u * m.nescA;
+        pair_begin_ready<kShift>(ds, gA, gB, rbk.x, rbk.y, R, hasB ? R : 0, cA, cB, la, lb, p.status, emA, emB);
+        const uint32_t ebA = cA + 16u * (n16A + n16B), ebB = ebA + 64u * nescA;
         const uint32_t stride = 16u * uint32_t(R);
         const uint32_t smA = st + smoff + 16u * uint32_t(lane), smB = smA + 64u * uint32_t(R);
         // kPrivate: the pair's bytes in global memory, and the next pair's
@@ -238,8 +231,9 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
         const bool more = j + 1 < npairs;
         PairCursor nxt = cur;
         nxt.next(k0, k1);
-        uint32_t Rn = 0;
-        const uint8_t *sm_nxt = kPrivate && more ? pair_sm_base(v, nxt.rb, nxt.kgA, nxt.rb * gpr + nxt.kgA, Rn) : sm_cur;
+        const uint32_t Rn = nxt.rb < v.nfull ? uint32_t(kTileRows) : v.tail_rows;
+        const uint8_t *sm_nxt =
+            kPrivate && more ? rec_sm(v, ring + kRecBytes * ((j + 1) % uint32_t(kRecRing))) : sm_cur;
         // an escaped group is redone after the loop from its sign+mantissa
         // bytes in global memory: have them in L1 by then
         if (kPrivate && ((emA | emB) >> lane) & 1u) {
@@ -323,16 +317,13 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
         fence_proxy_async_smem();
         __syncwarp();
         if (nissued < npairs) {
-            if constexpr (kPrivate)
-                pair_issue_codes(v, o_next, issue.rb, issue.kgA, issue.kgA + 1 < k1, issue.rb * gpr + issue.kgA, st,
-                                 bar, meta + s);
-            else
-                pair_issue(v, o_next, issue.rb, issue.kgA, issue.kgA + 1 < k1, issue.rb * gpr + issue.kgA, st, smoff,
-                           bar, meta + s);
-            issue.next(k0, k1);
+            pair_issue_rec<!kPrivate>(v, ring + kRecBytes * (nissued % uint32_t(kRecRing)), st, smoff, bar);
+            // the next round's records, kRecRound - 2 pairs before the first is
+            // issued (its ring slots belong to pairs already decoded)
+            if (nissued % uint32_t(kRecRound) == 2u && nissued - 2u + uint32_t(kRecRound) < npairs)
+                pair_recs_store(v, ring, span, nissued - 2u + uint32_t(kRecRound),
+                                pair_recs_load(v, span, nissued - 2u + uint32_t(kRecRound)));
             nissued++;
-            if (nissued < npairs)
-                o_next = pair_offsets_load(v, issue.rb * gpr + issue.kgA);
         }
         __syncwarp();
     }
@@ -536,7 +527,7 @@ size_t kg_smem(int warps, int rb_per_cta, int src, bool priv, uint32_t tdata, in
         return 32768 + size_t(kP4TableBytes) + size_t(gpr) * 128 + red;
     const size_t sbytes = priv ? code_stage_bytes(tdata) : pair_stage_bytes(tdata);
     return (priv ? size_t(kPrivateLutBytes) : 0) + size_t(kCommonSmemBytes) + red + 128 +
-           size_t(warps) * kPairStages * sbytes;
+           size_t(warps) * (kPairStages * sbytes + size_t(kRecRing) * kRecBytes);
 }
 
 template <int W, int kSrc, bool kPrivate>

@@ -159,6 +159,123 @@ __device__ __forceinline__ void pair_issue_codes(const BlobView &v, uint32_t o, 
     }
 }
 
+// What issuing a pair and decoding it need from the tile tables, worked out
+// for kRecRound pairs at a time (lane i: the round's pair i, all offsets in
+// one round trip) and kept in a ring of kRecRing records per warp, so that
+// issuing a pair is two shared-memory loads and the copies.
+constexpr int kRecRound = 8;
+constexpr int kRecRing = 2 * kRecRound;
+constexpr uint32_t kRecBytes = 32;
+
+// Record layout (8 words):
+//   0 c0      first 16-byte unit of tile A's codes
+//   1 bytes   code bytes | escape bytes << 16 (both 0 for a bad pair)
+//   2 e0      first escaped group of tile A
+//   3 sizes   n16A | n16B << 8 | nescA << 16 | (glen bytes / 32) << 22 | (R * tiles) << 24
+//   4 pkA     n16 | nesc << 8 | bad << 16 of tile A (as TileMeta.pk)
+//   5 pkB     the same for tile B (0 without B)
+//   6, 7      q0, the pair's first group (64-bit)
+// Lanes 0..kRecRound-1 fill the records of pairs base .. base+kRecRound-1
+// (pair j: row block rb0 + j / ppr, group kA = k0 + 2 (j % ppr), B present
+// when kA + 1 < k1): pair_recs_load issues the table loads, pair_recs_store
+// (after other work, if any) writes the records.
+struct PairRecSpan {
+    uint32_t npairs, rb0, k0, k1, ppr;
+};
+struct RecLoad {
+    uint32_t c0, c1, c2, e0, e1, e2;
+};
+
+__device__ __forceinline__ void rec_pair(const PairRecSpan &sp, uint32_t j, uint32_t gpr, uint32_t &rb, uint32_t &kgA,
+                                         bool &hasB) {
+    rb = sp.rb0 + j / sp.ppr;
+    kgA = sp.k0 + 2u * (j % sp.ppr);
+    hasB = kgA + 1 < sp.k1;
+}
+
+__device__ __forceinline__ RecLoad pair_recs_load(const BlobView &v, const PairRecSpan &sp, uint32_t base) {
+    const uint32_t lane = threadIdx.x & 31, j = base + lane;
+    RecLoad r{};
+    if (lane < uint32_t(kRecRound) && j < sp.npairs) {
+        uint32_t rb, kgA;
+        bool hasB;
+        rec_pair(sp, j, v.gpr, rb, kgA, hasB);
+        const uint32_t t = rb * v.gpr + kgA;
+        auto at = [&](const uint32_t *tab, uint32_t k) { return __ldg(tab + (k < v.ntiles ? k : v.ntiles)); };
+        r.c0 = at(v.tcode, t);
+        r.c1 = at(v.tcode, t + 1);
+        r.c2 = at(v.tcode, t + (hasB ? 2u : 1u));
+        r.e0 = at(v.tesc, t);
+        r.e1 = at(v.tesc, t + 1);
+        r.e2 = at(v.tesc, t + (hasB ? 2u : 1u));
+    }
+    return r;
+}
+
+__device__ __forceinline__ void pair_recs_store(const BlobView &v, uint32_t ring, const PairRecSpan &sp, uint32_t base,
+                                                const RecLoad &r) {
+    const uint32_t lane = threadIdx.x & 31, j = base + lane;
+    if (lane < uint32_t(kRecRound) && j < sp.npairs) {
+        uint32_t rb, kgA;
+        bool hasB;
+        rec_pair(sp, j, v.gpr, rb, kgA, hasB);
+        const uint32_t t = rb * v.gpr + kgA;
+        const bool full = rb < v.nfull;
+        const uint32_t R = full ? uint32_t(kTileRows) : v.tail_rows;
+        const uint32_t n16A = r.c1 - r.c0, n16B = r.c2 - r.c1, nescA = r.e1 - r.e0, nescB = r.e2 - r.e1;
+        const uint32_t lim16 = uint32_t(kMaxTileCodeBytes / 16);
+        const bool bad = n16A > lim16 || n16B > lim16 || nescA > R || nescB > R || n16A * 16u + nescA * 64u > v.tdata ||
+                         n16B * 16u + nescB * 64u > v.tdata || r.c2 > v.code16 || r.e2 > v.n_esc32;
+        const uint32_t ntile = hasB ? 2u : 1u;
+        const uint64_t q0 = uint64_t(t) * kTileRows - (full ? 0u : (kTileRows - R) * kgA);
+        const uint32_t bytes = bad ? 0u : ((r.c2 - r.c0) * 16u) | (((r.e2 - r.e0) * 64u) << 16);
+        const uint32_t sizes = (bad ? 0u : (n16A | (n16B << 8) | (nescA << 16))) | ((full ? ntile : 0u) << 22) |
+                               ((R * ntile) << 24);
+        const uint32_t pkA = bad ? (1u << 16) : (n16A | (nescA << 8));
+        const uint32_t pkB = !hasB ? 0u : bad ? (1u << 16) : (n16B | (nescB << 8));
+        const uint32_t a = ring + kRecBytes * (j % uint32_t(kRecRing));
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" :: "r"(a), "r"(r.c0), "r"(bytes), "r"(r.e0),
+                     "r"(sizes) : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" :: "r"(a + 16u), "r"(pkA), "r"(pkB),
+                     "r"(uint32_t(q0)), "r"(uint32_t(q0 >> 32)) : "memory");
+    }
+    __syncwarp();
+}
+
+// The pair's sign+mantissa bytes (tile A's first; B's follow 64 * R later).
+__device__ __forceinline__ const uint8_t *rec_sm(const BlobView &v, uint32_t rec) {
+    const uint4 b = lds128(rec + 16u);
+    return v.sm + ((uint64_t(b.w) << 32) | b.z) * kGroup;
+}
+
+// Start the bulk copies of a pair from its record (one lane issues):
+//   [0, 64)                  glen of A and B (full row blocks only)
+//   [64, 64 + 2*tdata)       code regions of A then B, then escaped exponents of A then B
+//   [smoff, smoff + 128*R)   kStageSm: sign+mantissa bytes of A then B;
+//                            otherwise they are only prefetched into L2
+template <bool kStageSm>
+__device__ __forceinline__ void pair_issue_rec(const BlobView &v, uint32_t rec, uint32_t st, uint32_t smoff,
+                                               uint32_t bar) {
+    if ((threadIdx.x & 31) == 0) {
+        const uint4 a = lds128(rec), b = lds128(rec + 16u);
+        const uint32_t code_bytes = a.y & 0xFFFFu, esc_bytes = a.y >> 16;
+        const uint32_t glen_bytes = ((a.w >> 22) & 3u) * 32u, sm_bytes = (a.w >> 24) * uint32_t(kGroup);
+        const uint64_t q0 = (uint64_t(b.w) << 32) | b.z;
+        mbar_expect_tx(bar, code_bytes + esc_bytes + glen_bytes + (kStageSm ? sm_bytes : 0u));
+        if (glen_bytes)
+            bulk_g2s(st, v.glen + q0, glen_bytes, bar);
+        if (code_bytes)
+            bulk_g2s(st + 64u, v.code + size_t(a.x) * 16, code_bytes, bar);
+        if (esc_bytes)
+            bulk_g2s(st + 64u + code_bytes, v.esc + size_t(a.z) * 64, esc_bytes, bar);
+        if constexpr (kStageSm)
+            bulk_g2s(st + smoff, v.sm + q0 * kGroup, sm_bytes, bar);
+        else
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(v.sm + q0 * kGroup), "r"(sm_bytes)
+                         : "memory");
+    }
+}
+
 // The warp's pairs in order: row block by row block, group pairs within
 // [k0, k1).
 struct PairCursor {
