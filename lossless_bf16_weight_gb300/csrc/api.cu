@@ -93,12 +93,14 @@ constexpr uint32_t kWorstTileData = kWorstTileBuf - kTileSlack;
 // Tensor-core default.  Producer groups: the most whose x stages fit for
 // this weight source (the kernel needs two K steps per group in flight).
 // K split: the one with the least estimated time, waves of the grid times
-// the K columns a CTA decodes, each split adding the partial sums it writes
-// and the last CTA reads back (np rows x 128 fp32 per CTA, weighted like six
-// K columns per batch row, fitted to the splits the chain tuner picks on
-// the MLP shapes); ties (within 2%) go to fewer splits.  This keeps one
-// split for 14336 x 4096 from batch 64 on and splits 4096 x 14336, whose 32
-// row blocks would fill a fifth of the GPU.
+// a CTA's cost in K columns: a fixed part (tables, tensor memory, the first
+// codes' round trips: ~900 columns' worth, ~10 us, fitted to one against four
+// splits at batch 16), the K columns it decodes, and with a split the
+// partial sums it writes and the last CTA reads back (np rows x 128 fp32,
+// weighted like six K columns per batch row, fitted to the splits the chain
+// tuner picks on the MLP shapes); ties (within 2%) go to fewer splits.  This
+// keeps one split for 14336 x 4096 and splits 4096 x 14336 four ways, whose
+// 32 row blocks would fill a fifth of the GPU.
 // The result does not depend on the number of groups (the MMAs accumulate
 // in K order), so the source only changes the speed.
 int default_tc_variant(int64_t rows, int64_t cols, int64_t batch, int src, uint32_t tdata) {
@@ -116,7 +118,7 @@ int default_tc_variant(int64_t rows, int64_t cols, int64_t batch, int src, uint3
         const int64_t sp = std::min<int64_t>(int64_t(1) << si, gpr);
         const int64_t waves = (mblocks * sp + sms - 1) / sms;
         const double k = double(cols) / double(sp);
-        const double cost = double(waves) * (k + (sp > 1 ? 6.0 * double(np) : 0.0));
+        const double cost = double(waves) * (900.0 + k + (sp > 1 ? 6.0 * double(np) : 0.0));
         if (si == 0 || cost < best_cost * 0.98) {
             best_cost = cost;
             best = si;

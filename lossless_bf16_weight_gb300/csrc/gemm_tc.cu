@@ -102,12 +102,17 @@ __device__ __forceinline__ void sm_chunks(const uint8_t *g_lane, uint32_t stride
         sm[c] = __ldg(reinterpret_cast<const uint4 *>(g_lane + c * stride));
 }
 
-template <int G, int kSrc, bool kSmStaged>
+// kPrivate (Huffman source, codes-only stages): the pair table as 32
+// lane-private copies, every lookup one shared-memory wavefront, as in the
+// batch-1 GEMV; it fits beside the x stages up to batch ~64.
+template <int G, int kSrc, bool kSmStaged, bool kPrivate>
 __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
     constexpr int P = 4 * G;  // producer warps
     constexpr bool kCompressed = kSrc == kSrcHuffman;
     constexpr bool kP4 = kSrc == kSrcPalette4;
     constexpr bool kExp = kSrc == kSrcExponent;
+    static_assert(!kPrivate || (kSrc == kSrcHuffman && !kSmStaged), "private tables: Huffman codes-only stages");
+    constexpr int kShift = kPrivate ? kShiftPrivate : kShiftShared;
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[2 * kTcMaxStages + 1];
     __shared__ __align__(8) uint64_t pbars[P * kPairStages];
@@ -126,12 +131,14 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
     const uint32_t nk = kg_hi - kg_lo, npr = (nk + 1) / 2;
     const uint32_t a0col = p.a0col;  // first tensor-memory column of the A stages
 
-    // shared memory: [pad to 1024][B stages][decode tables][per producer warp kPairStages pair stages]
+    // shared memory: [pad to 1024][B stages][private tables (kPrivate)][decode
+    // tables][per producer warp kPairStages pair stages]
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
     const uint32_t bstage = uint32_t(Np) * 128u;
     const uint32_t b0 = raw + pad;
-    unsigned char *dec = smem_raw + pad + size_t(S) * bstage;
+    const uint32_t priv = b0 + uint32_t(S) * bstage;
+    unsigned char *dec = smem_raw + pad + size_t(S) * bstage + (kPrivate ? size_t(kPrivateLutBytes) : 0);
     const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[kTcMaxStages]);
     const uint32_t done = smem_addr(&bars[2 * kTcMaxStages]);
     // pair stages: with the sign+mantissa bytes (kSmStaged) or codes only
@@ -196,6 +203,10 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
                 o_next = pair_offsets_load(v, rb * gpr + kg_lo + 2u * (uint32_t(grp) + nissued * G));
         }
     }
+    if constexpr (kPrivate) {
+        __syncthreads();
+        replicate_private(ds, priv);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -205,7 +216,7 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
     grid_dep_launch();
     grid_dep_wait();  // x (and the twin's weights) may come from the kernel before; the split partials are reused
     const uint32_t tmem = tmem_slot;
-    const uint32_t lut = kCompressed ? smem_addr(ds.lut) : 0u;
+    const uint32_t lut = !kCompressed ? 0u : kPrivate ? priv + 4u * uint32_t(lane) : smem_addr(ds.lut);
 
     if (producer) {
         const int R = !rb_ok ? 0 : rb < v.nfull || !kCompressed ? int(std::min<int64_t>(kTileRows, p.rows - int64_t(rb) * kTileRows))
@@ -248,8 +259,9 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
                     }
                     LaneStream la, lb;
                     const uint32_t cA = st + 64u, cB = cA + 16u * m.n16A;
-                    const uint32_t emA = tile_begin_ready(ds, TileMeta{gA, 0u, m.pkA}, R, cA, la, p.status);
-                    const uint32_t emB = tile_begin_ready(ds, TileMeta{gB, 0u, m.pkB}, hasB ? R : 0, cB, lb, p.status);
+                    uint32_t emA, emB;
+                    pair_begin_ready<kShift>(ds, gA, gB, m.pkA, m.pkB, R, hasB ? R : 0, cA, cB, la, lb, p.status, emA,
+                                             emB);
                     const uint32_t ebA = cA + 16u * (m.n16A + m.n16B), ebB = ebA + 64u * m.nescA;
                     // sign+mantissa bytes straight from L2 (prefetched there with the codes), one
                     // 16-byte chunk ahead; chunk 0 of this pair was loaded during the previous one
@@ -284,8 +296,8 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
                                 nB = __ldg(reinterpret_cast<const uint4 *>(kgN1 + 1 < kg_hi ? a + 64u * Rn : a));
                             }
                         }
-                        qA[I] = decode_pair(la, lut, I, word4(sA, (I >> 1) & 3));
-                        qB[I] = decode_pair(lb, lut, I, word4(sB, (I >> 1) & 3));
+                        qA[I] = decode_pair<kShift>(la, lut, I, word4(sA, (I >> 1) & 3));
+                        qB[I] = decode_pair<kShift>(lb, lut, I, word4(sB, (I >> 1) & 3));
                         if ((I & 7) == 7) {
                             sA = nA;
                             sB = nB;
@@ -507,20 +519,20 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
         p.counters[mb] = 0;
 }
 
-template <int G, int kSrc, bool kSmStaged>
+template <int G, int kSrc, bool kSmStaged, bool kPrivate>
 uw_status launch_tc_one(const TcParams &p, size_t smem, cudaStream_t stream) {
-    auto kern = gemm_tc_kernel<G, kSrc, kSmStaged>;
+    auto kern = gemm_tc_kernel<G, kSrc, kSmStaged, kPrivate>;
     if (!ensure_smem(kern, smem))
         return UW_ERR_CUDA;
     const dim3 grid(unsigned((p.rows + kTcM - 1) / kTcM), unsigned(p.splits));
     return launch_overlapped(kern, grid, dim3((4 * G + 2) * 32), smem, stream, p) == cudaSuccess ? UW_OK : UW_ERR_CUDA;
 }
 
-template <int kSrc, bool kSmStaged>
+template <int kSrc, bool kSmStaged, bool kPrivate = false>
 uw_status launch_tc_g(const TcParams &p, int G, size_t smem, cudaStream_t stream) {
-    return G == 1 ? launch_tc_one<1, kSrc, kSmStaged>(p, smem, stream)
-           : G == 2 ? launch_tc_one<2, kSrc, kSmStaged>(p, smem, stream)
-                    : launch_tc_one<3, kSrc, kSmStaged>(p, smem, stream);
+    return G == 1 ? launch_tc_one<1, kSrc, kSmStaged, kPrivate>(p, smem, stream)
+           : G == 2 ? launch_tc_one<2, kSrc, kSmStaged, kPrivate>(p, smem, stream)
+                    : launch_tc_one<3, kSrc, kSmStaged, kPrivate>(p, smem, stream);
 }
 
 // Tensor-memory columns before the A stages (the accumulator's Np, rounded up to 32).
@@ -528,9 +540,9 @@ uint32_t a0_col(int Np) { return (uint32_t(Np) + 31u) & ~31u; }
 
 // Shared memory of a launch; `staged` (Huffman source): the producers' pair
 // stages hold the sign+mantissa bytes too (otherwise the producers read
-// those from L2).
-size_t tc_smem(int G, int S, int Np, int src, bool staged, uint32_t tdata) {
-    size_t s = 1024 + size_t(S) * size_t(Np) * 128;
+// those from L2); `priv`: 32 lane-private copies of the pair table.
+size_t tc_smem(int G, int S, int Np, int src, bool staged, uint32_t tdata, bool priv = false) {
+    size_t s = 1024 + size_t(S) * size_t(Np) * 128 + (priv ? size_t(kPrivateLutBytes) : 0);
     if (src == kSrcHuffman)
         s += size_t(kCommonSmemBytes) + 128 +
              size_t(4 * G) * kPairStages * (staged ? pair_stage_bytes(tdata) : code_stage_bytes(tdata));
@@ -539,9 +551,9 @@ size_t tc_smem(int G, int S, int Np, int src, bool staged, uint32_t tdata) {
     return s;
 }
 
-int tc_stages(int G, int Np, int src, bool staged, uint32_t tdata) {
+int tc_stages(int G, int Np, int src, bool staged, uint32_t tdata, bool priv = false) {
     int S = std::min<int>(kTcMaxStages, int((kTmemCols - a0_col(Np)) / 32));
-    while (S > 1 && tc_smem(G, S, Np, src, staged, tdata) > size_t(kMaxSmemPerBlock - 1024))
+    while (S > 1 && tc_smem(G, S, Np, src, staged, tdata, priv) > size_t(kMaxSmemPerBlock - 1024))
         S--;
     return S;
 }
@@ -607,11 +619,16 @@ uw_status launch_gemm_tc(const TcParams &base, int G, int src, cudaStream_t stre
         // Huffman source: stage the sign+mantissa bytes in shared memory when that
         // leaves each producer group its two K steps (and some slack); read them
         // from L2 otherwise
-        const bool staged = src == kSrcHuffman && tc_stages(G, p.Np, kSrcHuffman, true, p.v.tdata) >= 2 * G + 2;
-        p.S = tc_stages(G, p.Np, src, staged, p.v.tdata);
+        // Huffman source, first choice: lane-private tables (conflict-free
+        // lookups) with codes-only stages, when they leave each producer group
+        // its two K steps and some slack
+        const bool priv = src == kSrcHuffman && tc_stages(G, p.Np, kSrcHuffman, false, p.v.tdata, true) >= 2 * G + 2;
+        const bool staged =
+            !priv && src == kSrcHuffman && tc_stages(G, p.Np, kSrcHuffman, true, p.v.tdata) >= 2 * G + 2;
+        p.S = tc_stages(G, p.Np, src, staged, p.v.tdata, priv);
         if (p.S < 2 * G)
             return UW_ERR_UNSUPPORTED;  // each producer group works on two K steps at once
-        const size_t smem = tc_smem(G, p.S, p.Np, src, staged, p.v.tdata);
+        const size_t smem = tc_smem(G, p.S, p.Np, src, staged, p.v.tdata, priv);
         uw_status s;
         if (src == kSrcBf16)
             s = launch_tc_g<kSrcBf16, false>(p, G, smem, stream);
@@ -619,6 +636,8 @@ uw_status launch_gemm_tc(const TcParams &base, int G, int src, cudaStream_t stre
             s = launch_tc_g<kSrcPalette4, false>(p, G, smem, stream);
         else if (src == kSrcExponent)
             s = launch_tc_g<kSrcExponent, false>(p, G, smem, stream);
+        else if (priv)
+            s = launch_tc_g<kSrcHuffman, false, true>(p, G, smem, stream);
         else if (staged)
             s = launch_tc_g<kSrcHuffman, true>(p, G, smem, stream);
         else
