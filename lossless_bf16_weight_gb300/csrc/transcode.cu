@@ -16,11 +16,12 @@
 // weight 32c + 2i + b is nibble b (0 = low) of byte i.  Escaped groups hold
 // index 0: their exponents stay in the blob's escape section.
 //
-// Each warp decodes consecutive tiles with the shared tile decoder
-// (decode.cuh) through a pair table whose entries carry palette indices (or
-// exponents); lane j packs row j's 64 indices into 32 bytes (or its 64
-// exponents into 64 bytes) and stores its chunks (32 lanes x 16 bytes = 512
-// contiguous bytes per store).
+// Persistent CTAs, one per SM, each with the pair table (whose entries carry
+// palette indices or exponents) replicated into 32 lane-private copies, so
+// that every lookup is one shared-memory wavefront.  Each warp walks runs of
+// consecutive tiles with the shared tile decoder (decode.cuh); lane j packs
+// row j's 64 indices into 32 bytes (or its 64 exponents into 64 bytes) and
+// stores its chunks (32 lanes x 16 bytes = 512 contiguous bytes per store).
 #include "decode.cuh"
 #include "kernels.h"
 
@@ -28,20 +29,27 @@ namespace uw {
 
 namespace {
 
-constexpr int kTcdWarps = 8;        // warps of a CTA launched over the whole matrix (two CTAs per SM)
-constexpr int kTcdWarpsSplit = 16;  // warps of a CTA of a capped, persistent grid (one CTA per SM)
+constexpr int kTcdWarps = 16;
 constexpr int kTcdTilesPerWarp = 4;
 
-template <bool kP4, int W>
-__global__ void __launch_bounds__(W * 32, 16 / W)
+// Shared memory: [32 private table copies][common tables][W x 2 tile buffers].
+size_t transcode_smem(uint32_t tbuf) {
+    return size_t(kPrivateLutBytes) + size_t(kCommonSmemBytes) + size_t(kTcdWarps) * 2 * size_t(tbuf);
+}
+
+template <bool kP4>
+__global__ void __launch_bounds__(kTcdWarps * 32, 1)
     transcode_kernel(const BlobView v, uint8_t *__restrict__ out, uint32_t *status) {
+    constexpr int W = kTcdWarps;
     extern __shared__ __align__(16) unsigned char smem[];
     grid_dep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const DecodeShared ds = carve_common(smem);
-    const uint32_t lut = smem_addr(ds.lut);
+    const uint32_t priv = smem_addr(smem);
+    unsigned char *common = smem + kPrivateLutBytes;
+    const DecodeShared ds = carve_common(common);
+    const uint32_t lut = priv + 4u * uint32_t(lane);  // this lane's copy
     const uint32_t tbuf = v.tbuf;
-    const uint32_t cbuf0 = smem_addr(smem + kCommonSmemBytes + size_t(warp) * 2 * tbuf);
+    const uint32_t cbuf0 = smem_addr(common + kCommonSmemBytes + size_t(warp) * 2 * tbuf);
 
     const uint32_t gpr = v.gpr, ntiles = v.ntiles;
     const uint32_t step = gridDim.x * uint32_t(W * kTcdTilesPerWarp);
@@ -62,13 +70,15 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     else
         build_tables(ds, v);
     __syncthreads();
+    replicate_private(ds, priv);  // while the first tiles' copies fly
+    __syncthreads();
     grid_dep_wait();  // the output may still be read by the kernel before
 
     for (uint32_t i = 0; cur.t < ntiles; i++) {
         const int R = tile_rows32(v, cur.rb);
         const uint32_t cbuf = cbuf0 + (i & 1u) * tbuf;
         LaneStream ls;
-        const uint32_t esc_mask = tile_begin(ds, meta, R, cbuf, ls, status);
+        const uint32_t esc_mask = tile_begin<kShiftPrivate>(ds, meta, R, cbuf, ls, status);
         const uint32_t ebase = escape_base(meta, cbuf);  // before meta is reused for the next tile
         TileWalk n2 = nxt;
         if (nxt.t < ntiles) {
@@ -85,7 +95,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
                 wd[k] = 0u;
 #pragma unroll
             for (int I = 0; I < 32; I++) {
-                const uint32_t ent = decode_entry(ls, lut);
+                const uint32_t ent = decode_entry<kShiftPrivate>(ls, lut);
                 const uint32_t byte = ((ent >> 7) & 15u) | ((ent >> 19) & 0xF0u);  // weights 2I (low), 2I+1
                 wd[I >> 2] |= byte << (8 * (I & 3));
             }
@@ -107,7 +117,7 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
                 wd[k] = 0u;
 #pragma unroll
             for (int I = 0; I < 32; I++) {
-                const uint32_t ent = decode_entry(ls, lut);
+                const uint32_t ent = decode_entry<kShiftPrivate>(ls, lut);
                 const uint32_t two = ((ent >> 7) & 0xFFu) | ((ent >> 15) & 0xFF00u);  // exponents of 2I, 2I+1
                 wd[I >> 1] |= two << (16 * (I & 1));
             }
@@ -130,31 +140,26 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
     }
 }
 
-template <int W>
-uw_status launch_transcode_w(const BlobView &v, uint8_t *out, bool palette4, uint32_t *status, int64_t grid,
-                             size_t min_smem, cudaStream_t stream) {
-    size_t smem = size_t(kCommonSmemBytes) + size_t(W) * 2 * size_t(v.tbuf);
-    smem = smem < min_smem ? min_smem : smem;
-    auto kern = palette4 ? transcode_kernel<true, W> : transcode_kernel<false, W>;
-    if (!ensure_smem(kern, smem))
-        return UW_ERR_CUDA;
-    return launch_overlapped(kern, dim3(unsigned(grid)), dim3(W * 32), smem, stream, v, out, status) == cudaSuccess
-               ? UW_OK
-               : UW_ERR_CUDA;
-}
-
 }  // namespace
 
 uw_status launch_transcode(const BlobView &v, uint8_t *out, bool palette4, uint32_t *status, cudaStream_t stream,
                            int max_ctas) {
+    const size_t smem = transcode_smem(v.tbuf);  // tile buffers are at most 2112 bytes: 198 KB at most
+    if (smem > size_t(kMaxSmemPerBlock))
+        return UW_ERR_INTERNAL;
     const int64_t per_cta = int64_t(kTcdWarps) * kTcdTilesPerWarp;
-    const int64_t grid = (int64_t(v.ntiles) + per_cta - 1) / per_cta;
-    if (max_ctas <= 0 || max_ctas >= grid)
-        return launch_transcode_w<kTcdWarps>(v, out, palette4, status, grid, 0, stream);
-    // capped: persistent CTAs of 16 warps, each holding an SM to itself
-    const int64_t per_split = int64_t(kTcdWarpsSplit) * kTcdTilesPerWarp;
-    const int64_t g = std::min<int64_t>(max_ctas, (int64_t(v.ntiles) + per_split - 1) / per_split);
-    return launch_transcode_w<kTcdWarpsSplit>(v, out, palette4, status, g, kExclusiveSmem, stream);
+    int64_t grid = std::min<int64_t>(sm_count(), (int64_t(v.ntiles) + per_cta - 1) / per_cta);
+    if (max_ctas > 0)  // capped: the SM share of a transcode running beside a matmul
+        grid = std::min<int64_t>(grid, max_ctas);
+    grid = std::max<int64_t>(grid, 1);
+    // more than half of an SM's shared memory: every CTA holds an SM alone
+    auto kern = palette4 ? transcode_kernel<true> : transcode_kernel<false>;
+    if (!ensure_smem(kern, smem))
+        return UW_ERR_CUDA;
+    return launch_overlapped(kern, dim3(unsigned(grid)), dim3(kTcdWarps * 32), smem, stream, v, out, status) ==
+                   cudaSuccess
+               ? UW_OK
+               : UW_ERR_CUDA;
 }
 
 }  // namespace uw
