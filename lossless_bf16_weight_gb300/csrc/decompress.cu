@@ -5,10 +5,12 @@
 // replicates it into 32 lane-private copies (entry w of copy l at word
 // 32*w + l), so every lookup of the decode loop is one shared-memory
 // wavefront whatever the 32 lanes' windows are.  Each warp then walks runs
-// of consecutive tiles with the shared tile decoder (decode.cuh).  Lane j
-// produces the 64 BF16 weights of row j; they pass through a per-warp 4 KB
-// shared-memory buffer (16-byte chunks XOR-swizzled by row, conflict-free
-// both ways) so that the global stores are coalesced 128-byte row segments.
+// of consecutive tiles with the shared tile decoder (decode.cuh); a tile's
+// sign+mantissa bytes are prefetched into L2 two tiles ahead and loaded
+// into registers one tile ahead.  Lane j produces the 64 BF16 weights of
+// row j; they pass through a per-warp 4 KB shared-memory buffer (16-byte
+// chunks XOR-swizzled by row, conflict-free both ways) so that the global
+// stores are coalesced 128-byte row segments.
 #include "decode.cuh"
 #include "kernels.h"
 
@@ -53,8 +55,10 @@ __global__ void __launch_bounds__(kDecompMaxWarps * 32, 1)
     const uint32_t cbuf0 = smem_addr(common + kCommonSmemBytes + size_t(warp) * 2 * tbuf);
     if (cur.t < ntiles) {
         tile_fetch(v, tile_loc32(v, cur.rb, cur.kg, cur.t), tile_offsets_load32(v, cur.t), cbuf0, meta, smn);
-        if (nxt.t < ntiles)
+        if (nxt.t < ntiles) {
             offs_next = tile_offsets_load32(v, nxt.t);
+            tile_prefetch_sm_l2(tile_loc32(v, nxt.rb, nxt.kg, nxt.t));
+        }
     }
     build_tables(ds, v);
     __syncthreads();
@@ -76,8 +80,12 @@ __global__ void __launch_bounds__(kDecompMaxWarps * 32, 1)
         if (nxt.t < ntiles) {
             tile_fetch(v, tile_loc32(v, nxt.rb, nxt.kg, nxt.t), offs_next, cbuf0 + ((i + 1) & 1u) * tbuf, meta, smn);
             walk_next(n2, kTilesPerWarp, step, ntiles, gpr);
-            if (n2.t < ntiles)
+            if (n2.t < ntiles) {
                 offs_next = tile_offsets_load32(v, n2.t);
+                // its sign+mantissa bytes go to registers one tile from now:
+                // have L2 hold them by then
+                tile_prefetch_sm_l2(tile_loc32(v, n2.rb, n2.kg, n2.t));
+            }
         }
         uint32_t q[4];
 #pragma unroll
