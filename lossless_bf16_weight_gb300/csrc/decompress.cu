@@ -1,16 +1,11 @@
 // Decompress a blob back to BF16 weights in HBM (the Unweight blog's "full
 // decode" pipeline: the restored matrix can then go to any GEMM).
 //
-// Persistent CTAs, one per SM: each CTA builds the pair table once and
-// replicates it into 32 lane-private copies (entry w of copy l at word
-// 32*w + l), so every lookup of the decode loop is one shared-memory
-// wavefront whatever the 32 lanes' windows are.  Each warp then walks runs
-// of consecutive tiles with the shared tile decoder (decode.cuh); a tile's
-// sign+mantissa bytes are prefetched into L2 two tiles ahead and loaded
-// into registers one tile ahead.  Lane j produces the 64 BF16 weights of
-// row j; they pass through a per-warp 4 KB shared-memory buffer (16-byte
-// chunks XOR-swizzled by row, conflict-free both ways) so that the global
-// stores are coalesced 128-byte row segments.
+// Each warp decodes consecutive tiles with the shared tile decoder
+// (decode.cuh).  Lane j produces the 64 BF16 weights of row j; they pass
+// through a per-warp 4 KB shared-memory buffer (16-byte chunks XOR-swizzled
+// by row, conflict-free both ways) so that the global stores are coalesced
+// 128-byte row segments.
 #include "decode.cuh"
 #include "kernels.h"
 
@@ -18,33 +13,27 @@ namespace uw {
 
 namespace {
 
-constexpr int kDecompMaxWarps = 16;
+constexpr int kDecompWarps = 8;        // warps of a CTA launched over the whole matrix (two CTAs per SM)
+constexpr int kDecompWarpsSplit = 16;  // warps of a CTA of a capped, persistent grid (one CTA per SM)
 constexpr int kTilesPerWarp = 4;
 constexpr int kOutBufBytes = kTileRows * kGroup * 2;  // 4096
 
-// Shared memory of a CTA of nw warps: [32 private table copies][common
-// tables][nw x 2 tile buffers][nw x output buffer].
-size_t decompress_smem(int nw, uint32_t tbuf) {
-    return size_t(kPrivateLutBytes) + size_t(kCommonSmemBytes) + size_t(nw) * (2 * size_t(tbuf) + kOutBufBytes);
-}
-
-__global__ void __launch_bounds__(kDecompMaxWarps * 32, 1)
+template <int W>
+__global__ void __launch_bounds__(W * 32, 16 / W)
     decompress_kernel(const BlobView v, uint16_t *__restrict__ out, uint32_t *status) {
     extern __shared__ __align__(16) unsigned char smem[];
     grid_dep_launch();
-    const uint32_t nw = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t priv = smem_addr(smem);
-    unsigned char *common = smem + kPrivateLutBytes;
-    const DecodeShared ds = carve_common(common);
-    const uint32_t lut = priv + 4u * uint32_t(lane);  // this lane's copy
+    const DecodeShared ds = carve_common(smem);
+    const uint32_t lut = smem_addr(ds.lut);
     const uint32_t tbuf = v.tbuf;
-    uint4 *obuf = reinterpret_cast<uint4 *>(common + kCommonSmemBytes + size_t(nw) * 2 * tbuf +
+    uint32_t *wbuf = reinterpret_cast<uint32_t *>(smem + kCommonSmemBytes + size_t(warp) * 2 * tbuf);
+    uint4 *obuf = reinterpret_cast<uint4 *>(smem + kCommonSmemBytes + size_t(W) * 2 * tbuf +
                                             size_t(warp) * kOutBufBytes);
 
     const uint32_t gpr = v.gpr, ntiles = v.ntiles;
-    const uint32_t step = gridDim.x * nw * uint32_t(kTilesPerWarp);
-    const uint64_t first = (uint64_t(blockIdx.x) * nw + warp) * kTilesPerWarp;
+    const uint32_t step = gridDim.x * uint32_t(W * kTilesPerWarp);
+    const uint64_t first = (uint64_t(blockIdx.x) * W + warp) * kTilesPerWarp;
     TileWalk cur, nxt;
     walk_seek(cur, first < ntiles ? uint32_t(first) : ntiles, gpr);
     nxt = cur;
@@ -52,17 +41,13 @@ __global__ void __launch_bounds__(kDecompMaxWarps * 32, 1)
     TileMeta meta{};
     uint4 smn[4];
     uint32_t offs_next = 0;
-    const uint32_t cbuf0 = smem_addr(common + kCommonSmemBytes + size_t(warp) * 2 * tbuf);
+    const uint32_t cbuf0 = smem_addr(wbuf);
     if (cur.t < ntiles) {
         tile_fetch(v, tile_loc32(v, cur.rb, cur.kg, cur.t), tile_offsets_load32(v, cur.t), cbuf0, meta, smn);
-        if (nxt.t < ntiles) {
+        if (nxt.t < ntiles)
             offs_next = tile_offsets_load32(v, nxt.t);
-            tile_prefetch_sm_l2(tile_loc32(v, nxt.rb, nxt.kg, nxt.t));
-        }
     }
     build_tables(ds, v);
-    __syncthreads();
-    replicate_private(ds, priv);  // while the first tiles' copies fly
     __syncthreads();
     grid_dep_wait();  // the output may still be read by the kernel before
 
@@ -74,23 +59,19 @@ __global__ void __launch_bounds__(kDecompMaxWarps * 32, 1)
         for (int c = 0; c < 4; c++)
             sm[c] = smn[c];
         LaneStream ls;
-        const uint32_t esc_mask = tile_begin<kShiftPrivate>(ds, meta, R, cbuf, ls, status);
+        const uint32_t esc_mask = tile_begin(ds, meta, R, cbuf, ls, status);
         const uint32_t ebase = escape_base(meta, cbuf);
         TileWalk n2 = nxt;
         if (nxt.t < ntiles) {
             tile_fetch(v, tile_loc32(v, nxt.rb, nxt.kg, nxt.t), offs_next, cbuf0 + ((i + 1) & 1u) * tbuf, meta, smn);
             walk_next(n2, kTilesPerWarp, step, ntiles, gpr);
-            if (n2.t < ntiles) {
+            if (n2.t < ntiles)
                 offs_next = tile_offsets_load32(v, n2.t);
-                // its sign+mantissa bytes go to registers one tile from now:
-                // have L2 hold them by then
-                tile_prefetch_sm_l2(tile_loc32(v, n2.rb, n2.kg, n2.t));
-            }
         }
         uint32_t q[4];
 #pragma unroll
         for (int I = 0; I < 32; I++) {
-            q[I & 3] = decode_pair<kShiftPrivate>(ls, lut, I, sm_word(sm, I >> 1));
+            q[I & 3] = decode_pair(ls, lut, I, sm_word(sm, I >> 1));
             if ((I & 3) == 3) {
                 const int c = I >> 2;  // 16-byte chunk of the row segment
                 obuf[lane * 8 + (c ^ (lane & 7))] = make_uint4(q[0], q[1], q[2], q[3]);
@@ -130,29 +111,30 @@ __global__ void __launch_bounds__(kDecompMaxWarps * 32, 1)
     }
 }
 
+template <int W>
+uw_status launch_decompress_w(const BlobView &v, uint16_t *w_out, uint32_t *status, int64_t grid, size_t min_smem,
+                              cudaStream_t stream) {
+    size_t smem = size_t(kCommonSmemBytes) + size_t(W) * (2 * size_t(v.tbuf) + kOutBufBytes);
+    smem = smem < min_smem ? min_smem : smem;
+    if (!ensure_smem(decompress_kernel<W>, smem))
+        return UW_ERR_CUDA;
+    return launch_overlapped(decompress_kernel<W>, dim3(unsigned(grid)), dim3(W * 32), smem, stream, v, w_out,
+                             status) == cudaSuccess
+               ? UW_OK
+               : UW_ERR_CUDA;
+}
+
 }  // namespace
 
 uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status, cudaStream_t stream, int max_ctas) {
-    // as many warps as the shared memory holds beside the private tables
-    // (tile buffers are at most 2112 bytes, so at least 11)
-    int nw = kDecompMaxWarps;
-    while (nw > 1 && decompress_smem(nw, v.tbuf) > size_t(kMaxSmemPerBlock))
-        nw--;
-    const size_t smem = decompress_smem(nw, v.tbuf);
-    if (smem > size_t(kMaxSmemPerBlock))
-        return UW_ERR_INTERNAL;
-    const int64_t per_cta = int64_t(nw) * kTilesPerWarp;
-    int64_t grid = std::min<int64_t>(sm_count(), (int64_t(v.ntiles) + per_cta - 1) / per_cta);
-    if (max_ctas > 0)  // capped: the SM share of a decode running beside a matmul
-        grid = std::min<int64_t>(grid, max_ctas);
-    grid = std::max<int64_t>(grid, 1);
-    // more than half of an SM's shared memory: every CTA holds an SM alone
-    if (!ensure_smem(decompress_kernel, smem))
-        return UW_ERR_CUDA;
-    return launch_overlapped(decompress_kernel, dim3(unsigned(grid)), dim3(unsigned(nw) * 32u), smem, stream, v,
-                             w_out, status) == cudaSuccess
-               ? UW_OK
-               : UW_ERR_CUDA;
+    const int64_t per_cta = int64_t(kDecompWarps) * kTilesPerWarp;
+    const int64_t grid = (int64_t(v.ntiles) + per_cta - 1) / per_cta;
+    if (max_ctas <= 0 || max_ctas >= grid)
+        return launch_decompress_w<kDecompWarps>(v, w_out, status, grid, 0, stream);
+    // capped: persistent CTAs of 16 warps, each holding an SM to itself
+    const int64_t per_split = int64_t(kDecompWarpsSplit) * kTilesPerWarp;
+    const int64_t g = std::min<int64_t>(max_ctas, (int64_t(v.ntiles) + per_split - 1) / per_split);
+    return launch_decompress_w<kDecompWarpsSplit>(v, w_out, status, g, kExclusiveSmem, stream);
 }
 
 }  // namespace uw

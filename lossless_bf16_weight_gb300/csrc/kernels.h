@@ -74,11 +74,15 @@ int gemm_tc_stages(int G, int Np, int src, uint32_t tdata);
 int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits);
 uw_status launch_gemm_tc(const TcParams &p, int G, int src, cudaStream_t stream);
 
-// Preprocess kernels: persistent CTAs, one per SM, each holding 32
+// Preprocess kernels.  max_ctas > 0 caps the grid (the SM split of a
+// preprocess kernel running beside a matmul on another stream) and leaves
+// the other SMs whole.  Decompress: over the whole matrix, 8-warp CTAs two
+// per SM with one shared pair table; capped, persistent CTAs that each ask
+// for kExclusiveSmem of shared memory so that each holds an SM by itself.
+// Transcode: always persistent CTAs, one per SM, each holding 32
 // lane-private copies of the pair table (more than half of an SM's shared
-// memory, so a CTA always has its SM to itself).  max_ctas > 0 caps the grid
-// (the SM split of a preprocess kernel running beside a matmul on another
-// stream) and leaves the other SMs whole.
+// memory, so a CTA always has its SM to itself).
+constexpr size_t kExclusiveSmem = 116 * 1024;
 uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status, cudaStream_t stream,
                             int max_ctas = 0);
 // Palette-4 form (rows*cols/2 bytes) or exponent form (rows*cols bytes) of a
