@@ -563,8 +563,23 @@ int uwo_read_header(const uint8_t *blob, int64_t bytes, uwo_info *info)
     if (info->n_groups != info->rows * gpr ||
         info->n_tiles != (info->rows + UWO_TROWS - 1) / UWO_TROWS * gpr)
         return -1;
-    if (info->off_esc + 64 * (uint64_t)info->n_escaped > (uint64_t)info->blob_bytes)
+    /* every section inside the blob, in the order the format lays them out
+     * (sizes kept below 2^62 first, so the sums cannot wrap) */
+    if (info->rows > ((int64_t)1 << 31) || info->cols > ((int64_t)1 << 31) || info->n_escaped < 0 ||
+        info->n_escaped > info->n_groups || info->blob_bytes < UWO_HEADER)
         return -1;
+    const uint64_t end = (uint64_t)info->blob_bytes;
+    const uint64_t tiles4 = 4 * ((uint64_t)info->n_tiles + 1);
+    const uint64_t start[6] = {info->off_sm, info->off_glen, info->off_tcode,
+                               info->off_tesc, info->off_code, info->off_esc};
+    const uint64_t size[6] = {(uint64_t)(info->rows * info->cols), (uint64_t)info->n_groups, tiles4,
+                              tiles4, 0, 64 * (uint64_t)info->n_escaped};
+    uint64_t prev = UWO_HEADER;
+    for (int s = 0; s < 6; s++) {
+        if (start[s] < prev || start[s] > end || size[s] > end - start[s])
+            return -1;
+        prev = start[s] + size[s];
+    }
     return 0;
 }
 
