@@ -111,6 +111,43 @@ def test_blob_info_rejects_corruption(lib):
     assert lib.blob_info_status(blob.tobytes()[:200]) == 4                  # shorter than header
 
 
+@pytest.mark.parametrize("name", ["heavy", "normal"])
+def test_blob_info_and_oracle_under_random_corruption(lib, oracle, name):
+    # Seeded random byte changes in the header, glen and tile tables (the
+    # sections a decoder trusts for addresses).  Neither decoder may crash;
+    # whatever the library's host check accepts must be structurally sound
+    # for the oracle's independent reader too: at most a bad code or a group
+    # length that disagrees with its codes, which only decoding can reveal
+    # (the GPU reports those through its status word).
+    w = (wl.heavy_tailed_weights(96, 512, seed=3) if name == "heavy"
+         else wl.normal_weights(70, 256, 0.02, seed=5))
+    blob = lib.compress(w).tobytes()
+    d = lib.blob_info(blob)
+    regions = [(0, 256), (d.off_glen, d.off_tcode), (d.off_tcode, d.off_tesc), (d.off_tesc, d.off_code)]
+    rng = np.random.default_rng(11)
+    accepted = 0
+    for _ in range(1500):
+        lo, hi = regions[int(rng.integers(len(regions)))]
+        pos = int(rng.integers(lo, hi))
+        mb = bytearray(blob)
+        new = int(rng.integers(256))
+        if new == mb[pos]:
+            continue
+        mb[pos] = new
+        mb = bytes(mb)
+        sl = lib.blob_info_status(mb)
+        so = oracle.decompress_status(mb)
+        assert sl in (0, 4), (pos, new, sl)
+        assert so in (0, -1, -2, -3, -4), (pos, new, so)
+        if sl == 0:
+            accepted += 1
+            assert so in (0, -2, -3), (pos, new, so)
+    assert accepted > 0
+    for cut in rng.integers(0, len(blob), 50):
+        assert lib.blob_info_status(blob[:int(cut)]) == 4
+        assert oracle.decompress_status(blob[:int(cut)]) == -1
+
+
 def test_compression_ratio_and_statistics(lib):
     # ~30% fewer bytes for N(0, 0.02) weights (blog: ~30% on MLP weights).
     w = wl.normal_weights(1024, 4096, 0.02, seed=0)
