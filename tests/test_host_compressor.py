@@ -59,6 +59,37 @@ def test_blob_identical_to_oracle(lib, oracle, name):
     assert np.array_equal(oracle.decompress(lb.tobytes()), w)
 
 
+def _random_matrix(rng):
+    rows = int(rng.integers(1, 100))
+    cols = 64 * int(rng.integers(1, 9))
+    kind = int(rng.integers(4))
+    if kind == 0:  # normal at a random scale
+        sigma = float(10.0 ** rng.uniform(-4, 1))
+        return wl.normal_weights(rows, cols, sigma, seed=int(rng.integers(1 << 30)))
+    if kind == 1:  # raw random bit patterns: every exponent, most groups escaped
+        return rng.integers(0, 1 << 16, (rows, cols)).astype(np.uint16)
+    sm = rng.integers(0, 1 << 16, (rows, cols)).astype(np.uint16) & np.uint16(0x807F)
+    if kind == 2:  # a few exponents with random weights, a sprinkle of rare ones
+        m = int(rng.integers(1, 21))
+        vals = rng.choice(256, size=m, replace=False)
+        e = vals[rng.choice(m, size=(rows, cols), p=rng.dirichlet(np.ones(m)))]
+        rare = rng.random((rows, cols)) < 0.002
+        e = np.where(rare, rng.integers(0, 256, (rows, cols)), e)
+    else:  # the extremes: zero / subnormal and Inf / NaN exponents mixed with ordinary ones
+        e = rng.choice(np.array([0, 0, 255, 120, 121, 122]), size=(rows, cols))
+    return (sm | (e.astype(np.uint16) << 7)).astype(np.uint16)
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_blob_identical_to_oracle_random_matrices(lib, oracle, seed):
+    w = _random_matrix(np.random.default_rng(1000 + seed))
+    ob, oinfo = oracle.compress(w)
+    lb = lib.compress(w)
+    assert lb.tobytes() == ob
+    assert lib.blob_info_status(lb) == 0
+    assert np.array_equal(oracle.decompress(ob), w)
+
+
 def test_blob_identical_to_oracle_gate_proj_shape(lib, oracle):
     w = wl.normal_weights(1024, 4096, 0.02, seed=11)
     assert lib.compress(w).tobytes() == oracle.compress(w)[0]
