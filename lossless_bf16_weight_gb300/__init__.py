@@ -17,6 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libuw.so")
 
 UW_OK = 0
+UW_ERR_BUFFER_TOO_SMALL = 3
 STATUS_NAMES = {0: "UW_OK", 1: "UW_ERR_INVALID_ARG", 2: "UW_ERR_SHAPE", 3: "UW_ERR_BUFFER_TOO_SMALL",
                 4: "UW_ERR_CORRUPT", 5: "UW_ERR_CUDA", 6: "UW_ERR_TIMEOUT", 7: "UW_ERR_UNSUPPORTED",
                 8: "UW_ERR_INTERNAL"}
@@ -149,6 +150,41 @@ def _plan_ptr(plan):
     return None if plan is None else ctypes.byref(plan)
 
 
+def _nbytes(t) -> int:
+    return t.nbytes if isinstance(t, np.ndarray) else t.numel() * t.element_size()
+
+
+def _contiguous(t) -> bool:
+    return t.flags.c_contiguous if isinstance(t, np.ndarray) else t.is_contiguous()
+
+
+def _short(*bufs) -> str | None:
+    """The C ABI sees plain pointers, so a buffer smaller than what a call
+    reads or writes would make a kernel run past its end.  Each argument is
+    (buffer, bytes the call touches, name); returns why the first one that
+    is not contiguous or too small is refused, or None."""
+    for t, need, name in bufs:
+        if not _contiguous(t):
+            return "%s is not contiguous" % name
+        if _nbytes(t) < need:
+            return "%s holds %d bytes, the call needs %d" % (name, _nbytes(t), need)
+    return None
+
+
+def _refuse(why: str | None, what: str):
+    if why is not None:
+        raise UwError(UW_ERR_BUFFER_TOO_SMALL, "%s (%s)" % (what, why))
+
+
+def _batch(x) -> int:
+    return x.shape[0] if x.dim() == 2 else 1
+
+
+def _mm_bufs(desc, blob_dev, x, y):
+    b = _batch(x)
+    return [(blob_dev, desc.blob_bytes, "blob_dev"), (x, 2 * b * desc.cols, "x"), (y, 2 * b * desc.rows, "y")]
+
+
 # ---------------------------------------------------------------- host side
 def compress(w: np.ndarray) -> np.ndarray:
     """uw_compress: BF16 weight matrix (uint16 bits, [rows, cols]) -> blob bytes (uint8)."""
@@ -215,33 +251,42 @@ def workspace_init(ws, stream=None):
 
 
 def decompress(desc: Desc, blob_dev, w_out, ws, stream=None):
+    _refuse(_short((blob_dev, desc.blob_bytes, "blob_dev"), (w_out, 2 * desc.rows * desc.cols, "w_out")),
+            "uw_decompress")
     _check(load().uw_decompress(ctypes.byref(desc), _ptr(blob_dev), _ptr(w_out), _ptr(ws),
                                 ws.numel() * ws.element_size(), _stream(stream)), "uw_decompress")
 
 
 def matmul(desc: Desc, blob_dev, x, y, ws, plan: Plan | None = None, stream=None):
     """y[batch, rows] = x[batch, cols] W^T with W compressed in blob_dev."""
-    batch = x.shape[0] if x.dim() == 2 else 1
+    _refuse(_short(*_mm_bufs(desc, blob_dev, x, y)), "uw_matmul")
+    batch = _batch(x)
     _check(load().uw_matmul(ctypes.byref(desc), _ptr(blob_dev), _ptr(x), batch, _ptr(y), _plan_ptr(plan),
                             _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "uw_matmul")
 
 
 def matmul_status(desc: Desc, blob_dev, x, y, ws, plan: Plan | None = None, stream=None) -> int:
-    batch = x.shape[0] if x.dim() == 2 else 1
+    if _short(*_mm_bufs(desc, blob_dev, x, y)):
+        return UW_ERR_BUFFER_TOO_SMALL
+    batch = _batch(x)
     return int(load().uw_matmul(ctypes.byref(desc), _ptr(blob_dev), _ptr(x), batch, _ptr(y), _plan_ptr(plan),
                                 _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def matmul_noalloc(desc: Desc, blob_dev, x, y, stream=None) -> int:
     """uw_matmul_noalloc: fused matmul with library-held scratch; returns the status."""
-    batch = x.shape[0] if x.dim() == 2 else 1
+    if _short(*_mm_bufs(desc, blob_dev, x, y)):
+        return UW_ERR_BUFFER_TOO_SMALL
+    batch = _batch(x)
     return int(load().uw_matmul_noalloc(ctypes.byref(desc), _ptr(blob_dev), _ptr(x), batch, _ptr(y),
                                         _stream(stream)))
 
 
 def matmul_bf16(w, x, y, ws, variant: int = -1, stream=None):
     rows, cols = w.shape
-    batch = x.shape[0] if x.dim() == 2 else 1
+    batch = _batch(x)
+    _refuse(_short((w, 2 * rows * cols, "w"), (x, 2 * batch * cols, "x"), (y, 2 * batch * rows, "y")),
+            "uw_matmul_bf16")
     _check(load().uw_matmul_bf16(_ptr(w), rows, cols, _ptr(x), batch, _ptr(y), variant, _ptr(ws),
                                  ws.numel() * ws.element_size(), _stream(stream)), "uw_matmul_bf16")
 
@@ -262,12 +307,16 @@ def palette4_bytes(desc: Desc) -> int:
 
 def transcode_palette4(desc: Desc, blob_dev, p4_out, ws, stream=None):
     """uw_transcode_palette4: the 4-bit palette index of every weight into p4_out."""
+    _refuse(_short((blob_dev, desc.blob_bytes, "blob_dev"), (p4_out, desc.rows * desc.cols // 2, "p4_out")),
+            "uw_transcode_palette4")
     _check(load().uw_transcode_palette4(ctypes.byref(desc), _ptr(blob_dev), _ptr(p4_out), _ptr(ws),
                                         ws.numel() * ws.element_size(), _stream(stream)), "uw_transcode_palette4")
 
 
 def matmul_palette4_status(desc: Desc, blob_dev, p4, x, y, ws, variant: int = -1, stream=None) -> int:
-    batch = x.shape[0] if x.dim() == 2 else 1
+    if _short(*_mm_bufs(desc, blob_dev, x, y), (p4, desc.rows * desc.cols // 2, "p4")):
+        return UW_ERR_BUFFER_TOO_SMALL
+    batch = _batch(x)
     return int(load().uw_matmul_palette4(ctypes.byref(desc), _ptr(blob_dev), _ptr(p4), _ptr(x), batch, _ptr(y),
                                          variant, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
@@ -285,12 +334,16 @@ def exponent_bytes(desc: Desc) -> int:
 
 def decode_exponents(desc: Desc, blob_dev, e_out, ws, stream=None):
     """uw_decode_exponents: the exponent byte of every weight into e_out."""
+    _refuse(_short((blob_dev, desc.blob_bytes, "blob_dev"), (e_out, desc.rows * desc.cols, "e_out")),
+            "uw_decode_exponents")
     _check(load().uw_decode_exponents(ctypes.byref(desc), _ptr(blob_dev), _ptr(e_out), _ptr(ws),
                                       ws.numel() * ws.element_size(), _stream(stream)), "uw_decode_exponents")
 
 
 def matmul_exponents_status(desc: Desc, blob_dev, e, x, y, ws, variant: int = -1, stream=None) -> int:
-    batch = x.shape[0] if x.dim() == 2 else 1
+    if _short(*_mm_bufs(desc, blob_dev, x, y), (e, desc.rows * desc.cols, "e")):
+        return UW_ERR_BUFFER_TOO_SMALL
+    batch = _batch(x)
     return int(load().uw_matmul_exponents(ctypes.byref(desc), _ptr(blob_dev), _ptr(e), _ptr(x), batch, _ptr(y),
                                           variant, _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
@@ -301,6 +354,8 @@ def matmul_exponents(desc: Desc, blob_dev, e, x, y, ws, variant: int = -1, strea
 
 
 def swiglu(g, u, h, stream=None):
+    n = g.numel()
+    _refuse(_short((g, 2 * n, "g"), (u, 2 * n, "u"), (h, 2 * n, "h")), "uw_swiglu")
     _check(load().uw_swiglu(_ptr(g), _ptr(u), _ptr(h), g.numel(), _stream(stream)), "uw_swiglu")
 
 
@@ -311,6 +366,7 @@ def mlp_matrices(entries) -> ctypes.Array:
     the array is used."""
     arr = (MlpMatrix * len(entries))()
     for i, (d, blob, form, plan) in enumerate(entries):
+        _refuse(_short((blob, d.blob_bytes, "blob_dev")), "uw_mlp_matrix %d" % i)
         arr[i].desc = ctypes.pointer(d)
         arr[i].blob_dev = _ptr(blob)
         arr[i].form_dev = None if form is None else _ptr(form)
@@ -335,8 +391,17 @@ def mlp_workspace_size(mats, batch: int, sched: Schedule | None = None) -> int:
     return int(n.value)
 
 
+def _chain_short(mats, x, y) -> str | None:
+    if len(mats) < 3:
+        return None  # the library refuses an empty chain itself
+    dim_in, dim_out = mats[0].desc.contents.cols, mats[len(mats) // 3 * 3 - 1].desc.contents.rows
+    return _short((x, 2 * x.shape[0] * dim_in, "x"), (y, 2 * x.shape[0] * dim_out, "y"))
+
+
 def mlp_forward_status(mats, x, y, ws, sched: Schedule | None = None, stream=None, side_stream=None) -> int:
     """uw_mlp_forward: y = the chain of len(mats)//3 SwiGLU MLP layers applied to x."""
+    if _chain_short(mats, x, y):
+        return UW_ERR_BUFFER_TOO_SMALL
     return int(load().uw_mlp_forward(mats, len(mats) // 3, _ptr(x), x.shape[0], _ptr(y), _sched_ptr(sched),
                                      _ptr(ws), ws.numel() * ws.element_size(), _stream(stream),
                                      _side(side_stream)))
@@ -356,6 +421,7 @@ def mlp_autotune_workspace_size(mats, batch: int) -> int:
 def mlp_autotune(mats, x, y, ws, passes: int = 2, stream=None, side_stream=None):
     """uw_mlp_autotune: (6 plans: gate, up, down without a form, then with
     one; Schedule) by coordinate descent."""
+    _refuse(_chain_short(mats, x, y), "uw_mlp_autotune")
     plans = (Plan * 6)()
     sched = Schedule()
     _check(load().uw_mlp_autotune(mats, len(mats) // 3, _ptr(x), x.shape[0], _ptr(y), passes, plans,
