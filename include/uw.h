@@ -81,7 +81,13 @@ enum {
 };
 
 /* Description of a compressed matrix, filled by uw_blob_info from the blob
- * header (host copy).  All offsets are byte offsets from the blob start. */
+ * header (host copy).  All offsets are byte offsets from the blob start.
+ * Every entry point that reads a blob re-checks the descriptor it is given
+ * (sizes and counts consistent, at most 2^31 rows and columns, sections in
+ * order inside blob_bytes, code lengths a prefix code of at most 5 bits) and
+ * returns UW_ERR_INVALID_ARG for one that uw_blob_info could not have filled.
+ * The size queries (uw_workspace_size, uw_palette4_bytes, ...) read only rows
+ * and cols. */
 typedef struct {
     int64_t rows, cols;
     uint64_t blob_bytes;     /* total blob size                              */

@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "format.h"
+#include "desc_check.h"
 #include "kernels.h"
 #include "uw.h"
 
@@ -380,6 +381,49 @@ extern "C" const char *uw_status_string(uw_status s) {
     return "unknown status";
 }
 
+namespace uw {
+
+// The checks on a blob's header that need nothing but the header: sizes, the
+// counts they imply, the sections in order inside blob_bytes, and a prefix
+// code on the palette.  Sizes stay small enough that no section size wraps
+// and every tile and escape index fits the kernels' 32-bit arithmetic.
+bool desc_ok(const uw_desc &d) {
+    if (d.lmax != kLmax || d.n_palette < 0 || d.n_palette > kPalette)
+        return false;
+    if (d.rows <= 0 || d.cols <= 0 || d.cols % kGroup || d.rows > (int64_t(1) << 31) || d.cols > (int64_t(1) << 31))
+        return false;
+    const uint64_t rows = uint64_t(d.rows), cols = uint64_t(d.cols);
+    const uint64_t gpr = cols / kGroup;
+    const uint64_t ntiles = (rows + kTileRows - 1) / kTileRows * gpr;
+    if (d.n_groups != rows * gpr || d.n_tiles != ntiles || d.n_escaped > d.n_groups ||
+        ntiles >= (uint64_t(1) << 32) || d.n_escaped >= (uint64_t(1) << 32))
+        return false;
+    const uint64_t sec[6] = {d.off_sm, d.off_glen, d.off_tcode, d.off_tesc, d.off_code, d.off_esc};
+    if (d.blob_bytes >= (uint64_t(1) << 62))
+        return false;
+    for (uint64_t o : sec)
+        if (o % kSectionAlign || o > d.blob_bytes)
+            return false;
+    if (d.off_sm != uint64_t(kHeaderBytes) || d.off_glen < d.off_sm + rows * cols ||
+        d.off_tcode < d.off_glen + d.n_groups || d.off_tesc < d.off_tcode + 4 * (ntiles + 1) ||
+        d.off_code < d.off_tesc + 4 * (ntiles + 1) || d.off_esc < d.off_code ||
+        d.off_esc + 64 * d.n_escaped > d.blob_bytes)
+        return false;
+    double kraft = 0.0;
+    for (int s = 0; s < kPalette; s++) {
+        if (d.code_len[s] > kLmax || (s >= d.n_palette && d.code_len[s]))
+            return false;
+        if (d.code_len[s])
+            kraft += 1.0 / double(1u << d.code_len[s]);
+        for (int t = 0; t < s && s < d.n_palette; t++)
+            if (d.palette[t] == d.palette[s])
+                return false;
+    }
+    return kraft <= 1.0;
+}
+
+}  // namespace uw
+
 extern "C" uw_status uw_blob_info(const void *blob_host, size_t bytes, uw_desc *out) {
     if (!blob_host || !out)
         return UW_ERR_INVALID_ARG;
@@ -406,38 +450,11 @@ extern "C" uw_status uw_blob_info(const void *blob_host, size_t bytes, uw_desc *
     d.off_esc = rd64(b + hdr::off_esc);
     d.blob_bytes = rd64(b + hdr::blob_bytes);
     if (rd32(b + hdr::group) != uint32_t(kGroup) || rd32(b + hdr::tile_rows) != uint32_t(kTileRows) ||
-        d.lmax != kLmax || d.n_palette < 0 || d.n_palette > kPalette)
-        return UW_ERR_CORRUPT;
-    if (d.rows <= 0 || d.cols <= 0 || d.cols % kGroup || d.rows > (int64_t(1) << 40) || d.cols > (int64_t(1) << 40))
+        !desc_ok(d) || d.blob_bytes > bytes)
         return UW_ERR_CORRUPT;
     const uint64_t rows = uint64_t(d.rows), cols = uint64_t(d.cols);
     const uint64_t gpr = cols / kGroup;
     const uint64_t ntiles = (rows + kTileRows - 1) / kTileRows * gpr;
-    if (d.n_groups != rows * gpr || d.n_tiles != ntiles || d.n_escaped > d.n_groups)
-        return UW_ERR_CORRUPT;
-    // sections in order, 256-aligned, inside the blob
-    const uint64_t sec[6] = {d.off_sm, d.off_glen, d.off_tcode, d.off_tesc, d.off_code, d.off_esc};
-    for (uint64_t o : sec)
-        if (o % kSectionAlign)
-            return UW_ERR_CORRUPT;
-    if (d.off_sm != uint64_t(kHeaderBytes) || d.off_glen < d.off_sm + rows * cols ||
-        d.off_tcode < d.off_glen + d.n_groups || d.off_tesc < d.off_tcode + 4 * (ntiles + 1) ||
-        d.off_code < d.off_tesc + 4 * (ntiles + 1) || d.off_esc < d.off_code ||
-        d.off_esc + 64 * d.n_escaped > d.blob_bytes || d.blob_bytes > bytes)
-        return UW_ERR_CORRUPT;
-    // a prefix code on the palette, lengths within the limit
-    double kraft = 0.0;
-    for (int s = 0; s < kPalette; s++) {
-        if (d.code_len[s] > kLmax || (s >= d.n_palette && d.code_len[s]))
-            return UW_ERR_CORRUPT;
-        if (d.code_len[s])
-            kraft += 1.0 / double(1u << d.code_len[s]);
-        for (int t = 0; t < s && s < d.n_palette; t++)
-            if (d.palette[t] == d.palette[s])
-                return UW_ERR_CORRUPT;
-    }
-    if (kraft > 1.0)
-        return UW_ERR_CORRUPT;
     // tile tables against the group lengths
     const uint32_t *tcode = reinterpret_cast<const uint32_t *>(b + d.off_tcode);
     const uint32_t *tesc = reinterpret_cast<const uint32_t *>(b + d.off_tesc);
@@ -505,7 +522,7 @@ extern "C" uw_status uw_check_status(void *ws, void *stream) {
 
 extern "C" uw_status uw_decompress(const uw_desc *d, const void *blob_dev, uint16_t *w_dev, void *ws,
                                    size_t ws_bytes, void *stream) {
-    if (!d || !blob_dev || !w_dev || !ws || (reinterpret_cast<uintptr_t>(w_dev) & 15))
+    if (!d || !blob_dev || !w_dev || !ws || (reinterpret_cast<uintptr_t>(w_dev) & 15) || !desc_ok(*d))
         return UW_ERR_INVALID_ARG;
     if (ws_bytes < 256)
         return UW_ERR_BUFFER_TOO_SMALL;
@@ -516,7 +533,7 @@ extern "C" uw_status uw_decompress(const uw_desc *d, const void *blob_dev, uint1
 
 extern "C" uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uint16_t *x, int64_t batch,
                                uint16_t *y, const uw_plan *plan, void *ws, size_t ws_bytes, void *stream) {
-    if (!d || !blob_dev || !x || !y || !ws || batch <= 0 || (reinterpret_cast<uintptr_t>(x) & 15))
+    if (!d || !blob_dev || !x || !y || !ws || batch <= 0 || (reinterpret_cast<uintptr_t>(x) & 15) || !desc_ok(*d))
         return UW_ERR_INVALID_ARG;
     ResolvedPlan rp;
     uw_status s = resolve_plan(plan, d->rows, d->cols, batch, &rp, tile_data_bytes(*d));
@@ -565,7 +582,7 @@ extern "C" uw_status uw_palette4_bytes(const uw_desc *d, size_t *bytes) {
 
 extern "C" uw_status uw_transcode_palette4(const uw_desc *d, const void *blob_dev, void *p4_dev, void *ws,
                                            size_t ws_bytes, void *stream) {
-    if (!d || !blob_dev || !p4_dev || !ws || (reinterpret_cast<uintptr_t>(p4_dev) & 15))
+    if (!d || !blob_dev || !p4_dev || !ws || (reinterpret_cast<uintptr_t>(p4_dev) & 15) || !desc_ok(*d))
         return UW_ERR_INVALID_ARG;
     if (ws_bytes < 256)
         return UW_ERR_BUFFER_TOO_SMALL;
@@ -579,7 +596,7 @@ namespace {
 uw_status matmul_formed(const uw_desc *d, const void *blob_dev, const void *form_dev, const uint16_t *x, int64_t batch,
                         uint16_t *y, int32_t variant, void *ws, size_t ws_bytes, void *stream, int src) {
     if (!d || !blob_dev || !form_dev || !x || !y || !ws || batch <= 0 || (reinterpret_cast<uintptr_t>(x) & 15) ||
-        (reinterpret_cast<uintptr_t>(form_dev) & 15))
+        (reinterpret_cast<uintptr_t>(form_dev) & 15) || !desc_ok(*d))
         return UW_ERR_INVALID_ARG;
     if (variant >= kGemvVariants)
         return UW_ERR_INVALID_ARG;
@@ -619,7 +636,7 @@ extern "C" uw_status uw_exponent_bytes(const uw_desc *d, size_t *bytes) {
 
 extern "C" uw_status uw_decode_exponents(const uw_desc *d, const void *blob_dev, void *e_dev, void *ws,
                                          size_t ws_bytes, void *stream) {
-    if (!d || !blob_dev || !e_dev || !ws || (reinterpret_cast<uintptr_t>(e_dev) & 15))
+    if (!d || !blob_dev || !e_dev || !ws || (reinterpret_cast<uintptr_t>(e_dev) & 15) || !uw::desc_ok(*d))
         return UW_ERR_INVALID_ARG;
     if (ws_bytes < 256)
         return UW_ERR_BUFFER_TOO_SMALL;

@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "format.h"
+#include "desc_check.h"
 #include "kernels.h"
 #include "uw.h"
 
@@ -69,7 +70,7 @@ extern "C" uw_status uw_autotune_workspace_size(const uw_desc *d, const int64_t 
 
 extern "C" uw_status uw_autotune(const uw_desc *d, const void *blob_dev, const int64_t *batches, int32_t n,
                                  uw_plan *plans_out, void *ws, size_t ws_bytes, void *stream) {
-    if (!d || !blob_dev || !batches || n <= 0 || !plans_out || !ws)
+    if (!d || !blob_dev || !batches || n <= 0 || !plans_out || !ws || !uw::desc_ok(*d))
         return UW_ERR_INVALID_ARG;
     size_t need = 0;
     uw_status s = uw_autotune_workspace_size(d, batches, n, &need);

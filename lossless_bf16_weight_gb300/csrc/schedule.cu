@@ -15,6 +15,7 @@
 #include <cstring>
 #include <vector>
 
+#include "desc_check.h"
 #include "kernels.h"
 #include "uw.h"
 
@@ -60,7 +61,7 @@ ChainLayout chain_layout(const Chain &c, int64_t batch, int slots) {
 }
 
 bool valid_desc(const uw_mlp_matrix &m) {
-    return m.desc && m.blob_dev && m.desc->rows > 0 && m.desc->cols > 0 && m.desc->cols % kGroup == 0;
+    return m.desc && m.blob_dev && desc_ok(*m.desc);
 }
 
 // Resolve every matrix's plan and size the workspace.  role_plans, when
