@@ -121,7 +121,10 @@ typedef struct {
  *   blob_out   host buffer of *blob_bytes bytes, or NULL to query the size.
  *   blob_bytes in: capacity of blob_out; out: size of the blob.
  * Returns UW_ERR_BUFFER_TOO_SMALL (with *blob_bytes set) when blob_out is
- * NULL or too small.  Uses the host's cores (OpenMP); deterministic. */
+ * NULL or too small, UW_ERR_SHAPE when cols is not a positive multiple of 64
+ * or rows is not positive, UW_ERR_UNSUPPORTED beyond 2^31 rows or columns or
+ * when the tile tables' 32-bit offsets would overflow.  Uses the host's cores
+ * (OpenMP); deterministic. */
 uw_status uw_compress(const uint16_t *w_host, int64_t rows, int64_t cols,
                       void *blob_out, size_t *blob_bytes);
 

@@ -193,6 +193,8 @@ extern "C" uw_status uw_compress(const uint16_t *w, int64_t rows, int64_t cols, 
         return UW_ERR_INVALID_ARG;
     if (rows <= 0 || cols <= 0 || cols % kGroup)
         return UW_ERR_SHAPE;
+    if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31))
+        return UW_ERR_UNSUPPORTED;  // the blob descriptor's limit (no size product can wrap)
     const int64_t gpr = cols / kGroup;
     const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
     const int64_t ntiles = nrb * gpr;

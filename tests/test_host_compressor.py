@@ -118,6 +118,9 @@ def test_compress_rejects_bad_shapes(lib):
     assert L.uw_compress(w.ctypes.data, 4, 0, None, ctypes.byref(n)) == 2
     assert L.uw_compress(None, 4, 64, None, ctypes.byref(n)) == 1
     assert L.uw_compress(w.ctypes.data, 4, 64, None, ctypes.byref(n)) == 3 and n.value > 0
+    # beyond 2^31 rows or columns (checked before the data is read)
+    assert L.uw_compress(w.ctypes.data, 1, (1 << 31) + 64, None, ctypes.byref(n)) == 7
+    assert L.uw_compress(w.ctypes.data, (1 << 31) + 1, 64, None, ctypes.byref(n)) == 7
 
 
 def _corrupt(blob, pos, value):
