@@ -169,7 +169,8 @@ uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uint16_t *x_de
  * baseline that compression is measured against.
  *   w_dev   [rows, cols] BF16 device weights, x_dev [batch, cols]; both
  *           16-byte aligned (UW_ERR_INVALID_ARG otherwise).  variant as in
- *           uw_plan. */
+ *           uw_plan.  cols a positive multiple of 64 (UW_ERR_SHAPE), rows and
+ *           cols at most 2^31 (UW_ERR_UNSUPPORTED), as for compressed matrices. */
 uw_status uw_matmul_bf16(const uint16_t *w_dev, int64_t rows, int64_t cols,
                          const uint16_t *x_dev, int64_t batch, uint16_t *y_dev,
                          int32_t variant, void *ws_dev, size_t ws_bytes, void *stream);

@@ -660,6 +660,8 @@ extern "C" uw_status uw_matmul_bf16(const uint16_t *w, int64_t rows, int64_t col
         return UW_ERR_INVALID_ARG;
     if (rows <= 0 || cols <= 0 || cols % kGroup)
         return UW_ERR_SHAPE;
+    if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31))
+        return UW_ERR_UNSUPPORTED;  // the same limit as compressed matrices
     if (variant >= kGemvVariants)
         return UW_ERR_INVALID_ARG;
     const int v = variant < 0 ? default_gemv_variant(rows, cols, batch, kSrcBf16) : variant;

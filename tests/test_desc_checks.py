@@ -82,3 +82,11 @@ def test_inconsistent_descriptors_are_refused(uw, what):
     MUTATIONS[what](d)
     for name, call in _entry_points(L, uw, d).items():
         assert call() == INVALID, (what, name)
+
+
+def test_uncompressed_twin_has_the_same_size_limit(uw):
+    L = uw.load()
+    assert L.uw_matmul_bf16(P, (1 << 31) + 32, 64, P, 1, P, -1, P, 0, None) == 7  # UW_ERR_UNSUPPORTED
+    assert L.uw_matmul_bf16(P, 32, (1 << 31) + 64, P, 1, P, -1, P, 0, None) == 7
+    assert L.uw_matmul_bf16(P, 32, 96, P, 1, P, -1, P, 0, None) == 2              # UW_ERR_SHAPE
+    assert L.uw_matmul_bf16(P, 32, 128, P, 1, P, -1, P, 0, None) == TOO_SMALL
