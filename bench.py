@@ -395,14 +395,15 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.out = None
 
     def start(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
-        os.close(fd)
+        self.out = os.fdopen(fd, "w")
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
-                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         time.sleep(0.3)
@@ -417,6 +418,7 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        self.out.close()
         rows = []
         try:
             with open(self.path) as f:

@@ -78,3 +78,12 @@ def test_peak_comes_from_the_measured_file_when_present():
         assert kind == "measured"
     else:
         assert (value, kind) == (bench.FALLBACK_HBM_GBS, "fallback")
+
+
+def test_clock_sampler_without_nvidia_smi(monkeypatch):
+    # No nvidia-smi on the path: no samples, and the temporary file is gone.
+    monkeypatch.setenv("PATH", "")
+    c = bench.ClockSampler(0)
+    c.start()
+    assert c.stop() == []
+    assert not os.path.exists(c.path)
