@@ -418,7 +418,8 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-        self.out.close()
+        if self.out is not None:
+            self.out.close()
         rows = []
         try:
             with open(self.path) as f:
