@@ -95,8 +95,9 @@ def test_heavy_tailed_batches(g, uw, oracle, heavy, batch):
 
 
 def test_model_slice_autotuned(g, uw, oracle):
-    # Layers 0 and 31 of the 32-layer model (the sigmas at both ends of the
-    # draw), every matrix autotuned over a spread of batches.
+    # The first and the last layer of the 32-layer model, every matrix
+    # autotuned over a spread of batches (the layers with the smallest and
+    # largest sigma are compared with the oracle on the CPU).
     batches = [1, 16, 256]
     for layer in (0, 31):
         for j in range(3):

@@ -90,6 +90,18 @@ def test_blob_identical_to_oracle_random_matrices(lib, oracle, seed):
     assert np.array_equal(oracle.decompress(ob), w)
 
 
+@pytest.mark.parametrize("j", [0, 2])
+def test_blob_identical_to_oracle_on_the_extreme_sigma_layers(lib, oracle, j):
+    # The 32-layer model's smallest and largest sigma (layers argmin and
+    # argmax of the draw), on a slice of rows of the gate and down matrices.
+    sig = wl.model_sigmas()
+    for layer in (int(np.argmin(sig)), int(np.argmax(sig))):
+        w = np.ascontiguousarray(wl.model_matrix(layer, j)[:96])
+        ob, _ = oracle.compress(w)
+        assert lib.compress(w).tobytes() == ob
+        assert np.array_equal(oracle.decompress(ob), w)
+
+
 def test_blob_identical_to_oracle_gate_proj_shape(lib, oracle):
     w = wl.normal_weights(1024, 4096, 0.02, seed=11)
     assert lib.compress(w).tobytes() == oracle.compress(w)[0]
