@@ -27,8 +27,11 @@
  *     round-to-nearest-even to BF16.
  *   - cols must be a positive multiple of 64 and rows positive, otherwise
  *     UW_ERR_SHAPE.
- *   - The caller owns all memory.  The library allocates no device memory:
- *     pointers marked _dev are device pointers, _host host pointers.
+ *   - The caller owns all memory.  The library allocates no device memory,
+ *     with one exception: the 1 MiB scratch array of uw_matmul_noalloc, a
+ *     static device array that every GPU which loads the library holds until
+ *     the process exits.  Pointers marked _dev are device pointers, _host
+ *     host pointers.
  *     Scratch space ("workspace") is passed in by the caller; its size comes
  *     from uw_workspace_size and it must be cleared once with
  *     uw_workspace_init before first use.  Kernels leave it ready for the
@@ -269,6 +272,18 @@ uw_status uw_autotune_workspace_size(const uw_desc *d, const int64_t *batches, i
  * that. */
 uw_status uw_matmul_noalloc(const uw_desc *d, const void *blob_dev, const uint16_t *x_dev,
                             int64_t batch, uint16_t *y_dev, void *stream);
+
+/* uw_selftest_bounded_wait -- exercises the failure path of the kernels'
+ * bounded waits.  Launches one small kernel that waits, with the same wait
+ * routine the matmul and decode kernels use, on a shared-memory barrier
+ * that nothing arrives on; after `tries` attempts (1 .. 2^22, the kernels'
+ * own limit) the wait gives up, records a timeout in the workspace's status
+ * word and the kernel returns.  uw_check_status(ws) then reports
+ * UW_ERR_TIMEOUT (and clears the word); the CUDA context stays usable.
+ *   ws_dev   a workspace of at least 256 bytes (only its status word is used).
+ * Returns UW_ERR_INVALID_ARG for tries outside 1 .. 2^22.  Diagnostic only:
+ * the Unweight blog has no counterpart. */
+uw_status uw_selftest_bounded_wait(void *ws_dev, size_t ws_bytes, uint32_t tries, void *stream);
 
 /* uw_swiglu -- h = bf16(silu(g) * u), silu(z) = z / (1 + e^-z) in fp32,
  * the glue between the gate/up and down projections of a SwiGLU MLP.

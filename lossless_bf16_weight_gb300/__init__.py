@@ -99,6 +99,7 @@ SIGNATURES = [
     ("uw_mlp_autotune_workspace_size", ctypes.c_int, [ctypes.POINTER(MlpMatrix), _I32, _I64,
                                                       ctypes.POINTER(_SZ)]),
     ("uw_check_status", ctypes.c_int, [_P, _P]),
+    ("uw_selftest_bounded_wait", ctypes.c_int, [_P, _SZ, ctypes.c_uint32, _P]),
     ("uw_variant_name", ctypes.c_char_p, [_I32, _I32]),
     ("uw_variant_count", ctypes.c_int32, [_I32]),
     ("uw_status_string", ctypes.c_char_p, [ctypes.c_int]),
@@ -428,6 +429,13 @@ def mlp_autotune(mats, x, y, ws, passes: int = 2, stream=None, side_stream=None)
                                   ctypes.byref(sched), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream),
                                   _side(side_stream)), "uw_mlp_autotune")
     return list(plans), sched
+
+
+def selftest_bounded_wait(ws, tries: int, stream=None) -> None:
+    """uw_selftest_bounded_wait: a kernel whose bounded wait runs out; read
+    the result with check_status."""
+    _check(load().uw_selftest_bounded_wait(_ptr(ws), ws.numel() * ws.element_size(), int(tries), _stream(stream)),
+           "uw_selftest_bounded_wait")
 
 
 def check_status(ws, stream=None) -> int:

@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["compress.cpp", "api.cu", "autotune.cu", "gemv.cu", "gemv_kg.cu", "gemm_tc.cu", "decompress.cu", "transcode.cu", "swiglu.cu",
-           "noalloc.cu", "schedule.cu"]
+           "noalloc.cu", "schedule.cu", "diag.cu"]
 
 
 def _nvcc() -> str:

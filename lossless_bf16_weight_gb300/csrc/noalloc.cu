@@ -7,8 +7,10 @@
 // exits.  The call itself allocates nothing: no cudaMalloc, no cudaFree.
 #include <cuda_runtime.h>
 
+#include <cstdint>
 #include <mutex>
 
+#include "desc_check.h"
 #include "uw.h"
 
 namespace {
@@ -41,6 +43,10 @@ void *scratch_address(int device, uw_status *err) {
 extern "C" uw_status uw_matmul_noalloc(const uw_desc *d, const void *blob_dev, const uint16_t *x_dev,
                                        int64_t batch, uint16_t *y_dev, void *stream) {
     if (!d || !blob_dev || !x_dev || !y_dev || batch <= 0)
+        return UW_ERR_INVALID_ARG;
+    // the checks uw_matmul makes, before any size is worked out from the
+    // descriptor and before anything is queued on the stream
+    if (!uw::desc_ok(*d) || (reinterpret_cast<uintptr_t>(x_dev) & 15u) != 0)
         return UW_ERR_INVALID_ARG;
     size_t need = 0;
     uw_status s = uw_workspace_size(d, batch, nullptr, &need);

@@ -44,13 +44,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed; false (and
-// `flag` set in *status) if it did not within kWaitTries attempts.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *status, uint32_t flag) {
-    for (uint32_t i = 0; i < kWaitTries; i++)
+// `flag` set in *status) if it did not within `tries` attempts.
+__device__ __forceinline__ bool mbar_wait_tries(uint32_t bar, uint32_t parity, uint32_t *status, uint32_t flag,
+                                                uint32_t tries) {
+    for (uint32_t i = 0; i < tries; i++)
         if (mbar_try_wait(bar, parity))
             return true;
     atomicOr(status, flag);
     return false;
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *status, uint32_t flag) {
+    return mbar_wait_tries(bar, parity, status, flag, kWaitTries);
 }
 
 // Arrive on the mbarrier and add `bytes` to the transaction count its

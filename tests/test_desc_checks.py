@@ -1,5 +1,6 @@
 """Every entry point that reads a blob checks the descriptor it is given
-before any device work: one filled by uw_blob_info passes, one with
+before any device work (uw_matmul_noalloc included): one filled by
+uw_blob_info passes, one with
 inconsistent sizes, sections or code lengths is refused with
 UW_ERR_INVALID_ARG.  The calls get a zero-byte workspace, so a descriptor
 that passes stops at UW_ERR_BUFFER_TOO_SMALL; no pointer is dereferenced
@@ -82,6 +83,16 @@ def test_inconsistent_descriptors_are_refused(uw, what):
     MUTATIONS[what](d)
     for name, call in _entry_points(L, uw, d).items():
         assert call() == INVALID, (what, name)
+    # the entry point without a workspace refuses it before it sizes or
+    # clears any scratch (nothing is queued on a stream)
+    assert L.uw_matmul_noalloc(ctypes.byref(d), P, P, ctypes.c_int64(1), P, None) == INVALID, what
+
+
+def test_noalloc_refuses_unaligned_x_before_device_work(uw):
+    L = uw.load()
+    d = uw.blob_info(uw.compress(wl.normal_weights(96, 256, 0.02, seed=1)))
+    assert L.uw_matmul_noalloc(ctypes.byref(d), P, ctypes.c_void_p(4096 + 8), ctypes.c_int64(1), P,
+                               None) == INVALID
 
 
 def test_uncompressed_twin_has_the_same_size_limit(uw):

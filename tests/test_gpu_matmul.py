@@ -121,6 +121,6 @@ def test_autotune_picks_a_runnable_plan(g, uw):
     plans = uw.autotune(c.desc, c.blob_dev, [1, 4], ws)
     assert [p.batch for p in plans] == [1, 4]
     for p in plans:
-        assert p.us > 0 and p.strategy in (0, 1) and 0 <= p.variant < uw.variant_count(p.strategy)
+        assert p.us > 0 and p.strategy in (uw.STRATEGY_DECOMPRESS_GEMM, uw.STRATEGY_FUSED, uw.STRATEGY_PALETTE4, uw.STRATEGY_EXPONENT) and 0 <= p.variant < uw.variant_count(p.strategy)
     xd = g.dev_bits(x)
     assert np.array_equal(c.matmul(xd, plans[0]), c.matmul(xd))

@@ -5,7 +5,8 @@ batches 1, 16, 64 and 256, and a slice of the 32-layer model with the
 autotuner choosing the plan per matrix and batch.
 
 Checks: every fused output equals the same kernel fed uncompressed BF16
-weights bit for bit; sampled outputs lie within 4 * 2^-8 * sum_k |x_k w_k| of
+weights bit for bit; every MLP output at batch <= 8, and sampled outputs
+elsewhere, lie within 4 * 2^-8 * sum_k |x_k w_k| of
 the fp64 oracle; the SwiGLU output lies within one BF16 ulp of silu(g) * u
 computed in fp64 from the GPU's own g and u; the down projection is checked
 against the oracle fed the GPU's h, so that stage-to-stage rounding does not
@@ -35,6 +36,14 @@ def _check_rows(g, oracle, x, w, y, rows):
         g.assert_within_bound(y[:, n:n + 1], y_ref, absum)
 
 
+def _check_all_or_rows(g, oracle, x, w, y, rows):
+    if rows is None:
+        y_ref, absum = oracle.matmul_f64(x, w)
+        g.assert_within_bound(y, y_ref, absum)
+    else:
+        _check_rows(g, oracle, x, w, y, rows)
+
+
 @pytest.fixture(scope="module")
 def mlp(g):
     mats = []
@@ -53,9 +62,11 @@ def test_mlp_layer(g, uw, oracle, mlp, batch):
     up = cu.matmul(xd)
     assert np.array_equal(gate, g.matmul_bf16(wgd, xd))
     assert np.array_equal(up, g.matmul_bf16(wud, xd))
-    rows = _sample_rows(wl.GATE_SHAPE[0], 16, batch)
-    _check_rows(g, oracle, x, wg, gate, rows)
-    _check_rows(g, oracle, x, wu, up, rows)
+    # every output at batch <= 8, a seeded sample of rows above that
+    full = batch <= 8
+    rows = None if full else _sample_rows(wl.GATE_SHAPE[0], 16, batch)
+    _check_all_or_rows(g, oracle, x, wg, gate, rows)
+    _check_all_or_rows(g, oracle, x, wu, up, rows)
 
     h_dev = g.empty_bits(batch, wl.GATE_SHAPE[0])
     uw.swiglu(g.dev_bits(gate), g.dev_bits(up), h_dev)
@@ -68,7 +79,7 @@ def test_mlp_layer(g, uw, oracle, mlp, batch):
 
     y = cd.matmul(h_dev)
     assert np.array_equal(y, g.matmul_bf16(wdd, h_dev))
-    _check_rows(g, oracle, h, wd, y, _sample_rows(wl.DOWN_SHAPE[0], 16, batch + 1))
+    _check_all_or_rows(g, oracle, h, wd, y, None if full else _sample_rows(wl.DOWN_SHAPE[0], 16, batch + 1))
 
 
 @pytest.fixture(scope="module")

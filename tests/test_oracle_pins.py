@@ -129,6 +129,49 @@ def _cost(freq, lens):
     return sum(f * l for f, l in zip(freq, lens))
 
 
+def _package_merge_lengths(freq, lmax):
+    """Optimal length-limited code lengths by package-merge (Larmore and
+    Hirschberg, 1990), written here independently of the oracle's exhaustive
+    search: the coin collector's problem over lmax denominations.  Each of
+    the n used symbols is a coin of every width 2^-1 .. 2^-lmax with its
+    frequency as numismatic value; repeatedly pair up the cheapest coins of
+    the narrowest width (packages) and merge them with the next width's
+    coins; the 2n - 2 cheapest items of the widest list pay for total width
+    n - 1, and a symbol's code length is the number of chosen items that
+    contain it."""
+    used = [i for i, f in enumerate(freq) if f > 0]
+    lens = [0] * len(freq)
+    if len(used) == 1:
+        lens[used[0]] = 1
+        return lens
+    if not used:
+        return lens
+    leaves = sorted(((int(freq[i]), (i,)) for i in used), key=lambda t: t[0])
+    items = list(leaves)
+    for _ in range(lmax - 1):
+        packages = [(items[j][0] + items[j + 1][0], items[j][1] + items[j + 1][1])
+                    for j in range(0, len(items) - 1, 2)]
+        items = sorted(leaves + packages, key=lambda t: t[0])
+    for _, members in items[: 2 * len(used) - 2]:
+        for i in members:
+            lens[i] += 1
+    return lens
+
+
+def _skewed_histogram(rng):
+    """Counts of 16 palette symbols shaped like trained-layer exponents: a
+    geometric-ish decay with a random rate, random noise, and now and then a
+    few near-ties or a very rare symbol."""
+    rate = rng.uniform(0.45, 0.9)
+    base = rng.uniform(1e3, 1e6) * rate ** np.arange(16) * rng.uniform(0.7, 1.3, 16)
+    if rng.random() < 0.3:
+        base[rng.integers(0, 16)] = rng.integers(1, 5)
+    if rng.random() < 0.3:
+        j = int(rng.integers(0, 15))
+        base[j + 1] = base[j]
+    return [max(1, int(v)) for v in base]
+
+
 def _kraft(lens):
     return sum(2.0 ** -l for l in lens if l > 0)
 
@@ -179,20 +222,52 @@ def test_code_lengths_equal_textbook_huffman_when_limit_is_loose(oracle, seed):
     assert abs(_kraft(lens) - 1.0) < 1e-12          # an optimal code is complete
 
 
+@pytest.mark.parametrize("seed", range(36))
+@pytest.mark.parametrize("lmax", [5, 6])
+def test_code_lengths_equal_package_merge_cost_16_symbols(oracle, seed, lmax):
+    # The shipped configuration: a full 16-symbol palette under a binding
+    # length limit (5 is the format's; 6 too).  The optimal total cost is
+    # unique even where the lengths are not, so the oracle's cost must equal
+    # package-merge's, and its lengths must form a valid prefix code.
+    rng = np.random.default_rng(7000 + seed)
+    freq = _skewed_histogram(rng)
+    lens = oracle.code_lengths(freq, lmax)
+    ref = _package_merge_lengths(freq, lmax)
+    assert max(ref) <= lmax and _kraft(ref) <= 1.0
+    assert max(lens) <= lmax and _kraft(lens) <= 1.0 and min(lens) >= 1
+    assert _cost(freq, lens) == _cost(freq, ref)
+
+
+def test_package_merge_agrees_with_brute_force():
+    # the test-side package-merge itself, against enumeration on tiny alphabets
+    for seed in range(30):
+        rng = np.random.default_rng(9000 + seed)
+        m = int(rng.integers(2, 7))
+        lmax = int(rng.integers(max(1, math.ceil(math.log2(m))), 6))
+        freq = [int(v) for v in rng.integers(1, 60, m)]
+        assert _cost(freq, _package_merge_lengths(freq, lmax)) == _brute_force_min_cost(freq, lmax)
+
+
 def test_mean_length_within_one_bit_of_entropy(oracle):
     # Textbook bound H <= L < H + 1 on the symbol distribution of the coded
-    # groups of a N(0, 0.02) matrix (the blog: ~2.6 bits of entropy).
+    # groups of a N(0, 0.02) matrix (the blog: ~2.6 bits of entropy), at the
+    # code-length limit the format ships (oracle.LMAX).  The limit binds here
+    # (an unlimited code would be shorter), and the bound still holds.
+    assert oracle.LMAX == 5
     w = wl.normal_weights(512, 1024, 0.02, seed=0)
     pal = oracle.palette(oracle.histogram(w))
     flags = oracle.escape_flags(w, pal).astype(bool)
     e = ((w.astype(np.uint32) >> 7) & 0xFF).reshape(-1, 64)[~flags]
     freq = np.array([(e == v).sum() for v in pal], np.float64)
-    lens = oracle.code_lengths(freq.astype(np.uint64), 6)
+    lens = oracle.code_lengths(freq.astype(np.uint64), oracle.LMAX)
     p = freq / freq.sum()
     H = -(p[p > 0] * np.log2(p[p > 0])).sum()
     L = (p * np.array(lens)).sum()
     assert H <= L < H + 1
     assert 2.4 < H < 2.8
+    assert _cost(freq.astype(np.int64), lens) == _cost(freq.astype(np.int64),
+                                                       _package_merge_lengths(freq.astype(np.int64), oracle.LMAX))
+    assert _cost(freq.astype(np.int64), lens) > _huffman_cost([int(v) for v in freq])   # the limit binds
 
 
 # ---------------------------------------------------------------- canonical codes

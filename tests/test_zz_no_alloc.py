@@ -36,11 +36,16 @@ def _call(uw, desc, blob_dev, xd, yd):
     return status
 
 
-@pytest.mark.parametrize("rows,cols,batch", [(1024, 1024, 1), (4096, 14336, 1), (300, 640, 5)])
+# (64, 4096, 4): two row blocks, so the default row kernel splits K and the
+# second call reuses arrival counters and partial sums the first one left;
+# (1024, 1024, 16): the tensor-core kernel.
+@pytest.mark.parametrize("rows,cols,batch", [(1024, 1024, 1), (4096, 14336, 1), (300, 640, 5), (64, 4096, 4),
+                                             (1024, 1024, 16)])
 def test_noalloc_matches_workspace_entry_point_twice(g, uw, oracle, rows, cols, batch):
     w = wl.normal_weights(rows, cols, 0.02, seed=rows)
     x = wl.activations(batch, cols, seed=rows)
     c = g.Compressed(w)
+    assert uw.workspace_size(c.desc, batch) <= (1 << 20)
     xd = g.dev_bits(x)
     expected = c.matmul(xd)                      # uw_matmul with a caller workspace, default plan
     y_ref, absum = oracle.matmul_f64(x, w)
