@@ -10,17 +10,23 @@
 //     exclusive warp prefix sum (shuffles); ballot + popc give each escaped
 //     group its rank among the tile's escaped groups;
 //   * read as little-endian 32-bit words, stream bit i is bit i%32 of word
-//     i/32, so a funnel shift right brings the next bits to the bottom;
+//     i/32; a lane keeps two consecutive words as one 64-bit window and a
+//     64-bit shift right brings its next bits to the bottom;
 //   * every step looks up a 10-bit window in a 1024-entry table that decodes
 //     two codes at once (codes are at most 5 bits).  An entry holds both
 //     exponents already in BF16 position (bits 14..7 and 30..23) and the bits
-//     the two codes take (bits 3..0).  The funnel shift starts kShift bits
-//     early so that the window arrives pre-scaled: by 4 (kShift = 2) to index
-//     one shared table, or by 128 (kShift = 7) to index 32 lane-private
+//     the two codes take (bits 3..0).  The entry's address is the window
+//     times a stride plus a base, one integer multiply-add (which runs on the
+//     FMA pipe, leaving the half-rate ALU pipe to the shifts and masks):
+//     stride 4 indexes one shared table, stride 128 indexes 32 lane-private
 //     copies of it, copy l holding entry w at word 32*w + l.  Lane l then
 //     always reads bank l, so a lookup is a single shared-memory wavefront
 //     whatever the 32 windows are (one shared table costs about four: the
 //     windows are random);
+//   * two codes take at most 10 bits, so three steps from a bit offset below
+//     32 stay inside the 64-bit window; the window moves on by a word (a
+//     predicated refill from the word already loaded after it) only after
+//     every third step, not after every step;
 //   * the exponent pair is merged with two raw sign+mantissa bytes by one
 //     byte permute (sign-replicating) and one three-input logic op, giving
 //     two BF16 weights in one 32-bit register (the blog's reconstruction:
@@ -86,9 +92,7 @@ constexpr uint32_t kMaxTileData = 2048;
 constexpr uint32_t kTileSlack = 64;
 constexpr int kCommonSmemBytes = kLutEntries * 4 + kZeroWords * 4 + kPrefixEntries * 2;
 
-// Shared memory common to every decoding CTA.  The tile buffers must come
-// after it: a lane whose codes start on a word boundary begins reading one
-// word before its buffer.
+// Shared memory common to every decoding CTA.
 struct DecodeShared {
     uint32_t *lut;       // [1024] pair table (or, when built private, 32 copies elsewhere)
     uint32_t *zero;      // [32]   zero bytes: the stream of lanes without codes
@@ -161,7 +165,7 @@ __device__ __forceinline__ void build_tables_palette_index(const DecodeShared &s
 // Second half of a private-table build: after build_tables and a
 // __syncthreads(), copy the pair table into 32 lane-private copies at shared
 // address `priv` (kPrivateLutBytes, 16-byte aligned; entry w of copy l at
-// word 32*w + l) for decode_pair<kShiftPrivate>.  Must be followed by
+// word 32*w + l) for decode_pair<kStridePrivate>.  Must be followed by
 // __syncthreads() before use.
 __device__ __forceinline__ void replicate_private(const DecodeShared &s, uint32_t priv) {
     for (int i = threadIdx.x; i < kLutEntries * 8; i += blockDim.x) {
@@ -170,8 +174,8 @@ __device__ __forceinline__ void replicate_private(const DecodeShared &s, uint32_
     }
 }
 
-constexpr int kShiftShared = 2;   // window x 4: byte offset into one table
-constexpr int kShiftPrivate = 7;  // window x 128: byte offset of the entry's row of 32 copies
+constexpr int kStrideShared = 4;    // bytes between entries of one table
+constexpr int kStridePrivate = 128; // bytes between rows of 32 lane-private copies
 
 // PTX prmt in its generic mode: a selector nibble with bit 3 set fills the
 // target byte with the sign bit of the selected byte.
@@ -376,26 +380,38 @@ __device__ __forceinline__ void tile_fetch(const BlobView &v, const TileLoc &L, 
 }
 
 // Per-tile, per-lane decode state.  Addresses are 32-bit shared addresses.
-// With P the shared-memory bit address of the next code bit and lo the word
-// at byte address A, the low five bits of c are P - 8A - kShift, P - 8A in
-// [kShift, kShift + 32): the funnel shift by c puts the next 10 stream bits
-// at bits kShift .. kShift+9.  c only grows; bit 5 flips whenever the window
-// moves past a word.
+// The lane's next code bit is bit c of the 64-bit window {hi:lo}, where lo
+// is the word at wp - 12 and hi the word after it; nx (the word at wp - 4)
+// is already loaded.  c is below 32 at the start of every round of three
+// steps.  The bit address of the next code bit is 8 * wp + c - 96 whatever
+// the refills did.
 struct LaneStream {
-    uint32_t lo, hi, nx;   // current, next and (already loaded) following stream word
-    uint32_t c;            // see above; low 7 bits exact
+    uint32_t lo, hi, nx;   // window words and the (already loaded) following word
+    uint32_t c;            // bit offset of the next code bit in {hi:lo}
     uint32_t wp;           // address of the next word to load
-    uint32_t expect;       // 8 * wp + (c & 31) after the lane's last code, + 0..7; 0: unchecked
+    uint32_t expect;       // 8 * wp + c after the lane's last code, + 0..7; 0: unchecked
 };
+
+// Set up a lane's stream at byte offset `off` of the tile buffer at `cbuf`
+// (coded lanes), or at the zero stream.  The lane's group has g code bytes.
+__device__ __forceinline__ void stream_setup(const DecodeShared &s, bool coded, uint32_t cbuf, uint32_t off,
+                                             uint32_t g, LaneStream &ls) {
+    const uint32_t w0 = coded ? cbuf + (off & ~3u) : smem_addr(s.zero);
+    const uint32_t c0 = coded ? 8u * (off & 3u) : 0u;
+    ls.lo = lds32(w0);
+    ls.hi = lds32(w0 + 4);
+    ls.nx = lds32(w0 + 8);
+    ls.wp = w0 + 12;
+    ls.c = c0;
+    ls.expect = coded ? 8u * ls.wp + c0 + 8u * g : 0u;
+}
 
 // Wait for the tile's codes, validate, and set up every lane's stream.
 // Returns the mask of lanes whose group is escaped (0 for a bad tile, whose
 // lanes all decode the zero stream; the error is recorded in *status).
 // tile_begin for data already in shared memory (nothing to wait for).
-template <int kShift = kShiftShared>
 __device__ __forceinline__ uint32_t tile_begin_ready(const DecodeShared &s, const TileMeta &m, int R, uint32_t cbuf,
                                                      LaneStream &ls, uint32_t *status) {
-    static_assert(kShift >= 0 && kShift <= 8, "a stream starting at byte 1..3 of a word must have P - 8A >= kShift");
     const int lane = threadIdx.x & 31;
     const bool valid = lane < R;
     const uint32_t n16 = m.pk & 0xFFu, nesc = (m.pk >> 8) & 0xFFu;
@@ -414,17 +430,7 @@ __device__ __forceinline__ uint32_t tile_begin_ready(const DecodeShared &s, cons
     const bool bad = over || uint32_t(__popc(esc_mask)) != nesc;
     if (bad && lane == 0)
         atomicOr(status, over ? kStatusBadTile : kStatusBadEscape);
-    const bool coded = !bad && g != 0;
-    // a stream starting on a word boundary begins one word early (P - 8A = 32)
-    const uint32_t sub = (off & 3u) ? 0u : 4u;
-    const uint32_t w0 = coded ? cbuf + (off & ~3u) - sub : smem_addr(s.zero);
-    const uint32_t c0 = (8u * (off & 3u) - uint32_t(kShift)) & 31u;
-    ls.lo = lds32(w0);
-    ls.hi = lds32(w0 + 4);
-    ls.nx = lds32(w0 + 8);
-    ls.wp = w0 + 12;
-    ls.c = c0;
-    ls.expect = coded ? 8u * ls.wp + c0 + 8u * g : 0u;
+    stream_setup(s, !bad && g != 0, cbuf, off, g, ls);
     return bad ? 0u : esc_mask;
 }
 
@@ -433,7 +439,6 @@ __device__ __forceinline__ uint32_t tile_begin_ready(const DecodeShared &s, cons
 // (a tile's sum is at most 32 * 255 < 2^16, so the halves never carry into
 // each other), the source lane's existence taken from the shuffle's own
 // predicate.  Returns both escape masks.
-template <int kShift = kShiftShared>
 __device__ __forceinline__ void pair_begin_ready(const DecodeShared &s, uint32_t gA, uint32_t gB, uint32_t pkA,
                                                  uint32_t pkB, int R, int RB, uint32_t cbA, uint32_t cbB,
                                                  LaneStream &la, LaneStream &lb, uint32_t *status, uint32_t &emA,
@@ -460,28 +465,18 @@ __device__ __forceinline__ void pair_begin_ready(const DecodeShared &s, uint32_t
         const bool bad = over || uint32_t(__popc(esc_mask)) != nesc;
         if (bad && lane == 0)
             atomicOr(status, over ? kStatusBadTile : kStatusBadEscape);
-        const bool coded = !bad && g != 0;
-        const uint32_t sub = (off & 3u) ? 0u : 4u;  // a stream starting on a word boundary begins one word early
-        const uint32_t w0 = coded ? cbuf + (off & ~3u) - sub : smem_addr(s.zero);
-        const uint32_t c0 = (8u * (off & 3u) - uint32_t(kShift)) & 31u;
-        ls.lo = lds32(w0);
-        ls.hi = lds32(w0 + 4);
-        ls.nx = lds32(w0 + 8);
-        ls.wp = w0 + 12;
-        ls.c = c0;
-        ls.expect = coded ? 8u * ls.wp + c0 + 8u * g : 0u;
+        stream_setup(s, !bad && g != 0, cbuf, off, g, ls);
         return bad ? 0u : esc_mask;
     };
     emA = setup(ga, off2 & 0xFFFFu, tot2 & 0xFFFFu, mA, pkA, cbA, la);
     emB = setup(gb, off2 >> 16, tot2 >> 16, mB, pkB, cbB, lb);
 }
 
-template <int kShift = kShiftShared>
 __device__ __forceinline__ uint32_t tile_begin(const DecodeShared &s, const TileMeta &m, int R, uint32_t cbuf,
                                                LaneStream &ls, uint32_t *status) {
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
-    return tile_begin_ready<kShift>(s, m, R, cbuf, ls, status);
+    return tile_begin_ready(s, m, R, cbuf, ls, status);
 }
 
 // Shared address of a fetched tile's raw escape bytes (after its codes).
@@ -504,47 +499,99 @@ __device__ __forceinline__ void escape_read(uint32_t ebase, uint32_t esc_mask, u
 // One step of the lane's stream: look up the next two codes and advance past
 // them; returns the table entry (both exponents in BF16 position, or both
 // palette indices, and the bits taken).  `lut` is the shared address of the
-// pair table (kShiftShared), or of the lane's column of the private copies,
-// i.e. their base + 4 * lane (kShiftPrivate).
-template <int kShift = kShiftShared>
-__device__ __forceinline__ uint32_t decode_entry(LaneStream &ls, uint32_t lut) {
-    // window << kShift = funnel(lo, hi) >> c, masked; entry = table[window];
-    // c += entry (its bits above 6 only add junk above the exact low 7);
-    // when bit 5 of c flips the window has moved into the next word: shift
-    // the words and load the one after, predicated rather than branched.  The
-    // loaded word is needed only at the following crossing, so the load is
-    // off the step-to-step dependency chain.
+// pair table (kStrideShared), or of the lane's column of the private copies,
+// i.e. their base + 4 * lane (kStridePrivate).  `I` is the step's index
+// within the tile (a compile-time constant once the caller's 32-step loop is
+// unrolled): after steps 2, 5, ..., 29 the window moves on by a word if the
+// last three steps took it past one.
+template <int kStride = kStrideShared>
+__device__ __forceinline__ uint32_t decode_entry(LaneStream &ls, uint32_t lut, int I) {
+    // window = ({hi:lo} >> c) & 1023; entry = table[window]; c += bits taken.
+    // The refill's load is needed only three steps later, so it is off the
+    // step-to-step dependency chain.
     uint32_t ent;
     asm volatile(
         "{\n\t"
-        ".reg .b32 win, addr, c2, t;\n\t"
-        ".reg .pred p;\n\t"
-        "shf.r.wrap.b32 win, %1, %2, %4;\n\t"
-        "and.b32 win, win, %7;\n\t"
-        "add.u32 addr, win, %6;\n\t"
-        "ld.shared.u32 %0, [addr];\n\t"
-        "add.u32 c2, %0, %4;\n\t"
-        "xor.b32 t, c2, %4;\n\t"
-        "and.b32 t, t, 32;\n\t"
-        "setp.ne.u32 p, t, 0;\n\t"
-        "@p mov.b32 %1, %2;\n\t"
-        "@p mov.b32 %2, %3;\n\t"
-        "@p ld.shared.u32 %3, [%5];\n\t"
-        "@p add.u32 %5, %5, 4;\n\t"
-        "mov.b32 %4, c2;\n\t"
+        ".reg .b64 b;\n\t"
+        ".reg .b32 w, t;\n\t"
+        "mov.b64 b, {%1, %2};\n\t"
+        "shr.b64 b, b, %3;\n\t"
+        "cvt.u32.u64 w, b;\n\t"
+        "and.b32 w, w, 1023;\n\t"
+        "mad.lo.u32 w, w, %5, %4;\n\t"
+        "ld.shared.u32 %0, [w];\n\t"
+        "and.b32 t, %0, 15;\n\t"
+        "add.u32 %3, %3, t;\n\t"
         "}"
-        : "=r"(ent), "+r"(ls.lo), "+r"(ls.hi), "+r"(ls.nx), "+r"(ls.c), "+r"(ls.wp)
-        : "r"(lut), "n"((kLutEntries - 1) << kShift)
+        : "=r"(ent), "+r"(ls.lo), "+r"(ls.hi), "+r"(ls.c)
+        : "r"(lut), "n"(kStride)
         : "memory");
+    if ((I % 3) == 2 && I < 30) {
+        asm volatile(
+            "{\n\t"
+            ".reg .pred p;\n\t"
+            "setp.gt.u32 p, %3, 31;\n\t"
+            "@p mov.b32 %0, %1;\n\t"
+            "@p mov.b32 %1, %2;\n\t"
+            "@p ld.shared.u32 %2, [%4];\n\t"
+            "@p add.u32 %4, %4, 4;\n\t"
+            "@p sub.u32 %3, %3, 32;\n\t"
+            "}"
+            : "+r"(ls.lo), "+r"(ls.hi), "+r"(ls.nx), "+r"(ls.c), "+r"(ls.wp)
+            :
+            : "memory");
+    }
+    return ent;
+}
+
+// decode_entry with the entry stride in a register (a lane may walk its own
+// short list of entries with stride 4 instead of the table; see the batch-1
+// GEMV's escaped groups), and the bit counter advanced by a multiply-add
+// with `one` (1 held in a register), which runs on the FMA pipe instead of
+// the half-rate ALU pipe that the shift and the masks already load.
+__device__ __forceinline__ uint32_t decode_entry_rs(LaneStream &ls, uint32_t lut, uint32_t stride, uint32_t one,
+                                                    int I) {
+    uint32_t ent;
+    asm volatile(
+        "{\n\t"
+        ".reg .b64 b;\n\t"
+        ".reg .b32 w, t;\n\t"
+        "mov.b64 b, {%1, %2};\n\t"
+        "shr.b64 b, b, %3;\n\t"
+        "cvt.u32.u64 w, b;\n\t"
+        "and.b32 w, w, 1023;\n\t"
+        "mad.lo.u32 w, w, %5, %4;\n\t"
+        "ld.shared.u32 %0, [w];\n\t"
+        "and.b32 t, %0, 15;\n\t"
+        "mad.lo.u32 %3, t, %6, %3;\n\t"
+        "}"
+        : "=r"(ent), "+r"(ls.lo), "+r"(ls.hi), "+r"(ls.c)
+        : "r"(lut), "r"(stride), "r"(one)
+        : "memory");
+    if ((I % 3) == 2 && I < 30) {
+        asm volatile(
+            "{\n\t"
+            ".reg .pred p;\n\t"
+            "setp.gt.u32 p, %3, 31;\n\t"
+            "@p mov.b32 %0, %1;\n\t"
+            "@p mov.b32 %1, %2;\n\t"
+            "@p ld.shared.u32 %2, [%4];\n\t"
+            "@p add.u32 %4, %4, 4;\n\t"
+            "@p sub.u32 %3, %3, 32;\n\t"
+            "}"
+            : "+r"(ls.lo), "+r"(ls.hi), "+r"(ls.nx), "+r"(ls.c), "+r"(ls.wp)
+            :
+            : "memory");
+    }
     return ent;
 }
 
 // One step: decode the exponents of weights 2i, 2i+1 and merge them with the
 // sign+mantissa bytes.  `sm4` holds the bytes of weights 4*(i/2)..+3.  `I`
 // is a compile-time constant once the caller's 32-step loop is unrolled.
-template <int kShift = kShiftShared>
+template <int kStride = kStrideShared>
 __device__ __forceinline__ uint32_t decode_pair(LaneStream &ls, uint32_t lut, int I, uint32_t sm4) {
-    const uint32_t ent = decode_entry<kShift>(ls, lut);
+    const uint32_t ent = decode_entry<kStride>(ls, lut, I);
     // sign-replicate byte permute: bytes (b0, sign(b0), b1, sign(b1)) for the
     // even pair of the word, (b2, sign(b2), b3, sign(b3)) for the odd one
     const uint32_t y = prmt(sm4, 0u, (I & 1) ? 0xB3A2u : 0x9180u);
@@ -554,7 +601,7 @@ __device__ __forceinline__ uint32_t decode_pair(LaneStream &ls, uint32_t lut, in
 // After the 32 steps: every lane with codes must have used its byte length
 // exactly (its last code ends in the length's final byte).
 __device__ __forceinline__ void tile_check(const LaneStream &ls, uint32_t *status) {
-    const uint32_t pos = 8u * ls.wp + (ls.c & 31u);
+    const uint32_t pos = 8u * ls.wp + ls.c;
     if (ls.expect != 0u && ls.expect - pos >= 8u)
         atomicOr(status, uint32_t(kStatusBadCode));
 }
@@ -562,7 +609,7 @@ __device__ __forceinline__ void tile_check(const LaneStream &ls, uint32_t *statu
 // The same check folded into a per-lane flag (nonzero: some group was bad);
 // report it once with tile_check_flush.
 __device__ __forceinline__ uint32_t tile_check_bits(const LaneStream &ls) {
-    const uint32_t pos = 8u * ls.wp + (ls.c & 31u);
+    const uint32_t pos = 8u * ls.wp + ls.c;
     return (ls.expect != 0u) & (ls.expect - pos >= 8u);
 }
 

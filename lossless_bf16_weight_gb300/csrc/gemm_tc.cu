@@ -112,7 +112,7 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
     constexpr bool kP4 = kSrc == kSrcPalette4;
     constexpr bool kExp = kSrc == kSrcExponent;
     static_assert(!kPrivate || (kSrc == kSrcHuffman && !kSmStaged), "private tables: Huffman codes-only stages");
-    constexpr int kShift = kPrivate ? kShiftPrivate : kShiftShared;
+    constexpr int kStride = kPrivate ? kStridePrivate : kStrideShared;
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[2 * kTcMaxStages + 1];
     __shared__ __align__(8) uint64_t pbars[P * kPairStages];
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
                     LaneStream la, lb;
                     const uint32_t cA = st + 64u, cB = cA + 16u * m.n16A;
                     uint32_t emA, emB;
-                    pair_begin_ready<kShift>(ds, gA, gB, m.pkA, m.pkB, R, hasB ? R : 0, cA, cB, la, lb, p.status, emA,
+                    pair_begin_ready(ds, gA, gB, m.pkA, m.pkB, R, hasB ? R : 0, cA, cB, la, lb, p.status, emA,
                                              emB);
                     const uint32_t ebA = cA + 16u * (m.n16A + m.n16B), ebB = ebA + 64u * m.nescA;
                     // sign+mantissa bytes straight from L2 (prefetched there with the codes), one
@@ -296,8 +296,8 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
                                 nB = __ldg(reinterpret_cast<const uint4 *>(kgN1 + 1 < kg_hi ? a + 64u * Rn : a));
                             }
                         }
-                        qA[I] = decode_pair<kShift>(la, lut, I, word4(sA, (I >> 1) & 3));
-                        qB[I] = decode_pair<kShift>(lb, lut, I, word4(sB, (I >> 1) & 3));
+                        qA[I] = decode_pair<kStride>(la, lut, I, word4(sA, (I >> 1) & 3));
+                        qB[I] = decode_pair<kStride>(lb, lut, I, word4(sB, (I >> 1) & 3));
                         if ((I & 7) == 7) {
                             sA = nA;
                             sB = nB;

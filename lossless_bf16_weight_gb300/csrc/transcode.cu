@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kTcdWarps * 32, 1)
         const int R = tile_rows32(v, cur.rb);
         const uint32_t cbuf = cbuf0 + (i & 1u) * tbuf;
         LaneStream ls;
-        const uint32_t esc_mask = tile_begin<kShiftPrivate>(ds, meta, R, cbuf, ls, status);
+        const uint32_t esc_mask = tile_begin(ds, meta, R, cbuf, ls, status);
         const uint32_t ebase = escape_base(meta, cbuf);  // before meta is reused for the next tile
         TileWalk n2 = nxt;
         if (nxt.t < ntiles) {
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kTcdWarps * 32, 1)
                 wd[k] = 0u;
 #pragma unroll
             for (int I = 0; I < 32; I++) {
-                const uint32_t ent = decode_entry<kShiftPrivate>(ls, lut);
+                const uint32_t ent = decode_entry<kStridePrivate>(ls, lut, I);
                 const uint32_t byte = ((ent >> 7) & 15u) | ((ent >> 19) & 0xF0u);  // weights 2I (low), 2I+1
                 wd[I >> 2] |= byte << (8 * (I & 3));
             }
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kTcdWarps * 32, 1)
                 wd[k] = 0u;
 #pragma unroll
             for (int I = 0; I < 32; I++) {
-                const uint32_t ent = decode_entry<kShiftPrivate>(ls, lut);
+                const uint32_t ent = decode_entry<kStridePrivate>(ls, lut, I);
                 const uint32_t two = ((ent >> 7) & 0xFFu) | ((ent >> 15) & 0xFF00u);  // exponents of 2I, 2I+1
                 wd[I >> 1] |= two << (16 * (I & 1));
             }
