@@ -44,8 +44,6 @@ cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 //          follow from the matrix and the SM count
 //   27..38 tensor-core CTAs (gemm_tc.cu): producer groups G (1, 2, 3) x K
 //          splits (1, 2, 4, 8, capped at the number of 64-column groups)
-//   39     half-row-block CTAs, batch 1 only (gemv_kg.cu): two 8-warp CTAs
-//          per SM, each row block's two halves added in order
 constexpr int kWarpChoices[3] = {4, 8, 16};
 constexpr int kSplitChoices = 5;  // 1, 2, 4, 8, 16
 constexpr int kRowVariants = 3 * kSplitChoices;
@@ -55,11 +53,10 @@ constexpr int kTcGroups[3] = {1, 2, 3};
 constexpr int kTcSplitChoices = 4;  // 1, 2, 4, 8
 constexpr int kTcVariants = 3 * kTcSplitChoices;
 constexpr int kTcFirst = kRowVariants + kColVariants;
-constexpr int kHalfVariant = kTcFirst + kTcVariants;
-constexpr int kGemvVariants = kHalfVariant + 1;
+constexpr int kGemvVariants = kTcFirst + kTcVariants;
 constexpr int kMaxBatchChunk = 8;
 
-enum class Kind { kRow, kColumn, kTensor, kHalf };
+enum class Kind { kRow, kColumn, kTensor };
 
 struct GemvVariant {
     Kind kind;
@@ -73,8 +70,6 @@ GemvVariant gemv_variant(int v, int64_t rows, int64_t cols, uint32_t tbuf = kWor
     const int64_t gpr = cols / kGroup;
     if (v < kRowVariants)
         return {Kind::kRow, kWarpChoices[v % 3], 1 << (v / 3), 0};
-    if (v == kHalfVariant)
-        return {Kind::kHalf, 8, 2, 0};
     if (v >= kTcFirst) {
         const int i = v - kTcFirst;
         const int64_t splits = std::min<int64_t>(int64_t(1) << (i % kTcSplitChoices), gpr);
@@ -164,7 +159,7 @@ WsLayout layout_for(int64_t rows, int64_t cols, int64_t batch, int strategy, int
     WsLayout L;
     const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
     const GemvVariant gv = gemv_variant(variant, rows, cols);
-    const int bp = (gv.kind == Kind::kColumn || gv.kind == Kind::kHalf) ? 1 : pad_batch(batch);
+    const int bp = gv.kind == Kind::kColumn ? 1 : pad_batch(batch);
     const uint64_t partial_floats = gv.kind == Kind::kTensor
                                         ? uint64_t(gemm_tc_partial_floats(rows, batch, gv.splits))
                                         : uint64_t(nrb) * gv.splits * bp * 32;
@@ -189,7 +184,7 @@ struct ResolvedPlan {
 // Default variant of the palette-4 kernels: the column GEMV at batch 1, the
 // tensor cores otherwise (there is no palette-4 row kernel).
 int default_p4_variant(int64_t rows, int64_t cols, int64_t batch, int src) {
-    return batch == 1 ? kRowVariants + 2 : default_tc_variant(rows, cols, batch, src, 0);
+    return batch == 1 ? default_gemv_variant(rows, cols, 1) : default_tc_variant(rows, cols, batch, src, 0);
 }
 
 // tdata: the blob's tile data bytes (sizes the Huffman stages of the default).
@@ -242,11 +237,6 @@ uw_status run_gemv(GemvParams p, int variant, int src, cudaStream_t stream) {
         t.batch = p.batch;
         t.splits = gv.splits;
         return launch_gemm_tc(t, gv.warps, src, stream);
-    }
-    if (gv.kind == Kind::kHalf) {
-        if (p.batch != 1)
-            return UW_ERR_UNSUPPORTED;
-        return launch_gemv_half(p, src, stream);
     }
     if (gv.kind == Kind::kColumn) {
         if (p.batch != 1)
@@ -712,7 +702,7 @@ extern "C" const char *uw_variant_name(int32_t strategy, int32_t variant) {
         "col_w4x1", "col_w8x1", "col_w16x1", "col_w4x2", "col_w8x2", "col_w16x2",
         "col_w4x3", "col_w8x3", "col_w16x3", "col_w4x4", "col_w8x4", "col_w16x4",
         "tc_g1s1", "tc_g1s2", "tc_g1s4", "tc_g1s8", "tc_g2s1", "tc_g2s2", "tc_g2s4", "tc_g2s8",
-        "tc_g3s1", "tc_g3s2", "tc_g3s4", "tc_g3s8", "half_w8"};
+        "tc_g3s1", "tc_g3s2", "tc_g3s4", "tc_g3s8"};
     if (uw_variant_count(strategy) == 0 || variant < 0 || variant >= kGemvVariants)
         return nullptr;
     return names[variant];

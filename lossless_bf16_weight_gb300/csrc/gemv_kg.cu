@@ -364,201 +364,209 @@ __device__ __forceinline__ void expand_escapes(uint32_t n, uint32_t eb, uint32_t
     }
 }
 
-// How a CTA's work is cut into segments.  Whole row blocks: segment s is
-// row block s and every warp owns the groups [kwo, kwe) of it.  Halves:
-// segment s is half s & 1 of row block s >> 1 (two CTAs share a row block;
-// see half_reduce), and a warp owns [kwo, kwe) of that half's hg groups.
-struct Segs {
-    uint32_t seg0, seg1;  // the CTA's segments
-    uint32_t hg;          // groups per half (0: whole row blocks)
-    uint32_t kwo, kwe;    // the warp's groups within a segment
-    uint32_t ppr;         // the warp's pairs per segment
-    __device__ __forceinline__ uint32_t rb(uint32_t seg) const { return hg ? seg >> 1 : seg; }
-    __device__ __forceinline__ uint32_t kbase(uint32_t seg) const { return hg ? (seg & 1u) * hg : 0u; }
+// Per-warp constants of the batch-1 private-table GEMV.
+struct PrivCtx {
+    uint32_t lut;    // the lane's column of the private table copies
+    uint32_t zero;   // zero stream
+    uint32_t cnt;    // counting stream (escaped groups)
+    uint32_t slots;  // the warp's escape slots
+    uint32_t below;  // lanes below this one
+    uint32_t one;    // 1, held in a register
 };
 
-// The warp's pairs in order, segment by segment.
-struct SegCursor {
-    uint32_t seg, kgA, kend;
-    __device__ __forceinline__ void start(const Segs &g) {
-        seg = g.seg0;
-        kgA = g.kbase(seg) + g.kwo;
-        kend = g.kbase(seg) + g.kwe;
-    }
-    __device__ __forceinline__ void next(const Segs &g) {
-        kgA += 2;
-        if (kgA >= kend) {
-            seg++;
-            kgA = g.kbase(seg) + g.kwo;
-            kend = g.kbase(seg) + g.kwe;
-        }
-    }
-};
-
-// Pair records (the layout pair_issue_rec reads) for pairs base ..
-// base + kRecRound - 1 of the warp, lane i making pair base + i: the tile
-// tables' loads, then (seg_recs_store) the checked sizes.
-__device__ __forceinline__ void seg_pair(const Segs &g, uint32_t j, uint32_t &rb, uint32_t &kgA, bool &hasB) {
-    const uint32_t seg = g.seg0 + j / g.ppr;
-    const uint32_t kb = g.kbase(seg);
-    rb = g.rb(seg);
-    kgA = kb + g.kwo + 2u * (j % g.ppr);
-    hasB = kgA + 1 < kb + g.kwe;
-}
-
-__device__ __forceinline__ RecLoad seg_recs_load(const BlobView &v, const Segs &g, uint32_t npairs, uint32_t base) {
-    const uint32_t lane = threadIdx.x & 31, j = base + lane;
-    RecLoad r{};
-    if (lane < uint32_t(kRecRound) && j < npairs) {
-        uint32_t rb, kgA;
-        bool hasB;
-        seg_pair(g, j, rb, kgA, hasB);
-        const uint32_t t = rb * v.gpr + kgA;
-        auto at = [&](const uint32_t *tab, uint32_t k) { return __ldg(tab + (k < v.ntiles ? k : v.ntiles)); };
-        r.c0 = at(v.tcode, t);
-        r.c1 = at(v.tcode, t + 1);
-        r.c2 = at(v.tcode, t + (hasB ? 2u : 1u));
-        r.e0 = at(v.tesc, t);
-        r.e1 = at(v.tesc, t + 1);
-        r.e2 = at(v.tesc, t + (hasB ? 2u : 1u));
-    }
-    return r;
-}
-
-__device__ __forceinline__ void seg_recs_store(const BlobView &v, uint32_t ring, const Segs &g, uint32_t npairs,
-                                               uint32_t base, const RecLoad &r) {
-    const uint32_t lane = threadIdx.x & 31, j = base + lane;
-    if (lane < uint32_t(kRecRound) && j < npairs) {
-        uint32_t rb, kgA;
-        bool hasB;
-        seg_pair(g, j, rb, kgA, hasB);
-        const uint32_t t = rb * v.gpr + kgA;
-        const bool full = rb < v.nfull;
-        const uint32_t R = full ? uint32_t(kTileRows) : v.tail_rows;
-        const uint32_t n16A = r.c1 - r.c0, n16B = r.c2 - r.c1, nescA = r.e1 - r.e0, nescB = r.e2 - r.e1;
-        const uint32_t lim16 = uint32_t(kMaxTileCodeBytes / 16);
-        const bool bad = n16A > lim16 || n16B > lim16 || nescA > R || nescB > R || n16A * 16u + nescA * 64u > v.tdata ||
-                         n16B * 16u + nescB * 64u > v.tdata || r.c2 > v.code16 || r.e2 > v.n_esc32;
-        const uint32_t ntile = hasB ? 2u : 1u;
-        const uint64_t q0 = uint64_t(t) * kTileRows - (full ? 0u : (kTileRows - R) * kgA);
-        const uint32_t bytes = bad ? 0u : ((r.c2 - r.c0) * 16u) | (((r.e2 - r.e0) * 64u) << 16);
-        const uint32_t sizes = (bad ? 0u : (n16A | (n16B << 8) | (nescA << 16))) | ((full ? ntile : 0u) << 22) |
-                               ((R * ntile) << 24);
-        const uint32_t pkA = bad ? (1u << 16) : (n16A | (nescA << 8));
-        const uint32_t pkB = !hasB ? 0u : bad ? (1u << 16) : (n16B | (nescB << 8));
-        const uint32_t a = ring + kRecBytes * (j % uint32_t(kRecRing));
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" :: "r"(a), "r"(r.c0), "r"(bytes), "r"(r.e0),
-                     "r"(sizes) : "memory");
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" :: "r"(a + 16u), "r"(pkA), "r"(pkB),
-                     "r"(uint32_t(q0)), "r"(uint32_t(q0 >> 32)) : "memory");
-    }
-    __syncwarp();
-}
-
-// The CTA's segments, and the calling warp's share of each.
-template <int W>
-__device__ __forceinline__ Segs cta_segs(const BlobView &v, uint32_t gpr, uint32_t nrb, bool halves, int rb_per_cta) {
-    Segs g;
-    const int warp = threadIdx.x >> 5;
-    if (halves) {
-        const uint32_t units = 2u * nrb;
-        g.seg0 = uint32_t(uint64_t(units) * blockIdx.x / gridDim.x);
-        g.seg1 = uint32_t(uint64_t(units) * (blockIdx.x + 1) / gridDim.x);
-        g.hg = gpr / 2;
-        warp_cols(g.hg, warp, W, g.kwo, g.kwe);
+// One pair (tiles A = (rb, kgA), B = (rb, kgA + 1) when hasB) staged at `st`:
+// returns the two tiles' partials pA = acc_even + acc_odd of A, pB of B.
+// kFull: a full row block (32 rows: constant strides, glen in the stage).
+// sm: the pair's first sign+mantissa byte; chunk 0 of each tile arrives in
+// c0A / c0B and chunk 0 of the next pair (at sm_nxt, Rn rows, B when nhasB) leaves
+// in them.
+template <bool kFull>
+__device__ __forceinline__ void priv_pair(const GemvParams &p, const PrivCtx &k, uint32_t st, uint32_t pkA,
+                                          uint32_t pkB, uint64_t q0, uint32_t Rr, bool hasB, const uint8_t *sm,
+                                          const uint4 *xA, bool more, const uint8_t *sm_nxt, uint32_t Rn, bool nhasB,
+                                          uint4 &c0A, uint4 &c0B, uint32_t &bad, float &pA, float &pB) {
+    const BlobView &v = p.v;
+    const int lane = threadIdx.x & 31;
+    const uint32_t R = kFull ? uint32_t(kTileRows) : Rr;
+    const uint32_t n16A = pkA & 0xFFu, n16B = pkB & 0xFFu;
+    const uint32_t nescA = (pkA >> 8) & 0xFFu, nescB = (pkB >> 8) & 0xFFu;
+    uint32_t gA, gB;
+    if (kFull) {
+        gA = lds_u8(st + uint32_t(lane));
+        gB = lds_u8(st + 32u + uint32_t(lane));
     } else {
-        g.seg0 = blockIdx.x * uint32_t(rb_per_cta);
-        g.seg1 = g.seg0 + uint32_t(rb_per_cta) < nrb ? g.seg0 + uint32_t(rb_per_cta) : nrb;
-        g.hg = 0;
-        warp_cols(gpr, warp, W, g.kwo, g.kwe);
+        const uint32_t l = uint32_t(lane) < R ? uint32_t(lane) : 0u;
+        gA = __ldg(v.glen + q0 + l);
+        gB = hasB ? __ldg(v.glen + q0 + R + l) : 0u;
     }
-    g.ppr = (g.kwe - g.kwo + 1) / 2;
-    return g;
-}
-
-// y for the CTA's half-row-block units.  Unit u's partial for row j is the
-// warp partials added in warp order; y = bf16(partial(half 0) + partial(half
-// 1)).  When both halves are in this CTA the warp of the second adds them;
-// otherwise each half's warp stores its partial in the workspace and the
-// second of the two CTAs to arrive (an atomic count per row block, reset to
-// zero after use) reads the other one and writes y.  Same order either way.
-template <int W>
-__device__ __forceinline__ void half_reduce(const GemvParams &p, const float *red, const Segs &g) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (uint32_t u = g.seg0 + uint32_t(warp); u < g.seg1; u += W) {
-        const uint32_t ul = u - g.seg0, rb = u >> 1, h = u & 1u;
-        float s = red[(ul * W) * 32 + lane];
+    // one warp prefix sum over both tiles' group lengths (16-bit halves)
+    const bool vA = kFull || uint32_t(lane) < R, vB = hasB && vA;
+    uint32_t ga = vA ? gA : 0u, gb = vB ? gB : 0u;
+    const uint32_t g2 = ga | (gb << 16);
+    uint32_t incl = g2;
 #pragma unroll
-        for (int w = 1; w < W; w++)
-            s += red[(ul * W + w) * 32 + lane];
-        const int64_t n = int64_t(rb) * kTileRows + lane;
-        if (h == 0u && u + 1 < g.seg1)
-            continue;  // the next unit's warp finishes this row block
-        float y;
-        if (h == 1u && u > g.seg0) {
-            float s0 = red[((ul - 1) * W) * 32 + lane];
-#pragma unroll
-            for (int w = 1; w < W; w++)
-                s0 += red[((ul - 1) * W + w) * 32 + lane];
-            y = s0 + s;
-        } else {
-            p.partial[size_t(u) * 32 + lane] = s;
-            __threadfence();
-            __syncwarp();
-            uint32_t old = 0;
-            if (lane == 0)
-                old = atomicAdd(p.counters + rb, 1u);
-            old = __shfl_sync(0xffffffffu, old, 0);
-            if (old == 0u)
-                continue;  // the other half's CTA finishes this row block
-            __threadfence();
-            const float o = __ldcg(p.partial + size_t(u ^ 1u) * 32 + lane);
-            y = h == 0u ? s + o : o + s;
-            if (lane == 0)
-                p.counters[rb] = 0u;
+    for (int d = 1; d < 32; d <<= 1)
+        asm("{\n\t.reg .b32 u;\n\t.reg .pred q;\n\t"
+            "shfl.sync.up.b32 u|q, %0, %1, 0, -1;\n\t"
+            "@q add.u32 %0, %0, u;\n\t}"
+            : "+r"(incl) : "r"(d));
+    const uint32_t off2 = incl - g2;
+    const uint32_t tot2 = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t emA = __ballot_sync(0xffffffffu, vA && ga == 0u);
+    uint32_t emB = __ballot_sync(0xffffffffu, vB && gb == 0u);
+    // A pair whose tables or group lengths do not add up (a device copy
+    // damaged after its header was checked) is flagged and decodes the zero
+    // stream in every lane, so no read leaves the stage.
+    if (((pkA | pkB) >> 16) != 0u || (tot2 & 0xFFFFu) > 16u * n16A || (tot2 >> 16) > 16u * n16B ||
+        uint32_t(__popc(emA)) != nescA || uint32_t(__popc(emB)) != nescB) {
+        if (lane == 0)
+            atomicOr(p.status, uint32_t(kStatusBadTile));
+        ga = 0u;
+        gb = 0u;
+        emA = 0u;
+        emB = 0u;
+    }
+    const uint32_t cA = st + 64u, cB = cA + 16u * n16A;
+    const uint32_t ebA = cB + 16u * n16B, ebB = ebA + 64u * nescA;
+    // escaped groups: slots 0.. for A's, then B's, at most kEscSlots
+    uint32_t wzA = k.zero, wzB = k.zero, lutA = k.lut, lutB = k.lut, sA_ = kStridePrivate, sB_ = kStridePrivate;
+    bool xa = false, xb = false;
+    if ((emA | emB) != 0u) {
+        const uint32_t pa = __popc(emA), pb = __popc(emB);
+        const uint32_t nA = pa < uint32_t(kEscSlots) ? pa : uint32_t(kEscSlots);
+        const uint32_t nB = pb < uint32_t(kEscSlots) - nA ? pb : uint32_t(kEscSlots) - nA;
+        expand_escapes(nA, ebA, k.slots, 0u);
+        expand_escapes(nB, ebB, k.slots, nA);
+        __syncwarp();
+        const uint32_t rA = __popc(emA & k.below), rB = nA + __popc(emB & k.below);
+        xa = (emA >> lane) & 1u;
+        xb = (emB >> lane) & 1u;
+        if (xa && rA < nA) {
+            wzA = k.cnt;
+            lutA = k.slots + kEscSlotBytes * rA;
+            sA_ = 4u;
+            xa = false;  // decoded in the main loop
         }
-        if (n < p.rows)
-            p.y[n] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+        if (xb && rB < nA + nB) {
+            wzB = k.cnt;
+            lutB = k.slots + kEscSlotBytes * rB;
+            sB_ = 4u;
+            xb = false;
+        }
     }
+    LaneStream la, lb;
+    {
+        const uint32_t offA = off2 & 0xFFFFu, offB = off2 >> 16;
+        const uint32_t wA = ga != 0u ? ((cA + offA) & ~3u) : wzA;
+        const uint32_t wB = gb != 0u ? ((cB + offB) & ~3u) : wzB;
+        la.lo = lds32(wA);
+        la.hi = lds32(wA + 4);
+        la.nx = lds32(wA + 8);
+        la.wp = wA + 12;
+        la.c = ga != 0u ? 8u * (offA & 3u) : 0u;
+        la.expect = ga != 0u ? 8u * (la.wp + ga) + la.c : 0u;
+        lb.lo = lds32(wB);
+        lb.hi = lds32(wB + 4);
+        lb.nx = lds32(wB + 8);
+        lb.wp = wB + 12;
+        lb.c = gb != 0u ? 8u * (offB & 3u) : 0u;
+        lb.expect = gb != 0u ? 8u * (lb.wp + gb) + lb.c : 0u;
+    }
+    const uint32_t stride = 16u * R;
+    const uint32_t lc = (kFull || uint32_t(lane) < R) ? uint32_t(lane) : 0u;
+    const uint8_t *gA_sm = sm + 16u * lc, *gB_sm = hasB ? gA_sm + 64u * R : gA_sm;
+    const uint4 *xB = xA + (hasB ? 8 : 0);
+    float aA0 = 0.f, aA1 = 0.f, aB0 = 0.f, aB1 = 0.f;
+    uint4 sA = c0A, sB = c0B, nA = sA, nB = sB;
+    uint4 x4A = __ldg(xA), x4B = __ldg(xB), nxA = x4A, nxB = x4B;
+#pragma unroll
+    for (int I = 0; I < 32; I++) {
+        if ((I & 7) == 0) {  // next chunk of sign+mantissa bytes
+            if (I < 24) {
+                nA = __ldg(reinterpret_cast<const uint4 *>(gA_sm + uint32_t((I >> 3) + 1) * stride));
+                nB = __ldg(reinterpret_cast<const uint4 *>(gB_sm + uint32_t((I >> 3) + 1) * stride));
+            } else if (more) {  // chunk 0 of the next pair
+                const uint8_t *a = sm_nxt + 16u * (uint32_t(lane) < Rn ? uint32_t(lane) : 0u);
+                nA = __ldg(reinterpret_cast<const uint4 *>(a));
+                nB = __ldg(reinterpret_cast<const uint4 *>(nhasB ? a + 64u * Rn : a));
+            }
+        }
+        if ((I & 3) == 0) {
+            if (I > 0) {
+                x4A = nxA;
+                x4B = nxB;
+            }
+            if (I < 28) {
+                nxA = __ldg(xA + (I >> 2) + 1);
+                nxB = __ldg(xB + (I >> 2) + 1);
+            }
+        }
+        const uint32_t eA = decode_entry_rs(la, lutA, sA_, k.one, I);
+        const uint32_t eB = decode_entry_rs(lb, lutB, sB_, k.one, I);
+        const uint32_t sel = (I & 1) ? 0xB3A2u : 0x9180u;
+        fma_bf16x2(aA0, aA1, lop3_merge(prmt(word4(sA, (I >> 1) & 3), 0u, sel), eA), word4(x4A, I));
+        fma_bf16x2(aB0, aB1, lop3_merge(prmt(word4(sB, (I >> 1) & 3), 0u, sel), eB), word4(x4B, I));
+        if ((I & 7) == 7) {
+            sA = nA;
+            sB = nB;
+        }
+    }
+    bad |= tile_check_bits(la) | tile_check_bits(lb);
+    if (xa | xb) {  // escaped groups beyond the slots: second pass
+        if (xa) {
+            const float2 r = escaped_sum_global(ebA, emA, gA_sm, stride, reinterpret_cast<const uint32_t *>(xA));
+            aA0 = r.x;
+            aA1 = r.y;
+        }
+        if (xb) {
+            const float2 r = escaped_sum_global(ebB, emB, gB_sm, stride, reinterpret_cast<const uint32_t *>(xB));
+            aB0 = r.x;
+            aB1 = r.y;
+        }
+    }
+    c0A = sA;  // chunk 0 of the next pair
+    c0B = sB;
+    pA = aA0 + aA1;
+    pB = aB0 + aB1;
 }
 
-// The batch-1 Huffman GEMV with lane-private copies of the pair table,
-// escaped groups decoded inside the main loop (see expand_escape above).
-// kHalves: two CTAs per SM of half-row-block units, 16 copies of the table
-// (64 KB: lanes l and l + 16 share copy l % 16, entry w of copy c at byte
-// 64 w + 4 c, so a lookup is one or two shared-memory wavefronts); while one
-// CTA of an SM finishes, the next launch's CTA builds its tables and fetches
-// its first codes beside it.  Otherwise one CTA per SM of whole row blocks
-// and 32 copies (128 KB).
-template <int W, bool kHalves>
+// The batch-1 Huffman GEMV with 32 lane-private copies of the pair table
+// (taken whenever they fit, as for every matrix measured): one CTA per SM of
+// whole row blocks, the pair loop of gemv_col_compressed with escaped groups
+// decoded inside the main loop (see expand_escapes above) and full row
+// blocks on a path with constant strides.
+template <int W>
 __device__ __forceinline__ void gemv_private(const GemvParams &p, int rb_per_cta) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t bars[kMaxColWarps * kPairStages];
-    constexpr int kCopies = kHalves ? 16 : 32;
-    constexpr uint32_t kTabBytes = uint32_t(kLutEntries) * kCopies * 4u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const BlobView &v = p.v;
     const uint32_t gpr = v.gpr;
     const uint32_t nrb = v.nfull + (v.tail_rows ? 1u : 0u);
-    const Segs g = cta_segs<W>(v, gpr, nrb, kHalves, rb_per_cta);
-    const uint32_t nseg = g.seg1 - g.seg0;
-    const uint32_t npairs = g.ppr * nseg;
+    const uint32_t rb0 = blockIdx.x * uint32_t(rb_per_cta);
+    const uint32_t rb1 = rb0 + uint32_t(rb_per_cta) < nrb ? rb0 + uint32_t(rb_per_cta) : nrb;
+    const uint32_t nrbc = rb1 - rb0;
+    uint32_t k0, k1;
+    warp_cols(gpr, warp, W, k0, k1);
+    const uint32_t np = (k1 - k0 + 1) / 2;  // pairs per row block
+    const uint32_t npairs = np * nrbc;
     const uint32_t sbytes = code_stage_bytes(v.tdata);
 
     // shared memory: [private tables][common tables][counting stream][warp
-    // partials nseg x W x 32][pad to 128][per warp kPairStages stages]
+    // partials nrbc x W x 32][pad to 128][per warp kPairStages stages]
     // [per warp kRecRing pair records][per warp kEscSlots escape slots]
     const uint32_t priv = smem_addr(smem);
-    unsigned char *common = smem + kTabBytes;
+    unsigned char *common = smem + kPrivateLutBytes;
     const DecodeShared ds = carve_common(common);
     const uint32_t cnt = smem_addr(common) + uint32_t(kCommonSmemBytes);
     float *red = reinterpret_cast<float *>(common + kCommonSmemBytes + kCountWords * 4);
-    const uint32_t stage_lo = (smem_addr(red) + nseg * W * 128u + 127u) & ~127u;
+    const uint32_t stage_lo = (smem_addr(red) + uint32_t(rb_per_cta) * W * 128u + 127u) & ~127u;
     const uint32_t st0 = stage_lo + uint32_t(warp) * kPairStages * sbytes;
     const uint32_t bar0 = smem_addr(&bars[warp * kPairStages]);
     const uint32_t ring = stage_lo + uint32_t(W) * kPairStages * sbytes + uint32_t(warp) * kRecRing * kRecBytes;
     const uint32_t slots = stage_lo + uint32_t(W) * (kPairStages * sbytes + kRecRing * kRecBytes) +
                            uint32_t(warp) * kEscSlots * kEscSlotBytes;
+    const PairRecSpan span{npairs, rb0, k0, k1, np};
 
     if (lane == 0) {
 #pragma unroll
@@ -572,9 +580,9 @@ __device__ __forceinline__ void gemv_private(const GemvParams &p, int rb_per_cta
     // first copies, chunk 0 of the first pair's sign+mantissa bytes, the
     // counting stream, the private copies.
     uint32_t nissued = 0;
-    const RecLoad first = seg_recs_load(v, g, npairs, 0);
+    const RecLoad first = pair_recs_load(v, span, 0);
     build_tables(ds, v);
-    seg_recs_store(v, ring, g, npairs, 0, first);
+    pair_recs_store(v, ring, span, 0, first);
 #pragma unroll
     for (int s = 0; s < kPairStages; s++) {
         if (nissued < npairs) {
@@ -582,17 +590,14 @@ __device__ __forceinline__ void gemv_private(const GemvParams &p, int rb_per_cta
             nissued++;
         }
     }
-    SegCursor cur;
-    cur.start(g);
     const uint8_t *sm_cur = nullptr;
     uint4 c0A = make_uint4(0, 0, 0, 0), c0B = c0A;
     if (npairs > 0) {
-        const uint32_t rb = g.rb(cur.seg);
-        const uint32_t R0 = rb < v.nfull ? uint32_t(kTileRows) : v.tail_rows;
+        const uint32_t R0 = rb0 < v.nfull ? uint32_t(kTileRows) : v.tail_rows;
         sm_cur = rec_sm(v, ring);
         const uint8_t *a = sm_cur + 16u * (uint32_t(lane) < R0 ? uint32_t(lane) : 0u);
         c0A = __ldg(reinterpret_cast<const uint4 *>(a));
-        c0B = __ldg(reinterpret_cast<const uint4 *>(cur.kgA + 1 < cur.kend ? a + 64u * R0 : a));
+        c0B = __ldg(reinterpret_cast<const uint4 *>(k0 + 1 < k1 ? a + 64u * R0 : a));
     }
     if (threadIdx.x < uint32_t(kCountWords)) {
         // word k of the stream holding the 10-bit values 0, 1, ..., 31 in order
@@ -606,190 +611,55 @@ __device__ __forceinline__ void gemv_private(const GemvParams &p, int rb_per_cta
         asm volatile("st.shared.u32 [%0], %1;" :: "r"(cnt + 4u * uint32_t(k)), "r"(wv) : "memory");
     }
     __syncthreads();
-    // copy c of entry w at byte (kCopies * w + c) * 4
-    for (int i = threadIdx.x; i < kLutEntries * kCopies / 4; i += blockDim.x) {
-        const uint32_t e = ds.lut[uint32_t(i) / (kCopies / 4)];
-        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" :: "r"(priv + 16u * uint32_t(i)), "r"(e) : "memory");
-    }
+    replicate_private(ds, priv);
     __syncthreads();
     grid_dep_wait();  // x may come from the kernel before
-    const uint32_t lut = priv + 4u * (uint32_t(lane) % uint32_t(kCopies));
-    constexpr uint32_t kStride = uint32_t(kCopies) * 4u;
-    const uint32_t zero = smem_addr(ds.zero);
-    const uint32_t one = gpr != 0u ? 1u : 0u;  // 1, held in a register
-    const uint32_t below = (1u << lane) - 1u;
+    PrivCtx kc;
+    kc.lut = priv + 4u * uint32_t(lane);
+    kc.zero = smem_addr(ds.zero);
+    kc.cnt = cnt;
+    kc.slots = slots;
+    kc.below = (1u << lane) - 1u;
+    kc.one = gpr != 0u ? 1u : 0u;
 
-    float s_w = 0.f;  // this warp's partial for row `lane` of segment cur.seg
+    PairCursor cur{rb0, k0};
+    float s_w = 0.f;  // this warp's partial for row `lane` of row block cur.rb
     uint32_t bad = 0;
     if (npairs == 0)
-        for (uint32_t sl = 0; sl < nseg; sl++)
-            red[(sl * W + warp) * 32 + lane] = 0.f;
+        for (uint32_t rl = 0; rl < nrbc; rl++)
+            red[(rl * W + warp) * 32 + lane] = 0.f;
 
 #pragma unroll 1
     for (uint32_t j = 0; j < npairs; j++) {
         const uint32_t st = st0 + (j & 1u) * sbytes, bar = bar0 + 8u * (j & 1u);
         mbar_wait(bar, (j >> 1) & 1u, p.status, kStatusTimeout);
         const uint4 rbk = lds128(ring + kRecBytes * (j % uint32_t(kRecRing)) + 16u);  // pkA, pkB, q0
-        const uint32_t pkA = rbk.x, pkB = rbk.y;
-        const uint32_t n16A = pkA & 0xFFu, n16B = pkB & 0xFFu;
-        const uint32_t nescA = (pkA >> 8) & 0xFFu, nescB = (pkB >> 8) & 0xFFu;
-        const bool hasB = cur.kgA + 1 < cur.kend;
-        const uint32_t rb = g.rb(cur.seg);
-        const bool full = rb < v.nfull;
-        const uint32_t R = full ? uint32_t(kTileRows) : v.tail_rows;
-        uint32_t gA, gB;
-        if (full) {
-            gA = lds_u8(st + uint32_t(lane));
-            gB = lds_u8(st + 32u + uint32_t(lane));
-        } else {
-            const uint64_t q0 = (uint64_t(rbk.w) << 32) | rbk.z;
-            const uint32_t l = uint32_t(lane) < R ? uint32_t(lane) : 0u;
-            gA = __ldg(v.glen + q0 + l);
-            gB = hasB ? __ldg(v.glen + q0 + R + l) : 0u;
-        }
-        // one warp prefix sum over both tiles' group lengths (16-bit halves)
-        const bool vA = uint32_t(lane) < R, vB = hasB && vA;
-        uint32_t ga = vA ? gA : 0u, gb = vB ? gB : 0u;
-        const uint32_t g2 = ga | (gb << 16);
-        uint32_t incl = g2;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1)
-            asm("{\n\t.reg .b32 u;\n\t.reg .pred q;\n\t"
-                "shfl.sync.up.b32 u|q, %0, %1, 0, -1;\n\t"
-                "@q add.u32 %0, %0, u;\n\t}"
-                : "+r"(incl) : "r"(d));
-        const uint32_t off2 = incl - g2;
-        const uint32_t tot2 = __shfl_sync(0xffffffffu, incl, 31);
-        uint32_t emA = __ballot_sync(0xffffffffu, vA && ga == 0u);
-        uint32_t emB = __ballot_sync(0xffffffffu, vB && gb == 0u);
-        // A pair whose tables or group lengths do not add up (a device copy
-        // damaged after its header was checked) is flagged and decodes the
-        // zero stream in every lane, so no read leaves the stage.
-        if (((pkA | pkB) >> 16) != 0u || (tot2 & 0xFFFFu) > 16u * n16A || (tot2 >> 16) > 16u * n16B ||
-            uint32_t(__popc(emA)) != nescA || uint32_t(__popc(emB)) != nescB) {
-            if (lane == 0)
-                atomicOr(p.status, uint32_t(kStatusBadTile));
-            ga = 0u;
-            gb = 0u;
-            emA = 0u;
-            emB = 0u;
-        }
-        const uint32_t cA = st + 64u, cB = cA + 16u * n16A;
-        const uint32_t ebA = cB + 16u * n16B, ebB = ebA + 64u * nescA;
-        // escaped groups: slots 0.. for A's, then B's, at most kEscSlots
-        uint32_t wzA = zero, wzB = zero, lutA = lut, lutB = lut, sA_ = kStride, sB_ = kStride;
-        bool xa = false, xb = false;
-        if ((emA | emB) != 0u) {
-            const uint32_t pa = __popc(emA), pb = __popc(emB);
-            const uint32_t nA = pa < uint32_t(kEscSlots) ? pa : uint32_t(kEscSlots);
-            const uint32_t nB = pb < uint32_t(kEscSlots) - nA ? pb : uint32_t(kEscSlots) - nA;
-            expand_escapes(nA, ebA, slots, 0u);
-            expand_escapes(nB, ebB, slots, nA);
-            __syncwarp();
-            const uint32_t rA = __popc(emA & below), rB = nA + __popc(emB & below);
-            xa = (emA >> lane) & 1u;
-            xb = (emB >> lane) & 1u;
-            if (xa && rA < nA) {
-                wzA = cnt;
-                lutA = slots + kEscSlotBytes * rA;
-                sA_ = 4u;
-                xa = false;  // decoded in the main loop
-            }
-            if (xb && rB < nA + nB) {
-                wzB = cnt;
-                lutB = slots + kEscSlotBytes * rB;
-                sB_ = 4u;
-                xb = false;
-            }
-        }
-        LaneStream la, lb;
-        {
-            const uint32_t offA = off2 & 0xFFFFu, offB = off2 >> 16;
-            const uint32_t wA = ga != 0u ? ((cA + offA) & ~3u) : wzA;
-            const uint32_t wB = gb != 0u ? ((cB + offB) & ~3u) : wzB;
-            la.lo = lds32(wA);
-            la.hi = lds32(wA + 4);
-            la.nx = lds32(wA + 8);
-            la.wp = wA + 12;
-            la.c = ga != 0u ? 8u * (offA & 3u) : 0u;
-            la.expect = ga != 0u ? 8u * (la.wp + ga) + la.c : 0u;
-            lb.lo = lds32(wB);
-            lb.hi = lds32(wB + 4);
-            lb.nx = lds32(wB + 8);
-            lb.wp = wB + 12;
-            lb.c = gb != 0u ? 8u * (offB & 3u) : 0u;
-            lb.expect = gb != 0u ? 8u * (lb.wp + gb) + lb.c : 0u;
-        }
-        const uint32_t stride = 16u * R;
-        const uint32_t lc = uint32_t(lane) < R ? uint32_t(lane) : 0u;
-        const uint8_t *gA_sm = sm_cur + 16u * lc, *gB_sm = hasB ? gA_sm + 64u * R : gA_sm;
+        const bool hasB = cur.kgA + 1 < k1;
+        const bool full = cur.rb < v.nfull;
         const bool more = j + 1 < npairs;
-        SegCursor nxt = cur;
-        nxt.next(g);
-        const uint32_t rbn = g.rb(nxt.seg);
-        const uint32_t Rn = rbn < v.nfull ? uint32_t(kTileRows) : v.tail_rows;
+        PairCursor nxt = cur;
+        nxt.next(k0, k1);
+        const uint32_t Rn = nxt.rb < v.nfull ? uint32_t(kTileRows) : v.tail_rows;
         const uint8_t *sm_nxt = more ? rec_sm(v, ring + kRecBytes * ((j + 1) % uint32_t(kRecRing))) : sm_cur;
         const uint4 *xA = reinterpret_cast<const uint4 *>(p.x) + size_t(cur.kgA) * 8;
-        const uint4 *xB = xA + (hasB ? 8 : 0);
-        float aA0 = 0.f, aA1 = 0.f, aB0 = 0.f, aB1 = 0.f;
-        uint4 sA = c0A, sB = c0B, nA = sA, nB = sB;
-        uint4 x4A = __ldg(xA), x4B = __ldg(xB), nxA = x4A, nxB = x4B;
-#pragma unroll
-        for (int I = 0; I < 32; I++) {
-            if ((I & 7) == 0) {  // next chunk of sign+mantissa bytes
-                if (I < 24) {
-                    nA = __ldg(reinterpret_cast<const uint4 *>(gA_sm + uint32_t((I >> 3) + 1) * stride));
-                    nB = __ldg(reinterpret_cast<const uint4 *>(gB_sm + uint32_t((I >> 3) + 1) * stride));
-                } else if (more) {  // chunk 0 of the next pair
-                    const uint8_t *a = sm_nxt + 16u * (uint32_t(lane) < Rn ? uint32_t(lane) : 0u);
-                    nA = __ldg(reinterpret_cast<const uint4 *>(a));
-                    nB = __ldg(reinterpret_cast<const uint4 *>(nxt.kgA + 1 < nxt.kend ? a + 64u * Rn : a));
-                }
-            }
-            if ((I & 3) == 0) {
-                if (I > 0) {
-                    x4A = nxA;
-                    x4B = nxB;
-                }
-                if (I < 28) {
-                    nxA = __ldg(xA + (I >> 2) + 1);
-                    nxB = __ldg(xB + (I >> 2) + 1);
-                }
-            }
-            const uint32_t eA = decode_entry_rs(la, lutA, sA_, one, I);
-            const uint32_t eB = decode_entry_rs(lb, lutB, sB_, one, I);
-            const uint32_t sel = (I & 1) ? 0xB3A2u : 0x9180u;
-            fma_bf16x2(aA0, aA1, lop3_merge(prmt(word4(sA, (I >> 1) & 3), 0u, sel), eA), word4(x4A, I));
-            fma_bf16x2(aB0, aB1, lop3_merge(prmt(word4(sB, (I >> 1) & 3), 0u, sel), eB), word4(x4B, I));
-            if ((I & 7) == 7) {
-                sA = nA;
-                sB = nB;
-            }
-        }
-        bad |= tile_check_bits(la) | tile_check_bits(lb);
-        if (xa | xb) {  // escaped groups beyond the slots: second pass
-            if (xa) {
-                const float2 r = escaped_sum_global(ebA, emA, gA_sm, stride, reinterpret_cast<const uint32_t *>(xA));
-                aA0 = r.x;
-                aA1 = r.y;
-            }
-            if (xb) {
-                const float2 r = escaped_sum_global(ebB, emB, gB_sm, stride, reinterpret_cast<const uint32_t *>(xB));
-                aB0 = r.x;
-                aB1 = r.y;
-            }
-        }
-        c0A = sA;  // chunk 0 of the next pair
-        c0B = sB;
+        const uint64_t q0 = (uint64_t(rbk.w) << 32) | rbk.z;
+        float pA, pB;
+        if (full)
+            priv_pair<true>(p, kc, st, rbk.x, rbk.y, q0, kTileRows, hasB, sm_cur, xA, more, sm_nxt, Rn,
+                            nxt.kgA + 1 < k1, c0A, c0B, bad, pA, pB);
+        else
+            priv_pair<false>(p, kc, st, rbk.x, rbk.y, q0, v.tail_rows, hasB, sm_cur, xA, more, sm_nxt, Rn,
+                             nxt.kgA + 1 < k1, c0A, c0B, bad, pA, pB);
         sm_cur = sm_nxt;
-        s_w = s_w + (aA0 + aA1);
+        s_w = s_w + pA;
         if (hasB)
-            s_w = s_w + (aB0 + aB1);
-        if (nxt.seg != cur.seg) {  // the warp's last pair of this segment
-            red[((cur.seg - g.seg0) * W + warp) * 32 + lane] = s_w;
+            s_w = s_w + pB;
+        const uint32_t rb_done = cur.rb;
+        cur = nxt;
+        if (cur.rb != rb_done) {  // the warp's last pair of this row block
+            red[((rb_done - rb0) * W + warp) * 32 + lane] = s_w;
             s_w = 0.f;
         }
-        cur = nxt;
         // the stage is free: start the pair kPairStages ahead (the reads above
         // come before the copy engine's writes)
         fence_proxy_async_smem();
@@ -797,69 +667,15 @@ __device__ __forceinline__ void gemv_private(const GemvParams &p, int rb_per_cta
         if (nissued < npairs) {
             pair_issue_rec<false>(v, ring + kRecBytes * (nissued % uint32_t(kRecRing)), st, 0u, bar);
             if (nissued % uint32_t(kRecRound) == 2u && nissued - 2u + uint32_t(kRecRound) < npairs)
-                seg_recs_store(v, ring, g, npairs, nissued - 2u + uint32_t(kRecRound),
-                               seg_recs_load(v, g, npairs, nissued - 2u + uint32_t(kRecRound)));
+                pair_recs_store(v, ring, span, nissued - 2u + uint32_t(kRecRound),
+                                pair_recs_load(v, span, nissued - 2u + uint32_t(kRecRound)));
             nissued++;
         }
         __syncwarp();
     }
     tile_check_flush(bad, p.status);
     __syncthreads();
-    if constexpr (kHalves)
-        half_reduce<W>(p, red, g);
-    else
-        cta_reduce<W>(p, red, g.seg0, nseg);
-}
-
-// The uncompressed twin of the half-row-block GEMV: the same units, warps,
-// groups and order of every sum, the weights loaded from their BF16 rows.
-template <int W>
-__device__ __forceinline__ void gemv_half_bf16(const GemvParams &p) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t gpr = uint32_t(p.cols / kGroup);
-    const uint32_t nrb = uint32_t((p.rows + kTileRows - 1) / kTileRows);
-    BlobView dummy{};
-    const Segs g = cta_segs<W>(dummy, gpr, nrb, true, 0);
-    const uint32_t nseg = g.seg1 - g.seg0;
-    // shared memory: [x slab gpr x 32 pairs][warp partials nseg x W x 32]
-    uint32_t *xs = reinterpret_cast<uint32_t *>(smem);
-    float *red = reinterpret_cast<float *>(smem + size_t(gpr) * 128);
-    grid_dep_wait();  // x may come from the kernel before
-    load_x_all(p, xs, gpr);
-    __syncthreads();
-#pragma unroll 1
-    for (uint32_t seg = g.seg0; seg < g.seg1; seg++) {
-        const int64_t n = int64_t(g.rb(seg)) * kTileRows + lane;
-        const bool ok = n < p.rows;
-        const uint4 *row = reinterpret_cast<const uint4 *>(p.w + (ok ? n : 0) * p.cols);
-        const uint32_t k0 = g.kbase(seg) + g.kwo, k1 = g.kbase(seg) + g.kwe;
-        float s_w = 0.f;
-        uint4 cur[8], nxt[8];
-#pragma unroll
-        for (int c = 0; c < 8; c++)
-            nxt[c] = (ok && k0 < k1) ? __ldg(row + size_t(k0) * 8 + c) : make_uint4(0, 0, 0, 0);
-#pragma unroll 1
-        for (uint32_t kg = k0; kg < k1; kg++) {
-#pragma unroll
-            for (int c = 0; c < 8; c++)
-                cur[c] = nxt[c];
-            if (kg + 1 < k1) {
-#pragma unroll
-                for (int c = 0; c < 8; c++)
-                    nxt[c] = ok ? __ldg(row + size_t(kg + 1) * 8 + c) : make_uint4(0, 0, 0, 0);
-            }
-            const uint32_t xaddr = smem_addr(xs) + kg * 128u;
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int I = 0; I < 32; I++)
-                fma_bf16x2(a0, a1, word4(cur[I >> 2], I & 3), lds32(xaddr + 4u * I));
-            s_w = s_w + (a0 + a1);
-        }
-        red[((seg - g.seg0) * W + warp) * 32 + lane] = s_w;
-    }
-    __syncthreads();
-    half_reduce<W>(p, red, g);
+    cta_reduce<W>(p, red, rb0, nrbc);
 }
 
 template <int W>
@@ -1042,34 +858,13 @@ template <int W, int kSrc, bool kPrivate>
 __global__ void __launch_bounds__(W * 32, 1) gemv_kg_kernel(const GemvParams p, int rb_per_cta) {
     grid_dep_launch();
     if constexpr (kSrc == kSrcHuffman && kPrivate)
-        gemv_private<W, false>(p, rb_per_cta);
+        gemv_private<W>(p, rb_per_cta);
     else if constexpr (kSrc == kSrcHuffman)
         gemv_col_compressed<W, false>(p, rb_per_cta);
     else if constexpr (kSrc == kSrcPalette4 || kSrc == kSrcExponent)
         gemv_col_formed<W, kSrc>(p, rb_per_cta);
     else
         gemv_col_bf16<W>(p, rb_per_cta);
-}
-
-// Half-row-block units, two CTAs per SM (see gemv_private).
-constexpr int kHalfWarps = 8;
-
-template <int kSrc>
-__global__ void __launch_bounds__(kHalfWarps * 32, 2) gemv_half_kernel(const GemvParams p) {
-    grid_dep_launch();
-    if constexpr (kSrc == kSrcHuffman)
-        gemv_private<kHalfWarps, true>(p, 0);
-    else
-        gemv_half_bf16<kHalfWarps>(p);
-}
-
-size_t half_smem(int src, uint32_t tdata, uint32_t gpr, uint32_t nseg) {
-    const size_t red = size_t(nseg) * kHalfWarps * 128;
-    if (src == kSrcBf16)
-        return size_t(gpr) * 128 + red;
-    return size_t(kLutEntries) * 16 * 4 + size_t(kCommonSmemBytes) + kCountWords * 4 + red + 128 +
-           size_t(kHalfWarps) * (kPairStages * code_stage_bytes(tdata) + size_t(kRecRing) * kRecBytes +
-                                 kEscSlots * kEscSlotBytes);
 }
 
 size_t kg_smem(int warps, int rb_per_cta, int src, bool priv, uint32_t tdata, int gpr) {
@@ -1116,48 +911,7 @@ uw_status launch_kg_src(const GemvParams &p, int rb_per_cta, int src, cudaStream
     return launch_kg_one<W, kSrcHuffman, false>(p, rb_per_cta, stream);
 }
 
-template <int kSrc>
-uw_status launch_half_one(const GemvParams &p, cudaStream_t stream) {
-    const uint32_t gpr = uint32_t(p.cols / kGroup);
-    const uint32_t units = 2u * uint32_t((p.rows + kTileRows - 1) / kTileRows);
-    auto kern = gemv_half_kernel<kSrc>;
-    // resident CTAs per SM at the shared memory one CTA needs with the most
-    // units it can get (ceil(units / grid)); the grid is one wave of those
-    const uint32_t sms = uint32_t(sm_count());
-    uint32_t grid = units < 2u * sms ? units : 2u * sms;
-    size_t smem = half_smem(kSrc, p.v.tdata, gpr, (units + grid - 1) / grid);
-    if (smem > size_t(kMaxSmemPerBlock) - 1024)
-        return UW_ERR_UNSUPPORTED;
-    if (!ensure_smem(kern, smem))
-        return UW_ERR_CUDA;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kHalfWarps * 32, smem) != cudaSuccess)
-        return UW_ERR_CUDA;
-    if (per_sm < 2 && grid > sms) {  // one CTA per SM fits: one wave of sms CTAs
-        grid = units < sms ? units : sms;
-        smem = half_smem(kSrc, p.v.tdata, gpr, (units + grid - 1) / grid);
-        if (smem > size_t(kMaxSmemPerBlock) - 1024)
-            return UW_ERR_UNSUPPORTED;
-        if (!ensure_smem(kern, smem))
-            return UW_ERR_CUDA;
-    }
-    return launch_overlapped(kern, dim3(grid), dim3(kHalfWarps * 32), smem, stream, p) == cudaSuccess ? UW_OK
-                                                                                                 : UW_ERR_CUDA;
-}
-
 }  // namespace
-
-uw_status launch_gemv_half(const GemvParams &p, int src, cudaStream_t stream) {
-    if (p.batch != 1 || (p.cols / kGroup) % 2 != 0)
-        return UW_ERR_UNSUPPORTED;
-    if (uint64_t(p.rows / kTileRows + 1) * (p.cols / kGroup) >= (uint64_t(1) << 32))
-        return UW_ERR_UNSUPPORTED;  // tile indices are 32-bit
-    if (src == kSrcHuffman)
-        return launch_half_one<kSrcHuffman>(p, stream);
-    if (src == kSrcBf16)
-        return launch_half_one<kSrcBf16>(p, stream);
-    return UW_ERR_UNSUPPORTED;  // no half-row-block kernel for the intermediate forms
-}
 
 size_t gemv_kg_smem_bytes(int warps, int rb_per_cta, bool compressed, uint32_t tdata, int gpr) {
     return kg_smem(warps, rb_per_cta, compressed ? kSrcHuffman : kSrcBf16, false, tdata, gpr);

@@ -46,9 +46,6 @@ uw_status launch_gemv(const GemvParams &p, int warps, int bp, bool compressed, c
 // rb_per_cta row blocks per CTA, one CTA per SM.
 size_t gemv_kg_smem_bytes(int warps, int rb_per_cta, bool compressed, uint32_t tdata, int gpr);
 uw_status launch_gemv_kg(const GemvParams &p, int warps, int rb_per_cta, int src, cudaStream_t stream);
-// Batch 1, half-row-block units on two CTAs per SM (Huffman and BF16 sources;
-// cols / 64 even); split partials and counters as a two-way K split.
-uw_status launch_gemv_half(const GemvParams &p, int src, cudaStream_t stream);
 
 // Tensor-core matmul (gemm_tc.cu): CTAs of 4G producer warps + 1 MMA warp,
 // 128 rows of W each, `splits` K ranges; batches above kTcMaxBatch run as
