@@ -600,6 +600,21 @@ bool encode_x_map(CUtensorMap *m, const uint16_t *x, int64_t cols, int64_t batch
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// W [rows, cols] as a 2-D tensor (cols inner), boxes of one 32-row x
+// 64-column tile with the 128-byte swizzle; rows past the end read as zeros.
+bool encode_w_tile_map(CUtensorMap *m, const uint16_t *w, int64_t rows, int64_t cols) {
+    const auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(kGroup), cuuint32_t(kTileRows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(w), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 uw_status launch_gemm_tc(const TcParams &base, int G, int src, cudaStream_t stream) {
     const int64_t gpr = base.cols / kGroup;
     if (base.splits < 1 || base.splits > gpr || G < 1 || G > 3)

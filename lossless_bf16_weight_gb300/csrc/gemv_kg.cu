@@ -730,6 +730,94 @@ __device__ __forceinline__ void gemv_col_bf16(const GemvParams &p, int rb_per_ct
     cta_reduce<W>(p, red, rb0, nrbc);
 }
 
+// The uncompressed twin with its tiles brought by the copy engine: one
+// 32-row x 64-column tile of W per 2-D tensor-map copy (128-byte swizzle:
+// 16-byte chunk c of tile row r at chunk position c ^ (r % 8), so the 32
+// lanes' 16-byte reads of one chunk hit distinct banks), kTwinStages tiles in
+// flight per warp.  Same warps, groups and order of every sum as
+// gemv_col_bf16 (and the compressed paths), so the same bits.
+constexpr uint32_t kTwinTileBytes = kTileRows * kGroup * 2;  // 4 KB
+
+size_t twin_tma_smem(int warps, int rb_per_cta, int gpr, int stages) {
+    return size_t(gpr) * 128 + size_t(rb_per_cta) * warps * 128 + 1024 + size_t(warps) * stages * kTwinTileBytes;
+}
+
+template <int W, int kS>
+__global__ void __launch_bounds__(W * 32, 1)
+    gemv_kg_twin_tma_kernel(const __grid_constant__ GemvParams p, const __grid_constant__ CUtensorMap wmap,
+                            int rb_per_cta) {
+    grid_dep_launch();
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) uint64_t bars[kMaxColWarps * kS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t gpr = uint32_t(p.cols / kGroup);
+    const uint32_t nrb = uint32_t((p.rows + kTileRows - 1) / kTileRows);
+    const uint32_t rb0 = blockIdx.x * uint32_t(rb_per_cta);
+    const uint32_t rb1 = rb0 + uint32_t(rb_per_cta) < nrb ? rb0 + uint32_t(rb_per_cta) : nrb;
+    const uint32_t nrbc = rb1 - rb0;
+    uint32_t k0, k1;
+    warp_cols(gpr, warp, W, k0, k1);
+    const uint32_t per = k1 - k0, ntile = per * nrbc;
+    // shared memory: [x slab gpr x 32 pairs][warp partials][pad to 1024][per warp kS tiles]
+    uint32_t *xs = reinterpret_cast<uint32_t *>(smem);
+    float *red = reinterpret_cast<float *>(smem + size_t(gpr) * 128);
+    const uint32_t tiles0 = (smem_addr(red) + uint32_t(rb_per_cta) * W * 128u + 1023u) & ~1023u;
+    const uint32_t st0 = tiles0 + uint32_t(warp) * kS * kTwinTileBytes;
+    const uint32_t bar0 = smem_addr(&bars[warp * kS]);
+    auto issue = [&](uint32_t i) {  // tile i of the warp: row block rb0 + i / per, group k0 + i % per
+        const uint32_t s = i % uint32_t(kS);
+        mbar_expect_tx(bar0 + 8u * s, kTwinTileBytes);
+        tma_load_2d(st0 + s * kTwinTileBytes, &wmap, int((k0 + i % per) * kGroup), int((rb0 + i / per) * kTileRows),
+                    bar0 + 8u * s);
+    };
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < kS; s++)
+            mbar_init(bar0 + 8u * s, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    grid_dep_wait();  // x and W may come from the kernel before (W from a decompress)
+    if (lane == 0)
+        for (uint32_t i = 0; i < uint32_t(kS) && i < ntile; i++)
+            issue(i);
+    load_x_all(p, xs, gpr);
+    __syncthreads();
+    float s_w = 0.f;
+    if (ntile == 0)
+        for (uint32_t rl = 0; rl < nrbc; rl++)
+            red[(rl * W + warp) * 32 + lane] = 0.f;
+#pragma unroll 1
+    for (uint32_t i = 0; i < ntile; i++) {
+        const uint32_t s = i % uint32_t(kS);
+        mbar_wait(bar0 + 8u * s, (i / uint32_t(kS)) & 1u, p.status, kStatusTimeout);
+        const uint32_t kg = k0 + i % per;
+        const uint32_t row = st0 + s * kTwinTileBytes + uint32_t(lane) * 128u;
+        const uint32_t xaddr = smem_addr(xs) + kg * 128u;
+        uint4 wv[8];
+#pragma unroll
+        for (int c = 0; c < 8; c++)
+            wv[c] = lds128(row + 16u * (uint32_t(c) ^ (uint32_t(lane) & 7u)));
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int I = 0; I < 32; I++)
+            fma_bf16x2(a0, a1, word4(wv[I >> 2], I & 3), lds32(xaddr + 4u * I));
+        s_w = s_w + (a0 + a1);
+        if (i % per == per - 1) {  // the warp's last group of this row block
+            red[((i / per) * W + warp) * 32 + lane] = s_w;
+            s_w = 0.f;
+        }
+        // the stage is free once every lane has read it: refill it
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && i + kS < ntile)
+            issue(i + kS);
+        __syncwarp();
+    }
+    __syncthreads();
+    cta_reduce<W>(p, red, rb0, nrbc);
+}
+
 // Palette-4 and exponent sources (the blog's palette and exponent-only
 // pipelines): the twin's loop -- same warps, groups and order of every sum,
 // so the results are bit-identical -- with each group's BF16 pairs rebuilt
@@ -898,10 +986,37 @@ uw_status launch_kg_one(const GemvParams &p, int rb_per_cta, cudaStream_t stream
 // Huffman source: the private-table form when its shared memory fits, else
 // one shared table.  Both decode the same weights, so the results are
 // identical.
+template <int W, int kS>
+uw_status launch_twin_tma(const GemvParams &p, const CUtensorMap &m, int rb_per_cta, size_t smem, cudaStream_t stream) {
+    auto kern = gemv_kg_twin_tma_kernel<W, kS>;
+    if (!ensure_smem(kern, smem))
+        return UW_ERR_CUDA;
+    const int64_t nrb = (p.rows + kTileRows - 1) / kTileRows;
+    const dim3 grid(unsigned((nrb + rb_per_cta - 1) / rb_per_cta));
+    return launch_overlapped(kern, grid, dim3(W * 32), smem, stream, p, m, rb_per_cta) == cudaSuccess ? UW_OK
+                                                                                                  : UW_ERR_CUDA;
+}
+
+// The uncompressed twin: tiles by tensor-map copies when W can be described
+// by a tensor map and three (else two) stages per warp fit; otherwise the
+// per-lane loads of gemv_col_bf16.  All give the same bits.
+template <int W>
+uw_status launch_twin(const GemvParams &p, int rb_per_cta, cudaStream_t stream) {
+    const int gpr = int(p.cols / kGroup);
+    CUtensorMap m;
+    if (encode_w_tile_map(&m, p.w, p.rows, p.cols)) {
+        if (twin_tma_smem(W, rb_per_cta, gpr, 3) <= size_t(kMaxSmemPerBlock) - 1024)
+            return launch_twin_tma<W, 3>(p, m, rb_per_cta, twin_tma_smem(W, rb_per_cta, gpr, 3), stream);
+        if (twin_tma_smem(W, rb_per_cta, gpr, 2) <= size_t(kMaxSmemPerBlock) - 1024)
+            return launch_twin_tma<W, 2>(p, m, rb_per_cta, twin_tma_smem(W, rb_per_cta, gpr, 2), stream);
+    }
+    return launch_kg_one<W, kSrcBf16, false>(p, rb_per_cta, stream);
+}
+
 template <int W>
 uw_status launch_kg_src(const GemvParams &p, int rb_per_cta, int src, cudaStream_t stream) {
     if (src == kSrcBf16)
-        return launch_kg_one<W, kSrcBf16, false>(p, rb_per_cta, stream);
+        return launch_twin<W>(p, rb_per_cta, stream);
     if (src == kSrcPalette4)
         return launch_kg_one<W, kSrcPalette4, false>(p, rb_per_cta, stream);
     if (src == kSrcExponent)

@@ -73,6 +73,9 @@ struct TcParams {
 int gemm_tc_stages(int G, int Np, int src, uint32_t tdata);
 int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits);
 uw_status launch_gemm_tc(const TcParams &p, int G, int src, cudaStream_t stream);
+// W [rows, cols] BF16 as a tensor map of 32-row x 64-column tiles, 128-byte
+// swizzle (the batch-1 uncompressed GEMV's stages).
+bool encode_w_tile_map(CUtensorMap *m, const uint16_t *w, int64_t rows, int64_t cols);
 
 // Preprocess kernels.  max_ctas > 0 caps the grid (the SM split of a
 // preprocess kernel running beside a matmul on another stream) and leaves
