@@ -344,25 +344,7 @@ __device__ __forceinline__ void gemv_col_compressed(const GemvParams &p, int rb_
 // bit-identical results with no second pass.  More than kEscSlots escaped
 // groups in one pair (rare outside heavy-tailed matrices) fall back to the
 // second pass from raw exponents.
-constexpr int kEscSlots = 4;             // expanded escaped groups per warp and pair
-constexpr uint32_t kEscSlotBytes = 128;  // 32 entry words
-constexpr int kCountWords = 16;          // counting stream (320 bits) and read slack
-
-// Expand escaped groups into entry words, all 32 lanes at once (lane i
-// makes word i = e[2i] << 7 | e[2i+1] << 23 | 10 of each): the first n
-// escaped groups whose raw exponents start at shared address `eb` (64 bytes
-// each, in lane order) go to slots s0, s0 + 1, ... at `slots`.
-__device__ __forceinline__ void expand_escapes(uint32_t n, uint32_t eb, uint32_t slots, uint32_t s0) {
-    const uint32_t lane = threadIdx.x & 31;
-#pragma unroll 1
-    for (uint32_t r = 0; r < n; r++) {
-        uint32_t two;
-        asm volatile("ld.shared.u16 %0, [%1];" : "=r"(two) : "r"(eb + 64u * r + 2u * lane) : "memory");
-        const uint32_t e = prmt(two, 0u, 0x4140u) * 128u + 10u;
-        asm volatile("st.shared.u32 [%0], %1;" :: "r"(slots + kEscSlotBytes * (s0 + r) + 4u * lane), "r"(e)
-                     : "memory");
-    }
-}
+// (kEscSlots, expand_escapes and the counting stream: pair_stage.cuh)
 
 // Per-warp constants of the batch-1 private-table GEMV.
 struct PrivCtx {
@@ -599,17 +581,7 @@ __device__ __forceinline__ void gemv_private(const GemvParams &p, int rb_per_cta
         c0A = __ldg(reinterpret_cast<const uint4 *>(a));
         c0B = __ldg(reinterpret_cast<const uint4 *>(k0 + 1 < k1 ? a + 64u * R0 : a));
     }
-    if (threadIdx.x < uint32_t(kCountWords)) {
-        // word k of the stream holding the 10-bit values 0, 1, ..., 31 in order
-        const int k = int(threadIdx.x);
-        uint32_t wv = 0;
-        for (int i = 0; i < 32; i++) {
-            const int lo = 10 * i - 32 * k;
-            if (lo > -10 && lo < 32)
-                wv |= lo >= 0 ? uint32_t(i) << lo : uint32_t(i) >> -lo;
-        }
-        asm volatile("st.shared.u32 [%0], %1;" :: "r"(cnt + 4u * uint32_t(k)), "r"(wv) : "memory");
-    }
+    build_count_stream(cnt);
     __syncthreads();
     replicate_private(ds, priv);
     __syncthreads();

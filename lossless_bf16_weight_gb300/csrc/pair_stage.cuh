@@ -289,4 +289,49 @@ struct PairCursor {
     }
 };
 
+// Escaped groups decoded in the main loop of the private-table kernels.  An
+// escaped group's raw exponents are expanded once into 32 table-entry words
+// (both exponents of a weight pair in BF16 position, bit count 10) in a
+// per-warp slot; the lane then runs the same 32 steps as every other lane
+// over a constant "counting" stream whose 10-bit windows are 0, 1, ..., 31,
+// with the slot as its table and stride 4, so step I reads entry I.  More
+// than kEscSlots escaped groups in one pair (rare outside heavy-tailed
+// matrices) go to a second pass from their raw exponents.
+constexpr int kEscSlots = 4;             // expanded escaped groups per warp and pair
+constexpr uint32_t kEscSlotBytes = 128;  // 32 entry words
+constexpr int kCountWords = 16;          // counting stream (320 bits) and read slack
+
+// Expand escaped groups into entry words, all 32 lanes at once (lane i
+// makes word i = e[2i] << 7 | e[2i+1] << 23 | 10 of each): the first n
+// escaped groups whose raw exponents start at shared address `eb` (64 bytes
+// each, in lane order) go to slots s0, s0 + 1, ... at `slots`.
+__device__ __forceinline__ void expand_escapes(uint32_t n, uint32_t eb, uint32_t slots, uint32_t s0) {
+    const uint32_t lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (uint32_t r = 0; r < n; r++) {
+        uint32_t two;
+        asm volatile("ld.shared.u16 %0, [%1];" : "=r"(two) : "r"(eb + 64u * r + 2u * lane) : "memory");
+        const uint32_t e = prmt(two, 0u, 0x4140u) * 128u + 10u;
+        asm volatile("st.shared.u32 [%0], %1;" :: "r"(slots + kEscSlotBytes * (s0 + r) + 4u * lane), "r"(e)
+                     : "memory");
+    }
+}
+
+// The counting stream at shared address `cnt` (kCountWords words; threads
+// 0 .. kCountWords - 1 each write one): word k holds stream bits 32k ..
+// 32k + 31 of the 10-bit values 0, 1, ..., 31 in order.  Follow with a
+// __syncthreads() before use.
+__device__ __forceinline__ void build_count_stream(uint32_t cnt) {
+    if (threadIdx.x < uint32_t(kCountWords)) {
+        const int k = int(threadIdx.x);
+        uint32_t wv = 0;
+        for (int i = 0; i < 32; i++) {
+            const int lo = 10 * i - 32 * k;
+            if (lo > -10 && lo < 32)
+                wv |= lo >= 0 ? uint32_t(i) << lo : uint32_t(i) >> -lo;
+        }
+        asm volatile("st.shared.u32 [%0], %1;" :: "r"(cnt + 4u * uint32_t(k)), "r"(wv) : "memory");
+    }
+}
+
 }  // namespace uw

@@ -73,6 +73,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x0), "r"(x1), "r"(bar) : "memory");
 }
 
+// One box from shared memory at `src` to a 2-D tensor (kernel-parameter
+// tensor map at `tmap`) at coordinates (x0, x1), in the calling thread's
+// bulk group (x0's byte offset must be a multiple of 16; elements outside
+// the tensor are not written).  Follow with tma_store_commit, and wait with
+// tma_store_wait_read before the source is written again.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, int x0, int x1, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 :: "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x0), "r"(x1), "r"(src) : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The thread's committed stores have finished reading their shared sources.
+__device__ __forceinline__ void tma_store_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// The thread's committed stores are complete.
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Bulk copy global -> shared by the copy engine; completion is counted on
 // the mbarrier.  Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
