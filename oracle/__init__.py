@@ -85,6 +85,11 @@ def _L():
         lib.uwo_swiglu_f64.argtypes = [P, P, I64, P]
         lib.uwo_palette4.argtypes = [P, I64, I64, P, ctypes.c_int, P]
         lib.uwo_exponents.argtypes = [P, I64, I64, P]
+        lib.uwo_stored_cols.argtypes = [I64]
+        lib.uwo_stored_cols.restype = I64
+        lib.uwo_filler.argtypes = [P, ctypes.c_int]
+        lib.uwo_filler.restype = ctypes.c_uint16
+        lib.uwo_pad.argtypes = [P, I64, I64, P, ctypes.c_int, P]
         lib.uwo_join.argtypes = [ctypes.c_uint, ctypes.c_uint]
         lib.uwo_join.restype = ctypes.c_uint16
         _lib = lib
@@ -233,6 +238,30 @@ def swiglu_f64(g, u) -> np.ndarray:
     h = np.zeros(g.size, np.float64)
     _L().uwo_swiglu_f64(_p(g), _p(u), g.size, _p(h))
     return h
+
+
+def stored_cols(cols: int) -> int:
+    """Columns the blob stores for a row of `cols` weights: the next multiple
+    of 64 (a ragged row is extended with filler weights)."""
+    return int(_L().uwo_stored_cols(int(cols)))
+
+
+def filler(pal) -> int:
+    """The filler weight (bf16 bits) of a matrix with this palette."""
+    p = np.zeros(16, np.uint8)
+    p[: len(pal)] = pal
+    return int(_L().uwo_filler(_p(p), len(pal)))
+
+
+def pad(w, pal) -> np.ndarray:
+    """W [rows, cols] extended to [rows, stored_cols(cols)] with the filler."""
+    w = _u16(w)
+    rows, cols = w.shape
+    p = np.zeros(16, np.uint8)
+    p[: len(pal)] = pal
+    out = np.zeros((rows, stored_cols(cols)), np.uint16)
+    _L().uwo_pad(_p(w), rows, cols, _p(p), len(pal), _p(out))
+    return out
 
 
 def palette4(w, pal) -> np.ndarray:

@@ -49,6 +49,15 @@
  *     bit up (stream bit i is bit i%8 of byte i/8, the convention of
  *     DEFLATE); each code enters the stream most significant code bit
  *     first; each group starts on a byte boundary.
+ *   - a row whose length is not a multiple of 64 (the page's matrices all
+ *     are) is extended to the next multiple with filler weights: sign and
+ *     mantissa 0, exponent = the first palette exponent below 255 (a
+ *     finite weight, in the palette, so the last group is escaped only if
+ *     its own weights force it), or 0 when the palette has none.  The
+ *     palette is chosen from the matrix's own weights; everything after it
+ *     (escape flags, code lengths, encoding) runs on the extended matrix.
+ *     The header keeps the true column count; the sections are laid out
+ *     for the extended one.
  *
  * The fp64 matrix product is the plain definition y[b,n] = sum_k x[b,k] W[n,k].
  */
@@ -330,6 +339,30 @@ typedef struct {
     uint64_t off_sm, off_glen, off_tcode, off_tesc, off_code, off_esc;
 } uwo_info;
 
+/* Stored columns: cols rounded up to a whole number of groups. */
+int64_t uwo_stored_cols(int64_t cols) { return (cols + UWO_GROUP - 1) / UWO_GROUP * UWO_GROUP; }
+
+/* The filler weight of a matrix with this palette: sign and mantissa 0,
+ * exponent the first palette entry below 255, else 0. */
+uint16_t uwo_filler(const uint8_t *palette, int npal)
+{
+    for (int s = 0; s < npal; s++)
+        if (palette[s] != 255)
+            return (uint16_t)((unsigned)palette[s] << 7);
+    return 0;
+}
+
+/* W [rows, cols] extended to [rows, uwo_stored_cols(cols)] with the filler
+ * weight of the palette (out: rows * stored columns values). */
+void uwo_pad(const uint16_t *w, int64_t rows, int64_t cols, const uint8_t *palette, int npal, uint16_t *out)
+{
+    int64_t cp = uwo_stored_cols(cols);
+    uint16_t f = uwo_filler(palette, npal);
+    for (int64_t n = 0; n < rows; n++)
+        for (int64_t k = 0; k < cp; k++)
+            out[n * cp + k] = k < cols ? w[n * cols + k] : f;
+}
+
 /* Compress W [rows, cols] (row-major bf16 bits).  If len_override is not
  * NULL its 16 code lengths are used instead of the optimum (the caller must
  * pass a valid prefix code).  Writes the blob when blob != NULL and
@@ -339,21 +372,34 @@ int64_t uwo_compress(const uint16_t *w, int64_t rows, int64_t cols,
                      const uint8_t *len_override, uint8_t *blob, int64_t cap,
                      uwo_info *info)
 {
-    if (rows <= 0 || cols <= 0 || cols % UWO_GROUP != 0)
+    if (rows <= 0 || cols <= 0)
         return -1;
-    int64_t gpr = cols / UWO_GROUP;
-    int64_t nrb = (rows + UWO_TROWS - 1) / UWO_TROWS;
-    int64_t ntiles = nrb * gpr;
-    int64_t ngroups = rows * gpr;
-
+    const int64_t cols_true = cols;
     uint64_t count[256];
     uint8_t palette[UWO_PAL];
     uwo_histogram(w, rows * cols, count);
     int npal = uwo_palette(count, palette);
 
+    /* a ragged row length: the rest of the encoder runs on the extended matrix */
+    uint16_t *padded = NULL;
+    if (cols % UWO_GROUP != 0) {
+        padded = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(rows * uwo_stored_cols(cols)));
+        if (!padded)
+            return -3;
+        uwo_pad(w, rows, cols, palette, npal, padded);
+        w = padded;
+        cols = uwo_stored_cols(cols);
+    }
+    int64_t gpr = cols / UWO_GROUP;
+    int64_t nrb = (rows + UWO_TROWS - 1) / UWO_TROWS;
+    int64_t ntiles = nrb * gpr;
+    int64_t ngroups = rows * gpr;
+
     uint8_t *esc = (uint8_t *)malloc((size_t)ngroups);
-    if (!esc)
+    if (!esc) {
+        free(padded);
         return -3;
+    }
     uwo_escape_flags(w, rows, cols, palette, npal, esc);
 
     /* symbol frequencies over the groups that are coded */
@@ -378,6 +424,7 @@ int64_t uwo_compress(const uint16_t *w, int64_t rows, int64_t cols,
             len[s] = len_override[s];
             if (len[s] > UWO_LMAX || (s >= npal && len[s]) || (freq[s] && !len[s])) {
                 free(esc);
+                free(padded);
                 return -2;
             }
             if (len[s])
@@ -385,6 +432,7 @@ int64_t uwo_compress(const uint16_t *w, int64_t rows, int64_t cols,
         }
         if (kraft > 1.0) {
             free(esc);
+            free(padded);
             return -2;
         }
     } else {
@@ -398,7 +446,7 @@ int64_t uwo_compress(const uint16_t *w, int64_t rows, int64_t cols,
     uint32_t *tcode = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)(ntiles + 1));
     uint32_t *tesc = (uint32_t *)malloc(sizeof(uint32_t) * (size_t)(ntiles + 1));
     if (!glen || !tcode || !tesc) {
-        free(esc); free(glen); free(tcode); free(tesc);
+        free(esc); free(glen); free(tcode); free(tesc); free(padded);
         return -3;
     }
     int64_t code_bits = 0, code16 = 0, escs = 0;
@@ -443,7 +491,7 @@ int64_t uwo_compress(const uint16_t *w, int64_t rows, int64_t cols,
     if (info) {
         memset(info, 0, sizeof *info);
         info->rows = rows;
-        info->cols = cols;
+        info->cols = cols_true;
         info->n_groups = ngroups;
         info->n_escaped = nesc;
         info->n_tiles = ntiles;
@@ -466,7 +514,7 @@ int64_t uwo_compress(const uint16_t *w, int64_t rows, int64_t cols,
         put_u32(blob + 0, UWO_MAGIC);
         put_u32(blob + 4, UWO_VERSION);
         put_u64(blob + 8, (uint64_t)rows);
-        put_u64(blob + 16, (uint64_t)cols);
+        put_u64(blob + 16, (uint64_t)cols_true);
         put_u32(blob + 24, UWO_GROUP);
         put_u32(blob + 28, UWO_TROWS);
         put_u32(blob + 32, UWO_LMAX);
@@ -526,6 +574,7 @@ int64_t uwo_compress(const uint16_t *w, int64_t rows, int64_t cols,
     free(glen);
     free(tcode);
     free(tesc);
+    free(padded);
     return (int64_t)total;
 }
 
@@ -555,11 +604,14 @@ int uwo_read_header(const uint8_t *blob, int64_t bytes, uwo_info *info)
     info->off_code = get_u64(blob + 136);
     info->off_esc = get_u64(blob + 144);
     info->blob_bytes = (int64_t)get_u64(blob + 152);
-    if (info->rows <= 0 || info->cols <= 0 || info->cols % UWO_GROUP)
+    if (info->rows <= 0 || info->cols <= 0)
         return -1;
     if (info->blob_bytes > bytes || info->lmax != UWO_LMAX || info->n_palette > UWO_PAL)
         return -1;
-    int64_t gpr = info->cols / UWO_GROUP;
+    if (info->rows > ((int64_t)1 << 31) || info->cols > ((int64_t)1 << 31))
+        return -1;
+    int64_t cp = uwo_stored_cols(info->cols);
+    int64_t gpr = cp / UWO_GROUP;
     if (info->n_groups != info->rows * gpr ||
         info->n_tiles != (info->rows + UWO_TROWS - 1) / UWO_TROWS * gpr)
         return -1;
@@ -572,7 +624,7 @@ int uwo_read_header(const uint8_t *blob, int64_t bytes, uwo_info *info)
     const uint64_t tiles4 = 4 * ((uint64_t)info->n_tiles + 1);
     const uint64_t start[6] = {info->off_sm, info->off_glen, info->off_tcode,
                                info->off_tesc, info->off_code, info->off_esc};
-    const uint64_t size[6] = {(uint64_t)(info->rows * info->cols), (uint64_t)info->n_groups, tiles4,
+    const uint64_t size[6] = {(uint64_t)(info->rows * cp), (uint64_t)info->n_groups, tiles4,
                               tiles4, 0, 64 * (uint64_t)info->n_escaped};
     uint64_t prev = UWO_HEADER;
     for (int s = 0; s < 6; s++) {
@@ -594,7 +646,7 @@ int uwo_decompress(const uint8_t *blob, int64_t bytes, uint16_t *w)
         return -1;
     uint16_t code[UWO_PAL];
     uwo_canonical_codes(I.code_len, UWO_PAL, code);
-    int64_t rows = I.rows, cols = I.cols, gpr = cols / UWO_GROUP;
+    int64_t rows = I.rows, cols = uwo_stored_cols(I.cols), gpr = cols / UWO_GROUP;
     int64_t nrb = (rows + UWO_TROWS - 1) / UWO_TROWS;
     uint64_t code_end = I.off_esc; /* code section ends before esc section */
     for (int64_t rb = 0; rb < nrb; rb++) {
@@ -637,11 +689,13 @@ int uwo_decompress(const uint8_t *blob, int64_t bytes, uint16_t *w)
                         return -3;
                     cpos += gl;
                 }
-                uint16_t *out = w + n * cols + kg * UWO_GROUP;
+                /* the output keeps only the matrix's own columns */
                 for (int c = 0; c < 4; c++)
                     for (int b = 0; b < 16; b++) {
                         uint64_t at = I.off_sm + (uint64_t)(UWO_TROWS * rb * cols + 64 * R * kg + (c * R + j) * 16 + b);
-                        out[16 * c + b] = uwo_join(e[16 * c + b], blob[at]);
+                        int64_t k = kg * UWO_GROUP + 16 * c + b;
+                        if (k < I.cols)
+                            w[n * I.cols + k] = uwo_join(e[16 * c + b], blob[at]);
                     }
             }
         }

@@ -324,6 +324,51 @@ def test_worked_example_blob(oracle):
     assert np.array_equal(oracle.decompress(blob), w)
 
 
+def test_worked_ragged_row_example(oracle):
+    # A row of 70 weights: extended to 128 with the filler, true width kept.
+    with open(os.path.join(GOLD, "worked_example_ragged_1x70.json")) as f:
+        g = json.load(f)
+    i = np.arange(g["cols"])
+    w = (((120 + (i % 2)) << 7) | i).astype(np.uint16)[None, :]
+    blob, info = oracle.compress(w)
+    b = np.frombuffer(blob, np.uint8)
+    assert info["cols"] == 70 and info["rows"] == 1
+    assert info["palette"] == g["palette"] and info["code_len"][:2] == g["code_len"]
+    assert info["code_bits"] == g["code_bits"] and info["n_groups"] == g["n_groups"]
+    assert info["n_tiles"] == g["n_tiles"] and len(blob) == g["blob_bytes"]
+    for k, v in g["sections"].items():
+        assert info[k] == v
+    assert oracle.filler(info["palette"]) == g["filler"]
+    assert list(b[512:514]) == g["glen"]
+    assert list(np.frombuffer(blob[768:780], np.uint32)) == g["tcode"]
+    assert list(np.frombuffer(blob[1024:1036], np.uint32)) == g["tesc"]
+    assert b[1280:1312].tobytes().hex() == g["code_region_hex"]
+    assert list(b[256:384]) == list(range(70)) + [0] * 58          # sign+mantissa, then the filler's
+    assert np.array_equal(oracle.decompress(blob), w)
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (3, 100), (33, 130), (77, 4097), (40, 14335)])
+def test_ragged_round_trip(oracle, shape):
+    w = wl.normal_weights(*shape, 0.02, seed=shape[1])
+    blob, info = oracle.compress(w)
+    assert info["cols"] == shape[1]
+    assert np.array_equal(oracle.decompress(blob), w)
+    # the blob is the extended matrix's blob apart from the recorded width
+    wp = oracle.pad(w, info["palette"])
+    assert wp.shape[1] % 64 == 0 and np.array_equal(wp[:, : shape[1]], w)
+    assert np.all(wp[:, shape[1]:] == oracle.filler(info["palette"]))
+    blob_p, info_p = oracle.compress(wp)
+    a, bb = np.frombuffer(blob, np.uint8), np.frombuffer(blob_p, np.uint8)
+    assert a.size == bb.size and np.array_equal(a[:16], bb[:16]) and np.array_equal(a[24:], bb[24:])
+
+
+def test_filler_rule(oracle):
+    assert oracle.filler([121, 120]) == 121 << 7
+    assert oracle.filler([255, 3]) == 3 << 7          # never an Inf/NaN exponent
+    assert oracle.filler([255]) == 0
+    assert oracle.stored_cols(1) == 64 and oracle.stored_cols(64) == 64 and oracle.stored_cols(65) == 128
+
+
 def test_worked_escape_example(oracle):
     g = _golden("worked_example_escape_1x128.json")
     k = np.arange(128)
