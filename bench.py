@@ -786,11 +786,8 @@ def context_measurements(torch, uw, w, x, desc, blobs, xd, stream, plan):
     wcopies = max(3, math.ceil(2.5 * l2 / bf16_bytes) + 1)
     wdev = [torch.from_numpy(w.view(np.int16)).cuda() for _ in range(wcopies)]
     yd = torch.empty(BATCH, ROWS, dtype=torch.int16, device="cuda")
-    d = uw.Desc()
-    d.rows, d.cols = ROWS, COLS
     variant = plan.variant
-    ws = torch.empty(uw.workspace_size(d, BATCH, uw.Plan(uw.STRATEGY_FUSED, variant, BATCH, 0.0)),
-                     dtype=torch.uint8, device="cuda")
+    ws = torch.empty(uw.workspace_size_bf16(ROWS, COLS, BATCH, variant), dtype=torch.uint8, device="cuda")
     uw.workspace_init(ws, stream)
     us = _time_steps(torch, lambda i: uw.matmul_bf16(wdev[i % wcopies], xd, yd, ws, variant, stream), steps, stream,
                      wcopies)
@@ -803,7 +800,7 @@ def context_measurements(torch, uw, w, x, desc, blobs, xd, stream, plan):
     for v in range(uw.variant_count(1)):
         if v == variant:
             continue
-        wsv = torch.empty(uw.workspace_size(d, BATCH, uw.Plan(1, v, BATCH, 0.0)), dtype=torch.uint8, device="cuda")
+        wsv = torch.empty(uw.workspace_size_bf16(ROWS, COLS, BATCH, v), dtype=torch.uint8, device="cuda")
         uw.workspace_init(wsv, stream)
         try:
             u2 = _time_steps(torch, lambda i: uw.matmul_bf16(wdev[i % wcopies], xd, yd, wsv, v, stream), 500,

@@ -25,8 +25,15 @@
  *     Activations x are [batch, cols] row-major BF16; outputs y are
  *     [batch, rows] row-major BF16; y = x W^T with fp32 accumulation and
  *     round-to-nearest-even to BF16.
- *   - cols must be a positive multiple of 64 and rows positive, otherwise
- *     UW_ERR_SHAPE.
+ *   - rows and cols must be positive, otherwise UW_ERR_SHAPE.  A row whose
+ *     length is not a multiple of 64 ("ragged") is stored extended to the
+ *     next multiple, cp = 64 * ceil(cols / 64), with filler weights (sign
+ *     and mantissa 0, exponent the first palette exponent below 255, else
+ *     0); the descriptor keeps the true cols.  The blog's matrices all have
+ *     whole rows of 64; this extension is the library's reading for the
+ *     rest.  The matmuls run on the stored width with the activations
+ *     copied into zero-extended rows in the workspace (a filler weight
+ *     times zero adds nothing); uw_decompress writes the true columns only.
  *   - The caller owns all memory.  The library allocates no device memory,
  *     with one exception: the 1 MiB scratch array of uw_matmul_noalloc, a
  *     static device array that every GPU which loads the library holds until
@@ -58,7 +65,8 @@ extern "C" {
 typedef enum {
     UW_OK = 0,
     UW_ERR_INVALID_ARG = 1,      /* NULL pointer, negative size, bad plan      */
-    UW_ERR_SHAPE = 2,            /* rows <= 0, cols <= 0 or cols % 64 != 0     */
+    UW_ERR_SHAPE = 2,            /* rows <= 0 or cols <= 0; the MLP chain also
+                                    refuses cols % 64 != 0                     */
     UW_ERR_BUFFER_TOO_SMALL = 3, /* output or workspace buffer too small       */
     UW_ERR_CORRUPT = 4,          /* blob header or data inconsistent           */
     UW_ERR_CUDA = 5,             /* a CUDA runtime call failed                 */
@@ -95,9 +103,9 @@ typedef struct {
     int64_t rows, cols;
     uint64_t blob_bytes;     /* total blob size                              */
     uint64_t code_bits;      /* Huffman bits of all coded groups (no padding) */
-    uint64_t n_groups;       /* rows * cols / 64                              */
+    uint64_t n_groups;       /* rows * cp / 64 (cp: cols rounded up to 64)    */
     uint64_t n_escaped;      /* groups stored with raw exponents              */
-    uint64_t n_tiles;        /* ceil(rows / 32) * cols / 64                   */
+    uint64_t n_tiles;        /* ceil(rows / 32) * cp / 64                     */
     int32_t n_palette;       /* palette entries in use (0..16)                */
     int32_t lmax;            /* longest code length (5 in format version 2)   */
     uint8_t palette[16];     /* exponent value of each symbol                 */
@@ -124,8 +132,8 @@ typedef struct {
  *   blob_out   host buffer of *blob_bytes bytes, or NULL to query the size.
  *   blob_bytes in: capacity of blob_out; out: size of the blob.
  * Returns UW_ERR_BUFFER_TOO_SMALL (with *blob_bytes set) when blob_out is
- * NULL or too small, UW_ERR_SHAPE when cols is not a positive multiple of 64
- * or rows is not positive, UW_ERR_UNSUPPORTED beyond 2^31 rows or columns or
+ * NULL or too small, UW_ERR_SHAPE when rows or cols is not positive,
+ * UW_ERR_UNSUPPORTED beyond 2^31 rows or columns or
  * when the tile tables' 32-bit offsets would overflow.  Uses the host's cores
  * (OpenMP); deterministic. */
 uw_status uw_compress(const uint16_t *w_host, int64_t rows, int64_t cols,
@@ -172,11 +180,19 @@ uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uint16_t *x_de
  * baseline that compression is measured against.
  *   w_dev   [rows, cols] BF16 device weights, x_dev [batch, cols]; both
  *           16-byte aligned (UW_ERR_INVALID_ARG otherwise).  variant as in
- *           uw_plan.  cols a positive multiple of 64 (UW_ERR_SHAPE), rows and
- *           cols at most 2^31 (UW_ERR_UNSUPPORTED), as for compressed matrices. */
+ *           uw_plan.  rows and cols positive (UW_ERR_SHAPE) and at most 2^31
+ *           (UW_ERR_UNSUPPORTED), as for compressed matrices.  Ragged rows
+ *           (cols % 64 != 0) are copied with x into zero-extended rows in the
+ *           workspace first.
+ *   ws_dev  workspace of at least uw_workspace_size_bf16 bytes. */
 uw_status uw_matmul_bf16(const uint16_t *w_dev, int64_t rows, int64_t cols,
                          const uint16_t *x_dev, int64_t batch, uint16_t *y_dev,
                          int32_t variant, void *ws_dev, size_t ws_bytes, void *stream);
+
+/* uw_workspace_size_bf16 -- bytes of workspace uw_matmul_bf16 needs for this
+ * shape, batch and variant (-1: the default). */
+uw_status uw_workspace_size_bf16(int64_t rows, int64_t cols, int64_t batch, int32_t variant,
+                                 size_t *bytes);
 
 /* The palette-4 form of a blob (the blog's palette pipelines: the Huffman
  * codes turned into 4-bit palette indices at run time, or once when the
@@ -186,10 +202,12 @@ uw_status uw_matmul_bf16(const uint16_t *w_dev, int64_t rows, int64_t cols,
  * like the blob's sign+mantissa section at half the width: group q (row j of
  * row block rb, column group kg; R rows in the block) owns 32 bytes in two
  * 16-byte chunks, chunk c (weights 32c..32c+31) at byte 32*q0 + (c*R + j)*16
- * with q0 = 32*rb*(cols/64) + R*kg, weight 32c + 2i + b in nibble b (0 = low)
+ * with q0 = 32*rb*(cp/64) + R*kg, weight 32c + 2i + b in nibble b (0 = low)
  * of byte i.  Escaped groups hold index 0; their exponents stay in the blob.
  *
- * uw_palette4_bytes -- size of the form: rows * cols / 2 bytes. */
+ * Ragged matrices have the form of their stored width cp.
+ *
+ * uw_palette4_bytes -- size of the form: rows * cp / 2 bytes. */
 uw_status uw_palette4_bytes(const uw_desc *d, size_t *bytes);
 
 /* uw_transcode_palette4 -- write the palette-4 form of the blob.
@@ -221,7 +239,7 @@ uw_status uw_matmul_palette4(const uw_desc *d, const void *blob_dev, const void 
  * chunks, chunk c (weights 16c..16c+15) at byte 64*q0 + (c*R + j)*16 with q0
  * and R as for the palette-4 form, weight 16c + b at byte b of the chunk.
  *
- * uw_exponent_bytes -- size of the form: rows * cols bytes. */
+ * uw_exponent_bytes -- size of the form: rows * cp bytes. */
 uw_status uw_exponent_bytes(const uw_desc *d, size_t *bytes);
 
 /* uw_decode_exponents -- write the exponent form of the blob.
@@ -341,7 +359,8 @@ uw_status uw_mlp_workspace_size(const uw_mlp_matrix *m, int32_t n_layers, int64_
 
 /* uw_mlp_forward -- run the chain on `stream`, preprocessing on side_stream.
  *   m          3 * n_layers matrices (gate, up, down per layer); shapes as
- *              above with one D for all layers (UW_ERR_SHAPE otherwise).
+ *              above with one D for all layers, D and every F multiples of
+ *              64 (UW_ERR_SHAPE otherwise).
  *   x_dev      [batch, D] BF16, 16-byte aligned;  y_dev [batch, D] BF16 (written).
  *   sched      slots and SM split, or NULL (2 slots, no split).
  *   ws_dev     at least uw_mlp_workspace_size bytes, cleared once by

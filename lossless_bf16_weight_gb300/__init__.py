@@ -74,6 +74,7 @@ SIGNATURES = [
     ("uw_compress", ctypes.c_int, [_P, _I64, _I64, _P, ctypes.POINTER(_SZ)]),
     ("uw_blob_info", ctypes.c_int, [_P, _SZ, ctypes.POINTER(Desc)]),
     ("uw_workspace_size", ctypes.c_int, [ctypes.POINTER(Desc), _I64, ctypes.POINTER(Plan), ctypes.POINTER(_SZ)]),
+    ("uw_workspace_size_bf16", ctypes.c_int, [_I64, _I64, _I64, _I32, ctypes.POINTER(_SZ)]),
     ("uw_workspace_init", ctypes.c_int, [_P, _SZ, _P]),
     ("uw_decompress", ctypes.c_int, [ctypes.POINTER(Desc), _P, _P, _P, _SZ, _P]),
     ("uw_matmul", ctypes.c_int, [ctypes.POINTER(Desc), _P, _P, _I64, _P, ctypes.POINTER(Plan), _P, _SZ, _P]),
@@ -181,6 +182,12 @@ def _batch(x) -> int:
     return x.shape[0] if x.dim() == 2 else 1
 
 
+def _form_bytes(desc) -> int:
+    """Weights of a blob's stored width (rows extended to whole 64-column
+    groups): the exponent form's bytes, twice the palette-4 form's."""
+    return desc.rows * (-(-desc.cols // 64) * 64)
+
+
 def _mm_bufs(desc, blob_dev, x, y):
     b = _batch(x)
     return [(blob_dev, desc.blob_bytes, "blob_dev"), (x, 2 * b * desc.cols, "x"), (y, 2 * b * desc.rows, "y")]
@@ -221,6 +228,13 @@ def workspace_size(desc: Desc, batch: int = 0, plan: Plan | None = None) -> int:
     n = ctypes.c_size_t(0)
     _check(load().uw_workspace_size(ctypes.byref(desc), batch, _plan_ptr(plan), ctypes.byref(n)),
            "uw_workspace_size")
+    return n.value
+
+
+def workspace_size_bf16(rows: int, cols: int, batch: int = 1, variant: int = -1) -> int:
+    """Workspace bytes of matmul_bf16 for this shape, batch and variant."""
+    n = ctypes.c_size_t(0)
+    _check(load().uw_workspace_size_bf16(rows, cols, batch, variant, ctypes.byref(n)), "uw_workspace_size_bf16")
     return n.value
 
 
@@ -308,14 +322,14 @@ def palette4_bytes(desc: Desc) -> int:
 
 def transcode_palette4(desc: Desc, blob_dev, p4_out, ws, stream=None):
     """uw_transcode_palette4: the 4-bit palette index of every weight into p4_out."""
-    _refuse(_short((blob_dev, desc.blob_bytes, "blob_dev"), (p4_out, desc.rows * desc.cols // 2, "p4_out")),
+    _refuse(_short((blob_dev, desc.blob_bytes, "blob_dev"), (p4_out, _form_bytes(desc) // 2, "p4_out")),
             "uw_transcode_palette4")
     _check(load().uw_transcode_palette4(ctypes.byref(desc), _ptr(blob_dev), _ptr(p4_out), _ptr(ws),
                                         ws.numel() * ws.element_size(), _stream(stream)), "uw_transcode_palette4")
 
 
 def matmul_palette4_status(desc: Desc, blob_dev, p4, x, y, ws, variant: int = -1, stream=None) -> int:
-    if _short(*_mm_bufs(desc, blob_dev, x, y), (p4, desc.rows * desc.cols // 2, "p4")):
+    if _short(*_mm_bufs(desc, blob_dev, x, y), (p4, _form_bytes(desc) // 2, "p4")):
         return UW_ERR_BUFFER_TOO_SMALL
     batch = _batch(x)
     return int(load().uw_matmul_palette4(ctypes.byref(desc), _ptr(blob_dev), _ptr(p4), _ptr(x), batch, _ptr(y),
@@ -335,14 +349,14 @@ def exponent_bytes(desc: Desc) -> int:
 
 def decode_exponents(desc: Desc, blob_dev, e_out, ws, stream=None):
     """uw_decode_exponents: the exponent byte of every weight into e_out."""
-    _refuse(_short((blob_dev, desc.blob_bytes, "blob_dev"), (e_out, desc.rows * desc.cols, "e_out")),
+    _refuse(_short((blob_dev, desc.blob_bytes, "blob_dev"), (e_out, _form_bytes(desc), "e_out")),
             "uw_decode_exponents")
     _check(load().uw_decode_exponents(ctypes.byref(desc), _ptr(blob_dev), _ptr(e_out), _ptr(ws),
                                       ws.numel() * ws.element_size(), _stream(stream)), "uw_decode_exponents")
 
 
 def matmul_exponents_status(desc: Desc, blob_dev, e, x, y, ws, variant: int = -1, stream=None) -> int:
-    if _short(*_mm_bufs(desc, blob_dev, x, y), (e, desc.rows * desc.cols, "e")):
+    if _short(*_mm_bufs(desc, blob_dev, x, y), (e, _form_bytes(desc), "e")):
         return UW_ERR_BUFFER_TOO_SMALL
     batch = _batch(x)
     return int(load().uw_matmul_exponents(ctypes.byref(desc), _ptr(blob_dev), _ptr(e), _ptr(x), batch, _ptr(y),

@@ -155,8 +155,12 @@ int default_gemv_variant(int64_t rows, int64_t cols, int64_t batch, int src = kS
     return 1 + 3 * si;
 }
 
-WsLayout layout_for(int64_t rows, int64_t cols, int64_t batch, int strategy, int variant) {
+// cols: the matrix's own columns.  Ragged rows (cols % 64 != 0) run on the
+// stored width with x (and, for the uncompressed matmul, W) copied into
+// zero-extended rows at the end of the workspace.
+WsLayout layout_for(int64_t rows, int64_t cols_true, int64_t batch, int strategy, int variant, bool pad_w = false) {
     WsLayout L;
+    const int64_t cols = stored_cols(cols_true);
     const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
     const GemvVariant gv = gemv_variant(variant, rows, cols);
     const int bp = gv.kind == Kind::kColumn ? 1 : pad_batch(batch);
@@ -174,6 +178,13 @@ WsLayout layout_for(int64_t rows, int64_t cols, int64_t batch, int strategy, int
         L.total = align_up(L.weights + uint64_t(rows) * uint64_t(cols) / 2, 256);
     else if (strategy == UW_STRATEGY_EXPONENT)  // the exponent form, a byte per weight
         L.total = align_up(L.weights + uint64_t(rows) * uint64_t(cols), 256);
+    L.xpad = L.wpad = L.total;
+    if (cols != cols_true) {
+        L.total = align_up(L.xpad + 2 * uint64_t(batch) * uint64_t(cols), 256);
+        L.wpad = L.total;
+        if (pad_w)
+            L.total = align_up(L.wpad + 2 * uint64_t(rows) * uint64_t(cols), 256);
+    }
     return L;
 }
 
@@ -188,8 +199,9 @@ int default_p4_variant(int64_t rows, int64_t cols, int64_t batch, int src) {
 }
 
 // tdata: the blob's tile data bytes (sizes the Huffman stages of the default).
-uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t batch, ResolvedPlan *out,
+uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols_true, int64_t batch, ResolvedPlan *out,
                        uint32_t tdata = kWorstTileData) {
+    const int64_t cols = stored_cols(cols_true);
     out->strategy = UW_STRATEGY_FUSED;
     out->variant = -1;
     if (plan) {
@@ -214,6 +226,18 @@ uw_status resolve_plan(const uw_plan *plan, int64_t rows, int64_t cols, int64_t 
         }
     }
     return UW_OK;
+}
+
+// A ragged matrix's activations, copied into zero-extended rows of the
+// stored width (p.cols) at dst; p.x then points there.
+uw_status pad_x(GemvParams &p, const uint16_t *x, int64_t cols_true, uint8_t *dst, cudaStream_t stream) {
+    if (p.cols == cols_true)
+        return UW_OK;
+    uint16_t *xp = reinterpret_cast<uint16_t *>(dst);
+    const uw_status s = launch_pad_rows(x, p.batch, cols_true, xp, p.cols, stream);
+    if (s == UW_OK)
+        p.x = xp;
+    return s;
 }
 
 // Batch rows go through the CUDA-core row kernels in chunks of at most 8;
@@ -338,14 +362,15 @@ void fill_blob_view(const uw_desc &d, const void *blob_dev, BlobView *v) {
     v->n_escaped = d.n_escaped;
     v->code16 = uint32_t((d.off_esc - d.off_code) / 16 > 0xFFFFFFFFull ? 0xFFFFFFFFull : (d.off_esc - d.off_code) / 16);
     v->n_esc32 = uint32_t(d.n_escaped);
-    v->gpr = uint32_t(d.cols / kGroup);
+    v->gpr = uint32_t(stored_cols(d.cols) / kGroup);
     v->nfull = uint32_t(d.rows / kTileRows);
     v->tail_rows = uint32_t(d.rows % kTileRows);
     v->ntiles = uint32_t(std::min<uint64_t>(d.n_tiles, 0xFFFFFFFFull));
     v->tdata = tile_data_bytes(d);
     v->tbuf = v->tdata + kTileSlack;
     v->rows = d.rows;
-    v->cols = d.cols;
+    v->cols = stored_cols(d.cols);
+    v->ocols = d.cols;
     uint16_t code[16];
     canonical_code_values(d.code_len, code);
     std::memcpy(v->palette, d.palette, sizeof v->palette);
@@ -370,7 +395,7 @@ extern "C" const char *uw_status_string(uw_status s) {
     switch (s) {
         case UW_OK: return "ok";
         case UW_ERR_INVALID_ARG: return "invalid argument";
-        case UW_ERR_SHAPE: return "unsupported shape (rows, cols > 0 and cols % 64 == 0 required)";
+        case UW_ERR_SHAPE: return "unsupported shape (rows and cols must be positive)";
         case UW_ERR_BUFFER_TOO_SMALL: return "buffer too small";
         case UW_ERR_CORRUPT: return "corrupt blob";
         case UW_ERR_CUDA: return "CUDA error";
@@ -390,9 +415,9 @@ namespace uw {
 bool desc_ok(const uw_desc &d) {
     if (d.lmax != kLmax || d.n_palette < 0 || d.n_palette > kPalette)
         return false;
-    if (d.rows <= 0 || d.cols <= 0 || d.cols % kGroup || d.rows > (int64_t(1) << 31) || d.cols > (int64_t(1) << 31))
+    if (d.rows <= 0 || d.cols <= 0 || d.rows > (int64_t(1) << 31) || d.cols > (int64_t(1) << 31))
         return false;
-    const uint64_t rows = uint64_t(d.rows), cols = uint64_t(d.cols);
+    const uint64_t rows = uint64_t(d.rows), cols = uint64_t(stored_cols(d.cols));
     const uint64_t gpr = cols / kGroup;
     const uint64_t ntiles = (rows + kTileRows - 1) / kTileRows * gpr;
     if (d.n_groups != rows * gpr || d.n_tiles != ntiles || d.n_escaped > d.n_groups ||
@@ -452,7 +477,7 @@ extern "C" uw_status uw_blob_info(const void *blob_host, size_t bytes, uw_desc *
     if (rd32(b + hdr::group) != uint32_t(kGroup) || rd32(b + hdr::tile_rows) != uint32_t(kTileRows) ||
         !desc_ok(d) || d.blob_bytes > bytes)
         return UW_ERR_CORRUPT;
-    const uint64_t rows = uint64_t(d.rows), cols = uint64_t(d.cols);
+    const uint64_t rows = uint64_t(d.rows), cols = uint64_t(stored_cols(d.cols));
     const uint64_t gpr = cols / kGroup;
     const uint64_t ntiles = (rows + kTileRows - 1) / kTileRows * gpr;
     // tile tables against the group lengths
@@ -551,11 +576,15 @@ extern "C" uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uin
     p.counters = reinterpret_cast<uint32_t *>(wsb + L.counters);
     p.status = reinterpret_cast<uint32_t *>(wsb + L.status);
     p.rows = d->rows;
-    p.cols = d->cols;
+    p.cols = p.v.cols;
     p.batch = batch;
     if (rp.strategy == UW_STRATEGY_DECOMPRESS_GEMM) {
         uint16_t *w = reinterpret_cast<uint16_t *>(wsb + L.weights);
-        s = launch_decompress(p.v, w, p.status, as_stream(stream));
+        BlobView stored = p.v;  // the stored width, filler columns included
+        stored.ocols = stored.cols;
+        s = launch_decompress(stored, w, p.status, as_stream(stream));
+        if (s == UW_OK)
+            s = pad_x(p, x, d->cols, wsb + L.xpad, as_stream(stream));
         if (s != UW_OK)
             return s;
         p.w = w;
@@ -565,18 +594,21 @@ extern "C" uw_status uw_matmul(const uw_desc *d, const void *blob_dev, const uin
         const bool pal = rp.strategy == UW_STRATEGY_PALETTE4;
         uint8_t *form = wsb + L.weights;
         s = launch_transcode(p.v, form, pal, p.status, as_stream(stream));
+        if (s == UW_OK)
+            s = pad_x(p, x, d->cols, wsb + L.xpad, as_stream(stream));
         if (s != UW_OK)
             return s;
         p.p4 = form;
         return run_gemv(p, rp.variant, pal ? kSrcPalette4 : kSrcExponent, as_stream(stream));
     }
-    return run_gemv(p, rp.variant, kSrcHuffman, as_stream(stream));
+    s = pad_x(p, x, d->cols, wsb + L.xpad, as_stream(stream));
+    return s != UW_OK ? s : run_gemv(p, rp.variant, kSrcHuffman, as_stream(stream));
 }
 
 extern "C" uw_status uw_palette4_bytes(const uw_desc *d, size_t *bytes) {
     if (!d || !bytes)
         return UW_ERR_INVALID_ARG;
-    *bytes = size_t(uint64_t(d->rows) * uint64_t(d->cols) / 2);
+    *bytes = size_t(uint64_t(d->rows) * uint64_t(stored_cols(d->cols)) / 2);
     return UW_OK;
 }
 
@@ -600,7 +632,7 @@ uw_status matmul_formed(const uw_desc *d, const void *blob_dev, const void *form
         return UW_ERR_INVALID_ARG;
     if (variant >= kGemvVariants)
         return UW_ERR_INVALID_ARG;
-    const int v = variant < 0 ? default_p4_variant(d->rows, d->cols, batch, src) : variant;
+    const int v = variant < 0 ? default_p4_variant(d->rows, stored_cols(d->cols), batch, src) : variant;
     const WsLayout L = layout_for(d->rows, d->cols, batch, UW_STRATEGY_FUSED, v);
     if (ws_bytes < L.total)
         return UW_ERR_BUFFER_TOO_SMALL;
@@ -614,9 +646,10 @@ uw_status matmul_formed(const uw_desc *d, const void *blob_dev, const void *form
     p.counters = reinterpret_cast<uint32_t *>(wsb + L.counters);
     p.status = reinterpret_cast<uint32_t *>(wsb + L.status);
     p.rows = d->rows;
-    p.cols = d->cols;
+    p.cols = p.v.cols;
     p.batch = batch;
-    return run_gemv(p, v, src, as_stream(stream));
+    const uw_status s = pad_x(p, x, d->cols, wsb + L.xpad, as_stream(stream));
+    return s != UW_OK ? s : run_gemv(p, v, src, as_stream(stream));
 }
 }  // namespace
 }  // namespace uw
@@ -630,7 +663,7 @@ extern "C" uw_status uw_matmul_palette4(const uw_desc *d, const void *blob_dev, 
 extern "C" uw_status uw_exponent_bytes(const uw_desc *d, size_t *bytes) {
     if (!d || !bytes)
         return UW_ERR_INVALID_ARG;
-    *bytes = size_t(uint64_t(d->rows) * uint64_t(d->cols));
+    *bytes = size_t(uint64_t(d->rows) * uint64_t(uw::stored_cols(d->cols)));
     return UW_OK;
 }
 
@@ -658,14 +691,15 @@ extern "C" uw_status uw_matmul_bf16(const uint16_t *w, int64_t rows, int64_t col
     if (!w || !x || !y || !ws || batch <= 0 || (reinterpret_cast<uintptr_t>(x) & 15) ||
         (reinterpret_cast<uintptr_t>(w) & 15))
         return UW_ERR_INVALID_ARG;
-    if (rows <= 0 || cols <= 0 || cols % kGroup)
+    if (rows <= 0 || cols <= 0)
         return UW_ERR_SHAPE;
     if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31))
         return UW_ERR_UNSUPPORTED;  // the same limit as compressed matrices
     if (variant >= kGemvVariants)
         return UW_ERR_INVALID_ARG;
-    const int v = variant < 0 ? default_gemv_variant(rows, cols, batch, kSrcBf16) : variant;
-    const WsLayout L = layout_for(rows, cols, batch, UW_STRATEGY_FUSED, v);
+    const int64_t cp = stored_cols(cols);
+    const int v = variant < 0 ? default_gemv_variant(rows, cp, batch, kSrcBf16) : variant;
+    const WsLayout L = layout_for(rows, cols, batch, UW_STRATEGY_FUSED, v, true);
     if (ws_bytes < L.total)
         return UW_ERR_BUFFER_TOO_SMALL;
     uint8_t *wsb = static_cast<uint8_t *>(ws);
@@ -677,9 +711,33 @@ extern "C" uw_status uw_matmul_bf16(const uint16_t *w, int64_t rows, int64_t col
     p.counters = reinterpret_cast<uint32_t *>(wsb + L.counters);
     p.status = reinterpret_cast<uint32_t *>(wsb + L.status);
     p.rows = rows;
-    p.cols = cols;
+    p.cols = cp;
     p.batch = batch;
-    return run_gemv(p, v, kSrcBf16, as_stream(stream));
+    if (cp != cols) {  // ragged rows: W and x copied into zero-extended rows
+        uint16_t *wp = reinterpret_cast<uint16_t *>(wsb + L.wpad);
+        const uw_status s = launch_pad_rows(w, rows, cols, wp, cp, as_stream(stream));
+        if (s != UW_OK)
+            return s;
+        p.w = wp;
+    }
+    const uw_status s = pad_x(p, x, cols, wsb + L.xpad, as_stream(stream));
+    return s != UW_OK ? s : run_gemv(p, v, kSrcBf16, as_stream(stream));
+}
+
+extern "C" uw_status uw_workspace_size_bf16(int64_t rows, int64_t cols, int64_t batch, int32_t variant,
+                                          size_t *bytes) {
+    if (!bytes || batch < 0)
+        return UW_ERR_INVALID_ARG;
+    if (rows <= 0 || cols <= 0)
+        return UW_ERR_SHAPE;
+    if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31))
+        return UW_ERR_UNSUPPORTED;
+    if (variant >= kGemvVariants)
+        return UW_ERR_INVALID_ARG;
+    const int64_t b = std::max<int64_t>(batch, 1);
+    const int v = variant < 0 ? default_gemv_variant(rows, stored_cols(cols), b, kSrcBf16) : variant;
+    *bytes = layout_for(rows, cols, b, UW_STRATEGY_FUSED, v, true).total;
+    return UW_OK;
 }
 
 extern "C" uw_status uw_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h, int64_t n, void *stream) {

@@ -191,10 +191,16 @@ extern "C" uw_status uw_compress(const uint16_t *w, int64_t rows, int64_t cols, 
     using namespace uw;
     if (!w || !blob_bytes)
         return UW_ERR_INVALID_ARG;
-    if (rows <= 0 || cols <= 0 || cols % kGroup)
+    if (rows <= 0 || cols <= 0)
         return UW_ERR_SHAPE;
     if (rows > (int64_t(1) << 31) || cols > (int64_t(1) << 31))
         return UW_ERR_UNSUPPORTED;  // the blob descriptor's limit (no size product can wrap)
+    // A row whose length is not a multiple of 64 is stored extended to the
+    // next multiple with filler weights (sign and mantissa 0, exponent the
+    // first palette exponent below 255, else 0); the palette is chosen from
+    // the matrix's own weights and the header keeps the true column count.
+    const int64_t cols_true = cols;
+    cols = stored_cols(cols);
     const int64_t gpr = cols / kGroup;
     const int64_t nrb = (rows + kTileRows - 1) / kTileRows;
     const int64_t ntiles = nrb * gpr;
@@ -209,8 +215,8 @@ extern "C" uw_status uw_compress(const uint16_t *w, int64_t rows, int64_t cols, 
         uint64_t local[256] = {};
 #pragma omp for schedule(static)
         for (int64_t n = 0; n < rows; n++) {
-            const uint16_t *r = w + n * cols;
-            for (int64_t k = 0; k < cols; k++)
+            const uint16_t *r = w + n * cols_true;
+            for (int64_t k = 0; k < cols_true; k++)
                 local[exponent_of(r[k])]++;
         }
 #pragma omp critical
@@ -231,6 +237,23 @@ extern "C" uw_status uw_compress(const uint16_t *w, int64_t rows, int64_t cols, 
             cb.sym_of[ex[i]] = static_cast<int8_t>(cb.npal);
             cb.npal++;
         }
+    }
+
+    // the extended matrix, when the rows are ragged
+    std::vector<uint16_t> extended;
+    if (cols != cols_true) {
+        uint16_t filler = 0;
+        for (int i = 0; i < cb.npal; i++)
+            if (cb.pal[i] != 255) {
+                filler = static_cast<uint16_t>(cb.pal[i] << 7);
+                break;
+            }
+        extended.resize(size_t(rows) * size_t(cols));
+#pragma omp parallel for schedule(static)
+        for (int64_t n = 0; n < rows; n++)
+            for (int64_t k = 0; k < cols; k++)
+                extended[size_t(n) * cols + k] = k < cols_true ? w[n * cols_true + k] : filler;
+        w = extended.data();
     }
 
     // 3-4. escaped groups and symbol frequencies of the coded ones
@@ -327,7 +350,7 @@ extern "C" uw_status uw_compress(const uint16_t *w, int64_t rows, int64_t cols, 
     put32(h + hdr::magic, kMagic);
     put32(h + hdr::version, kVersion);
     put64(h + hdr::rows, rows);
-    put64(h + hdr::cols, cols);
+    put64(h + hdr::cols, cols_true);
     put32(h + hdr::group, kGroup);
     put32(h + hdr::tile_rows, kTileRows);
     put32(h + hdr::lmax, kLmax);

@@ -74,7 +74,8 @@ struct BlobView {
     uint32_t nfull;       // full 32-row blocks
     uint32_t tail_rows;   // rows of the last, partial block (0: none)
     uint32_t ntiles;      // tiles (the tile tables hold ntiles + 1 entries)
-    int64_t rows, cols;
+    int64_t rows, cols;   // cols: the stored width, a multiple of 64
+    int64_t ocols;        // the matrix's own columns (cols rounded up to 64 gives cols)
     // kLmax-bit prefix -> (exponent << 4) | code length; 0 where no code
     // starts with that prefix.
     uint16_t prefix[kPrefixEntries];

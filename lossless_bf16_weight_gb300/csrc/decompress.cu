@@ -101,10 +101,18 @@ __global__ void __launch_bounds__(W * 32, 16 / W)
 #pragma unroll
         for (int it = 0; it < 8; it++) {
             const int r = it * 4 + (lane >> 3);
-            if (r < R) {
+            const int64_t col = int64_t(cur.kg) * kGroup + c * 8;
+            if (r < R && col < v.ocols) {
                 const uint4 val = obuf[r * 8 + (c ^ (r & 7))];
-                uint16_t *dst = out + (int64_t(cur.rb) * kTileRows + r) * v.cols + int64_t(cur.kg) * kGroup + c * 8;
-                *reinterpret_cast<uint4 *>(dst) = val;
+                uint16_t *dst = out + (int64_t(cur.rb) * kTileRows + r) * v.ocols + col;
+                if ((v.ocols & 7) == 0) {
+                    *reinterpret_cast<uint4 *>(dst) = val;
+                } else {  // ragged rows not 16-byte aligned: the true columns one by one
+                    const uint16_t *h = reinterpret_cast<const uint16_t *>(&val);
+                    const int n = v.ocols - col < 8 ? int(v.ocols - col) : 8;
+                    for (int k = 0; k < n; k++)
+                        dst[k] = h[k];
+                }
             }
         }
         __syncwarp();
@@ -428,10 +436,14 @@ uw_status launch_decompress_w(const BlobView &v, uint16_t *w_out, uint32_t *stat
 
 uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status, cudaStream_t stream, int max_ctas) {
     // lane-private tables when they fit: one CTA per SM (or per allowed SM)
-    // with whole row blocks
+    // with whole row blocks.  The output map has the matrix's own width, so
+    // the tensor-map stores drop the filler columns of ragged rows; a row
+    // pitch that is not a multiple of 16 bytes (no tensor map) goes to the
+    // tile kernel, which stores the true columns one by one.
     const size_t psmem = priv_smem(v.tdata);
     CUtensorMap omap;
-    if (psmem <= size_t(kMaxSmemPerBlock) - 1024 && v.gpr >= 1 && encode_w_tile_map(&omap, w_out, v.rows, v.cols)) {
+    if (psmem <= size_t(kMaxSmemPerBlock) - 1024 && v.gpr >= 1 && (v.ocols & 7) == 0 &&
+        encode_w_tile_map(&omap, w_out, v.rows, v.ocols)) {
         const int64_t nrb = int64_t(v.nfull) + (v.tail_rows ? 1 : 0);
         int64_t ctas = sm_count();
         if (max_ctas > 0 && max_ctas < ctas)

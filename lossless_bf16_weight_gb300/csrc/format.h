@@ -1,5 +1,10 @@
 // Blob layout "UWB1" shared by the library's host and device code.
 //
+// Rows whose length is not a multiple of 64 are stored extended to the next
+// multiple (stored_cols) with filler weights; the header's `cols` is the
+// matrix's own column count and every section below is laid out for the
+// stored width.
+//
 // A blob is position independent (offsets only) so the same bytes serve as
 // the on-disk bundle, the host copy and the device copy.  All integers are
 // little endian; every section starts at a multiple of 256 bytes.
@@ -50,5 +55,10 @@ constexpr int magic = 0, version = 4, rows = 8, cols = 16, group = 24, tile_rows
 }  // namespace hdr
 
 inline uint64_t align_up(uint64_t v, uint64_t a) { return (v + a - 1) / a * a; }
+
+// Columns a blob stores for rows of `cols` weights: the next multiple of the
+// group (a ragged row is extended with filler weights; the header keeps
+// `cols`).
+constexpr int64_t stored_cols(int64_t cols) { return (cols + kGroup - 1) / kGroup * kGroup; }
 
 }  // namespace uw

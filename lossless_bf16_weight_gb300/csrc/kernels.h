@@ -93,6 +93,10 @@ uw_status launch_decompress(const BlobView &v, uint16_t *w_out, uint32_t *status
 uw_status launch_transcode(const BlobView &v, uint8_t *out, bool palette4, uint32_t *status, cudaStream_t stream,
                            int max_ctas = 0);
 uw_status launch_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h, int64_t n, cudaStream_t stream);
+// dst[r, k] = k < cols ? src[r, k] : 0 for rows of cp (a multiple of 64)
+// values; dst 16-byte aligned.
+uw_status launch_pad_rows(const uint16_t *src, int64_t rows, int64_t cols, uint16_t *dst, int64_t cp,
+                          cudaStream_t stream);
 
 // SMs of the current device (152 if the query fails).
 int sm_count();
@@ -137,7 +141,7 @@ uint32_t tile_data_bytes(const uw_desc &d);  // a blob's tile buffer capacity
 
 // Workspace layout: [status word | counters | split partials | weights].
 struct WsLayout {
-    size_t status = 0, counters = 0, partial = 0, weights = 0, total = 0;
+    size_t status = 0, counters = 0, partial = 0, weights = 0, xpad = 0, wpad = 0, total = 0;
 };
 
 // Plan resolution and matmul dispatch (api.cu), shared by the MLP chain.

@@ -78,8 +78,9 @@ uw_status plan_chain(const uw_mlp_matrix *m, int32_t n_layers, int64_t batch, co
     c.D = m[0].desc->cols;
     for (int32_t l = 0; l < n_layers; l++) {
         const uw_desc &g = *m[3 * l].desc, &u = *m[3 * l + 1].desc, &d = *m[3 * l + 2].desc;
-        if (g.cols != c.D || u.cols != c.D || d.rows != c.D || u.rows != g.rows || d.cols != g.rows)
-            return UW_ERR_SHAPE;
+        if (g.cols != c.D || u.cols != c.D || d.rows != c.D || u.rows != g.rows || d.cols != g.rows ||
+            c.D % kGroup || g.rows % kGroup)
+            return UW_ERR_SHAPE;  // the chain keeps whole 64-column groups (no ragged rows)
         c.Fmax = std::max<int64_t>(c.Fmax, g.rows);
     }
     c.steps.resize(size_t(3) * n_layers);

@@ -1,6 +1,11 @@
-// SwiGLU glue of an MLP layer: h = bf16(silu(g) * u), silu(z) = z / (1 + e^-z)
-// computed in fp32 with CUDA's expf.  Memory bound: 8 values per thread per
-// 16-byte load, grid-stride.
+// Element-wise glue around the matmuls.
+//   swiglu    h = bf16(silu(g) * u), silu(z) = z / (1 + e^-z) in fp32 with
+//             CUDA's expf.  Memory bound: 8 values per thread per 16-byte
+//             load, grid-stride.
+//   pad_rows  rows of `cols` values copied into rows of `cp` (a multiple of
+//             64) with zeros after them: the activations (and, for the
+//             uncompressed matmul, the weights) of a matrix whose rows are
+//             stored extended with filler weights.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -39,7 +44,41 @@ __global__ void swiglu_kernel(const uint16_t *__restrict__ g, const uint16_t *__
         h[i] = swiglu1(g[i], u[i]);
 }
 
+__global__ void pad_rows_kernel(const uint16_t *__restrict__ src, int64_t rows, int64_t cols,
+                                uint16_t *__restrict__ dst, int64_t cp) {
+    grid_dep_launch();
+    grid_dep_wait();  // src may come from the kernel before; dst may still be read by it
+    const int64_t per_row = cp / 8;
+    const int64_t n = rows * per_row;
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const int64_t r = i / per_row, k0 = (i - r * per_row) * 8;
+        const uint16_t *row = src + r * cols;
+        uint4 v;
+        uint16_t *h = reinterpret_cast<uint16_t *>(&v);
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            h[k] = k0 + k < cols ? row[k0 + k] : uint16_t(0);
+        reinterpret_cast<uint4 *>(dst)[i] = v;
+    }
+}
+
 }  // namespace
+
+uw_status launch_pad_rows(const uint16_t *src, int64_t rows, int64_t cols, uint16_t *dst, int64_t cp,
+                          cudaStream_t stream) {
+    if (rows <= 0)
+        return UW_OK;
+    if (cp % kGroup || cp < cols || (reinterpret_cast<uintptr_t>(dst) & 15u))
+        return UW_ERR_INVALID_ARG;
+    int64_t blocks = (rows * (cp / 8) + 255) / 256;
+    if (blocks > 152 * 16)
+        blocks = 152 * 16;
+    return launch_overlapped(pad_rows_kernel, dim3(unsigned(blocks)), dim3(256), 0, stream, src, rows, cols, dst,
+                             cp) == cudaSuccess
+               ? UW_OK
+               : UW_ERR_CUDA;
+}
 
 uw_status launch_swiglu(const uint16_t *g, const uint16_t *u, uint16_t *h, int64_t n, cudaStream_t stream) {
     if (n <= 0)

@@ -58,10 +58,7 @@ class Compressed:
 
 def matmul_bf16(w_dev: torch.Tensor, x_dev: torch.Tensor, variant: int = -1) -> np.ndarray:
     rows, cols = w_dev.shape
-    d = uw.Desc()
-    d.rows, d.cols = rows, cols
-    plan = uw.Plan(uw.STRATEGY_FUSED, variant, x_dev.shape[0], 0.0)
-    ws = workspace(uw.workspace_size(d, x_dev.shape[0], plan))
+    ws = workspace(uw.workspace_size_bf16(rows, cols, x_dev.shape[0], variant))
     y = empty_bits(x_dev.shape[0], rows)
     uw.matmul_bf16(w_dev, x_dev, y, ws, variant)
     torch.cuda.synchronize()

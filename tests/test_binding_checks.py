@@ -129,3 +129,27 @@ def test_chain_checks_activations_and_blobs(uw):
         assert rec.calls == ["uw_mlp_forward"]
     finally:
         uw._lib = real
+
+
+@pytest.fixture(scope="module")
+def ragged(uw):
+    blob = uw.compress(wl.normal_weights(40, 100, 0.02, seed=4))
+    return uw.blob_info(blob), torch.from_numpy(blob)
+
+
+def test_ragged_forms_are_sized_for_the_stored_width(uw, ragged, fake):
+    # 100 columns are stored as 128: the forms hold rows * 128 weights
+    d, blob = ragged
+    assert (d.rows, d.cols) == (40, 100)
+    ws = torch.zeros(4096, dtype=torch.uint8)
+    n = 40 * 128
+    uw.transcode_palette4(d, blob, torch.zeros(n // 2, dtype=torch.uint8), ws, stream=0)
+    uw.decode_exponents(d, blob, torch.zeros(n, dtype=torch.uint8), ws, stream=0)
+    _refused(uw, uw.transcode_palette4, d, blob, torch.zeros(40 * 100 // 2, dtype=torch.uint8), ws, stream=0)
+    _refused(uw, uw.decode_exponents, d, blob, torch.zeros(40 * 100, dtype=torch.uint8), ws, stream=0)
+    x, y = _bits(2, 100), _bits(2, 40)
+    assert uw.matmul_palette4_status(d, blob, torch.zeros(n // 2, dtype=torch.uint8), x, y, ws, stream=0) == 0
+    assert uw.matmul_exponents_status(d, blob, torch.zeros(40 * 100, dtype=torch.uint8), x, y, ws,
+                                      stream=0) == uw.UW_ERR_BUFFER_TOO_SMALL
+    uw.decompress(d, blob, _bits(40, 100), ws, stream=0)   # the true columns only
+    assert fake.calls == ["uw_transcode_palette4", "uw_decode_exponents", "uw_matmul_palette4", "uw_decompress"]

@@ -33,7 +33,7 @@ def _entry_points(L, uw, d):
 
 def _descs(uw):
     mats = [wl.normal_weights(96, 256, 0.02, seed=1), wl.heavy_tailed_weights(64, 512, seed=2),
-            wl.all_bf16_patterns(), np.zeros((33, 128), np.uint16)]
+            wl.all_bf16_patterns(), np.zeros((33, 128), np.uint16), wl.normal_weights(40, 100, 0.02, seed=3)]
     return [uw.blob_info(uw.compress(w)) for w in mats]
 
 
@@ -52,7 +52,8 @@ def _copy(d):
 
 MUTATIONS = {
     "no rows": lambda d: setattr(d, "rows", 0),
-    "cols not a multiple of 64": lambda d: setattr(d, "cols", d.cols - 32),
+    "cols beyond the group count": lambda d: setattr(d, "cols", d.cols + 32),
+    "no cols": lambda d: setattr(d, "cols", 0),
     "rows beyond 2^31": lambda d: setattr(d, "rows", d.rows << 32),
     "tile count": lambda d: setattr(d, "n_tiles", d.n_tiles + 1),
     "group count": lambda d: setattr(d, "n_groups", d.n_groups - 1),
@@ -99,5 +100,20 @@ def test_uncompressed_twin_has_the_same_size_limit(uw):
     L = uw.load()
     assert L.uw_matmul_bf16(P, (1 << 31) + 32, 64, P, 1, P, -1, P, 0, None) == 7  # UW_ERR_UNSUPPORTED
     assert L.uw_matmul_bf16(P, 32, (1 << 31) + 64, P, 1, P, -1, P, 0, None) == 7
-    assert L.uw_matmul_bf16(P, 32, 96, P, 1, P, -1, P, 0, None) == 2              # UW_ERR_SHAPE
+    assert L.uw_matmul_bf16(P, 32, 0, P, 1, P, -1, P, 0, None) == 2               # UW_ERR_SHAPE
+    assert L.uw_matmul_bf16(P, 0, 64, P, 1, P, -1, P, 0, None) == 2
+    assert L.uw_matmul_bf16(P, 32, 96, P, 1, P, -1, P, 0, None) == TOO_SMALL      # ragged rows are fine
     assert L.uw_matmul_bf16(P, 32, 128, P, 1, P, -1, P, 0, None) == TOO_SMALL
+
+
+def test_ragged_workspaces_hold_the_zero_extended_rows(uw):
+    # a ragged matmul needs room for x (and, uncompressed, W) at the stored width
+    for rows, cols, batch in [(96, 100, 1), (64, 4097, 4), (33, 14335, 16)]:
+        cp = -(-cols // 64) * 64
+        whole = uw.workspace_size_bf16(rows, cp, batch)
+        assert uw.workspace_size_bf16(rows, cols, batch) >= whole + 2 * batch * cp + 2 * rows * cp
+        d = uw.blob_info(uw.compress(wl.normal_weights(rows, cols, 0.02, seed=rows)))
+        assert d.cols == cols and d.n_groups == rows * cp // 64
+        dw = uw.blob_info(uw.compress(wl.normal_weights(rows, cp, 0.02, seed=rows)))
+        assert uw.workspace_size(d, batch) >= uw.workspace_size(dw, batch) + 2 * batch * cp
+        assert uw.exponent_bytes(d) == rows * cp and uw.palette4_bytes(d) == rows * cp // 2

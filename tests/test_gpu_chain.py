@@ -82,10 +82,7 @@ def twin_chain(g, uw, layers, x_dev, variants):
 
 
 def _twin(g, uw, c, x, y, variant):
-    d = uw.Desc()
-    d.rows, d.cols = c.desc.rows, c.desc.cols
-    plan = uw.Plan(uw.STRATEGY_FUSED, variant, x.shape[0], 0.0)
-    ws = g.workspace(uw.workspace_size(d, x.shape[0], plan))
+    ws = g.workspace(uw.workspace_size_bf16(c.desc.rows, c.desc.cols, x.shape[0], variant))
     uw.matmul_bf16(c.w_dev, x, y, ws, variant)
 
 

@@ -77,3 +77,17 @@ def test_chain_argument_checks(uw, layer):
     # a load-time form must be 16-byte aligned
     mis, _ = mats(uw, layer, [uw.STRATEGY_PALETTE4] * 3, forms=[fake[1:]] * 3)
     assert fwd(mis, 1) == 1
+
+
+def test_chain_refuses_ragged_rows(uw):
+    # consistent shapes, but D = 100 is not a multiple of 64: the chain keeps
+    # whole groups (the single matmuls take ragged rows)
+    fake = np.zeros(64, np.uint8)
+    entries = []
+    for (rows, cols), seed in zip([(128, 100), (128, 100), (100, 128)], (1, 2, 3)):
+        blob = uw.compress(wl.normal_weights(rows, cols, 0.02, seed))
+        entries.append((uw.blob_info(blob), blob, None, None))
+    m = uw.mlp_matrices(entries)
+    L = uw.load()
+    assert L.uw_mlp_forward(m, 1, fake.ctypes.data, 4, fake.ctypes.data, None, fake.ctypes.data, 1 << 30,
+                            None, None) == 2         # UW_ERR_SHAPE

@@ -107,6 +107,31 @@ def test_blob_identical_to_oracle_gate_proj_shape(lib, oracle):
     assert lib.compress(w).tobytes() == oracle.compress(w)[0]
 
 
+RAGGED = [(1, 1), (3, 70), (33, 100), (40, 200), (2, 4097), (31, 127), (65, 14335)]
+
+
+@pytest.mark.parametrize("rows,cols", RAGGED)
+def test_blob_identical_to_oracle_ragged_rows(lib, oracle, rows, cols):
+    # rows of any length: filler to the next multiple of 64, true cols in the
+    # header, the true columns back from the oracle's decompression
+    for w in (wl.normal_weights(rows, cols, 0.02, seed=cols), wl.heavy_tailed_weights(rows, cols, seed=rows)):
+        ob, _ = oracle.compress(w)
+        assert lib.compress(w).tobytes() == ob
+        assert np.array_equal(oracle.decompress(ob), w)
+
+
+def test_blob_identical_to_oracle_ragged_with_escapes(lib, oracle):
+    # a rare exponent in the last, partial group of a row escapes that group
+    w = wl.normal_weights(40, 1000, 0.02, seed=5)
+    w[7, 999] = np.uint16(0x7F80)  # +inf: exponent 255
+    w[8, 970] = np.uint16(0x4000)  # 2.0: exponent 128
+    ob, info = oracle.compress(w)
+    assert info["n_palette"] == 16 and 255 not in info["palette"] and 128 not in info["palette"]
+    assert info["n_escaped"] >= 2
+    assert lib.compress(w).tobytes() == ob
+    assert np.array_equal(oracle.decompress(ob), w)
+
+
 @pytest.mark.parametrize("seed", range(12))
 def test_code_lengths_equal_oracle_on_skewed_histograms(lib, oracle, seed):
     # Random exponent histograms (through real matrices) exercise the code
@@ -125,11 +150,11 @@ def test_compress_rejects_bad_shapes(lib):
     L = lib.load()
     n = ctypes.c_size_t(0)
     w = np.zeros((4, 64), np.uint16)
-    assert L.uw_compress(w.ctypes.data, 4, 63, None, ctypes.byref(n)) == 2
     assert L.uw_compress(w.ctypes.data, 0, 64, None, ctypes.byref(n)) == 2
     assert L.uw_compress(w.ctypes.data, 4, 0, None, ctypes.byref(n)) == 2
     assert L.uw_compress(None, 4, 64, None, ctypes.byref(n)) == 1
     assert L.uw_compress(w.ctypes.data, 4, 64, None, ctypes.byref(n)) == 3 and n.value > 0
+    assert L.uw_compress(w.ctypes.data, 4, 63, None, ctypes.byref(n)) == 3 and n.value > 0  # ragged rows
     # beyond 2^31 rows or columns (checked before the data is read)
     assert L.uw_compress(w.ctypes.data, 1, (1 << 31) + 64, None, ctypes.byref(n)) == 7
     assert L.uw_compress(w.ctypes.data, (1 << 31) + 1, 64, None, ctypes.byref(n)) == 7

@@ -38,9 +38,10 @@ def _call(uw, desc, blob_dev, xd, yd):
 
 # (64, 4096, 4): two row blocks, so the default row kernel splits K and the
 # second call reuses arrival counters and partial sums the first one left;
-# (1024, 1024, 16): the tensor-core kernel.
+# (1024, 1024, 16): the tensor-core kernel; (96, 100, 1) and (33, 4097, 3):
+# ragged rows, whose zero-extended activations sit in the scratch too.
 @pytest.mark.parametrize("rows,cols,batch", [(1024, 1024, 1), (4096, 14336, 1), (300, 640, 5), (64, 4096, 4),
-                                             (1024, 1024, 16)])
+                                             (1024, 1024, 16), (96, 100, 1), (33, 4097, 3)])
 def test_noalloc_matches_workspace_entry_point_twice(g, uw, oracle, rows, cols, batch):
     w = wl.normal_weights(rows, cols, 0.02, seed=rows)
     x = wl.activations(batch, cols, seed=rows)
