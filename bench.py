@@ -187,7 +187,7 @@ def run_workloads(args):
         p4 = torch.empty(uw.palette4_bytes(m.desc), dtype=torch.uint8, device="cuda")
         ws0 = m.ws(1, None)
         uw.transcode_palette4(m.desc, m.dev, p4, ws0, stream)
-        cands = {1: [15, 16, 17, 23, 26], 16: [27, 31, 35, 38], 64: [31, 35, 38, 34], 256: [31, 35, 32, 33]}
+        cands = {1: [15, 16, 17, 23, 26], 16: [27, 28, 29], 64: [27, 28, 29], 256: [27, 28, 29]}
         strategies = [("decompress+gemm", uw.STRATEGY_DECOMPRESS_GEMM), ("exponent", uw.STRATEGY_EXPONENT),
                       ("palette4_runtime", uw.STRATEGY_PALETTE4), ("fused_huffman", uw.STRATEGY_FUSED)]
         rows = []

@@ -42,16 +42,15 @@ cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 //   15..26 column CTAs, batch 1 only (gemv_kg.cu): warps per CTA x grid
 //          size in full waves (1..4) of the GPU; the row blocks per CTA
 //          follow from the matrix and the SM count
-//   27..38 tensor-core CTAs (gemm_tc.cu): producer groups G (1, 2, 3) x K
-//          splits (1, 2, 4, 8, capped at the number of 64-column groups)
+//   27..29 tensor-core CTAs (gemm_tc.cu): producer groups G (2, 3, 4),
+//          stream-K over every SM
 constexpr int kWarpChoices[3] = {4, 8, 16};
 constexpr int kSplitChoices = 5;  // 1, 2, 4, 8, 16
 constexpr int kRowVariants = 3 * kSplitChoices;
 constexpr int kColWaves = 4;
 constexpr int kColVariants = 3 * kColWaves;
-constexpr int kTcGroups[3] = {1, 2, 3};
-constexpr int kTcSplitChoices = 4;  // 1, 2, 4, 8
-constexpr int kTcVariants = 3 * kTcSplitChoices;
+constexpr int kTcGroups[3] = {2, 3, 4};
+constexpr int kTcVariants = 3;
 constexpr int kTcFirst = kRowVariants + kColVariants;
 constexpr int kGemvVariants = kTcFirst + kTcVariants;
 constexpr int kMaxBatchChunk = 8;
@@ -70,11 +69,8 @@ GemvVariant gemv_variant(int v, int64_t rows, int64_t cols, uint32_t tbuf = kWor
     const int64_t gpr = cols / kGroup;
     if (v < kRowVariants)
         return {Kind::kRow, kWarpChoices[v % 3], 1 << (v / 3), 0};
-    if (v >= kTcFirst) {
-        const int i = v - kTcFirst;
-        const int64_t splits = std::min<int64_t>(int64_t(1) << (i % kTcSplitChoices), gpr);
-        return {Kind::kTensor, kTcGroups[i / kTcSplitChoices], int(splits), 0};
-    }
+    if (v >= kTcFirst)
+        return {Kind::kTensor, kTcGroups[v - kTcFirst], 1, 0};
     const int i = v - kRowVariants;
     const int w = kWarpChoices[i % 3];
     const int waves = 1 + i / 3;
@@ -91,41 +87,18 @@ GemvVariant gemv_variant(int v, int64_t rows, int64_t cols, uint32_t tbuf = kWor
 // Tile data bytes assumed for a Huffman blob that is not at hand.
 constexpr uint32_t kWorstTileData = kWorstTileBuf - kTileSlack;
 
-// Tensor-core default.  Producer groups: the most whose x stages fit for
-// this weight source (the kernel needs two K steps per group in flight).
-// K split: the one with the least estimated time, waves of the grid times
-// a CTA's cost in K columns: a fixed part (tables, tensor memory, the first
-// codes' round trips: ~900 columns' worth, ~10 us, fitted to one against four
-// splits at batch 16), the K columns it decodes, and with a split the
-// partial sums it writes and the last CTA reads back (np rows x 128 fp32,
-// weighted like six K columns per batch row, fitted to the splits the chain
-// tuner picks on the MLP shapes); ties (within 2%) go to fewer splits.  This
-// keeps one split for 14336 x 4096 and splits 4096 x 14336 four ways, whose
-// 32 row blocks would fill a fifth of the GPU.
-// The result does not depend on the number of groups (the MMAs accumulate
-// in K order), so the source only changes the speed.
+// Tensor-core default: the most producer groups (decode throughput) whose
+// stages fit this weight source and batch.  The result does not depend on
+// the number of groups (the MMAs accumulate in K order over the same
+// stream-K cut), so the source only changes the speed.
 int default_tc_variant(int64_t rows, int64_t cols, int64_t batch, int src, uint32_t tdata) {
-    const int64_t np = std::min<int64_t>((batch + 15) / 16 * 16, kTcMaxBatch);
-    int gi = 0;
-    for (int i = 2; i > 0; i--)
-        if (gemm_tc_stages(kTcGroups[i], int(np), src, tdata) >= 2 * kTcGroups[i]) {
-            gi = i;
-            break;
-        }
-    const int64_t mblocks = (rows + 127) / 128, gpr = cols / kGroup, sms = sm_count();
-    int best = 0;
-    double best_cost = 0.0;
-    for (int si = 0; si < kTcSplitChoices; si++) {
-        const int64_t sp = std::min<int64_t>(int64_t(1) << si, gpr);
-        const int64_t waves = (mblocks * sp + sms - 1) / sms;
-        const double k = double(cols) / double(sp);
-        const double cost = double(waves) * (900.0 + k + (sp > 1 ? 6.0 * double(np) : 0.0));
-        if (si == 0 || cost < best_cost * 0.98) {
-            best_cost = cost;
-            best = si;
-        }
-    }
-    return kTcFirst + gi * kTcSplitChoices + best;
+    (void)rows;
+    (void)cols;
+    const int np = int(std::min<int64_t>((batch + 15) / 16 * 16, kTcMaxBatch));
+    for (int i = kTcVariants - 1; i > 0; i--)
+        if (gemm_tc_fits(kTcGroups[i], np, src, tdata))
+            return kTcFirst + i;
+    return kTcFirst;
 }
 
 int pad_batch(int64_t b) {
@@ -165,7 +138,7 @@ WsLayout layout_for(int64_t rows, int64_t cols_true, int64_t batch, int strategy
     const GemvVariant gv = gemv_variant(variant, rows, cols);
     const int bp = gv.kind == Kind::kColumn ? 1 : pad_batch(batch);
     const uint64_t partial_floats = gv.kind == Kind::kTensor
-                                        ? uint64_t(gemm_tc_partial_floats(rows, batch, gv.splits))
+                                        ? uint64_t(gemm_tc_partial_floats(rows, cols, batch))
                                         : uint64_t(nrb) * gv.splits * bp * 32;
     L.status = 0;
     L.counters = 256;
@@ -243,7 +216,7 @@ uw_status pad_x(GemvParams &p, const uint16_t *x, int64_t cols_true, uint8_t *ds
 // Batch rows go through the CUDA-core row kernels in chunks of at most 8;
 // the column kernels take batch 1 only; the tensor-core kernels take any
 // batch (chunks of 256 inside the launcher).
-uw_status run_gemv(GemvParams p, int variant, int src, cudaStream_t stream) {
+uw_status run_gemv(GemvParams p, int variant, int src, cudaStream_t stream, int max_ctas = 0) {
     const bool compressed = src == kSrcHuffman;
     const GemvVariant gv = gemv_variant(variant, p.rows, p.cols, compressed ? p.v.tbuf : kWorstTileBuf, src);
     if (gv.kind == Kind::kTensor) {
@@ -259,8 +232,7 @@ uw_status run_gemv(GemvParams p, int variant, int src, cudaStream_t stream) {
         t.rows = p.rows;
         t.cols = p.cols;
         t.batch = p.batch;
-        t.splits = gv.splits;
-        return launch_gemm_tc(t, gv.warps, src, stream);
+        return launch_gemm_tc(t, gv.warps, src, stream, max_ctas);
     }
     if (gv.kind == Kind::kColumn) {
         if (p.batch != 1)
@@ -298,8 +270,8 @@ WsLayout run_layout(int64_t rows, int64_t cols, int64_t batch, int variant) {
     return layout_for(rows, cols, batch, UW_STRATEGY_FUSED, variant);
 }
 
-uw_status run_matmul(const GemvParams &p, int variant, int src, cudaStream_t stream) {
-    return run_gemv(p, variant, src, stream);
+uw_status run_matmul(const GemvParams &p, int variant, int src, cudaStream_t stream, int max_ctas) {
+    return run_gemv(p, variant, src, stream, max_ctas);
 }
 
 bool ensure_smem_limit(const void *kernel, size_t bytes) {
@@ -759,8 +731,7 @@ extern "C" const char *uw_variant_name(int32_t strategy, int32_t variant) {
         "w4s8", "w8s8", "w16s8", "w4s16", "w8s16", "w16s16",
         "col_w4x1", "col_w8x1", "col_w16x1", "col_w4x2", "col_w8x2", "col_w16x2",
         "col_w4x3", "col_w8x3", "col_w16x3", "col_w4x4", "col_w8x4", "col_w16x4",
-        "tc_g1s1", "tc_g1s2", "tc_g1s4", "tc_g1s8", "tc_g2s1", "tc_g2s2", "tc_g2s4", "tc_g2s8",
-        "tc_g3s1", "tc_g3s2", "tc_g3s4", "tc_g3s8"};
+        "tc_g2", "tc_g3", "tc_g4"};
     if (uw_variant_count(strategy) == 0 || variant < 0 || variant >= kGemvVariants)
         return nullptr;
     return names[variant];

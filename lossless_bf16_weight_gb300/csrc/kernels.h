@@ -47,9 +47,9 @@ uw_status launch_gemv(const GemvParams &p, int warps, int bp, bool compressed, c
 size_t gemv_kg_smem_bytes(int warps, int rb_per_cta, bool compressed, uint32_t tdata, int gpr);
 uw_status launch_gemv_kg(const GemvParams &p, int warps, int rb_per_cta, int src, cudaStream_t stream);
 
-// Tensor-core matmul (gemm_tc.cu): CTAs of 4G producer warps + 1 MMA warp,
-// 128 rows of W each, `splits` K ranges; batches above kTcMaxBatch run as
-// several launches.
+// Tensor-core matmul (gemm_tc.cu): persistent CTAs of 4G producer warps, an
+// MMA warp and an x loader, stream-K over (128-row block, 64-column group)
+// units on every SM; batches above kTcMaxBatch run as several launches.
 constexpr int kTcMaxBatch = 256;
 struct TcParams {
     BlobView v;            // compressed weights (fused kernel)
@@ -57,22 +57,24 @@ struct TcParams {
     const uint8_t *p4;     // palette-4 indices or exponent bytes (sign+mantissa etc. from v)
     const uint16_t *x;     // [batch, cols]
     uint16_t *y;           // [batch, rows]
-    float *partial;        // [row blocks of 128][splits][Np][128] split partial sums
-    uint32_t *counters;    // [row blocks of 128] arrival counters, left at zero
+    float *partial;        // [128-row blocks][maxseg][Np][128] segment partial sums
+    uint32_t *counters;    // [128-row blocks] arrival counters, left at zero
     uint32_t *status;      // device error word
     int64_t rows, cols, batch;
-    int splits;
-    int S, Np;             // stages, padded batch (set by the launcher)
-    uint32_t tmem_cols;    // tensor-memory columns allocated (set by the launcher)
-    uint32_t a0col;        // first tensor-memory column of the A stages (set by the launcher)
-    CUtensorMap xmap;      // x as a 2-D tensor (cols x batch rows), 64 x Np boxes, 128-byte
-                           // swizzle (set by the launcher)
+    // set by the launcher
+    uint32_t T, V, nk, maxseg;  // units, workers, K steps per block, segments per block at most
+    int SX, Np;            // x stages (shared memory), padded batch
+    uint32_t a0col;        // first tensor-memory column of the A stages
+    CUtensorMap xmap;      // x as a 2-D tensor (cols x batch rows), 64 x Np boxes, 128-byte swizzle
+    CUtensorMap wmap;      // uncompressed W (cols x rows), 64 x 128 boxes, 128-byte swizzle
 };
-// x stages the tensor-core kernel can keep with G producer groups, batch
-// rows Np, weights from `src` (tile data bytes tdata for the Huffman source).
-int gemm_tc_stages(int G, int Np, int src, uint32_t tdata);
-int64_t gemm_tc_partial_floats(int64_t rows, int64_t batch, int splits);
-uw_status launch_gemm_tc(const TcParams &p, int G, int src, cudaStream_t stream);
+// Whether G producer groups, batch rows Np and weights from `src` (tile
+// data bytes tdata for the Huffman source) fit one CTA.
+bool gemm_tc_fits(int G, int Np, int src, uint32_t tdata);
+// Workspace floats of the segment partials.
+int64_t gemm_tc_partial_floats(int64_t rows, int64_t cols, int64_t batch);
+// max_ctas > 0: launch at most that many CTAs (the result does not change).
+uw_status launch_gemm_tc(const TcParams &p, int G, int src, cudaStream_t stream, int max_ctas = 0);
 // W [rows, cols] BF16 as a tensor map of 32-row x 64-column tiles, 128-byte
 // swizzle (the batch-1 uncompressed GEMV's stages).
 bool encode_w_tile_map(CUtensorMap *m, const uint16_t *w, int64_t rows, int64_t cols);
@@ -152,6 +154,6 @@ struct WsLayout {
 //                      run_layout says, p.w / p.p4 / p.v by `src`.
 uw_status plan_resolve(const uw_plan *plan, const uw_desc &d, int64_t batch, int *strategy, int *variant);
 WsLayout run_layout(int64_t rows, int64_t cols, int64_t batch, int variant);
-uw_status run_matmul(const GemvParams &p, int variant, int src, cudaStream_t stream);
+uw_status run_matmul(const GemvParams &p, int variant, int src, cudaStream_t stream, int max_ctas = 0);
 
 }  // namespace uw

@@ -54,53 +54,10 @@ __device__ __forceinline__ uint32_t pair_offsets_shift(uint32_t o) { return __sh
 // shared memory next to the stage so that the loop body is not duplicated).
 struct PairMeta {
     uint32_t pkA, pkB;   // n16 | nesc << 8 | bad << 16 of each tile
-    uint32_t n16A, n16B, nescA, pad[3];
+    uint32_t n16A, n16B, nescA;
+    uint32_t R;          // rows of the pair's tiles | 0x100 when tile B is present (0: no pair)
+    uint32_t sm_lo, sm_hi;  // address of the pair's sign+mantissa bytes (tile A's; B's follow 64 * R later)
 };
-
-// Validate the pair's offsets `o` and start its bulk copies into stage `st`:
-//   [0, 64)                      glen of A and B (full row blocks only)
-//   [64, 64 + 2*tdata)           code regions of A then B, then escaped exponents of A then B
-//   [smoff, smoff + 128*R)       sign+mantissa bytes of A then B
-// A pair with bad offsets copies no codes and is decoded as zeros (the error
-// is recorded by tile_begin).
-__device__ __forceinline__ void pair_issue(const BlobView &v, uint32_t o, uint32_t rb, uint32_t kgA, bool hasB,
-                                           uint32_t t, uint32_t st, uint32_t smoff, uint32_t bar, PairMeta *meta) {
-    const int lane = threadIdx.x & 31;
-    const uint32_t c0 = __shfl_sync(0xffffffffu, o, 0), c1 = __shfl_sync(0xffffffffu, o, 1);
-    const uint32_t c2r = __shfl_sync(0xffffffffu, o, 2), e0 = __shfl_sync(0xffffffffu, o, 3);
-    const uint32_t e1 = __shfl_sync(0xffffffffu, o, 4), e2r = __shfl_sync(0xffffffffu, o, 5);
-    const uint32_t c2 = hasB ? c2r : c1, e2 = hasB ? e2r : e1;
-    const bool full = rb < v.nfull;
-    const uint32_t R = full ? uint32_t(kTileRows) : v.tail_rows;
-    const uint32_t n16A = c1 - c0, n16B = c2 - c1, nescA = e1 - e0, nescB = e2 - e1;
-    const uint32_t lim16 = uint32_t(kMaxTileCodeBytes / 16);
-    const bool bad = n16A > lim16 || n16B > lim16 || nescA > R || nescB > R || n16A * 16u + nescA * 64u > v.tdata ||
-                     n16B * 16u + nescB * 64u > v.tdata || c2 > v.code16 || e2 > v.n_esc32;
-    if (lane == 0) {
-        meta->pkA = bad ? (1u << 16) : (n16A | (nescA << 8));
-        meta->pkB = !hasB ? 0u : bad ? (1u << 16) : (n16B | (nescB << 8));
-        meta->n16A = bad ? 0u : n16A;
-        meta->n16B = bad ? 0u : n16B;
-        meta->nescA = bad ? 0u : nescA;
-    }
-    const uint32_t ntile = hasB ? 2u : 1u;
-    const uint64_t q0 = uint64_t(t) * kTileRows - (full ? 0u : (kTileRows - R) * kgA);  // first group of A
-    const uint32_t code_bytes = bad ? 0u : (c2 - c0) * 16u;
-    const uint32_t esc_bytes = bad ? 0u : (e2 - e0) * 64u;
-    const uint32_t sm_bytes = uint32_t(kGroup) * R * ntile;
-    const uint32_t glen_bytes = full ? uint32_t(kTileRows) * ntile : 0u;
-    if (lane == 0) {
-        mbar_expect_tx(bar, code_bytes + esc_bytes + sm_bytes + glen_bytes);
-        if (glen_bytes)
-            bulk_g2s(st, v.glen + q0, glen_bytes, bar);
-        if (code_bytes)
-            bulk_g2s(st + 64u, v.code + size_t(c0) * 16, code_bytes, bar);
-        if (esc_bytes)
-            bulk_g2s(st + 64u + code_bytes, v.esc + size_t(e0) * 64, esc_bytes, bar);
-        bulk_g2s(st + smoff, v.sm + q0 * kGroup, sm_bytes, bar);
-    }
-}
-
 
 // Code stage of a pair without its sign+mantissa bytes:
 //   [0, 64)                      glen of A and B (full row blocks only)
@@ -120,8 +77,13 @@ __device__ __forceinline__ const uint8_t *pair_sm_base(const BlobView &v, uint32
     return v.sm + q0 * kGroup;
 }
 
-// pair_issue without the sign+mantissa bytes (the caller reads those from
-// global memory), plus an L2 prefetch of them.
+// Validate the pair's offsets `o` (pair_offsets_load) and start its bulk
+// copies into stage `st`:
+//   [0, 64)                      glen of A and B (full row blocks only)
+//   [64, 64 + 2*tdata)           code regions of A then B, then escaped exponents of A then B
+// plus an L2 prefetch of the pair's sign+mantissa bytes, which the caller
+// reads from global memory.  A pair with bad offsets copies no codes and is
+// decoded as zeros (the error is recorded when it is decoded).
 __device__ __forceinline__ void pair_issue_codes(const BlobView &v, uint32_t o, uint32_t rb, uint32_t kgA, bool hasB,
                                                  uint32_t t, uint32_t st, uint32_t bar, PairMeta *meta) {
     const int lane = threadIdx.x & 31;
@@ -147,6 +109,9 @@ __device__ __forceinline__ void pair_issue_codes(const BlobView &v, uint32_t o, 
         meta->n16A = bad ? 0u : n16A;
         meta->n16B = bad ? 0u : n16B;
         meta->nescA = bad ? 0u : nescA;
+        meta->R = R | (hasB ? 0x100u : 0u);
+        meta->sm_lo = uint32_t(reinterpret_cast<uint64_t>(sm));
+        meta->sm_hi = uint32_t(reinterpret_cast<uint64_t>(sm) >> 32);
         mbar_expect_tx(bar, code_bytes + esc_bytes + glen_bytes);
         if (glen_bytes)
             bulk_g2s(st, v.glen + q0, glen_bytes, bar);

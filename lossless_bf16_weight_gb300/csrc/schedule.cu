@@ -250,7 +250,10 @@ uw_status run_chain(const uw_mlp_matrix *m, int32_t n_layers, const uint16_t *x,
         } else if (stp.src == kSrcPalette4) {
             p.p4 = static_cast<const uint8_t *>(m[i].form_dev);
         }
-        if ((e = run_matmul(p, stp.variant, stp.src, st)) != UW_OK)
+        // beside a capped preprocess kernel, the persistent tensor-core CTAs
+        // leave it its SMs (the sums do not depend on the CTA count)
+        const int mm_cap = conc && sch.dec_ctas > 0 && sch.dec_ctas < sm_count() ? sm_count() - sch.dec_ctas : 0;
+        if ((e = run_matmul(p, stp.variant, stp.src, st, mm_cap)) != UW_OK)
             return e;
         if (stp.pre >= 0) {
             if (conc && (e = cuda_ok(cudaEventRecord(freed[h % S], st))) != UW_OK)
@@ -280,8 +283,7 @@ uw_status run_chain(const uw_mlp_matrix *m, int32_t n_layers, const uint16_t *x,
     return s;
 }
 
-// Tensor-core variants with two or three producer groups (any K split;
-// split 1 leaves SMs to a preprocess kernel beside the matmul), by name.
+// Tensor-core variants with two or three producer groups, by name.
 std::vector<int> tc_variants() {
     std::vector<int> out;
     const int n = uw_variant_count(UW_STRATEGY_FUSED);

@@ -61,9 +61,9 @@ def test_fixed_plan_names_a_variant():
     plan = bench.fixed_plan(uw, "fused:col_w16x1")
     assert plan.strategy == uw.STRATEGY_FUSED
     assert uw.variant_name(uw.STRATEGY_FUSED, plan.variant) == "col_w16x1"
-    plan = bench.fixed_plan(uw, "exponent:tc_g3s1")
+    plan = bench.fixed_plan(uw, "exponent:tc_g3")
     assert plan.strategy == uw.STRATEGY_EXPONENT
-    assert uw.variant_name(uw.STRATEGY_EXPONENT, plan.variant) == "tc_g3s1"
+    assert uw.variant_name(uw.STRATEGY_EXPONENT, plan.variant) == "tc_g3"
 
 
 def test_fixed_plan_rejects_an_unknown_variant():

@@ -89,8 +89,8 @@ def _twin(g, uw, c, x, y, variant):
 # variant of each strategy at each batch (the twin runs the same variant)
 VARIANTS = {
     1: {"fused": "col_w16x1", "palette4": "col_w16x1", "exponent": "col_w16x1", "decompress": "col_w16x1"},
-    4: {"fused": "w8s1", "palette4": "tc_g1s1", "exponent": "tc_g1s1", "decompress": "w8s1"},
-    32: {"fused": "tc_g2s1", "palette4": "tc_g1s2", "exponent": "tc_g3s1", "decompress": "tc_g2s2"},
+    4: {"fused": "w8s1", "palette4": "tc_g2", "exponent": "tc_g2", "decompress": "w8s1"},
+    32: {"fused": "tc_g2", "palette4": "tc_g3", "exponent": "tc_g3", "decompress": "tc_g4"},
 }
 STRATEGY = {"fused": 1, "palette4": 2, "exponent": 3, "decompress": 0}
 
@@ -243,7 +243,7 @@ def test_chain_model_shapes_batch256(g, uw):
     entries, variants = [], []
     for l, L in enumerate(big):
         for c, role in zip(L.mats, roles(l)):
-            v = vid(uw, "tc_g2s1")
+            v = vid(uw, "tc_g2")
             entries.append((c.desc, c.blob_dev, None, uw.Plan(STRATEGY[role], v, batch, 0.0)))
             variants.append(v)
     mats = uw.mlp_matrices(entries)

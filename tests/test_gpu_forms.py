@@ -18,7 +18,7 @@ import workloads as wl
 pytestmark = pytest.mark.gpu
 
 COL_VARIANTS = list(range(15, 27))   # col_w{4,8,16}x{1..4}
-TC_VARIANTS = list(range(27, 39))    # tc_g{1,2,3}s{1,2,4,8}
+TC_VARIANTS = list(range(27, 30))    # tc_g2, tc_g3, tc_g4
 UNSUPPORTED = 7
 
 
@@ -122,7 +122,7 @@ def test_gate_proj_full_size(g, uw, oracle, gate, batch, form):
 def test_strategy_palette4_equals_fused(g, uw):
     w = wl.heavy_tailed_weights(640, 2048, seed=3)
     c = g.Compressed(w)
-    for batch, variant in ((1, 17), (16, 35), (48, 31)):
+    for batch, variant in ((1, 17), (16, 28), (48, 27)):
         xd = g.dev_bits(wl.activations(batch, 2048, seed=batch))
         fused = c.matmul(xd, uw.Plan(uw.STRATEGY_FUSED, variant, batch, 0.0))
         for strategy in (uw.STRATEGY_PALETTE4, uw.STRATEGY_EXPONENT):
@@ -172,7 +172,7 @@ def test_degenerate_matrices(g, uw, oracle, name, form):
     assert np.array_equal(fdev.cpu().numpy(), _oracle_form(oracle, c, form))
     wd = g.dev_bits(w)
     call = uw.matmul_palette4_status if form == "palette4" else uw.matmul_exponents_status
-    for batch, variant in ((1, 17), (16, 35)):
+    for batch, variant in ((1, 17), (16, 28)):
         x = wl.activations(batch, w.shape[1], seed=batch)
         xd = g.dev_bits(x)
         ws = c.ws(batch, uw.Plan(uw.STRATEGY_FUSED, variant, batch, 0.0))

@@ -17,7 +17,7 @@ import workloads as wl
 pytestmark = pytest.mark.gpu
 
 SHAPES = [(96, 100), (64, 4097), (33, 14335), (40, 200), (1, 1), (31, 127), (300, 4104)]
-COL_W16X1, TC = 17, (27, 32, 37)   # col_w16x1, tc_g1s1 / tc_g2s2 / tc_g3s4
+COL_W16X1, TC = 17, (27, 28, 29)   # col_w16x1, tc_g2 / tc_g3 / tc_g4
 ROW = (1, 4, 7, 10, 13)            # w8s1 .. w8s16: K split 1 to 16 ways (long rows need the splits)
 UNSUPPORTED = 7                    # UW_ERR_UNSUPPORTED: the variant does not fit this shape
 
