@@ -776,9 +776,17 @@ def _time_steps(torch, fn, steps, stream, copies):
     return e0.elapsed_time(e1) / steps * 1e3  # microseconds per step
 
 
+def variant_id(uw, name):
+    for v in range(uw.variant_count(uw.STRATEGY_FUSED)):
+        if uw.variant_name(uw.STRATEGY_FUSED, v) == name:
+            return v
+    raise SystemExit("no variant " + name)
+
+
 def context_measurements(torch, uw, w, x, desc, blobs, xd, stream, plan):
     """Same library's uncompressed GEMV, the decompress-then-GEMV strategy
     and cuBLAS (torch.matmul) on the same shape, each from HBM."""
+    import workloads as wl
     out = {}
     steps = 2000
     bf16_bytes = 2 * ROWS * COLS
@@ -832,7 +840,30 @@ def context_measurements(torch, uw, w, x, desc, blobs, xd, stream, plan):
                                                   "CUDA events on the launching stream",
                            "fused_us": round(us_f, 3), "uncompressed_us": round(us, 3), "cublas_us": round(us_c, 3),
                            "fused_GBps_compressed": round(desc.blob_bytes / us_f / 1e3, 1)}
+    # the tensor-core path on the same matrix: the default plan at batch 16 and 256, the same
+    # variant on the uncompressed weights, and cuBLAS, in the same harness
+    tc = {}
+    for b in (16, 256):
+        xb_dev = torch.from_numpy(wl.activations(b, COLS, seed=b).view(np.int16)).cuda()
+        yb = torch.empty(b, ROWS, dtype=torch.int16, device="cuda")
+        v = variant_id(uw, "tc_g2" if b <= 64 else "tc_g3")  # the library's default at this batch
+        pl = uw.Plan(uw.STRATEGY_FUSED, v, b, 0.0)
+        wsb = torch.empty(uw.workspace_size(desc, b, pl), dtype=torch.uint8, device="cuda")
+        uw.workspace_init(wsb, stream)
+        us_tf = _time_steps(torch, lambda i: uw.matmul(desc, blobs[i % len(blobs)], xb_dev, yb, wsb, pl, stream), 500,
+                            stream, len(blobs))
+        wst = torch.empty(uw.workspace_size_bf16(ROWS, COLS, b, v), dtype=torch.uint8, device="cuda")
+        uw.workspace_init(wst, stream)
+        us_tt = _time_steps(torch, lambda i: uw.matmul_bf16(wdev[i % wcopies], xb_dev, yb, wst, v, stream), 500,
+                            stream, wcopies)
+        xbb = xb_dev.view(torch.bfloat16)
+        us_tc = _time_steps(torch, lambda i: torch.matmul(xbb, wb[i % wcopies].t()), 500, stream, wcopies)
+        tc["batch%d" % b] = {"variant": uw.variant_name(1, v), "fused_us": round(us_tf, 3),
+                             "uncompressed_us": round(us_tt, 3), "cublas_us": round(us_tc, 3),
+                             "tflops_uncompressed": round(2.0 * b * ROWS * COLS / us_tt / 1e6, 1)}
+    out["tensor_cores"] = tc
     return out
+
 
 
 def e2e_measurement(torch, uw, desc, blobs, x, stream, plan, args):

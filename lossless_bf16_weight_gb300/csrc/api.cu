@@ -87,15 +87,18 @@ GemvVariant gemv_variant(int v, int64_t rows, int64_t cols, uint32_t tbuf = kWor
 // Tile data bytes assumed for a Huffman blob that is not at hand.
 constexpr uint32_t kWorstTileData = kWorstTileBuf - kTileSlack;
 
-// Tensor-core default: the most producer groups (decode throughput) whose
-// stages fit this weight source and batch.  The result does not depend on
-// the number of groups (the MMAs accumulate in K order over the same
-// stream-K cut), so the source only changes the speed.
+// Tensor-core default: two producer groups up to 64 batch rows, three above
+// (measured on the gate matrix: the fastest within 3% at 16..256 rows; four
+// groups leave the producers 96 registers and spill), when their stages fit
+// this weight source.  The result does not depend on the number of groups
+// (the MMAs accumulate in K order over the same cut), so the choice only
+// changes the speed.
 int default_tc_variant(int64_t rows, int64_t cols, int64_t batch, int src, uint32_t tdata) {
     (void)rows;
     (void)cols;
     const int np = int(std::min<int64_t>((batch + 15) / 16 * 16, kTcMaxBatch));
-    for (int i = kTcVariants - 1; i > 0; i--)
+    const int want = np <= 64 ? 0 : 1;  // index into kTcGroups
+    for (int i = want; i >= 0; i--)
         if (gemm_tc_fits(kTcGroups[i], np, src, tdata))
             return kTcFirst + i;
     return kTcFirst;
