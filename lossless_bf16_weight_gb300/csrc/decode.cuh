@@ -85,6 +85,7 @@ struct BlobView {
 constexpr int kWindowBits = 2 * kLmax;                     // two codes always fit
 constexpr int kLutEntries = 1 << kWindowBits;              // 1024
 constexpr int kPrivateLutBytes = kLutEntries * 32 * 4;     // 32 lane-private copies: 128 KB
+constexpr int kHalfLutBytes = kLutEntries * 16 * 4;        // 16 copies (lanes l, l + 16 share one): 64 KB
 constexpr int kZeroWords = 32;                             // zero stream for lanes without codes
 // One tile's shared buffer: its code region, then the raw exponent bytes of
 // its escaped groups ((32 - e) * 48 + 64 * e <= 2048 bytes), then read
@@ -175,8 +176,19 @@ __device__ __forceinline__ void replicate_private(const DecodeShared &s, uint32_
     }
 }
 
+// The same with 16 copies (entry w of copy c at word 16w + c), read by
+// lane l from copy l % 16: a lookup is one or two wavefronts (lanes l and
+// l + 16 meet in a bank when their entries' parities agree).
+__device__ __forceinline__ void replicate_half(const DecodeShared &s, uint32_t tab) {
+    for (int i = threadIdx.x; i < kLutEntries * 4; i += blockDim.x) {
+        const uint32_t e = s.lut[uint32_t(i) >> 2];
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" :: "r"(tab + 16u * uint32_t(i)), "r"(e) : "memory");
+    }
+}
+
 constexpr int kStrideShared = 4;    // bytes between entries of one table
 constexpr int kStridePrivate = 128; // bytes between rows of 32 lane-private copies
+constexpr int kStrideHalf = 64;     // bytes between rows of 16 copies shared by lanes l and l + 16
 
 // PTX prmt in its generic mode: a selector nibble with bit 3 set fills the
 // target byte with the sign bit of the selected byte.

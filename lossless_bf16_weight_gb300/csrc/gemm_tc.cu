@@ -264,19 +264,21 @@ __device__ __forceinline__ void fixup_block(const TcParams &p, uint32_t mb, uint
     }
 }
 
-// kPrivate (Huffman source): the pair table as 32 lane-private copies, every
-// lookup one shared-memory wavefront, as in the batch-1 GEMV; taken when it
-// fits beside the x stages (batches up to ~64).
-template <int G, int kSrc, bool kPrivate>
+// kTab (Huffman source): the pair table as 32 lane-private copies (2: every
+// lookup one shared-memory wavefront, as in the batch-1 GEMV; fits beside
+// the x stages up to batch ~64), as 16 copies shared by lane pairs (1: one or
+// two wavefronts, 64 KB; wider batches) or as one table (0).
+template <int G, int kSrc, int kTab>
 __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
     constexpr int P = 4 * G;  // producer warps
     constexpr bool kCompressed = kSrc == kSrcHuffman;
     constexpr bool kP4 = kSrc == kSrcPalette4;
     constexpr bool kExp = kSrc == kSrcExponent;
     constexpr bool kTma = kSrc == kSrcBf16;  // A tiles by tensor-map copies into the x stages
-    static_assert(!kPrivate || kCompressed, "private tables: Huffman source");
+    static_assert(kTab == 0 || kCompressed, "table copies: Huffman source");
     static_assert(P <= kMaxProducers, "producer warps");
-    constexpr int kStride = kPrivate ? kStridePrivate : kStrideShared;
+    constexpr int kStride = kTab == 2 ? kStridePrivate : kTab == 1 ? kStrideHalf : kStrideShared;
+    constexpr size_t kTabBytes = kTab == 2 ? kPrivateLutBytes : kTab == 1 ? kHalfLutBytes : 0;
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bars[2 * kStagesA + 2 * kMaxX + 2];
     __shared__ __align__(8) uint64_t pbars[P * kPairStages];
@@ -294,13 +296,13 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
     const uint32_t xstage = abytes + xbytes;
     const uint32_t a0col = p.a0col;  // first tensor-memory column of the A stages
 
-    // shared memory: [pad to 1024][x stages][private tables (kPrivate)][decode
+    // shared memory: [pad to 1024][x stages][table copies (kTab)][decode
     // tables, or the palette-4 pair table][per producer warp kPairStages code stages]
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
     const uint32_t xs0 = raw + pad;
     const uint32_t priv = xs0 + uint32_t(SX) * xstage;
-    unsigned char *dec = smem_raw + pad + size_t(SX) * xstage + (kPrivate ? size_t(kPrivateLutBytes) : 0);
+    unsigned char *dec = smem_raw + pad + size_t(SX) * xstage + kTabBytes;
     const uint32_t sbytes = code_stage_bytes(v.tdata);
     const uint32_t pst0 = (smem_addr(dec + kCommonSmemBytes) + 127u) & ~127u;
     const uint32_t afull0 = smem_addr(&bars[0]), aempty0 = smem_addr(&bars[kStagesA]);
@@ -384,9 +386,12 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
                 o_next = pair_offsets_load(v, walk_tile(iss));
         }
     }
-    if constexpr (kPrivate) {
+    if constexpr (kTab != 0) {
         __syncthreads();
-        replicate_private(ds, priv);
+        if constexpr (kTab == 2)
+            replicate_private(ds, priv);
+        else
+            replicate_half(ds, priv);
     }
     tc_fence_before();
     __syncthreads();
@@ -397,7 +402,10 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
     grid_dep_launch();
     grid_dep_wait();  // x (and the uncompressed weights) may come from the kernel before; the partials are reused
     const uint32_t tmem = tmem_slot;
-    const uint32_t lut = !kCompressed ? 0u : kPrivate ? priv + 4u * uint32_t(lane) : smem_addr(ds.lut);
+    const uint32_t lut = !kCompressed ? 0u
+                         : kTab == 2  ? priv + 4u * uint32_t(lane)
+                         : kTab == 1  ? priv + 4u * uint32_t(lane & 15)
+                                      : smem_addr(ds.lut);
 
     if (producer) {
         const uint32_t trow = tmem + (uint32_t(32 * q) << 16) + a0col;
@@ -751,9 +759,9 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
         tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int G, int kSrc, bool kPrivate>
+template <int G, int kSrc, int kTab>
 uw_status launch_tc_one(const TcParams &p, size_t smem, int grid, cudaStream_t stream) {
-    auto kern = gemm_tc_kernel<G, kSrc, kPrivate>;
+    auto kern = gemm_tc_kernel<G, kSrc, kTab>;
     if (!ensure_smem(kern, smem))
         return UW_ERR_CUDA;
     return launch_overlapped(kern, dim3(unsigned(grid)), dim3((4 * G + 2) * 32), smem, stream, p) == cudaSuccess
@@ -761,24 +769,24 @@ uw_status launch_tc_one(const TcParams &p, size_t smem, int grid, cudaStream_t s
                : UW_ERR_CUDA;
 }
 
-template <int kSrc, bool kPrivate = false>
+template <int kSrc, int kTab = 0>
 uw_status launch_tc_g(const TcParams &p, int G, size_t smem, int grid, cudaStream_t stream) {
     if constexpr (kSrc == kSrcBf16)  // no producers: the warps that would be run the epilogue
-        return launch_tc_one<3, kSrc, false>(p, smem, grid, stream);
+        return launch_tc_one<3, kSrc, 0>(p, smem, grid, stream);
     else
-        return G == 2 ? launch_tc_one<2, kSrc, kPrivate>(p, smem, grid, stream)
-               : G == 3 ? launch_tc_one<3, kSrc, kPrivate>(p, smem, grid, stream)
-                        : launch_tc_one<4, kSrc, kPrivate>(p, smem, grid, stream);
+        return G == 2 ? launch_tc_one<2, kSrc, kTab>(p, smem, grid, stream)
+               : G == 3 ? launch_tc_one<3, kSrc, kTab>(p, smem, grid, stream)
+                        : launch_tc_one<4, kSrc, kTab>(p, smem, grid, stream);
 }
 
 // Tensor-memory columns before the A stages (the accumulator's Np, rounded up to 32).
 uint32_t a0_col(int Np) { return (uint32_t(Np) + 31u) & ~31u; }
 
-// Shared memory of a launch with SX x stages; `priv`: 32 lane-private
-// copies of the pair table (Huffman source).
-size_t tc_smem(int G, int SX, int Np, int src, uint32_t tdata, bool priv) {
+// Shared memory of a launch with SX x stages; `tab`: copies of the pair
+// table (Huffman source: 2 = 32 lane-private, 1 = 16, 0 = one table).
+size_t tc_smem(int G, int SX, int Np, int src, uint32_t tdata, int tab) {
     const size_t stage = size_t(Np) * 128 + (src == kSrcBf16 ? size_t(kTcM) * 128 : 0);  // [A tile][x rows]
-    size_t s = 1024 + size_t(SX) * stage + (priv ? size_t(kPrivateLutBytes) : 0);
+    size_t s = 1024 + size_t(SX) * stage + (tab == 2 ? size_t(kPrivateLutBytes) : tab == 1 ? size_t(kHalfLutBytes) : 0);
     if (src == kSrcHuffman)
         s += size_t(kCommonSmemBytes) + 128 + size_t(4 * G) * kPairStages * code_stage_bytes(tdata);
     else if (src == kSrcPalette4)
@@ -788,28 +796,27 @@ size_t tc_smem(int G, int SX, int Np, int src, uint32_t tdata, bool priv) {
 
 struct TcConfig {
     int SX;
-    bool priv;
+    int tab;  // table copies (Huffman source)
     size_t smem;
 };
 
 // Stages for G producer groups and Np batch rows: A stages in the tensor
 // memory the accumulator leaves; x stages in shared memory (with the A tile
-// for the uncompressed source), the most that fit up to kMaxX (lane-private
-// tables first for the Huffman source, when they leave three x stages; at
-// least two otherwise).
+// for the uncompressed source), the most that fit up to kMaxX (for the
+// Huffman source the most table copies that leave three x stages, else one
+// table and at least two).
 bool tc_config(int G, int Np, int src, uint32_t tdata, TcConfig &c) {
     if (a0_col(Np) + 32u * kStagesA > kTmemCols)
         return false;
     const size_t lim = size_t(kMaxSmemPerBlock) - 1024;
-    for (int pass = 0; pass < 2; pass++) {
-        const bool priv = src == kSrcHuffman && pass == 0;
-        if (pass == 0 && src != kSrcHuffman)
+    for (int tab = 2; tab >= 0; tab--) {
+        if (tab != 0 && src != kSrcHuffman)
             continue;
-        for (int sx = kMaxX; sx >= (priv ? 3 : 2); sx--)
-            if (tc_smem(G, sx, Np, src, tdata, priv) <= lim) {
+        for (int sx = kMaxX; sx >= (tab != 0 ? 3 : 2); sx--)
+            if (tc_smem(G, sx, Np, src, tdata, tab) <= lim) {
                 c.SX = sx;
-                c.priv = priv;
-                c.smem = std::max(tc_smem(G, sx, Np, src, tdata, priv), kExclusiveSmem);
+                c.tab = tab;
+                c.smem = std::max(tc_smem(G, sx, Np, src, tdata, tab), kExclusiveSmem);
                 return true;
             }
     }
@@ -954,10 +961,12 @@ uw_status launch_gemm_tc(const TcParams &base, int G, int src, cudaStream_t stre
             s = launch_tc_g<kSrcPalette4>(p, G, c.smem, grid, stream);
         else if (src == kSrcExponent)
             s = launch_tc_g<kSrcExponent>(p, G, c.smem, grid, stream);
-        else if (c.priv)
-            s = launch_tc_g<kSrcHuffman, true>(p, G, c.smem, grid, stream);
+        else if (c.tab == 2)
+            s = launch_tc_g<kSrcHuffman, 2>(p, G, c.smem, grid, stream);
+        else if (c.tab == 1)
+            s = launch_tc_g<kSrcHuffman, 1>(p, G, c.smem, grid, stream);
         else
-            s = launch_tc_g<kSrcHuffman, false>(p, G, c.smem, grid, stream);
+            s = launch_tc_g<kSrcHuffman, 0>(p, G, c.smem, grid, stream);
         if (s != UW_OK)
             return s;
     }
