@@ -846,7 +846,7 @@ def context_measurements(torch, uw, w, x, desc, blobs, xd, stream, plan):
     for b in (16, 256):
         xb_dev = torch.from_numpy(wl.activations(b, COLS, seed=b).view(np.int16)).cuda()
         yb = torch.empty(b, ROWS, dtype=torch.int16, device="cuda")
-        v = variant_id(uw, "tc_g2" if b <= 64 else "tc_g3")  # the library's default at this batch
+        v = variant_id(uw, "tc_g3")  # the library's default at this batch
         pl = uw.Plan(uw.STRATEGY_FUSED, v, b, 0.0)
         wsb = torch.empty(uw.workspace_size(desc, b, pl), dtype=torch.uint8, device="cuda")
         uw.workspace_init(wsb, stream)

@@ -87,21 +87,17 @@ GemvVariant gemv_variant(int v, int64_t rows, int64_t cols, uint32_t tbuf = kWor
 // Tile data bytes assumed for a Huffman blob that is not at hand.
 constexpr uint32_t kWorstTileData = kWorstTileBuf - kTileSlack;
 
-// Tensor-core default: two producer groups up to 64 batch rows, three above
-// (measured on the gate matrix: the fastest within 3% at 16..256 rows; four
-// groups leave the producers 96 registers and spill), when their stages fit
-// this weight source.  The result does not depend on the number of groups
-// (the MMAs accumulate in K order over the same cut), so the choice only
-// changes the speed.
+// Tensor-core default: three producer groups when their stages fit this
+// weight source and batch (measured on the gate matrix: the fastest at 16 and
+// 64 batch rows, within 2% of two groups at 256; four groups leave the
+// producers 96 registers and spill), else two.  The result does not depend on
+// the number of groups (the MMAs accumulate in K order over the same cut), so
+// the choice only changes the speed.
 int default_tc_variant(int64_t rows, int64_t cols, int64_t batch, int src, uint32_t tdata) {
     (void)rows;
     (void)cols;
     const int np = int(std::min<int64_t>((batch + 15) / 16 * 16, kTcMaxBatch));
-    const int want = np <= 64 ? 0 : 1;  // index into kTcGroups
-    for (int i = want; i >= 0; i--)
-        if (gemm_tc_fits(kTcGroups[i], np, src, tdata))
-            return kTcFirst + i;
-    return kTcFirst;
+    return gemm_tc_fits(kTcGroups[1], np, src, tdata) ? kTcFirst + 1 : kTcFirst;
 }
 
 int pad_batch(int64_t b) {

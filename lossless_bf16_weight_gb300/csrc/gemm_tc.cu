@@ -69,6 +69,7 @@ constexpr int kMaxX = 8;           // x stages in shared memory
 constexpr int kMaxProducers = 16;  // 4G, G <= 4
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kMinUnits = 4;  // K steps per worker at least
+constexpr uint32_t kYBufBytes = 32 * kTcM * 2;  // a producer group's y chunk: 32 columns x 128 rows BF16
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
     asm volatile(
@@ -106,6 +107,15 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 // Barrier 1 over the producer warps only (barrier 0 is __syncthreads).
 __device__ __forceinline__ void producers_sync(int nthreads) {
     asm volatile("bar.sync 1, %0;" :: "r"(nthreads) : "memory");
+}
+
+// Barrier 2 + g over the four producer warps of group g.
+__device__ __forceinline__ void group_sync(int g) {
+    asm volatile("bar.sync %0, 128;" :: "r"(2 + g) : "memory");
+}
+
+__device__ __forceinline__ void sts16(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" :: "r"(addr), "h"(uint16_t(v)) : "memory");
 }
 
 // An escaped group's 32 BF16 pairs, from its raw exponents (in the pair
@@ -262,6 +272,37 @@ __device__ __forceinline__ void fixup_block(const TcParams &p, uint32_t mb, uint
                     yb[n0 + k] = __bfloat16_as_ushort(__float2bfloat16_rn(t4[k]));
         }
     }
+}
+
+// One 32-column chunk of a whole segment's y: the group's four warps write
+// their rows into the group's shared buffer ([32 columns][128 rows] BF16),
+// then one tensor-map store sends whole 256-byte rows of y.
+__device__ __forceinline__ void y_chunk_store(const TcParams &p, uint32_t ybuf, int g, int q, uint32_t mb, int c0,
+                                              bool two, const uint32_t (&va)[16], const uint32_t (&vb)[16]) {
+    const int lane = threadIdx.x & 31;
+    if (q == 0 && lane == 0)
+        tma_store_wait_read();  // the previous chunk's store has read the buffer
+    group_sync(g);
+    const uint32_t row = ybuf + 2u * uint32_t(32 * q + lane);
+#pragma unroll
+    for (int jj = 0; jj < 16; jj++)
+        sts16(row + 256u * uint32_t(jj), __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(va[jj]))));
+    if (two) {
+#pragma unroll
+        for (int jj = 0; jj < 16; jj++)
+            sts16(row + 256u * uint32_t(16 + jj), __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(vb[jj]))));
+    }
+    fence_proxy_async_smem();
+    group_sync(g);
+    if (q == 0 && lane == 0) {
+        tma_store_2d(&p.ymap, int(mb * kTcM), c0, ybuf);
+        tma_store_commit();
+    }
+}
+
+__device__ __noinline__ void y_chunk_store_call(const TcParams &p, uint32_t ybuf, int g, int q, uint32_t mb, int c0,
+                                                bool two, const uint32_t (&va)[16], const uint32_t (&vb)[16]) {
+    y_chunk_store(p, ybuf, g, q, mb, c0, two, va, vb);
 }
 
 // kTab (Huffman source): the pair table as 32 lane-private copies (2: every
@@ -643,6 +684,10 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
             const int64_t n = int64_t(s.mb) * kTcM + 32 * q + lane;
             const bool whole = s.nseg == 1;
             float *part = p.partial + (uint64_t(s.mb) * p.maxseg + s.j) * uint64_t(Np) * kTcM + 32 * q + lane;
+            // y of a whole segment through the group's shared buffer ([32 columns][128 rows]
+            // BF16) and one tensor-map store per chunk, whole 256-byte rows of y
+            const bool ytma = whole && p.ystage != 0;
+            const uint32_t ybuf = xs0 + p.ybuf_off + uint32_t(g) * kYBufBytes;
 #pragma unroll 1
             for (int c0 = 32 * g; c0 < Np; c0 += 32 * G) {
                 uint32_t va[16], vb[16];
@@ -650,6 +695,14 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
                 if (c0 + 16 < Np)
                     tmem_ld16(tmem + (uint32_t(32 * q) << 16) + uint32_t(c0 + 16), vb);
                 tmem_ld_wait();
+                if (ytma) {
+                    // out of line beside producers, so that it does not weigh on their registers
+                    if constexpr (kTma)
+                        y_chunk_store(p, ybuf, g, q, s.mb, c0, c0 + 16 < Np, va, vb);
+                    else
+                        y_chunk_store_call(p, ybuf, g, q, s.mb, c0, c0 + 16 < Np, va, vb);
+                    continue;
+                }
                 auto put = [&](int b, uint32_t bits) {
                     if (b < p.batch) {
                         const float f = __uint_as_float(bits);
@@ -689,6 +742,8 @@ __global__ void __launch_bounds__((4 * G + 2) * 32, 1) gemm_tc_kernel(const __gr
                 }
             }
         }
+        if (p.ystage != 0 && q == 0 && lane == 0)
+            tma_store_wait_all();
         tile_check_flush(bad, p.status);
     } else if (warp == P) {
         if (lane == 0) {  // the MMA warp
@@ -798,6 +853,9 @@ struct TcConfig {
     int SX;
     int tab;  // table copies (Huffman source)
     size_t smem;
+    uint32_t ybuf_off;  // offset of the y buffers from the 1024-aligned base, when they fit
+    bool ystage;
+    size_t smem_base;   // without the y buffers
 };
 
 // Stages for G producer groups and Np batch rows: A stages in the tensor
@@ -816,7 +874,13 @@ bool tc_config(int G, int Np, int src, uint32_t tdata, TcConfig &c) {
             if (tc_smem(G, sx, Np, src, tdata, tab) <= lim) {
                 c.SX = sx;
                 c.tab = tab;
-                c.smem = std::max(tc_smem(G, sx, Np, src, tdata, tab), kExclusiveSmem);
+                const size_t base = tc_smem(G, sx, Np, src, tdata, tab);
+                const int groups = src == kSrcBf16 ? 3 : G;  // the uncompressed form runs three groups
+                c.ybuf_off = uint32_t((base - 1024 + 127) / 128 * 128);
+                c.ystage = 1024 + size_t(c.ybuf_off) + size_t(groups) * kYBufBytes <= lim;
+                c.smem = std::max(c.ystage ? 1024 + size_t(c.ybuf_off) + size_t(groups) * kYBufBytes : base,
+                                  kExclusiveSmem);
+                c.smem_base = base;
                 return true;
             }
     }
@@ -900,6 +964,21 @@ bool encode_x_map(CUtensorMap *m, const uint16_t *x, int64_t cols, int64_t batch
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// y [batch, rows] as a 2-D tensor (rows inner), boxes of 128 rows x 32 batch
+// rows, no swizzle (the epilogue's shared buffer is [32][128] BF16).
+bool encode_y_map(CUtensorMap *m, const uint16_t *y, int64_t rows, int64_t batch) {
+    const auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {cuuint64_t(rows), cuuint64_t(batch)};
+    const cuuint64_t strides[1] = {cuuint64_t(rows) * 2};
+    const cuuint32_t box[2] = {cuuint32_t(kTcM), 32u};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(y), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // W [rows, cols] as a 2-D tensor (cols inner), boxes of a 128-row block x
 // 64 columns with the 128-byte swizzle (the tensor-core A operand's layout);
 // rows past the end read as zeros.
@@ -954,19 +1033,27 @@ uw_status launch_gemm_tc(const TcParams &base, int G, int src, cudaStream_t stre
             return UW_ERR_CUDA;
         if (src == kSrcBf16 && !encode_w_block_map(&p.wmap, p.w, p.rows, p.cols))
             return UW_ERR_CUDA;
+        // y by tensor-map stores when every block is whole (wide batches; a stream-K cut
+        // writes y only for the rare whole segment, and the buffers would cost L1) and its
+        // rows are whole 16-byte units
+        const uint64_t nmb = uint64_t(p.rows + kTcM - 1) / kTcM;
+        p.ystage = c.ystage && p.V == nmb && p.T == nmb * p.nk && p.rows % 8 == 0 &&
+                   (reinterpret_cast<uintptr_t>(p.y) & 15u) == 0 && encode_y_map(&p.ymap, p.y, p.rows, p.batch);
+        const size_t smem = p.ystage ? c.smem : std::max(c.smem_base, kExclusiveSmem);
+        p.ybuf_off = c.ybuf_off;
         uw_status s;
         if (src == kSrcBf16)
-            s = launch_tc_g<kSrcBf16>(p, G, c.smem, grid, stream);
+            s = launch_tc_g<kSrcBf16>(p, G, smem, grid, stream);
         else if (src == kSrcPalette4)
-            s = launch_tc_g<kSrcPalette4>(p, G, c.smem, grid, stream);
+            s = launch_tc_g<kSrcPalette4>(p, G, smem, grid, stream);
         else if (src == kSrcExponent)
-            s = launch_tc_g<kSrcExponent>(p, G, c.smem, grid, stream);
+            s = launch_tc_g<kSrcExponent>(p, G, smem, grid, stream);
         else if (c.tab == 2)
-            s = launch_tc_g<kSrcHuffman, 2>(p, G, c.smem, grid, stream);
+            s = launch_tc_g<kSrcHuffman, 2>(p, G, smem, grid, stream);
         else if (c.tab == 1)
-            s = launch_tc_g<kSrcHuffman, 1>(p, G, c.smem, grid, stream);
+            s = launch_tc_g<kSrcHuffman, 1>(p, G, smem, grid, stream);
         else
-            s = launch_tc_g<kSrcHuffman, 0>(p, G, c.smem, grid, stream);
+            s = launch_tc_g<kSrcHuffman, 0>(p, G, smem, grid, stream);
         if (s != UW_OK)
             return s;
     }

@@ -67,6 +67,9 @@ struct TcParams {
     uint32_t a0col;        // first tensor-memory column of the A stages
     CUtensorMap xmap;      // x as a 2-D tensor (cols x batch rows), 64 x Np boxes, 128-byte swizzle
     CUtensorMap wmap;      // uncompressed W (cols x rows), 64 x 128 boxes, 128-byte swizzle
+    CUtensorMap ymap;      // y (rows x batch rows), 128 x 32 boxes, when ystage
+    int ystage;            // whole segments store y through shared memory and ymap
+    uint32_t ybuf_off;     // the y buffers' offset from the 1024-aligned shared base
 };
 // Whether G producer groups, batch rows Np and weights from `src` (tile
 // data bytes tdata for the Huffman source) fit one CTA.
