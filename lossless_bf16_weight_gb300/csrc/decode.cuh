@@ -176,6 +176,26 @@ __device__ __forceinline__ void replicate_private(const DecodeShared &s, uint32_
     }
 }
 
+// The 32 lane-private copies made directly, without the single table in
+// between (after build_prefix_zero): each warp makes 32 entries at a time,
+// one per lane, and writes their rows (entry w of copy l at word 32w + l,
+// as replicate_private lays them out) four rows at a time, 512 contiguous
+// bytes per store instruction.  Needs no barrier between warps; follow with
+// __syncthreads() before use.
+__device__ __forceinline__ void build_private(const DecodeShared &s, uint32_t priv) {
+    const uint32_t lane = threadIdx.x & 31u, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (uint32_t base = 32u * warp; base < uint32_t(kLutEntries); base += 32u * nw) {
+        const uint32_t e = pair_entry(s.prefix, base + lane);
+#pragma unroll
+        for (uint32_t i = 0; i < 8u; i++) {
+            const uint32_t r = 4u * i + (lane >> 3);
+            const uint32_t er = __shfl_sync(0xffffffffu, e, int(r));
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};"
+                         :: "r"(priv + 128u * (base + r) + 16u * (lane & 7u)), "r"(er) : "memory");
+        }
+    }
+}
+
 // The same with 16 copies (entry w of copy c at word 16w + c), read by
 // lane l from copy l % 16: a lookup is one or two wavefronts (lanes l and
 // l + 16 meet in a bank when their entries' parities agree).

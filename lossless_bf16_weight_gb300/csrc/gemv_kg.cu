@@ -558,19 +558,19 @@ __device__ __forceinline__ void gemv_private(const GemvParams &p, int rb_per_cta
     }
     __syncwarp();
 
-    // Prologue: offsets of the first pairs (one round trip), the table, the
-    // first copies, chunk 0 of the first pair's sign+mantissa bytes, the
-    // counting stream, the private copies.
+    // Prologue: offsets of the first pairs (one round trip, under the table
+    // build), the private table copies, the first pair's copies and chunk 0
+    // of its sign+mantissa bytes, the counting stream.  The second pair is
+    // issued at the top of the loop, so that every warp's first copies are
+    // queued before any second ones.
     uint32_t nissued = 0;
     const RecLoad first = pair_recs_load(v, span, 0);
-    build_tables(ds, v);
+    build_prefix_zero(ds, v);
+    build_private(ds, priv);
     pair_recs_store(v, ring, span, 0, first);
-#pragma unroll
-    for (int s = 0; s < kPairStages; s++) {
-        if (nissued < npairs) {
-            pair_issue_rec<false>(v, ring + kRecBytes * nissued, st0 + uint32_t(s) * sbytes, 0u, bar0 + 8u * s);
-            nissued++;
-        }
+    if (npairs > 0) {
+        pair_issue_rec<false>(v, ring, st0, 0u, bar0);
+        nissued = 1;
     }
     const uint8_t *sm_cur = nullptr;
     uint4 c0A = make_uint4(0, 0, 0, 0), c0B = c0A;
@@ -582,8 +582,6 @@ __device__ __forceinline__ void gemv_private(const GemvParams &p, int rb_per_cta
         c0B = __ldg(reinterpret_cast<const uint4 *>(k0 + 1 < k1 ? a + 64u * R0 : a));
     }
     build_count_stream(cnt);
-    __syncthreads();
-    replicate_private(ds, priv);
     __syncthreads();
     grid_dep_wait();  // x may come from the kernel before
     PrivCtx kc;
@@ -604,6 +602,10 @@ __device__ __forceinline__ void gemv_private(const GemvParams &p, int rb_per_cta
 #pragma unroll 1
     for (uint32_t j = 0; j < npairs; j++) {
         const uint32_t st = st0 + (j & 1u) * sbytes, bar = bar0 + 8u * (j & 1u);
+        if (j == 0 && nissued < npairs) {  // the second pair (see the prologue)
+            pair_issue_rec<false>(v, ring + kRecBytes, st0 + sbytes, 0u, bar0 + 8u);
+            nissued++;
+        }
         mbar_wait(bar, (j >> 1) & 1u, p.status, kStatusTimeout);
         const uint4 rbk = lds128(ring + kRecBytes * (j % uint32_t(kRecRing)) + 16u);  // pkA, pkB, q0
         const bool hasB = cur.kgA + 1 < k1;
