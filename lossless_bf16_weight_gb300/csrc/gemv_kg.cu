@@ -38,6 +38,16 @@ namespace {
 
 constexpr int kMaxColWarps = 32;
 
+// A 16-byte read-only load that does not allocate in L1: the sign+mantissa
+// chunks are read once, and beside 224 KB of shared memory L1 is small
+// enough that they would evict x.
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
 __device__ __forceinline__ void fma_bf16x2(float &a0, float &a1, uint32_t w, uint32_t x) {
     asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\t"
         "mov.b32 {wl, wh}, %2;\n\t"
@@ -465,12 +475,12 @@ __device__ __forceinline__ void priv_pair(const GemvParams &p, const PrivCtx &k,
     for (int I = 0; I < 32; I++) {
         if ((I & 7) == 0) {  // next chunk of sign+mantissa bytes
             if (I < 24) {
-                nA = __ldg(reinterpret_cast<const uint4 *>(gA_sm + uint32_t((I >> 3) + 1) * stride));
-                nB = __ldg(reinterpret_cast<const uint4 *>(gB_sm + uint32_t((I >> 3) + 1) * stride));
+                nA = ldg_stream(gA_sm + uint32_t((I >> 3) + 1) * stride);
+                nB = ldg_stream(gB_sm + uint32_t((I >> 3) + 1) * stride);
             } else if (more) {  // chunk 0 of the next pair
                 const uint8_t *a = sm_nxt + 16u * (uint32_t(lane) < Rn ? uint32_t(lane) : 0u);
-                nA = __ldg(reinterpret_cast<const uint4 *>(a));
-                nB = __ldg(reinterpret_cast<const uint4 *>(nhasB ? a + 64u * Rn : a));
+                nA = ldg_stream(a);
+                nB = ldg_stream(nhasB ? a + 64u * Rn : a);
             }
         }
         if ((I & 3) == 0) {
