@@ -366,22 +366,18 @@ struct PrivCtx {
     uint32_t one;    // 1, held in a register
 };
 
-// One pair (tiles A = (rb, kgA), B = (rb, kgA + 1) when hasB) staged at `st`:
-// returns the two tiles' partials pA = acc_even + acc_odd of A, pB of B.
-// kFull: a full row block (32 rows: constant strides, glen in the stage).
-// sm: the pair's first sign+mantissa byte; chunk 0 of each tile arrives in
-// c0A / c0B and chunk 0 of the next pair (at sm_nxt, Rn rows, B when nhasB) leaves
-// in them.
+// A pair's group lengths reduced over the warp: the lane's own (A | B << 16;
+// zero for rows past a partial block and without tile B), their exclusive
+// prefix sums and totals (16-bit halves) and the masks of escaped groups.
+struct PairScan {
+    uint32_t g2, off2, tot2, emA, emB;
+};
+
+// The scan of the pair staged at `st` (full row block: glen in the stage;
+// partial block of R rows: glen read at group q0).
 template <bool kFull>
-__device__ __forceinline__ void priv_pair(const GemvParams &p, const PrivCtx &k, uint32_t st, uint32_t pkA,
-                                          uint32_t pkB, uint64_t q0, uint32_t Rr, bool hasB, const uint8_t *sm,
-                                          const uint4 *xA, bool more, const uint8_t *sm_nxt, uint32_t Rn, bool nhasB,
-                                          uint4 &c0A, uint4 &c0B, uint32_t &bad, float &pA, float &pB) {
-    const BlobView &v = p.v;
+__device__ __forceinline__ PairScan pair_scan(const BlobView &v, uint32_t st, uint64_t q0, uint32_t R, bool hasB) {
     const int lane = threadIdx.x & 31;
-    const uint32_t R = kFull ? uint32_t(kTileRows) : Rr;
-    const uint32_t n16A = pkA & 0xFFu, n16B = pkB & 0xFFu;
-    const uint32_t nescA = (pkA >> 8) & 0xFFu, nescB = (pkB >> 8) & 0xFFu;
     uint32_t gA, gB;
     if (kFull) {
         gA = lds_u8(st + uint32_t(lane));
@@ -391,21 +387,53 @@ __device__ __forceinline__ void priv_pair(const GemvParams &p, const PrivCtx &k,
         gA = __ldg(v.glen + q0 + l);
         gB = hasB ? __ldg(v.glen + q0 + R + l) : 0u;
     }
-    // one warp prefix sum over both tiles' group lengths (16-bit halves)
     const bool vA = kFull || uint32_t(lane) < R, vB = hasB && vA;
-    uint32_t ga = vA ? gA : 0u, gb = vB ? gB : 0u;
-    const uint32_t g2 = ga | (gb << 16);
-    uint32_t incl = g2;
+    const uint32_t ga = vA ? gA : 0u, gb = vB ? gB : 0u;
+    PairScan s;
+    s.g2 = ga | (gb << 16);
+    uint32_t incl = s.g2;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1)
         asm("{\n\t.reg .b32 u;\n\t.reg .pred q;\n\t"
             "shfl.sync.up.b32 u|q, %0, %1, 0, -1;\n\t"
             "@q add.u32 %0, %0, u;\n\t}"
             : "+r"(incl) : "r"(d));
-    const uint32_t off2 = incl - g2;
-    const uint32_t tot2 = __shfl_sync(0xffffffffu, incl, 31);
-    uint32_t emA = __ballot_sync(0xffffffffu, vA && ga == 0u);
-    uint32_t emB = __ballot_sync(0xffffffffu, vB && gb == 0u);
+    s.off2 = incl - s.g2;
+    s.tot2 = __shfl_sync(0xffffffffu, incl, 31);
+    s.emA = __ballot_sync(0xffffffffu, vA && ga == 0u);
+    s.emB = __ballot_sync(0xffffffffu, vB && gb == 0u);
+    return s;
+}
+
+// The pair after the current one, scanned halfway through the current
+// pair's decode so that the scan's round trips overlap the decode.
+struct NextPair {
+    uint32_t st, bar, parity, R;
+    uint64_t q0;
+    bool hasB, full;
+};
+
+// One pair (tiles A = (rb, kgA), B = (rb, kgA + 1) when hasB) staged at `st`
+// and scanned (`sc`): returns the two tiles' partials pA = acc_even + acc_odd
+// of A, pB of B.  kFull: a full row block (32 rows: constant strides).  sm:
+// the pair's first sign+mantissa byte; chunk 0 of each tile arrives in c0A /
+// c0B and chunk 0 of the next pair (at sm_nxt, Rn rows, B when nhasB) leaves
+// in them; when `more`, the next pair's stage is waited for and scanned into
+// `nsc` after the 16th step.
+template <bool kFull>
+__device__ __forceinline__ void priv_pair(const GemvParams &p, const PrivCtx &k, uint32_t st, uint32_t pkA,
+                                          uint32_t pkB, const PairScan &sc, const NextPair &nb, PairScan &nsc,
+                                          uint32_t Rr, bool hasB, const uint8_t *sm, const uint4 *xA, bool more,
+                                          const uint8_t *sm_nxt, uint32_t Rn, bool nhasB, uint4 &c0A, uint4 &c0B,
+                                          uint32_t &bad, float &pA, float &pB) {
+    const BlobView &v = p.v;
+    const int lane = threadIdx.x & 31;
+    const uint32_t R = kFull ? uint32_t(kTileRows) : Rr;
+    const uint32_t n16A = pkA & 0xFFu, n16B = pkB & 0xFFu;
+    const uint32_t nescA = (pkA >> 8) & 0xFFu, nescB = (pkB >> 8) & 0xFFu;
+    uint32_t ga = sc.g2 & 0xFFFFu, gb = sc.g2 >> 16;
+    const uint32_t off2 = sc.off2, tot2 = sc.tot2;
+    uint32_t emA = sc.emA, emB = sc.emB;
     // A pair whose tables or group lengths do not add up (a device copy
     // damaged after its header was checked) is flagged and decodes the zero
     // stream in every lane, so no read leaves the stage.
@@ -492,6 +520,11 @@ __device__ __forceinline__ void priv_pair(const GemvParams &p, const PrivCtx &k,
                 nxA = __ldg(xA + (I >> 2) + 1);
                 nxB = __ldg(xB + (I >> 2) + 1);
             }
+        }
+        if (I == 16 && more) {  // the next pair: its stage and scan
+            mbar_wait(nb.bar, nb.parity, p.status, kStatusTimeout);
+            nsc = nb.full ? pair_scan<true>(v, nb.st, nb.q0, kTileRows, nb.hasB)
+                          : pair_scan<false>(v, nb.st, nb.q0, nb.R, nb.hasB);
         }
         const uint32_t eA = decode_entry_rs(la, lutA, sA_, k.one, I);
         const uint32_t eB = decode_entry_rs(lb, lutB, sB_, k.one, I);
@@ -608,15 +641,24 @@ __device__ __forceinline__ void gemv_private(const GemvParams &p, int rb_per_cta
     if (npairs == 0)
         for (uint32_t rl = 0; rl < nrbc; rl++)
             red[(rl * W + warp) * 32 + lane] = 0.f;
+    // the second pair (see the prologue), then the first pair's stage and scan;
+    // every later pair is waited for and scanned halfway through the one before
+    PairScan sc{};
+    if (npairs > 0) {
+        if (nissued < npairs) {
+            pair_issue_rec<false>(v, ring + kRecBytes, st0 + sbytes, 0u, bar0 + 8u);
+            nissued++;
+        }
+        mbar_wait(bar0, 0u, p.status, kStatusTimeout);
+        const uint4 r0 = lds128(ring + 16u);
+        const uint64_t q00 = (uint64_t(r0.w) << 32) | r0.z;
+        sc = rb0 < v.nfull ? pair_scan<true>(v, st0, q00, kTileRows, k0 + 1 < k1)
+                           : pair_scan<false>(v, st0, q00, v.tail_rows, k0 + 1 < k1);
+    }
 
 #pragma unroll 1
     for (uint32_t j = 0; j < npairs; j++) {
         const uint32_t st = st0 + (j & 1u) * sbytes, bar = bar0 + 8u * (j & 1u);
-        if (j == 0 && nissued < npairs) {  // the second pair (see the prologue)
-            pair_issue_rec<false>(v, ring + kRecBytes, st0 + sbytes, 0u, bar0 + 8u);
-            nissued++;
-        }
-        mbar_wait(bar, (j >> 1) & 1u, p.status, kStatusTimeout);
         const uint4 rbk = lds128(ring + kRecBytes * (j % uint32_t(kRecRing)) + 16u);  // pkA, pkB, q0
         const bool hasB = cur.kgA + 1 < k1;
         const bool full = cur.rb < v.nfull;
@@ -624,16 +666,30 @@ __device__ __forceinline__ void gemv_private(const GemvParams &p, int rb_per_cta
         PairCursor nxt = cur;
         nxt.next(k0, k1);
         const uint32_t Rn = nxt.rb < v.nfull ? uint32_t(kTileRows) : v.tail_rows;
-        const uint8_t *sm_nxt = more ? rec_sm(v, ring + kRecBytes * ((j + 1) % uint32_t(kRecRing))) : sm_cur;
+        NextPair nb{};
+        const uint8_t *sm_nxt = sm_cur;
+        if (more) {
+            const uint4 rn = lds128(ring + kRecBytes * ((j + 1) % uint32_t(kRecRing)) + 16u);
+            nb.q0 = (uint64_t(rn.w) << 32) | rn.z;
+            sm_nxt = v.sm + nb.q0 * kGroup;
+            nb.st = st0 + ((j + 1) & 1u) * sbytes;
+            nb.bar = bar0 + 8u * ((j + 1) & 1u);
+            nb.parity = ((j + 1) >> 1) & 1u;
+            nb.R = Rn;
+            nb.hasB = nxt.kgA + 1 < k1;
+            nb.full = nxt.rb < v.nfull;
+        }
         const uint4 *xA = reinterpret_cast<const uint4 *>(p.x) + size_t(cur.kgA) * 8;
-        const uint64_t q0 = (uint64_t(rbk.w) << 32) | rbk.z;
         float pA, pB;
+        PairScan nsc = sc;
         if (full)
-            priv_pair<true>(p, kc, st, rbk.x, rbk.y, q0, kTileRows, hasB, sm_cur, xA, more, sm_nxt, Rn,
+            priv_pair<true>(p, kc, st, rbk.x, rbk.y, sc, nb, nsc, kTileRows, hasB, sm_cur, xA, more, sm_nxt, Rn,
                             nxt.kgA + 1 < k1, c0A, c0B, bad, pA, pB);
         else
-            priv_pair<false>(p, kc, st, rbk.x, rbk.y, q0, v.tail_rows, hasB, sm_cur, xA, more, sm_nxt, Rn,
+            priv_pair<false>(p, kc, st, rbk.x, rbk.y, sc, nb, nsc, v.tail_rows, hasB, sm_cur, xA, more, sm_nxt, Rn,
                              nxt.kgA + 1 < k1, c0A, c0B, bad, pA, pB);
+        sc = nsc;
+        (void)bar;
         sm_cur = sm_nxt;
         s_w = s_w + pA;
         if (hasB)
