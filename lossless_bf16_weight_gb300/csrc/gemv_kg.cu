@@ -689,7 +689,6 @@ __device__ __forceinline__ void gemv_private(const GemvParams &p, int rb_per_cta
             priv_pair<false>(p, kc, st, rbk.x, rbk.y, sc, nb, nsc, v.tail_rows, hasB, sm_cur, xA, more, sm_nxt, Rn,
                              nxt.kgA + 1 < k1, c0A, c0B, bad, pA, pB);
         sc = nsc;
-        (void)bar;
         sm_cur = sm_nxt;
         s_w = s_w + pA;
         if (hasB)
