@@ -604,8 +604,8 @@ __device__ __forceinline__ void gemv_private(const GemvParams &p, int rb_per_cta
     // Prologue: offsets of the first pairs (one round trip, under the table
     // build), the private table copies, the first pair's copies and chunk 0
     // of its sign+mantissa bytes, the counting stream.  The second pair is
-    // issued at the top of the loop, so that every warp's first copies are
-    // queued before any second ones.
+    // issued after the dependency wait, so that every warp's first copies
+    // are queued before any second ones.
     uint32_t nissued = 0;
     const RecLoad first = pair_recs_load(v, span, 0);
     build_prefix_zero(ds, v);
